@@ -1,0 +1,351 @@
+"""Plain, slow, fp64 CPU oracle of the Llama-style decoder block forward pass.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports this module; the
+tests, the smoke check and the CPU-baseline leg of the benchmark do. It shares
+no code, table or constant generator with the CUDA library.
+
+Every step is written the way the pages state it, in float64, with no blocking,
+fusion or reordering. NumPy's matmul is the only library primitive used (for
+the projections and the per-head score/value products).
+
+Sources (page title, section):
+  * "LlamaForCausalLM-32L-4096d" sheet, "Implementing it": the block pseudo-code
+    (rmsnorm -> q/k/v projections -> rope(theta=10000) -> softmax(q k^T / sqrt(128),
+    causal) v -> o_proj -> residual -> rmsnorm -> silu(gate) * up -> down ->
+    residual).
+  * nnterp encyclopedia "arcee", "The block, in order": the two pre-norm
+    sublayers and the ungated squared-ReLU MLP ``down_proj(relu(up_proj(z)) ** 2)``;
+    "Grouped-query attention, 128-wide heads": key/value head j serves a
+    contiguous group of query heads (repeat_kv); "The API": tap names/layouts.
+  * nnterp encyclopedia "apertus", "The MLP has no gate, and its activation is
+    learned per block": xIELU and its parameter transform; "Queries and keys are
+    normed per head, before the rotary": q_norm/k_norm over head_dim, one gain for
+    every head, applied before RoPE.
+
+Readings where the pages leave a step open:
+  * RMSNorm is x / sqrt(mean(x^2) + eps) * g over the last axis (eps inside the
+    square root, no mean-centering, no bias).
+  * RoPE pairs element i with element i + d/2 ("rotate half"), with
+    inv_freq_i = theta^(-2i/d) for i < d/2 and angle = position * inv_freq_i.
+  * Key j is visible to query i iff position(j) <= position(i).
+  * xIELU at exactly x = 0 takes the negative branch (the positive one is
+    written for x > 0 only).
+
+Every function here is pinned by the not-gpu tests (closed forms, page-printed
+values, invariants, brute force on tiny inputs); SwiGLU's silu is pinned by its
+textbook properties only.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+F64 = np.float64
+
+
+@dataclass(frozen=True)
+class BlockConfig:
+    """The block's configuration, in the pages' config-key vocabulary.
+
+    Keys follow the "Config" tables of the nnterp encyclopedia pages
+    (hidden_size, num_attention_heads, num_key_value_heads, head_dim,
+    intermediate_size, hidden_act, rms_norm_eps, rope_theta).
+    """
+
+    hidden_size: int
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    intermediate_size: int
+    hidden_act: str  # "silu" (gated SwiGLU), "relu2", "xielu"
+    rms_norm_eps: float = 1e-5
+    rope_theta: float = 10000.0
+    qk_norm: bool = False
+    xielu_alpha_p: float = 0.8  # effective value (after the softplus transform)
+    xielu_alpha_n: float = 0.8  # effective value (after beta + softplus)
+    xielu_beta: float = 0.5
+    xielu_eps: float = -1e-6
+
+    def __post_init__(self):
+        if self.hidden_act not in ("silu", "relu2", "xielu"):
+            raise ValueError(f"unknown hidden_act {self.hidden_act!r}")
+        if self.num_heads % self.num_kv_heads:
+            raise ValueError("num_heads must be a multiple of num_kv_heads")
+        if self.head_dim % 2:
+            raise ValueError("head_dim must be even for the rotary")
+
+
+# --------------------------------------------------------------------------
+# Elementary operations
+# --------------------------------------------------------------------------
+
+def rms_norm(x, gain, eps):
+    """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * gain.
+
+    Pages: "arcee" printout ``ArceeRMSNorm((2560,), eps=1e-05)``; the
+    "LlamaForCausalLM-32L-4096d" pseudo-code ``rmsnorm(x, ..., eps=1e-05)``;
+    "afmoe", "The contributions are the post-norms' outputs" (scale-invariant up
+    to eps).
+    """
+    x = np.asarray(x, dtype=F64)
+    mean_sq = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(mean_sq + eps) * np.asarray(gain, dtype=F64)
+
+
+def rope_inv_freq(head_dim, theta):
+    """inv_freq_i = theta^(-2i/head_dim), i = 0 .. head_dim/2 - 1."""
+    i = np.arange(head_dim // 2, dtype=F64)
+    return np.power(F64(theta), -2.0 * i / head_dim)
+
+
+def rope(x, positions, theta):
+    """Rotary embedding of x[..., T, d] at the given positions (length T).
+
+    Pages: "LlamaForCausalLM-32L-4096d" ``q, k = rope(q, k, theta=10000)``;
+    "apertus" ("at position 0, where the rotation is the identity").
+    Element i is rotated together with element i + d/2 by the angle
+    position * inv_freq_i.
+    """
+    x = np.asarray(x, dtype=F64)
+    d = x.shape[-1]
+    half = d // 2
+    pos = np.asarray(positions, dtype=F64)
+    ang = pos[:, None] * rope_inv_freq(d, theta)[None, :]  # [T, d/2]
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def causal_gqa_attention(q, k, v, q_positions, k_positions, return_pattern=False):
+    """softmax(q k^T / sqrt(d), causal) v per query head, grouped over KV heads.
+
+    q: [H, Tq, d], k, v: [Hkv, Tk, d] (one sequence). Query head h reads KV head
+    h // (H / Hkv) ("arcee": "an edit to key/value head j reaches query heads 5j
+    to 5j + 4"). Key j is visible to query i iff k_positions[j] <= q_positions[i].
+    Returns head outputs [H, Tq, d] (and the masked scores and probabilities).
+    """
+    q = np.asarray(q, dtype=F64)
+    k = np.asarray(k, dtype=F64)
+    v = np.asarray(v, dtype=F64)
+    H, Tq, d = q.shape
+    Hkv = k.shape[0]
+    group = H // Hkv
+    visible = np.asarray(k_positions)[None, :] <= np.asarray(q_positions)[:, None]
+    out = np.empty((H, Tq, d), dtype=F64)
+    scores_all, probs_all = [], []
+    for h in range(H):
+        j = h // group
+        s = (q[h] @ k[j].T) / np.sqrt(F64(d))
+        s = np.where(visible, s, -np.inf)
+        m = np.max(s, axis=-1, keepdims=True)
+        e = np.exp(s - m)
+        p = e / np.sum(e, axis=-1, keepdims=True)
+        out[h] = p @ v[j]
+        if return_pattern:
+            scores_all.append(s)
+            probs_all.append(p)
+    if return_pattern:
+        return out, np.stack(scores_all), np.stack(probs_all)
+    return out
+
+
+def silu(u):
+    """silu(u) = u / (1 + exp(-u)) (the gated MLP's act_fn)."""
+    u = np.asarray(u, dtype=F64)
+    with np.errstate(over="ignore"):
+        return u / (1.0 + np.exp(-u))
+
+
+def relu2(u):
+    """relu(u) ** 2 ("arcee": ``down_proj(relu(up_proj(z)) ** 2)``)."""
+    u = np.asarray(u, dtype=F64)
+    r = np.maximum(u, 0.0)
+    return r * r
+
+
+def softplus(t):
+    """softplus(t) = log(1 + exp(t)), evaluated without overflow."""
+    t = np.asarray(t, dtype=F64)
+    return np.logaddexp(0.0, t)
+
+
+def xielu_effective(raw_alpha_p, raw_alpha_n, beta=0.5):
+    """Stored xIELU parameters -> the values the formula uses.
+
+    "apertus": the effective alpha_p is softplus(alpha_p) and the effective
+    alpha_n is beta + softplus(alpha_n).
+    """
+    return float(softplus(raw_alpha_p)), float(beta + softplus(raw_alpha_n))
+
+
+def xielu(u, alpha_p, alpha_n, beta=0.5, eps=-1e-6):
+    """xIELU with effective parameters.
+
+    "apertus": alpha_p * x^2 + beta * x for x > 0, and
+    alpha_n * (expm1(min(x, eps)) - x) + beta * x otherwise.
+    """
+    u = np.asarray(u, dtype=F64)
+    pos = alpha_p * u * u + beta * u
+    neg = alpha_n * (np.expm1(np.minimum(u, eps)) - u) + beta * u
+    return np.where(u > 0, pos, neg)
+
+
+# --------------------------------------------------------------------------
+# The block
+# --------------------------------------------------------------------------
+
+def _act(cfg, up, gate=None):
+    if cfg.hidden_act == "silu":
+        return silu(gate)
+    if cfg.hidden_act == "relu2":
+        return relu2(up)
+    return xielu(up, cfg.xielu_alpha_p, cfg.xielu_alpha_n, cfg.xielu_beta, cfg.xielu_eps)
+
+
+def _heads(t, n, d):
+    """[T, n*d] -> [n, T, d]."""
+    return t.reshape(t.shape[0], n, d).transpose(1, 0, 2)
+
+
+def _project_kv(cfg, w, h_norm, positions):
+    """Keys and values of every row: k_proj/v_proj, optional k_norm, RoPE on k."""
+    d = cfg.head_dim
+    k = _heads(h_norm @ w["k_proj"].T, cfg.num_kv_heads, d)
+    v = _heads(h_norm @ w["v_proj"].T, cfg.num_kv_heads, d)
+    if cfg.qk_norm:
+        k = rms_norm(k, w["k_norm"], cfg.rms_norm_eps)
+    k = rope(k, positions, cfg.rope_theta)
+    return k, v
+
+
+def _project_q(cfg, w, h_norm_rows, positions_rows):
+    d = cfg.head_dim
+    q = _heads(h_norm_rows @ w["q_proj"].T, cfg.num_heads, d)
+    if cfg.qk_norm:
+        q = rms_norm(q, w["q_norm"], cfg.rms_norm_eps)
+    return rope(q, positions_rows, cfg.rope_theta)
+
+
+def _finish_rows(cfg, w, x_rows, heads_out):
+    """o_proj, residual, second norm, MLP and residual for a set of rows.
+
+    heads_out: [H, R, d] per-head outputs of those rows.
+    """
+    taps = {}
+    R = x_rows.shape[0]
+    premix = heads_out.transpose(1, 0, 2).reshape(R, -1)  # [R, H*d]
+    attn_out = premix @ w["o_proj"].T
+    mid = x_rows + attn_out
+    h2 = rms_norm(mid, w["post_attention_layernorm"], cfg.rms_norm_eps)
+    up = h2 @ w["up_proj"].T
+    if cfg.hidden_act == "silu":
+        gate = h2 @ w["gate_proj"].T
+        act = _act(cfg, up, gate)
+        neurons = act * up
+        taps["mlp_gate_output"] = gate
+    else:
+        act = _act(cfg, up)
+        neurons = act
+    mlp_out = neurons @ w["down_proj"].T
+    out = mid + mlp_out
+    taps.update(
+        attention_head_outputs=heads_out.transpose(1, 0, 2),  # [R, H, d]
+        attention_output=attn_out,
+        layer_mid=mid,
+        mlp_norm_output=h2,
+        mlp_up_output=up,
+        mlp_activation=act,
+        mlp_neurons=neurons,
+        mlp_output=mlp_out,
+        layer_output=out,
+    )
+    return taps
+
+
+def block_forward(cfg, w, x, rows=None, positions=None, return_pattern=False):
+    """Forward pass of one decoder block over x[B, T, D] (fp64).
+
+    Follows the "LlamaForCausalLM-32L-4096d" pseudo-code, with the MLP variant
+    chosen by cfg.hidden_act ("arcee": relu2, "apertus": xielu) and the
+    optional per-head q/k RMSNorm before RoPE ("apertus").
+
+    rows: optional sorted list of sequence positions whose outputs are wanted
+    (keys/values are still formed for every position, as attention needs them).
+    positions: optional rotary positions of the T rows (default 0 .. T-1).
+
+    Returns a dict of taps, each with a leading batch axis, named as the nnterp
+    pages name them: attention_norm_output, attention_queries [B,H,R,d],
+    attention_keys [B,Hkv,T,d], attention_values, attention_head_outputs
+    [B,R,H,d], attention_output, layer_mid, mlp_norm_output, mlp_up_output,
+    (mlp_gate_output), mlp_activation, mlp_neurons, mlp_output, layer_output.
+    """
+    x = np.asarray(x, dtype=F64)
+    B, T, D = x.shape
+    assert D == cfg.hidden_size
+    if rows is None:
+        rows = np.arange(T)
+    rows = np.asarray(rows)
+    if positions is None:
+        positions = np.arange(T)
+    positions = np.asarray(positions)
+    per_batch = []
+    for b in range(B):
+        taps = {}
+        h = rms_norm(x[b], w["input_layernorm"], cfg.rms_norm_eps)  # [T, D]
+        k, v = _project_kv(cfg, w, h, positions)
+        q = _project_q(cfg, w, h[rows], positions[rows])
+        res = causal_gqa_attention(q, k, v, positions[rows], positions, return_pattern)
+        if return_pattern:
+            heads, scores, probs = res
+            taps["attention_scores"] = scores
+            taps["attention_probabilities"] = probs
+        else:
+            heads = res
+        taps.update(_finish_rows(cfg, w, x[b][rows], heads))
+        taps.update(
+            layer_input=x[b][rows],
+            attention_norm_output=h[rows],
+            attention_queries=q,
+            attention_keys=k,
+            attention_values=v,
+        )
+        per_batch.append(taps)
+    return {key: np.stack([t[key] for t in per_batch]) for key in per_batch[0]}
+
+
+def decode_step(cfg, w, x, cache_k, cache_v, lens):
+    """One decode step: one new token per sequence attends to its KV cache.
+
+    x: [B, D] new tokens; cache_k, cache_v: [B, Hkv, capacity, d] holding keys
+    (after k_norm and RoPE) and values for positions 0 .. lens[b]-1; lens: [B].
+    The new token sits at position lens[b]; its key/value join the cache at slot
+    lens[b] and it attends over lens[b] + 1 keys. The pages define no cache;
+    this is the prefill block restricted to its last row, with earlier keys
+    read from the cache instead of recomputed.
+
+    Returns the taps of the new rows ([B, ...], row axis dropped) plus
+    new_key [B, Hkv, d] and new_value [B, Hkv, d].
+    """
+    x = np.asarray(x, dtype=F64)
+    B, D = x.shape
+    per_batch = []
+    for b in range(B):
+        L = int(lens[b])
+        pos = np.array([L])
+        h = rms_norm(x[b:b + 1], w["input_layernorm"], cfg.rms_norm_eps)  # [1, D]
+        k_new, v_new = _project_kv(cfg, w, h, pos)  # [Hkv, 1, d]
+        q = _project_q(cfg, w, h, pos)  # [H, 1, d]
+        k_all = np.concatenate([np.asarray(cache_k[b, :, :L], dtype=F64), k_new], axis=1)
+        v_all = np.concatenate([np.asarray(cache_v[b, :, :L], dtype=F64), v_new], axis=1)
+        heads = causal_gqa_attention(q, k_all, v_all, pos, np.arange(L + 1))
+        taps = _finish_rows(cfg, w, x[b:b + 1], heads)
+        taps = {key: val[0] for key, val in taps.items()}
+        taps.update(
+            attention_norm_output=h[0],
+            attention_queries=q[:, 0],
+            new_key=k_new[:, 0],
+            new_value=v_new[:, 0],
+        )
+        per_batch.append(taps)
+    return {key: np.stack([t[key] for t in per_batch]) for key in per_batch[0]}

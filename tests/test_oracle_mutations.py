@@ -1,0 +1,156 @@
+"""Plants plausible mistakes in the oracle (CPU only) and checks a pin catches each.
+
+This guards the pins themselves: a dropped term, a wrong sign or index, or a
+misread pairing in any oracle step must make at least one pin test fail.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import oracle.block as ob
+from tests import test_oracle_pins as pins
+
+F64 = np.float64
+
+
+def _rms_eps_outside(x, gain, eps):
+    x = np.asarray(x, dtype=F64)
+    return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps) * gain
+
+
+def _rms_sum(x, gain, eps):
+    x = np.asarray(x, dtype=F64)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps) * gain
+
+
+def _rope_interleaved(x, positions, theta):
+    x = np.asarray(x, dtype=F64)
+    d = x.shape[-1]
+    ang = np.asarray(positions, dtype=F64)[:, None] * ob.rope_inv_freq(d, theta)[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x1 * c - x2 * s
+    out[..., 1::2] = x2 * c + x1 * s
+    return out
+
+
+def _inv_freq_wrong(head_dim, theta):
+    i = np.arange(head_dim // 2, dtype=F64)
+    return np.power(F64(theta), -i / head_dim)
+
+
+def _rope_sign(x, positions, theta):
+    x = np.asarray(x, dtype=F64)
+    d = x.shape[-1]
+    ang = np.asarray(positions, dtype=F64)[:, None] * ob.rope_inv_freq(d, theta)[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., : d // 2], x[..., d // 2:]
+    return np.concatenate([x1 * c + x2 * s, x2 * c - x1 * s], axis=-1)
+
+
+def _attn_factory(scale=True, gqa="div", strict=False):
+    def attn(q, k, v, q_positions, k_positions, return_pattern=False):
+        q, k, v = (np.asarray(a, dtype=F64) for a in (q, k, v))
+        H, Tq, d = q.shape
+        Hkv = k.shape[0]
+        qp, kp = np.asarray(q_positions), np.asarray(k_positions)
+        vis = (kp[None, :] < qp[:, None]) | (kp[None, :] == 0) if strict else kp[None, :] <= qp[:, None]
+        out = np.empty((H, Tq, d))
+        ss, pp = [], []
+        for h in range(H):
+            j = h // (H // Hkv) if gqa == "div" else h % Hkv
+            s = q[h] @ k[j].T / (np.sqrt(F64(d)) if scale else 1.0)
+            s = np.where(vis, s, -np.inf)
+            e = np.exp(s - s.max(-1, keepdims=True))
+            p = e / e.sum(-1, keepdims=True)
+            out[h] = p @ v[j]
+            ss.append(s)
+            pp.append(p)
+        return (out, np.stack(ss), np.stack(pp)) if return_pattern else out
+    return attn
+
+
+def _xielu_beta_sign(u, alpha_p, alpha_n, beta=0.5, eps=-1e-6):
+    u = np.asarray(u, dtype=F64)
+    return np.where(u > 0, alpha_p * u * u + beta * u, alpha_n * (np.expm1(np.minimum(u, eps)) - u) - beta * u)
+
+
+def _xielu_no_min(u, alpha_p, alpha_n, beta=0.5, eps=-1e-6):
+    u = np.asarray(u, dtype=F64)
+    return np.where(u > 0, alpha_p * u * u + beta * u, alpha_n * (np.expm1(u) + u) + beta * u)
+
+
+def _silu_wrong(u):
+    u = np.asarray(u, dtype=F64)
+    return u / (1.0 + np.exp(u))
+
+
+def _relu_not_squared(u):
+    return np.maximum(np.asarray(u, dtype=F64), 0.0)
+
+
+def _finish_swapped(cfg, w, x_rows, heads_out):
+    # silu applied to up instead of gate
+    w2 = dict(w)
+    if cfg.hidden_act == "silu":
+        w2["gate_proj"], w2["up_proj"] = w["up_proj"], w["gate_proj"]
+    return _orig_finish(cfg, w2, x_rows, heads_out)
+
+
+def _finish_no_residual(cfg, w, x_rows, heads_out):
+    taps = _orig_finish(cfg, w, x_rows, heads_out)
+    taps["layer_output"] = taps["layer_output"] - x_rows
+    return taps
+
+
+_orig_finish = ob._finish_rows
+
+MUTATIONS = {
+    "rms_eps_outside_sqrt": [("rms_norm", _rms_eps_outside)],
+    "rms_sum_not_mean": [("rms_norm", _rms_sum)],
+    "rope_interleaved_pairs": [("rope", _rope_interleaved)],
+    "rope_inv_freq_exponent": [("rope_inv_freq", _inv_freq_wrong)],
+    "rope_rotation_sign": [("rope", _rope_sign)],
+    "attn_no_scale": [("causal_gqa_attention", _attn_factory(scale=False))],
+    "attn_gqa_modulo": [("causal_gqa_attention", _attn_factory(gqa="mod"))],
+    "attn_mask_off_by_one": [("causal_gqa_attention", _attn_factory(strict=True))],
+    "xielu_beta_sign": [("xielu", _xielu_beta_sign)],
+    "xielu_dropped_min_and_sign": [("xielu", _xielu_no_min)],
+    "silu_sign": [("silu", _silu_wrong)],
+    "relu_not_squared": [("relu2", _relu_not_squared)],
+    "swiglu_gate_up_swapped": [("_finish_rows", _finish_swapped)],
+    "missing_residual": [("_finish_rows", _finish_no_residual)],
+}
+
+PIN_TESTS = [
+    pins.test_rmsnorm_worked_example,
+    pins.test_rmsnorm_eps_inside_sqrt,
+    pins.test_rope_worked_values,
+    pins.test_rope_matches_complex_rotation,
+    pins.test_attention_brute_force,
+    pins.test_attention_special_cases,
+    pins.test_attention_gqa_reach,
+    pins.test_relu2_exact_zeros,
+    pins.test_xielu_page_values,
+    pins.test_silu_textbook_properties,
+    lambda: pins.test_block_brute_force("silu", False, 2, 2),
+    lambda: pins.test_block_brute_force("relu2", False, 4, 2),
+    lambda: pins.test_block_brute_force("xielu", True, 4, 1),
+    pins.test_block_identity_and_taps,
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, monkeypatch):
+    for attr, fn in MUTATIONS[name]:
+        monkeypatch.setattr(ob, attr, fn)
+        if hasattr(oracle, attr):
+            monkeypatch.setattr(oracle, attr, fn)
+    caught = []
+    for t in PIN_TESTS:
+        try:
+            t()
+        except AssertionError:
+            caught.append(getattr(t, "__name__", "block"))
+    assert caught, f"no pin caught mutation {name}"
