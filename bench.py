@@ -1,0 +1,356 @@
+"""Benchmark of one decoder-block forward pass on GB300, as one JSON line.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one blk_forward over the workload's synthetic batch (all stages of the
+block). Default workload: the Llama-7B-shape bf16 prefill block, batch 1 x 2048
+tokens. Inputs and weights are resident in HBM before timing; L2 is flushed
+(a 256 MiB write) between timed steps, outside the timed events. value is
+whole-job tokens/s; e2e repeats the measurement with the input copied from
+pinned host memory and the output read back inside each step.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (the only other place this script runs the oracle is the
+cpu_baseline leg of our own line).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decoder-block tokens/s (bf16, 1×GB300) and % of BF16 tensor-core / HBM roofline"
+DEFAULT_WORKLOAD = "llama7b_bf16_B1_T2048"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- work counts
+
+def work_counts(wl):
+    """Algorithmic FLOPs and bytes of the block and of each stage (one step)."""
+    B, T, D, H, Hkv, d, F = wl.batch, wl.seq, wl.hidden_size, wl.num_heads, wl.num_kv_heads, wl.head_dim, \
+        wl.intermediate_size
+    M = B * T
+    es = 2 if wl.dtype == "bf16" else 4
+    n_up = 2 * F if wl.hidden_act == "silu" else F
+    g = {"qkv": 2.0 * M * D * (H + 2 * Hkv) * d, "o": 2.0 * M * H * d * D, "up": 2.0 * M * D * n_up,
+         "down": 2.0 * M * F * D}
+    if wl.cache_len:
+        L = wl.cache_len + 1
+        g["attn"] = 4.0 * B * H * d * L
+        kv_bytes = 2.0 * B * Hkv * L * d * es
+    else:
+        g["attn"] = 4.0 * B * H * d * T * (T + 1) / 2
+        kv_bytes = 0.0
+    weight_bytes = es * (D * (H + 2 * Hkv) * d + H * d * D + n_up * D + F * D + 2 * D)
+    return g, weight_bytes, kv_bytes
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+
+def oracle_tokens_per_s(wl, w_cpu, x_cpu, cache_cpu, tokens_cap):
+    """fp64 oracle on a bounded sample of the workload; returns (tokens/s, sample text, seconds)."""
+    import numpy as np
+
+    import oracle
+    cfg = oracle.BlockConfig(wl.hidden_size, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.intermediate_size,
+                             wl.hidden_act, wl.rms_norm_eps, wl.rope_theta, wl.qk_norm, wl.xielu_alpha_p,
+                             wl.xielu_alpha_n)
+    wn = {k: v.double().numpy() for k, v in w_cpu.items()}
+    t0 = time.perf_counter()
+    if wl.cache_len:
+        nb = max(1, min(wl.batch, tokens_cap))
+        kc, vc = cache_cpu
+        lens = np.full(nb, wl.cache_len)
+        oracle.decode_step(cfg, wn, x_cpu[:nb, 0].double().numpy(), kc[:nb].double().numpy(),
+                           vc[:nb].double().numpy(), lens)
+        ntok = nb
+        sample = f"{nb} of {wl.batch} sequences, one decode token each over a {wl.cache_len}-position cache"
+    else:
+        T = min(wl.seq, tokens_cap)
+        oracle.block_forward(cfg, wn, x_cpu[:1, :T].double().numpy())
+        ntok = T
+        sample = f"sequence 0, first {T} of {wl.seq} tokens (full block, causal prefix)"
+    dt = time.perf_counter() - t0
+    return ntok / dt, sample, dt
+
+
+def run_reference(args, wl):
+    """--impl reference: the fp64 oracle on the host cores, same metric/unit/config."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from llama_family_decoder_gb300.synth import make_input, make_kv_cache, make_weights
+    w = make_weights(wl)
+    x = make_input(wl)
+    cache = make_kv_cache(wl) if wl.cache_len else None
+    cap = 2 if wl.cache_len else 256  # per step: a bounded sample (seconds)
+    times, sample = [], ""
+    for i in range(args.warmup + args.steps):
+        tps, sample, dt = oracle_tokens_per_s(wl, w, x, cache, cap)
+        if i >= args.warmup:
+            times.append(dt)
+    ntok = cap if not wl.cache_len else min(cap, wl.batch)
+    ntok = min(ntok, wl.seq) if not wl.cache_len else ntok
+    value = ntok * len(times) / sum(times)
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def config_of(wl, n):
+    c = {"workload": wl.name, "batch": wl.batch, "seq": wl.seq, "hidden": wl.hidden_size, "heads": wl.num_heads,
+         "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "ffn": wl.intermediate_size, "act": wl.hidden_act,
+         "qk_norm": wl.qk_norm, "l2": "flushed between timed steps (256 MiB write)",
+         "parallelism": "replicas" if n > 1 else "single"}
+    if wl.cache_len:
+        c["cache_len"] = wl.cache_len
+    return c
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    from llama_family_decoder_gb300 import DecoderBlock
+    from llama_family_decoder_gb300.synth import make_input, make_kv_cache, make_weights
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+
+    w_cpu = make_weights(wl, seed=wl.seed + 17 * rank)
+    x_cpu = make_input(wl, seed=wl.seed + 17 * rank)
+    w = {k: v.to(dev) for k, v in w_cpu.items()}
+    x = x_cpu.to(dev)
+    decode = wl.cache_len > 0
+    cache = None
+    cache_cpu = None
+    if decode:
+        cache_cpu = make_kv_cache(wl)
+        kc, vc = (t.to(dev) for t in cache_cpu)
+        lens0 = torch.full((wl.batch,), wl.cache_len, dtype=torch.int32, device=dev)
+        cache = {"k": kc, "v": vc, "lens": lens0.clone()}
+    blk = DecoderBlock.from_workload(wl)
+    out = torch.empty_like(x)
+    ws = torch.empty(blk.workspace_bytes(wl.batch, wl.seq, decode), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if decode:
+            cache["lens"].copy_(lens0)  # every step decodes the same token position
+        blk.forward(x, w, cache=cache, out=out, workspace=ws, stream=stream,
+                    host_lens_max=wl.cache_len if decode else -1)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    blk.profile(True)
+    blk.profile_reset()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            if decode:
+                cache["lens"].copy_(lens0)
+            starts[i].record(stream)
+            blk.forward(x, w, cache=cache, out=out, workspace=ws, stream=stream,
+                        host_lens_max=wl.cache_len if decode else -1)
+            ends[i].record(stream)
+            blk.profile_collect()  # waits for this step; adds its per-stage event times
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    stages = blk.profile_collect()
+    blk.profile(False)
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens = wl.batch * wl.seq
+    value = world * tokens * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the C ABI with host buffers
+    x_host = x_cpu.pin_memory()
+    out_host = torch.empty_like(x_cpu).pin_memory()
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        if decode:
+            cache["lens"].copy_(lens0)
+        e_starts[i].record(stream)
+        x.copy_(x_host, non_blocking=True)
+        blk.forward(x, w, cache=cache, out=out, workspace=ws, stream=stream,
+                    host_lens_max=wl.cache_len if decode else -1)
+        out_host.copy_(out, non_blocking=True)
+        e_ends[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    nbytes = x_cpu.numel() * x_cpu.element_size()
+
+    # ---- roofline of the dominant kernel (its live event times)
+    peaks = _peaks()
+    g, weight_bytes, kv_bytes = work_counts(wl)
+    launches = sum(n for _, n in stages.values())
+    if decode:
+        name = "attention_splitkv"
+        ms = stages[name][0] / args.steps
+        es = 2 if wl.dtype == "bf16" else 4
+        algo = kv_bytes + wl.batch * wl.num_heads * wl.head_dim * es * 2
+        achieved = algo / (ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "attn_decode_kernel (split-KV)", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "algorithmic_bytes": algo, "peak_source": peaks["source"]}
+    else:
+        name = "mlp_up_gemm_act"
+        ms = stages[name][0] / args.steps
+        achieved = g["up"] / (ms / 1e3) / 1e12
+        pk = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "kernel": "tc_gemm_kernel (MLP up/gate + activation)", "achieved": achieved,
+                "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk, "traffic": None, "algorithmic_flops": g["up"],
+                "peak_source": f"{peaks['source']} sustained bf16 (burst {peaks['bf16_tflops']})"}
+    total_flops = sum(g.values())
+    block = {"tflops": total_flops / (ms_per_step / 1e3) / 1e12,
+             "frac_of_bf16_sustained": total_flops / (ms_per_step / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
+             "frac_of_bf16_spec_2250": total_flops / (ms_per_step / 1e3) / 1e12 / 2250.0,
+             "hbm_gbs_weights_plus_kv": (weight_bytes + kv_bytes) / (ms_per_step / 1e3) / 1e9}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded N(0,0.02) weights, N(0,1) input)",
+            "config": config_of(wl, world), "roofline": roof,
+            "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
+                    "d2h_bytes_per_step": nbytes},
+            "gpu_launches": launches, "clocks": clk.summary(),
+            "stages_ms": {k: v[0] / args.steps for k, v in stages.items()}, "block": block}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cap = 4 if decode else wl.seq
+        tps, sample, dt = oracle_tokens_per_s(wl, w_cpu, x_cpu, cache_cpu, cap)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": sample, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from llama_family_decoder_gb300.synth import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,244 @@
+/*
+ * blk.h — C ABI of a GB300 (sm_103a) library for the forward pass of one
+ * Llama-style decoder block.
+ *
+ * The block (nnterp encyclopedia "arcee", "The block, in order"; the
+ * "LlamaForCausalLM-32L-4096d" sheet, "Implementing it"):
+ *
+ *   h   = x + o_proj(attn(rope(qk_norm(q_proj(n1))), rope(qk_norm(k_proj(n1))), v_proj(n1)))
+ *         with n1 = rmsnorm(x, input_layernorm)
+ *   out = h + down_proj(act(...(rmsnorm(h, post_attention_layernorm))))
+ *
+ * act is gated SiLU (silu(gate) * up, the sheet's pseudo-code), squared ReLU
+ * ("arcee": relu(up)^2) or xIELU ("apertus", "The MLP has no gate").
+ * q_norm/k_norm are optional per-head RMSNorms before the rotary ("apertus",
+ * "Queries and keys are normed per head, before the rotary"). Attention is
+ * causal softmax(q k^T / sqrt(head_dim)) v with key/value head j serving query
+ * heads j*G .. j*G+G-1, G = num_heads / num_kv_heads ("arcee", "Grouped-query
+ * attention, 128-wide heads").
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers are CUDA device addresses owned by the
+ *    caller; the library never frees or keeps them past the call. Host
+ *    pointers (descriptors, weight tables) are read during the call only.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Calls enqueue work and return; they never synchronise, except
+ *    blk_last_status, which reads a device word synchronously.
+ *  - Return values are blk_status codes; no exceptions cross the ABI and the
+ *    library never exits the process. blk_error_string() names a code;
+ *    blk_last_error_message() gives the detail of the last failure on this
+ *    thread.
+ *  - Activation tensors are row-major with the innermost dimension contiguous.
+ *    Weights are PyTorch Linear weights: [out_features, in_features] row-major,
+ *    used as h @ W^T, no bias.
+ *  - Every device pointer must be 16-byte aligned (TMA and 128-bit loads);
+ *    otherwise the call returns BLK_ERR_ALIGNMENT.
+ *  - Element type is the descriptor's dtype (fp32 or bf16) for every tensor of
+ *    a call, including weights, gains and the KV cache.
+ */
+#ifndef BLK_H_
+#define BLK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BLK_OK = 0,
+  BLK_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, inconsistent shape */
+  BLK_ERR_UNSUPPORTED = 2,  /* a shape/dtype combination this build has no kernel for */
+  BLK_ERR_ALIGNMENT = 3,    /* a pointer not 16-byte aligned */
+  BLK_ERR_CACHE_FULL = 4,   /* a decode step would write past the KV cache capacity */
+  BLK_ERR_CUDA = 5,         /* a CUDA runtime/driver call or a launch failed */
+  BLK_ERR_TIMEOUT = 6,      /* a device-side wait hit its iteration budget (blk_last_status) */
+  BLK_ERR_WORKSPACE = 7     /* workspace missing or smaller than blk_workspace_bytes() */
+} blk_status;
+
+typedef enum {
+  BLK_ACT_SWIGLU = 0, /* silu(h W_gate^T) * (h W_up^T)  ("LlamaForCausalLM-32L-4096d") */
+  BLK_ACT_RELU2 = 1,  /* relu(h W_up^T)^2              ("arcee") */
+  BLK_ACT_XIELU = 2   /* xielu(h W_up^T)               ("apertus") */
+} blk_act;
+
+typedef enum { BLK_F32 = 0, BLK_BF16 = 1 } blk_dtype;
+
+/* Block description, in the pages' config keys (hidden_size, num_attention_heads,
+ * num_key_value_heads, head_dim, intermediate_size, hidden_act, rms_norm_eps,
+ * rope_theta). */
+typedef struct {
+  int hidden;        /* hidden_size D */
+  int n_heads;       /* num_attention_heads H */
+  int n_kv_heads;    /* num_key_value_heads Hkv; H % Hkv == 0 */
+  int head_dim;      /* d; even */
+  int ffn;           /* intermediate_size F */
+  float rope_theta;  /* RoPE base (10000 in the pages' configs) */
+  float eps;         /* rms_norm_eps, used by both block norms and q/k norms */
+  blk_act act;
+  float xielu_alpha_p; /* EFFECTIVE alpha_p (after softplus), see blk_xielu_effective */
+  float xielu_alpha_n; /* EFFECTIVE alpha_n (after beta + softplus) */
+  float xielu_beta;    /* 0.5 on the pages */
+  float xielu_eps;     /* -1e-6 on the pages */
+  int qk_norm;       /* 1: per-head RMSNorm of q and k over head_dim before RoPE */
+  blk_dtype dtype;   /* storage type of every tensor; accumulation is fp32 */
+  int max_batch;     /* largest batch a call may pass */
+  int max_seq;       /* largest rotary position + 1 a call may use (prefill length, or cache length + 1) */
+} blk_desc;
+
+/* Block weights: device pointers in the descriptor's dtype.
+ * Shapes: ln1_g, ln2_g [D]; wq [H*d, D]; wk, wv [Hkv*d, D]; q_norm_g, k_norm_g
+ * [d] (ignored unless qk_norm); wo [D, H*d]; w_gate [F, D] (SWIGLU only, else
+ * NULL); w_up [F, D]; w_down [D, F]. */
+typedef struct {
+  const void *ln1_g, *wq, *wk, *wv, *q_norm_g, *k_norm_g, *wo, *ln2_g;
+  const void *w_gate, *w_up, *w_down;
+} blk_weights;
+
+/* KV cache for decode: k, v are [batch, Hkv, capacity, d] in the descriptor's
+ * dtype, holding keys AFTER k_norm and RoPE. lens is a device int
+ * array [batch]: positions already filled. A decode step writes its new key and
+ * value at slot lens[b], attends over lens[b] + 1 keys and then increments
+ * lens[b] on the device. */
+typedef struct {
+  void *k, *v;
+  int capacity;
+  int *lens;
+} blk_kv_cache;
+
+/* Optional debug outputs of blk_forward (nnterp tap names, "arcee", "The API").
+ * Any member may be NULL. Device pointers in the descriptor's dtype:
+ *   attention_queries [B,H,T,d], attention_keys / attention_values [B,Hkv,T,d]
+ *   (prefill only), attention_head_outputs [B,T,H,d], attention_output,
+ *   layer_mid, mlp_output [B,T,D], mlp_neurons [B,T,F].
+ * Requesting taps may launch extra copies; it does not change layer_output. */
+typedef struct {
+  void *attention_queries, *attention_keys, *attention_values;
+  void *attention_head_outputs, *attention_output, *layer_mid;
+  void *mlp_neurons, *mlp_output;
+} blk_taps;
+
+typedef struct blk_handle blk_handle;
+
+/* Validates the descriptor and builds the handle: it owns a small device
+ * status word and the RoPE cos/sin table (max_seq x head_dim/2, fp32, computed
+ * in double on the host). No weights are copied. Requires a current CUDA
+ * device. Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+blk_status blk_create(const blk_desc* desc, blk_handle** out);
+
+/* Frees the handle and its device tables. Safe on NULL. Synchronises nothing:
+ * the caller must ensure no work using the handle is still in flight. */
+blk_status blk_destroy(blk_handle* h);
+
+/* Bytes of caller-owned device workspace blk_forward needs for this batch and
+ * sequence length (seq == 1 with a cache is a decode step; pass decode != 0).
+ * Returns 0 for invalid sizes. */
+size_t blk_workspace_bytes(const blk_handle* h, int batch, int seq, int decode);
+
+/* The whole block: out[B,T,D] = block(x[B,T,D]).
+ * cache == NULL: prefill, positions 0..T-1 per sequence, causal.
+ * cache != NULL: decode step, T must be 1; see blk_kv_cache.
+ * workspace: device scratch of at least blk_workspace_bytes(h, B, T, cache!=NULL).
+ * out must not alias x. taps may be NULL. Errors: INVALID_ARG, ALIGNMENT,
+ * UNSUPPORTED, WORKSPACE, CACHE_FULL (checked on the host only when the
+ * caller passes host_lens_max >= 0: the largest lens[b] before the step),
+ * CUDA. */
+blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const blk_weights* w,
+                       blk_kv_cache* cache, int host_lens_max, void* out, void* workspace,
+                       size_t workspace_bytes, const blk_taps* taps, void* stream);
+
+/* Stage: RMSNorm of each row (nnterp "input_layernorm" / "post_attention_layernorm"):
+ * y[r, :] = x[r, :] / sqrt(mean(x[r, :]^2) + eps) * g, statistics in fp32.
+ * x, y [rows, n], g [n], device, dtype elements; n % 8 == 0 (bf16) or n % 4 == 0
+ * (fp32), n <= 16384. y may alias x. */
+blk_status blk_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y,
+                       blk_dtype dtype, void* stream);
+
+/* Stage: Q/K/V projections of normed rows y[B*T, D], optional per-head q/k
+ * RMSNorm, RoPE at positions pos0[b] + t (pos0: device int[B], NULL = 0), and the
+ * scatter to head-major layouts q [B,H,T,d], k, v [B,Hkv,T,d].
+ * workspace: device scratch of blk_stage_workspace_bytes(h, B*T). */
+blk_status blk_qkv_rope(blk_handle* h, const void* y, const blk_weights* w, int batch, int seq,
+                        const int* pos0, void* q, void* k, void* v, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* Stage: causal grouped-query attention.
+ * q [B,H,Tq,d]; k, v with row stride kv_stride rows per (b, kv head):
+ * element (b, j, s, :) at ((b*Hkv + j)*kv_stride + s)*d. kv_lens: device int[B]
+ * with the number of valid keys per sequence, or NULL for kv_len = Tq (plain
+ * prefill). Query i of sequence b sits at position kv_len[b] - Tq + i and sees
+ * keys at positions <= its own. Output o [B,Tq,H,d] (nnterp attention_head_outputs).
+ * workspace: device scratch of blk_stage_workspace_bytes(h, B*Tq). */
+blk_status blk_attn_gqa(blk_handle* h, const void* q, const void* k, const void* v, int batch,
+                        int seq_q, int kv_stride, const int* kv_lens, void* o, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* Stage: MLP sublayer with the residual add of its rows:
+ * out[r] = resid[r] + down(act(h_normed[r])) for rows r < rows, shapes [rows, D].
+ * workspace: device scratch of blk_stage_workspace_bytes(h, rows).
+ * out may not alias h_normed; it may alias resid. */
+blk_status blk_mlp(blk_handle* h, const void* resid, const void* h_normed, const blk_weights* w,
+                   int rows, void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Scratch bytes a stage entry point needs for `rows` token rows. */
+size_t blk_stage_workspace_bytes(const blk_handle* h, int rows);
+
+/* Device-side status after the caller has synchronised the stream: BLK_OK, or
+ * BLK_ERR_TIMEOUT if a kernel's bounded wait gave up (its outputs are then
+ * invalid). Clears the word. Reads device memory synchronously. */
+blk_status blk_last_status(blk_handle* h);
+
+/* Host helper for xIELU ("apertus"): stored parameters -> effective values
+ * alpha_p = softplus(raw_p), alpha_n = beta + softplus(raw_n). */
+void blk_xielu_effective(float raw_alpha_p, float raw_alpha_n, float beta, float* alpha_p,
+                         float* alpha_n);
+
+/* Static name of a status code. */
+const char* blk_error_string(blk_status s);
+
+/* Detail of the last failing call on the calling thread ("" if none). */
+const char* blk_last_error_message(void);
+
+/* Debug knob: wall-time limit, in nanoseconds, of every device-side mbarrier
+ * wait in later launches; <= 0 restores the default (2 s). A wait that runs
+ * out records BLK_ERR_TIMEOUT in the handle's status word, waits (again with a
+ * limit) for its own copies and MMAs in flight, frees its TMEM and returns,
+ * leaving the CUDA context usable. Process-wide. */
+void blk_debug_set_wait_timeout_ns(long long ns);
+
+/* Per-stage device timing of later blk_forward calls on this handle: when on,
+ * each stage's launches are bracketed by CUDA events recorded on the caller's
+ * stream (the stages of a call run back to back; recording adds no sync).
+ * Errors: INVALID_ARG, CUDA. */
+blk_status blk_profile_enable(blk_handle* h, int on);
+
+/* Waits for the last profiled blk_forward on the handle, adds its per-stage
+ * times to running totals and copies, for i < min(max_stages, stage count):
+ * total_ms[i] (milliseconds summed over collected calls), launches[i] (kernel
+ * launches summed likewise). Returns the number of stages of that call's path
+ * (prefill or decode), or -1 on error. Either array may be NULL. */
+int blk_profile_collect(blk_handle* h, double* total_ms, long long* launches, int max_stages);
+
+/* Name of stage i of the last profiled path ("" when out of range). */
+const char* blk_profile_stage_name(const blk_handle* h, int i);
+
+/* Zeroes the running totals. */
+void blk_profile_reset(blk_handle* h);
+
+/* Debug/test entry: the bare tcgen05 GEMM, c[M, N] = bf16(a[M, K] @ b[N, K]^T)
+ * with fp32 accumulation, all bf16 row-major device pointers, N-tile bn in
+ * {64, 128, 256}, split_k >= 1 (bn == 64 only: fp32 partial sums are then
+ * written to c as float [split_k][N][M] instead). K % 8 == 0.
+ * Errors: INVALID_ARG, ALIGNMENT, CUDA. */
+blk_status blk_debug_gemm_bf16(const void* a, const void* b, void* c, int M, int N, int K, int bn, int split_k,
+                               void* stream);
+
+/* Library version string. */
+const char* blk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BLK_H_ */

@@ -1,0 +1,832 @@
+// Host library behind the C ABI in include/blk.h: descriptor validation,
+// caller-owned workspace layout, and the launch sequence of the decoder block
+// ("LlamaForCausalLM-32L-4096d" sheet, "Implementing it"; nnterp "arcee" and
+// "apertus", "The block, in order").
+//
+// bf16 prefill:  rmsnorm -> tcgen05 QKV GEMM (+q/k norm, RoPE, head scatter)
+//                -> flash attention -> tcgen05 o_proj (+residual) -> rmsnorm
+//                -> tcgen05 up/gate GEMM (+activation) -> tcgen05 down (+residual)
+// bf16 decode:   rmsnorm -> weight-streaming tcgen05 GEMMs (tokens on N,
+//                split-K partials) with post kernels (q/k norm + RoPE + cache
+//                append; residual + next rmsnorm; activation) and split-KV
+//                attention.
+// fp32 path:     the same sequence on SIMT fp32 GEMMs and fp32 attention.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/blk.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace blk;
+
+// Per-stage event timing of blk_forward (blk_profile_*).
+struct StageProfile {
+  static constexpr int kMax = 24;
+  bool on = false;
+  bool pending = false;
+  int n = 0;
+  const char* names[kMax] = {};
+  int launches[kMax] = {};
+  cudaEvent_t ev[kMax + 1] = {};
+  double total_ms[kMax] = {};
+  long long total_launches[kMax] = {};
+};
+
+struct blk_handle {
+  blk_desc d;
+  int device;
+  int num_sms;
+  float2* rope;        // [max_seq][head_dim/2] (cos, sin) as fp32, from double
+  DevStatus* status;   // device
+  StageProfile prof;
+};
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<long long> g_wait_ns{2000000000LL};
+
+blk_status fail(blk_status s, const std::string& msg) {
+  g_err = msg;
+  return s;
+}
+
+blk_status cuda_fail(cudaError_t e, const char* where, const char* why = nullptr) {
+  std::string m = std::string(where) + ": " + cudaGetErrorString(e);
+  if (why) m += std::string(" (") + why + ")";
+  return fail(BLK_ERR_CUDA, m);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t esize(const blk_desc& d) { return d.dtype == BLK_BF16 ? 2 : 4; }
+
+// Bump allocator over the caller's workspace (or a size counter when base is null).
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(static_cast<uint8_t*>(b)) {}
+  void* take(size_t bytes) {
+    off = (off + 255) & ~size_t(255);
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+int qkv_cols(const blk_desc& d) { return (d.n_heads + 2 * d.n_kv_heads) * d.head_dim; }
+int mlp_cols(const blk_desc& d) { return d.act == BLK_ACT_SWIGLU ? 2 * d.ffn : d.ffn; }
+int max_cols(const blk_desc& d) {
+  int n = qkv_cols(d);
+  if (d.hidden > n) n = d.hidden;
+  if (mlp_cols(d) > n) n = mlp_cols(d);
+  return n;
+}
+
+constexpr int kMaxDecodeSplits = 16;
+
+// Workspace regions of a forward call.
+struct Ws {
+  void *y, *q, *k, *v, *o, *mid, *neur, *C, *attn;
+};
+
+Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, size_t* total) {
+  const blk_desc& d = h->d;
+  const size_t es = esize(d);
+  const size_t M = (size_t)B * T;
+  Carve c(base);
+  Ws w{};
+  w.y = c.take(M * d.hidden * es);
+  w.q = c.take(M * d.n_heads * d.head_dim * es);
+  if (!decode) {
+    w.k = c.take(M * d.n_kv_heads * d.head_dim * es);
+    w.v = c.take(M * d.n_kv_heads * d.head_dim * es);
+  }
+  w.o = c.take(M * d.n_heads * d.head_dim * es);
+  w.mid = c.take(M * d.hidden * es);
+  w.neur = c.take(M * d.ffn * es);
+  if (decode) {
+    const int splits = d.dtype == BLK_BF16 ? kMaxDecodeSplits : 1;
+    w.C = c.take((size_t)splits * M * max_cols(d) * sizeof(float));
+    if (d.dtype == BLK_BF16) {
+      const int s = attn_decode_splits(B, d.n_kv_heads, 1 << 30, h->num_sms);
+      w.attn = c.take(attn_decode_ws_bytes(B, d.n_heads, d.head_dim, s));
+    }
+  } else if (d.dtype == BLK_F32) {
+    w.C = c.take(M * max_cols(d) * sizeof(float));
+  }
+  *total = c.off;
+  return w;
+}
+
+// Split count for a weight-streaming GEMM: balance the work units over the SMs
+// (units = tiles x splits), charging each extra split for its partial-sum traffic.
+int choose_splits(int tiles, int num_kb, int num_sms) {
+  int best = 1;
+  double best_cost = 1e30;
+  for (int s = 1; s <= kMaxDecodeSplits && s <= num_kb / 4 + (s == 1); ++s) {
+    const double units = (double)tiles * s;
+    const double waves = std::ceil(units / num_sms);
+    const double cost = waves * num_sms / units + 0.03 * s;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+TcEpiArgs qkv_epi(const blk_handle* h, const blk_weights* w, int seq, const int* pos0, void* q, void* k, void* v) {
+  const blk_desc& d = h->d;
+  TcEpiArgs e;
+  e.q = q;
+  e.k = k;
+  e.v = v;
+  e.seq = seq;
+  e.n_heads = d.n_heads;
+  e.n_kv_heads = d.n_kv_heads;
+  e.head_dim = d.head_dim;
+  e.kv_stride = seq;
+  e.q_gain = w->q_norm_g;
+  e.k_gain = w->k_norm_g;
+  e.eps = d.eps;
+  e.rope = h->rope;
+  e.rope_max_pos = d.max_seq;
+  e.pos0 = pos0;
+  e.qk_norm = d.qk_norm;
+  return e;
+}
+
+// ------------------------------------------------------------------ bf16 prefill pieces
+
+blk_status tc(const blk_handle* h, const TcGemmDesc& g, cudaStream_t s, const char* what) {
+  const char* why = nullptr;
+  cudaError_t e = launch_tc_gemm(g, h->num_sms, h->status, (unsigned long long)g_wait_ns.load(), s, &why);
+  if (e != cudaSuccess) return cuda_fail(e, what, why);
+  return BLK_OK;
+}
+
+blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, int B, int T, const int* pos0, void* q,
+                    void* k, void* v, cudaStream_t s) {
+  const blk_desc& d = h->d;
+  TcGemmDesc g;
+  g.na = 1;
+  g.a[0] = {y, B * T, 0};
+  g.nb = 3;
+  g.b[0] = {w->wq, d.n_heads * d.head_dim, 0};
+  g.b[1] = {w->wk, d.n_kv_heads * d.head_dim, d.n_heads * d.head_dim};
+  g.b[2] = {w->wv, d.n_kv_heads * d.head_dim, (d.n_heads + d.n_kv_heads) * d.head_dim};
+  g.K = d.hidden;
+  g.bn = ((d.n_heads * d.head_dim) % 256 == 0 && (d.n_kv_heads * d.head_dim) % 256 == 0) ? 256 : 128;
+  g.epi = Epi::kQkv;
+  g.e = qkv_epi(h, w, T, pos0, q, k, v);
+  return tc(h, g, s, "QKV GEMM");
+}
+
+blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K, const void* W, int N,
+                             const void* resid, void* out, void* tap, cudaStream_t s, const char* what) {
+  TcGemmDesc g;
+  g.na = 1;
+  g.a[0] = {a, rows, 0};
+  g.nb = 1;
+  g.b[0] = {W, N, 0};
+  g.K = K;
+  g.bn = 256;
+  g.epi = Epi::kResid;
+  g.e.out = out;
+  g.e.ldo = N;
+  g.e.resid = resid;
+  g.e.tap = tap;
+  return tc(h, g, s, what);
+}
+
+blk_status bf16_mlp_up(const blk_handle* h, const void* y2, int rows, const blk_weights* w, void* neur,
+                       cudaStream_t s) {
+  const blk_desc& d = h->d;
+  TcGemmDesc g;
+  g.na = 1;
+  g.a[0] = {y2, rows, 0};
+  g.K = d.hidden;
+  g.bn = 256;
+  g.e.out = neur;
+  g.e.ldo = d.ffn;
+  if (d.act == BLK_ACT_SWIGLU) {
+    g.nb = 2;
+    g.b_paired = true;
+    g.b[0] = {w->w_gate, d.ffn, 0};
+    g.b[1] = {w->w_up, d.ffn, 0};
+    g.epi = Epi::kSwiglu;
+  } else {
+    g.nb = 1;
+    g.b[0] = {w->w_up, d.ffn, 0};
+    g.epi = d.act == BLK_ACT_RELU2 ? Epi::kRelu2 : Epi::kXielu;
+    g.e.alpha_p = d.xielu_alpha_p;
+    g.e.alpha_n = d.xielu_alpha_n;
+    g.e.beta = d.xielu_beta;
+    g.e.xeps = d.xielu_eps;
+  }
+  return tc(h, g, s, "MLP up GEMM");
+}
+
+// ------------------------------------------------------------------ decode pieces (bf16)
+
+blk_status bf16_stream_gemm(const blk_handle* h, const TcSeg* segs, int nseg, const void* x, int B, int K, float* C,
+                            int ldc, int* splits_out, cudaStream_t s, const char* what) {
+  TcGemmDesc g;
+  g.na = nseg;
+  int tiles = 0;
+  for (int i = 0; i < nseg; ++i) {
+    g.a[i] = segs[i];
+    tiles += (segs[i].rows + 127) / 128;
+  }
+  g.nb = 1;
+  g.b[0] = {x, B, 0};
+  g.K = K;
+  g.bn = B <= 64 ? 64 : (B <= 128 ? 128 : 256);
+  const int n_tiles = (B + g.bn - 1) / g.bn;
+  g.k_splits = choose_splits(tiles * n_tiles, (K + 63) / 64, h->num_sms);
+  g.epi = Epi::kPartialT;
+  g.e.out = C;
+  g.e.part_ld = ldc;
+  g.e.n_tok = B;
+  *splits_out = g.k_splits;
+  return tc(h, g, s, what);
+}
+
+void prof_mark(blk_handle* h, const char* name, int launches, cudaStream_t s) {
+  StageProfile& p = h->prof;
+  if (!p.on || p.n >= StageProfile::kMax) return;
+  cudaEventRecord(p.ev[p.n], s);
+  p.names[p.n] = name;
+  p.launches[p.n] = launches;
+  ++p.n;
+}
+
+void prof_begin(blk_handle* h) {
+  if (h->prof.on) h->prof.n = 0;
+}
+
+void prof_end(blk_handle* h, cudaStream_t s) {
+  StageProfile& p = h->prof;
+  if (!p.on || p.n == 0) return;
+  cudaEventRecord(p.ev[p.n], s);
+  p.pending = true;
+}
+
+blk_status check_cuda(cudaError_t e, const char* where, const char* why = nullptr) {
+  return e == cudaSuccess ? BLK_OK : cuda_fail(e, where, why);
+}
+
+#define BLK_TRY(expr)                  \
+  do {                                 \
+    blk_status st_ = (expr);           \
+    if (st_ != BLK_OK) return st_;     \
+  } while (0)
+
+template <typename P>
+P tap_or(const blk_taps* t, P blk_taps::*m, P dflt) {
+  return (t && t->*m) ? t->*m : dflt;
+}
+
+// ------------------------------------------------------------------ forward variants
+
+blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, const blk_weights* w, void* out,
+                                const Ws& ws, const blk_taps* taps, cudaStream_t s) {
+  const blk_desc& d = h->d;
+  const int M = B * T;
+  const bool bf = true;
+  void* q = tap_or(taps, &blk_taps::attention_queries, ws.q);
+  void* k = tap_or(taps, &blk_taps::attention_keys, ws.k);
+  void* v = tap_or(taps, &blk_taps::attention_values, ws.v);
+  void* o = tap_or(taps, &blk_taps::attention_head_outputs, ws.o);
+  void* mid = tap_or(taps, &blk_taps::layer_mid, ws.mid);
+  void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
+  prof_mark(h, "rmsnorm1", 1, s);
+  BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, M, d.hidden, d.eps, ws.y, bf, s), "rmsnorm 1"));
+  prof_mark(h, "qkv_gemm_rope", 1, s);
+  BLK_TRY(bf16_qkv(h, ws.y, w, B, T, nullptr, q, k, v, s));
+  prof_mark(h, "attention", 1, s);
+  const char* why = nullptr;
+  cudaError_t e = launch_attn_prefill_bf16(q, k, v, o, B, d.n_heads, d.n_kv_heads, T, d.head_dim, T, s, &why);
+  BLK_TRY(check_cuda(e, "attention", why));
+  prof_mark(h, "o_proj_gemm_resid", 1, s);
+  BLK_TRY(bf16_linear_resid(h, o, M, d.n_heads * d.head_dim, w->wo, d.hidden, x, mid,
+                            taps ? taps->attention_output : nullptr, s, "o_proj GEMM"));
+  prof_mark(h, "rmsnorm2", 1, s);
+  BLK_TRY(check_cuda(launch_rmsnorm(mid, w->ln2_g, M, d.hidden, d.eps, ws.y, bf, s), "rmsnorm 2"));
+  prof_mark(h, "mlp_up_gemm_act", 1, s);
+  BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s));
+  prof_mark(h, "down_gemm_resid", 1, s);
+  BLK_TRY(bf16_linear_resid(h, neur, M, d.ffn, w->w_down, d.hidden, mid, out, taps ? taps->mlp_output : nullptr, s,
+                            "down GEMM"));
+  prof_end(h, s);
+  return BLK_OK;
+}
+
+blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_weights* w, blk_kv_cache* cache,
+                               int max_len, void* out, const Ws& ws, const blk_taps* taps, cudaStream_t s) {
+  const blk_desc& d = h->d;
+  const bool bf = true;
+  const int Hd = d.n_heads * d.head_dim, KVd = d.n_kv_heads * d.head_dim;
+  float* C = static_cast<float*>(ws.C);
+  void* q = tap_or(taps, &blk_taps::attention_queries, ws.q);
+  void* o = tap_or(taps, &blk_taps::attention_head_outputs, ws.o);
+  void* mid = tap_or(taps, &blk_taps::layer_mid, ws.mid);
+  void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
+  int sp = 1;
+  prof_mark(h, "rmsnorm1", 1, s);
+  BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, B, d.hidden, d.eps, ws.y, bf, s), "rmsnorm 1"));
+  prof_mark(h, "qkv_gemm", 1, s);
+  {
+    const TcSeg segs[3] = {{w->wq, Hd, 0}, {w->wk, KVd, Hd}, {w->wv, KVd, Hd + KVd}};
+    BLK_TRY(bf16_stream_gemm(h, segs, 3, ws.y, B, d.hidden, C, qkv_cols(d), &sp, s, "decode QKV GEMM"));
+  }
+  prof_mark(h, "qkv_post_rope_append", 1, s);
+  BLK_TRY(check_cuda(launch_post_qkv(C, sp, B, qkv_cols(d), 1, nullptr, cache->lens, d.n_heads, d.n_kv_heads,
+                                     d.head_dim, d.qk_norm, w->q_norm_g, w->k_norm_g, d.eps, h->rope, d.max_seq, q,
+                                     cache->k, cache->v, cache->capacity, bf, s),
+                     "decode qkv post"));
+  prof_mark(h, "attention_splitkv", 2, s);
+  const char* why = nullptr;
+  cudaError_t e = launch_attn_decode_bf16(q, cache->k, cache->v, o, B, d.n_heads, d.n_kv_heads, d.head_dim,
+                                          cache->capacity, cache->lens, 1, max_len, ws.attn, h->num_sms, s, &why);
+  BLK_TRY(check_cuda(e, "decode attention", why));
+  prof_mark(h, "o_proj_gemm", 1, s);
+  {
+    const TcSeg segs[1] = {{w->wo, d.hidden, 0}};
+    BLK_TRY(bf16_stream_gemm(h, segs, 1, o, B, Hd, C, d.hidden, &sp, s, "decode o_proj GEMM"));
+  }
+  prof_mark(h, "o_post_resid_rmsnorm2", 1, s);
+  BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, x, mid, taps ? taps->attention_output : nullptr,
+                                       w->ln2_g, d.eps, ws.y, nullptr, bf, s),
+                     "decode o_proj post"));
+  prof_mark(h, "mlp_up_gemm", 1, s);
+  if (d.act == BLK_ACT_SWIGLU) {
+    const TcSeg segs[2] = {{w->w_gate, d.ffn, 0}, {w->w_up, d.ffn, d.ffn}};
+    BLK_TRY(bf16_stream_gemm(h, segs, 2, ws.y, B, d.hidden, C, 2 * d.ffn, &sp, s, "decode gate/up GEMM"));
+  } else {
+    const TcSeg segs[1] = {{w->w_up, d.ffn, 0}};
+    BLK_TRY(bf16_stream_gemm(h, segs, 1, ws.y, B, d.hidden, C, d.ffn, &sp, s, "decode up GEMM"));
+  }
+  prof_mark(h, "mlp_act", 1, s);
+  BLK_TRY(check_cuda(launch_post_act(C, sp, B, d.ffn, mlp_cols(d), (int)d.act, d.xielu_alpha_p, d.xielu_alpha_n,
+                                     d.xielu_beta, d.xielu_eps, neur, bf, s),
+                     "decode activation"));
+  prof_mark(h, "down_gemm", 1, s);
+  {
+    const TcSeg segs[1] = {{w->w_down, d.hidden, 0}};
+    BLK_TRY(bf16_stream_gemm(h, segs, 1, neur, B, d.ffn, C, d.hidden, &sp, s, "decode down GEMM"));
+  }
+  prof_mark(h, "down_post_resid", 1, s);
+  BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, mid, out, taps ? taps->mlp_output : nullptr,
+                                       nullptr, 0.f, nullptr, cache->lens, bf, s),
+                     "decode down post"));
+  prof_end(h, s);
+  return BLK_OK;
+}
+
+// fp32 path: prefill (cache == null) or decode (cache != null, T == 1).
+blk_status forward_f32(blk_handle* h, const void* x, int B, int T, const blk_weights* w, blk_kv_cache* cache,
+                       void* out, const Ws& ws, const blk_taps* taps, cudaStream_t s) {
+  const blk_desc& d = h->d;
+  const bool bf = false;
+  const int M = B * T;
+  const int Hd = d.n_heads * d.head_dim, KVd = d.n_kv_heads * d.head_dim;
+  float* C = static_cast<float*>(ws.C);
+  const bool decode = cache != nullptr;
+  void* q = tap_or(taps, &blk_taps::attention_queries, ws.q);
+  void* k = decode ? cache->k : tap_or(taps, &blk_taps::attention_keys, ws.k);
+  void* v = decode ? cache->v : tap_or(taps, &blk_taps::attention_values, ws.v);
+  const int kv_stride = decode ? cache->capacity : T;
+  void* o = tap_or(taps, &blk_taps::attention_head_outputs, ws.o);
+  void* mid = tap_or(taps, &blk_taps::layer_mid, ws.mid);
+  void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
+  const float* y = static_cast<const float*>(ws.y);
+  prof_mark(h, "fp32_block", d.act == BLK_ACT_SWIGLU ? 13 : 12, s);
+  BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, M, d.hidden, d.eps, ws.y, bf, s), "rmsnorm 1"));
+  const int nq = qkv_cols(d);
+  BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->wq, C, nq, M, Hd, d.hidden, s), "q GEMM"));
+  BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->wk, C + Hd, nq, M, KVd, d.hidden, s), "k GEMM"));
+  BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->wv, C + Hd + KVd, nq, M, KVd, d.hidden, s), "v GEMM"));
+  BLK_TRY(check_cuda(launch_post_qkv(C, 1, M, nq, T, nullptr, decode ? cache->lens : nullptr, d.n_heads,
+                                     d.n_kv_heads, d.head_dim, d.qk_norm, w->q_norm_g, w->k_norm_g, d.eps, h->rope,
+                                     d.max_seq, q, k, v, kv_stride, bf, s),
+                     "qkv post"));
+  BLK_TRY(check_cuda(launch_attn_f32((const float*)q, (const float*)k, (const float*)v, (float*)o, B, d.n_heads,
+                                     d.n_kv_heads, T, d.head_dim, kv_stride, decode ? cache->lens : nullptr,
+                                     decode ? 1 : 0, s),
+                     "attention"));
+  BLK_TRY(check_cuda(launch_gemm_f32((const float*)o, (const float*)w->wo, C, d.hidden, M, d.hidden, Hd, s),
+                     "o_proj GEMM"));
+  BLK_TRY(check_cuda(launch_post_resid(C, 1, M, d.hidden, d.hidden, x, mid, taps ? taps->attention_output : nullptr,
+                                       w->ln2_g, d.eps, ws.y, nullptr, bf, s),
+                     "o_proj post"));
+  const int nm = mlp_cols(d);
+  if (d.act == BLK_ACT_SWIGLU) {
+    BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->w_gate, C, nm, M, d.ffn, d.hidden, s), "gate GEMM"));
+    BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->w_up, C + d.ffn, nm, M, d.ffn, d.hidden, s), "up GEMM"));
+  } else {
+    BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->w_up, C, nm, M, d.ffn, d.hidden, s), "up GEMM"));
+  }
+  BLK_TRY(check_cuda(launch_post_act(C, 1, M, d.ffn, nm, (int)d.act, d.xielu_alpha_p, d.xielu_alpha_n, d.xielu_beta,
+                                     d.xielu_eps, neur, bf, s),
+                     "activation"));
+  BLK_TRY(check_cuda(launch_gemm_f32((const float*)neur, (const float*)w->w_down, C, d.hidden, M, d.hidden, d.ffn, s),
+                     "down GEMM"));
+  BLK_TRY(check_cuda(launch_post_resid(C, 1, M, d.hidden, d.hidden, mid, out, taps ? taps->mlp_output : nullptr,
+                                       nullptr, 0.f, nullptr, decode ? cache->lens : nullptr, bf, s),
+                     "down post"));
+  prof_end(h, s);
+  return BLK_OK;
+}
+
+blk_status check_weights(const blk_desc& d, const blk_weights* w) {
+  if (!w) return fail(BLK_ERR_INVALID_ARG, "weights is NULL");
+  const void* req[] = {w->ln1_g, w->wq, w->wk, w->wv, w->wo, w->ln2_g, w->w_up, w->w_down};
+  for (const void* p : req) {
+    if (!p) return fail(BLK_ERR_INVALID_ARG, "a required weight pointer is NULL");
+    if (!aligned16(p)) return fail(BLK_ERR_ALIGNMENT, "a weight pointer is not 16-byte aligned");
+  }
+  if (d.act == BLK_ACT_SWIGLU && (!w->w_gate || !aligned16(w->w_gate)))
+    return fail(w->w_gate ? BLK_ERR_ALIGNMENT : BLK_ERR_INVALID_ARG, "SWIGLU needs an aligned w_gate");
+  if (d.qk_norm && (!w->q_norm_g || !w->k_norm_g || !aligned16(w->q_norm_g) || !aligned16(w->k_norm_g)))
+    return fail(BLK_ERR_INVALID_ARG, "qk_norm needs aligned q_norm_g and k_norm_g");
+  return BLK_OK;
+}
+
+}  // namespace
+
+// ================================================================== C ABI
+
+extern "C" {
+
+const char* blk_version(void) { return "gb300-decoder-block 0.1 (sm_103a)"; }
+
+const char* blk_error_string(blk_status s) {
+  switch (s) {
+    case BLK_OK: return "BLK_OK";
+    case BLK_ERR_INVALID_ARG: return "BLK_ERR_INVALID_ARG";
+    case BLK_ERR_UNSUPPORTED: return "BLK_ERR_UNSUPPORTED";
+    case BLK_ERR_ALIGNMENT: return "BLK_ERR_ALIGNMENT";
+    case BLK_ERR_CACHE_FULL: return "BLK_ERR_CACHE_FULL";
+    case BLK_ERR_CUDA: return "BLK_ERR_CUDA";
+    case BLK_ERR_TIMEOUT: return "BLK_ERR_TIMEOUT";
+    case BLK_ERR_WORKSPACE: return "BLK_ERR_WORKSPACE";
+  }
+  return "BLK_ERR_UNKNOWN";
+}
+
+const char* blk_last_error_message(void) { return g_err.c_str(); }
+
+void blk_debug_set_wait_timeout_ns(long long ns) { g_wait_ns.store(ns > 0 ? ns : 2000000000LL); }
+
+void blk_xielu_effective(float raw_alpha_p, float raw_alpha_n, float beta, float* alpha_p, float* alpha_n) {
+  auto softplus = [](double t) { return t > 30.0 ? t : std::log1p(std::exp(t)); };
+  if (alpha_p) *alpha_p = (float)softplus(raw_alpha_p);
+  if (alpha_n) *alpha_n = (float)(beta + softplus(raw_alpha_n));
+}
+
+blk_status blk_create(const blk_desc* desc, blk_handle** out) {
+  if (!desc || !out) return fail(BLK_ERR_INVALID_ARG, "desc/out is NULL");
+  *out = nullptr;
+  const blk_desc& d = *desc;
+  if (d.hidden <= 0 || d.n_heads <= 0 || d.n_kv_heads <= 0 || d.head_dim <= 0 || d.ffn <= 0 || d.max_batch <= 0 ||
+      d.max_seq <= 0)
+    return fail(BLK_ERR_INVALID_ARG, "sizes must be positive");
+  if (d.n_heads % d.n_kv_heads) return fail(BLK_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
+  if (d.head_dim % 2) return fail(BLK_ERR_INVALID_ARG, "head_dim must be even");
+  if (!(d.eps > 0.f) || !(d.rope_theta > 0.f)) return fail(BLK_ERR_INVALID_ARG, "eps and rope_theta must be > 0");
+  if (d.act != BLK_ACT_SWIGLU && d.act != BLK_ACT_RELU2 && d.act != BLK_ACT_XIELU)
+    return fail(BLK_ERR_INVALID_ARG, "unknown activation");
+  if (d.dtype != BLK_F32 && d.dtype != BLK_BF16) return fail(BLK_ERR_INVALID_ARG, "unknown dtype");
+  if (d.dtype == BLK_BF16) {
+    if (d.head_dim != 128) return fail(BLK_ERR_UNSUPPORTED, "bf16 path: head_dim must be 128");
+    if (d.hidden % 8 || d.ffn % 8) return fail(BLK_ERR_UNSUPPORTED, "bf16 path: hidden and ffn must be multiples of 8");
+    if (d.hidden > 16384 * 4) return fail(BLK_ERR_UNSUPPORTED, "hidden too large");
+    if (d.hidden / 8 > 8 * 256) return fail(BLK_ERR_UNSUPPORTED, "bf16 rmsnorm: hidden <= 16384");
+    if (d.n_heads / d.n_kv_heads > 16) return fail(BLK_ERR_UNSUPPORTED, "bf16 decode: at most 16 heads per KV head");
+  } else {
+    if (d.hidden % 4) return fail(BLK_ERR_UNSUPPORTED, "fp32 path: hidden must be a multiple of 4");
+    if (d.hidden / 4 > 8 * 256) return fail(BLK_ERR_UNSUPPORTED, "fp32 rmsnorm: hidden <= 8192");
+    if (d.head_dim > 256) return fail(BLK_ERR_UNSUPPORTED, "fp32 path: head_dim <= 256");
+    if (d.max_seq > 50000) return fail(BLK_ERR_UNSUPPORTED, "fp32 attention: max_seq <= 50000");
+  }
+  blk_handle* h = new blk_handle();
+  h->d = d;
+  h->rope = nullptr;
+  h->status = nullptr;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "blk_create: device query");
+  }
+  const int half = d.head_dim / 2;
+  std::vector<float2> table((size_t)d.max_seq * half);
+  for (int p = 0; p < d.max_seq; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double inv_freq = std::pow((double)d.rope_theta, -2.0 * i / (double)d.head_dim);
+      const double ang = (double)p * inv_freq;
+      table[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+    }
+  e = cudaMalloc(&h->rope, table.size() * sizeof(float2));
+  if (e == cudaSuccess) e = cudaMemcpy(h->rope, table.data(), table.size() * sizeof(float2), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMalloc(&h->status, sizeof(DevStatus));
+  if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(DevStatus));
+  if (e != cudaSuccess) {
+    if (h->rope) cudaFree(h->rope);
+    if (h->status) cudaFree(h->status);
+    delete h;
+    return cuda_fail(e, "blk_create: allocation");
+  }
+  *out = h;
+  return BLK_OK;
+}
+
+blk_status blk_destroy(blk_handle* h) {
+  if (!h) return BLK_OK;
+  blk_profile_enable(h, 0);
+  if (h->rope) cudaFree(h->rope);
+  if (h->status) cudaFree(h->status);
+  delete h;
+  return BLK_OK;
+}
+
+size_t blk_workspace_bytes(const blk_handle* h, int batch, int seq, int decode) {
+  if (!h || batch <= 0 || seq <= 0) return 0;
+  size_t total = 0;
+  carve_forward(h, nullptr, batch, seq, decode != 0, &total);
+  return total;
+}
+
+blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const blk_weights* w, blk_kv_cache* cache,
+                       int host_lens_max, void* out, void* workspace, size_t workspace_bytes, const blk_taps* taps,
+                       void* stream) {
+  if (!h || !x || !out) return fail(BLK_ERR_INVALID_ARG, "handle, x and out must be non-NULL");
+  const blk_desc& d = h->d;
+  if (batch <= 0 || seq <= 0) return fail(BLK_ERR_INVALID_ARG, "batch and seq must be positive");
+  if (batch > d.max_batch) return fail(BLK_ERR_INVALID_ARG, "batch exceeds max_batch");
+  if (!aligned16(x) || !aligned16(out)) return fail(BLK_ERR_ALIGNMENT, "x/out not 16-byte aligned");
+  if (x == out) return fail(BLK_ERR_INVALID_ARG, "out must not alias x");
+  BLK_TRY(check_weights(d, w));
+  if (taps) {
+    void* tp[] = {taps->attention_queries, taps->attention_keys, taps->attention_values,
+                  taps->attention_head_outputs, taps->attention_output, taps->layer_mid,
+                  taps->mlp_neurons, taps->mlp_output};
+    for (void* p : tp)
+      if (p && !aligned16(p)) return fail(BLK_ERR_ALIGNMENT, "a tap pointer is not 16-byte aligned");
+  }
+  const bool decode = cache != nullptr;
+  int max_len = 0;
+  if (decode) {
+    if (seq != 1) return fail(BLK_ERR_INVALID_ARG, "a decode step takes seq == 1");
+    if (!cache->k || !cache->v || !cache->lens || cache->capacity <= 0)
+      return fail(BLK_ERR_INVALID_ARG, "incomplete KV cache");
+    if (!aligned16(cache->k) || !aligned16(cache->v)) return fail(BLK_ERR_ALIGNMENT, "cache not 16-byte aligned");
+    if (host_lens_max >= 0) {
+      if (host_lens_max + 1 > cache->capacity) return fail(BLK_ERR_CACHE_FULL, "cache capacity exceeded");
+      if (host_lens_max + 1 > d.max_seq) return fail(BLK_ERR_INVALID_ARG, "position beyond max_seq");
+      max_len = host_lens_max + 1;
+    } else {
+      max_len = cache->capacity < d.max_seq ? cache->capacity : d.max_seq;
+    }
+  } else if (seq > d.max_seq) {
+    return fail(BLK_ERR_INVALID_ARG, "seq exceeds max_seq");
+  }
+  size_t need = 0;
+  Ws ws = carve_forward(h, workspace, batch, seq, decode, &need);
+  if (!workspace || workspace_bytes < need) return fail(BLK_ERR_WORKSPACE, "workspace missing or too small");
+  if (!aligned16(workspace)) return fail(BLK_ERR_ALIGNMENT, "workspace not 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  prof_begin(h);
+  if (d.dtype == BLK_F32) return forward_f32(h, x, batch, seq, w, cache, out, ws, taps, s);
+  if (decode) return forward_decode_bf16(h, x, batch, w, cache, max_len, out, ws, taps, s);
+  return forward_prefill_bf16(h, x, batch, seq, w, out, ws, taps, s);
+}
+
+blk_status blk_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y, blk_dtype dtype,
+                       void* stream) {
+  if (!x || !g || !y) return fail(BLK_ERR_INVALID_ARG, "x, g and y must be non-NULL");
+  if (rows < 0 || n <= 0) return fail(BLK_ERR_INVALID_ARG, "bad sizes");
+  if (!aligned16(x) || !aligned16(g) || !aligned16(y)) return fail(BLK_ERR_ALIGNMENT, "pointers not 16-byte aligned");
+  const int vec = dtype == BLK_BF16 ? 8 : 4;
+  if (n % vec) return fail(BLK_ERR_UNSUPPORTED, "n must be a multiple of 8 (bf16) or 4 (fp32)");
+  if (n / vec > 8 * 256) return fail(BLK_ERR_UNSUPPORTED, "n too large");
+  return check_cuda(launch_rmsnorm(x, g, rows, n, eps, y, dtype == BLK_BF16, static_cast<cudaStream_t>(stream)),
+                    "rmsnorm");
+}
+
+size_t blk_stage_workspace_bytes(const blk_handle* h, int rows) {
+  if (!h || rows <= 0) return 0;
+  const blk_desc& d = h->d;
+  Carve c(nullptr);
+  c.take((size_t)rows * d.ffn * esize(d));                              // neurons
+  c.take((size_t)rows * max_cols(d) * sizeof(float));                   // fp32 GEMM output
+  const int s = attn_decode_splits(rows, d.n_kv_heads, 1 << 30, h->num_sms);
+  c.take(attn_decode_ws_bytes(rows, d.n_heads, d.head_dim, s));         // decode attention partials
+  return c.off;
+}
+
+blk_status blk_qkv_rope(blk_handle* h, const void* y, const blk_weights* w, int batch, int seq, const int* pos0,
+                        void* q, void* k, void* v, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h || !y || !w || !q || !k || !v) return fail(BLK_ERR_INVALID_ARG, "NULL argument");
+  const blk_desc& d = h->d;
+  if (batch <= 0 || seq <= 0) return fail(BLK_ERR_INVALID_ARG, "bad sizes");
+  if (!aligned16(y) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return fail(BLK_ERR_ALIGNMENT, "alignment");
+  if (!w->wq || !w->wk || !w->wv) return fail(BLK_ERR_INVALID_ARG, "wq/wk/wv NULL");
+  if (d.qk_norm && (!w->q_norm_g || !w->k_norm_g)) return fail(BLK_ERR_INVALID_ARG, "q/k norm gains NULL");
+  if (!pos0 && seq > d.max_seq) return fail(BLK_ERR_INVALID_ARG, "seq exceeds max_seq");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d.dtype == BLK_BF16) return bf16_qkv(h, y, w, batch, seq, pos0, q, k, v, s);
+  const int M = batch * seq;
+  if (!workspace || workspace_bytes < blk_stage_workspace_bytes(h, M)) return fail(BLK_ERR_WORKSPACE, "workspace");
+  Carve c(workspace);
+  c.take((size_t)M * d.ffn * esize(d));
+  float* C = static_cast<float*>(c.take((size_t)M * max_cols(d) * sizeof(float)));
+  const int Hd = d.n_heads * d.head_dim, KVd = d.n_kv_heads * d.head_dim, nq = qkv_cols(d);
+  const float* yy = static_cast<const float*>(y);
+  BLK_TRY(check_cuda(launch_gemm_f32(yy, (const float*)w->wq, C, nq, M, Hd, d.hidden, s), "q GEMM"));
+  BLK_TRY(check_cuda(launch_gemm_f32(yy, (const float*)w->wk, C + Hd, nq, M, KVd, d.hidden, s), "k GEMM"));
+  BLK_TRY(check_cuda(launch_gemm_f32(yy, (const float*)w->wv, C + Hd + KVd, nq, M, KVd, d.hidden, s), "v GEMM"));
+  return check_cuda(launch_post_qkv(C, 1, M, nq, seq, pos0, nullptr, d.n_heads, d.n_kv_heads, d.head_dim, d.qk_norm,
+                                    w->q_norm_g, w->k_norm_g, d.eps, h->rope, d.max_seq, q, k, v, seq, false, s),
+                    "qkv post");
+}
+
+blk_status blk_attn_gqa(blk_handle* h, const void* q, const void* k, const void* v, int batch, int seq_q,
+                        int kv_stride, const int* kv_lens, void* o, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  if (!h || !q || !k || !v || !o) return fail(BLK_ERR_INVALID_ARG, "NULL argument");
+  const blk_desc& d = h->d;
+  if (batch <= 0 || seq_q <= 0 || kv_stride < (kv_lens ? 1 : seq_q)) return fail(BLK_ERR_INVALID_ARG, "bad sizes");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return fail(BLK_ERR_ALIGNMENT, "alignment");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const char* why = nullptr;
+  if (d.dtype == BLK_F32) {
+    if ((size_t)kv_stride * 4 > 200 * 1024) return fail(BLK_ERR_UNSUPPORTED, "fp32 attention: kv_stride too large");
+    return check_cuda(launch_attn_f32((const float*)q, (const float*)k, (const float*)v, (float*)o, batch, d.n_heads,
+                                      d.n_kv_heads, seq_q, d.head_dim, kv_stride, kv_lens, 0, s),
+                      "attention");
+  }
+  if (!kv_lens) {
+    if (kv_stride != seq_q) return fail(BLK_ERR_UNSUPPORTED, "bf16 prefill attention: kv_stride must equal seq_q");
+    return check_cuda(launch_attn_prefill_bf16(q, k, v, o, batch, d.n_heads, d.n_kv_heads, seq_q, d.head_dim,
+                                               kv_stride, s, &why),
+                      "attention", why);
+  }
+  if (seq_q != 1) return fail(BLK_ERR_UNSUPPORTED, "bf16 attention over a cache: one query per sequence");
+  if (!workspace || workspace_bytes < blk_stage_workspace_bytes(h, batch)) return fail(BLK_ERR_WORKSPACE, "workspace");
+  Carve c(workspace);
+  c.take((size_t)batch * d.ffn * esize(d));
+  c.take((size_t)batch * max_cols(d) * sizeof(float));
+  void* aw = c.take(0);
+  return check_cuda(launch_attn_decode_bf16(q, k, v, o, batch, d.n_heads, d.n_kv_heads, d.head_dim, kv_stride, kv_lens,
+                                            0, kv_stride, aw, h->num_sms, s, &why),
+                    "decode attention", why);
+}
+
+blk_status blk_mlp(blk_handle* h, const void* resid, const void* h_normed, const blk_weights* w, int rows, void* out,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h || !resid || !h_normed || !w || !out) return fail(BLK_ERR_INVALID_ARG, "NULL argument");
+  const blk_desc& d = h->d;
+  if (rows <= 0) return fail(BLK_ERR_INVALID_ARG, "bad sizes");
+  if (!aligned16(resid) || !aligned16(h_normed) || !aligned16(out)) return fail(BLK_ERR_ALIGNMENT, "alignment");
+  if (!w->w_up || !w->w_down || (d.act == BLK_ACT_SWIGLU && !w->w_gate))
+    return fail(BLK_ERR_INVALID_ARG, "MLP weights NULL");
+  if (!workspace || workspace_bytes < blk_stage_workspace_bytes(h, rows)) return fail(BLK_ERR_WORKSPACE, "workspace");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Carve c(workspace);
+  void* neur = c.take((size_t)rows * d.ffn * esize(d));
+  float* C = static_cast<float*>(c.take((size_t)rows * max_cols(d) * sizeof(float)));
+  if (d.dtype == BLK_BF16) {
+    BLK_TRY(bf16_mlp_up(h, h_normed, rows, w, neur, s));
+    return bf16_linear_resid(h, neur, rows, d.ffn, w->w_down, d.hidden, resid, out, nullptr, s, "down GEMM");
+  }
+  const float* y = static_cast<const float*>(h_normed);
+  const int nm = mlp_cols(d);
+  if (d.act == BLK_ACT_SWIGLU) {
+    BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->w_gate, C, nm, rows, d.ffn, d.hidden, s), "gate GEMM"));
+    BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->w_up, C + d.ffn, nm, rows, d.ffn, d.hidden, s), "up GEMM"));
+  } else {
+    BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->w_up, C, nm, rows, d.ffn, d.hidden, s), "up GEMM"));
+  }
+  BLK_TRY(check_cuda(launch_post_act(C, 1, rows, d.ffn, nm, (int)d.act, d.xielu_alpha_p, d.xielu_alpha_n,
+                                     d.xielu_beta, d.xielu_eps, neur, false, s),
+                     "activation"));
+  BLK_TRY(check_cuda(launch_gemm_f32((const float*)neur, (const float*)w->w_down, C, d.hidden, rows, d.hidden, d.ffn, s),
+                     "down GEMM"));
+  return check_cuda(launch_post_resid(C, 1, rows, d.hidden, d.hidden, resid, out, nullptr, nullptr, 0.f, nullptr,
+                                      nullptr, false, s),
+                    "down post");
+}
+
+blk_status blk_profile_enable(blk_handle* h, int on) {
+  if (!h) return fail(BLK_ERR_INVALID_ARG, "NULL handle");
+  StageProfile& p = h->prof;
+  if (on && !p.on) {
+    for (auto& e : p.ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return fail(BLK_ERR_CUDA, "cudaEventCreate");
+    p.on = true;
+    p.n = 0;
+    p.pending = false;
+  } else if (!on && p.on) {
+    for (auto& e : p.ev) {
+      cudaEventDestroy(e);
+      e = nullptr;
+    }
+    p.on = false;
+    p.pending = false;
+  }
+  return BLK_OK;
+}
+
+int blk_profile_collect(blk_handle* h, double* total_ms, long long* launches, int max_stages) {
+  if (!h || !h->prof.on) return -1;
+  StageProfile& p = h->prof;
+  if (p.pending) {
+    if (cudaEventSynchronize(p.ev[p.n]) != cudaSuccess) return -1;
+    for (int i = 0; i < p.n; ++i) {
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, p.ev[i], p.ev[i + 1]);
+      p.total_ms[i] += ms;
+      p.total_launches[i] += p.launches[i];
+    }
+    p.pending = false;
+  }
+  for (int i = 0; i < p.n && i < max_stages; ++i) {
+    if (total_ms) total_ms[i] = p.total_ms[i];
+    if (launches) launches[i] = p.total_launches[i];
+  }
+  return p.n;
+}
+
+const char* blk_profile_stage_name(const blk_handle* h, int i) {
+  if (!h || i < 0 || i >= h->prof.n || !h->prof.names[i]) return "";
+  return h->prof.names[i];
+}
+
+void blk_profile_reset(blk_handle* h) {
+  if (!h) return;
+  for (int i = 0; i < StageProfile::kMax; ++i) {
+    h->prof.total_ms[i] = 0.0;
+    h->prof.total_launches[i] = 0;
+  }
+}
+
+blk_status blk_debug_gemm_bf16(const void* a, const void* b, void* c, int M, int N, int K, int bn, int split_k,
+                               void* stream) {
+  if (!a || !b || !c) return fail(BLK_ERR_INVALID_ARG, "NULL argument");
+  if (M <= 0 || N <= 0 || K <= 0 || K % 8 || (bn != 64 && bn != 128 && bn != 256) || split_k < 1)
+    return fail(BLK_ERR_INVALID_ARG, "bad sizes");
+  if (split_k > 1 && bn != 64) return fail(BLK_ERR_INVALID_ARG, "split_k > 1 needs bn == 64");
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return fail(BLK_ERR_ALIGNMENT, "alignment");
+  if (split_k == 1 && N % 8) return fail(BLK_ERR_INVALID_ARG, "N % 8 != 0");
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  TcGemmDesc g;
+  g.na = 1;
+  g.nb = 1;
+  g.K = K;
+  g.bn = bn;
+  g.k_splits = split_k;
+  if (split_k == 1) {
+    g.a[0] = {a, M, 0};
+    g.b[0] = {b, N, 0};
+    g.epi = Epi::kStore;
+    g.e.out = c;
+    g.e.ldo = N;
+  } else {  // swap-AB partials: "weights" b on the MMA rows, tokens a on its columns
+    g.a[0] = {b, N, 0};
+    g.b[0] = {a, M, 0};
+    g.epi = Epi::kPartialT;
+    g.e.out = c;
+    g.e.part_ld = N;
+    g.e.n_tok = M;
+  }
+  const char* why = nullptr;
+  cudaError_t e = launch_tc_gemm(g, sms, nullptr, (unsigned long long)g_wait_ns.load(),
+                                 static_cast<cudaStream_t>(stream), &why);
+  return e == cudaSuccess ? BLK_OK : cuda_fail(e, "debug GEMM", why);
+}
+
+blk_status blk_last_status(blk_handle* h) {
+  if (!h) return fail(BLK_ERR_INVALID_ARG, "NULL handle");
+  DevStatus st{0, 0};
+  cudaError_t e = cudaMemcpy(&st, h->status, sizeof(st), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "blk_last_status");
+  if (st.code != 0) {
+    cudaMemset(h->status, 0, sizeof(DevStatus));
+    char buf[96];
+    snprintf(buf, sizeof(buf), "device wait timed out (site 0x%x)", st.where);
+    return fail((blk_status)st.code, buf);
+  }
+  return BLK_OK;
+}
+
+}  // extern "C"

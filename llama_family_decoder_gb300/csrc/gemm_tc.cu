@@ -1,0 +1,618 @@
+// tcgen05 / TMEM GEMM for sm_103a: C = A * B^T with A [M, K] and B [N, K] both
+// K-major bf16, fp32 accumulation in tensor memory, operands staged by TMA.
+//
+// One persistent CTA per SM (192 threads):
+//   warp 0      TMA producer: fills a ring of shared-memory stages (A tile
+//               128 x 64, B tile BN x 64, 128-byte swizzled) on mbarriers.
+//   warp 1      allocates 2*BN TMEM columns; lane 0 issues tcgen05.mma
+//               (128 x BN x 16 per instruction, 4 per stage) into one of two
+//               accumulators and commits stage releases / accumulator-ready.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
+//               fused post-processing, stores to global memory.
+// The two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+//
+// Fused epilogues cover the projections of the decoder block ("LlamaForCausalLM-
+// 32L-4096d" sheet, "Implementing it"): per-head q/k RMSNorm + RoPE + scatter
+// to head-major q/k/v ("apertus", "Queries and keys are normed per head, before
+// the rotary"), the residual adds after o_proj and down_proj, SiLU-gated,
+// squared-ReLU ("arcee") and xIELU ("apertus") activations, and transposed
+// split-K partials for the weight-streaming decode GEMMs (tokens on the MMA's
+// N dimension).
+//
+// Every wait is bounded in wall time; on expiry the CTA records a timeout in
+// the status word, drains its own copies and MMAs in flight, frees its TMEM
+// and returns.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace blk {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+// Drains after an abort wait for copies/MMAs already issued; they use their
+// own limit so that a tiny debug timeout cannot cut them short.
+constexpr unsigned long long kDrainNs = 2000000000ULL;
+
+template <int BN>
+struct TcCfg {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+};
+
+struct TcParams {
+  CUtensorMap ta[3];
+  CUtensorMap tb[3];
+  int a_tiles[4];  // prefix sums of m-tiles per A segment
+  int a_rows[3];
+  int a_out[3];
+  int b_tiles[4];  // prefix sums of n-tiles per B segment
+  int b_rows[3];
+  int b_out[3];
+  int na, nb;
+  int b_paired;
+  int num_kb;
+  int k_splits;
+  int m_tiles, n_tiles;
+  int num_units;
+  TcEpiArgs e;
+  DevStatus* status;
+  unsigned long long wait_ns;
+};
+
+struct Unit {
+  int a_seg, a_row0;  // A segment and first row of the tile inside it
+  int b_seg, b_row0;
+  int m_tile;
+  int ks, kb_begin, kb_end;
+};
+
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u, int bn_rows) {
+  Unit r;
+  const int tile = u / p.k_splits;
+  r.ks = u - tile * p.k_splits;
+  const int m_tile = tile % p.m_tiles;
+  const int n_tile = tile / p.m_tiles;
+  r.m_tile = m_tile;
+  int s = 0;
+  while (s + 1 < p.na && m_tile >= p.a_tiles[s + 1]) ++s;
+  r.a_seg = s;
+  r.a_row0 = (m_tile - p.a_tiles[s]) * kBM;
+  s = 0;
+  while (s + 1 < p.nb && n_tile >= p.b_tiles[s + 1]) ++s;
+  r.b_seg = p.b_paired ? 0 : s;
+  r.b_row0 = (n_tile - p.b_tiles[r.b_seg]) * bn_rows;
+  r.kb_begin = (int)(((long long)r.ks * p.num_kb) / p.k_splits);
+  r.kb_end = (int)(((long long)(r.ks + 1) * p.num_kb) / p.k_splits);
+  return r;
+}
+
+// ------------------------------------------------------------------ epilogues
+
+template <typename F>
+__device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float* v, int n_valid, F&& f) {
+  // writes up to 16 values (f applied) to dst[0..16) with the tail predicated
+  if (n_valid >= 16) {
+    uint4 a, b;
+    a.x = pack_bf16x2(f(v[0], 0), f(v[1], 1));
+    a.y = pack_bf16x2(f(v[2], 2), f(v[3], 3));
+    a.z = pack_bf16x2(f(v[4], 4), f(v[5], 5));
+    a.w = pack_bf16x2(f(v[6], 6), f(v[7], 7));
+    b.x = pack_bf16x2(f(v[8], 8), f(v[9], 9));
+    b.y = pack_bf16x2(f(v[10], 10), f(v[11], 11));
+    b.z = pack_bf16x2(f(v[12], 12), f(v[13], 13));
+    b.w = pack_bf16x2(f(v[14], 14), f(v[15], 15));
+    reinterpret_cast<uint4*>(dst)[0] = a;
+    reinterpret_cast<uint4*>(dst)[1] = b;
+  } else {
+    for (int i = 0; i < n_valid; ++i) dst[i] = __float2bfloat16_rn(f(v[i], i));
+  }
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+template <int BN, int EPI>
+__device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, uint32_t taddr, int r_in_tile) {
+  const TcEpiArgs& e = p.e;
+  if constexpr (EPI == (int)Epi::kPartialT) {
+    // rows of the tile are output features, columns are tokens
+    const int f_local = un.a_row0 + r_in_tile;
+    const bool ok = f_local < p.a_rows[un.a_seg];
+    const int f = p.a_out[un.a_seg] + f_local;
+    float* part = reinterpret_cast<float*>(e.out) + (size_t)un.ks * e.n_tok * e.part_ld;
+    const int tok0 = un.b_row0;  // tokens are the B rows
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      if (tok0 + c0 >= e.n_tok) break;  // uniform across the warp
+      float v0[16], v1[16];
+      tmem_ld16(taddr + c0, v0);
+      tmem_ld16(taddr + c0 + 16, v1);
+      tc_wait_ld();
+      if (ok) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (tok0 + c0 + j < e.n_tok) part[(size_t)(tok0 + c0 + j) * e.part_ld + f] = v0[j];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (tok0 + c0 + 16 + j < e.n_tok) part[(size_t)(tok0 + c0 + 16 + j) * e.part_ld + f] = v1[j];
+      }
+    }
+    return;
+  } else {
+    const int row = un.m_tile * kBM + r_in_tile;  // activations are a single A segment
+    const bool row_ok = row < p.a_rows[0];
+    if constexpr (EPI == (int)Epi::kQkv) {
+      const int d = e.head_dim;  // 128
+      const int seg = un.b_seg;
+      const int b = row_ok ? row / e.seq : 0;
+      const int t = row_ok ? row - b * e.seq : 0;
+      const int pos = (e.pos0 ? e.pos0[b] : 0) + t;
+      const float2* cs = e.rope + (size_t)min(pos, e.rope_max_pos - 1) * (d / 2);
+#pragma unroll 1
+      for (int hh = 0; hh < BN / 128; ++hh) {
+        const int head = (un.b_row0 >> 7) + hh;
+        const uint32_t tcol = taddr + hh * 128;
+        __nv_bfloat16* dst;
+        if (seg == 0)
+          dst = reinterpret_cast<__nv_bfloat16*>(e.q) + (((size_t)b * e.n_heads + head) * e.seq + t) * d;
+        else
+          dst = reinterpret_cast<__nv_bfloat16*>(seg == 1 ? e.k : e.v) +
+                (((size_t)b * e.n_kv_heads + head) * e.kv_stride + t) * d;
+        if (seg == 2) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            float v0[16], v1[16];
+            tmem_ld16(tcol + c0, v0);
+            tmem_ld16(tcol + c0 + 16, v1);
+            tc_wait_ld();
+            if (row_ok) {
+              auto id = [](float x, int) { return x; };
+              store_bf16_row(dst + c0, v0, 16, id);
+              store_bf16_row(dst + c0 + 16, v1, 16, id);
+            }
+          }
+          continue;
+        }
+        float r = 1.0f;
+        const __nv_bfloat16* gain = nullptr;
+        if (e.qk_norm) {
+          gain = reinterpret_cast<const __nv_bfloat16*>(seg == 0 ? e.q_gain : e.k_gain);
+          float ss = 0.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            float v0[16], v1[16];
+            tmem_ld16(tcol + c0, v0);
+            tmem_ld16(tcol + c0 + 16, v1);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ss += v0[j] * v0[j] + v1[j] * v1[j];
+          }
+          r = rsqrtf(ss / 128.0f + e.eps);
+        }
+#pragma unroll 1
+        for (int i0 = 0; i0 < 64; i0 += 16) {
+          float x1[16], x2[16];
+          tmem_ld16(tcol + i0, x1);
+          tmem_ld16(tcol + 64 + i0, x2);
+          tc_wait_ld();
+          float y1[16], y2[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float a = x1[j], c = x2[j];
+            if (gain) {
+              a = a * r * __bfloat162float(gain[i0 + j]);
+              c = c * r * __bfloat162float(gain[64 + i0 + j]);
+            }
+            const float2 sc = cs[i0 + j];
+            y1[j] = a * sc.x - c * sc.y;
+            y2[j] = c * sc.x + a * sc.y;
+          }
+          if (row_ok) {
+            auto id = [](float x, int) { return x; };
+            store_bf16_row(dst + i0, y1, 16, id);
+            store_bf16_row(dst + 64 + i0, y2, 16, id);
+          }
+        }
+      }
+      return;
+    } else if constexpr (EPI == (int)Epi::kSwiglu) {
+      // B halves: gate rows at TMEM columns [0, BN/2), up rows at [BN/2, BN)
+      const int col0 = un.b_row0;
+      const int n_valid = p.b_rows[0] - col0;
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(e.out) + (size_t)row * e.ldo + col0;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+        float g[16], u[16];
+        tmem_ld16(taddr + c0, g);
+        tmem_ld16(taddr + BN / 2 + c0, u);
+        tc_wait_ld();
+        if (row_ok && c0 < n_valid) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = silu_f(g[j]) * u[j];
+          auto id = [](float x, int) { return x; };
+          store_bf16_row(out + c0, v, min(16, n_valid - c0), id);
+        }
+      }
+      return;
+    } else {
+      const int col0 = p.b_out[un.b_seg] + un.b_row0;
+      const int n_valid = p.b_rows[un.b_seg] - un.b_row0;
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(e.out) + (size_t)row * e.ldo + col0;
+      const __nv_bfloat16* res = nullptr;
+      __nv_bfloat16* tap = nullptr;
+      if constexpr (EPI == (int)Epi::kResid) {
+        res = reinterpret_cast<const __nv_bfloat16*>(e.resid) + (size_t)row * e.ldo + col0;
+        if (e.tap) tap = reinterpret_cast<__nv_bfloat16*>(e.tap) + (size_t)row * e.ldo + col0;
+      }
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tmem_ld16(taddr + c0, *reinterpret_cast<float(*)[16]>(&v[0]));
+        tmem_ld16(taddr + c0 + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
+        tc_wait_ld();
+        if (!row_ok || c0 >= n_valid) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int cc = c0 + 16 * h;
+          if (cc >= n_valid) break;
+          const int nv = min(16, n_valid - cc);
+          float* vv = &v[16 * h];
+          if constexpr (EPI == (int)Epi::kStore) {
+            store_bf16_row(out + cc, vv, nv, [](float x, int) { return x; });
+          } else if constexpr (EPI == (int)Epi::kRelu2) {
+            store_bf16_row(out + cc, vv, nv, [](float x, int) {
+              const float r = fmaxf(x, 0.0f);
+              return r * r;
+            });
+          } else if constexpr (EPI == (int)Epi::kXielu) {
+            const float ap = e.alpha_p, an = e.alpha_n, be = e.beta, xe = e.xeps;
+            store_bf16_row(out + cc, vv, nv, [=](float x, int) {
+              return x > 0.0f ? ap * x * x + be * x : an * (expm1f(fminf(x, xe)) - x) + be * x;
+            });
+          } else if constexpr (EPI == (int)Epi::kResid) {
+            // contribution rounded to bf16 first, then added to the residual in fp32
+            float rr[16];
+            if (nv == 16) {
+              const uint4 ra = reinterpret_cast<const uint4*>(res + cc)[0];
+              const uint4 rb = reinterpret_cast<const uint4*>(res + cc)[1];
+              const uint32_t w[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float2 f2 = unpack_bf16x2(w[j]);
+                rr[2 * j] = f2.x;
+                rr[2 * j + 1] = f2.y;
+              }
+            } else {
+              for (int j = 0; j < nv; ++j) rr[j] = __bfloat162float(res[cc + j]);
+            }
+            if (tap) store_bf16_row(tap + cc, vv, nv, [](float x, int) { return x; });
+            store_bf16_row(out + cc, vv, nv, [&](float x, int j) { return rr[j] + round_to<__nv_bfloat16>(x); });
+          }
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  using C = TcCfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * C::kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::kBBytes);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[S + s]); };
+  auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * S + a]); };
+  auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * S + 2 + a]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * S + 4]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < p.na; ++i) tma_prefetch_desc(&p.ta[i]);
+    for (int i = 0; i < p.nb; ++i) tma_prefetch_desc(&p.tb[i]);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int bn_rows = p.b_paired ? BN / 2 : BN;
+  const unsigned long long budget = p.wait_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int stage = 0;
+      uint32_t ph = 0;
+      uint32_t issued_mask = 0, parity_mask = 0;
+      bool failed = false;
+      for (int u = blockIdx.x; u < p.num_units && !failed; u += gridDim.x) {
+        const Unit un = decode_unit(p, u, bn_rows);
+        for (int kb = un.kb_begin; kb < un.kb_end; ++kb) {
+          if (!mbar_wait(empty_bar(stage), ph ^ 1, budget, abort_flag)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
+          const uint32_t a_dst = smem_u32(sA + stage * C::kABytes);
+          const uint32_t b_dst = smem_u32(sB + stage * C::kBBytes);
+          tma_load_2d(a_dst, &p.ta[un.a_seg], kb * kBK, un.a_row0, full_bar(stage));
+          if (p.b_paired) {
+            tma_load_2d(b_dst, &p.tb[0], kb * kBK, un.b_row0, full_bar(stage));
+            tma_load_2d(b_dst + (BN / 2) * kBK * 2, &p.tb[1], kb * kBK, un.b_row0, full_bar(stage));
+          } else {
+            tma_load_2d(b_dst, &p.tb[un.b_seg], kb * kBK, un.b_row0, full_bar(stage));
+          }
+          issued_mask |= 1u << stage;
+          parity_mask = (parity_mask & ~(1u << stage)) | (ph << stage);
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (failed) {
+        *abort_flag = 1;
+        report_timeout(p.status, 0x10 + 0);
+        // drain: every issued load must land before the CTA exits
+        for (int s = 0; s < S; ++s)
+          if (issued_mask & (1u << s)) {
+            volatile int never = 0;
+            mbar_wait(full_bar(s), (parity_mask >> s) & 1, kDrainNs, &never);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      int stage = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool failed = false, issued_any = false;
+      for (int u = blockIdx.x; u < p.num_units && !failed; u += gridDim.x, ++it) {
+        const Unit un = decode_unit(p, u, bn_rows);
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait(tempty_bar(acc), aph ^ 1, budget, abort_flag)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = un.kb_begin; kb < un.kb_end; ++kb) {
+          if (!mbar_wait(full_bar(stage), ph, budget, abort_flag)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * C::kABytes));
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + stage * C::kBBytes));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // advance 16 elements (32 bytes) along K inside the swizzle atom
+            tc_mma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                        (kb > un.kb_begin || kk > 0) ? 1u : 0u);
+          }
+          issued_any = true;
+          tc_commit(empty_bar(stage));
+          if (++stage == S) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+        if (failed) break;
+        tc_commit(tfull_bar(acc));
+      }
+      if (failed) {
+        *abort_flag = 1;
+        report_timeout(p.status, 0x10 + 1);
+        if (issued_any) {
+          tc_commit(drain_bar);
+          volatile int never = 0;
+          mbar_wait(drain_bar, 0, kDrainNs, &never);
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5: TMEM lane quarter = warp % 4
+    const int quarter = warp & 3;
+    int it = 0;
+    bool failed = false;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
+      const Unit un = decode_unit(p, u, bn_rows);
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!mbar_wait(tfull_bar(acc), aph, budget, abort_flag)) {
+        failed = true;
+        break;
+      }
+      __syncwarp();
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane);
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+    }
+    if (failed) {
+      *abort_flag = 1;
+      if (lane == 0) report_timeout(p.status, 0x10 + 2);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* ptr, int rows, int K, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t s) {
+  using C = TcCfg<BN>;
+  static bool configured = false;  // per instantiation; attribute is per function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  tc_gemm_kernel<BN, EPI><<<grid, kThreads, C::kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t dispatch_epi(const TcParams& p, Epi epi, int grid, cudaStream_t s) {
+  switch (epi) {
+    case Epi::kStore: return launch_one<BN, (int)Epi::kStore>(p, grid, s);
+    case Epi::kResid: return launch_one<BN, (int)Epi::kResid>(p, grid, s);
+    case Epi::kQkv: return launch_one<BN, (int)Epi::kQkv>(p, grid, s);
+    case Epi::kSwiglu: return launch_one<BN, (int)Epi::kSwiglu>(p, grid, s);
+    case Epi::kRelu2: return launch_one<BN, (int)Epi::kRelu2>(p, grid, s);
+    case Epi::kXielu: return launch_one<BN, (int)Epi::kXielu>(p, grid, s);
+    case Epi::kPartialT: return launch_one<BN, (int)Epi::kPartialT>(p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int tc_gemm_units(const TcGemmDesc& d) {
+  const int bn_rows = d.b_paired ? d.bn / 2 : d.bn;
+  int mt = 0, nt = 0;
+  for (int i = 0; i < d.na; ++i) mt += (d.a[i].rows + kBM - 1) / kBM;
+  if (d.b_paired)
+    nt = (d.b[0].rows + bn_rows - 1) / bn_rows;
+  else
+    for (int i = 0; i < d.nb; ++i) nt += (d.b[i].rows + bn_rows - 1) / bn_rows;
+  return mt * nt * d.k_splits;
+}
+
+cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, unsigned long long wait_ns,
+                           cudaStream_t s, const char** why) {
+  TcParams p;
+  memset(static_cast<void*>(&p), 0, sizeof(p));
+  const int bn_rows = d.b_paired ? d.bn / 2 : d.bn;
+  if (d.bn != 64 && d.bn != 128 && d.bn != 256) {
+    *why = "tcgen05 GEMM: BN must be 64, 128 or 256";
+    return cudaErrorInvalidValue;
+  }
+  if (d.K <= 0 || d.K % 8 != 0) {
+    *why = "tcgen05 GEMM: K must be a positive multiple of 8 (16-byte rows)";
+    return cudaErrorInvalidValue;
+  }
+  if (d.na < 1 || d.na > 3 || d.nb < 1 || d.nb > 3 || (d.b_paired && d.nb != 2)) {
+    *why = "tcgen05 GEMM: bad segment count";
+    return cudaErrorInvalidValue;
+  }
+  p.na = d.na;
+  p.nb = d.nb;
+  p.a_tiles[0] = 0;
+  for (int i = 0; i < d.na; ++i) {
+    if (!make_map(&p.ta[i], d.a[i].ptr, d.a[i].rows, d.K, kBM)) {
+      *why = "cuTensorMapEncodeTiled failed for an A operand";
+      return cudaErrorInvalidValue;
+    }
+    p.a_rows[i] = d.a[i].rows;
+    p.a_out[i] = d.a[i].out_offset;
+    p.a_tiles[i + 1] = p.a_tiles[i] + (d.a[i].rows + kBM - 1) / kBM;
+  }
+  p.b_tiles[0] = 0;
+  for (int i = 0; i < d.nb; ++i) {
+    if (!make_map(&p.tb[i], d.b[i].ptr, d.b[i].rows, d.K, bn_rows)) {
+      *why = "cuTensorMapEncodeTiled failed for a B operand";
+      return cudaErrorInvalidValue;
+    }
+    p.b_rows[i] = d.b[i].rows;
+    p.b_out[i] = d.b[i].out_offset;
+    p.b_tiles[i + 1] = p.b_tiles[i] + (d.b[i].rows + bn_rows - 1) / bn_rows;
+  }
+  p.b_paired = d.b_paired ? 1 : 0;
+  p.m_tiles = p.a_tiles[d.na];
+  p.n_tiles = d.b_paired ? (d.b[0].rows + bn_rows - 1) / bn_rows : p.b_tiles[d.nb];
+  p.num_kb = (d.K + kBK - 1) / kBK;
+  p.k_splits = d.k_splits < 1 ? 1 : (d.k_splits > p.num_kb ? p.num_kb : d.k_splits);
+  p.num_units = p.m_tiles * p.n_tiles * p.k_splits;
+  p.e = d.e;
+  p.status = st;
+  p.wait_ns = wait_ns;
+  if (p.num_units == 0) return cudaSuccess;
+  const int grid = p.num_units < max_ctas ? p.num_units : max_ctas;
+  switch (d.bn) {
+    case 64: return dispatch_epi<64>(p, d.epi, grid, s);
+    case 128: return dispatch_epi<128>(p, d.epi, grid, s);
+    default: return dispatch_epi<256>(p, d.epi, grid, s);
+  }
+}
+
+}  // namespace blk

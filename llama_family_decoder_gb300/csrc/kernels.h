@@ -1,0 +1,128 @@
+// Internal launch interface between the host library (blk_api.cu) and the
+// kernel translation units. Not part of the public C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace blk {
+
+struct DevStatus;
+
+// ---------------------------------------------------------------- RMSNorm
+// y[r,:] = x[r,:] * rsqrt(mean(x[r,:]^2) + eps) * g   (fp32 statistics)
+cudaError_t launch_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y, bool bf16,
+                           cudaStream_t s);
+
+// ---------------------------------------------------------------- fp32 SIMT GEMM
+// C[m, c0 + n] = sum_k A[m, k] * B[n, k] for m < M, n < N  (fp32, row-major, ld = K for A/B).
+cudaError_t launch_gemm_f32(const float* A, const float* B, float* C, int ldc, int M, int N, int K, cudaStream_t s);
+
+// ---------------------------------------------------------------- tcgen05 GEMM (bf16 in, fp32 accumulate)
+
+enum class Epi : int {
+  kStore = 0,     // out[row, col] = bf16(acc)
+  kResid = 1,     // out = bf16(resid + bf16(acc)); optional tap = bf16(acc)
+  kQkv = 2,       // per-head optional RMSNorm, RoPE, scatter to q/k/v head-major layouts
+  kSwiglu = 3,    // paired B halves [gate | up]: out = bf16(silu(gate) * up)
+  kRelu2 = 4,     // out = bf16(relu(acc)^2)
+  kXielu = 5,     // out = bf16(xielu(acc))
+  kPartialT = 6,  // swap-AB split-K: part[split][token][feature] = acc^T (fp32)
+};
+
+// One row-segment of an operand: a contiguous [rows, K] bf16 matrix.
+struct TcSeg {
+  const void* ptr;
+  int rows;
+  int out_offset;  // where this segment's rows land in the concatenated output
+};
+
+struct TcEpiArgs {
+  void* out = nullptr;  // kStore/kResid/activations: bf16 [rows, ldo]; kPartialT: float partial base
+  int ldo = 0;
+  const void* resid = nullptr;  // kResid: bf16 [rows, ldo]
+  void* tap = nullptr;          // kResid: optional bf16 contribution [rows, ldo]
+  // kQkv
+  void* q = nullptr;
+  void* k = nullptr;
+  void* v = nullptr;
+  int seq = 0;          // tokens per sequence (row -> (b, t))
+  int n_heads = 0;
+  int n_kv_heads = 0;
+  int head_dim = 0;
+  int kv_stride = 0;    // rows per (b, kv head) in k/v (== seq for prefill)
+  const void* q_gain = nullptr;
+  const void* k_gain = nullptr;
+  float eps = 0.f;
+  const float2* rope = nullptr;  // [max_pos][head_dim/2] (cos, sin)
+  int rope_max_pos = 0;
+  const int* pos0 = nullptr;     // [B] first position of each sequence, or null
+  int qk_norm = 0;
+  // activations
+  float alpha_p = 0.f, alpha_n = 0.f, beta = 0.f, xeps = 0.f;
+  // kPartialT
+  int part_ld = 0;  // features per token row of the partial buffer
+  int n_tok = 0;    // valid tokens (B operand rows)
+};
+
+struct TcGemmDesc {
+  TcSeg a[3];
+  int na = 1;
+  TcSeg b[3];
+  int nb = 1;
+  bool b_paired = false;  // B tile = halves from b[0] and b[1] at the same rows (gate/up)
+  int K = 0;              // inner dimension; every segment has row stride K
+  int k_splits = 1;
+  int bn = 256;           // 64, 128 or 256
+  Epi epi = Epi::kStore;
+  TcEpiArgs e;
+};
+
+// Number of work units (tiles x splits) the descriptor produces.
+int tc_gemm_units(const TcGemmDesc& d);
+
+cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, unsigned long long wait_ns,
+                           cudaStream_t s, const char** why);
+
+// ---------------------------------------------------------------- post-GEMM kernels (fp32 partial sums in)
+// C is [splits][rows][ldc] fp32; each reads the split-sum of its elements.
+
+// Q/K/V from C columns [0, H*d) | [H*d, (H+Hkv)*d) | [.., (H+2Hkv)*d):
+// optional per-head RMSNorm (q/k), RoPE at pos, write q[b,h,t_q,:] (Tq rows per
+// (b,h)) and k/v at slot `pos` of [b, j, kv_stride, d] (prefill: slot t).
+// decode_lens != null: decode mode (seq == 1, pos = decode_lens[b]).
+cudaError_t launch_post_qkv(const float* C, int splits, int rows, int ldc, int seq, const int* pos0,
+                            const int* decode_lens, int H, int Hkv, int d, int qk_norm, const void* q_gain,
+                            const void* k_gain, float eps, const float2* rope, int rope_max_pos, void* q, void* k,
+                            void* v, int kv_stride, bool bf16, cudaStream_t s);
+
+// out[r, c] = round(resid[r, c] + round(sum_s C[s, r, c])) for c < n; optional
+// contribution tap; optional fused RMSNorm of the new row into y (gain g);
+// optional lens bump (lens[r] += 1 for r < rows).
+cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int ldc, const void* resid, void* out,
+                              void* tap, const void* g, float eps, void* y, int* bump_lens, bool bf16,
+                              cudaStream_t s);
+
+// neurons[r, f] = act(C) for f < F; SwiGLU reads gate at column f and up at F + f.
+cudaError_t launch_post_act(const float* C, int splits, int rows, int F, int ldc, int act, float alpha_p,
+                            float alpha_n, float beta, float xeps, void* out, bool bf16, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention
+// Causal GQA attention; q [B,H,Tq,d], k/v [B,Hkv,kv_stride,d], o [B,Tq,H,d].
+// kv_lens null: kv_len = Tq.
+cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, int B, int H, int Hkv, int Tq,
+                            int d, int kv_stride, const int* kv_lens, int len_add, cudaStream_t s);
+
+cudaError_t launch_attn_prefill_bf16(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv,
+                                     int T, int d, int kv_stride, cudaStream_t s, const char** why);
+
+// Decode (Tq == 1), split over the keys: partial results in ws, combined into o.
+size_t attn_decode_ws_bytes(int B, int H, int d, int max_splits);
+// Keys per sequence: kv_lens[b] + len_add (<= max_len, which sizes the splits).
+cudaError_t launch_attn_decode_bf16(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv,
+                                    int d, int kv_stride, const int* kv_lens, int len_add, int max_len, void* ws,
+                                    int num_sms, cudaStream_t s, const char** why);
+int attn_decode_splits(int B, int Hkv, int max_len, int num_sms);
+
+}  // namespace blk

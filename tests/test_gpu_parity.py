@@ -1,0 +1,205 @@
+"""GPU parity of the CUDA path against the fp64 oracle, on seeded inputs at sizes
+the oracle finishes in seconds (several tiles plus ragged tails), through the
+C ABI. Bounds: max|err| / RMS(oracle) <= 1e-4 (fp32 path), <= 2e-2 (bf16 path).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from llama_family_decoder_gb300 import DecoderBlock, rmsnorm
+from llama_family_decoder_gb300.synth import WORKLOADS, Workload, make_input, make_kv_cache, make_weights
+from tests.helpers import TOL, bf16_floor, cfg_of, np64, rel_err, to_dev, weights_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+SMALL_BF16 = [
+    # several 128-row tiles with a ragged tail; ffn not a multiple of 64/128 (K and N tails)
+    Workload("small_swiglu_mha", "bf16", 2, 200, 512, 4, 4, 128, 1000, "silu", seed=11),
+    Workload("small_relu2_gqa", "bf16", 1, 320, 1024, 8, 2, 128, 1536, "relu2", seed=12),
+    Workload("small_xielu_qknorm", "bf16", 3, 130, 512, 4, 1, 128, 776, "xielu", qk_norm=True, seed=13),
+    Workload("small_swiglu_gqa_qknorm", "bf16", 1, 64, 256, 4, 2, 128, 512, "silu", qk_norm=True, seed=14),
+]
+
+TAPS = ["attention_queries", "attention_keys", "attention_values", "attention_head_outputs", "attention_output",
+        "layer_mid", "mlp_neurons", "mlp_output"]
+
+
+def _tap_buffers(wl, dt):
+    B, T, D, H, Hkv, d, F = wl.batch, wl.seq, wl.hidden_size, wl.num_heads, wl.num_kv_heads, wl.head_dim, \
+        wl.intermediate_size
+    shapes = {"attention_queries": (B, H, T, d), "attention_keys": (B, Hkv, T, d),
+              "attention_values": (B, Hkv, T, d), "attention_head_outputs": (B, T, H, d),
+              "attention_output": (B, T, D), "layer_mid": (B, T, D), "mlp_neurons": (B, T, F),
+              "mlp_output": (B, T, D)}
+    return {k: torch.empty(s, dtype=dt, device=DEV) for k, s in shapes.items()}
+
+
+def _run(wl, gain_std=0.0, taps=False):
+    w = make_weights(wl, gain_std=gain_std)
+    x = make_input(wl)
+    blk = DecoderBlock.from_workload(wl)
+    xd = x.to(DEV)
+    tb = _tap_buffers(wl, xd.dtype) if taps else None
+    out = blk.forward(xd, to_dev(w), taps=tb)
+    torch.cuda.synchronize()
+    assert blk.last_status() == 0
+    ref = oracle.block_forward(cfg_of(wl), weights_np(w), np64(x))
+    return out, tb, ref, x
+
+
+# ------------------------------------------------------------------ RMSNorm stage
+
+@pytest.mark.parametrize("dt,tol", [(torch.float32, 1e-6), (torch.bfloat16, 8e-3)])
+def test_rmsnorm_stage(dt, tol):
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(37, 4096, generator=g)
+    x[3] *= 1e4  # a sink-like row
+    gain = 1 + 0.1 * torch.randn(4096, generator=g)
+    x, gain = x.to(dt), gain.to(dt)
+    y = rmsnorm(x.to(DEV), gain.to(DEV), 1e-5)
+    torch.cuda.synchronize()
+    ref = oracle.rms_norm(np64(x), np64(gain), 1e-5)
+    assert np.all(np.isfinite(np64(y)))
+    assert rel_err(y, ref) <= tol
+
+
+# ------------------------------------------------------------------ fp32 path
+
+@pytest.mark.parametrize("gain_std", [0.0, 0.1])
+def test_tiny_f32_block(gain_std):
+    wl = WORKLOADS["tiny_f32_T64_D256"]
+    out, tb, ref, x = _run(wl, gain_std, taps=True)
+    assert rel_err(out, ref["layer_output"]) <= TOL["f32"]
+    for name in TAPS:
+        assert rel_err(tb[name], ref[name]) <= TOL["f32"] * 10, name
+    # the block identity holds exactly (each contribution rounded, then added)
+    xd = x.to(DEV)
+    assert torch.equal(xd + tb["attention_output"] + tb["mlp_output"], out)
+
+
+# ------------------------------------------------------------------ bf16 prefill
+
+@pytest.mark.parametrize("wl", SMALL_BF16, ids=lambda w: w.name)
+def test_bf16_block_small(wl):
+    out, tb, ref, x = _run(wl, gain_std=0.1 if wl.qk_norm else 0.0, taps=True)
+    err = rel_err(out, ref["layer_output"])
+    assert err <= TOL["bf16"], (err, bf16_floor(ref["layer_output"]))
+    for name in TAPS:
+        e = rel_err(tb[name], ref[name])
+        assert e <= TOL["bf16"], (name, e)
+    # "arcee"/"apertus" identity: layer_input + attention_output + mlp_output == layer_output
+    assert torch.equal(x.to(DEV) + tb["attention_output"] + tb["mlp_output"], out)
+    # "apertus": at position 0 the rotation is the identity, so queries there are
+    # the normed projections (checked against the oracle's q_norm output)
+    if wl.hidden_act == "relu2":
+        n = np64(tb["mlp_neurons"])
+        assert n.min() >= 0.0
+        assert 0.3 < np.mean(n == 0.0) < 0.7
+
+
+def test_bf16_padding_after_prompt_is_invisible():
+    # alpha-er docstring: padding after the prompt cannot influence it (causal).
+    wl = SMALL_BF16[1]
+    w = to_dev(make_weights(wl))
+    x = make_input(wl).to(DEV)
+    pad = torch.randn(1, 64, wl.hidden_size, generator=torch.Generator().manual_seed(3)).to(x.dtype).to(DEV) * 30
+    blk = DecoderBlock.from_workload(wl, max_seq=wl.seq + 64)
+    a = blk.forward(x, w)
+    b = blk.forward(torch.cat([x, pad], dim=1), w)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b[:, : wl.seq])
+
+
+# ------------------------------------------------------------------ stages
+
+@pytest.mark.parametrize("wl", [SMALL_BF16[2], WORKLOADS["tiny_f32_T64_D256"]], ids=lambda w: w.name)
+def test_stage_qkv_attn_mlp(wl):
+    w = make_weights(wl, gain_std=0.1)
+    x = make_input(wl)
+    cfg = cfg_of(wl)
+    ref = oracle.block_forward(cfg, weights_np(w), np64(x))
+    blk = DecoderBlock.from_workload(wl)
+    wd = to_dev(w)
+    dt = x.dtype
+    B, T, H, Hkv, d = wl.batch, wl.seq, wl.num_heads, wl.num_kv_heads, wl.head_dim
+    y = rmsnorm(x.to(DEV), wd["input_layernorm"], wl.rms_norm_eps)
+    q = torch.empty(B, H, T, d, dtype=dt, device=DEV)
+    k = torch.empty(B, Hkv, T, d, dtype=dt, device=DEV)
+    v = torch.empty(B, Hkv, T, d, dtype=dt, device=DEV)
+    blk.qkv_rope(y, wd, B, T, q, k, v)
+    o = torch.empty(B, T, H, d, dtype=dt, device=DEV)
+    blk.attn_gqa(q, k, v, o)
+    # MLP stage on the oracle's own layer_mid / mlp_norm_output (cast to the storage type)
+    mid = torch.from_numpy(ref["layer_mid"]).to(dt).to(DEV)
+    h2 = torch.from_numpy(ref["mlp_norm_output"]).to(dt).to(DEV)
+    out = torch.empty_like(mid)
+    blk.mlp(mid, h2, wd, out)
+    torch.cuda.synchronize()
+    tol = TOL[wl.dtype] * (10 if wl.dtype == "f32" else 1)
+    assert rel_err(q, ref["attention_queries"]) <= tol
+    assert rel_err(k, ref["attention_keys"]) <= tol
+    assert rel_err(v, ref["attention_values"]) <= tol
+    assert rel_err(o, ref["attention_head_outputs"]) <= tol
+    # out = mid + mlp(h2) on the oracle's own (storage-rounded) inputs
+    assert rel_err(out, ref["layer_output"]) <= tol
+
+
+# ------------------------------------------------------------------ decode
+
+def _decode_case(wl, lens):
+    w = make_weights(wl, gain_std=0.1 if wl.qk_norm else 0.0)
+    x = make_input(wl)[:, 0]  # [B, D]
+    cap = int(max(lens)) + 9
+    kc, vc = make_kv_cache(wl.scaled(cache_len=int(max(lens))), capacity=cap)
+    for b, L in enumerate(lens):  # only the first lens[b] slots are in use
+        kc[b, :, L:] = 0
+        vc[b, :, L:] = 0
+    return w, x, kc, vc
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_step_small(dtype):
+    if dtype == "bf16":
+        wl = Workload("small_decode", "bf16", 5, 1, 512, 8, 2, 128, 1000, "silu", seed=21)
+    else:
+        wl = Workload("small_decode_f32", "f32", 3, 1, 256, 4, 2, 64, 512, "xielu", qk_norm=True, seed=22)
+    lens = [17, 200, 63, 64, 1][: wl.batch]
+    w, x, kc, vc = _decode_case(wl, lens)
+    blk = DecoderBlock.from_workload(wl, max_seq=kc.shape[2] + 1)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    out = blk.forward(x[:, None].to(DEV), to_dev(w), cache={"k": kd, "v": vd, "lens": lens_d},
+                      host_lens_max=max(lens))
+    torch.cuda.synchronize()
+    assert blk.last_status() == 0
+    ref = oracle.decode_step(cfg_of(wl), weights_np(w), np64(x), np64(kc), np64(vc), np.array(lens))
+    tol = TOL[wl.dtype]
+    assert rel_err(out[:, 0], ref["layer_output"]) <= tol
+    assert lens_d.tolist() == [L + 1 for L in lens]
+    for b, L in enumerate(lens):  # the new key/value landed in slot lens[b]
+        assert rel_err(kd[b, :, L], ref["new_key"][b]) <= tol
+        assert rel_err(vd[b, :, L], ref["new_value"][b]) <= tol
+        assert torch.equal(kd[b, :, :L].cpu(), kc[b, :, :L])
+
+
+def test_decode_matches_prefill_last_row():
+    wl = Workload("small_prefill_decode", "bf16", 2, 96, 512, 4, 2, 128, 1000, "silu", seed=23)
+    w = to_dev(make_weights(wl))
+    x = make_input(wl).to(DEV)
+    blk = DecoderBlock.from_workload(wl, max_seq=128)
+    B, T, Hkv, d = wl.batch, wl.seq, wl.num_kv_heads, wl.head_dim
+    tb = _tap_buffers(wl, x.dtype)
+    full = blk.forward(x, w, taps=tb)
+    cap = T + 4
+    kc = torch.zeros(B, Hkv, cap, d, dtype=x.dtype, device=DEV)
+    vc = torch.zeros_like(kc)
+    kc[:, :, : T - 1] = tb["attention_keys"][:, :, : T - 1]
+    vc[:, :, : T - 1] = tb["attention_values"][:, :, : T - 1]
+    lens = torch.full((B,), T - 1, dtype=torch.int32, device=DEV)
+    dec = blk.forward(x[:, T - 1: T].contiguous(), w, cache={"k": kc, "v": vc, "lens": lens}, host_lens_max=T - 1)
+    torch.cuda.synchronize()
+    assert rel_err(dec[:, 0], np64(full[:, T - 1])) <= TOL["bf16"]
+    assert rel_err(kc[:, :, T - 1], np64(tb["attention_keys"][:, :, T - 1])) <= TOL["bf16"]
