@@ -44,7 +44,7 @@ def _peaks():
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks/throttle reasons sampled every 50 ms during the timed region."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -62,10 +62,17 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         return self
+
+    def wait_first_sample(self, timeout=3.0):
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < timeout:
+            if os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.02)
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -232,6 +239,10 @@ def run_ours(args, wl):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    if args.ncu:  # one more forward for a profiler to capture, nothing timed
+        step()
+        torch.cuda.synchronize()
+        return
 
     blk.profile(True)
     blk.profile_reset()
@@ -242,6 +253,7 @@ def run_ours(args, wl):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(gpu_index) as clk:
+        clk.wait_first_sample()
         for i in range(args.steps):
             flush.zero_()
             if decode:
@@ -338,11 +350,12 @@ def run_ours(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu", action="store_true", help="warm up, run one more forward for a profiler, exit")
     args = ap.parse_args()
     from llama_family_decoder_gb300.synth import WORKLOADS
     wl = WORKLOADS[args.workload]

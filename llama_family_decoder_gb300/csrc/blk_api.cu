@@ -108,7 +108,7 @@ Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, siz
     w.v = c.take(M * d.n_kv_heads * d.head_dim * es);
   }
   w.o = c.take(M * d.n_heads * d.head_dim * es);
-  w.mid = c.take(M * d.hidden * es);
+  w.mid = c.take(M * d.hidden * sizeof(float));  // the residual stream after attention, kept in fp32
   w.neur = c.take(M * d.ffn * es);
   if (decode) {
     const int splits = d.dtype == BLK_BF16 ? kMaxDecodeSplits : 1;
@@ -189,7 +189,8 @@ blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, in
 }
 
 blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K, const void* W, int N,
-                             const void* resid, void* out, void* tap, cudaStream_t s, const char* what) {
+                             const void* resid, bool resid_f32, void* out, bool out_f32, void* out2, void* tap,
+                             cudaStream_t s, const char* what) {
   TcGemmDesc g;
   g.na = 1;
   g.a[0] = {a, rows, 0};
@@ -201,6 +202,9 @@ blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K
   g.e.out = out;
   g.e.ldo = N;
   g.e.resid = resid;
+  g.e.resid_f32 = resid_f32 ? 1 : 0;
+  g.e.out_f32 = out_f32 ? 1 : 0;
+  g.e.out2 = out2;
   g.e.tap = tap;
   return tc(h, g, s, what);
 }
@@ -304,7 +308,7 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
   void* k = tap_or(taps, &blk_taps::attention_keys, ws.k);
   void* v = tap_or(taps, &blk_taps::attention_values, ws.v);
   void* o = tap_or(taps, &blk_taps::attention_head_outputs, ws.o);
-  void* mid = tap_or(taps, &blk_taps::layer_mid, ws.mid);
+  void* mid_tap = taps ? taps->layer_mid : nullptr;
   void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
   prof_mark(h, "rmsnorm1", 1, s);
   BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, M, d.hidden, d.eps, ws.y, bf, s), "rmsnorm 1"));
@@ -315,15 +319,15 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
   cudaError_t e = launch_attn_prefill_bf16(q, k, v, o, B, d.n_heads, d.n_kv_heads, T, d.head_dim, T, s, &why);
   BLK_TRY(check_cuda(e, "attention", why));
   prof_mark(h, "o_proj_gemm_resid", 1, s);
-  BLK_TRY(bf16_linear_resid(h, o, M, d.n_heads * d.head_dim, w->wo, d.hidden, x, mid,
+  BLK_TRY(bf16_linear_resid(h, o, M, d.n_heads * d.head_dim, w->wo, d.hidden, x, false, ws.mid, true, mid_tap,
                             taps ? taps->attention_output : nullptr, s, "o_proj GEMM"));
   prof_mark(h, "rmsnorm2", 1, s);
-  BLK_TRY(check_cuda(launch_rmsnorm(mid, w->ln2_g, M, d.hidden, d.eps, ws.y, bf, s), "rmsnorm 2"));
+  BLK_TRY(check_cuda(launch_rmsnorm(ws.mid, w->ln2_g, M, d.hidden, d.eps, ws.y, bf, s, true), "rmsnorm 2"));
   prof_mark(h, "mlp_up_gemm_act", 1, s);
   BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s));
   prof_mark(h, "down_gemm_resid", 1, s);
-  BLK_TRY(bf16_linear_resid(h, neur, M, d.ffn, w->w_down, d.hidden, mid, out, taps ? taps->mlp_output : nullptr, s,
-                            "down GEMM"));
+  BLK_TRY(bf16_linear_resid(h, neur, M, d.ffn, w->w_down, d.hidden, ws.mid, true, out, false, nullptr,
+                            taps ? taps->mlp_output : nullptr, s, "down GEMM"));
   prof_end(h, s);
   return BLK_OK;
 }
@@ -336,7 +340,7 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
   float* C = static_cast<float*>(ws.C);
   void* q = tap_or(taps, &blk_taps::attention_queries, ws.q);
   void* o = tap_or(taps, &blk_taps::attention_head_outputs, ws.o);
-  void* mid = tap_or(taps, &blk_taps::layer_mid, ws.mid);
+  void* mid_tap = taps ? taps->layer_mid : nullptr;
   void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
   int sp = 1;
   prof_mark(h, "rmsnorm1", 1, s);
@@ -362,8 +366,8 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
     BLK_TRY(bf16_stream_gemm(h, segs, 1, o, B, Hd, C, d.hidden, &sp, s, "decode o_proj GEMM"));
   }
   prof_mark(h, "o_post_resid_rmsnorm2", 1, s);
-  BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, x, mid, taps ? taps->attention_output : nullptr,
-                                       w->ln2_g, d.eps, ws.y, nullptr, bf, s),
+  BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, x, false, ws.mid, true, mid_tap,
+                                       taps ? taps->attention_output : nullptr, w->ln2_g, d.eps, ws.y, nullptr, bf, s),
                      "decode o_proj post"));
   prof_mark(h, "mlp_up_gemm", 1, s);
   if (d.act == BLK_ACT_SWIGLU) {
@@ -383,8 +387,8 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
     BLK_TRY(bf16_stream_gemm(h, segs, 1, neur, B, d.ffn, C, d.hidden, &sp, s, "decode down GEMM"));
   }
   prof_mark(h, "down_post_resid", 1, s);
-  BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, mid, out, taps ? taps->mlp_output : nullptr,
-                                       nullptr, 0.f, nullptr, cache->lens, bf, s),
+  BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, ws.mid, true, out, false, nullptr,
+                                       taps ? taps->mlp_output : nullptr, nullptr, 0.f, nullptr, cache->lens, bf, s),
                      "decode down post"));
   prof_end(h, s);
   return BLK_OK;
@@ -423,8 +427,8 @@ blk_status forward_f32(blk_handle* h, const void* x, int B, int T, const blk_wei
                      "attention"));
   BLK_TRY(check_cuda(launch_gemm_f32((const float*)o, (const float*)w->wo, C, d.hidden, M, d.hidden, Hd, s),
                      "o_proj GEMM"));
-  BLK_TRY(check_cuda(launch_post_resid(C, 1, M, d.hidden, d.hidden, x, mid, taps ? taps->attention_output : nullptr,
-                                       w->ln2_g, d.eps, ws.y, nullptr, bf, s),
+  BLK_TRY(check_cuda(launch_post_resid(C, 1, M, d.hidden, d.hidden, x, true, mid, true, nullptr,
+                                       taps ? taps->attention_output : nullptr, w->ln2_g, d.eps, ws.y, nullptr, bf, s),
                      "o_proj post"));
   const int nm = mlp_cols(d);
   if (d.act == BLK_ACT_SWIGLU) {
@@ -438,8 +442,9 @@ blk_status forward_f32(blk_handle* h, const void* x, int B, int T, const blk_wei
                      "activation"));
   BLK_TRY(check_cuda(launch_gemm_f32((const float*)neur, (const float*)w->w_down, C, d.hidden, M, d.hidden, d.ffn, s),
                      "down GEMM"));
-  BLK_TRY(check_cuda(launch_post_resid(C, 1, M, d.hidden, d.hidden, mid, out, taps ? taps->mlp_output : nullptr,
-                                       nullptr, 0.f, nullptr, decode ? cache->lens : nullptr, bf, s),
+  BLK_TRY(check_cuda(launch_post_resid(C, 1, M, d.hidden, d.hidden, mid, true, out, true, nullptr,
+                                       taps ? taps->mlp_output : nullptr, nullptr, 0.f, nullptr,
+                                       decode ? cache->lens : nullptr, bf, s),
                      "down post"));
   prof_end(h, s);
   return BLK_OK;
@@ -511,8 +516,8 @@ blk_status blk_create(const blk_desc* desc, blk_handle** out) {
     if (d.hidden / 8 > 8 * 256) return fail(BLK_ERR_UNSUPPORTED, "bf16 rmsnorm: hidden <= 16384");
     if (d.n_heads / d.n_kv_heads > 16) return fail(BLK_ERR_UNSUPPORTED, "bf16 decode: at most 16 heads per KV head");
   } else {
-    if (d.hidden % 4) return fail(BLK_ERR_UNSUPPORTED, "fp32 path: hidden must be a multiple of 4");
-    if (d.hidden / 4 > 8 * 256) return fail(BLK_ERR_UNSUPPORTED, "fp32 rmsnorm: hidden <= 8192");
+    if (d.hidden % 8) return fail(BLK_ERR_UNSUPPORTED, "fp32 path: hidden must be a multiple of 8");
+    if (d.hidden / 8 > 8 * 256) return fail(BLK_ERR_UNSUPPORTED, "fp32 rmsnorm: hidden <= 16384");
     if (d.head_dim > 256) return fail(BLK_ERR_UNSUPPORTED, "fp32 path: head_dim <= 256");
     if (d.max_seq > 50000) return fail(BLK_ERR_UNSUPPORTED, "fp32 attention: max_seq <= 50000");
   }
@@ -614,9 +619,8 @@ blk_status blk_rmsnorm(const void* x, const void* g, int rows, int n, float eps,
   if (!x || !g || !y) return fail(BLK_ERR_INVALID_ARG, "x, g and y must be non-NULL");
   if (rows < 0 || n <= 0) return fail(BLK_ERR_INVALID_ARG, "bad sizes");
   if (!aligned16(x) || !aligned16(g) || !aligned16(y)) return fail(BLK_ERR_ALIGNMENT, "pointers not 16-byte aligned");
-  const int vec = dtype == BLK_BF16 ? 8 : 4;
-  if (n % vec) return fail(BLK_ERR_UNSUPPORTED, "n must be a multiple of 8 (bf16) or 4 (fp32)");
-  if (n / vec > 8 * 256) return fail(BLK_ERR_UNSUPPORTED, "n too large");
+  if (n % 8) return fail(BLK_ERR_UNSUPPORTED, "n must be a multiple of 8");
+  if (n / 8 > 8 * 256) return fail(BLK_ERR_UNSUPPORTED, "n too large (<= 16384)");
   return check_cuda(launch_rmsnorm(x, g, rows, n, eps, y, dtype == BLK_BF16, static_cast<cudaStream_t>(stream)),
                     "rmsnorm");
 }
@@ -705,7 +709,8 @@ blk_status blk_mlp(blk_handle* h, const void* resid, const void* h_normed, const
   float* C = static_cast<float*>(c.take((size_t)rows * max_cols(d) * sizeof(float)));
   if (d.dtype == BLK_BF16) {
     BLK_TRY(bf16_mlp_up(h, h_normed, rows, w, neur, s));
-    return bf16_linear_resid(h, neur, rows, d.ffn, w->w_down, d.hidden, resid, out, nullptr, s, "down GEMM");
+    return bf16_linear_resid(h, neur, rows, d.ffn, w->w_down, d.hidden, resid, false, out, false, nullptr, nullptr, s,
+                             "down GEMM");
   }
   const float* y = static_cast<const float*>(h_normed);
   const int nm = mlp_cols(d);
@@ -720,8 +725,8 @@ blk_status blk_mlp(blk_handle* h, const void* resid, const void* h_normed, const
                      "activation"));
   BLK_TRY(check_cuda(launch_gemm_f32((const float*)neur, (const float*)w->w_down, C, d.hidden, rows, d.hidden, d.ffn, s),
                      "down GEMM"));
-  return check_cuda(launch_post_resid(C, 1, rows, d.hidden, d.hidden, resid, out, nullptr, nullptr, 0.f, nullptr,
-                                      nullptr, false, s),
+  return check_cuda(launch_post_resid(C, 1, rows, d.hidden, d.hidden, resid, true, out, true, nullptr, nullptr,
+                                      nullptr, 0.f, nullptr, nullptr, false, s),
                     "down post");
 }
 

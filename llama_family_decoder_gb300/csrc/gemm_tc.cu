@@ -283,9 +283,23 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
               return x > 0.0f ? ap * x * x + be * x : an * (expm1f(fminf(x, xe)) - x) + be * x;
             });
           } else if constexpr (EPI == (int)Epi::kResid) {
-            // contribution rounded to bf16 first, then added to the residual in fp32
+            // residual stream carried in fp32: out = resid + acc, rounded once
             float rr[16];
-            if (nv == 16) {
+            if (e.resid_f32) {
+              const float* rf = reinterpret_cast<const float*>(e.resid) + (size_t)row * e.ldo + col0 + cc;
+              if (nv == 16) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float4 f4 = reinterpret_cast<const float4*>(rf)[j];
+                  rr[4 * j] = f4.x;
+                  rr[4 * j + 1] = f4.y;
+                  rr[4 * j + 2] = f4.z;
+                  rr[4 * j + 3] = f4.w;
+                }
+              } else {
+                for (int j = 0; j < nv; ++j) rr[j] = rf[j];
+              }
+            } else if (nv == 16) {
               const uint4 ra = reinterpret_cast<const uint4*>(res + cc)[0];
               const uint4 rb = reinterpret_cast<const uint4*>(res + cc)[1];
               const uint32_t w[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
@@ -298,8 +312,25 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
             } else {
               for (int j = 0; j < nv; ++j) rr[j] = __bfloat162float(res[cc + j]);
             }
-            if (tap) store_bf16_row(tap + cc, vv, nv, [](float x, int) { return x; });
-            store_bf16_row(out + cc, vv, nv, [&](float x, int j) { return rr[j] + round_to<__nv_bfloat16>(x); });
+            float o[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = rr[j] + vv[j];
+            auto id = [](float x, int) { return x; };
+            if (tap) store_bf16_row(tap + cc, vv, nv, id);
+            if (e.out_f32) {
+              float* of = reinterpret_cast<float*>(e.out) + (size_t)row * e.ldo + col0 + cc;
+              if (nv == 16) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  reinterpret_cast<float4*>(of)[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+              } else {
+                for (int j = 0; j < nv; ++j) of[j] = o[j];
+              }
+            } else {
+              store_bf16_row(out + cc, o, nv, id);
+            }
+            if (e.out2)
+              store_bf16_row(reinterpret_cast<__nv_bfloat16*>(e.out2) + (size_t)row * e.ldo + col0 + cc, o, nv, id);
           }
         }
       }

@@ -12,8 +12,9 @@ struct DevStatus;
 
 // ---------------------------------------------------------------- RMSNorm
 // y[r,:] = x[r,:] * rsqrt(mean(x[r,:]^2) + eps) * g   (fp32 statistics)
+// x_f32: x is fp32 while g and y have the storage type (the bf16 path's fp32 residual stream).
 cudaError_t launch_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y, bool bf16,
-                           cudaStream_t s);
+                           cudaStream_t s, bool x_f32 = false);
 
 // ---------------------------------------------------------------- fp32 SIMT GEMM
 // C[m, c0 + n] = sum_k A[m, k] * B[n, k] for m < M, n < N  (fp32, row-major, ld = K for A/B).
@@ -23,7 +24,7 @@ cudaError_t launch_gemm_f32(const float* A, const float* B, float* C, int ldc, i
 
 enum class Epi : int {
   kStore = 0,     // out[row, col] = bf16(acc)
-  kResid = 1,     // out = bf16(resid + bf16(acc)); optional tap = bf16(acc)
+  kResid = 1,     // out = resid + acc (fp32 sum, stored fp32 or bf16); optional bf16 copy and tap = bf16(acc)
   kQkv = 2,       // per-head optional RMSNorm, RoPE, scatter to q/k/v head-major layouts
   kSwiglu = 3,    // paired B halves [gate | up]: out = bf16(silu(gate) * up)
   kRelu2 = 4,     // out = bf16(relu(acc)^2)
@@ -41,7 +42,10 @@ struct TcSeg {
 struct TcEpiArgs {
   void* out = nullptr;  // kStore/kResid/activations: bf16 [rows, ldo]; kPartialT: float partial base
   int ldo = 0;
-  const void* resid = nullptr;  // kResid: bf16 [rows, ldo]
+  const void* resid = nullptr;  // kResid: [rows, ldo], bf16 or (resid_f32) fp32
+  int resid_f32 = 0;
+  int out_f32 = 0;              // kResid: out is fp32 (the block's residual stream)
+  void* out2 = nullptr;         // kResid: optional bf16 copy of out
   void* tap = nullptr;          // kResid: optional bf16 contribution [rows, ldo]
   // kQkv
   void* q = nullptr;
@@ -97,12 +101,14 @@ cudaError_t launch_post_qkv(const float* C, int splits, int rows, int ldc, int s
                             const void* k_gain, float eps, const float2* rope, int rope_max_pos, void* q, void* k,
                             void* v, int kv_stride, bool bf16, cudaStream_t s);
 
-// out[r, c] = round(resid[r, c] + round(sum_s C[s, r, c])) for c < n; optional
-// contribution tap; optional fused RMSNorm of the new row into y (gain g);
-// optional lens bump (lens[r] += 1 for r < rows).
-cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int ldc, const void* resid, void* out,
-                              void* tap, const void* g, float eps, void* y, int* bump_lens, bool bf16,
-                              cudaStream_t s);
+// out[r, c] = resid[r, c] + sum_s C[s, r, c] for c < n (fp32 sum, stored as
+// fp32 when out_f32, else in the storage type); optional storage-type copy
+// out2 and contribution tap; optional fused RMSNorm of the new row into y
+// (gain g); optional lens bump (lens[r] += 1 for r < rows). resid is fp32 when
+// resid_f32, else the storage type.
+cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int ldc, const void* resid, bool resid_f32,
+                              void* out, bool out_f32, void* out2, void* tap, const void* g, float eps, void* y,
+                              int* bump_lens, bool bf16, cudaStream_t s);
 
 // neurons[r, f] = act(C) for f < F; SwiGLU reads gate at column f and up at F + f.
 cudaError_t launch_post_act(const float* C, int splits, int rows, int F, int ldc, int act, float alpha_p,

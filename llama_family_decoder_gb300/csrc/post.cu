@@ -5,8 +5,8 @@
 //    pairing, angle = position * theta^(-2i/d)), scatter to head-major q and
 //    to the K/V buffers or cache slots;
 //  * post_resid: residual add after o_proj / down_proj ("arcee", "The block, in
-//    order"), with the contribution rounded to the storage type first, and the
-//    next RMSNorm fused;
+//    order"), summed in fp32 (the residual stream stays fp32 inside the block),
+//    with the next RMSNorm fused;
 //  * post_act: SiLU-gated, squared-ReLU and xIELU activations.
 #include "common.cuh"
 #include "kernels.h"
@@ -92,21 +92,25 @@ __global__ void post_qkv_kernel(const float* __restrict__ C, int splits, int row
   }
 }
 
-template <typename T>
+// TR: residual type, TO: output type, TY: storage type (gain, y, out2, tap).
+template <typename TR, typename TO, typename TY>
 __global__ void post_resid_kernel(const float* __restrict__ C, int splits, int rows, int n, int ldc,
-                                  const T* __restrict__ resid, T* __restrict__ out, T* __restrict__ tap,
-                                  const T* __restrict__ g, float eps, T* __restrict__ y, int* __restrict__ bump_lens) {
+                                  const TR* __restrict__ resid, TO* __restrict__ out, TY* __restrict__ out2,
+                                  TY* __restrict__ tap, const TY* __restrict__ g, float eps, TY* __restrict__ y,
+                                  int* __restrict__ bump_lens) {
   __shared__ float red[32];
   const int r = blockIdx.x;
   if (r >= rows) return;
   const size_t sstride = (size_t)rows * ldc;
   float ss = 0.f;
   for (int c = threadIdx.x; c < n; c += blockDim.x) {
-    const float contrib = round_to<T>(split_sum(C, splits, sstride, (size_t)r * ldc + c));
-    const T o = from_f32<T>(to_f32<T>(resid[(size_t)r * n + c]) + contrib);
-    out[(size_t)r * n + c] = o;
-    if (tap) tap[(size_t)r * n + c] = from_f32<T>(contrib);
-    const float of = to_f32<T>(o);
+    const float contrib = split_sum(C, splits, sstride, (size_t)r * ldc + c);
+    const float o = to_f32<TR>(resid[(size_t)r * n + c]) + contrib;  // the residual stream, summed in fp32
+    const TO os = from_f32<TO>(o);
+    out[(size_t)r * n + c] = os;
+    if (out2) out2[(size_t)r * n + c] = from_f32<TY>(o);
+    if (tap) tap[(size_t)r * n + c] = from_f32<TY>(contrib);
+    const float of = to_f32<TO>(os);
     ss += of * of;
   }
   if (g == nullptr) {
@@ -120,7 +124,7 @@ __global__ void post_resid_kernel(const float* __restrict__ C, int splits, int r
   for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
   const float inv = rsqrtf(tot / (float)n + eps);
   for (int c = threadIdx.x; c < n; c += blockDim.x)
-    y[(size_t)r * n + c] = from_f32<T>(to_f32<T>(out[(size_t)r * n + c]) * inv * to_f32<T>(g[c]));
+    y[(size_t)r * n + c] = from_f32<TY>(to_f32<TO>(out[(size_t)r * n + c]) * inv * to_f32<TY>(g[c]));
   if (bump_lens && threadIdx.x == 0) bump_lens[r] += 1;
 }
 
@@ -172,21 +176,28 @@ cudaError_t launch_post_qkv(const float* C, int splits, int rows, int ldc, int s
   return cudaGetLastError();
 }
 
-cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int ldc, const void* resid, void* out,
-                              void* tap, const void* g, float eps, void* y, int* bump_lens, bool bf16,
-                              cudaStream_t s) {
+cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int ldc, const void* resid, bool resid_f32,
+                              void* out, bool out_f32, void* out2, void* tap, const void* g, float eps, void* y,
+                              int* bump_lens, bool bf16, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  if (bf16) {
-    using T = __nv_bfloat16;
-    post_resid_kernel<T><<<rows, 256, 0, s>>>(C, splits, rows, n, ldc, static_cast<const T*>(resid),
-                                             static_cast<T*>(out), static_cast<T*>(tap), static_cast<const T*>(g),
-                                             eps, static_cast<T*>(y), bump_lens);
+  using B = __nv_bfloat16;
+#define BLK_POST_RESID(TR, TO, TY)                                                                              \
+  post_resid_kernel<TR, TO, TY><<<rows, 256, 0, s>>>(C, splits, rows, n, ldc, static_cast<const TR*>(resid),   \
+                                                     static_cast<TO*>(out), static_cast<TY*>(out2),             \
+                                                     static_cast<TY*>(tap), static_cast<const TY*>(g), eps,     \
+                                                     static_cast<TY*>(y), bump_lens)
+  if (!bf16) {
+    BLK_POST_RESID(float, float, float);
+  } else if (resid_f32 && out_f32) {
+    BLK_POST_RESID(float, float, B);
+  } else if (resid_f32) {
+    BLK_POST_RESID(float, B, B);
+  } else if (out_f32) {
+    BLK_POST_RESID(B, float, B);
   } else {
-    using T = float;
-    post_resid_kernel<T><<<rows, 256, 0, s>>>(C, splits, rows, n, ldc, static_cast<const T*>(resid),
-                                             static_cast<T*>(out), static_cast<T*>(tap), static_cast<const T*>(g),
-                                             eps, static_cast<T*>(y), bump_lens);
+    BLK_POST_RESID(B, B, B);
   }
+#undef BLK_POST_RESID
   return cudaGetLastError();
 }
 

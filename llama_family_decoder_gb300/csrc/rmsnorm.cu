@@ -1,8 +1,9 @@
 // Row-wise RMSNorm (nnterp "input_layernorm" / "post_attention_layernorm";
 // "LlamaForCausalLM-32L-4096d" sheet: rmsnorm(x, ..., eps=1e-05)):
 //   y[r, :] = x[r, :] * rsqrt(mean(x[r, :]^2) + eps) * g
-// Statistics in fp32. HBM-bound: one read and one write of the row, 128-bit
-// loads/stores, the row held in registers between the two passes.
+// Statistics in fp32. HBM-bound: one read and one write of the row with
+// 128-bit accesses, the row held in registers between the two passes. x may be
+// fp32 while g and y are bf16 (the bf16 path keeps its residual stream in fp32).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -13,57 +14,55 @@ namespace {
 constexpr int kThreads = 256;
 
 template <typename T>
-struct Vec;
+__device__ __forceinline__ void load8(const T* p, float (&f)[8]);
 template <>
-struct Vec<float> {
-  static constexpr int N = 4;
-  static __device__ __forceinline__ void unpack(const uint4& u, float* f) {
-    f[0] = __uint_as_float(u.x);
-    f[1] = __uint_as_float(u.y);
-    f[2] = __uint_as_float(u.z);
-    f[3] = __uint_as_float(u.w);
-  }
-  static __device__ __forceinline__ uint4 pack(const float* f) {
-    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
-  }
-};
+__device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w, f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+}
 template <>
-struct Vec<__nv_bfloat16> {
-  static constexpr int N = 8;
-  static __device__ __forceinline__ void unpack(const uint4& u, float* f) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 p = unpack_bf16x2(w[i]);
-      f[2 * i] = p.x;
-      f[2 * i + 1] = p.y;
-    }
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = unpack_bf16x2(w[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
   }
-  static __device__ __forceinline__ uint4 pack(const float* f) {
-    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                      pack_bf16x2(f[6], f[7]));
-  }
-};
+}
 
-template <typename T, int NV>
-__global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ g, int rows,
-                                                           int n, float eps, T* __restrict__ y) {
-  constexpr int E = Vec<T>::N;
+template <typename T>
+__device__ __forceinline__ void store8(T* p, const float (&f)[8]);
+template <>
+__device__ __forceinline__ void store8<float>(float* p, const float (&f)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+template <>
+__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* p, const float (&f)[8]) {
+  *reinterpret_cast<uint4*>(p) =
+      make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+}
+
+// NC = chunks of 8 elements per thread
+template <typename TX, typename TY, int NC>
+__global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const TX* __restrict__ x, const TY* __restrict__ g,
+                                                           int rows, int n, float eps, TY* __restrict__ y) {
   __shared__ float red[kThreads / 32];
-  const int nvec = n / E;
+  const int nchunk = n / 8;
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * n);
-    uint4 buf[NV];
+    const TX* xr = x + (size_t)r * n;
+    float buf[NC][8];
     float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const int v = threadIdx.x + j * kThreads;
-      if (v < nvec) {
-        buf[j] = xr[v];
-        float f[E];
-        Vec<T>::unpack(buf[j], f);
+    for (int j = 0; j < NC; ++j) {
+      const int c = threadIdx.x + j * kThreads;
+      if (c < nchunk) {
+        load8<TX>(xr + c * 8, buf[j]);
 #pragma unroll
-        for (int i = 0; i < E; ++i) ss += f[i] * f[i];
+        for (int i = 0; i < 8; ++i) ss += buf[j][i] * buf[j][i];
       }
     }
     ss = warp_sum(ss);
@@ -74,43 +73,40 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const T* __restrict__
     for (int w = 0; w < kThreads / 32; ++w) tot += red[w];
     __syncthreads();  // red is reused by the next row
     const float inv = rsqrtf(tot / (float)n + eps);
-    uint4* yr = reinterpret_cast<uint4*>(y + (size_t)r * n);
-    const uint4* gv = reinterpret_cast<const uint4*>(g);
+    TY* yr = y + (size_t)r * n;
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const int v = threadIdx.x + j * kThreads;
-      if (v < nvec) {
-        float f[E], gg[E];
-        Vec<T>::unpack(buf[j], f);
-        Vec<T>::unpack(gv[v], gg);
+    for (int j = 0; j < NC; ++j) {
+      const int c = threadIdx.x + j * kThreads;
+      if (c < nchunk) {
+        float gg[8], o[8];
+        load8<TY>(g + c * 8, gg);
 #pragma unroll
-        for (int i = 0; i < E; ++i) f[i] = f[i] * inv * gg[i];
-        yr[v] = Vec<T>::pack(f);
+        for (int i = 0; i < 8; ++i) o[i] = buf[j][i] * inv * gg[i];
+        store8<TY>(yr + c * 8, o);
       }
     }
   }
 }
 
-template <typename T>
+template <typename TX, typename TY>
 cudaError_t launch_t(const void* x, const void* g, int rows, int n, float eps, void* y, cudaStream_t s) {
-  const int nvec = n / Vec<T>::N;
-  const int nv = (nvec + kThreads - 1) / kThreads;
+  const int nc = (n / 8 + kThreads - 1) / kThreads;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = rows < sms * 8 ? rows : sms * 8;
-  auto X = static_cast<const T*>(x);
-  auto G = static_cast<const T*>(g);
-  auto Y = static_cast<T*>(y);
-  switch (nv) {
-    case 1: rmsnorm_kernel<T, 1><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 2: rmsnorm_kernel<T, 2><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 3: rmsnorm_kernel<T, 3><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 4: rmsnorm_kernel<T, 4><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 5: rmsnorm_kernel<T, 5><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 6: rmsnorm_kernel<T, 6><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 7: rmsnorm_kernel<T, 7><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 8: rmsnorm_kernel<T, 8><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
+  auto X = static_cast<const TX*>(x);
+  auto G = static_cast<const TY*>(g);
+  auto Y = static_cast<TY*>(y);
+  switch (nc) {
+    case 1: rmsnorm_kernel<TX, TY, 1><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
+    case 2: rmsnorm_kernel<TX, TY, 2><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
+    case 3: rmsnorm_kernel<TX, TY, 3><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
+    case 4: rmsnorm_kernel<TX, TY, 4><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
+    case 5: rmsnorm_kernel<TX, TY, 5><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
+    case 6: rmsnorm_kernel<TX, TY, 6><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
+    case 7: rmsnorm_kernel<TX, TY, 7><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
+    case 8: rmsnorm_kernel<TX, TY, 8><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -119,9 +115,12 @@ cudaError_t launch_t(const void* x, const void* g, int rows, int n, float eps, v
 }  // namespace
 
 cudaError_t launch_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y, bool bf16,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool x_f32) {
   if (rows <= 0) return cudaSuccess;
-  return bf16 ? launch_t<__nv_bfloat16>(x, g, rows, n, eps, y, s) : launch_t<float>(x, g, rows, n, eps, y, s);
+  if (n % 8) return cudaErrorInvalidValue;
+  if (!bf16) return launch_t<float, float>(x, g, rows, n, eps, y, s);
+  if (x_f32) return launch_t<float, __nv_bfloat16>(x, g, rows, n, eps, y, s);
+  return launch_t<__nv_bfloat16, __nv_bfloat16>(x, g, rows, n, eps, y, s);
 }
 
 }  // namespace blk

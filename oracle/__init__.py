@@ -16,5 +16,6 @@ from .block import (  # noqa: F401
     xielu_effective,
     softplus,
     block_forward,
+    mlp,
     decode_step,
 )

@@ -227,38 +227,45 @@ def _project_q(cfg, w, h_norm_rows, positions_rows):
     return rope(q, positions_rows, cfg.rope_theta)
 
 
-def _finish_rows(cfg, w, x_rows, heads_out):
-    """o_proj, residual, second norm, MLP and residual for a set of rows.
+def mlp(cfg, w, h):
+    """The MLP sublayer on normed rows h [..., D] (no residual).
 
-    heads_out: [H, R, d] per-head outputs of those rows.
+    "LlamaForCausalLM-32L-4096d": (silu(h gate^T) * (h up^T)) down^T; "arcee":
+    down_proj(relu(up_proj(z)) ** 2); "apertus": down_proj(xielu(up_proj(z))).
+    Returns mlp_up_output, (mlp_gate_output), mlp_activation, mlp_neurons, mlp_output.
     """
+    h = np.asarray(h, dtype=F64)
     taps = {}
-    R = x_rows.shape[0]
-    premix = heads_out.transpose(1, 0, 2).reshape(R, -1)  # [R, H*d]
-    attn_out = premix @ w["o_proj"].T
-    mid = x_rows + attn_out
-    h2 = rms_norm(mid, w["post_attention_layernorm"], cfg.rms_norm_eps)
-    up = h2 @ w["up_proj"].T
+    up = h @ w["up_proj"].T
     if cfg.hidden_act == "silu":
-        gate = h2 @ w["gate_proj"].T
+        gate = h @ w["gate_proj"].T
         act = _act(cfg, up, gate)
         neurons = act * up
         taps["mlp_gate_output"] = gate
     else:
         act = _act(cfg, up)
         neurons = act
-    mlp_out = neurons @ w["down_proj"].T
-    out = mid + mlp_out
+    taps.update(mlp_up_output=up, mlp_activation=act, mlp_neurons=neurons, mlp_output=neurons @ w["down_proj"].T)
+    return taps
+
+
+def _finish_rows(cfg, w, x_rows, heads_out):
+    """o_proj, residual, second norm, MLP and residual for a set of rows.
+
+    heads_out: [H, R, d] per-head outputs of those rows.
+    """
+    R = x_rows.shape[0]
+    premix = heads_out.transpose(1, 0, 2).reshape(R, -1)  # [R, H*d]
+    attn_out = premix @ w["o_proj"].T
+    mid = x_rows + attn_out
+    h2 = rms_norm(mid, w["post_attention_layernorm"], cfg.rms_norm_eps)
+    taps = mlp(cfg, w, h2)
     taps.update(
         attention_head_outputs=heads_out.transpose(1, 0, 2),  # [R, H, d]
         attention_output=attn_out,
         layer_mid=mid,
         mlp_norm_output=h2,
-        mlp_up_output=up,
-        mlp_activation=act,
-        mlp_neurons=neurons,
-        mlp_output=mlp_out,
-        layer_output=out,
+        layer_output=mid + taps["mlp_output"],
     )
     return taps
 

@@ -1,0 +1,62 @@
+"""Full-size parity: the pages' workload shapes, run exactly as bench.py runs them
+(one blk_forward over the whole batch), checked on sampled output rows that the
+fp64 oracle computes one by one (keys/values of the whole prefix included)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from llama_family_decoder_gb300 import DecoderBlock
+from llama_family_decoder_gb300.synth import WORKLOADS, make_input, make_kv_cache, make_weights
+from tests.helpers import TOL, bf16_floor, cfg_of, np64, rel_err, weights_np
+
+pytestmark = pytest.mark.gpu
+
+PREFILL = ["llama7b_bf16_B1_T2048", "arcee_gqa_bf16_B4_T2048", "apertus_qknorm_bf16_B2_T4096"]
+
+
+@pytest.mark.parametrize("name", PREFILL)
+def test_prefill_full_size_sampled_rows(name):
+    wl = WORKLOADS[name]
+    w = make_weights(wl)
+    x = make_input(wl)
+    blk = DecoderBlock.from_workload(wl)
+    out = blk.forward(x.cuda(), {k: v.cuda() for k, v in w.items()})
+    torch.cuda.synchronize()
+    assert blk.last_status() == 0
+    out = out.cpu()
+    del blk
+    wn = weights_np(w)
+    T = wl.seq
+    rows = sorted({0, 1, 63, 64, 127, 128, 129, 1000, T // 2 + 3, T - 129, T - 2, T - 1})
+    for b in sorted({0, wl.batch - 1}):
+        ref = oracle.block_forward(cfg_of(wl), wn, np64(x[b:b + 1]), rows=rows)["layer_output"][0]
+        got = out[b, rows]
+        err, floor = rel_err(got, ref), bf16_floor(ref)
+        print(f"{name} batch {b}: max|err|/RMS {err:.4f} (bf16 floor {floor:.4f})")
+        assert err <= TOL["bf16"], (err, floor)
+        assert torch.isfinite(out[b]).all()
+
+
+def test_decode_full_size_sampled_sequences():
+    wl = WORKLOADS["llama7b_decode_bf16_B64_L4096"]
+    w = make_weights(wl)
+    x = make_input(wl)[:, 0]
+    kc, vc = make_kv_cache(wl)
+    blk = DecoderBlock.from_workload(wl)
+    lens = torch.full((wl.batch,), wl.cache_len, dtype=torch.int32, device="cuda")
+    kd, vd = kc.cuda(), vc.cuda()
+    out = blk.forward(x[:, None].cuda(), {k: v.cuda() for k, v in w.items()},
+                      cache={"k": kd, "v": vd, "lens": lens}, host_lens_max=wl.cache_len)
+    torch.cuda.synchronize()
+    assert blk.last_status() == 0
+    assert (lens == wl.cache_len + 1).all()
+    seqs = [0, 31, 63]
+    ref = oracle.decode_step(cfg_of(wl), weights_np(w), np64(x[seqs]), np64(kc[seqs]), np64(vc[seqs]),
+                             np.full(len(seqs), wl.cache_len))
+    got = out[seqs, 0].cpu()
+    err, floor = rel_err(got, ref["layer_output"]), bf16_floor(ref["layer_output"])
+    print(f"decode: max|err|/RMS {err:.4f} (bf16 floor {floor:.4f})")
+    assert err <= TOL["bf16"], (err, floor)
+    assert rel_err(kd[seqs, :, wl.cache_len].cpu(), ref["new_key"]) <= TOL["bf16"]
+    assert rel_err(vd[seqs, :, wl.cache_len].cpu(), ref["new_value"]) <= TOL["bf16"]

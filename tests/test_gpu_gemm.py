@@ -29,11 +29,13 @@ def test_gemm_matches_fp64(M, N, K, bn):
     c = debug_gemm_bf16(a.cuda(), b.cuda(), bn=bn)
     torch.cuda.synchronize()
     ref = a.double() @ b.double().T
-    err = (c.double().cpu() - ref).abs().max() / ref.pow(2).mean().sqrt()
-    assert err < 8e-3, float(err)  # bf16 output rounding only
+    # bf16 output rounding (<= 2^-9 relative) plus a small fp32-accumulation allowance
+    bound = 2.0 ** -8 * ref.abs() + 1e-4 * ref.pow(2).mean().sqrt()
+    bad = ((c.double().cpu() - ref).abs() > bound).sum()
+    assert bad == 0, int(bad)
 
 
-@pytest.mark.parametrize("M,N,K,splits", [(64, 384, 4096, 4), (5, 1000, 1000, 3), (64, 6144, 512, 1)])
+@pytest.mark.parametrize("M,N,K,splits", [(64, 384, 4096, 4), (5, 1000, 1000, 3), (64, 6144, 512, 2)])
 def test_gemm_split_partials(M, N, K, splits):
     a, b = _operands(M, N, K, seed=7 * M + N)
     parts = debug_gemm_bf16(a.cuda(), b.cuda(), bn=64, split_k=splits)

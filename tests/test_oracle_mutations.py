@@ -90,12 +90,12 @@ def _relu_not_squared(u):
     return np.maximum(np.asarray(u, dtype=F64), 0.0)
 
 
-def _finish_swapped(cfg, w, x_rows, heads_out):
+def _mlp_swapped(cfg, w, h):
     # silu applied to up instead of gate
     w2 = dict(w)
     if cfg.hidden_act == "silu":
         w2["gate_proj"], w2["up_proj"] = w["up_proj"], w["gate_proj"]
-    return _orig_finish(cfg, w2, x_rows, heads_out)
+    return _orig_mlp(cfg, w2, h)
 
 
 def _finish_no_residual(cfg, w, x_rows, heads_out):
@@ -105,6 +105,7 @@ def _finish_no_residual(cfg, w, x_rows, heads_out):
 
 
 _orig_finish = ob._finish_rows
+_orig_mlp = ob.mlp
 
 MUTATIONS = {
     "rms_eps_outside_sqrt": [("rms_norm", _rms_eps_outside)],
@@ -119,7 +120,7 @@ MUTATIONS = {
     "xielu_dropped_min_and_sign": [("xielu", _xielu_no_min)],
     "silu_sign": [("silu", _silu_wrong)],
     "relu_not_squared": [("relu2", _relu_not_squared)],
-    "swiglu_gate_up_swapped": [("_finish_rows", _finish_swapped)],
+    "swiglu_gate_up_swapped": [("mlp", _mlp_swapped)],
     "missing_residual": [("_finish_rows", _finish_no_residual)],
 }
 
