@@ -194,6 +194,36 @@ blk_status blk_last_status(blk_handle* h);
 void blk_xielu_effective(float raw_alpha_p, float raw_alpha_n, float beta, float* alpha_p,
                          float* alpha_n);
 
+/* Allocation-free decode attention. This entry point has no counterpart in the
+ * paper; it exists for callers that cannot call cudaMalloc: for instance a host
+ * plugin interface that hands over only input and output pointers and no
+ * workspace, a runtime that has already given all device memory to its own
+ * pool, or a latency-critical loop that cannot afford cudaMalloc's implicit
+ * device synchronisation. Such a caller cannot create a handle (blk_create
+ * allocates), so this call needs none.
+ *
+ * It computes the same thing as blk_attn_gqa with kv_lens and seq_q == 1 on
+ * the bf16 path: for each sequence b and query head h, o[b, h, :] =
+ * softmax(q[b, h] . k[b, j, s] / sqrt(d), s < kv_lens[b]) @ v[b, j, s, :] with
+ * j = h / (n_heads / n_kv_heads). q [B, H, 1, 128] and o [B, H, 128] (i.e.
+ * [B, 1, H, 128]); k, v [B, Hkv, kv_stride, 128]; kv_lens device int[B] with
+ * 1 <= kv_lens[b] <= kv_stride; all bf16 device pointers, 16-byte aligned.
+ *
+ * Its per-split partial results live in one file-scope 16 MiB device array
+ * that every GPU loading the library holds until exit. The limit is
+ * batch * n_heads * (head_dim + 2) * 4 bytes <= 16 MiB (e.g. 64 x 32 heads);
+ * larger calls return BLK_ERR_UNSUPPORTED with that reason. Every call shares
+ * the array and it keeps the last call's contents; every value a call reads
+ * from it is written earlier in the same call, so nothing needs clearing, but
+ * calls that overlap on the GPU (other streams, other host threads) race on
+ * it and must be serialised by the caller. The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture. It calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA. */
+blk_status blk_attn_decode_noalloc(const void* q, const void* k, const void* v, const int* kv_lens, int batch,
+                                   int n_heads, int n_kv_heads, int head_dim, int kv_stride, void* o, void* stream);
+
 /* Static name of a status code. */
 const char* blk_error_string(blk_status s);
 

@@ -70,6 +70,8 @@ SIGNATURES = {
     "blk_profile_stage_name": (c_char_p, [c_void_p, c_int]),
     "blk_profile_reset": (None, [c_void_p]),
     "blk_debug_gemm_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "blk_attn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                        c_void_p, c_void_p]),
 }
 
 _lib_handle = None
@@ -262,3 +264,15 @@ def debug_gemm_bf16(a, b, bn=256, split_k=1, out=None, stream=None):
             out = torch.empty(split_k, M, N, dtype=torch.float32, device=a.device)
     _check(lib().blk_debug_gemm_bf16(_ptr(a), _ptr(b), _ptr(out), M, N, K, bn, split_k, _stream_ptr(stream)))
     return out
+
+
+def attn_decode_noalloc(q, k, v, kv_lens, o, stream=None):
+    """Decode attention through blk_attn_decode_noalloc (no workspace, no handle).
+
+    q [B, H, 1, d], k/v [B, Hkv, kv_stride, d], kv_lens int32 [B], o [B, 1, H, d]; bf16 on the device.
+    """
+    B, H = q.shape[0], q.shape[1]
+    Hkv, kv_stride, d = k.shape[1], k.shape[2], k.shape[3]
+    _check(lib().blk_attn_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_lens), B, H, Hkv, d, kv_stride, _ptr(o),
+                                         _stream_ptr(stream)))
+    return o

@@ -13,6 +13,8 @@
 // split), puts the G = H/Hkv query heads of the group on the MMA's rows, and
 // its four warps each own 16 keys of every 64-key tile (their partial softmax
 // states merge at the end). Splits are merged by a second small kernel.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -487,6 +489,85 @@ cudaError_t launch_attn_decode_bf16(const void* q, const void* k, const void* v,
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
       static_cast<const __nv_bfloat16*>(v), ws_ml, ws_o, H, Hkv, kv_stride, kv_lens, len_add, chunk, splits);
   cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_decode_combine_kernel<<<dim3(H, B), kD, 0, s>>>(ws_ml, ws_o, static_cast<__nv_bfloat16*>(o), H, splits);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ allocation-free decode variant
+
+// Fixed device scratch for the allocation-free decode attention entry point:
+// the per-split softmax partials (max, sum, unnormalised output) that the
+// workspace-taking path keeps in caller memory. Every device that loads the
+// library holds it until exit; every call shares it.
+static __device__ __align__(256) float g_decode_scratch[kDecodeStaticScratchBytes / sizeof(float)];
+
+namespace {
+std::mutex g_scratch_mu;
+constexpr int kMaxDevices = 64;
+float* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_decode_scratch on the current device, looked up once
+// per device (host code cannot use the symbol itself as a device pointer).
+cudaError_t scratch_address(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    float* p = nullptr;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_attn_decode_bf16_static(const void* q, const void* k, const void* v, void* o, int B, int H,
+                                           int Hkv, int d, int kv_stride, const int* kv_lens, int num_sms,
+                                           cudaStream_t s, const char** why) {
+  if (d != kD) {
+    *why = "bf16 attention: head_dim must be 128";
+    return cudaErrorInvalidValue;
+  }
+  if (H / Hkv > 16) {
+    *why = "bf16 decode attention: at most 16 query heads per KV head";
+    return cudaErrorInvalidValue;
+  }
+  if (B <= 0) return cudaSuccess;
+  const size_t per_split = (size_t)B * H * (2 + d) * sizeof(float);
+  if (per_split > kDecodeStaticScratchBytes) {
+    *why = "allocation-free decode attention: batch * n_heads * (head_dim + 2) * 4 bytes exceeds the 16 MiB scratch";
+    return cudaErrorInvalidValue;
+  }
+  float* scratch = nullptr;
+  cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess) {
+    *why = "cudaGetSymbolAddress of the decode scratch failed";
+    return e;
+  }
+  static bool configured = false;
+  if (!configured) {
+    e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  int splits = attn_decode_splits(B, Hkv, kv_stride, num_sms);
+  const int fit = (int)(kDecodeStaticScratchBytes / per_split);
+  if (splits > fit) splits = fit;
+  int chunk = (kv_stride + splits - 1) / splits;
+  chunk = (chunk + kTileKeys - 1) / kTileKeys * kTileKeys;
+  // every partial the combine step reads is written by this call first: nothing to clear
+  float* ws_ml = scratch;
+  float* ws_o = ws_ml + (size_t)B * H * splits * 2;
+  dim3 grid(splits, Hkv, B);
+  attn_decode_kernel<<<grid, kDThreads, kDSmem, s>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+      static_cast<const __nv_bfloat16*>(v), ws_ml, ws_o, H, Hkv, kv_stride, kv_lens, 0, chunk, splits);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_decode_combine_kernel<<<dim3(H, B), kD, 0, s>>>(ws_ml, ws_o, static_cast<__nv_bfloat16*>(o), H, splits);
   return cudaGetLastError();

@@ -820,6 +820,27 @@ blk_status blk_debug_gemm_bf16(const void* a, const void* b, void* c, int M, int
   return e == cudaSuccess ? BLK_OK : cuda_fail(e, "debug GEMM", why);
 }
 
+blk_status blk_attn_decode_noalloc(const void* q, const void* k, const void* v, const int* kv_lens, int batch,
+                                   int n_heads, int n_kv_heads, int head_dim, int kv_stride, void* o, void* stream) {
+  if (!q || !k || !v || !kv_lens || !o) return fail(BLK_ERR_INVALID_ARG, "NULL argument");
+  if (batch <= 0 || n_heads <= 0 || n_kv_heads <= 0 || kv_stride <= 0 || n_heads % n_kv_heads)
+    return fail(BLK_ERR_INVALID_ARG, "bad sizes");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return fail(BLK_ERR_ALIGNMENT, "alignment");
+  if (head_dim != 128) return fail(BLK_ERR_UNSUPPORTED, "head_dim must be 128");
+  if (n_heads / n_kv_heads > 16) return fail(BLK_ERR_UNSUPPORTED, "at most 16 query heads per KV head");
+  if ((size_t)batch * n_heads * (head_dim + 2) * sizeof(float) > kDecodeStaticScratchBytes)
+    return fail(BLK_ERR_UNSUPPORTED,
+                "batch * n_heads * (head_dim + 2) * 4 bytes exceeds the 16 MiB allocation-free scratch");
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  const char* why = nullptr;
+  e = launch_attn_decode_bf16_static(q, k, v, o, batch, n_heads, n_kv_heads, head_dim, kv_stride, kv_lens, sms,
+                                     static_cast<cudaStream_t>(stream), &why);
+  return e == cudaSuccess ? BLK_OK : cuda_fail(e, "allocation-free decode attention", why);
+}
+
 blk_status blk_last_status(blk_handle* h) {
   if (!h) return fail(BLK_ERR_INVALID_ARG, "NULL handle");
   DevStatus st{0, 0};

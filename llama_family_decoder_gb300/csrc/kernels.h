@@ -131,4 +131,11 @@ cudaError_t launch_attn_decode_bf16(const void* q, const void* k, const void* v,
                                     int num_sms, cudaStream_t s, const char** why);
 int attn_decode_splits(int B, int Hkv, int max_len, int num_sms);
 
+// Decode attention with its split partials in a fixed file-scope device array
+// (no workspace, no allocation); kv_lens[b] keys per sequence, <= kv_stride.
+constexpr size_t kDecodeStaticScratchBytes = 16u << 20;
+cudaError_t launch_attn_decode_bf16_static(const void* q, const void* k, const void* v, void* o, int B, int H,
+                                           int Hkv, int d, int kv_stride, const int* kv_lens, int num_sms,
+                                           cudaStream_t s, const char** why);
+
 }  // namespace blk
