@@ -148,6 +148,27 @@ blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const b
                        blk_kv_cache* cache, int host_lens_max, void* out, void* workspace,
                        size_t workspace_bytes, const blk_taps* taps, void* stream);
 
+/* A recorded forward: the launches one blk_forward makes for fixed arguments,
+ * captured once into a CUDA graph so that replaying it costs one launch. */
+typedef struct blk_graph blk_graph;
+
+/* Records blk_forward(h, x, ..., taps) with exactly these arguments (captured on
+ * a private stream; nothing runs now) and instantiates the graph. Replays read
+ * and write the same buffers, so the caller refreshes inputs in place between
+ * replays. A decode graph bumps lens on every replay, as blk_forward does. If
+ * profiling is on for h, the graph also records the per-stage events and
+ * blk_profile_collect reads them after a replay (keep profiling on while the
+ * graph exists). Errors: those of blk_forward, CUDA. */
+blk_status blk_forward_graph_create(blk_handle* h, const void* x, int batch, int seq, const blk_weights* w,
+                                    blk_kv_cache* cache, int host_lens_max, void* out, void* workspace,
+                                    size_t workspace_bytes, const blk_taps* taps, blk_graph** out_graph);
+
+/* Enqueues one replay on the caller's stream. Errors: INVALID_ARG, CUDA. */
+blk_status blk_graph_launch(blk_graph* g, void* stream);
+
+/* Frees the graph (the caller ensures no replay is in flight). Safe on NULL. */
+blk_status blk_graph_destroy(blk_graph* g);
+
 /* Stage: RMSNorm of each row (nnterp "input_layernorm" / "post_attention_layernorm"):
  * y[r, :] = x[r, :] / sqrt(mean(x[r, :]^2) + eps) * g, statistics in fp32.
  * x, y [rows, n], g [n], device, dtype elements; n % 8 == 0 (bf16) or n % 4 == 0

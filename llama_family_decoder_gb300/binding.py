@@ -70,6 +70,11 @@ SIGNATURES = {
     "blk_profile_stage_name": (c_char_p, [c_void_p, c_int]),
     "blk_profile_reset": (None, [c_void_p]),
     "blk_debug_gemm_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "blk_forward_graph_create": (c_int, [c_void_p, c_void_p, c_int, c_int, POINTER(blk_weights),
+                                         POINTER(blk_kv_cache), c_int, c_void_p, c_void_p, c_size_t,
+                                         POINTER(blk_taps), POINTER(c_void_p)]),
+    "blk_graph_launch": (c_int, [c_void_p, c_void_p]),
+    "blk_graph_destroy": (c_int, [c_void_p]),
     "blk_attn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                         c_void_p, c_void_p]),
 }
@@ -200,6 +205,21 @@ class DecoderBlock:
                                  _stream_ptr(stream)))
         return out
 
+    def forward_graph(self, x, weights, out, workspace, cache=None, taps=None, host_lens_max=-1):
+        """Records blk_forward for these exact buffers into a CUDA graph (ForwardGraph)."""
+        B, T, _ = x.shape
+        wst = weights if isinstance(weights, blk_weights) else make_weights_struct(weights)
+        kvc = None
+        if cache is not None:
+            kvc = blk_kv_cache(_ptr(cache["k"]), _ptr(cache["v"]), cache["k"].shape[2], _ptr(cache["lens"]))
+        tp = blk_taps(*[_ptr(taps.get(n)) for n in TAP_NAMES]) if taps else None
+        g = c_void_p()
+        _check(lib().blk_forward_graph_create(self.handle, _ptr(x), B, T, ctypes.byref(wst),
+                                              ctypes.byref(kvc) if kvc is not None else None, int(host_lens_max),
+                                              _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                              ctypes.byref(tp) if tp is not None else None, ctypes.byref(g)))
+        return ForwardGraph(g, keep=(x, weights, out, workspace, cache, taps, wst, kvc, tp))
+
     def qkv_rope(self, y, weights, batch, seq, q, k, v, pos0=None, stream=None):
         need = self.stage_workspace_bytes(batch * seq)
         ws = self._workspace(need, y.device)
@@ -239,6 +259,28 @@ class DecoderBlock:
         if n < 0:
             raise BlkError(5, "profiling is off or a CUDA error occurred")
         return {lib().blk_profile_stage_name(self.handle, i).decode(): (ms[i], ln[i]) for i in range(n)}
+
+
+class ForwardGraph:
+    """A recorded blk_forward (blk_graph); launch() replays it on a stream."""
+
+    def __init__(self, handle, keep):
+        self.handle = handle
+        self._keep = keep  # the buffers the graph reads and writes stay alive with it
+
+    def launch(self, stream=None):
+        _check(lib().blk_graph_launch(self.handle, _stream_ptr(stream)))
+
+    def close(self):
+        if self.handle:
+            lib().blk_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def rmsnorm(x, g, eps=1e-5, out=None, stream=None):

@@ -265,7 +265,8 @@ blk_status bf16_stream_gemm(const blk_handle* h, const TcSeg* segs, int nseg, co
 void prof_mark(blk_handle* h, const char* name, int launches, cudaStream_t s) {
   StageProfile& p = h->prof;
   if (!p.on || p.n >= StageProfile::kMax) return;
-  cudaEventRecord(p.ev[p.n], s);
+  // External: under stream capture this becomes an event-record node of the graph
+  cudaEventRecordWithFlags(p.ev[p.n], s, cudaEventRecordExternal);
   p.names[p.n] = name;
   p.launches[p.n] = launches;
   ++p.n;
@@ -278,7 +279,7 @@ void prof_begin(blk_handle* h) {
 void prof_end(blk_handle* h, cudaStream_t s) {
   StageProfile& p = h->prof;
   if (!p.on || p.n == 0) return;
-  cudaEventRecord(p.ev[p.n], s);
+  cudaEventRecordWithFlags(p.ev[p.n], s, cudaEventRecordExternal);
   p.pending = true;
 }
 
@@ -612,6 +613,58 @@ blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const b
   if (d.dtype == BLK_F32) return forward_f32(h, x, batch, seq, w, cache, out, ws, taps, s);
   if (decode) return forward_decode_bf16(h, x, batch, w, cache, max_len, out, ws, taps, s);
   return forward_prefill_bf16(h, x, batch, seq, w, out, ws, taps, s);
+}
+
+struct blk_graph {
+  blk_handle* h;
+  cudaGraphExec_t exec;
+  bool profiled;
+};
+
+blk_status blk_forward_graph_create(blk_handle* h, const void* x, int batch, int seq, const blk_weights* w,
+                                    blk_kv_cache* cache, int host_lens_max, void* out, void* workspace,
+                                    size_t workspace_bytes, const blk_taps* taps, blk_graph** out_graph) {
+  if (!h || !out_graph) return fail(BLK_ERR_INVALID_ARG, "NULL handle or out_graph");
+  *out_graph = nullptr;
+  cudaStream_t cs = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(e, "graph: stream");
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return cuda_fail(e, "graph: begin capture");
+  }
+  blk_status st = blk_forward(h, x, batch, seq, w, cache, host_lens_max, out, workspace, workspace_bytes, taps, cs);
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamEndCapture(cs, &graph);
+  h->prof.pending = false;  // nothing ran: the events fire on replays
+  cudaStreamDestroy(cs);
+  if (st != BLK_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return st;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "graph: end capture");
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return cuda_fail(e, "graph: instantiate");
+  *out_graph = new blk_graph{h, exec, h->prof.on};
+  return BLK_OK;
+}
+
+blk_status blk_graph_launch(blk_graph* g, void* stream) {
+  if (!g) return fail(BLK_ERR_INVALID_ARG, "NULL graph");
+  cudaError_t e = cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "graph launch");
+  if (g->profiled && g->h->prof.on) g->h->prof.pending = true;
+  return BLK_OK;
+}
+
+blk_status blk_graph_destroy(blk_graph* g) {
+  if (!g) return BLK_OK;
+  cudaGraphExecDestroy(g->exec);
+  delete g;
+  return BLK_OK;
 }
 
 blk_status blk_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y, blk_dtype dtype,

@@ -220,3 +220,48 @@ def test_decode_matches_prefill_last_row():
     torch.cuda.synchronize()
     assert rel_err(dec[:, 0], np64(full[:, T - 1])) <= TOL["bf16"]
     assert rel_err(kc[:, :, T - 1], np64(tb["attention_keys"][:, :, T - 1])) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------------ recorded forward (CUDA graph)
+
+def test_forward_graph_replay_matches_direct_call():
+    wl = SMALL_BF16[1]
+    w = to_dev(make_weights(wl))
+    x = make_input(wl).to(DEV)
+    blk = DecoderBlock.from_workload(wl)
+    direct = blk.forward(x, w)
+    out = torch.empty_like(x)
+    ws = torch.empty(blk.workspace_bytes(wl.batch, wl.seq), dtype=torch.uint8, device=DEV)
+    g = blk.forward_graph(x, w, out, ws)
+    g.launch()
+    torch.cuda.synchronize()
+    assert torch.equal(out, direct)
+    x.mul_(0.5)  # inputs are refreshed in place between replays
+    g.launch()
+    direct2 = blk.forward(x, w)
+    torch.cuda.synchronize()
+    assert torch.equal(out, direct2)
+    g.close()
+
+
+def test_forward_graph_decode_bumps_lens_each_replay():
+    wl = Workload("graph_decode", "bf16", 4, 1, 512, 8, 2, 128, 1000, "silu", seed=24)
+    lens = [5, 9, 60, 33]
+    w, x, kc, vc = _decode_case(wl, lens)
+    blk = DecoderBlock.from_workload(wl, max_seq=kc.shape[2] + 4)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    cache = {"k": kd, "v": vd, "lens": lens_d}
+    xd = x[:, None].to(DEV).contiguous()
+    out = torch.empty_like(xd)
+    ws = torch.empty(blk.workspace_bytes(wl.batch, 1, True), dtype=torch.uint8, device=DEV)
+    g = blk.forward_graph(xd, to_dev(w), out, ws, cache=cache, host_lens_max=max(lens) + 1)
+    g.launch()
+    g.launch()
+    torch.cuda.synchronize()
+    assert lens_d.tolist() == [L + 2 for L in lens]
+    ref = oracle.decode_step(cfg_of(wl), weights_np(w), np64(x), np64(kd.cpu()), np64(vd.cpu()),
+                             np.array([L + 1 for L in lens]))
+    # the second replay decoded the same token at position lens + 1
+    assert rel_err(out[:, 0], ref["layer_output"]) <= TOL["bf16"]
+    g.close()
