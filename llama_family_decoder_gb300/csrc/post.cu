@@ -17,11 +17,13 @@ namespace {
 
 __device__ __forceinline__ float split_sum(const float* C, int splits, size_t split_stride, size_t idx) {
   float v = 0.f;
+#pragma unroll 4
   for (int s = 0; s < splits; ++s) v += C[s * split_stride + idx];
   return v;
 }
 
 constexpr int kMaxPairsPerLane = 4;  // head_dim <= 256
+constexpr int kQkvWarps = 4;
 
 template <typename T>
 __global__ void post_qkv_kernel(const float* __restrict__ C, int splits, int rows, int ldc, int seq,
@@ -32,14 +34,16 @@ __global__ void post_qkv_kernel(const float* __restrict__ C, int splits, int row
                                 T* __restrict__ v, int kv_stride) {
   const int r = blockIdx.x;
   if (r >= rows) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = r / seq, t = r - b * seq;
   const int pos = decode_lens ? decode_lens[b] : (pos0 ? pos0[b] : 0) + t;
   const int slot = decode_lens ? pos : t;
   const int rpos = min(max(pos, 0), rope_max_pos - 1);  // the host checks positions; never read past the table
   const size_t sstride = (size_t)rows * ldc;
   const int half = d / 2;
-  for (int hid = warp; hid < H + 2 * Hkv; hid += nwarps) {
+  {
+    const int hid = blockIdx.y * kQkvWarps + warp;  // one warp per (row, head)
+    if (hid >= H + 2 * Hkv) return;
     const int seg = hid < H ? 0 : (hid < H + Hkv ? 1 : 2);
     const int head = seg == 0 ? hid : (seg == 1 ? hid - H : hid - H - Hkv);
     const size_t base = (size_t)r * ldc + (size_t)hid * d;
@@ -55,7 +59,7 @@ __global__ void post_qkv_kernel(const float* __restrict__ C, int splits, int row
         ss += x1[j] * x1[j] + x2[j] * x2[j];
       }
     }
-    if (seg != 0 && (slot < 0 || slot >= kv_stride)) continue;  // a full cache: never write past it
+    if (seg != 0 && (slot < 0 || slot >= kv_stride)) return;  // a full cache: never write past it
     T* dst;
     if (seg == 0)
       dst = q + (((size_t)b * H + head) * seq + t) * d;
@@ -70,7 +74,7 @@ __global__ void post_qkv_kernel(const float* __restrict__ C, int splits, int row
           dst[half + i] = from_f32<T>(x2[j]);
         }
       }
-      continue;
+      return;
     }
     float rr = 1.f;
     const T* gain = seg == 0 ? q_gain : k_gain;
@@ -92,40 +96,129 @@ __global__ void post_qkv_kernel(const float* __restrict__ C, int splits, int row
   }
 }
 
+template <typename T>
+__device__ __forceinline__ float4 ld4(const T* p);
+template <>
+__device__ __forceinline__ float4 ld4<float>(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+template <>
+__device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y);
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <typename T>
+__device__ __forceinline__ void st4(T* p, float4 v);
+template <>
+__device__ __forceinline__ void st4<float>(float* p, float4 v) {
+  *reinterpret_cast<float4*>(p) = v;
+}
+template <>
+__device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+  *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+
+template <typename T>
+__device__ __forceinline__ float4 round4(float4 v) {
+  return make_float4(round_to<T>(v.x), round_to<T>(v.y), round_to<T>(v.z), round_to<T>(v.w));
+}
+
+__device__ __forceinline__ float4 split_sum4(const float* C, int splits, size_t split_stride, size_t idx) {
+  float4 acc = *reinterpret_cast<const float4*>(C + idx);
+#pragma unroll 4
+  for (int s = 1; s < splits; ++s) {
+    const float4 t = *reinterpret_cast<const float4*>(C + s * split_stride + idx);
+    acc.x += t.x;
+    acc.y += t.y;
+    acc.z += t.z;
+    acc.w += t.w;
+  }
+  return acc;
+}
+
+constexpr int kResidThreads = 256;
+
+// One CTA per row; each thread owns VPT groups of 4 columns, issues all their
+// loads up front and keeps the sums in registers for the fused RMSNorm.
 // TR: residual type, TO: output type, TY: storage type (gain, y, out2, tap).
-template <typename TR, typename TO, typename TY>
-__global__ void post_resid_kernel(const float* __restrict__ C, int splits, int rows, int n, int ldc,
-                                  const TR* __restrict__ resid, TO* __restrict__ out, TY* __restrict__ out2,
-                                  TY* __restrict__ tap, const TY* __restrict__ g, float eps, TY* __restrict__ y,
-                                  int* __restrict__ bump_lens) {
-  __shared__ float red[32];
+template <typename TR, typename TO, typename TY, int VPT>
+__global__ void __launch_bounds__(kResidThreads) post_resid_kernel(
+    const float* __restrict__ C, int splits, int rows, int n, int ldc, const TR* __restrict__ resid,
+    TO* __restrict__ out, TY* __restrict__ out2, TY* __restrict__ tap, const TY* __restrict__ g, float eps,
+    TY* __restrict__ y, int* __restrict__ bump_lens) {
+  __shared__ float red[kResidThreads / 32];
   const int r = blockIdx.x;
   if (r >= rows) return;
   const size_t sstride = (size_t)rows * ldc;
+  const int nv = n / 4;
+  float4 o[VPT];
   float ss = 0.f;
-  for (int c = threadIdx.x; c < n; c += blockDim.x) {
-    const float contrib = split_sum(C, splits, sstride, (size_t)r * ldc + c);
-    const float o = to_f32<TR>(resid[(size_t)r * n + c]) + contrib;  // the residual stream, summed in fp32
-    const TO os = from_f32<TO>(o);
-    out[(size_t)r * n + c] = os;
-    if (out2) out2[(size_t)r * n + c] = from_f32<TY>(o);
-    if (tap) tap[(size_t)r * n + c] = from_f32<TY>(contrib);
-    const float of = to_f32<TO>(os);
-    ss += of * of;
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = threadIdx.x + j * kResidThreads;
+    if (v < nv) {
+      const float4 contrib = split_sum4(C, splits, sstride, (size_t)r * ldc + 4 * v);
+      const float4 rr = ld4<TR>(resid + (size_t)r * n + 4 * v);
+      // the residual stream, summed in fp32
+      const float4 oo = make_float4(rr.x + contrib.x, rr.y + contrib.y, rr.z + contrib.z, rr.w + contrib.w);
+      st4<TO>(out + (size_t)r * n + 4 * v, oo);
+      if (out2) st4<TY>(out2 + (size_t)r * n + 4 * v, oo);
+      if (tap) st4<TY>(tap + (size_t)r * n + 4 * v, contrib);
+      o[j] = round4<TO>(oo);
+      ss += o[j].x * o[j].x + o[j].y * o[j].y + o[j].z * o[j].z + o[j].w * o[j].w;
+    }
   }
-  if (g == nullptr) {
-    if (bump_lens && threadIdx.x == 0) bump_lens[r] += 1;
-    return;
+  if (g != nullptr) {
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kResidThreads / 32; ++w) tot += red[w];
+    const float inv = rsqrtf(tot / (float)n + eps);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int v = threadIdx.x + j * kResidThreads;
+      if (v < nv) {
+        const float4 gg = ld4<TY>(g + 4 * v);
+        st4<TY>(y + (size_t)r * n + 4 * v,
+                make_float4(o[j].x * inv * gg.x, o[j].y * inv * gg.y, o[j].z * inv * gg.z, o[j].w * inv * gg.w));
+      }
+    }
   }
-  ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  float tot = 0.f;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
-  const float inv = rsqrtf(tot / (float)n + eps);
-  for (int c = threadIdx.x; c < n; c += blockDim.x)
-    y[(size_t)r * n + c] = from_f32<TY>(to_f32<TO>(out[(size_t)r * n + c]) * inv * to_f32<TY>(g[c]));
   if (bump_lens && threadIdx.x == 0) bump_lens[r] += 1;
+}
+
+__device__ __forceinline__ float act_one(int act, float gt, float u, float alpha_p, float alpha_n, float beta,
+                                         float xeps) {
+  if (act == 0) return gt / (1.0f + expf(-gt)) * u;  // SwiGLU: silu(gate) * up
+  if (act == 1) {
+    const float rl = fmaxf(u, 0.f);
+    return rl * rl;
+  }
+  return u > 0.f ? alpha_p * u * u + beta * u : alpha_n * (expm1f(fminf(u, xeps)) - u) + beta * u;
+}
+
+// Four consecutive neurons per thread (F % 4 == 0).
+template <typename T>
+__global__ void post_act4_kernel(const float* __restrict__ C, int splits, int rows, int F, int ldc, int act,
+                                 float alpha_p, float alpha_n, float beta, float xeps, T* __restrict__ out) {
+  const int F4 = F / 4;
+  const int total = rows * F4;
+  const size_t sstride = (size_t)rows * ldc;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int r = i / F4, f = (i - r * F4) * 4;
+    const size_t base = (size_t)r * ldc;
+    const float4 u = act == 0 ? split_sum4(C, splits, sstride, base + F + f) : split_sum4(C, splits, sstride, base + f);
+    const float4 gt = act == 0 ? split_sum4(C, splits, sstride, base + f) : u;
+    const float4 n = make_float4(act_one(act, gt.x, u.x, alpha_p, alpha_n, beta, xeps),
+                                 act_one(act, gt.y, u.y, alpha_p, alpha_n, beta, xeps),
+                                 act_one(act, gt.z, u.z, alpha_p, alpha_n, beta, xeps),
+                                 act_one(act, gt.w, u.w, alpha_p, alpha_n, beta, xeps));
+    st4<T>(out + (size_t)r * F + f, n);
+  }
 }
 
 template <typename T>
@@ -136,21 +229,9 @@ __global__ void post_act_kernel(const float* __restrict__ C, int splits, int row
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
     const int r = (int)(idx / F), f = (int)(idx - (size_t)r * F);
     const size_t base = (size_t)r * ldc;
-    float n;
-    if (act == 0) {  // SwiGLU: silu(gate) * up
-      const float gt = split_sum(C, splits, sstride, base + f);
-      const float up = split_sum(C, splits, sstride, base + F + f);
-      n = gt / (1.0f + expf(-gt)) * up;
-    } else {
-      const float u = split_sum(C, splits, sstride, base + f);
-      if (act == 1) {
-        const float rl = fmaxf(u, 0.f);
-        n = rl * rl;
-      } else {
-        n = u > 0.f ? alpha_p * u * u + beta * u : alpha_n * (expm1f(fminf(u, xeps)) - u) + beta * u;
-      }
-    }
-    out[idx] = from_f32<T>(n);
+    const float u = split_sum(C, splits, sstride, base + (act == 0 ? F + f : f));
+    const float gt = act == 0 ? split_sum(C, splits, sstride, base + f) : u;
+    out[idx] = from_f32<T>(act_one(act, gt, u, alpha_p, alpha_n, beta, xeps));
   }
 }
 
@@ -164,12 +245,12 @@ cudaError_t launch_post_qkv(const float* C, int splits, int rows, int ldc, int s
   if (d > 2 * 32 * kMaxPairsPerLane || d % 2) return cudaErrorInvalidValue;
   if (bf16) {
     using T = __nv_bfloat16;
-    post_qkv_kernel<T><<<rows, 256, 0, s>>>(C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
+    post_qkv_kernel<T><<<dim3(rows, (H + 2 * Hkv + kQkvWarps - 1) / kQkvWarps), 32 * kQkvWarps, 0, s>>>(C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
                                            static_cast<const T*>(q_gain), static_cast<const T*>(k_gain), eps, rope, rope_max_pos,
                                            static_cast<T*>(q), static_cast<T*>(k), static_cast<T*>(v), kv_stride);
   } else {
     using T = float;
-    post_qkv_kernel<T><<<rows, 256, 0, s>>>(C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
+    post_qkv_kernel<T><<<dim3(rows, (H + 2 * Hkv + kQkvWarps - 1) / kQkvWarps), 32 * kQkvWarps, 0, s>>>(C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
                                            static_cast<const T*>(q_gain), static_cast<const T*>(k_gain), eps, rope, rope_max_pos,
                                            static_cast<T*>(q), static_cast<T*>(k), static_cast<T*>(v), kv_stride);
   }
@@ -180,12 +261,29 @@ cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int l
                               void* out, bool out_f32, void* out2, void* tap, const void* g, float eps, void* y,
                               int* bump_lens, bool bf16, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
+  if (n % 4 || ldc % 4) return cudaErrorInvalidValue;
+  const int nv = n / 4;
+  const int vpt = (nv + kResidThreads - 1) / kResidThreads;
   using B = __nv_bfloat16;
-#define BLK_POST_RESID(TR, TO, TY)                                                                              \
-  post_resid_kernel<TR, TO, TY><<<rows, 256, 0, s>>>(C, splits, rows, n, ldc, static_cast<const TR*>(resid),   \
-                                                     static_cast<TO*>(out), static_cast<TY*>(out2),             \
-                                                     static_cast<TY*>(tap), static_cast<const TY*>(g), eps,     \
-                                                     static_cast<TY*>(y), bump_lens)
+#define BLK_POST_RESID_V(TR, TO, TY, V)                                                                        \
+  post_resid_kernel<TR, TO, TY, V><<<rows, kResidThreads, 0, s>>>(                                           \
+      C, splits, rows, n, ldc, static_cast<const TR*>(resid), static_cast<TO*>(out), static_cast<TY*>(out2),  \
+      static_cast<TY*>(tap), static_cast<const TY*>(g), eps, static_cast<TY*>(y), bump_lens)
+#define BLK_POST_RESID(TR, TO, TY)                  \
+  do {                                              \
+    if (vpt <= 1)                                   \
+      BLK_POST_RESID_V(TR, TO, TY, 1);              \
+    else if (vpt <= 2)                              \
+      BLK_POST_RESID_V(TR, TO, TY, 2);              \
+    else if (vpt <= 4)                              \
+      BLK_POST_RESID_V(TR, TO, TY, 4);              \
+    else if (vpt <= 8)                              \
+      BLK_POST_RESID_V(TR, TO, TY, 8);              \
+    else if (vpt <= 16)                             \
+      BLK_POST_RESID_V(TR, TO, TY, 16);             \
+    else                                            \
+      return cudaErrorInvalidValue;                 \
+  } while (0)
   if (!bf16) {
     BLK_POST_RESID(float, float, float);
   } else if (resid_f32 && out_f32) {
@@ -198,21 +296,32 @@ cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int l
     BLK_POST_RESID(B, B, B);
   }
 #undef BLK_POST_RESID
+#undef BLK_POST_RESID_V
   return cudaGetLastError();
 }
 
 cudaError_t launch_post_act(const float* C, int splits, int rows, int F, int ldc, int act, float alpha_p,
                             float alpha_n, float beta, float xeps, void* out, bool bf16, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  const size_t total = (size_t)rows * F;
+  const bool vec = F % 4 == 0 && ldc % 4 == 0;
+  const size_t total = (size_t)rows * F / (vec ? 4 : 1);
   int grid = (int)((total + 255) / 256);
-  if (grid > 4096) grid = 4096;
-  if (bf16)
-    post_act_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
-                                                        static_cast<__nv_bfloat16*>(out));
-  else
-    post_act_kernel<float><<<grid, 256, 0, s>>>(C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
-                                                static_cast<float*>(out));
+  if (grid > 8192) grid = 8192;
+  if (vec) {
+    if (bf16)
+      post_act4_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta,
+                                                           xeps, static_cast<__nv_bfloat16*>(out));
+    else
+      post_act4_kernel<float><<<grid, 256, 0, s>>>(C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
+                                                   static_cast<float*>(out));
+  } else {
+    if (bf16)
+      post_act_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
+                                                          static_cast<__nv_bfloat16*>(out));
+    else
+      post_act_kernel<float><<<grid, 256, 0, s>>>(C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
+                                                  static_cast<float*>(out));
+  }
   return cudaGetLastError();
 }
 
