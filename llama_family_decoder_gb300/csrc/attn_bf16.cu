@@ -1,15 +1,12 @@
-// bf16 causal grouped-query attention ("LlamaForCausalLM-32L-4096d" sheet:
-// softmax(q @ k.T / sqrt(128), mask=causal) @ v, per head; "arcee", "Grouped-
-// query attention, 128-wide heads": query head h reads KV head h / (H / Hkv)).
+// bf16 decode attention over a KV cache ("LlamaForCausalLM-32L-4096d" sheet:
+// softmax(q @ k.T / sqrt(128)) @ v, per head; "arcee", "Grouped-query
+// attention, 128-wide heads": query head h reads KV head h / (H / Hkv)).
+// HBM-bound: K/V tiles of 64 keys stream through a double-buffered,
+// XOR-swizzled shared-memory ring (cp.async, zero-filled past the valid keys);
+// the small products run on bf16 mma.sync with fp32 accumulation and an
+// online softmax (running max and sum in the log2 domain).
 //
-// Prefill: flash-style, one CTA per (64-query tile, head, sequence), 4 warps
-// of 16 query rows. K/V tiles of 64 keys stream through a double-buffered,
-// XOR-swizzled shared-memory ring (cp.async, zero-filled past the sequence
-// end); S = Q K^T and O += P V run on bf16 mma.sync with fp32 accumulation;
-// the softmax is online (running max and sum in the log2 domain), P stays in
-// registers. Heaviest (last) query tiles are scheduled first.
-//
-// Decode: one query per sequence; a CTA takes one (sequence, KV head, key
+// One query per sequence; a CTA takes one (sequence, KV head, key
 // split), puts the G = H/Hkv query heads of the group on the MMA's rows, and
 // its four warps each own 16 keys of every 64-key tile (their partial softmax
 // states merge at the end). Splits are merged by a second small kernel.
@@ -74,167 +71,6 @@ __device__ __forceinline__ void load_tile(uint32_t s_base, const __nv_bfloat16* 
       const __nv_bfloat16* src = g + (size_t)(ok ? r : 0) * kD + ch * 8;
       cp_async16(s_base + swz(r, ch), src, ok);
     }
-  }
-}
-
-// ------------------------------------------------------------------ prefill
-
-constexpr int kPM = 64;  // queries per CTA
-constexpr int kPWarps = 4;
-constexpr int kPThreads = kPWarps * 32;
-constexpr int kPSmem = kPM * kRowBytes + 4 * kTileKeys * kRowBytes;  // Q + 2x(K,V)
-
-__global__ void __launch_bounds__(kPThreads) attn_prefill_kernel(const __nv_bfloat16* __restrict__ q,
-                                                                 const __nv_bfloat16* __restrict__ k,
-                                                                 const __nv_bfloat16* __restrict__ v,
-                                                                 __nv_bfloat16* __restrict__ o, int B, int H, int Hkv,
-                                                                 int T, int kv_stride, int n_mtiles) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK0 = sQ + kPM * kRowBytes;
-  // buffers: K0, V0, K1, V1
-  const int id = blockIdx.x;
-  const int hb = id % (H * B);
-  const int m_tile = n_mtiles - 1 - id / (H * B);
-  const int h = hb % H, b = hb / H;
-  const int kvh = h / (H / Hkv);
-  const int m0 = m_tile * kPM;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tq = lane & 3;
-
-  const __nv_bfloat16* qg = q + (((size_t)b * H + h) * T + m0) * kD;
-  const __nv_bfloat16* kg = k + ((size_t)b * Hkv + kvh) * kv_stride * kD;
-  const __nv_bfloat16* vg = v + ((size_t)b * Hkv + kvh) * kv_stride * kD;
-  const int kv_end = min(T, m0 + kPM);  // causal: no key beyond the last query of the tile
-  const int n_tiles = (kv_end + kTileKeys - 1) / kTileKeys;
-
-  auto kbuf = [&](int i) { return sK0 + (uint32_t)((i & 1) * 2 * kTileKeys * kRowBytes); };
-  auto vbuf = [&](int i) { return kbuf(i) + (uint32_t)(kTileKeys * kRowBytes); };
-
-  load_tile<kPM, kPThreads>(sQ, qg, T - m0);
-  load_tile<kTileKeys, kPThreads>(kbuf(0), kg, T);
-  load_tile<kTileKeys, kPThreads>(vbuf(0), vg, T);
-  cp_async_commit();
-
-  uint32_t qf[8][4];
-  float acc[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-  const float sl2 = kLog2e * rsqrtf((float)kD);
-  const int q_row0 = m0 + warp * 16 + g;  // and q_row0 + 8
-
-  for (int it = 0; it < n_tiles; ++it) {
-    if (it + 1 < n_tiles) {
-      const int n1 = (it + 1) * kTileKeys;
-      load_tile<kTileKeys, kPThreads>(kbuf(it + 1), kg + (size_t)n1 * kD, T - n1);
-      load_tile<kTileKeys, kPThreads>(vbuf(it + 1), vg + (size_t)n1 * kD, T - n1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    if (it == 0) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int row = warp * 16 + rr + 8 * (mi & 1);
-        ldsm_x4(sQ + swz(row, kk * 2 + (mi >> 1)), qf[kk]);
-      }
-    }
-    const int n0 = it * kTileKeys;
-    const uint32_t sK = kbuf(it), sV = vbuf(it);
-    float s[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-    for (int jp = 0; jp < 4; ++jp) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int mi = lane >> 3, rr = lane & 7;
-        uint32_t bb[4];
-        ldsm_x4(sK + swz(jp * 16 + rr + 8 * (mi >> 1), kk * 2 + (mi & 1)), bb);
-        mma_bf16(s[2 * jp], qf[kk], bb[0], bb[1]);
-        mma_bf16(s[2 * jp + 1], qf[kk], bb[2], bb[3]);
-      }
-    }
-    // scale to log2 domain, mask, online softmax
-    const bool need_mask = (n0 + kTileKeys - 1 > m0 + warp * 16) || (n0 + kTileKeys > T);
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float x = s[j][e] * sl2;
-        if (need_mask) {
-          const int key = n0 + j * 8 + 2 * tq + (e & 1);
-          const int qr = q_row0 + ((e >> 1) << 3);
-          if (key > qr || key >= T) x = -INFINITY;
-        }
-        s[j][e] = x;
-        mx[e >> 1] = fmaxf(mx[e >> 1], x);
-      }
-    }
-    float alpha[2], mu[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      const float mnew = fmaxf(mrow[r], mx[r]);
-      mu[r] = mnew == -INFINITY ? 0.f : mnew;
-      alpha[r] = exp2f(mrow[r] - mu[r]);
-      mrow[r] = mnew;
-      lrow[r] *= alpha[r];
-    }
-    uint32_t pa[4][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float p0 = exp2f(s[j][0] - mu[0]), p1 = exp2f(s[j][1] - mu[0]);
-      const float p2 = exp2f(s[j][2] - mu[1]), p3 = exp2f(s[j][3] - mu[1]);
-      lrow[0] += p0 + p1;
-      lrow[1] += p2 + p3;
-      pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-      pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p2, p3);
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      acc[i][0] *= alpha[0];
-      acc[i][1] *= alpha[0];
-      acc[i][2] *= alpha[1];
-      acc[i][3] *= alpha[1];
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      // A fragment of P for keys kk*16 .. kk*16+15: {row g k lo, row g+8 k lo, row g k hi, row g+8 k hi}
-      const uint32_t a[4] = {pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3]};
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        const int mi = lane >> 3, rr = lane & 7;
-        uint32_t bb[4];
-        ldsm_x4_t(sV + swz(kk * 16 + rr + 8 * (mi & 1), dp * 2 + (mi >> 1)), bb);
-        mma_bf16(acc[2 * dp], a, bb[0], bb[1]);
-        mma_bf16(acc[2 * dp + 1], a, bb[2], bb[3]);
-      }
-    }
-    __syncthreads();
-  }
-  // finalize: the row sums live spread over the quad
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-    lrow[r] = 1.0f / lrow[r];
-  }
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int t = q_row0 + 8 * r;
-    if (t >= T) continue;
-    __nv_bfloat16* orow = o + (((size_t)b * T + t) * H + h) * kD + 2 * tq;
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt)
-      *reinterpret_cast<uint32_t*>(orow + dt * 8) =
-          pack_bf16x2(acc[dt][2 * r] * lrow[r], acc[dt][2 * r + 1] * lrow[r]);
   }
 }
 
@@ -425,26 +261,6 @@ __global__ void attn_decode_combine_kernel(const float* __restrict__ ws_ml, cons
 }
 
 }  // namespace
-
-cudaError_t launch_attn_prefill_bf16(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv,
-                                     int T, int d, int kv_stride, cudaStream_t s, const char** why) {
-  if (d != kD) {
-    *why = "bf16 attention: head_dim must be 128";
-    return cudaErrorInvalidValue;
-  }
-  if (B <= 0 || T <= 0) return cudaSuccess;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  const int n_m = (T + kPM - 1) / kPM;
-  attn_prefill_kernel<<<n_m * H * B, kPThreads, kPSmem, s>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(o), B, H, Hkv, T, kv_stride, n_m);
-  return cudaGetLastError();
-}
 
 int attn_decode_splits(int B, int Hkv, int max_len, int num_sms) {
   const int units = B * Hkv;

@@ -1,0 +1,368 @@
+// Prefill attention on the 5th-generation tensor core (tcgen05 + TMEM), bf16,
+// causal, grouped-query, head_dim 128 ("LlamaForCausalLM-32L-4096d" sheet:
+// softmax(q @ k.T / sqrt(128), mask=causal) @ v per head; "arcee", "Grouped-
+// query attention, 128-wide heads": query head h reads KV head h / (H / Hkv)).
+//
+// One CTA per (128-query tile, head, sequence), heaviest tiles first, 192 threads:
+//   warp 0      TMA producer: the Q tile once, then K and V tiles of 128 keys
+//               through a 2-stage ring (128-byte swizzle, two 64-column boxes).
+//   warp 1      TMEM allocation; lane 0 issues S_j = Q K_j^T (M=128, N=128,
+//               K=16 x 8) into one of two TMEM score buffers, and O += P_j V_j
+//               (A = P from shared memory, B = V as an MN-major operand) into
+//               the TMEM output accumulator.
+//   warps 2..5  softmax, one query row per thread: read S_j from TMEM, mask,
+//               exponentiate in the log2 domain against a running reference
+//               max, write P_j (bf16, swizzled K-major) to shared memory;
+//               rescale O in TMEM only when the row max grew by more than 2^8
+//               (exact: softmax does not depend on the reference); finally
+//               O / l to the head-major output.
+// S_{j+1} runs on the tensor core while the softmax works on S_j.
+// Every wait is bounded; on expiry the CTA records a timeout, drains its own
+// copies and MMAs, frees its TMEM and returns.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace blk {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBQ = 128;  // queries per CTA (MMA M)
+constexpr int kBKeys = 128;  // keys per tile
+constexpr int kThreads = 192;
+constexpr int kSub = 128 * 128;          // one 64-column sub-tile of a 128-row tile (bytes)
+constexpr int kTile = 2 * kSub;          // 128 rows x 128 bf16
+constexpr int kStages = 2;
+constexpr int kSmem = 1024 + kTile * (2 + 2 * kStages) + 256;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr unsigned long long kDrainNs = 2000000000ULL;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct AttnParams {
+  CUtensorMap tq, tk, tv;
+  __nv_bfloat16* o;
+  int B, H, Hkv, T, n_qtiles;
+  float sl2;
+  DevStatus* status;
+  unsigned long long wait_ns;
+};
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
+  if (f16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  return pack_bf16x2(lo, hi);
+}
+
+// F16: q, k, v (and so P) are fp16; otherwise bf16. The output is bf16 either way.
+template <bool F16>
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + kTile;
+  uint8_t* sV = sK + kStages * kTile;
+  uint8_t* sP = sV + kStages * kTile;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTile);
+  // q_full, kv_full[2], kv_empty[2], s_full[2], p_ready, pv_done, drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 10);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  const uint32_t q_full = smem_u32(&bars[0]);
+  auto kv_full = [&](int s) { return smem_u32(&bars[1 + s]); };
+  auto kv_empty = [&](int s) { return smem_u32(&bars[3 + s]); };
+  auto s_full = [&](int s) { return smem_u32(&bars[5 + s]); };
+  const uint32_t p_ready = smem_u32(&bars[7]);
+  const uint32_t pv_done = smem_u32(&bars[8]);
+  const uint32_t drain = smem_u32(&bars[9]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int id = blockIdx.x;
+  const int hb = id % (p.H * p.B);
+  const int qt = p.n_qtiles - 1 - id / (p.H * p.B);
+  const int h = hb % p.H, b = hb / p.H;
+  const int kvh = h / (p.H / p.Hkv);
+  const int m0 = qt * kBQ;
+  const int kv_end = min(p.T, m0 + kBQ);
+  const int n_tiles = (kv_end + kBKeys - 1) / kBKeys;
+  const int q_row = (b * p.H + h) * p.T + m0;
+  const int kv_row = (b * p.Hkv + kvh) * p.T;
+  const unsigned long long budget = p.wait_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+      mbar_init(s_full(s), 1);
+    }
+    mbar_init(p_ready, 128);
+    mbar_init(pv_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tq);
+    tma_prefetch_desc(&p.tk);
+    tma_prefetch_desc(&p.tv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;  // S0: cols [0,128), S1: [128,256), O: [256,384)
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      bool failed = false;
+      uint32_t issued = 0, parity = 0;
+      mbar_arrive_expect_tx(q_full, kTile);
+      tma_load_2d(smem_u32(sQ), &p.tq, 0, q_row, q_full);
+      tma_load_2d(smem_u32(sQ + kSub), &p.tq, 64, q_row, q_full);
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(kv_empty(s), ph ^ 1, budget, abort_flag)) {
+          failed = true;
+          break;
+        }
+        mbar_arrive_expect_tx(kv_full(s), 2 * kTile);
+        const int row = kv_row + j * kBKeys;
+        tma_load_2d(smem_u32(sK + s * kTile), &p.tk, 0, row, kv_full(s));
+        tma_load_2d(smem_u32(sK + s * kTile + kSub), &p.tk, 64, row, kv_full(s));
+        tma_load_2d(smem_u32(sV + s * kTile), &p.tv, 0, row, kv_full(s));
+        tma_load_2d(smem_u32(sV + s * kTile + kSub), &p.tv, 64, row, kv_full(s));
+        issued |= 1u << s;
+        parity = (parity & ~(1u << s)) | (ph << s);
+      }
+      if (failed) {
+        *abort_flag = 1;
+        report_timeout(p.status, 0x20 + 0);
+        volatile int never = 0;
+        mbar_wait(q_full, 0, kDrainNs, &never);
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) mbar_wait(kv_full(s), (parity >> s) & 1, kDrainNs, &never);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      // kind::f16 operand formats: bf16 (1) or fp16 (0) for both A and B
+      constexpr uint32_t fmt_clear = F16 ? ~((7u << 7) | (7u << 10)) : ~0u;
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBKeys) & fmt_clear;
+      constexpr uint32_t idesc_pv = (idesc_bf16_f32(kBQ, kD) & fmt_clear) | (1u << 16);  // B (V) is MN-major
+      bool failed = !mbar_wait(q_full, 0, budget, abort_flag);
+      bool issued_any = false;
+      for (int j = 0; j <= n_tiles && !failed; ++j) {
+        if (j < n_tiles) {
+          const int s = j & 1;
+          if (!mbar_wait(kv_full(s), (j >> 1) & 1, budget, abort_flag)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t a = smem_desc_sw128(smem_u32(sQ + (kk >> 2) * kSub)) + (uint64_t)((kk & 3) * 2);
+            const uint64_t bd = smem_desc_sw128(smem_u32(sK + s * kTile + (kk >> 2) * kSub)) + (uint64_t)((kk & 3) * 2);
+            tc_mma_bf16(tmem + s * kBKeys, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          issued_any = true;
+          tc_commit(s_full(s));
+        }
+        if (j >= 1) {
+          const int jj = j - 1, s = jj & 1;
+          if (!mbar_wait(p_ready, jj & 1, budget, abort_flag)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBKeys / 16; ++kk) {
+            const uint64_t a = smem_desc_sw128(smem_u32(sP + (kk >> 2) * kSub)) + (uint64_t)((kk & 3) * 2);
+            const uint64_t bd = smem_desc_sw128_mn(smem_u32(sV + s * kTile + kk * 16 * 128), kSub, 1024);
+            tc_mma_bf16(tmem + 2 * kBKeys, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(pv_done);
+          tc_commit(kv_empty(s));
+        }
+      }
+      if (failed) {
+        *abort_flag = 1;
+        report_timeout(p.status, 0x20 + 1);
+        if (issued_any) {
+          tc_commit(drain);
+          volatile int never = 0;
+          mbar_wait(drain, 0, kDrainNs, &never);
+        }
+      }
+    }
+  } else {
+    // ---------------- softmax / correction / epilogue: one query row per thread
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int qi = m0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t o_taddr = tmem + lane_off + 2 * kBKeys;
+    float m_ref = -INFINITY, l = 0.f;
+    bool failed = false;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j & 1;
+      // warp-uniform: every lane waits, the warp gives up together
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full(s), (j >> 1) & 1, budget, abort_flag))) {
+        failed = true;
+        break;
+      }
+      __syncwarp();
+      tc_fence_after();
+      float x[kBKeys];
+#pragma unroll
+      for (int c = 0; c < kBKeys; c += 16) tmem_ld16(tmem + lane_off + s * kBKeys + c, *reinterpret_cast<float(*)[16]>(&x[c]));
+      tc_wait_ld();
+      const int n0 = j * kBKeys;
+      const bool need_mask = (n0 + kBKeys - 1 > m0) || (n0 + kBKeys > p.T);
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kBKeys; ++c) {
+        float v = x[c] * p.sl2;
+        if (need_mask && (n0 + c > qi || n0 + c >= p.T)) v = -INFINITY;
+        x[c] = v;
+        mt = fmaxf(mt, v);
+      }
+      const bool need = mt > m_ref + kRescaleLog2;
+      const bool any = __any_sync(0xffffffffu, need);
+      float alpha = 1.f;
+      if (need) {
+        alpha = exp2f(m_ref - mt);
+        m_ref = mt;
+      }
+      l *= alpha;
+      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+      uint32_t pk[kBKeys / 2];
+#pragma unroll
+      for (int c = 0; c < kBKeys; c += 2) {
+        const float p0 = exp2f(x[c] - mu), p1 = exp2f(x[c + 1] - mu);
+        l += p0 + p1;
+        pk[c / 2] = pack2(p0, p1, F16);
+      }
+      if (j >= 1) {  // P buffer and O are free once PV_{j-1} is done
+        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, budget, abort_flag))) {
+          failed = true;
+          break;
+        }
+        __syncwarp();
+        tc_fence_after();
+        if (any) {
+#pragma unroll 1
+          for (int c = 0; c < kD; c += 16) {
+            float ov[16];
+            tmem_ld16(o_taddr + c, ov);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] *= alpha;
+            tmem_st16(o_taddr + c, ov);
+          }
+          tc_wait_st();
+        }
+      }
+      // P row r: two 64-key sub-tiles, 128-byte rows, 16-byte chunks XOR-swizzled by (r & 7)
+#pragma unroll
+      for (int ch = 0; ch < kBKeys / 8; ++ch) {
+        const int sub = ch >> 3, c8 = ch & 7;
+        uint4 val = make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+        *reinterpret_cast<uint4*>(sP + sub * kSub + r * 128 + ((c8 ^ (r & 7)) << 4)) = val;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+    }
+    if (!failed && n_tiles > 0) {
+      if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (n_tiles - 1) & 1, budget, abort_flag))) failed = true;
+    }
+    if (!failed) {
+      __syncwarp();
+      tc_fence_after();
+      const float inv = 1.f / l;
+      __nv_bfloat16* orow = p.o + (((size_t)b * p.T + qi) * p.H + h) * kD;
+#pragma unroll 1
+      for (int c = 0; c < kD; c += 16) {
+        float ov[16];
+        tmem_ld16(o_taddr + c, ov);
+        tc_wait_ld();
+        if (qi < p.T) {
+          uint4 w0, w1;
+          w0.x = pack_bf16x2(ov[0] * inv, ov[1] * inv);
+          w0.y = pack_bf16x2(ov[2] * inv, ov[3] * inv);
+          w0.z = pack_bf16x2(ov[4] * inv, ov[5] * inv);
+          w0.w = pack_bf16x2(ov[6] * inv, ov[7] * inv);
+          w1.x = pack_bf16x2(ov[8] * inv, ov[9] * inv);
+          w1.y = pack_bf16x2(ov[10] * inv, ov[11] * inv);
+          w1.z = pack_bf16x2(ov[12] * inv, ov[13] * inv);
+          w1.w = pack_bf16x2(ov[14] * inv, ov[15] * inv);
+          reinterpret_cast<uint4*>(orow + c)[0] = w0;
+          reinterpret_cast<uint4*>(orow + c)[1] = w1;
+        }
+      }
+    } else {
+      *abort_flag = 1;
+      if (lane == 0) report_timeout(p.status, 0x20 + 2);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int T,
+                                   int d, bool f16, DevStatus* st, unsigned long long wait_ns, cudaStream_t s,
+                                   const char** why) {
+  if (d != kD) {
+    *why = "tcgen05 attention: head_dim must be 128";
+    return cudaErrorInvalidValue;
+  }
+  if (B <= 0 || T <= 0) return cudaSuccess;
+  AttnParams p;
+  memset(static_cast<void*>(&p), 0, sizeof(p));
+  if (!make_tma_2d_16b(&p.tq, q, B * H * T, kD, kBQ, f16) || !make_tma_2d_16b(&p.tk, k, B * Hkv * T, kD, kBKeys, f16) ||
+      !make_tma_2d_16b(&p.tv, v, B * Hkv * T, kD, kBKeys, f16)) {
+    *why = "cuTensorMapEncodeTiled failed for q/k/v";
+    return cudaErrorInvalidValue;
+  }
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.T = T;
+  p.n_qtiles = (T + kBQ - 1) / kBQ;
+  p.sl2 = kLog2e / sqrtf((float)kD);
+  p.status = st;
+  p.wait_ns = wait_ns;
+  static bool configured[2] = {false, false};
+  if (!configured[f16]) {
+    cudaError_t e = f16 ? cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)
+                        : cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured[f16] = true;
+  }
+  if (f16)
+    attn_tc_kernel<true><<<p.n_qtiles * H * B, kThreads, kSmem, s>>>(p);
+  else
+    attn_tc_kernel<false><<<p.n_qtiles * H * B, kThreads, kSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace blk

@@ -89,10 +89,15 @@ int max_cols(const blk_desc& d) {
 }
 
 constexpr int kMaxDecodeSplits = 16;
+constexpr int kResidBN = 256;  // N-tile of the residual GEMMs (o_proj, down)
+
+// Partial sums of squares per row that the o_proj epilogue leaves for the MLP's norm.
+int norm_parts(const blk_desc& d) { return (d.hidden + kResidBN - 1) / kResidBN; }
 
 // Workspace regions of a forward call.
 struct Ws {
   void *y, *q, *k, *v, *o, *mid, *neur, *C, *attn;
+  float *rs1, *ss2;  // bf16 prefill: input-norm 1/rms per row; post-attention sum of squares per row
 };
 
 Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, size_t* total) {
@@ -119,6 +124,9 @@ Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, siz
     }
   } else if (d.dtype == BLK_F32) {
     w.C = c.take(M * max_cols(d) * sizeof(float));
+  } else {
+    w.rs1 = static_cast<float*>(c.take(M * sizeof(float)));
+    w.ss2 = static_cast<float*>(c.take(M * norm_parts(d) * sizeof(float)));
   }
   *total = c.off;
   return w;
@@ -172,7 +180,7 @@ blk_status tc(const blk_handle* h, const TcGemmDesc& g, cudaStream_t s, const ch
 }
 
 blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, int B, int T, const int* pos0, void* q,
-                    void* k, void* v, cudaStream_t s) {
+                    void* k, void* v, cudaStream_t s, const float* row_scale = nullptr, bool f16 = false) {
   const blk_desc& d = h->d;
   TcGemmDesc g;
   g.na = 1;
@@ -185,19 +193,22 @@ blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, in
   g.bn = ((d.n_heads * d.head_dim) % 256 == 0 && (d.n_kv_heads * d.head_dim) % 256 == 0) ? 256 : 128;
   g.epi = Epi::kQkv;
   g.e = qkv_epi(h, w, T, pos0, q, k, v);
+  g.e.row_scale = row_scale;
+  g.e.qkv_f16 = f16 ? 1 : 0;
   return tc(h, g, s, "QKV GEMM");
 }
 
 blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K, const void* W, int N,
                              const void* resid, bool resid_f32, void* out, bool out_f32, void* out2, void* tap,
-                             cudaStream_t s, const char* what) {
+                             cudaStream_t s, const char* what, void* norm_out = nullptr,
+                             const void* norm_gain = nullptr, float* norm_ss = nullptr) {
   TcGemmDesc g;
   g.na = 1;
   g.a[0] = {a, rows, 0};
   g.nb = 1;
   g.b[0] = {W, N, 0};
   g.K = K;
-  g.bn = 256;
+  g.bn = kResidBN;
   g.epi = Epi::kResid;
   g.e.out = out;
   g.e.ldo = N;
@@ -206,13 +217,21 @@ blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K
   g.e.out_f32 = out_f32 ? 1 : 0;
   g.e.out2 = out2;
   g.e.tap = tap;
+  g.e.norm_out = norm_out;
+  g.e.norm_gain = norm_gain;
+  g.e.norm_ss = norm_ss;
+  g.e.norm_parts = (N + kResidBN - 1) / kResidBN;
   return tc(h, g, s, what);
 }
 
 blk_status bf16_mlp_up(const blk_handle* h, const void* y2, int rows, const blk_weights* w, void* neur,
-                       cudaStream_t s) {
+                       cudaStream_t s, const float* row_ss = nullptr) {
   const blk_desc& d = h->d;
   TcGemmDesc g;
+  g.e.row_ss = row_ss;  // set: y2 rows are un-normalised (gain applied); 1/rms from their sum of squares
+  g.e.ss_parts = norm_parts(d);
+  g.e.ss_n = d.hidden;
+  g.e.ss_eps = d.eps;
   g.na = 1;
   g.a[0] = {y2, rows, 0};
   g.K = d.hidden;
@@ -302,30 +321,38 @@ P tap_or(const blk_taps* t, P blk_taps::*m, P dflt) {
 
 blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, const blk_weights* w, void* out,
                                 const Ws& ws, const blk_taps* taps, cudaStream_t s) {
+  // Both RMSNorms are split around the GEMMs they feed: the gain multiplies the
+  // GEMM's A rows (x * g1 is x itself when g1 == 1), the per-row 1/rms multiplies
+  // the accumulator in the epilogue. q/k/v and P are kept in fp16 (3 more
+  // mantissa bits than bf16 at the same tensor-core rate); o and the neurons,
+  // which meet bf16 weights, stay bf16.
   const blk_desc& d = h->d;
   const int M = B * T;
-  const bool bf = true;
-  void* q = tap_or(taps, &blk_taps::attention_queries, ws.q);
-  void* k = tap_or(taps, &blk_taps::attention_keys, ws.k);
-  void* v = tap_or(taps, &blk_taps::attention_values, ws.v);
   void* o = tap_or(taps, &blk_taps::attention_head_outputs, ws.o);
   void* mid_tap = taps ? taps->layer_mid : nullptr;
   void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
-  prof_mark(h, "rmsnorm1", 1, s);
-  BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, M, d.hidden, d.eps, ws.y, bf, s), "rmsnorm 1"));
+  prof_mark(h, "norm1_prep", 1, s);
+  BLK_TRY(check_cuda(launch_norm_prep(x, w->ln1_g, M, d.hidden, d.eps, ws.y, ws.rs1, nullptr, s), "input norm"));
   prof_mark(h, "qkv_gemm_rope", 1, s);
-  BLK_TRY(bf16_qkv(h, ws.y, w, B, T, nullptr, q, k, v, s));
+  BLK_TRY(bf16_qkv(h, ws.y, w, B, T, nullptr, ws.q, ws.k, ws.v, s, ws.rs1, true));
+  if (taps) {  // the taps are bf16
+    const size_t nq = (size_t)M * d.n_heads * d.head_dim, nkv = (size_t)M * d.n_kv_heads * d.head_dim;
+    if (taps->attention_queries)
+      BLK_TRY(check_cuda(launch_cast_f16_bf16(ws.q, taps->attention_queries, nq, s), "q tap"));
+    if (taps->attention_keys) BLK_TRY(check_cuda(launch_cast_f16_bf16(ws.k, taps->attention_keys, nkv, s), "k tap"));
+    if (taps->attention_values)
+      BLK_TRY(check_cuda(launch_cast_f16_bf16(ws.v, taps->attention_values, nkv, s), "v tap"));
+  }
   prof_mark(h, "attention", 1, s);
   const char* why = nullptr;
-  cudaError_t e = launch_attn_prefill_bf16(q, k, v, o, B, d.n_heads, d.n_kv_heads, T, d.head_dim, T, s, &why);
+  cudaError_t e = launch_attn_prefill_tc(ws.q, ws.k, ws.v, o, B, d.n_heads, d.n_kv_heads, T, d.head_dim, true,
+                                         h->status, (unsigned long long)g_wait_ns.load(), s, &why);
   BLK_TRY(check_cuda(e, "attention", why));
-  prof_mark(h, "o_proj_gemm_resid", 1, s);
+  prof_mark(h, "o_proj_gemm_resid_norm2", 1, s);
   BLK_TRY(bf16_linear_resid(h, o, M, d.n_heads * d.head_dim, w->wo, d.hidden, x, false, ws.mid, true, mid_tap,
-                            taps ? taps->attention_output : nullptr, s, "o_proj GEMM"));
-  prof_mark(h, "rmsnorm2", 1, s);
-  BLK_TRY(check_cuda(launch_rmsnorm(ws.mid, w->ln2_g, M, d.hidden, d.eps, ws.y, bf, s, true), "rmsnorm 2"));
+                            taps ? taps->attention_output : nullptr, s, "o_proj GEMM", ws.y, w->ln2_g, ws.ss2));
   prof_mark(h, "mlp_up_gemm_act", 1, s);
-  BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s));
+  BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s, ws.ss2));
   prof_mark(h, "down_gemm_resid", 1, s);
   BLK_TRY(bf16_linear_resid(h, neur, M, d.ffn, w->w_down, d.hidden, ws.mid, true, out, false, nullptr,
                             taps ? taps->mlp_output : nullptr, s, "down GEMM"));
@@ -732,8 +759,8 @@ blk_status blk_attn_gqa(blk_handle* h, const void* q, const void* k, const void*
   }
   if (!kv_lens) {
     if (kv_stride != seq_q) return fail(BLK_ERR_UNSUPPORTED, "bf16 prefill attention: kv_stride must equal seq_q");
-    return check_cuda(launch_attn_prefill_bf16(q, k, v, o, batch, d.n_heads, d.n_kv_heads, seq_q, d.head_dim,
-                                               kv_stride, s, &why),
+    return check_cuda(launch_attn_prefill_tc(q, k, v, o, batch, d.n_heads, d.n_kv_heads, seq_q, d.head_dim,
+                                             false, h->status, (unsigned long long)g_wait_ns.load(), s, &why),
                       "attention", why);
   }
   if (seq_q != 1) return fail(BLK_ERR_UNSUPPORTED, "bf16 attention over a cache: one query per sequence");

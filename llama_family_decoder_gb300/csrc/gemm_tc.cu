@@ -27,6 +27,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -121,7 +123,31 @@ __device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float* 
   }
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 16 values to 16 consecutive 2-byte elements: fp16 when f16, else bf16.
+__device__ __forceinline__ void store16_2b(void* dst, const float* v, bool f16) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = f16 ? pack_f16x2(v[2 * i], v[2 * i + 1]) : pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+// Per-row RMSNorm factor rsqrt(mean(row^2) + eps) from an accumulated sum of squares.
+// The partial sums of a row (one per producer tile) are added in a fixed order: deterministic.
+__device__ __forceinline__ float row_norm_factor(const TcEpiArgs& e, int row, bool row_ok) {
+  if (!e.row_ss || !row_ok) return 1.0f;
+  const float* ps = e.row_ss + (size_t)row * e.ss_parts;
+  float t = 0.f;
+  for (int i = 0; i < e.ss_parts; ++i) t += ps[i];
+  return rsqrtf(t / (float)e.ss_n + e.ss_eps);
+}
 
 template <int BN, int EPI>
 __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, uint32_t taddr, int r_in_tile) {
@@ -160,15 +186,18 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
       const int t = row_ok ? row - b * e.seq : 0;
       const int pos = (e.pos0 ? e.pos0[b] : 0) + t;
       const float2* cs = e.rope + (size_t)min(pos, e.rope_max_pos - 1) * (d / 2);
+      // the input RMSNorm's 1/rms, applied here instead of to the GEMM's A rows
+      const float rs = (e.row_scale && row_ok) ? e.row_scale[row] : 1.0f;
+      const bool f16 = e.qkv_f16 != 0;
 #pragma unroll 1
       for (int hh = 0; hh < BN / 128; ++hh) {
         const int head = (un.b_row0 >> 7) + hh;
         const uint32_t tcol = taddr + hh * 128;
-        __nv_bfloat16* dst;
+        uint16_t* dst;  // 2-byte elements (bf16 or fp16)
         if (seg == 0)
-          dst = reinterpret_cast<__nv_bfloat16*>(e.q) + (((size_t)b * e.n_heads + head) * e.seq + t) * d;
+          dst = reinterpret_cast<uint16_t*>(e.q) + (((size_t)b * e.n_heads + head) * e.seq + t) * d;
         else
-          dst = reinterpret_cast<__nv_bfloat16*>(seg == 1 ? e.k : e.v) +
+          dst = reinterpret_cast<uint16_t*>(seg == 1 ? e.k : e.v) +
                 (((size_t)b * e.n_kv_heads + head) * e.kv_stride + t) * d;
         if (seg == 2) {
 #pragma unroll 1
@@ -177,10 +206,14 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
             tmem_ld16(tcol + c0, v0);
             tmem_ld16(tcol + c0 + 16, v1);
             tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              v0[j] *= rs;
+              v1[j] *= rs;
+            }
             if (row_ok) {
-              auto id = [](float x, int) { return x; };
-              store_bf16_row(dst + c0, v0, 16, id);
-              store_bf16_row(dst + c0 + 16, v1, 16, id);
+              store16_2b(dst + c0, v0, f16);
+              store16_2b(dst + c0 + 16, v1, f16);
             }
           }
           continue;
@@ -199,7 +232,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
 #pragma unroll
             for (int j = 0; j < 16; ++j) ss += v0[j] * v0[j] + v1[j] * v1[j];
           }
-          r = rsqrtf(ss / 128.0f + e.eps);
+          r = rsqrtf(ss * rs * rs / 128.0f + e.eps);
         }
 #pragma unroll 1
         for (int i0 = 0; i0 < 64; i0 += 16) {
@@ -210,7 +243,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
           float y1[16], y2[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            float a = x1[j], c = x2[j];
+            float a = x1[j] * rs, c = x2[j] * rs;
             if (gain) {
               a = a * r * __bfloat162float(gain[i0 + j]);
               c = c * r * __bfloat162float(gain[64 + i0 + j]);
@@ -220,9 +253,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
             y2[j] = c * sc.x + a * sc.y;
           }
           if (row_ok) {
-            auto id = [](float x, int) { return x; };
-            store_bf16_row(dst + i0, y1, 16, id);
-            store_bf16_row(dst + 64 + i0, y2, 16, id);
+            store16_2b(dst + i0, y1, f16);
+            store16_2b(dst + 64 + i0, y2, f16);
           }
         }
       }
@@ -232,6 +264,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
       const int col0 = un.b_row0;
       const int n_valid = p.b_rows[0] - col0;
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(e.out) + (size_t)row * e.ldo + col0;
+      const float r2 = row_norm_factor(e, row, row_ok);  // the post-attention RMSNorm's 1/rms
 #pragma unroll 1
       for (int c0 = 0; c0 < BN / 2; c0 += 16) {
         float g[16], u[16];
@@ -241,7 +274,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
         if (row_ok && c0 < n_valid) {
           float v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = silu_f(g[j]) * u[j];
+          for (int j = 0; j < 16; ++j) v[j] = silu_f(g[j] * r2) * (u[j] * r2);
           auto id = [](float x, int) { return x; };
           store_bf16_row(out + c0, v, min(16, n_valid - c0), id);
         }
@@ -253,9 +286,12 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(e.out) + (size_t)row * e.ldo + col0;
       const __nv_bfloat16* res = nullptr;
       __nv_bfloat16* tap = nullptr;
+      float r2 = 1.0f, ss_part = 0.f;
       if constexpr (EPI == (int)Epi::kResid) {
         res = reinterpret_cast<const __nv_bfloat16*>(e.resid) + (size_t)row * e.ldo + col0;
         if (e.tap) tap = reinterpret_cast<__nv_bfloat16*>(e.tap) + (size_t)row * e.ldo + col0;
+      } else if constexpr (EPI == (int)Epi::kRelu2 || EPI == (int)Epi::kXielu) {
+        r2 = row_norm_factor(e, row, row_ok);  // the post-attention RMSNorm's 1/rms
       }
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -273,13 +309,14 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
           if constexpr (EPI == (int)Epi::kStore) {
             store_bf16_row(out + cc, vv, nv, [](float x, int) { return x; });
           } else if constexpr (EPI == (int)Epi::kRelu2) {
-            store_bf16_row(out + cc, vv, nv, [](float x, int) {
-              const float r = fmaxf(x, 0.0f);
+            store_bf16_row(out + cc, vv, nv, [=](float x, int) {
+              const float r = fmaxf(x * r2, 0.0f);
               return r * r;
             });
           } else if constexpr (EPI == (int)Epi::kXielu) {
             const float ap = e.alpha_p, an = e.alpha_n, be = e.beta, xe = e.xeps;
             store_bf16_row(out + cc, vv, nv, [=](float x, int) {
+              x *= r2;
               return x > 0.0f ? ap * x * x + be * x : an * (expm1f(fminf(x, xe)) - x) + be * x;
             });
           } else if constexpr (EPI == (int)Epi::kResid) {
@@ -331,8 +368,19 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
             }
             if (e.out2)
               store_bf16_row(reinterpret_cast<__nv_bfloat16*>(e.out2) + (size_t)row * e.ldo + col0 + cc, o, nv, id);
+            if (e.norm_out) {
+              // next RMSNorm, split: its gain here (out * g in bf16, the next GEMM's A), its
+              // 1/rms from the row's sum of squares, applied in that GEMM's epilogue
+              const __nv_bfloat16* gn = reinterpret_cast<const __nv_bfloat16*>(e.norm_gain) + col0 + cc;
+              for (int j = 0; j < nv; ++j) ss_part += o[j] * o[j];
+              store_bf16_row(reinterpret_cast<__nv_bfloat16*>(e.norm_out) + (size_t)row * e.ldo + col0 + cc, o, nv,
+                             [&](float x, int j) { return x * __bfloat162float(gn[j]); });
+            }
           }
         }
+      }
+      if constexpr (EPI == (int)Epi::kResid) {
+        if (e.norm_ss && row_ok) e.norm_ss[(size_t)row * e.norm_parts + un.b_row0 / BN] = ss_part;
       }
     }
   }
@@ -493,7 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const Unit un = decode_unit(p, u, bn_rows);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait(tfull_bar(acc), aph, budget, abort_flag)) {
+      // warp-uniform: every lane waits, the warp gives up together
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, budget, abort_flag))) {
         failed = true;
         break;
       }
@@ -535,18 +584,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* ptr, int rows, int K, int box_rows) {
+bool make_map(CUtensorMap* m, const void* ptr, int rows, int K, int box_rows, bool f16 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+}  // namespace
+
+bool make_tma_2d_16b(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows, bool f16) {
+  return make_map(m, ptr, rows, cols, box_rows, f16);
+}
+
+namespace {
 
 template <int BN, int EPI>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t s) {

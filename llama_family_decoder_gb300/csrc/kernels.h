@@ -2,6 +2,7 @@
 // kernel translation units. Not part of the public C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -15,6 +16,14 @@ struct DevStatus;
 // x_f32: x is fp32 while g and y have the storage type (the bf16 path's fp32 residual stream).
 cudaError_t launch_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y, bool bf16,
                            cudaStream_t s, bool x_f32 = false);
+
+// The input RMSNorm split for the fused bf16 prefill: row_scale[r] = rsqrt(mean(x[r]^2) + eps),
+// xg[r, :] = bf16(x[r, :] * g) (the QKV GEMM's A; x itself when g == 1); zeroes zero_rows[r].
+cudaError_t launch_norm_prep(const void* x, const void* g, int rows, int n, float eps, void* xg, float* row_scale,
+                             float* zero_rows, cudaStream_t s);
+
+// dst[i] = bf16(src[i]) for fp16 src (n elements).
+cudaError_t launch_cast_f16_bf16(const void* src, void* dst, size_t n, cudaStream_t s);
 
 // ---------------------------------------------------------------- fp32 SIMT GEMM
 // C[m, c0 + n] = sum_k A[m, k] * B[n, k] for m < M, n < N  (fp32, row-major, ld = K for A/B).
@@ -63,6 +72,20 @@ struct TcEpiArgs {
   int rope_max_pos = 0;
   const int* pos0 = nullptr;     // [B] first position of each sequence, or null
   int qk_norm = 0;
+  const float* row_scale = nullptr;  // kQkv: per-row factor of the accumulator (the input norm's 1/rms)
+  int qkv_f16 = 0;                   // kQkv: store q/k/v as fp16 (else bf16)
+  // activations: per-row RMSNorm of the A rows from a sum of squares, 1/rms = rsqrt(row_ss / ss_n + ss_eps)
+  // (row_ss holds ss_parts partial sums per row, summed in order)
+  const float* row_ss = nullptr;
+  int ss_parts = 0;
+  int ss_n = 0;
+  float ss_eps = 0.f;
+  // kResid: the next RMSNorm split in two: norm_out = bf16(out * norm_gain), and
+  // norm_ss[row * norm_parts + n_tile] = sum over the tile's columns of out^2
+  void* norm_out = nullptr;
+  const void* norm_gain = nullptr;
+  float* norm_ss = nullptr;
+  int norm_parts = 0;
   // activations
   float alpha_p = 0.f, alpha_n = 0.f, beta = 0.f, xeps = 0.f;
   // kPartialT
@@ -82,6 +105,10 @@ struct TcGemmDesc {
   Epi epi = Epi::kStore;
   TcEpiArgs e;
 };
+
+// 2-D TMA map over a row-major bf16 (or fp16) [rows, cols] matrix: boxes of 64
+// columns x box_rows rows, 128-byte swizzle, zero fill out of bounds.
+bool make_tma_2d_16b(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows, bool f16);
 
 // Number of work units (tiles x splits) the descriptor produces.
 int tc_gemm_units(const TcGemmDesc& d);
@@ -120,8 +147,11 @@ cudaError_t launch_post_act(const float* C, int splits, int rows, int F, int ldc
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, int B, int H, int Hkv, int Tq,
                             int d, int kv_stride, const int* kv_lens, int len_add, cudaStream_t s);
 
-cudaError_t launch_attn_prefill_bf16(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv,
-                                     int T, int d, int kv_stride, cudaStream_t s, const char** why);
+// tcgen05/TMEM flash attention (prefill, causal, kv_len == T, head_dim 128).
+// f16: q, k, v are fp16 (else bf16); o is bf16.
+cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int T,
+                                   int d, bool f16, DevStatus* st, unsigned long long wait_ns, cudaStream_t s,
+                                   const char** why);
 
 // Decode (Tq == 1), split over the keys: partial results in ws, combined into o.
 size_t attn_decode_ws_bytes(int B, int H, int d, int max_splits);

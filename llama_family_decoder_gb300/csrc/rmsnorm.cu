@@ -4,6 +4,8 @@
 // Statistics in fp32. HBM-bound: one read and one write of the row with
 // 128-bit accesses, the row held in registers between the two passes. x may be
 // fp32 while g and y are bf16 (the bf16 path keeps its residual stream in fp32).
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -112,7 +114,86 @@ cudaError_t launch_t(const void* x, const void* g, int rows, int n, float eps, v
   return cudaGetLastError();
 }
 
+template <int NC>
+__global__ void __launch_bounds__(kThreads) norm_prep_kernel(const __nv_bfloat16* __restrict__ x,
+                                                             const __nv_bfloat16* __restrict__ g, int rows, int n,
+                                                             float eps, __nv_bfloat16* __restrict__ xg,
+                                                             float* __restrict__ row_scale,
+                                                             float* __restrict__ zero_rows) {
+  __shared__ float red[kThreads / 32];
+  const int nchunk = n / 8;
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const __nv_bfloat16* xr = x + (size_t)r * n;
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      const int c = threadIdx.x + j * kThreads;
+      if (c < nchunk) {
+        float f[8], gg[8];
+        load8<__nv_bfloat16>(xr + c * 8, f);
+        load8<__nv_bfloat16>(g + c * 8, gg);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          ss += f[i] * f[i];
+          f[i] *= gg[i];
+        }
+        store8<__nv_bfloat16>(xg + (size_t)r * n + c * 8, f);
+      }
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) tot += red[w];
+      row_scale[r] = rsqrtf(tot / (float)n + eps);
+      if (zero_rows) zero_rows[r] = 0.f;
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void cast_f16_bf16_kernel(const __half* __restrict__ src, __nv_bfloat16* __restrict__ dst, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = __float2bfloat16_rn(__half2float(src[i]));
+}
+
 }  // namespace
+
+cudaError_t launch_norm_prep(const void* x, const void* g, int rows, int n, float eps, void* xg, float* row_scale,
+                             float* zero_rows, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (n % 8) return cudaErrorInvalidValue;
+  const int nc = (n / 8 + kThreads - 1) / kThreads;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = rows < sms * 8 ? rows : sms * 8;
+  auto X = static_cast<const __nv_bfloat16*>(x);
+  auto G = static_cast<const __nv_bfloat16*>(g);
+  auto XG = static_cast<__nv_bfloat16*>(xg);
+  switch (nc) {
+    case 1: norm_prep_kernel<1><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 2: norm_prep_kernel<2><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 3: norm_prep_kernel<3><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 4: norm_prep_kernel<4><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 5: norm_prep_kernel<5><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 6: norm_prep_kernel<6><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 7: norm_prep_kernel<7><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 8: norm_prep_kernel<8><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast_f16_bf16(const void* src, void* dst, size_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  size_t grid = (n + 255) / 256;
+  if (grid > 4096) grid = 4096;
+  cast_f16_bf16_kernel<<<(int)grid, 256, 0, s>>>(static_cast<const __half*>(src), static_cast<__nv_bfloat16*>(dst), n);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y, bool bf16,
                            cudaStream_t s, bool x_f32) {
