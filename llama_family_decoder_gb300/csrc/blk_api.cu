@@ -89,10 +89,37 @@ int max_cols(const blk_desc& d) {
 }
 
 constexpr int kMaxDecodeSplits = 16;
-constexpr int kResidBN = 256;  // N-tile of the residual GEMMs (o_proj, down)
 
-// Partial sums of squares per row that the o_proj epilogue leaves for the MLP's norm.
-int norm_parts(const blk_desc& d) { return (d.hidden + kResidBN - 1) / kResidBN; }
+// N-tile width for a GEMM with m_rows rows and n_cols output columns (per half
+// when paired): the fewest waves of tiles over the SMs, weighted by each width's
+// per-tile efficiency (narrower tiles re-read A more often).
+int choose_bn(int m_rows, int n_cols, bool paired, const int* cands, int ncand, int num_sms) {
+  int best = cands[0];
+  double best_cost = 1e30;
+  for (int i = 0; i < ncand; ++i) {
+    const int bn = cands[i];
+    const int cols = paired ? bn / 2 : bn;
+    const long long tiles = (long long)((m_rows + 127) / 128) * ((n_cols + cols - 1) / cols);
+    const long long waves = (tiles + num_sms - 1) / num_sms;
+    const double eff = bn >= 256 ? 1.0 : bn >= 224 ? 0.99 : bn >= 192 ? 0.90 : 0.88;
+    const double cost = (double)waves * cols / eff;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+// Tile width of the residual GEMMs (o_proj, down) for `rows` rows of hidden outputs.
+int resid_bn(const blk_handle* h, int rows, int n) {
+  static const int c[] = {256, 224, 192, 128};
+  return choose_bn(rows, n, false, c, 4, h->num_sms);
+}
+
+// Partial sums of squares per row that the o_proj epilogue leaves for the MLP's
+// norm: one per o_proj N-tile (at most hidden / 128 of them).
+int norm_parts(int hidden, int bn) { return (hidden + bn - 1) / bn; }
 
 // Workspace regions of a forward call.
 struct Ws {
@@ -126,7 +153,7 @@ Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, siz
     w.C = c.take(M * max_cols(d) * sizeof(float));
   } else {
     w.rs1 = static_cast<float*>(c.take(M * sizeof(float)));
-    w.ss2 = static_cast<float*>(c.take(M * norm_parts(d) * sizeof(float)));
+    w.ss2 = static_cast<float*>(c.take(M * norm_parts(d.hidden, 128) * sizeof(float)));
   }
   *total = c.off;
   return w;
@@ -190,7 +217,9 @@ blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, in
   g.b[1] = {w->wk, d.n_kv_heads * d.head_dim, d.n_heads * d.head_dim};
   g.b[2] = {w->wv, d.n_kv_heads * d.head_dim, (d.n_heads + d.n_kv_heads) * d.head_dim};
   g.K = d.hidden;
-  g.bn = ((d.n_heads * d.head_dim) % 256 == 0 && (d.n_kv_heads * d.head_dim) % 256 == 0) ? 256 : 128;
+  const bool whole256 = (d.n_heads * d.head_dim) % 256 == 0 && (d.n_kv_heads * d.head_dim) % 256 == 0;
+  static const int qkv_c[] = {256, 128};
+  g.bn = whole256 ? choose_bn(B * T, qkv_cols(d), false, qkv_c, 2, h->num_sms) : 128;
   g.epi = Epi::kQkv;
   g.e = qkv_epi(h, w, T, pos0, q, k, v);
   g.e.row_scale = row_scale;
@@ -208,7 +237,7 @@ blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K
   g.nb = 1;
   g.b[0] = {W, N, 0};
   g.K = K;
-  g.bn = kResidBN;
+  g.bn = resid_bn(h, rows, N);
   g.epi = Epi::kResid;
   g.e.out = out;
   g.e.ldo = N;
@@ -220,22 +249,23 @@ blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K
   g.e.norm_out = norm_out;
   g.e.norm_gain = norm_gain;
   g.e.norm_ss = norm_ss;
-  g.e.norm_parts = (N + kResidBN - 1) / kResidBN;
+  g.e.norm_parts = norm_parts(N, g.bn);
   return tc(h, g, s, what);
 }
 
 blk_status bf16_mlp_up(const blk_handle* h, const void* y2, int rows, const blk_weights* w, void* neur,
-                       cudaStream_t s, const float* row_ss = nullptr) {
+                       cudaStream_t s, const float* row_ss = nullptr, int ss_parts = 0) {
   const blk_desc& d = h->d;
   TcGemmDesc g;
   g.e.row_ss = row_ss;  // set: y2 rows are un-normalised (gain applied); 1/rms from their sum of squares
-  g.e.ss_parts = norm_parts(d);
+  g.e.ss_parts = ss_parts;
   g.e.ss_n = d.hidden;
   g.e.ss_eps = d.eps;
   g.na = 1;
   g.a[0] = {y2, rows, 0};
   g.K = d.hidden;
-  g.bn = 256;
+  static const int act_c[] = {256, 224, 192, 128};
+  g.bn = choose_bn(rows, d.ffn, d.act == BLK_ACT_SWIGLU, act_c, 4, h->num_sms);
   g.e.out = neur;
   g.e.ldo = d.ffn;
   if (d.act == BLK_ACT_SWIGLU) {
@@ -352,7 +382,7 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
   BLK_TRY(bf16_linear_resid(h, o, M, d.n_heads * d.head_dim, w->wo, d.hidden, x, false, ws.mid, true, mid_tap,
                             taps ? taps->attention_output : nullptr, s, "o_proj GEMM", ws.y, w->ln2_g, ws.ss2));
   prof_mark(h, "mlp_up_gemm_act", 1, s);
-  BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s, ws.ss2));
+  BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s, ws.ss2, norm_parts(d.hidden, resid_bn(h, M, d.hidden))));
   prof_mark(h, "down_gemm_resid", 1, s);
   BLK_TRY(bf16_linear_resid(h, neur, M, d.ffn, w->w_down, d.hidden, ws.mid, true, out, false, nullptr,
                             taps ? taps->mlp_output : nullptr, s, "down GEMM"));
@@ -866,7 +896,8 @@ void blk_profile_reset(blk_handle* h) {
 blk_status blk_debug_gemm_bf16(const void* a, const void* b, void* c, int M, int N, int K, int bn, int split_k,
                                void* stream) {
   if (!a || !b || !c) return fail(BLK_ERR_INVALID_ARG, "NULL argument");
-  if (M <= 0 || N <= 0 || K <= 0 || K % 8 || (bn != 64 && bn != 128 && bn != 256) || split_k < 1)
+  if (M <= 0 || N <= 0 || K <= 0 || K % 8 || (bn != 64 && bn != 128 && bn != 192 && bn != 224 && bn != 256) ||
+      split_k < 1)
     return fail(BLK_ERR_INVALID_ARG, "bad sizes");
   if (split_k > 1 && bn != 64) return fail(BLK_ERR_INVALID_ARG, "split_k > 1 needs bn == 64");
   if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return fail(BLK_ERR_ALIGNMENT, "alignment");

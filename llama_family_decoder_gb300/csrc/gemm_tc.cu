@@ -43,16 +43,37 @@ constexpr int kThreads = 192;
 // own limit so that a tiny debug timeout cannot cut them short.
 constexpr unsigned long long kDrainNs = 2000000000ULL;
 
+constexpr int kMaxSmem = 232448;  // 227 KB of dynamic shared memory per CTA
+
+constexpr int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p *= 2;
+  return p;
+}
+
 template <int BN>
 struct TcCfg {
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-  static constexpr int kTmemCols = 2 * BN;
   static constexpr int kBarBytes = 256;
+  static constexpr int kFit = (kMaxSmem - 1024 - kBarBytes) / kStageBytes;
+  static constexpr int kStages = kFit > 8 ? 8 : kFit;  // as deep a TMA ring as fits
+  static constexpr int kTmemCols = pow2_at_least(2 * BN);  // two accumulators
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static_assert(BN % 16 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
+  static_assert(kSmemBytes <= kMaxSmem, "shared memory");
 };
+
+// Tile widths built per epilogue (a GEMM picks its width on the host).
+template <int BN, int EPI>
+constexpr bool tc_supported() {
+  if (EPI == (int)Epi::kQkv) return BN == 128 || BN == 256;  // whole heads
+  if (EPI == (int)Epi::kPartialT) return BN == 64 || BN == 128 || BN == 256;
+  if (EPI == (int)Epi::kStore) return true;
+  if (EPI == (int)Epi::kSwiglu) return BN == 128 || BN == 192 || BN == 256 || BN == 224;
+  return BN == 128 || BN == 192 || BN == 224 || BN == 256;
+}
 
 struct TcParams {
   CUtensorMap ta[3];
@@ -619,16 +640,24 @@ cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int BN, int EPI>
+cudaError_t launch_if(const TcParams& p, int grid, cudaStream_t s) {
+  if constexpr (tc_supported<BN, EPI>())
+    return launch_one<BN, EPI>(p, grid, s);
+  else
+    return cudaErrorInvalidValue;
+}
+
 template <int BN>
 cudaError_t dispatch_epi(const TcParams& p, Epi epi, int grid, cudaStream_t s) {
   switch (epi) {
-    case Epi::kStore: return launch_one<BN, (int)Epi::kStore>(p, grid, s);
-    case Epi::kResid: return launch_one<BN, (int)Epi::kResid>(p, grid, s);
-    case Epi::kQkv: return launch_one<BN, (int)Epi::kQkv>(p, grid, s);
-    case Epi::kSwiglu: return launch_one<BN, (int)Epi::kSwiglu>(p, grid, s);
-    case Epi::kRelu2: return launch_one<BN, (int)Epi::kRelu2>(p, grid, s);
-    case Epi::kXielu: return launch_one<BN, (int)Epi::kXielu>(p, grid, s);
-    case Epi::kPartialT: return launch_one<BN, (int)Epi::kPartialT>(p, grid, s);
+    case Epi::kStore: return launch_if<BN, (int)Epi::kStore>(p, grid, s);
+    case Epi::kResid: return launch_if<BN, (int)Epi::kResid>(p, grid, s);
+    case Epi::kQkv: return launch_if<BN, (int)Epi::kQkv>(p, grid, s);
+    case Epi::kSwiglu: return launch_if<BN, (int)Epi::kSwiglu>(p, grid, s);
+    case Epi::kRelu2: return launch_if<BN, (int)Epi::kRelu2>(p, grid, s);
+    case Epi::kXielu: return launch_if<BN, (int)Epi::kXielu>(p, grid, s);
+    case Epi::kPartialT: return launch_if<BN, (int)Epi::kPartialT>(p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -651,8 +680,8 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
   TcParams p;
   memset(static_cast<void*>(&p), 0, sizeof(p));
   const int bn_rows = d.b_paired ? d.bn / 2 : d.bn;
-  if (d.bn != 64 && d.bn != 128 && d.bn != 256) {
-    *why = "tcgen05 GEMM: BN must be 64, 128 or 256";
+  if (d.bn != 64 && d.bn != 128 && d.bn != 192 && d.bn != 224 && d.bn != 256) {
+    *why = "tcgen05 GEMM: BN must be 64, 128, 192, 224 or 256";
     return cudaErrorInvalidValue;
   }
   if (d.K <= 0 || d.K % 8 != 0) {
@@ -696,11 +725,16 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
   p.wait_ns = wait_ns;
   if (p.num_units == 0) return cudaSuccess;
   const int grid = p.num_units < max_ctas ? p.num_units : max_ctas;
+  cudaError_t e;
   switch (d.bn) {
-    case 64: return dispatch_epi<64>(p, d.epi, grid, s);
-    case 128: return dispatch_epi<128>(p, d.epi, grid, s);
-    default: return dispatch_epi<256>(p, d.epi, grid, s);
+    case 64: e = dispatch_epi<64>(p, d.epi, grid, s); break;
+    case 128: e = dispatch_epi<128>(p, d.epi, grid, s); break;
+    case 192: e = dispatch_epi<192>(p, d.epi, grid, s); break;
+    case 224: e = dispatch_epi<224>(p, d.epi, grid, s); break;
+    default: e = dispatch_epi<256>(p, d.epi, grid, s); break;
   }
+  if (e == cudaErrorInvalidValue && !*why) *why = "tcgen05 GEMM: tile width not built for this epilogue";
+  return e;
 }
 
 }  // namespace blk

@@ -23,6 +23,8 @@ def _operands(M, N, K, seed):
     (300, 384, 520, 128),
     (64, 192, 4096, 64),
     (1000, 136, 136, 128),
+    (384, 4096, 1000, 224),   # 18 full 224-wide tiles plus a 64-column tail
+    (300, 1000, 520, 192),
 ])
 def test_gemm_matches_fp64(M, N, K, bn):
     a, b = _operands(M, N, K, seed=M + N + K)
