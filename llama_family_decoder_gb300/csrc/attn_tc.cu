@@ -49,6 +49,13 @@ struct AttnParams {
   unsigned long long wait_ns;
 };
 
+// 2^x on the MUFU unit (one instruction; -inf gives +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
   if (f16) {
     __half2 h = __floats2half2_rn(lo, hi);
@@ -227,31 +234,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int c = 0; c < kBKeys; c += 16) tmem_ld16(tmem + lane_off + s * kBKeys + c, *reinterpret_cast<float(*)[16]>(&x[c]));
       tc_wait_ld();
       const int n0 = j * kBKeys;
-      const bool need_mask = (n0 + kBKeys - 1 > m0) || (n0 + kBKeys > p.T);
-      float mt = -INFINITY;
+      // raw scores: masked entries become -inf (only tiles on the diagonal or past T)
+      if ((n0 + kBKeys - 1 > m0) || (n0 + kBKeys > p.T)) {
+        const int lim = min(qi, p.T - 1) - n0;  // keys n0 + c with c <= lim are visible
 #pragma unroll
-      for (int c = 0; c < kBKeys; ++c) {
-        float v = x[c] * p.sl2;
-        if (need_mask && (n0 + c > qi || n0 + c >= p.T)) v = -INFINITY;
-        x[c] = v;
-        mt = fmaxf(mt, v);
+        for (int c = 0; c < kBKeys; ++c)
+          if (c > lim) x[c] = -INFINITY;
       }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = x[i];
+#pragma unroll
+      for (int c = 8; c < kBKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+      const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float mt = mraw * p.sl2;  // the scale is positive: the max commutes with it
       const bool need = mt > m_ref + kRescaleLog2;
       const bool any = __any_sync(0xffffffffu, need);
       float alpha = 1.f;
       if (need) {
-        alpha = exp2f(m_ref - mt);
+        alpha = ex2_approx(m_ref - mt);
         m_ref = mt;
       }
-      l *= alpha;
-      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+      const float neg_mu = m_ref == -INFINITY ? 0.f : -m_ref;
       uint32_t pk[kBKeys / 2];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kBKeys; c += 2) {
-        const float p0 = exp2f(x[c] - mu), p1 = exp2f(x[c + 1] - mu);
-        l += p0 + p1;
+        const float p0 = ex2_approx(fmaf(x[c], p.sl2, neg_mu));
+        const float p1 = ex2_approx(fmaf(x[c + 1], p.sl2, neg_mu));
+        ls[(c >> 1) & 3] += p0 + p1;
         pk[c / 2] = pack2(p0, p1, F16);
       }
+      l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       if (j >= 1) {  // P buffer and O are free once PV_{j-1} is done
         if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, budget, abort_flag))) {
           failed = true;
