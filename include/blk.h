@@ -94,6 +94,7 @@ typedef struct {
 typedef struct {
   const void *ln1_g, *wq, *wk, *wv, *q_norm_g, *k_norm_g, *wo, *ln2_g;
   const void *w_gate, *w_up, *w_down;
+  const void* prepared; /* NULL, or the buffer blk_prepare_weights filled for these weights */
 } blk_weights;
 
 /* KV cache for decode: k, v are [batch, Hkv, capacity, d] in the descriptor's
@@ -126,6 +127,20 @@ typedef struct blk_handle blk_handle;
  * in double on the host). No weights are copied. Requires a current CUDA
  * device. Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 blk_status blk_create(const blk_desc* desc, blk_handle** out);
+
+/* Optional one-time weight preparation (bf16 path), the step an inference
+ * engine does when it loads a model: fp16 copies of wo, w_gate and w_up are
+ * written to `prepared`, a caller-owned device buffer of at least
+ * blk_prepared_bytes(h) bytes. With weights.prepared set, the prefill's o_proj
+ * and MLP-up GEMMs take fp16 operands (attention output and normed rows in fp16
+ * too): 3 more mantissa bits than bf16 at the same tensor-core rate. The
+ * conversion is exact for every bf16 weight with 2^-17 <= |w| <= 65504; smaller
+ * ones move by at most 2^-25. The copies must be refreshed whenever the bf16
+ * weights change. Synchronises `stream` (it checks the range on the device).
+ * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED (fp32 handle, or a
+ * weight outside the fp16 range: then use the weights unprepared), CUDA. */
+size_t blk_prepared_bytes(const blk_handle* h);
+blk_status blk_prepare_weights(blk_handle* h, const blk_weights* w, void* prepared, size_t bytes, void* stream);
 
 /* Frees the handle and its device tables. Safe on NULL. Synchronises nothing:
  * the caller must ensure no work using the handle is still in flight. */

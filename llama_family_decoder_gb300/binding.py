@@ -29,7 +29,7 @@ class blk_desc(ctypes.Structure):
 
 class blk_weights(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("ln1_g", "wq", "wk", "wv", "q_norm_g", "k_norm_g", "wo", "ln2_g",
-                                         "w_gate", "w_up", "w_down")]
+                                         "w_gate", "w_up", "w_down", "prepared")]
 
 
 class blk_kv_cache(ctypes.Structure):
@@ -75,6 +75,8 @@ SIGNATURES = {
                                          POINTER(blk_taps), POINTER(c_void_p)]),
     "blk_graph_launch": (c_int, [c_void_p, c_void_p]),
     "blk_graph_destroy": (c_int, [c_void_p]),
+    "blk_prepared_bytes": (c_size_t, [c_void_p]),
+    "blk_prepare_weights": (c_int, [c_void_p, POINTER(blk_weights), c_void_p, c_size_t, c_void_p]),
     "blk_attn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                         c_void_p, c_void_p]),
 }
@@ -135,7 +137,7 @@ def make_weights_struct(w: dict) -> blk_weights:
     g = w.get
     return blk_weights(_ptr(g("input_layernorm")), _ptr(g("q_proj")), _ptr(g("k_proj")), _ptr(g("v_proj")),
                        _ptr(g("q_norm")), _ptr(g("k_norm")), _ptr(g("o_proj")), _ptr(g("post_attention_layernorm")),
-                       _ptr(g("gate_proj")), _ptr(g("up_proj")), _ptr(g("down_proj")))
+                       _ptr(g("gate_proj")), _ptr(g("up_proj")), _ptr(g("down_proj")), _ptr(g("prepared")))
 
 
 class DecoderBlock:
@@ -169,6 +171,15 @@ class DecoderBlock:
             self.close()
         except Exception:
             pass
+
+    def prepare(self, weights, stream=None):
+        """fp16 copies of wo / w_gate / w_up (blk_prepare_weights); returns weights plus 'prepared'."""
+        import torch
+        buf = torch.empty(max(lib().blk_prepared_bytes(self.handle), 16), dtype=torch.uint8,
+                          device=weights["o_proj"].device)
+        wst = make_weights_struct(weights)
+        _check(lib().blk_prepare_weights(self.handle, ctypes.byref(wst), _ptr(buf), buf.numel(), _stream_ptr(stream)))
+        return dict(weights, prepared=buf)
 
     def workspace_bytes(self, batch, seq, decode=False):
         return lib().blk_workspace_bytes(self.handle, batch, seq, int(decode))

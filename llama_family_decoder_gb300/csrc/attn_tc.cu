@@ -42,7 +42,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnParams {
   CUtensorMap tq, tk, tv;
-  __nv_bfloat16* o;
+  void* o;
+  int o_f16;
   int B, H, Hkv, T, n_qtiles;
   float sl2;
   DevStatus* status;
@@ -305,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       __syncwarp();
       tc_fence_after();
       const float inv = 1.f / l;
-      __nv_bfloat16* orow = p.o + (((size_t)b * p.T + qi) * p.H + h) * kD;
+      uint16_t* orow = static_cast<uint16_t*>(p.o) + (((size_t)b * p.T + qi) * p.H + h) * kD;
+      const bool of16 = p.o_f16 != 0;
 #pragma unroll 1
       for (int c = 0; c < kD; c += 16) {
         float ov[16];
@@ -313,14 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         tc_wait_ld();
         if (qi < p.T) {
           uint4 w0, w1;
-          w0.x = pack_bf16x2(ov[0] * inv, ov[1] * inv);
-          w0.y = pack_bf16x2(ov[2] * inv, ov[3] * inv);
-          w0.z = pack_bf16x2(ov[4] * inv, ov[5] * inv);
-          w0.w = pack_bf16x2(ov[6] * inv, ov[7] * inv);
-          w1.x = pack_bf16x2(ov[8] * inv, ov[9] * inv);
-          w1.y = pack_bf16x2(ov[10] * inv, ov[11] * inv);
-          w1.z = pack_bf16x2(ov[12] * inv, ov[13] * inv);
-          w1.w = pack_bf16x2(ov[14] * inv, ov[15] * inv);
+          w0.x = pack2(ov[0] * inv, ov[1] * inv, of16);
+          w0.y = pack2(ov[2] * inv, ov[3] * inv, of16);
+          w0.z = pack2(ov[4] * inv, ov[5] * inv, of16);
+          w0.w = pack2(ov[6] * inv, ov[7] * inv, of16);
+          w1.x = pack2(ov[8] * inv, ov[9] * inv, of16);
+          w1.y = pack2(ov[10] * inv, ov[11] * inv, of16);
+          w1.z = pack2(ov[12] * inv, ov[13] * inv, of16);
+          w1.w = pack2(ov[14] * inv, ov[15] * inv, of16);
           reinterpret_cast<uint4*>(orow + c)[0] = w0;
           reinterpret_cast<uint4*>(orow + c)[1] = w1;
         }
@@ -343,8 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 }  // namespace
 
 cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int T,
-                                   int d, bool f16, DevStatus* st, unsigned long long wait_ns, cudaStream_t s,
-                                   const char** why) {
+                                   int d, bool f16, bool o_f16, DevStatus* st, unsigned long long wait_ns,
+                                   cudaStream_t s, const char** why) {
   if (d != kD) {
     *why = "tcgen05 attention: head_dim must be 128";
     return cudaErrorInvalidValue;
@@ -357,7 +359,8 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
     *why = "cuTensorMapEncodeTiled failed for q/k/v";
     return cudaErrorInvalidValue;
   }
-  p.o = static_cast<__nv_bfloat16*>(o);
+  p.o = o;
+  p.o_f16 = o_f16 ? 1 : 0;
   p.B = B;
   p.H = H;
   p.Hkv = Hkv;

@@ -43,6 +43,7 @@ struct blk_handle {
   int num_sms;
   float2* rope;        // [max_seq][head_dim/2] (cos, sin) as fp32, from double
   DevStatus* status;   // device
+  int* dev_flag;       // device int: weight-range check of blk_prepare_weights
   StageProfile prof;
 };
 
@@ -78,6 +79,21 @@ struct Carve {
     return p;
   }
 };
+
+// fp16 copies of the weights the prefill's fp16 GEMMs read (blk_prepare_weights).
+struct Prepared {
+  const void *wo, *wg, *wu;
+};
+
+size_t prepared_layout(const blk_desc& d, const void* base, Prepared* out) {
+  Carve c(const_cast<void*>(base));
+  Prepared p{};
+  p.wo = c.take((size_t)d.hidden * d.n_heads * d.head_dim * 2);
+  if (d.act == BLK_ACT_SWIGLU) p.wg = c.take((size_t)d.ffn * d.hidden * 2);
+  p.wu = c.take((size_t)d.ffn * d.hidden * 2);
+  if (out) *out = p;
+  return c.off;
+}
 
 int qkv_cols(const blk_desc& d) { return (d.n_heads + 2 * d.n_kv_heads) * d.head_dim; }
 int mlp_cols(const blk_desc& d) { return d.act == BLK_ACT_SWIGLU ? 2 * d.ffn : d.ffn; }
@@ -230,7 +246,7 @@ blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, in
 blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K, const void* W, int N,
                              const void* resid, bool resid_f32, void* out, bool out_f32, void* out2, void* tap,
                              cudaStream_t s, const char* what, void* norm_out = nullptr,
-                             const void* norm_gain = nullptr, float* norm_ss = nullptr) {
+                             const void* norm_gain = nullptr, float* norm_ss = nullptr, bool f16 = false) {
   TcGemmDesc g;
   g.na = 1;
   g.a[0] = {a, rows, 0};
@@ -250,11 +266,14 @@ blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K
   g.e.norm_gain = norm_gain;
   g.e.norm_ss = norm_ss;
   g.e.norm_parts = norm_parts(N, g.bn);
+  g.e.norm_f16 = f16 ? 1 : 0;  // the MLP-up GEMM that reads norm_out has the same operand type
+  g.f16 = f16;
   return tc(h, g, s, what);
 }
 
 blk_status bf16_mlp_up(const blk_handle* h, const void* y2, int rows, const blk_weights* w, void* neur,
-                       cudaStream_t s, const float* row_ss = nullptr, int ss_parts = 0) {
+                       cudaStream_t s, const float* row_ss = nullptr, int ss_parts = 0,
+                       const Prepared* prep = nullptr) {
   const blk_desc& d = h->d;
   TcGemmDesc g;
   g.e.row_ss = row_ss;  // set: y2 rows are un-normalised (gain applied); 1/rms from their sum of squares
@@ -271,18 +290,19 @@ blk_status bf16_mlp_up(const blk_handle* h, const void* y2, int rows, const blk_
   if (d.act == BLK_ACT_SWIGLU) {
     g.nb = 2;
     g.b_paired = true;
-    g.b[0] = {w->w_gate, d.ffn, 0};
-    g.b[1] = {w->w_up, d.ffn, 0};
+    g.b[0] = {prep ? prep->wg : w->w_gate, d.ffn, 0};
+    g.b[1] = {prep ? prep->wu : w->w_up, d.ffn, 0};
     g.epi = Epi::kSwiglu;
   } else {
     g.nb = 1;
-    g.b[0] = {w->w_up, d.ffn, 0};
+    g.b[0] = {prep ? prep->wu : w->w_up, d.ffn, 0};
     g.epi = d.act == BLK_ACT_RELU2 ? Epi::kRelu2 : Epi::kXielu;
     g.e.alpha_p = d.xielu_alpha_p;
     g.e.alpha_n = d.xielu_alpha_n;
     g.e.beta = d.xielu_beta;
     g.e.xeps = d.xielu_eps;
   }
+  g.f16 = prep != nullptr;
   return tc(h, g, s, "MLP up GEMM");
 }
 
@@ -373,16 +393,28 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
     if (taps->attention_values)
       BLK_TRY(check_cuda(launch_cast_f16_bf16(ws.v, taps->attention_values, nkv, s), "v tap"));
   }
+  // with prepared (fp16) weights, the attention output and the normed MLP input
+  // are fp16 operands of o_proj and of the MLP-up GEMM
+  Prepared prep{};
+  const bool f16 = w->prepared != nullptr;
+  if (f16) prepared_layout(d, w->prepared, &prep);
+  void* o_buf = f16 ? ws.o : o;
   prof_mark(h, "attention", 1, s);
   const char* why = nullptr;
-  cudaError_t e = launch_attn_prefill_tc(ws.q, ws.k, ws.v, o, B, d.n_heads, d.n_kv_heads, T, d.head_dim, true,
-                                         h->status, (unsigned long long)g_wait_ns.load(), s, &why);
+  cudaError_t e = launch_attn_prefill_tc(ws.q, ws.k, ws.v, o_buf, B, d.n_heads, d.n_kv_heads, T, d.head_dim, true,
+                                         f16, h->status, (unsigned long long)g_wait_ns.load(), s, &why);
   BLK_TRY(check_cuda(e, "attention", why));
+  if (f16 && taps && taps->attention_head_outputs)
+    BLK_TRY(check_cuda(launch_cast_f16_bf16(o_buf, taps->attention_head_outputs,
+                                            (size_t)M * d.n_heads * d.head_dim, s),
+                       "head-output tap"));
   prof_mark(h, "o_proj_gemm_resid_norm2", 1, s);
-  BLK_TRY(bf16_linear_resid(h, o, M, d.n_heads * d.head_dim, w->wo, d.hidden, x, false, ws.mid, true, mid_tap,
-                            taps ? taps->attention_output : nullptr, s, "o_proj GEMM", ws.y, w->ln2_g, ws.ss2));
+  BLK_TRY(bf16_linear_resid(h, o_buf, M, d.n_heads * d.head_dim, f16 ? prep.wo : w->wo, d.hidden, x, false, ws.mid,
+                            true, mid_tap, taps ? taps->attention_output : nullptr, s, "o_proj GEMM", ws.y, w->ln2_g,
+                            ws.ss2, f16));
   prof_mark(h, "mlp_up_gemm_act", 1, s);
-  BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s, ws.ss2, norm_parts(d.hidden, resid_bn(h, M, d.hidden))));
+  BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s, ws.ss2, norm_parts(d.hidden, resid_bn(h, M, d.hidden)),
+                      f16 ? &prep : nullptr));
   prof_mark(h, "down_gemm_resid", 1, s);
   BLK_TRY(bf16_linear_resid(h, neur, M, d.ffn, w->w_down, d.hidden, ws.mid, true, out, false, nullptr,
                             taps ? taps->mlp_output : nullptr, s, "down GEMM"));
@@ -519,6 +551,8 @@ blk_status check_weights(const blk_desc& d, const blk_weights* w) {
     return fail(w->w_gate ? BLK_ERR_ALIGNMENT : BLK_ERR_INVALID_ARG, "SWIGLU needs an aligned w_gate");
   if (d.qk_norm && (!w->q_norm_g || !w->k_norm_g || !aligned16(w->q_norm_g) || !aligned16(w->k_norm_g)))
     return fail(BLK_ERR_INVALID_ARG, "qk_norm needs aligned q_norm_g and k_norm_g");
+  if (w->prepared && (d.dtype != BLK_BF16 || !aligned16(w->prepared)))
+    return fail(BLK_ERR_INVALID_ARG, "prepared weights: bf16 handles only, 16-byte aligned");
   return BLK_OK;
 }
 
@@ -583,6 +617,7 @@ blk_status blk_create(const blk_desc* desc, blk_handle** out) {
   h->d = d;
   h->rope = nullptr;
   h->status = nullptr;
+  h->dev_flag = nullptr;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e != cudaSuccess) {
@@ -601,9 +636,11 @@ blk_status blk_create(const blk_desc* desc, blk_handle** out) {
   if (e == cudaSuccess) e = cudaMemcpy(h->rope, table.data(), table.size() * sizeof(float2), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMalloc(&h->status, sizeof(DevStatus));
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(DevStatus));
+  if (e == cudaSuccess) e = cudaMalloc(&h->dev_flag, sizeof(int));
   if (e != cudaSuccess) {
     if (h->rope) cudaFree(h->rope);
     if (h->status) cudaFree(h->status);
+    if (h->dev_flag) cudaFree(h->dev_flag);
     delete h;
     return cuda_fail(e, "blk_create: allocation");
   }
@@ -616,7 +653,37 @@ blk_status blk_destroy(blk_handle* h) {
   blk_profile_enable(h, 0);
   if (h->rope) cudaFree(h->rope);
   if (h->status) cudaFree(h->status);
+  if (h->dev_flag) cudaFree(h->dev_flag);
   delete h;
+  return BLK_OK;
+}
+
+size_t blk_prepared_bytes(const blk_handle* h) {
+  if (!h || h->d.dtype != BLK_BF16) return 0;
+  return prepared_layout(h->d, nullptr, nullptr);
+}
+
+blk_status blk_prepare_weights(blk_handle* h, const blk_weights* w, void* prepared, size_t bytes, void* stream) {
+  if (!h || !w || !prepared) return fail(BLK_ERR_INVALID_ARG, "NULL argument");
+  const blk_desc& d = h->d;
+  if (d.dtype != BLK_BF16) return fail(BLK_ERR_UNSUPPORTED, "prepared weights exist for the bf16 path only");
+  if (!w->wo || !w->w_up || (d.act == BLK_ACT_SWIGLU && !w->w_gate))
+    return fail(BLK_ERR_INVALID_ARG, "wo / w_up / w_gate NULL");
+  if (!aligned16(prepared)) return fail(BLK_ERR_ALIGNMENT, "prepared buffer not 16-byte aligned");
+  if (bytes < blk_prepared_bytes(h)) return fail(BLK_ERR_WORKSPACE, "prepared buffer too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Prepared p{};
+  prepared_layout(d, prepared, &p);
+  BLK_TRY(check_cuda(cudaMemsetAsync(h->dev_flag, 0, sizeof(int), s), "prepare"));
+  const size_t n_o = (size_t)d.hidden * d.n_heads * d.head_dim, n_f = (size_t)d.ffn * d.hidden;
+  BLK_TRY(check_cuda(launch_cast_bf16_f16(w->wo, const_cast<void*>(p.wo), n_o, h->dev_flag, s), "prepare wo"));
+  if (p.wg)
+    BLK_TRY(check_cuda(launch_cast_bf16_f16(w->w_gate, const_cast<void*>(p.wg), n_f, h->dev_flag, s), "prepare w_gate"));
+  BLK_TRY(check_cuda(launch_cast_bf16_f16(w->w_up, const_cast<void*>(p.wu), n_f, h->dev_flag, s), "prepare w_up"));
+  int overflow = 0;
+  BLK_TRY(check_cuda(cudaMemcpyAsync(&overflow, h->dev_flag, sizeof(int), cudaMemcpyDeviceToHost, s), "prepare"));
+  BLK_TRY(check_cuda(cudaStreamSynchronize(s), "prepare"));
+  if (overflow) return fail(BLK_ERR_UNSUPPORTED, "a weight lies outside the fp16 range: use the weights unprepared");
   return BLK_OK;
 }
 
@@ -790,7 +857,7 @@ blk_status blk_attn_gqa(blk_handle* h, const void* q, const void* k, const void*
   if (!kv_lens) {
     if (kv_stride != seq_q) return fail(BLK_ERR_UNSUPPORTED, "bf16 prefill attention: kv_stride must equal seq_q");
     return check_cuda(launch_attn_prefill_tc(q, k, v, o, batch, d.n_heads, d.n_kv_heads, seq_q, d.head_dim,
-                                             false, h->status, (unsigned long long)g_wait_ns.load(), s, &why),
+                                             false, false, h->status, (unsigned long long)g_wait_ns.load(), s, &why),
                       "attention", why);
   }
   if (seq_q != 1) return fail(BLK_ERR_UNSUPPORTED, "bf16 attention over a cache: one query per sequence");

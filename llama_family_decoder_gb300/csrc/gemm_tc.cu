@@ -86,6 +86,7 @@ struct TcParams {
   int b_out[3];
   int na, nb;
   int b_paired;
+  int f16;  // fp16 operands (else bf16)
   int num_kb;
   int k_splits;
   int m_tiles, n_tiles;
@@ -140,7 +141,9 @@ __device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float* 
     reinterpret_cast<uint4*>(dst)[0] = a;
     reinterpret_cast<uint4*>(dst)[1] = b;
   } else {
-    for (int i = 0; i < n_valid; ++i) dst[i] = __float2bfloat16_rn(f(v[i], i));
+#pragma unroll
+    for (int i = 0; i < 16; ++i)  // compile-time indices keep v in registers
+      if (i < n_valid) dst[i] = __float2bfloat16_rn(f(v[i], i));
   }
 }
 
@@ -355,7 +358,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
                   rr[4 * j + 3] = f4.w;
                 }
               } else {
-                for (int j = 0; j < nv; ++j) rr[j] = rf[j];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) rr[j] = j < nv ? rf[j] : 0.f;
               }
             } else if (nv == 16) {
               const uint4 ra = reinterpret_cast<const uint4*>(res + cc)[0];
@@ -368,7 +372,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
                 rr[2 * j + 1] = f2.y;
               }
             } else {
-              for (int j = 0; j < nv; ++j) rr[j] = __bfloat162float(res[cc + j]);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) rr[j] = j < nv ? __bfloat162float(res[cc + j]) : 0.f;
             }
             float o[16];
 #pragma unroll
@@ -382,7 +387,9 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
                 for (int j = 0; j < 4; ++j)
                   reinterpret_cast<float4*>(of)[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
               } else {
-                for (int j = 0; j < nv; ++j) of[j] = o[j];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (j < nv) of[j] = o[j];
               }
             } else {
               store_bf16_row(out + cc, o, nv, id);
@@ -393,9 +400,37 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
               // next RMSNorm, split: its gain here (out * g in bf16, the next GEMM's A), its
               // 1/rms from the row's sum of squares, applied in that GEMM's epilogue
               const __nv_bfloat16* gn = reinterpret_cast<const __nv_bfloat16*>(e.norm_gain) + col0 + cc;
-              for (int j = 0; j < nv; ++j) ss_part += o[j] * o[j];
-              store_bf16_row(reinterpret_cast<__nv_bfloat16*>(e.norm_out) + (size_t)row * e.ldo + col0 + cc, o, nv,
-                             [&](float x, int j) { return x * __bfloat162float(gn[j]); });
+              float og[16];
+              uint16_t* nd = reinterpret_cast<uint16_t*>(e.norm_out) + (size_t)row * e.ldo + col0 + cc;
+              if (nv == 16) {
+                uint4 g2[2];
+                g2[0] = reinterpret_cast<const uint4*>(gn)[0];
+                g2[1] = reinterpret_cast<const uint4*>(gn)[1];
+                const uint32_t* gw = reinterpret_cast<const uint32_t*>(g2);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float2 gf = unpack_bf16x2(gw[j]);
+                  ss_part += o[2 * j] * o[2 * j] + o[2 * j + 1] * o[2 * j + 1];
+                  og[2 * j] = o[2 * j] * gf.x;
+                  og[2 * j + 1] = o[2 * j + 1] * gf.y;
+                }
+                store16_2b(nd, og, e.norm_f16 != 0);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  if (j < nv) {
+                    ss_part += o[j] * o[j];
+                    const float v = o[j] * __bfloat162float(gn[j]);
+                    if (e.norm_f16) {
+                      const __half hv = __float2half_rn(v);
+                      nd[j] = *reinterpret_cast<const uint16_t*>(&hv);
+                    } else {
+                      const __nv_bfloat16 bv = __float2bfloat16_rn(v);
+                      nd[j] = *reinterpret_cast<const uint16_t*>(&bv);
+                    }
+                  }
+                }
+              }
             }
           }
         }
@@ -504,7 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      // kind::f16 operand formats: bf16 (1) or fp16 (0) for A and B
+      const uint32_t idesc = p.f16 ? (idesc_bf16_f32(kBM, BN) & ~((7u << 7) | (7u << 10))) : idesc_bf16_f32(kBM, BN);
       int stage = 0;
       uint32_t ph = 0;
       int it = 0;
@@ -696,7 +732,7 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
   p.nb = d.nb;
   p.a_tiles[0] = 0;
   for (int i = 0; i < d.na; ++i) {
-    if (!make_map(&p.ta[i], d.a[i].ptr, d.a[i].rows, d.K, kBM)) {
+    if (!make_map(&p.ta[i], d.a[i].ptr, d.a[i].rows, d.K, kBM, d.f16)) {
       *why = "cuTensorMapEncodeTiled failed for an A operand";
       return cudaErrorInvalidValue;
     }
@@ -706,7 +742,7 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
   }
   p.b_tiles[0] = 0;
   for (int i = 0; i < d.nb; ++i) {
-    if (!make_map(&p.tb[i], d.b[i].ptr, d.b[i].rows, d.K, bn_rows)) {
+    if (!make_map(&p.tb[i], d.b[i].ptr, d.b[i].rows, d.K, bn_rows, d.f16)) {
       *why = "cuTensorMapEncodeTiled failed for a B operand";
       return cudaErrorInvalidValue;
     }
@@ -715,6 +751,7 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
     p.b_tiles[i + 1] = p.b_tiles[i] + (d.b[i].rows + bn_rows - 1) / bn_rows;
   }
   p.b_paired = d.b_paired ? 1 : 0;
+  p.f16 = d.f16 ? 1 : 0;
   p.m_tiles = p.a_tiles[d.na];
   p.n_tiles = d.b_paired ? (d.b[0].rows + bn_rows - 1) / bn_rows : p.b_tiles[d.nb];
   p.num_kb = (d.K + kBK - 1) / kBK;

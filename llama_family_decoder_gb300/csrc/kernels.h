@@ -25,6 +25,9 @@ cudaError_t launch_norm_prep(const void* x, const void* g, int rows, int n, floa
 // dst[i] = bf16(src[i]) for fp16 src (n elements).
 cudaError_t launch_cast_f16_bf16(const void* src, void* dst, size_t n, cudaStream_t s);
 
+// dst[i] = fp16(src[i]) for bf16 src; *overflow = 1 if some |src[i]| > 65504.
+cudaError_t launch_cast_bf16_f16(const void* src, void* dst, size_t n, int* overflow, cudaStream_t s);
+
 // ---------------------------------------------------------------- fp32 SIMT GEMM
 // C[m, c0 + n] = sum_k A[m, k] * B[n, k] for m < M, n < N  (fp32, row-major, ld = K for A/B).
 cudaError_t launch_gemm_f32(const float* A, const float* B, float* C, int ldc, int M, int N, int K, cudaStream_t s);
@@ -83,6 +86,7 @@ struct TcEpiArgs {
   // kResid: the next RMSNorm split in two: norm_out = bf16(out * norm_gain), and
   // norm_ss[row * norm_parts + n_tile] = sum over the tile's columns of out^2
   void* norm_out = nullptr;
+  int norm_f16 = 0;  // norm_out in fp16 (else bf16)
   const void* norm_gain = nullptr;
   float* norm_ss = nullptr;
   int norm_parts = 0;
@@ -99,6 +103,7 @@ struct TcGemmDesc {
   TcSeg b[3];
   int nb = 1;
   bool b_paired = false;  // B tile = halves from b[0] and b[1] at the same rows (gate/up)
+  bool f16 = false;       // A and B are fp16 (else bf16)
   int K = 0;              // inner dimension; every segment has row stride K
   int k_splits = 1;
   int bn = 256;           // 64, 128 or 256
@@ -148,10 +153,10 @@ cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, floa
                             int d, int kv_stride, const int* kv_lens, int len_add, cudaStream_t s);
 
 // tcgen05/TMEM flash attention (prefill, causal, kv_len == T, head_dim 128).
-// f16: q, k, v are fp16 (else bf16); o is bf16.
+// f16: q, k, v are fp16 (else bf16); o_f16: o is fp16 (else bf16).
 cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int T,
-                                   int d, bool f16, DevStatus* st, unsigned long long wait_ns, cudaStream_t s,
-                                   const char** why);
+                                   int d, bool f16, bool o_f16, DevStatus* st, unsigned long long wait_ns,
+                                   cudaStream_t s, const char** why);
 
 // Decode (Tq == 1), split over the keys: partial results in ws, combined into o.
 size_t attn_decode_ws_bytes(int B, int H, int d, int max_splits);

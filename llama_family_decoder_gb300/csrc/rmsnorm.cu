@@ -159,7 +159,27 @@ __global__ void cast_f16_bf16_kernel(const __half* __restrict__ src, __nv_bfloat
     dst[i] = __float2bfloat16_rn(__half2float(src[i]));
 }
 
+__global__ void cast_bf16_f16_kernel(const __nv_bfloat16* __restrict__ src, __half* __restrict__ dst, size_t n,
+                                     int* __restrict__ overflow) {
+  bool bad = false;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float f = __bfloat162float(src[i]);
+    bad |= !(fabsf(f) <= 65504.f);
+    dst[i] = __float2half_rn(f);
+  }
+  if (bad) atomicExch(overflow, 1);
+}
+
 }  // namespace
+
+cudaError_t launch_cast_bf16_f16(const void* src, void* dst, size_t n, int* overflow, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  size_t grid = (n + 255) / 256;
+  if (grid > 8192) grid = 8192;
+  cast_bf16_f16_kernel<<<(int)grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), static_cast<__half*>(dst), n,
+                                                 overflow);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_norm_prep(const void* x, const void* g, int rows, int n, float eps, void* xg, float* row_scale,
                              float* zero_rows, cudaStream_t s) {

@@ -21,11 +21,12 @@ def test_prefill_full_size_sampled_rows(name):
     w = make_weights(wl)
     x = make_input(wl)
     blk = DecoderBlock.from_workload(wl)
-    out = blk.forward(x.cuda(), {k: v.cuda() for k, v in w.items()})
+    wd = blk.prepare({k: v.cuda() for k, v in w.items()})  # as bench.py runs it
+    out = blk.forward(x.cuda(), wd)
     torch.cuda.synchronize()
     assert blk.last_status() == 0
     out = out.cpu()
-    del blk
+    del blk, wd
     wn = weights_np(w)
     T = wl.seq
     rows = sorted({0, 1, 63, 64, 127, 128, 129, 1000, T // 2 + 3, T - 129, T - 2, T - 1})
@@ -60,3 +61,18 @@ def test_decode_full_size_sampled_sequences():
     assert err <= TOL["bf16"], (err, floor)
     assert rel_err(kd[seqs, :, wl.cache_len].cpu(), ref["new_key"]) <= TOL["bf16"]
     assert rel_err(vd[seqs, :, wl.cache_len].cpu(), ref["new_value"]) <= TOL["bf16"]
+
+
+def test_prefill_full_size_every_row():
+    # every output of the Llama-7B-shape workload (1 x 2048 x 4096) against the oracle
+    wl = WORKLOADS["llama7b_bf16_B1_T2048"]
+    w = make_weights(wl)
+    x = make_input(wl)
+    blk = DecoderBlock.from_workload(wl)
+    wd = blk.prepare({k: v.cuda() for k, v in w.items()})
+    out = blk.forward(x.cuda(), wd).cpu()
+    ref = oracle.block_forward(cfg_of(wl), weights_np(w), np64(x))["layer_output"]
+    e = np.abs(np64(out) - ref) / np.sqrt(np.mean(ref * ref))
+    print(f"llama7b every row: max {e.max():.4f}, 99.99th pct {np.quantile(e, 0.9999):.4f}, "
+          f"bf16 floor {bf16_floor(ref):.4f}")
+    assert e.max() <= TOL["bf16"]

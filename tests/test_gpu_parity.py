@@ -39,13 +39,16 @@ def _tap_buffers(wl, dt):
     return {k: torch.empty(s, dtype=dt, device=DEV) for k, s in shapes.items()}
 
 
-def _run(wl, gain_std=0.0, taps=False):
+def _run(wl, gain_std=0.0, taps=False, prepared=False):
     w = make_weights(wl, gain_std=gain_std)
     x = make_input(wl)
     blk = DecoderBlock.from_workload(wl)
     xd = x.to(DEV)
     tb = _tap_buffers(wl, xd.dtype) if taps else None
-    out = blk.forward(xd, to_dev(w), taps=tb)
+    wd = to_dev(w)
+    if prepared:
+        wd = blk.prepare(wd)
+    out = blk.forward(xd, wd, taps=tb)
     torch.cuda.synchronize()
     assert blk.last_status() == 0
     ref = oracle.block_forward(cfg_of(wl), weights_np(w), np64(x))
@@ -86,9 +89,10 @@ def test_tiny_f32_block(gain_std):
 
 # ------------------------------------------------------------------ bf16 prefill
 
+@pytest.mark.parametrize("prepared", [False, True], ids=["bf16_weights", "prepared_fp16"])
 @pytest.mark.parametrize("wl", SMALL_BF16, ids=lambda w: w.name)
-def test_bf16_block_small(wl):
-    out, tb, ref, x = _run(wl, gain_std=0.1 if wl.qk_norm else 0.0, taps=True)
+def test_bf16_block_small(wl, prepared):
+    out, tb, ref, x = _run(wl, gain_std=0.1 if wl.qk_norm else 0.0, taps=True, prepared=prepared)
     err = rel_err(out, ref["layer_output"])
     floor = bf16_floor(ref["layer_output"])
     print(f"{wl.name}: layer_output {err:.4f} (bf16 storage floor {floor:.4f})")
@@ -267,3 +271,13 @@ def test_forward_graph_decode_bumps_lens_each_replay():
     # the second replay decoded the same token at position lens + 1
     assert rel_err(out[:, 0], ref["layer_output"]) <= TOL["bf16"]
     g.close()
+
+
+def test_prepare_rejects_weights_outside_fp16():
+    from llama_family_decoder_gb300 import BlkError
+    wl = SMALL_BF16[0]
+    w = to_dev(make_weights(wl))
+    w["up_proj"][3, 7] = 1e5  # beyond fp16's 65504
+    blk = DecoderBlock.from_workload(wl)
+    with pytest.raises(BlkError, match="fp16 range"):
+        blk.prepare(w)
