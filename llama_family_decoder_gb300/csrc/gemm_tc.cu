@@ -163,6 +163,16 @@ __device__ __forceinline__ void store16_2b(void* dst, const float* v, bool f16) 
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+// e^x - 1 for x <= 0 to well within bf16 output precision: the Taylor series
+// x + x^2/2! + ... + x^5/5! near 0 (truncation below 1e-9 relative for |x| < 1/16),
+// 2^(x log2 e) - 1 on the MUFU unit elsewhere (|e^x - 1| >= 0.06 there).
+__device__ __forceinline__ float expm1_nonpos(float x) {
+  const float taylor = x * fmaf(x, fmaf(x, fmaf(x, fmaf(x, 1.0f / 120.0f, 1.0f / 24.0f), 1.0f / 6.0f), 0.5f), 1.0f);
+  float e2;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e2) : "f"(x * 1.4426950408889634f));
+  return x > -0.0625f ? taylor : e2 - 1.0f;
+}
+
 // Per-row RMSNorm factor rsqrt(mean(row^2) + eps) from an accumulated sum of squares.
 // The partial sums of a row (one per producer tile) are added in a fixed order: deterministic.
 __device__ __forceinline__ float row_norm_factor(const TcEpiArgs& e, int row, bool row_ok) {
@@ -341,7 +351,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
             const float ap = e.alpha_p, an = e.alpha_n, be = e.beta, xe = e.xeps;
             store_bf16_row(out + cc, vv, nv, [=](float x, int) {
               x *= r2;
-              return x > 0.0f ? ap * x * x + be * x : an * (expm1f(fminf(x, xe)) - x) + be * x;
+              return x > 0.0f ? ap * x * x + be * x : an * (expm1_nonpos(fminf(x, xe)) - x) + be * x;
             });
           } else if constexpr (EPI == (int)Epi::kResid) {
             // residual stream carried in fp32: out = resid + acc, rounded once
