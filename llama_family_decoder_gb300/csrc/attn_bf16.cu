@@ -1,15 +1,17 @@
 // bf16 decode attention over a KV cache ("LlamaForCausalLM-32L-4096d" sheet:
 // softmax(q @ k.T / sqrt(128)) @ v, per head; "arcee", "Grouped-query
 // attention, 128-wide heads": query head h reads KV head h / (H / Hkv)).
-// HBM-bound: K/V tiles of 64 keys stream through a double-buffered,
-// XOR-swizzled shared-memory ring (cp.async, zero-filled past the valid keys);
-// the small products run on bf16 mma.sync with fp32 accumulation and an
-// online softmax (running max and sum in the log2 domain).
+// HBM-bound: a persistent kernel whose producer warp streams K/V tiles of 64
+// keys through a 4-stage TMA ring (128-byte swizzle); the small products run
+// on bf16 mma.sync with fp32 accumulation and an online softmax (running max
+// and sum in the log2 domain).
 //
-// One query per sequence; a CTA takes one (sequence, KV head, key
-// split), puts the G = H/Hkv query heads of the group on the MMA's rows, and
-// its four warps each own 16 keys of every 64-key tile (their partial softmax
-// states merge at the end). Splits are merged by a second small kernel.
+// One query per sequence; a work unit is (sequence, KV head, key split of
+// about 512 keys): the G = H/Hkv query heads of the group sit on the MMA's
+// rows, and the four compute warps each own 16 keys of every tile (their
+// partial softmax states merge at the end of the unit). Splits are merged by
+// a second small kernel.
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -20,23 +22,8 @@ namespace blk {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kRowBytes = kD * 2;
 constexpr int kTileKeys = 64;
 constexpr float kLog2e = 1.4426950408889634f;
-
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return (uint32_t)(row * kRowBytes + ((chunk ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -57,190 +44,287 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Loads rows [0, rows) of a [*, 128] bf16 matrix into a swizzled smem tile;
-// rows >= valid are zero-filled (the source address is clamped in bounds).
-template <int ROWS, int THREADS>
-__device__ __forceinline__ void load_tile(uint32_t s_base, const __nv_bfloat16* g, int valid) {
-  constexpr int kChunks = ROWS * 16;
-#pragma unroll
-  for (int i = 0; i < (kChunks + THREADS - 1) / THREADS; ++i) {
-    const int idx = threadIdx.x + i * THREADS;
-    if (kChunks % THREADS == 0 || idx < kChunks) {
-      const int r = idx >> 4, ch = idx & 15;
-      const bool ok = r < valid;
-      const __nv_bfloat16* src = g + (size_t)(ok ? r : 0) * kD + ch * 8;
-      cp_async16(s_base + swz(r, ch), src, ok);
-    }
-  }
-}
-
 // ------------------------------------------------------------------ decode
 
-constexpr int kDWarps = 4;
-constexpr int kDThreads = kDWarps * 32;
-constexpr int kDSmem = 16 * kRowBytes + 4 * kTileKeys * kRowBytes;  // Q (16 rows) + 2x(K,V)
+constexpr int kStages = 4;                       // TMA ring depth (tiles of 64 keys)
+constexpr int kHalfBytes = kTileKeys * 128;      // one 64-column half of a 64-key tile (8 KB)
+constexpr int kStageBytes = 4 * kHalfBytes;      // K and V, two halves each (32 KB)
+constexpr int kCompute = 4;                      // compute warps; warp 4 is the TMA producer
+constexpr int kThreads = (kCompute + 1) * 32;
+constexpr int kMergeFloats = 2 * 64 + kCompute * 16 * kD;
+constexpr int kSmem = 1024 + kStages * kStageBytes + kMergeFloats * 4 + 128;
+constexpr unsigned long long kDrainNs = 2000000000ULL;
 
-__global__ void __launch_bounds__(kDThreads) attn_decode_kernel(
-    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-    float* __restrict__ ws_ml, float* __restrict__ ws_o, int H, int Hkv, int kv_stride, const int* __restrict__ kv_lens,
-    int len_add, int chunk, int splits) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK0 = sQ + 16 * kRowBytes;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int G = H / Hkv;
+struct DecodeParams {
+  CUtensorMap tk, tv;  // [B * Hkv * kv_stride, 128] bf16, boxes of 64 x 64, 128-byte swizzle
+  const __nv_bfloat16* q;
+  float* ws_ml;
+  float* ws_o;
+  const int* kv_lens;
+  int len_add, H, Hkv, kv_stride, chunk, splits, units;
+  DevStatus* status;
+  unsigned long long wait_ns;
+};
+
+// Byte offset of (row, 16-byte chunk C of 16) in a tile written by TMA with the
+// 128-byte swizzle: two 64-column halves, rows of 128 bytes, chunks XOR (row & 7).
+__device__ __forceinline__ uint32_t tsw(int row, int C) {
+  return (uint32_t)((C >> 3) * kHalfBytes + row * 128 + (((C & 7) ^ (row & 7)) << 4));
+}
+
+struct DecodeUnit {
+  int b, kvh, split, k0, n_keys, n_tiles;
+};
+
+__device__ __forceinline__ DecodeUnit decode_unit(const DecodeParams& p, int u) {
+  DecodeUnit r;
+  r.split = u % p.splits;
+  r.kvh = (u / p.splits) % p.Hkv;
+  r.b = u / (p.splits * p.Hkv);
+  const int kv_len = min(p.kv_lens[r.b] + p.len_add, p.kv_stride);  // never read past the cache
+  r.k0 = r.split * p.chunk;
+  r.n_keys = max(0, min(kv_len, r.k0 + p.chunk) - r.k0);
+  r.n_tiles = (r.n_keys + kTileKeys - 1) / kTileKeys;
+  return r;
+}
+
+// Persistent split-KV decode attention: each CTA walks the units (sequence, KV
+// head, key split) blockIdx.x, blockIdx.x + gridDim.x, ...; its producer warp
+// streams every unit's K/V tiles through a 4-stage TMA ring without pausing
+// between units, and the 4 compute warps each own 16 keys of every tile.
+__global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  float* merge = reinterpret_cast<float*>(ring + kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(merge + kMergeFloats);
+  // full[kStages], empty[kStages], csync
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages + 1);
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[kStages + s]); };
+  const uint32_t csync = smem_u32(&bars[2 * kStages]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tq = lane & 3;
-  const int kv_len = min(kv_lens[b] + len_add, kv_stride);  // never read past the cache
-  const int k_begin = split * chunk;
-  const int k_end = min(kv_len, k_begin + chunk);
-  const int n_keys = max(0, k_end - k_begin);
-  const int n_tiles = (n_keys + kTileKeys - 1) / kTileKeys;
+  const int G = p.H / p.Hkv;
+  const unsigned long long budget = p.wait_ns;
 
-  const __nv_bfloat16* qg = q + ((size_t)b * H + (size_t)kvh * G) * kD;
-  const __nv_bfloat16* kg = k + (((size_t)b * Hkv + kvh) * kv_stride + k_begin) * kD;
-  const __nv_bfloat16* vg = v + (((size_t)b * Hkv + kvh) * kv_stride + k_begin) * kD;
-  auto kbuf = [&](int i) { return sK0 + (uint32_t)((i & 1) * 2 * kTileKeys * kRowBytes); };
-  auto vbuf = [&](int i) { return kbuf(i) + (uint32_t)(kTileKeys * kRowBytes); };
-
-  load_tile<16, kDThreads>(sQ, qg, G);
-  if (n_tiles > 0) {
-    load_tile<kTileKeys, kDThreads>(kbuf(0), kg, n_keys);
-    load_tile<kTileKeys, kDThreads>(vbuf(0), vg, n_keys);
-  }
-  cp_async_commit();
-
-  uint32_t qf[8][4];
-  float acc[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-  const float sl2 = kLog2e * rsqrtf((float)kD);
-
-  for (int it = 0; it < n_tiles; ++it) {
-    if (it + 1 < n_tiles) {
-      const int n1 = (it + 1) * kTileKeys;
-      load_tile<kTileKeys, kDThreads>(kbuf(it + 1), kg + (size_t)n1 * kD, n_keys - n1);
-      load_tile<kTileKeys, kDThreads>(vbuf(it + 1), vg + (size_t)n1 * kD, n_keys - n1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(full(st), 1);
+      mbar_init(empty(st), kCompute);
     }
-    __syncthreads();
-    if (it == 0) {
+    mbar_init(csync, kCompute * 32);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kCompute) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      tma_prefetch_desc(&p.tk);
+      tma_prefetch_desc(&p.tv);
+      int stage = 0;
+      uint32_t ph = 0, issued = 0, parity = 0;
+      bool failed = false;
+      for (int u = blockIdx.x; u < p.units && !failed; u += gridDim.x) {
+        const DecodeUnit un = decode_unit(p, u);
+        const int row0 = (un.b * p.Hkv + un.kvh) * p.kv_stride + un.k0;
+        for (int t = 0; t < un.n_tiles; ++t) {
+          if (!mbar_wait(empty(stage), ph ^ 1, budget, abort_flag)) {
+            failed = true;
+            break;
+          }
+          const uint32_t dst = smem_u32(ring + stage * kStageBytes);
+          mbar_arrive_expect_tx(full(stage), kStageBytes);
+          const int row = row0 + t * kTileKeys;
+          tma_load_2d(dst, &p.tk, 0, row, full(stage));
+          tma_load_2d(dst + kHalfBytes, &p.tk, 64, row, full(stage));
+          tma_load_2d(dst + 2 * kHalfBytes, &p.tv, 0, row, full(stage));
+          tma_load_2d(dst + 3 * kHalfBytes, &p.tv, 64, row, full(stage));
+          issued |= 1u << stage;
+          parity = (parity & ~(1u << stage)) | (ph << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (failed) {
+        *abort_flag = 1;
+        report_timeout(p.status, 0x30);
+        volatile int never = 0;
+        for (int st = 0; st < kStages; ++st)
+          if (issued & (1u << st)) mbar_wait(full(st), (parity >> st) & 1, kDrainNs, &never);
+      }
+    }
+    return;
+  }
+
+  // ---------------- compute warps 0..3
+  const int g = lane >> 2, tq = lane & 3;
+  const float sl2 = kLog2e * rsqrtf((float)kD);
+  int stage = 0, n_sync = 0;
+  uint32_t ph = 0;
+  bool failed = false;
+  auto csync_all = [&]() {  // the 128 compute threads meet (bounded)
+    mbar_arrive(csync);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(csync, n_sync & 1, budget, abort_flag));
+    ++n_sync;
+    return ok;
+  };
+  for (int u = blockIdx.x; u < p.units && !failed; u += gridDim.x) {
+    const DecodeUnit un = decode_unit(p, u);
+    // Q fragments straight from global memory: rows = the group's heads (zero past G)
+    const __nv_bfloat16* qg = p.q + ((size_t)un.b * p.H + (size_t)un.kvh * G) * kD;
+    uint32_t qf[8][4];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int c = kk * 16 + 2 * tq;
+      qf[kk][0] = g < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)g * kD + c) : 0u;
+      qf[kk][1] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)(g + 8) * kD + c) : 0u;
+      qf[kk][2] = g < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)g * kD + c + 8) : 0u;
+      qf[kk][3] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)(g + 8) * kD + c + 8) : 0u;
+    }
+    float acc[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+    for (int t = 0; t < un.n_tiles; ++t) {
+      if (!__all_sync(0xffffffffu, mbar_wait(full(stage), ph, budget, abort_flag))) {
+        failed = true;
+        break;
+      }
+      const uint32_t sK = smem_u32(ring + stage * kStageBytes), sV = sK + 2 * kHalfBytes;
+      const int n0 = t * kTileKeys + warp * 16;  // this warp's 16 keys (within the unit)
+      const int valid = un.n_keys - n0;           // < 16: the rest of this warp's V rows are stale
+      if (valid < 16) {
+        // cache slots past the valid keys may hold anything: zero this warp's stale V rows
+        uint8_t* vb = ring + stage * kStageBytes + 2 * kHalfBytes;
+        for (int i = lane; i < 16 * 16; i += 32) {
+          const int rr = i >> 4, C = i & 15;
+          if (rr >= valid) *reinterpret_cast<uint4*>(vb + tsw(warp * 16 + rr, C)) = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const int mi = lane >> 3, rr = lane & 7;
-        ldsm_x4(sQ + swz(rr + 8 * (mi & 1), kk * 2 + (mi >> 1)), qf[kk]);
+        uint32_t bb[4];
+        ldsm_x4(sK + tsw(warp * 16 + rr + 8 * (mi >> 1), kk * 2 + (mi & 1)), bb);
+        mma_bf16(sc[0], qf[kk], bb[0], bb[1]);
+        mma_bf16(sc[1], qf[kk], bb[2], bb[3]);
+      }
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float x = sc[j][e] * sl2;
+          if (j * 8 + 2 * tq + (e & 1) >= valid) x = -INFINITY;
+          sc[j][e] = x;
+          mx[e >> 1] = fmaxf(mx[e >> 1], x);
+        }
+      float alpha[2], mu[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        const float mnew = fmaxf(mrow[r], mx[r]);
+        mu[r] = mnew == -INFINITY ? 0.f : mnew;
+        alpha[r] = exp2f(mrow[r] - mu[r]);
+        mrow[r] = mnew;
+        lrow[r] *= alpha[r];
+      }
+      uint32_t a[4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float p0 = exp2f(sc[j][0] - mu[0]), p1 = exp2f(sc[j][1] - mu[0]);
+        const float p2 = exp2f(sc[j][2] - mu[1]), p3 = exp2f(sc[j][3] - mu[1]);
+        lrow[0] += p0 + p1;
+        lrow[1] += p2 + p3;
+        a[j * 2 + 0] = pack_bf16x2(p0, p1);
+        a[j * 2 + 1] = pack_bf16x2(p2, p3);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        acc[i][0] *= alpha[0];
+        acc[i][1] *= alpha[0];
+        acc[i][2] *= alpha[1];
+        acc[i][3] *= alpha[1];
+      }
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        const int mi = lane >> 3, rr = lane & 7;
+        uint32_t bb[4];
+        ldsm_x4_t(sV + tsw(warp * 16 + rr + 8 * (mi & 1), dp * 2 + (mi >> 1)), bb);
+        mma_bf16(acc[2 * dp], a, bb[0], bb[1]);
+        mma_bf16(acc[2 * dp + 1], a, bb[2], bb[3]);
+      }
+      if (valid < 16) fence_proxy_async_smem();  // generic writes before the next TMA into this stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(stage));
+      if (++stage == kStages) {
+        stage = 0;
+        ph ^= 1;
       }
     }
-    const int n0 = it * kTileKeys + warp * 16;  // this warp's 16 keys (relative to k_begin)
-    const uint32_t sK = kbuf(it), sV = vbuf(it);
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int mi = lane >> 3, rr = lane & 7;
-      uint32_t bb[4];
-      ldsm_x4(sK + swz(warp * 16 + rr + 8 * (mi >> 1), kk * 2 + (mi & 1)), bb);
-      mma_bf16(s[0], qf[kk], bb[0], bb[1]);
-      mma_bf16(s[1], qf[kk], bb[2], bb[3]);
-    }
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float x = s[j][e] * sl2;
-        const int key = n0 + j * 8 + 2 * tq + (e & 1);
-        if (key >= n_keys) x = -INFINITY;
-        s[j][e] = x;
-        mx[e >> 1] = fmaxf(mx[e >> 1], x);
-      }
-    float alpha[2], mu[2];
+    if (failed) break;
+    // merge the four warps' softmax states (rows < G) and write this split's partial
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      const float mnew = fmaxf(mrow[r], mx[r]);
-      mu[r] = mnew == -INFINITY ? 0.f : mnew;
-      alpha[r] = exp2f(mrow[r] - mu[r]);
-      mrow[r] = mnew;
-      lrow[r] *= alpha[r];
+      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
+      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
     }
-    uint32_t a[4];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float p0 = exp2f(s[j][0] - mu[0]), p1 = exp2f(s[j][1] - mu[0]);
-      const float p2 = exp2f(s[j][2] - mu[1]), p3 = exp2f(s[j][3] - mu[1]);
-      lrow[0] += p0 + p1;
-      lrow[1] += p2 + p3;
-      a[j * 2 + 0] = pack_bf16x2(p0, p1);
-      a[j * 2 + 1] = pack_bf16x2(p2, p3);
+    float* sm_m = merge;
+    float* sm_l = merge + 64;
+    float* sm_o = merge + 128;
+    if (tq == 0) {
+      sm_m[warp * 16 + g] = mrow[0];
+      sm_m[warp * 16 + g + 8] = mrow[1];
+      sm_l[warp * 16 + g] = lrow[0];
+      sm_l[warp * 16 + g + 8] = lrow[1];
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      acc[i][0] *= alpha[0];
-      acc[i][1] *= alpha[0];
-      acc[i][2] *= alpha[1];
-      acc[i][3] *= alpha[1];
+    for (int dt = 0; dt < 16; ++dt) {
+      const int c = dt * 8 + 2 * tq;
+      sm_o[(warp * 16 + g) * kD + c] = acc[dt][0];
+      sm_o[(warp * 16 + g) * kD + c + 1] = acc[dt][1];
+      sm_o[(warp * 16 + g + 8) * kD + c] = acc[dt][2];
+      sm_o[(warp * 16 + g + 8) * kD + c + 1] = acc[dt][3];
     }
+    if (!csync_all()) {
+      failed = true;
+      break;
+    }
+    for (int idx = threadIdx.x; idx < G * kD; idx += kCompute * 32) {
+      const int r = idx / kD, c = idx - r * kD;
+      float m = -INFINITY;
 #pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      const int mi = lane >> 3, rr = lane & 7;
-      uint32_t bb[4];
-      ldsm_x4_t(sV + swz(warp * 16 + rr + 8 * (mi & 1), dp * 2 + (mi >> 1)), bb);
-      mma_bf16(acc[2 * dp], a, bb[0], bb[1]);
-      mma_bf16(acc[2 * dp + 1], a, bb[2], bb[3]);
+      for (int w = 0; w < kCompute; ++w) m = fmaxf(m, sm_m[w * 16 + r]);
+      const float mu = m == -INFINITY ? 0.f : m;
+      float l = 0.f, oo = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCompute; ++w) {
+        const float f = exp2f(sm_m[w * 16 + r] - mu);
+        l += sm_l[w * 16 + r] * f;
+        oo += sm_o[(w * 16 + r) * kD + c] * f;
+      }
+      const size_t hs = ((size_t)un.b * p.H + (size_t)un.kvh * G + r) * p.splits + un.split;
+      p.ws_o[hs * kD + c] = oo;
+      if (c == 0) {
+        p.ws_ml[hs * 2 + 0] = m;
+        p.ws_ml[hs * 2 + 1] = l;
+      }
     }
-    __syncthreads();
+    if (!csync_all()) {  // the merge buffer is reused by the next unit
+      failed = true;
+      break;
+    }
   }
-  cp_async_wait<0>();  // the Q copy is still in flight when the split is empty
-  // merge the four warps' states (rows < G) through shared memory
-  float* sm = reinterpret_cast<float*>(smem + 16 * kRowBytes);  // reuse the K/V ring
-  float* sm_m = sm;                    // [4][16]
-  float* sm_l = sm + 64;               // [4][16]
-  float* sm_o = sm + 128;              // [4][16][128]
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-  }
-  __syncthreads();
-  if (tq == 0) {
-    sm_m[warp * 16 + g] = mrow[0];
-    sm_m[warp * 16 + g + 8] = mrow[1];
-    sm_l[warp * 16 + g] = lrow[0];
-    sm_l[warp * 16 + g + 8] = lrow[1];
-  }
-#pragma unroll
-  for (int dt = 0; dt < 16; ++dt) {
-    const int c = dt * 8 + 2 * tq;
-    sm_o[(warp * 16 + g) * kD + c] = acc[dt][0];
-    sm_o[(warp * 16 + g) * kD + c + 1] = acc[dt][1];
-    sm_o[(warp * 16 + g + 8) * kD + c] = acc[dt][2];
-    sm_o[(warp * 16 + g + 8) * kD + c + 1] = acc[dt][3];
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < G * kD; idx += kDThreads) {
-    const int r = idx / kD, c = idx - r * kD;
-    float m = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDWarps; ++w) m = fmaxf(m, sm_m[w * 16 + r]);
-    const float mu = m == -INFINITY ? 0.f : m;
-    float l = 0.f, oo = 0.f;
-#pragma unroll
-    for (int w = 0; w < kDWarps; ++w) {
-      const float f = exp2f(sm_m[w * 16 + r] - mu);
-      l += sm_l[w * 16 + r] * f;
-      oo += sm_o[(w * 16 + r) * kD + c] * f;
-    }
-    const size_t hs = ((size_t)b * H + (size_t)kvh * G + r) * splits + split;
-    ws_o[hs * kD + c] = oo;
-    if (c == 0) {
-      ws_ml[hs * 2 + 0] = m;
-      ws_ml[hs * 2 + 1] = l;
-    }
+  if (failed) {
+    *abort_flag = 1;
+    if (lane == 0) report_timeout(p.status, 0x31);
   }
 }
 
@@ -262,11 +346,13 @@ __global__ void attn_decode_combine_kernel(const float* __restrict__ ws_ml, cons
 
 }  // namespace
 
+// Splits of about 512 keys (8 tiles): fine-grained units that the persistent
+// CTAs share evenly.
 int attn_decode_splits(int B, int Hkv, int max_len, int num_sms) {
-  const int units = B * Hkv;
-  int splits = (3 * num_sms + units - 1) / units;  // about three resident CTAs per SM
-  const int max_by_len = (max_len + kTileKeys - 1) / kTileKeys;
-  if (splits > max_by_len) splits = max_by_len;
+  (void)B;
+  (void)Hkv;
+  (void)num_sms;
+  int splits = (max_len + 511) / 512;
   if (splits < 1) splits = 1;
   if (splits > 64) splits = 64;
   return splits;
@@ -276,9 +362,53 @@ size_t attn_decode_ws_bytes(int B, int H, int d, int max_splits) {
   return (size_t)B * H * max_splits * (2 + d) * sizeof(float);
 }
 
+namespace {
+
+cudaError_t decode_core(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int kv_stride,
+                        const int* kv_lens, int len_add, int splits, int max_len, float* ws, int num_sms,
+                        DevStatus* st, unsigned long long wait_ns, cudaStream_t s, const char** why) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  DecodeParams p;
+  memset(static_cast<void*>(&p), 0, sizeof(p));
+  if (!make_tma_2d_16b(&p.tk, k, B * Hkv * kv_stride, kD, kTileKeys, false) ||
+      !make_tma_2d_16b(&p.tv, v, B * Hkv * kv_stride, kD, kTileKeys, false)) {
+    *why = "cuTensorMapEncodeTiled failed for the KV cache";
+    return cudaErrorInvalidValue;
+  }
+  int chunk = (max_len + splits - 1) / splits;
+  chunk = (chunk + kTileKeys - 1) / kTileKeys * kTileKeys;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.ws_ml = ws;
+  p.ws_o = ws + (size_t)B * H * splits * 2;
+  p.kv_lens = kv_lens;
+  p.len_add = len_add;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.kv_stride = kv_stride;
+  p.chunk = chunk;
+  p.splits = splits;
+  p.units = B * Hkv * splits;
+  p.status = st;
+  p.wait_ns = wait_ns;
+  const int grid = p.units < num_sms ? p.units : num_sms;
+  attn_decode_kernel<<<grid, kThreads, kSmem, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_decode_combine_kernel<<<dim3(H, B), kD, 0, s>>>(p.ws_ml, p.ws_o, static_cast<__nv_bfloat16*>(o), H, splits);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_attn_decode_bf16(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv,
-                                    int d, int kv_stride, const int* kv_lens, int len_add, int max_len, void* ws,
-                                    int num_sms, cudaStream_t s, const char** why) {
+                                    int d, int kv_stride, const int* kv_lens, int len_add, int max_len,
+                                    int split_cap, void* ws, int num_sms, DevStatus* st, unsigned long long wait_ns,
+                                    cudaStream_t s, const char** why) {
   if (d != kD) {
     *why = "bf16 attention: head_dim must be 128";
     return cudaErrorInvalidValue;
@@ -288,26 +418,11 @@ cudaError_t launch_attn_decode_bf16(const void* q, const void* k, const void* v,
     return cudaErrorInvalidValue;
   }
   if (B <= 0) return cudaSuccess;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   // max_len: upper bound of the keys per sequence this step (lens + len_add)
-  const int splits = attn_decode_splits(B, Hkv, max_len, num_sms);
-  int chunk = (max_len + splits - 1) / splits;
-  chunk = (chunk + kTileKeys - 1) / kTileKeys * kTileKeys;
-  float* ws_ml = static_cast<float*>(ws);
-  float* ws_o = ws_ml + (size_t)B * H * splits * 2;
-  dim3 grid(splits, Hkv, B);
-  attn_decode_kernel<<<grid, kDThreads, kDSmem, s>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), ws_ml, ws_o, H, Hkv, kv_stride, kv_lens, len_add, chunk, splits);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  attn_decode_combine_kernel<<<dim3(H, B), kD, 0, s>>>(ws_ml, ws_o, static_cast<__nv_bfloat16*>(o), H, splits);
-  return cudaGetLastError();
+  int splits = attn_decode_splits(B, Hkv, max_len, num_sms);
+  if (splits > split_cap) splits = split_cap;  // the workspace holds split_cap splits: chunks grow instead
+  return decode_core(q, k, v, o, B, H, Hkv, kv_stride, kv_lens, len_add, splits, max_len, static_cast<float*>(ws),
+                     num_sms, st, wait_ns, s, why);
 }
 
 // ------------------------------------------------------------------ allocation-free decode variant
@@ -365,28 +480,12 @@ cudaError_t launch_attn_decode_bf16_static(const void* q, const void* k, const v
     *why = "cudaGetSymbolAddress of the decode scratch failed";
     return e;
   }
-  static bool configured = false;
-  if (!configured) {
-    e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   int splits = attn_decode_splits(B, Hkv, kv_stride, num_sms);
   const int fit = (int)(kDecodeStaticScratchBytes / per_split);
   if (splits > fit) splits = fit;
-  int chunk = (kv_stride + splits - 1) / splits;
-  chunk = (chunk + kTileKeys - 1) / kTileKeys * kTileKeys;
   // every partial the combine step reads is written by this call first: nothing to clear
-  float* ws_ml = scratch;
-  float* ws_o = ws_ml + (size_t)B * H * splits * 2;
-  dim3 grid(splits, Hkv, B);
-  attn_decode_kernel<<<grid, kDThreads, kDSmem, s>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), ws_ml, ws_o, H, Hkv, kv_stride, kv_lens, 0, chunk, splits);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  attn_decode_combine_kernel<<<dim3(H, B), kD, 0, s>>>(ws_ml, ws_o, static_cast<__nv_bfloat16*>(o), H, splits);
-  return cudaGetLastError();
+  return decode_core(q, k, v, o, B, H, Hkv, kv_stride, kv_lens, 0, splits, kv_stride, scratch, num_sms, nullptr,
+                     2000000000ULL, s, why);
 }
 
 }  // namespace blk

@@ -162,7 +162,7 @@ Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, siz
     const int splits = d.dtype == BLK_BF16 ? kMaxDecodeSplits : 1;
     w.C = c.take((size_t)splits * M * max_cols(d) * sizeof(float));
     if (d.dtype == BLK_BF16) {
-      const int s = attn_decode_splits(B, d.n_kv_heads, 1 << 30, h->num_sms);
+      const int s = attn_decode_splits(B, d.n_kv_heads, d.max_seq, h->num_sms);
       w.attn = c.take(attn_decode_ws_bytes(B, d.n_heads, d.head_dim, s));
     }
   } else if (d.dtype == BLK_F32) {
@@ -448,7 +448,9 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
   prof_mark(h, "attention_splitkv", 2, s);
   const char* why = nullptr;
   cudaError_t e = launch_attn_decode_bf16(q, cache->k, cache->v, o, B, d.n_heads, d.n_kv_heads, d.head_dim,
-                                          cache->capacity, cache->lens, 1, max_len, ws.attn, h->num_sms, s, &why);
+                                          cache->capacity, cache->lens, 1, max_len,
+                                          attn_decode_splits(B, d.n_kv_heads, d.max_seq, h->num_sms), ws.attn,
+                                          h->num_sms, h->status, (unsigned long long)g_wait_ns.load(), s, &why);
   BLK_TRY(check_cuda(e, "decode attention", why));
   prof_mark(h, "o_proj_gemm", 1, s);
   {
@@ -808,7 +810,7 @@ size_t blk_stage_workspace_bytes(const blk_handle* h, int rows) {
   Carve c(nullptr);
   c.take((size_t)rows * d.ffn * esize(d));                              // neurons
   c.take((size_t)rows * max_cols(d) * sizeof(float));                   // fp32 GEMM output
-  const int s = attn_decode_splits(rows, d.n_kv_heads, 1 << 30, h->num_sms);
+  const int s = attn_decode_splits(rows, d.n_kv_heads, d.max_seq, h->num_sms);
   c.take(attn_decode_ws_bytes(rows, d.n_heads, d.head_dim, s));         // decode attention partials
   return c.off;
 }
@@ -867,7 +869,8 @@ blk_status blk_attn_gqa(blk_handle* h, const void* q, const void* k, const void*
   c.take((size_t)batch * max_cols(d) * sizeof(float));
   void* aw = c.take(0);
   return check_cuda(launch_attn_decode_bf16(q, k, v, o, batch, d.n_heads, d.n_kv_heads, d.head_dim, kv_stride, kv_lens,
-                                            0, kv_stride, aw, h->num_sms, s, &why),
+                                            0, kv_stride, attn_decode_splits(batch, d.n_kv_heads, d.max_seq, h->num_sms),
+                                            aw, h->num_sms, h->status, (unsigned long long)g_wait_ns.load(), s, &why),
                     "decode attention", why);
 }
 

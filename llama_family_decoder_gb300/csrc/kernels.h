@@ -160,10 +160,12 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
 
 // Decode (Tq == 1), split over the keys: partial results in ws, combined into o.
 size_t attn_decode_ws_bytes(int B, int H, int d, int max_splits);
-// Keys per sequence: kv_lens[b] + len_add (<= max_len, which sizes the splits).
+// Keys per sequence: kv_lens[b] + len_add (<= max_len, which sizes the splits; at most
+// split_cap of them, the number ws holds).
 cudaError_t launch_attn_decode_bf16(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv,
-                                    int d, int kv_stride, const int* kv_lens, int len_add, int max_len, void* ws,
-                                    int num_sms, cudaStream_t s, const char** why);
+                                    int d, int kv_stride, const int* kv_lens, int len_add, int max_len,
+                                    int split_cap, void* ws, int num_sms, DevStatus* st, unsigned long long wait_ns,
+                                    cudaStream_t s, const char** why);
 int attn_decode_splits(int B, int Hkv, int max_len, int num_sms);
 
 // Decode attention with its split partials in a fixed file-scope device array
