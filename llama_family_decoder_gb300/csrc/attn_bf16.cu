@@ -93,6 +93,7 @@ __device__ __forceinline__ DecodeUnit decode_unit(const DecodeParams& p, int u) 
 // streams every unit's K/V tiles through a 4-stage TMA ring without pausing
 // between units, and the 4 compute warps each own 16 keys of every tile.
 __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();  // the new key/value rows and q come from the previous kernel
 
   if (warp == kCompute) {
     if (lane == 0) {
@@ -330,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
 
 __global__ void attn_decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__ ws_o,
                                            __nv_bfloat16* __restrict__ o, int H, int splits) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
   const size_t base = ((size_t)b * H + h) * splits;
   float m = -INFINITY;
@@ -396,10 +400,10 @@ cudaError_t decode_core(const void* q, const void* k, const void* v, void* o, in
   p.status = st;
   p.wait_ns = wait_ns;
   const int grid = p.units < num_sms ? p.units : num_sms;
-  attn_decode_kernel<<<grid, kThreads, kSmem, s>>>(p);
+  launch_pdl(attn_decode_kernel, grid, kThreads, kSmem, s, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_decode_combine_kernel<<<dim3(H, B), kD, 0, s>>>(p.ws_ml, p.ws_o, static_cast<__nv_bfloat16*>(o), H, splits);
+  launch_pdl(attn_decode_combine_kernel, dim3(H, B), kD, 0, s, p.ws_ml, p.ws_o, static_cast<__nv_bfloat16*>(o), H, splits);
   return cudaGetLastError();
 }
 

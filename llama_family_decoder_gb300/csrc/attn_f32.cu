@@ -14,6 +14,8 @@ namespace {
 __global__ void attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
                                 float* __restrict__ o, int H, int Hkv, int Tq, int d, int kv_stride,
                                 const int* __restrict__ kv_lens, int len_add) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ float sc[];
   const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x;
@@ -61,7 +63,7 @@ cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, floa
     if (e != cudaSuccess) return e;
   }
   dim3 grid(Tq, H, B);
-  attn_f32_kernel<<<grid, 32, smem, s>>>(q, k, v, o, H, Hkv, Tq, d, kv_stride, kv_lens, len_add);
+  launch_pdl(attn_f32_kernel, grid, 32, smem, s, q, k, v, o, H, Hkv, Tq, d, kv_stride, kv_lens, len_add);
   return cudaGetLastError();
 }
 

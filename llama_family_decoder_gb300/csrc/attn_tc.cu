@@ -68,6 +68,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
 // F16: q, k, v (and so P) are fp16; otherwise bf16. The output is bf16 either way.
 template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // q, k, v come from the previous kernel
   const uint32_t tmem = *tmem_holder;  // S0: cols [0,128), S1: [128,256), O: [256,384)
 
   if (warp == 0) {
@@ -377,9 +379,9 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
     configured[f16] = true;
   }
   if (f16)
-    attn_tc_kernel<true><<<p.n_qtiles * H * B, kThreads, kSmem, s>>>(p);
+    launch_pdl(attn_tc_kernel<true>, p.n_qtiles * H * B, kThreads, kSmem, s, p);
   else
-    attn_tc_kernel<false><<<p.n_qtiles * H * B, kThreads, kSmem, s>>>(p);
+    launch_pdl(attn_tc_kernel<false>, p.n_qtiles * H * B, kThreads, kSmem, s, p);
   return cudaGetLastError();
 }
 

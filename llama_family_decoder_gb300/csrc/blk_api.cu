@@ -237,6 +237,7 @@ blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, in
   static const int qkv_c[] = {256, 128};
   g.bn = whole256 ? choose_bn(B * T, qkv_cols(d), false, qkv_c, 2, h->num_sms) : 128;
   g.epi = Epi::kQkv;
+  g.const_op = 2;
   g.e = qkv_epi(h, w, T, pos0, q, k, v);
   g.e.row_scale = row_scale;
   g.e.qkv_f16 = f16 ? 1 : 0;
@@ -255,6 +256,7 @@ blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K
   g.K = K;
   g.bn = resid_bn(h, rows, N);
   g.epi = Epi::kResid;
+  g.const_op = 2;
   g.e.out = out;
   g.e.ldo = N;
   g.e.resid = resid;
@@ -303,6 +305,7 @@ blk_status bf16_mlp_up(const blk_handle* h, const void* y2, int rows, const blk_
     g.e.xeps = d.xielu_eps;
   }
   g.f16 = prep != nullptr;
+  g.const_op = 2;
   return tc(h, g, s, "MLP up GEMM");
 }
 
@@ -324,6 +327,7 @@ blk_status bf16_stream_gemm(const blk_handle* h, const TcSeg* segs, int nseg, co
   const int n_tiles = (B + g.bn - 1) / g.bn;
   g.k_splits = choose_splits(tiles * n_tiles, (K + 63) / 64, h->num_sms);
   g.epi = Epi::kPartialT;
+  g.const_op = 1;  // A = the weight segments
   g.e.out = C;
   g.e.part_ld = ldc;
   g.e.n_tok = B;

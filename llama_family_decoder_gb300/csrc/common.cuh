@@ -251,4 +251,35 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 
 __device__ __forceinline__ bool elect_one_lane() { return (threadIdx.x & 31) == 0; }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of a forward is launched with programmatic stream serialization:
+// it may start while its predecessor on the stream still runs, once every CTA of
+// the predecessor has called pdl_launch_dependents(). pdl_wait() then blocks
+// until the predecessor has completed and its writes are visible. A kernel reads
+// nothing a predecessor writes, and writes nothing a predecessor reads, before
+// pdl_wait(); it may read the constant weights, set up barriers, allocate TMEM and
+// prefetch descriptors before it. Because each kernel waits before it finishes,
+// the chain is transitive: kernel i+2 never overlaps kernel i's memory effects.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kern` on `s` with the programmatic-serialization attribute.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 }  // namespace blk

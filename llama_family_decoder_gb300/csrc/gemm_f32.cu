@@ -14,6 +14,8 @@ constexpr int kBK = 16;
 
 __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__ A, const float* __restrict__ B,
                                                        float* __restrict__ C, int ldc, int M, int N, int K) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ float As[kBK][kTile + 4];
   __shared__ float Bs[kBK][kTile + 4];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -60,7 +62,7 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__
 cudaError_t launch_gemm_f32(const float* A, const float* B, float* C, int ldc, int M, int N, int K, cudaStream_t s) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   dim3 grid((N + kTile - 1) / kTile, (M + kTile - 1) / kTile);
-  gemm_f32_kernel<<<grid, 256, 0, s>>>(A, B, C, ldc, M, N, K);
+  launch_pdl(gemm_f32_kernel, grid, 256, 0, s, A, B, C, ldc, M, N, K);
   return cudaGetLastError();
 }
 

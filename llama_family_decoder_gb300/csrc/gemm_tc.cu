@@ -87,6 +87,7 @@ struct TcParams {
   int na, nb;
   int b_paired;
   int f16;  // fp16 operands (else bf16)
+  int const_op;  // 1: A, 2: B is constant over the stream (may be loaded before pdl_wait)
   int num_kb;
   int k_splits;
   int m_tiles, n_tiles;
@@ -458,6 +459,7 @@ template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<BN>;
   constexpr int S = C::kStages;
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -510,22 +512,51 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       uint32_t ph = 0;
       uint32_t issued_mask = 0, parity_mask = 0;
       bool failed = false;
+      auto load_a = [&](int st, const Unit& un, int kb) {
+        tma_load_2d(smem_u32(sA + st * C::kABytes), &p.ta[un.a_seg], kb * kBK, un.a_row0, full_bar(st));
+      };
+      auto load_b = [&](int st, const Unit& un, int kb) {
+        const uint32_t b_dst = smem_u32(sB + st * C::kBBytes);
+        if (p.b_paired) {
+          tma_load_2d(b_dst, &p.tb[0], kb * kBK, un.b_row0, full_bar(st));
+          tma_load_2d(b_dst + (BN / 2) * kBK * 2, &p.tb[1], kb * kBK, un.b_row0, full_bar(st));
+        } else {
+          tma_load_2d(b_dst, &p.tb[un.b_seg], kb * kBK, un.b_row0, full_bar(st));
+        }
+      };
+      // The weights of the first unit's first stages are fetched while the
+      // previous kernel finishes; the activations only after pdl_wait().
+      int pre = 0;
+      if (p.const_op != 0 && blockIdx.x < p.num_units) {
+        const Unit un = decode_unit(p, blockIdx.x, bn_rows);
+        pre = min(S, un.kb_end - un.kb_begin);
+        for (int i = 0; i < pre; ++i) {  // fresh ring: every stage is free
+          mbar_arrive_expect_tx(full_bar(i), C::kStageBytes);
+          if (p.const_op == 1)
+            load_a(i, un, un.kb_begin + i);
+          else
+            load_b(i, un, un.kb_begin + i);
+          issued_mask |= 1u << i;
+        }
+      }
+      pdl_wait();
+      int g = 0;  // k-blocks issued by this CTA
       for (int u = blockIdx.x; u < p.num_units && !failed; u += gridDim.x) {
         const Unit un = decode_unit(p, u, bn_rows);
-        for (int kb = un.kb_begin; kb < un.kb_end; ++kb) {
-          if (!mbar_wait(empty_bar(stage), ph ^ 1, budget, abort_flag)) {
-            failed = true;
-            break;
-          }
-          mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
-          const uint32_t a_dst = smem_u32(sA + stage * C::kABytes);
-          const uint32_t b_dst = smem_u32(sB + stage * C::kBBytes);
-          tma_load_2d(a_dst, &p.ta[un.a_seg], kb * kBK, un.a_row0, full_bar(stage));
-          if (p.b_paired) {
-            tma_load_2d(b_dst, &p.tb[0], kb * kBK, un.b_row0, full_bar(stage));
-            tma_load_2d(b_dst + (BN / 2) * kBK * 2, &p.tb[1], kb * kBK, un.b_row0, full_bar(stage));
+        for (int kb = un.kb_begin; kb < un.kb_end; ++kb, ++g) {
+          if (g < pre) {  // the stage's constant half is already in flight
+            if (p.const_op == 1)
+              load_b(stage, un, kb);
+            else
+              load_a(stage, un, kb);
           } else {
-            tma_load_2d(b_dst, &p.tb[un.b_seg], kb * kBK, un.b_row0, full_bar(stage));
+            if (!mbar_wait(empty_bar(stage), ph ^ 1, budget, abort_flag)) {
+              failed = true;
+              break;
+            }
+            mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
+            load_a(stage, un, kb);
+            load_b(stage, un, kb);
           }
           issued_mask |= 1u << stage;
           parity_mask = (parity_mask & ~(1u << stage)) | (ph << stage);
@@ -601,6 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
   } else {
     // ---------------- epilogue warps 2..5: TMEM lane quarter = warp % 4
+    pdl_wait();  // the epilogue reads and writes activations of earlier kernels
     const int quarter = warp & 3;
     int it = 0;
     bool failed = false;
@@ -682,7 +714,7 @@ cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  tc_gemm_kernel<BN, EPI><<<grid, kThreads, C::kSmemBytes, s>>>(p);
+  launch_pdl(tc_gemm_kernel<BN, EPI>, grid, kThreads, C::kSmemBytes, s, p);
   return cudaGetLastError();
 }
 
@@ -762,6 +794,7 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
   }
   p.b_paired = d.b_paired ? 1 : 0;
   p.f16 = d.f16 ? 1 : 0;
+  p.const_op = d.const_op;
   p.m_tiles = p.a_tiles[d.na];
   p.n_tiles = d.b_paired ? (d.b[0].rows + bn_rows - 1) / bn_rows : p.b_tiles[d.nb];
   p.num_kb = (d.K + kBK - 1) / kBK;

@@ -106,7 +106,11 @@ struct TcGemmDesc {
   bool f16 = false;       // A and B are fp16 (else bf16)
   int K = 0;              // inner dimension; every segment has row stride K
   int k_splits = 1;
-  int bn = 256;           // 64, 128 or 256
+  int bn = 256;           // 64, 128, 192, 224 or 256
+  // Operand that no earlier kernel of the stream writes (the weights): 1 = A,
+  // 2 = B, 0 = none. Its first ring stages are loaded before the kernel waits
+  // for its predecessor (programmatic dependent launch).
+  int const_op = 0;
   Epi epi = Epi::kStore;
   TcEpiArgs e;
 };

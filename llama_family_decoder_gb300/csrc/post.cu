@@ -32,6 +32,8 @@ __global__ void post_qkv_kernel(const float* __restrict__ C, int splits, int row
                                 float eps, const float2* __restrict__ rope, int rope_max_pos, T* __restrict__ q,
                                 T* __restrict__ k,
                                 T* __restrict__ v, int kv_stride) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int r = blockIdx.x;
   if (r >= rows) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -148,6 +150,8 @@ __global__ void __launch_bounds__(kResidThreads) post_resid_kernel(
     const float* __restrict__ C, int splits, int rows, int n, int ldc, const TR* __restrict__ resid,
     TO* __restrict__ out, TY* __restrict__ out2, TY* __restrict__ tap, const TY* __restrict__ g, float eps,
     TY* __restrict__ y, int* __restrict__ bump_lens) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ float red[kResidThreads / 32];
   const int r = blockIdx.x;
   if (r >= rows) return;
@@ -205,6 +209,8 @@ __device__ __forceinline__ float act_one(int act, float gt, float u, float alpha
 template <typename T>
 __global__ void post_act4_kernel(const float* __restrict__ C, int splits, int rows, int F, int ldc, int act,
                                  float alpha_p, float alpha_n, float beta, float xeps, T* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int F4 = F / 4;
   const int total = rows * F4;
   const size_t sstride = (size_t)rows * ldc;
@@ -224,6 +230,8 @@ __global__ void post_act4_kernel(const float* __restrict__ C, int splits, int ro
 template <typename T>
 __global__ void post_act_kernel(const float* __restrict__ C, int splits, int rows, int F, int ldc, int act,
                                 float alpha_p, float alpha_n, float beta, float xeps, T* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const size_t total = (size_t)rows * F;
   const size_t sstride = (size_t)rows * ldc;
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
@@ -245,12 +253,12 @@ cudaError_t launch_post_qkv(const float* C, int splits, int rows, int ldc, int s
   if (d > 2 * 32 * kMaxPairsPerLane || d % 2) return cudaErrorInvalidValue;
   if (bf16) {
     using T = __nv_bfloat16;
-    post_qkv_kernel<T><<<dim3(rows, (H + 2 * Hkv + kQkvWarps - 1) / kQkvWarps), 32 * kQkvWarps, 0, s>>>(C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
+    launch_pdl(post_qkv_kernel<T>, dim3(rows, (H + 2 * Hkv + kQkvWarps - 1) / kQkvWarps), 32 * kQkvWarps, 0, s, C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
                                            static_cast<const T*>(q_gain), static_cast<const T*>(k_gain), eps, rope, rope_max_pos,
                                            static_cast<T*>(q), static_cast<T*>(k), static_cast<T*>(v), kv_stride);
   } else {
     using T = float;
-    post_qkv_kernel<T><<<dim3(rows, (H + 2 * Hkv + kQkvWarps - 1) / kQkvWarps), 32 * kQkvWarps, 0, s>>>(C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
+    launch_pdl(post_qkv_kernel<T>, dim3(rows, (H + 2 * Hkv + kQkvWarps - 1) / kQkvWarps), 32 * kQkvWarps, 0, s, C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
                                            static_cast<const T*>(q_gain), static_cast<const T*>(k_gain), eps, rope, rope_max_pos,
                                            static_cast<T*>(q), static_cast<T*>(k), static_cast<T*>(v), kv_stride);
   }
@@ -266,7 +274,7 @@ cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int l
   const int vpt = (nv + kResidThreads - 1) / kResidThreads;
   using B = __nv_bfloat16;
 #define BLK_POST_RESID_V(TR, TO, TY, V)                                                                        \
-  post_resid_kernel<TR, TO, TY, V><<<rows, kResidThreads, 0, s>>>(                                           \
+  launch_pdl(post_resid_kernel<TR, TO, TY, V>, rows, kResidThreads, 0, s,                                            \
       C, splits, rows, n, ldc, static_cast<const TR*>(resid), static_cast<TO*>(out), static_cast<TY*>(out2),  \
       static_cast<TY*>(tap), static_cast<const TY*>(g), eps, static_cast<TY*>(y), bump_lens)
 #define BLK_POST_RESID(TR, TO, TY)                  \
@@ -309,17 +317,17 @@ cudaError_t launch_post_act(const float* C, int splits, int rows, int F, int ldc
   if (grid > 8192) grid = 8192;
   if (vec) {
     if (bf16)
-      post_act4_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta,
+      launch_pdl(post_act4_kernel<__nv_bfloat16>, grid, 256, 0, s, C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta,
                                                            xeps, static_cast<__nv_bfloat16*>(out));
     else
-      post_act4_kernel<float><<<grid, 256, 0, s>>>(C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
+      launch_pdl(post_act4_kernel<float>, grid, 256, 0, s, C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
                                                    static_cast<float*>(out));
   } else {
     if (bf16)
-      post_act_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
+      launch_pdl(post_act_kernel<__nv_bfloat16>, grid, 256, 0, s, C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
                                                           static_cast<__nv_bfloat16*>(out));
     else
-      post_act_kernel<float><<<grid, 256, 0, s>>>(C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
+      launch_pdl(post_act_kernel<float>, grid, 256, 0, s, C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
                                                   static_cast<float*>(out));
   }
   return cudaGetLastError();

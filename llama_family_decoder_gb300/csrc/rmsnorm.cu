@@ -52,6 +52,8 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* p, const fl
 template <typename TX, typename TY, int NC>
 __global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const TX* __restrict__ x, const TY* __restrict__ g,
                                                            int rows, int n, float eps, TY* __restrict__ y) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ float red[kThreads / 32];
   const int nchunk = n / 8;
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -101,14 +103,14 @@ cudaError_t launch_t(const void* x, const void* g, int rows, int n, float eps, v
   auto G = static_cast<const TY*>(g);
   auto Y = static_cast<TY*>(y);
   switch (nc) {
-    case 1: rmsnorm_kernel<TX, TY, 1><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 2: rmsnorm_kernel<TX, TY, 2><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 3: rmsnorm_kernel<TX, TY, 3><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 4: rmsnorm_kernel<TX, TY, 4><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 5: rmsnorm_kernel<TX, TY, 5><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 6: rmsnorm_kernel<TX, TY, 6><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 7: rmsnorm_kernel<TX, TY, 7><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
-    case 8: rmsnorm_kernel<TX, TY, 8><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, Y); break;
+    case 1: launch_pdl(rmsnorm_kernel<TX, TY, 1>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 2: launch_pdl(rmsnorm_kernel<TX, TY, 2>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 3: launch_pdl(rmsnorm_kernel<TX, TY, 3>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 4: launch_pdl(rmsnorm_kernel<TX, TY, 4>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 5: launch_pdl(rmsnorm_kernel<TX, TY, 5>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 6: launch_pdl(rmsnorm_kernel<TX, TY, 6>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 7: launch_pdl(rmsnorm_kernel<TX, TY, 7>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 8: launch_pdl(rmsnorm_kernel<TX, TY, 8>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -120,6 +122,8 @@ __global__ void __launch_bounds__(kThreads) norm_prep_kernel(const __nv_bfloat16
                                                              float eps, __nv_bfloat16* __restrict__ xg,
                                                              float* __restrict__ row_scale,
                                                              float* __restrict__ zero_rows) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ float red[kThreads / 32];
   const int nchunk = n / 8;
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -194,14 +198,14 @@ cudaError_t launch_norm_prep(const void* x, const void* g, int rows, int n, floa
   auto G = static_cast<const __nv_bfloat16*>(g);
   auto XG = static_cast<__nv_bfloat16*>(xg);
   switch (nc) {
-    case 1: norm_prep_kernel<1><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
-    case 2: norm_prep_kernel<2><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
-    case 3: norm_prep_kernel<3><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
-    case 4: norm_prep_kernel<4><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
-    case 5: norm_prep_kernel<5><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
-    case 6: norm_prep_kernel<6><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
-    case 7: norm_prep_kernel<7><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
-    case 8: norm_prep_kernel<8><<<grid, kThreads, 0, s>>>(X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 1: launch_pdl(norm_prep_kernel<1>, grid, kThreads, 0, s, X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 2: launch_pdl(norm_prep_kernel<2>, grid, kThreads, 0, s, X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 3: launch_pdl(norm_prep_kernel<3>, grid, kThreads, 0, s, X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 4: launch_pdl(norm_prep_kernel<4>, grid, kThreads, 0, s, X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 5: launch_pdl(norm_prep_kernel<5>, grid, kThreads, 0, s, X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 6: launch_pdl(norm_prep_kernel<6>, grid, kThreads, 0, s, X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 7: launch_pdl(norm_prep_kernel<7>, grid, kThreads, 0, s, X, G, rows, n, eps, XG, row_scale, zero_rows); break;
+    case 8: launch_pdl(norm_prep_kernel<8>, grid, kThreads, 0, s, X, G, rows, n, eps, XG, row_scale, zero_rows); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
