@@ -11,6 +11,7 @@
 //                append; residual + next rmsnorm; activation) and split-KV
 //                attention.
 // fp32 path:     the same sequence on SIMT fp32 GEMMs and fp32 attention.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -106,6 +107,12 @@ int max_cols(const blk_desc& d) {
 
 constexpr int kMaxDecodeSplits = 16;
 
+// Decode GEMMs: weight tiles of 128 rows, token tiles of 64, 128 or 256.
+int dec_bn(int B) { return B <= 64 ? 64 : (B <= 128 ? 128 : 256); }
+int dec_tiles_qkv(const blk_desc& d) {
+  return (d.n_heads * d.head_dim + 127) / 128 + 2 * ((d.n_kv_heads * d.head_dim + 127) / 128);
+}
+
 // N-tile width for a GEMM with m_rows rows and n_cols output columns (per half
 // when paired): the fewest waves of tiles over the SMs, weighted by each width's
 // per-tile efficiency (narrower tiles re-read A more often).
@@ -140,7 +147,7 @@ int norm_parts(int hidden, int bn) { return (hidden + bn - 1) / bn; }
 // Workspace regions of a forward call.
 struct Ws {
   void *y, *q, *k, *v, *o, *mid, *neur, *C, *attn;
-  float *rs1, *ss2;  // bf16 prefill: input-norm 1/rms per row; post-attention sum of squares per row
+  float *rs1, *ss2;  // bf16: input-norm 1/rms per row (prefill); post-attention partial sums of squares
 };
 
 Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, size_t* total) {
@@ -159,11 +166,13 @@ Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, siz
   w.mid = c.take(M * d.hidden * sizeof(float));  // the residual stream after attention, kept in fp32
   w.neur = c.take(M * d.ffn * es);
   if (decode) {
-    const int splits = d.dtype == BLK_BF16 ? kMaxDecodeSplits : 1;
-    w.C = c.take((size_t)splits * M * max_cols(d) * sizeof(float));
     if (d.dtype == BLK_BF16) {
+      w.C = c.take((size_t)kMaxDecodeSplits * M * max_cols(d) * sizeof(float));
       const int s = attn_decode_splits(B, d.n_kv_heads, d.max_seq, h->num_sms);
       w.attn = c.take(attn_decode_ws_bytes(B, d.n_heads, d.head_dim, s));
+      w.ss2 = static_cast<float*>(c.take(M * norm_parts(d.hidden, 128) * sizeof(float)));
+    } else {
+      w.C = c.take(M * max_cols(d) * sizeof(float));
     }
   } else if (d.dtype == BLK_F32) {
     w.C = c.take(M * max_cols(d) * sizeof(float));
@@ -311,6 +320,39 @@ blk_status bf16_mlp_up(const blk_handle* h, const void* y2, int rows, const blk_
 
 // ------------------------------------------------------------------ decode pieces (bf16)
 
+// Split count of a fused decode GEMM (the K splits of a tile form one cluster):
+// every CTA resident at once (units <= SMs, all clusters resident), at most 8
+// splits; 0 when no split count fits.
+int dec_fused_splits(const blk_handle* h, int tiles, int num_kb, int B, Epi epi) {
+  const int bn = dec_bn(B);
+  const int units1 = tiles * ((B + bn - 1) / bn);
+  if (units1 > h->num_sms) return 0;
+  int sp = std::min({choose_splits(units1, num_kb, h->num_sms), 8, h->num_sms / units1, std::max(num_kb, 1)});
+  for (; sp >= 1; --sp)
+    if (tc_dec_max_clusters(bn, epi, sp) >= units1) return sp;
+  return 0;
+}
+
+// A fused decode GEMM: the weight segments on the MMA's M side, the B tokens of x
+// on N, each tile's K splits one cluster that finishes the tile's post-op.
+blk_status dec_gemm(const blk_handle* h, const TcSeg* segs, int nseg, const void* x, int B, int K, int splits,
+                    Epi epi, TcEpiArgs e, cudaStream_t s, const char* what) {
+  TcGemmDesc g;
+  g.na = nseg;
+  for (int i = 0; i < nseg; ++i) g.a[i] = segs[i];
+  g.nb = 1;
+  g.b[0] = {x, B, 0};
+  g.K = K;
+  g.bn = dec_bn(B);
+  g.k_splits = splits;
+  g.epi = epi;
+  g.const_op = 1;  // A = the weights
+  e.n_tok = B;
+  g.e = e;
+  return tc(h, g, s, what);
+}
+
+// The unfused form: transposed split-K partials [split][token][column], summed by a post kernel.
 blk_status bf16_stream_gemm(const blk_handle* h, const TcSeg* segs, int nseg, const void* x, int B, int K, float* C,
                             int ldc, int* splits_out, cudaStream_t s, const char* what) {
   TcGemmDesc g;
@@ -323,7 +365,7 @@ blk_status bf16_stream_gemm(const blk_handle* h, const TcSeg* segs, int nseg, co
   g.nb = 1;
   g.b[0] = {x, B, 0};
   g.K = K;
-  g.bn = B <= 64 ? 64 : (B <= 128 ? 128 : 256);
+  g.bn = dec_bn(B);
   const int n_tiles = (B + g.bn - 1) / g.bn;
   g.k_splits = choose_splits(tiles * n_tiles, (K + 63) / 64, h->num_sms);
   g.epi = Epi::kPartialT;
@@ -431,40 +473,83 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
   const blk_desc& d = h->d;
   const bool bf = true;
   const int Hd = d.n_heads * d.head_dim, KVd = d.n_kv_heads * d.head_dim;
+  const int parts = norm_parts(d.hidden, 128);
   float* C = static_cast<float*>(ws.C);
   void* q = tap_or(taps, &blk_taps::attention_queries, ws.q);
   void* o = tap_or(taps, &blk_taps::attention_head_outputs, ws.o);
   void* mid_tap = taps ? taps->layer_mid : nullptr;
   void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
+  // QKV, o_proj and down finish their tiles inside the GEMM when every unit fits
+  // on the SMs at once; otherwise (and for the MLP-up GEMM, whose tiles outnumber
+  // the SMs) a post kernel sums the split partials.
+  const int hid_tiles = (d.hidden + 127) / 128;
+  const int s_qkv = dec_fused_splits(h, dec_tiles_qkv(d), (d.hidden + 63) / 64, B, Epi::kDecQkv);
+  const int s_o = dec_fused_splits(h, hid_tiles, (Hd + 63) / 64, B, Epi::kDecResid);
+  const int s_down = dec_fused_splits(h, hid_tiles, (d.ffn + 63) / 64, B, Epi::kDecResid);
   int sp = 1;
   prof_mark(h, "rmsnorm1", 1, s);
   BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, B, d.hidden, d.eps, ws.y, bf, s), "rmsnorm 1"));
-  prof_mark(h, "qkv_gemm", 1, s);
+  prof_mark(h, "qkv_gemm_rope_append", s_qkv ? 1 : 2, s);
   {
     const TcSeg segs[3] = {{w->wq, Hd, 0}, {w->wk, KVd, Hd}, {w->wv, KVd, Hd + KVd}};
-    BLK_TRY(bf16_stream_gemm(h, segs, 3, ws.y, B, d.hidden, C, qkv_cols(d), &sp, s, "decode QKV GEMM"));
+    if (s_qkv) {
+      TcEpiArgs e;
+      e.q = q;
+      e.k = cache->k;
+      e.v = cache->v;
+      e.n_heads = d.n_heads;
+      e.n_kv_heads = d.n_kv_heads;
+      e.head_dim = d.head_dim;
+      e.kv_stride = cache->capacity;
+      e.q_gain = w->q_norm_g;
+      e.k_gain = w->k_norm_g;
+      e.eps = d.eps;
+      e.rope = h->rope;
+      e.rope_max_pos = d.max_seq;
+      e.qk_norm = d.qk_norm;
+      e.lens = cache->lens;
+      BLK_TRY(dec_gemm(h, segs, 3, ws.y, B, d.hidden, s_qkv, Epi::kDecQkv, e, s, "decode QKV GEMM"));
+    } else {
+      BLK_TRY(bf16_stream_gemm(h, segs, 3, ws.y, B, d.hidden, C, qkv_cols(d), &sp, s, "decode QKV GEMM"));
+      BLK_TRY(check_cuda(launch_post_qkv(C, sp, B, qkv_cols(d), 1, nullptr, cache->lens, d.n_heads, d.n_kv_heads,
+                                         d.head_dim, d.qk_norm, w->q_norm_g, w->k_norm_g, d.eps, h->rope,
+                                         d.max_seq, q, cache->k, cache->v, cache->capacity, bf, s),
+                         "decode qkv post"));
+    }
   }
-  prof_mark(h, "qkv_post_rope_append", 1, s);
-  BLK_TRY(check_cuda(launch_post_qkv(C, sp, B, qkv_cols(d), 1, nullptr, cache->lens, d.n_heads, d.n_kv_heads,
-                                     d.head_dim, d.qk_norm, w->q_norm_g, w->k_norm_g, d.eps, h->rope, d.max_seq, q,
-                                     cache->k, cache->v, cache->capacity, bf, s),
-                     "decode qkv post"));
   prof_mark(h, "attention_splitkv", 2, s);
   const char* why = nullptr;
-  cudaError_t e = launch_attn_decode_bf16(q, cache->k, cache->v, o, B, d.n_heads, d.n_kv_heads, d.head_dim,
-                                          cache->capacity, cache->lens, 1, max_len,
-                                          attn_decode_splits(B, d.n_kv_heads, d.max_seq, h->num_sms), ws.attn,
-                                          h->num_sms, h->status, (unsigned long long)g_wait_ns.load(), s, &why);
-  BLK_TRY(check_cuda(e, "decode attention", why));
-  prof_mark(h, "o_proj_gemm", 1, s);
+  cudaError_t ce = launch_attn_decode_bf16(q, cache->k, cache->v, o, B, d.n_heads, d.n_kv_heads, d.head_dim,
+                                           cache->capacity, cache->lens, 1, max_len,
+                                           attn_decode_splits(B, d.n_kv_heads, d.max_seq, h->num_sms), ws.attn,
+                                           h->num_sms, h->status, (unsigned long long)g_wait_ns.load(), s, &why);
+  BLK_TRY(check_cuda(ce, "decode attention", why));
+  prof_mark(h, "o_proj_gemm_resid_norm2", s_o ? 1 : 2, s);
   {
     const TcSeg segs[1] = {{w->wo, d.hidden, 0}};
-    BLK_TRY(bf16_stream_gemm(h, segs, 1, o, B, Hd, C, d.hidden, &sp, s, "decode o_proj GEMM"));
+    if (s_o) {
+      // mid = x + o Wo^T (fp32), and the post-attention RMSNorm split: ws.y = mid * g2,
+      // ws.ss2 = per-tile sums of squares (the activation kernel applies 1/rms)
+      TcEpiArgs e;
+      e.out = ws.mid;
+      e.out_f32 = 1;
+      e.ldo = d.hidden;
+      e.resid = x;
+      e.out2 = mid_tap;
+      e.tap = taps ? taps->attention_output : nullptr;
+      e.norm_out = ws.y;
+      e.norm_gain = w->ln2_g;
+      e.norm_ss = ws.ss2;
+      e.norm_parts = parts;
+      BLK_TRY(dec_gemm(h, segs, 1, o, B, Hd, s_o, Epi::kDecResid, e, s, "decode o_proj GEMM"));
+    } else {
+      BLK_TRY(bf16_stream_gemm(h, segs, 1, o, B, Hd, C, d.hidden, &sp, s, "decode o_proj GEMM"));
+      BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, x, false, ws.mid, true, mid_tap,
+                                           taps ? taps->attention_output : nullptr, w->ln2_g, d.eps, ws.y, nullptr,
+                                           bf, s),
+                         "decode o_proj post"));
+    }
   }
-  prof_mark(h, "o_post_resid_rmsnorm2", 1, s);
-  BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, x, false, ws.mid, true, mid_tap,
-                                       taps ? taps->attention_output : nullptr, w->ln2_g, d.eps, ws.y, nullptr, bf, s),
-                     "decode o_proj post"));
   prof_mark(h, "mlp_up_gemm", 1, s);
   if (d.act == BLK_ACT_SWIGLU) {
     const TcSeg segs[2] = {{w->w_gate, d.ffn, 0}, {w->w_up, d.ffn, d.ffn}};
@@ -475,17 +560,29 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
   }
   prof_mark(h, "mlp_act", 1, s);
   BLK_TRY(check_cuda(launch_post_act(C, sp, B, d.ffn, mlp_cols(d), (int)d.act, d.xielu_alpha_p, d.xielu_alpha_n,
-                                     d.xielu_beta, d.xielu_eps, neur, bf, s),
+                                     d.xielu_beta, d.xielu_eps, neur, bf, s, s_o ? ws.ss2 : nullptr, parts,
+                                     d.hidden, d.eps),
                      "decode activation"));
-  prof_mark(h, "down_gemm", 1, s);
+  prof_mark(h, "down_gemm_resid", s_down ? 1 : 2, s);
   {
     const TcSeg segs[1] = {{w->w_down, d.hidden, 0}};
-    BLK_TRY(bf16_stream_gemm(h, segs, 1, neur, B, d.ffn, C, d.hidden, &sp, s, "decode down GEMM"));
+    if (s_down) {
+      TcEpiArgs e;
+      e.out = out;
+      e.ldo = d.hidden;
+      e.resid = ws.mid;
+      e.resid_f32 = 1;
+      e.tap = taps ? taps->mlp_output : nullptr;
+      e.bump_lens = cache->lens;
+      BLK_TRY(dec_gemm(h, segs, 1, neur, B, d.ffn, s_down, Epi::kDecResid, e, s, "decode down GEMM"));
+    } else {
+      BLK_TRY(bf16_stream_gemm(h, segs, 1, neur, B, d.ffn, C, d.hidden, &sp, s, "decode down GEMM"));
+      BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, ws.mid, true, out, false, nullptr,
+                                           taps ? taps->mlp_output : nullptr, nullptr, 0.f, nullptr, cache->lens,
+                                           bf, s),
+                         "decode down post"));
+    }
   }
-  prof_mark(h, "down_post_resid", 1, s);
-  BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, ws.mid, true, out, false, nullptr,
-                                       taps ? taps->mlp_output : nullptr, nullptr, 0.f, nullptr, cache->lens, bf, s),
-                     "decode down post"));
   prof_end(h, s);
   return BLK_OK;
 }

@@ -65,9 +65,15 @@ struct TcCfg {
   static_assert(kSmemBytes <= kMaxSmem, "shared memory");
 };
 
+template <int EPI>
+__host__ __device__ constexpr bool is_dec_epi() {
+  return EPI == (int)Epi::kDecQkv || EPI == (int)Epi::kDecResid;
+}
+
 // Tile widths built per epilogue (a GEMM picks its width on the host).
 template <int BN, int EPI>
-constexpr bool tc_supported() {
+__host__ __device__ constexpr bool tc_supported() {
+  if (is_dec_epi<EPI>()) return BN == 64 || BN == 128 || BN == 256;
   if (EPI == (int)Epi::kQkv) return BN == 128 || BN == 256;  // whole heads
   if (EPI == (int)Epi::kPartialT) return BN == 64 || BN == 128 || BN == 256;
   if (EPI == (int)Epi::kStore) return true;
@@ -185,9 +191,30 @@ __device__ __forceinline__ float row_norm_factor(const TcEpiArgs& e, int row, bo
 }
 
 template <int BN, int EPI>
-__device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, uint32_t taddr, int r_in_tile) {
+__device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, uint32_t taddr, int r_in_tile,
+                                             float* stage) {
   const TcEpiArgs& e = p.e;
-  if constexpr (EPI == (int)Epi::kPartialT) {
+  if constexpr (is_dec_epi<EPI>()) {
+    // decode finishers: this split's partial tile [token in tile][128 tile rows] in shared memory
+    // (the idle operand ring), read by the cluster's CTAs after a cluster barrier
+    float* blk = stage + r_in_tile;
+    const int ntok = min(BN, e.n_tok - un.b_row0);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      if (c0 >= ntok) break;  // uniform across the warp
+      float v0[16], v1[16];
+      tmem_ld16(taddr + c0, v0);
+      tmem_ld16(taddr + c0 + 16, v1);
+      tc_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < ntok) blk[(c0 + j) * kBM] = v0[j];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + 16 + j < ntok) blk[(c0 + 16 + j) * kBM] = v1[j];
+    }
+    return;
+  } else if constexpr (EPI == (int)Epi::kPartialT) {
     // rows of the tile are output features, columns are tokens
     const int f_local = un.a_row0 + r_in_tile;
     const bool ok = f_local < p.a_rows[un.a_seg];
@@ -453,6 +480,172 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
   }
 }
 
+// ------------------------------------------------------------------ decode finishers
+//
+// The decode GEMMs put the weights on the MMA's M side and the few tokens on N,
+// and split K over CTAs so that the weight stream covers every SM. Each split
+// stores its fp32 partial tile; the split that arrives last at the tile's
+// counter sums the partials in split order (the result does not depend on which
+// split that is) and applies the projection's post-op. Warp w of the epilogue
+// finishes tokens 4w..4w+3, 16+4w.., and lane l holds the tile's features
+// 4l..4l+3, so every per-token reduction or pairing is a warp shuffle.
+
+__device__ __forceinline__ void st_bf16x4(__nv_bfloat16* dst, float a, float b, float c, float d) {
+  *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(a, b), pack_bf16x2(c, d));
+}
+
+__device__ __forceinline__ float4 ld_bf16x4(const __nv_bfloat16* src) {
+  const uint2 u = *reinterpret_cast<const uint2*>(src);
+  const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y);
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// Decode finisher, run by the four epilogue warps of every CTA of a tile's
+// cluster (one CTA per K split, all resident together) after a cluster barrier:
+// CTA r takes tokens [r * ceil(ntok / S), ...) of the tile; for each token it
+// sums the S partials (distributed shared memory, in split order, so every
+// token's result is the same whichever CTA finishes it) and applies the
+// post-op. Warp w takes tokens w, w + 4, ... of the slice, four per step; lane
+// l holds the tile's features 4l .. 4l + 3, so per-token reductions and the
+// RoPE pairing are warp shuffles.
+template <int BN, int EPI>
+__device__ __forceinline__ void dec_finish(const TcParams& p, const Unit& un, int ew, int lane, const float* stage) {
+  const TcEpiArgs& e = p.e;
+  constexpr bool qkv = EPI == (int)Epi::kDecQkv;
+  const int S = p.k_splits;
+  const int rank = (int)cluster_ctarank();
+  const int ntok = min(BN, e.n_tok - un.b_row0);
+  const int per = (ntok + S - 1) / S;
+  const int lo = rank * per, hi = min(ntok, lo + per);
+  const int tok0 = un.b_row0;
+  const bool rope = qkv && un.a_seg != 2;
+  const int f0 = un.m_tile * kBM;                     // kDecResid: first feature of the tile
+  const bool fok = qkv || f0 + 4 * lane < e.ldo;      // kDecResid: this lane's features exist
+  const uint32_t stage_s = smem_u32(stage) + 16 * lane;
+  float4 gain = make_float4(1.f, 1.f, 1.f, 1.f);
+  if constexpr (qkv) {
+    if (rope && e.qk_norm)
+      gain = ld_bf16x4(reinterpret_cast<const __nv_bfloat16*>(un.a_seg == 0 ? e.q_gain : e.k_gain) + 4 * lane);
+  } else {
+    if (e.norm_out && fok) gain = ld_bf16x4(reinterpret_cast<const __nv_bfloat16*>(e.norm_gain) + f0 + 4 * lane);
+  }
+#pragma unroll 1
+  for (int b0 = lo + ew; b0 < hi; b0 += 16) {
+    // four tokens b0, b0 + 4, b0 + 8, b0 + 12 (those below hi); rows clamped so every address is valid
+    int tl[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) tl[k] = min(b0 + 4 * k, hi - 1);
+    // per-token inputs, one batch of independent loads
+    float4 side0[4], side1[4];
+    int pos[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if constexpr (qkv) {
+        pos[k] = e.lens[tok0 + tl[k]];
+      } else {
+        const size_t i = (size_t)(tok0 + tl[k]) * e.ldo + f0 + 4 * lane;
+        if (e.resid_f32) {
+          side0[k] = fok ? *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.resid) + i)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          const uint2 u = fok ? *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(e.resid) + i)
+                              : make_uint2(0u, 0u);
+          side0[k] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), 0.f, 0.f);  // unpacked below
+        }
+      }
+    }
+    if constexpr (qkv) {
+      if (rope) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int rpos = min(max(pos[k], 0), e.rope_max_pos - 1);
+          const float4* cs4 = reinterpret_cast<const float4*>(e.rope + (size_t)rpos * 64 + 4 * (lane & 15));
+          side0[k] = cs4[0];
+          side1[k] = cs4[1];
+        }
+      }
+    }
+    // the splits' partials, in split order
+    float v[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0.f;
+    for (int sp = 0; sp < S; ++sp) {
+      const uint32_t base = map_shared_rank(stage_s, (uint32_t)sp);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 a = ld_dsmem_f4(base + (uint32_t)tl[k] * (kBM * 4));
+        v[k][0] += a.x;
+        v[k][1] += a.y;
+        v[k][2] += a.z;
+        v[k][3] += a.w;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (b0 + 4 * k >= hi) break;  // warp-uniform
+      const int t = tok0 + tl[k];
+      float* vv = v[k];
+      if constexpr (qkv) {
+        // one head (head_dim 128) per tile; token t is sequence t, at position lens[t]
+        const int seg = un.a_seg;  // 0: q, 1: k, 2: v
+        const int head = un.a_row0 >> 7;
+        const bool write = seg == 0 || (pos[k] >= 0 && pos[k] < e.kv_stride);  // never past a full cache
+        if (rope) {
+          if (e.qk_norm) {
+            const float ss = warp_sum(vv[0] * vv[0] + vv[1] * vv[1] + vv[2] * vv[2] + vv[3] * vv[3]);
+            const float r = rsqrtf(ss * (1.0f / 128.0f) + e.eps);
+            vv[0] *= r * gain.x;
+            vv[1] *= r * gain.y;
+            vv[2] *= r * gain.z;
+            vv[3] *= r * gain.w;
+          }
+          // RoPE, rotate-half pairing: feature i (lane l < 16) with i + 64 (lane l + 16)
+          const float cs[4][2] = {{side0[k].x, side0[k].y}, {side0[k].z, side0[k].w},
+                                  {side1[k].x, side1[k].y}, {side1[k].z, side1[k].w}};
+          float pr[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) pr[c] = __shfl_xor_sync(0xffffffffu, vv[c], 16);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            vv[c] = lane < 16 ? vv[c] * cs[c][0] - pr[c] * cs[c][1] : vv[c] * cs[c][0] + pr[c] * cs[c][1];
+        }
+        if (write) {
+          __nv_bfloat16* dst = seg == 0 ? reinterpret_cast<__nv_bfloat16*>(e.q) + ((size_t)t * e.n_heads + head) * 128
+                                        : reinterpret_cast<__nv_bfloat16*>(seg == 1 ? e.k : e.v) +
+                                              (((size_t)t * e.n_kv_heads + head) * e.kv_stride + pos[k]) * 128;
+          st_bf16x4(dst + 4 * lane, vv[0], vv[1], vv[2], vv[3]);
+        }
+      } else {
+        // the residual stream, summed in fp32 and rounded once
+        float4 r = side0[k];
+        if (!e.resid_f32) {
+          const float2 a = unpack_bf16x2(__float_as_uint(r.x)), b = unpack_bf16x2(__float_as_uint(r.y));
+          r = make_float4(a.x, a.y, b.x, b.y);
+        }
+        const float o0 = r.x + vv[0], o1 = r.y + vv[1], o2 = r.z + vv[2], o3 = r.w + vv[3];
+        const size_t i = (size_t)t * e.ldo + f0 + 4 * lane;
+        if (fok) {
+          if (e.out_f32)
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out) + i) = make_float4(o0, o1, o2, o3);
+          else
+            st_bf16x4(reinterpret_cast<__nv_bfloat16*>(e.out) + i, o0, o1, o2, o3);
+          if (e.out2) st_bf16x4(reinterpret_cast<__nv_bfloat16*>(e.out2) + i, o0, o1, o2, o3);
+          if (e.tap) st_bf16x4(reinterpret_cast<__nv_bfloat16*>(e.tap) + i, vv[0], vv[1], vv[2], vv[3]);
+          // next RMSNorm, split: out * g here (the MLP GEMM's B), 1/rms from the tiles' sums of squares later
+          if (e.norm_out)
+            st_bf16x4(reinterpret_cast<__nv_bfloat16*>(e.norm_out) + i, o0 * gain.x, o1 * gain.y, o2 * gain.z,
+                      o3 * gain.w);
+        }
+        if (e.norm_ss) {
+          const float ss = warp_sum(fok ? o0 * o0 + o1 * o1 + o2 * o2 + o3 * o3 : 0.f);
+          if (lane == 0) e.norm_ss[(size_t)t * e.norm_parts + un.m_tile] = ss;
+        }
+        if (e.bump_lens && un.m_tile == 0 && lane == 0) atomicAdd(e.bump_lens + t, 1);  // no round trip
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 
 template <int BN, int EPI>
@@ -648,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       __syncwarp();
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane);
+      run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane, reinterpret_cast<float*>(smem));
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
     }
@@ -658,6 +851,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
   }
 
+  if constexpr (is_dec_epi<EPI>()) {
+    // Every thread of every CTA of the cluster reaches both barriers, whatever
+    // happened above (all earlier waits are bounded): the split partials are in
+    // shared memory before the first, and no CTA exits while others may still
+    // read its shared memory before the second.
+    __syncwarp();
+    cluster_sync_all();
+    if (warp >= 2) dec_finish<BN, EPI>(p, decode_unit(p, blockIdx.x, bn_rows), warp - 2, lane,
+                                       reinterpret_cast<const float*>(smem));
+    __syncwarp();
+    cluster_sync_all();
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -705,17 +910,59 @@ bool make_tma_2d_16b(CUtensorMap* m, const void* ptr, int rows, int cols, int bo
 namespace {
 
 template <int BN, int EPI>
+cudaError_t configure() {
+  static cudaError_t st = cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               TcCfg<BN>::kSmemBytes);  // once per instantiation
+  return st;
+}
+
+// Launch configuration of a decode GEMM: clusters of `splits` CTAs along x.
+template <int BN, int EPI>
+void cluster_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, int splits, cudaStream_t s) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->gridDim = dim3(grid);
+  cfg->blockDim = dim3(kThreads);
+  cfg->dynamicSmemBytes = TcCfg<BN>::kSmemBytes;
+  cfg->stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 2;
+}
+
+template <int BN, int EPI>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t s) {
-  using C = TcCfg<BN>;
-  static bool configured = false;  // per instantiation; attribute is per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+  cudaError_t e = configure<BN, EPI>();
+  if (e != cudaSuccess) return e;
+  if constexpr (is_dec_epi<EPI>()) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    cluster_config<BN, EPI>(&cfg, attr, grid, p.k_splits, s);
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, EPI>, p);
     if (e != cudaSuccess) return e;
-    configured = true;
+  } else {
+    launch_pdl(tc_gemm_kernel<BN, EPI>, grid, kThreads, TcCfg<BN>::kSmemBytes, s, p);
   }
-  launch_pdl(tc_gemm_kernel<BN, EPI>, grid, kThreads, C::kSmemBytes, s, p);
   return cudaGetLastError();
+}
+
+template <int BN, int EPI>
+int max_clusters(int splits) {
+  if (configure<BN, EPI>() != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  cluster_config<BN, EPI>(&cfg, attr, splits, splits, nullptr);
+  cfg.numAttrs = 1;  // the cluster shape alone
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, EPI>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 template <int BN, int EPI>
@@ -736,11 +983,34 @@ cudaError_t dispatch_epi(const TcParams& p, Epi epi, int grid, cudaStream_t s) {
     case Epi::kRelu2: return launch_if<BN, (int)Epi::kRelu2>(p, grid, s);
     case Epi::kXielu: return launch_if<BN, (int)Epi::kXielu>(p, grid, s);
     case Epi::kPartialT: return launch_if<BN, (int)Epi::kPartialT>(p, grid, s);
+    case Epi::kDecQkv: return launch_if<BN, (int)Epi::kDecQkv>(p, grid, s);
+    case Epi::kDecResid: return launch_if<BN, (int)Epi::kDecResid>(p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
+
+int tc_dec_max_clusters(int bn, Epi epi, int splits) {
+  if (splits < 1 || splits > 8) return 0;
+  static std::mutex mu;
+  static int cache[5][2][9] = {};  // bn index, epilogue, splits (0: not queried yet)
+  const int bi = bn == 64 ? 0 : bn == 128 ? 1 : bn == 256 ? 2 : -1;
+  const int ei = epi == Epi::kDecQkv ? 0 : epi == Epi::kDecResid ? 1 : -1;
+  if (bi < 0 || ei < 0) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = cache[bi][ei][splits];
+  if (c == 0) {
+    int n = 0;
+    if (bn == 64) n = ei == 0 ? max_clusters<64, (int)Epi::kDecQkv>(splits) : max_clusters<64, (int)Epi::kDecResid>(splits);
+    if (bn == 128)
+      n = ei == 0 ? max_clusters<128, (int)Epi::kDecQkv>(splits) : max_clusters<128, (int)Epi::kDecResid>(splits);
+    if (bn == 256)
+      n = ei == 0 ? max_clusters<256, (int)Epi::kDecQkv>(splits) : max_clusters<256, (int)Epi::kDecResid>(splits);
+    c = n > 0 ? n : -1;
+  }
+  return c > 0 ? c : 0;
+}
 
 int tc_gemm_units(const TcGemmDesc& d) {
   const int bn_rows = d.b_paired ? d.bn / 2 : d.bn;
@@ -800,6 +1070,14 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
   p.num_kb = (d.K + kBK - 1) / kBK;
   p.k_splits = d.k_splits < 1 ? 1 : (d.k_splits > p.num_kb ? p.num_kb : d.k_splits);
   p.num_units = p.m_tiles * p.n_tiles * p.k_splits;
+  if (d.epi == Epi::kDecQkv || d.epi == Epi::kDecResid) {
+    // one unit per CTA, the K splits of a tile forming one cluster (at most 8), all resident at once
+    if (d.nb != 1 || d.b_paired || d.e.n_tok != d.b[0].rows || p.k_splits > 8 || p.num_units > max_ctas ||
+        tc_dec_max_clusters(d.bn, d.epi, p.k_splits) < p.m_tiles * p.n_tiles) {
+      *why = "tcgen05 GEMM: a decode finisher needs one unit per CTA and every cluster of K splits resident";
+      return cudaErrorInvalidValue;
+    }
+  }
   p.e = d.e;
   p.status = st;
   p.wait_ns = wait_ns;

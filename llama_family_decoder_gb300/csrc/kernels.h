@@ -42,7 +42,17 @@ enum class Epi : int {
   kRelu2 = 4,     // out = bf16(relu(acc)^2)
   kXielu = 5,     // out = bf16(xielu(acc))
   kPartialT = 6,  // swap-AB split-K: part[split][token][feature] = acc^T (fp32)
+  // Decode (swap-AB) with the K splits of a tile launched as one thread-block
+  // cluster: each split keeps its fp32 partial in shared memory, and CTA r of
+  // the cluster sums slice r of the tile's tokens over all splits (distributed
+  // shared memory, split order) and applies the post-op.
+  kDecQkv = 7,    // per-head q/k RMSNorm, RoPE at position lens[t], q store, K/V cache append
+  kDecResid = 8,  // resid + acc (fp32), optional taps, next RMSNorm (gained rows + sum of squares)
 };
+
+// How many clusters of `splits` CTAs of the decode GEMM kernel (tile width bn,
+// epilogue epi) can be resident at once; 0 if the query fails.
+int tc_dec_max_clusters(int bn, Epi epi, int splits);
 
 // One row-segment of an operand: a contiguous [rows, K] bf16 matrix.
 struct TcSeg {
@@ -95,6 +105,9 @@ struct TcEpiArgs {
   // kPartialT
   int part_ld = 0;  // features per token row of the partial buffer
   int n_tok = 0;    // valid tokens (B operand rows)
+  // decode finishers
+  const int* lens = nullptr;  // kDecQkv: positions already in the cache, per sequence
+  int* bump_lens = nullptr;   // kDecResid: lens[t] += 1 once per token (the tile of m_tile 0)
 };
 
 struct TcGemmDesc {
@@ -146,9 +159,12 @@ cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int l
                               void* out, bool out_f32, void* out2, void* tap, const void* g, float eps, void* y,
                               int* bump_lens, bool bf16, cudaStream_t s);
 
-// neurons[r, f] = act(C) for f < F; SwiGLU reads gate at column f and up at F + f.
+// neurons[r, f] = act(C * rs[r]) for f < F; SwiGLU reads gate at column f and up at F + f.
+// rs[r] = rsqrt(sum of row_ss[r, 0..ss_parts) / ss_n + ss_eps) (the RMSNorm of the GEMM's
+// input rows, applied after the product), or 1 when row_ss is null.
 cudaError_t launch_post_act(const float* C, int splits, int rows, int F, int ldc, int act, float alpha_p,
-                            float alpha_n, float beta, float xeps, void* out, bool bf16, cudaStream_t s);
+                            float alpha_n, float beta, float xeps, void* out, bool bf16, cudaStream_t s,
+                            const float* row_ss = nullptr, int ss_parts = 0, int ss_n = 1, float ss_eps = 0.f);
 
 // ---------------------------------------------------------------- attention
 // Causal GQA attention; q [B,H,Tq,d], k/v [B,Hkv,kv_stride,d], o [B,Tq,H,d].

@@ -205,10 +205,19 @@ __device__ __forceinline__ float act_one(int act, float gt, float u, float alpha
   return u > 0.f ? alpha_p * u * u + beta * u : alpha_n * (expm1f(fminf(u, xeps)) - u) + beta * u;
 }
 
+// 1/rms of row r from its partial sums of squares (summed in order), or 1 without them.
+__device__ __forceinline__ float row_rms_factor(const float* row_ss, int ss_parts, int ss_n, float ss_eps, int r) {
+  if (!row_ss) return 1.0f;
+  float t = 0.f;
+  for (int i = 0; i < ss_parts; ++i) t += row_ss[(size_t)r * ss_parts + i];
+  return rsqrtf(t / (float)ss_n + ss_eps);
+}
+
 // Four consecutive neurons per thread (F % 4 == 0).
 template <typename T>
 __global__ void post_act4_kernel(const float* __restrict__ C, int splits, int rows, int F, int ldc, int act,
-                                 float alpha_p, float alpha_n, float beta, float xeps, T* __restrict__ out) {
+                                 float alpha_p, float alpha_n, float beta, float xeps, T* __restrict__ out,
+                                 const float* __restrict__ row_ss, int ss_parts, int ss_n, float ss_eps) {
   pdl_launch_dependents();
   pdl_wait();
   const int F4 = F / 4;
@@ -217,8 +226,11 @@ __global__ void post_act4_kernel(const float* __restrict__ C, int splits, int ro
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const int r = i / F4, f = (i - r * F4) * 4;
     const size_t base = (size_t)r * ldc;
-    const float4 u = act == 0 ? split_sum4(C, splits, sstride, base + F + f) : split_sum4(C, splits, sstride, base + f);
-    const float4 gt = act == 0 ? split_sum4(C, splits, sstride, base + f) : u;
+    const float rs = row_rms_factor(row_ss, ss_parts, ss_n, ss_eps, r);
+    float4 u = act == 0 ? split_sum4(C, splits, sstride, base + F + f) : split_sum4(C, splits, sstride, base + f);
+    float4 gt = act == 0 ? split_sum4(C, splits, sstride, base + f) : u;
+    u = make_float4(u.x * rs, u.y * rs, u.z * rs, u.w * rs);
+    gt = make_float4(gt.x * rs, gt.y * rs, gt.z * rs, gt.w * rs);
     const float4 n = make_float4(act_one(act, gt.x, u.x, alpha_p, alpha_n, beta, xeps),
                                  act_one(act, gt.y, u.y, alpha_p, alpha_n, beta, xeps),
                                  act_one(act, gt.z, u.z, alpha_p, alpha_n, beta, xeps),
@@ -229,7 +241,8 @@ __global__ void post_act4_kernel(const float* __restrict__ C, int splits, int ro
 
 template <typename T>
 __global__ void post_act_kernel(const float* __restrict__ C, int splits, int rows, int F, int ldc, int act,
-                                float alpha_p, float alpha_n, float beta, float xeps, T* __restrict__ out) {
+                                float alpha_p, float alpha_n, float beta, float xeps, T* __restrict__ out,
+                                const float* __restrict__ row_ss, int ss_parts, int ss_n, float ss_eps) {
   pdl_launch_dependents();
   pdl_wait();
   const size_t total = (size_t)rows * F;
@@ -237,8 +250,9 @@ __global__ void post_act_kernel(const float* __restrict__ C, int splits, int row
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
     const int r = (int)(idx / F), f = (int)(idx - (size_t)r * F);
     const size_t base = (size_t)r * ldc;
-    const float u = split_sum(C, splits, sstride, base + (act == 0 ? F + f : f));
-    const float gt = act == 0 ? split_sum(C, splits, sstride, base + f) : u;
+    const float rs = row_rms_factor(row_ss, ss_parts, ss_n, ss_eps, r);
+    const float u = split_sum(C, splits, sstride, base + (act == 0 ? F + f : f)) * rs;
+    const float gt = act == 0 ? split_sum(C, splits, sstride, base + f) * rs : u;
     out[idx] = from_f32<T>(act_one(act, gt, u, alpha_p, alpha_n, beta, xeps));
   }
 }
@@ -309,7 +323,8 @@ cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int l
 }
 
 cudaError_t launch_post_act(const float* C, int splits, int rows, int F, int ldc, int act, float alpha_p,
-                            float alpha_n, float beta, float xeps, void* out, bool bf16, cudaStream_t s) {
+                            float alpha_n, float beta, float xeps, void* out, bool bf16, cudaStream_t s,
+                            const float* row_ss, int ss_parts, int ss_n, float ss_eps) {
   if (rows <= 0) return cudaSuccess;
   const bool vec = F % 4 == 0 && ldc % 4 == 0;
   const size_t total = (size_t)rows * F / (vec ? 4 : 1);
@@ -318,17 +333,17 @@ cudaError_t launch_post_act(const float* C, int splits, int rows, int F, int ldc
   if (vec) {
     if (bf16)
       launch_pdl(post_act4_kernel<__nv_bfloat16>, grid, 256, 0, s, C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta,
-                                                           xeps, static_cast<__nv_bfloat16*>(out));
+                                                           xeps, static_cast<__nv_bfloat16*>(out), row_ss, ss_parts, ss_n, ss_eps);
     else
       launch_pdl(post_act4_kernel<float>, grid, 256, 0, s, C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
-                                                   static_cast<float*>(out));
+                                                   static_cast<float*>(out), row_ss, ss_parts, ss_n, ss_eps);
   } else {
     if (bf16)
       launch_pdl(post_act_kernel<__nv_bfloat16>, grid, 256, 0, s, C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
-                                                          static_cast<__nv_bfloat16*>(out));
+                                                          static_cast<__nv_bfloat16*>(out), row_ss, ss_parts, ss_n, ss_eps);
     else
       launch_pdl(post_act_kernel<float>, grid, 256, 0, s, C, splits, rows, F, ldc, act, alpha_p, alpha_n, beta, xeps,
-                                                  static_cast<float*>(out));
+                                                  static_cast<float*>(out), row_ss, ss_parts, ss_n, ss_eps);
   }
   return cudaGetLastError();
 }

@@ -208,6 +208,41 @@ def test_decode_step_small(dtype):
         assert torch.equal(kd[b, :, :L].cpu(), kc[b, :, :L])
 
 
+@pytest.mark.parametrize("act,qk_norm,batch,ffn", [("relu2", False, 7, 1000), ("xielu", True, 3, 1024),
+                                                   ("silu", True, 70, 968)])
+def test_decode_step_bf16_variants_and_taps(act, qk_norm, batch, ffn):
+    # every activation, q/k-norm with non-unit gains, a token tile wider than 64,
+    # ragged MLP tiles, and the per-stage taps of the decode path
+    wl = Workload(f"decode_{act}", "bf16", batch, 1, 512, 8, 2, 128, ffn, act, qk_norm=qk_norm, seed=25)
+    lens = [(37 * b + 11) % 190 + 1 for b in range(batch)]
+    w, x, kc, vc = _decode_case(wl, lens)
+    blk = DecoderBlock.from_workload(wl, max_seq=kc.shape[2] + 1)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    tb = _tap_buffers(wl, torch.bfloat16)
+    out = blk.forward(x[:, None].to(DEV), to_dev(w), cache={"k": kd, "v": vd, "lens": lens_d},
+                      host_lens_max=max(lens), taps=tb)
+    torch.cuda.synchronize()
+    assert blk.last_status() == 0
+    ref = oracle.decode_step(cfg_of(wl), weights_np(w), np64(x), np64(kc), np64(vc), np.array(lens))
+    assert rel_err(out[:, 0], ref["layer_output"]) <= TOL["bf16"]
+    assert lens_d.tolist() == [L + 1 for L in lens]
+    idx = torch.arange(batch)
+    got_k = kd[idx, :, torch.tensor(lens)]  # [B, Hkv, d]
+    got_v = vd[idx, :, torch.tensor(lens)]
+    assert rel_err(got_k, ref["new_key"]) <= TOL["bf16"]
+    assert rel_err(got_v, ref["new_value"]) <= TOL["bf16"]
+    for name, key, sl in [("attention_queries", "attention_queries", lambda t: t[:, :, 0]),
+                          ("attention_output", "attention_output", lambda t: t[:, 0]),
+                          ("layer_mid", "layer_mid", lambda t: t[:, 0]),
+                          ("mlp_neurons", "mlp_neurons", lambda t: t[:, 0]),
+                          ("mlp_output", "mlp_output", lambda t: t[:, 0])]:
+        r = ref[key]
+        err, floor = rel_err(sl(tb[name]), r), bf16_floor(r)
+        print(f"decode {act} tap {name}: {err:.4f} (floor {floor:.4f})")
+        assert err <= max(TOL["bf16"], 2 * floor + 5e-3), (name, err, floor)
+
+
 def test_decode_matches_prefill_last_row():
     wl = Workload("small_prefill_decode", "bf16", 2, 96, 512, 4, 2, 128, 1000, "silu", seed=23)
     w = to_dev(make_weights(wl))
