@@ -210,6 +210,29 @@ def config_of(wl, n):
     return c
 
 
+# ---------------------------------------------------------------- replicas (N > 1)
+
+def rank_seed(wl, rank):
+    """Each replica draws its own synthetic batch and weights."""
+    return wl.seed + 17 * rank
+
+
+def max_over_ranks(x, device):
+    """The slowest rank's value (the job's time); x itself on one rank."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_step, steps, total_ms):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_step * steps / (total_ms / 1e3)
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, wl):
@@ -230,8 +253,8 @@ def run_ours(args, wl):
     import __graft_entry__
     __graft_entry__.build()
 
-    w_cpu = make_weights(wl, seed=wl.seed + 17 * rank)
-    x_cpu = make_input(wl, seed=wl.seed + 17 * rank)
+    w_cpu = make_weights(wl, seed=rank_seed(wl, rank))
+    x_cpu = make_input(wl, seed=rank_seed(wl, rank))
     w = {k: v.to(dev) for k, v in w_cpu.items()}
     x = x_cpu.to(dev)
     decode = wl.cache_len > 0
@@ -307,14 +330,10 @@ def run_ours(args, wl):
     stages = blk.profile_collect()
     pgraph.close()
     blk.profile(False)  # the profiled graph recorded these events: drop them after it
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
     tokens = wl.batch * wl.seq
-    value = world * tokens * args.steps / (total_ms / 1e3)
+    value = job_tokens_per_s(world, tokens, args.steps, total_ms)
 
     # ---- end to end through the C ABI with host buffers
     x_host = x_cpu.pin_memory()
@@ -332,11 +351,7 @@ def run_ours(args, wl):
         e_ends[i].record(stream)
     torch.cuda.synchronize()
     graph.close()
-    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)) / args.steps, dev)
     nbytes = x_cpu.numel() * x_cpu.element_size()
 
     # ---- roofline of the dominant kernel (its live event times)
@@ -349,8 +364,10 @@ def run_ours(args, wl):
         es = 2 if wl.dtype == "bf16" else 4
         algo = kv_bytes + wl.batch * wl.num_heads * wl.head_dim * es * 2
         achieved = algo / (ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": "attn_decode_kernel (split-KV)", "achieved": achieved,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+        kname = "attn_decode_kernel (split-KV)"
+        roof = {"bound": "hbm", "kernel": kname, "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": _traffic(kname, wl.name),
                 "algorithmic_bytes": algo, "peak_source": peaks["source"]}
     else:
         name = "mlp_up_gemm_act"
@@ -372,7 +389,8 @@ def run_ours(args, wl):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded N(0,0.02) weights, N(0,1) input)",
             "config": config_of(wl, world), "roofline": roof,
-            "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
+            "e2e": {"value": job_tokens_per_s(world, tokens, 1, e2e_ms), "unit": "tokens/s",
+                    "h2d_bytes_per_step": nbytes,
                     "d2h_bytes_per_step": nbytes},
             "gpu_launches": launches, "clocks": clk.summary(),
             "stages_ms": {k: v[0] / args.steps for k, v in stages.items()},
