@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
       int stage = 0;
       uint32_t ph = 0, issued = 0, parity = 0;
       bool failed = false;
+      const uint64_t stream_once = l2_policy_evict_first();  // the cache is read once per step
       for (int u = blockIdx.x; u < p.units && !failed; u += gridDim.x) {
         const DecodeUnit un = decode_unit(p, u);
         const int row0 = (un.b * p.Hkv + un.kvh) * p.kv_stride + un.k0;
@@ -139,10 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
           const uint32_t dst = smem_u32(ring + stage * kStageBytes);
           mbar_arrive_expect_tx(full(stage), kStageBytes);
           const int row = row0 + t * kTileKeys;
-          tma_load_2d(dst, &p.tk, 0, row, full(stage));
-          tma_load_2d(dst + kHalfBytes, &p.tk, 64, row, full(stage));
-          tma_load_2d(dst + 2 * kHalfBytes, &p.tv, 0, row, full(stage));
-          tma_load_2d(dst + 3 * kHalfBytes, &p.tv, 64, row, full(stage));
+          tma_load_2d_hint(dst, &p.tk, 0, row, full(stage), stream_once);
+          tma_load_2d_hint(dst + kHalfBytes, &p.tk, 64, row, full(stage), stream_once);
+          tma_load_2d_hint(dst + 2 * kHalfBytes, &p.tv, 0, row, full(stage), stream_once);
+          tma_load_2d_hint(dst + 3 * kHalfBytes, &p.tv, 64, row, full(stage), stream_once);
           issued |= 1u << stage;
           parity = (parity & ~(1u << stage)) | (ph << stage);
           if (++stage == kStages) {
