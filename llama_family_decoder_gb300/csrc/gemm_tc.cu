@@ -505,84 +505,128 @@ __device__ __forceinline__ float4 ld_bf16x4(const __nv_bfloat16* src) {
 // CTA r takes tokens [r * ceil(ntok / S), ...) of the tile; for each token it
 // sums the S partials (distributed shared memory, in split order, so every
 // token's result is the same whichever CTA finishes it) and applies the
-// post-op. Warp w takes tokens w, w + 4, ... of the slice, four per step; lane
-// l holds the tile's features 4l .. 4l + 3, so per-token reductions and the
-// RoPE pairing are warp shuffles.
+// post-op. Warp w takes tokens lo + w + 4k (k = 0, 1, ...) of the slice, four
+// per step; lane l holds the tile's features 4l .. 4l + 3, so per-token
+// reductions and the RoPE pairing are warp shuffles.
+//
+// The per-token inputs of the first kDecPre tokens of each warp (positions and
+// RoPE rows, or residual rows) and the gains are loaded into registers by
+// dec_load_side while the MMA main loop still runs; the rest, if any, are loaded
+// in the finish itself.
+constexpr int kDecPre = 8;
+
+struct DecSide {
+  float4 a[kDecPre], b[kDecPre];  // kDecQkv: (cos, sin) of features 4l .. 4l + 3 (mod 64); kDecResid: residual (a)
+  int pos[kDecPre];               // kDecQkv: lens of the token
+  float4 gain;
+};
+
+struct DecSlice {
+  int lo, hi, tok0;
+};
+
+__device__ __forceinline__ DecSlice dec_slice(const TcParams& p, const Unit& un, int bn) {
+  const int S = p.k_splits;
+  const int ntok = min(bn, p.e.n_tok - un.b_row0);
+  const int per = (ntok + S - 1) / S;
+  DecSlice sl;
+  sl.lo = (int)cluster_ctarank() * per;
+  sl.hi = min(ntok, sl.lo + per);
+  sl.tok0 = un.b_row0;
+  return sl;
+}
+
+// Inputs of token row tl (tl < ntok) for one lane: RoPE rows and position, or the residual row.
+template <int EPI>
+__device__ __forceinline__ void dec_token_inputs(const TcParams& p, const Unit& un, int tok0, int tl, int lane,
+                                                 float4& a, float4& b, int& pos) {
+  const TcEpiArgs& e = p.e;
+  if constexpr (EPI == (int)Epi::kDecQkv) {
+    pos = e.lens[tok0 + tl];
+    if (un.a_seg != 2) {
+      const int rpos = min(max(pos, 0), e.rope_max_pos - 1);
+      const float4* cs4 = reinterpret_cast<const float4*>(e.rope + (size_t)rpos * 64 + 4 * (lane & 15));
+      a = cs4[0];
+      b = cs4[1];
+    }
+  } else {
+    const int f = un.m_tile * kBM + 4 * lane;
+    a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (f < e.ldo) {
+      const size_t i = (size_t)(tok0 + tl) * e.ldo + f;
+      if (e.resid_f32) {
+        a = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.resid) + i);
+      } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(e.resid) + i);
+        const float2 x = unpack_bf16x2(u.x), y = unpack_bf16x2(u.y);
+        a = make_float4(x.x, x.y, y.x, y.y);
+      }
+    }
+  }
+}
+
 template <int BN, int EPI>
-__device__ __forceinline__ void dec_finish(const TcParams& p, const Unit& un, int ew, int lane, const float* stage) {
+__device__ __forceinline__ void dec_load_side(const TcParams& p, const Unit& un, int ew, int lane, DecSide& sd) {
+  const TcEpiArgs& e = p.e;
+  const DecSlice sl = dec_slice(p, un, BN);
+  sd.gain = make_float4(1.f, 1.f, 1.f, 1.f);
+  if constexpr (EPI == (int)Epi::kDecQkv) {
+    if (un.a_seg != 2 && e.qk_norm)
+      sd.gain = ld_bf16x4(reinterpret_cast<const __nv_bfloat16*>(un.a_seg == 0 ? e.q_gain : e.k_gain) + 4 * lane);
+  } else {
+    const int f = un.m_tile * kBM + 4 * lane;
+    if (e.norm_out && f < e.ldo) sd.gain = ld_bf16x4(reinterpret_cast<const __nv_bfloat16*>(e.norm_gain) + f);
+  }
+  if (sl.hi <= sl.lo) return;
+#pragma unroll
+  for (int k = 0; k < kDecPre; ++k)  // rows clamped into the slice: every address is valid
+    dec_token_inputs<EPI>(p, un, sl.tok0, min(sl.lo + ew + 4 * k, sl.hi - 1), lane, sd.a[k], sd.b[k], sd.pos[k]);
+}
+
+template <int BN, int EPI>
+__device__ __forceinline__ void dec_finish(const TcParams& p, const Unit& un, int ew, int lane, const float* stage,
+                                           const DecSide& sd) {
   const TcEpiArgs& e = p.e;
   constexpr bool qkv = EPI == (int)Epi::kDecQkv;
   const int S = p.k_splits;
-  const int rank = (int)cluster_ctarank();
-  const int ntok = min(BN, e.n_tok - un.b_row0);
-  const int per = (ntok + S - 1) / S;
-  const int lo = rank * per, hi = min(ntok, lo + per);
-  const int tok0 = un.b_row0;
+  const DecSlice sl = dec_slice(p, un, BN);
+  const int lo = sl.lo, hi = sl.hi, tok0 = sl.tok0;
   const bool rope = qkv && un.a_seg != 2;
   const int f0 = un.m_tile * kBM;                     // kDecResid: first feature of the tile
   const bool fok = qkv || f0 + 4 * lane < e.ldo;      // kDecResid: this lane's features exist
   const uint32_t stage_s = smem_u32(stage) + 16 * lane;
-  float4 gain = make_float4(1.f, 1.f, 1.f, 1.f);
-  if constexpr (qkv) {
-    if (rope && e.qk_norm)
-      gain = ld_bf16x4(reinterpret_cast<const __nv_bfloat16*>(un.a_seg == 0 ? e.q_gain : e.k_gain) + 4 * lane);
-  } else {
-    if (e.norm_out && fok) gain = ld_bf16x4(reinterpret_cast<const __nv_bfloat16*>(e.norm_gain) + f0 + 4 * lane);
-  }
-#pragma unroll 1
-  for (int b0 = lo + ew; b0 < hi; b0 += 16) {
-    // four tokens b0, b0 + 4, b0 + 8, b0 + 12 (those below hi); rows clamped so every address is valid
-    int tl[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) tl[k] = min(b0 + 4 * k, hi - 1);
-    // per-token inputs, one batch of independent loads
-    float4 side0[4], side1[4];
-    int pos[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if constexpr (qkv) {
-        pos[k] = e.lens[tok0 + tl[k]];
-      } else {
-        const size_t i = (size_t)(tok0 + tl[k]) * e.ldo + f0 + 4 * lane;
-        if (e.resid_f32) {
-          side0[k] = fok ? *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.resid) + i)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-          const uint2 u = fok ? *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(e.resid) + i)
-                              : make_uint2(0u, 0u);
-          side0[k] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), 0.f, 0.f);  // unpacked below
-        }
-      }
-    }
-    if constexpr (qkv) {
-      if (rope) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int rpos = min(max(pos[k], 0), e.rope_max_pos - 1);
-          const float4* cs4 = reinterpret_cast<const float4*>(e.rope + (size_t)rpos * 64 + 4 * (lane & 15));
-          side0[k] = cs4[0];
-          side1[k] = cs4[1];
-        }
-      }
-    }
+  const float4 gain = sd.gain;
+  // one step: the warp's tokens k0 .. k0 + 3 (rows lo + ew + 4k below hi; tl clamped so every address is valid)
+  auto step = [&](int k0, const int (&tl)[4], const float4 (&side0)[4], const float4 (&side1)[4],
+                  const int (&pos)[4]) {
     // the splits' partials, in split order
     float v[4][4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) v[k][0] = v[k][1] = v[k][2] = v[k][3] = 0.f;
-    for (int sp = 0; sp < S; ++sp) {
-      const uint32_t base = map_shared_rank(stage_s, (uint32_t)sp);
+    for (int sp0 = 0; sp0 < S; sp0 += 4) {
+      // up to four splits' loads in flight together (ranks clamped: a valid CTA), then added in order
+      float4 a[4][4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 a = ld_dsmem_f4(base + (uint32_t)tl[k] * (kBM * 4));
-        v[k][0] += a.x;
-        v[k][1] += a.y;
-        v[k][2] += a.z;
-        v[k][3] += a.w;
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t base = map_shared_rank(stage_s, (uint32_t)min(sp0 + j, S - 1));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) a[j][k] = ld_dsmem_f4(base + (uint32_t)tl[k] * (kBM * 4));
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (sp0 + j >= S) break;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[k][0] += a[j][k].x;
+          v[k][1] += a[j][k].y;
+          v[k][2] += a[j][k].z;
+          v[k][3] += a[j][k].w;
+        }
       }
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      if (b0 + 4 * k >= hi) break;  // warp-uniform
+      if (lo + ew + 4 * (k0 + k) >= hi) break;  // warp-uniform
       const int t = tok0 + tl[k];
       float* vv = v[k];
       if constexpr (qkv) {
@@ -617,11 +661,7 @@ __device__ __forceinline__ void dec_finish(const TcParams& p, const Unit& un, in
         }
       } else {
         // the residual stream, summed in fp32 and rounded once
-        float4 r = side0[k];
-        if (!e.resid_f32) {
-          const float2 a = unpack_bf16x2(__float_as_uint(r.x)), b = unpack_bf16x2(__float_as_uint(r.y));
-          r = make_float4(a.x, a.y, b.x, b.y);
-        }
+        const float4 r = side0[k];
         const float o0 = r.x + vv[0], o1 = r.y + vv[1], o2 = r.z + vv[2], o3 = r.w + vv[3];
         const size_t i = (size_t)t * e.ldo + f0 + 4 * lane;
         if (fok) {
@@ -643,6 +683,31 @@ __device__ __forceinline__ void dec_finish(const TcParams& p, const Unit& un, in
         if (e.bump_lens && un.m_tile == 0 && lane == 0) atomicAdd(e.bump_lens + t, 1);  // no round trip
       }
     }
+  };
+  // tokens whose inputs were loaded during the main loop: compile-time indices, registers only
+#pragma unroll
+  for (int kb = 0; kb < kDecPre / 4; ++kb) {
+    const int k0 = 4 * kb;
+    if (lo + ew + 4 * k0 >= hi) break;  // warp-uniform
+    int tl[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) tl[k] = min(lo + ew + 4 * (k0 + k), hi - 1);
+    const float4 s0[4] = {sd.a[k0], sd.a[k0 + 1], sd.a[k0 + 2], sd.a[k0 + 3]};
+    const float4 s1[4] = {sd.b[k0], sd.b[k0 + 1], sd.b[k0 + 2], sd.b[k0 + 3]};
+    const int ps[4] = {sd.pos[k0], sd.pos[k0 + 1], sd.pos[k0 + 2], sd.pos[k0 + 3]};
+    step(k0, tl, s0, s1, ps);
+  }
+  // the rest (tiles of more than 32 tokens per CTA), inputs loaded here
+#pragma unroll 1
+  for (int k0 = kDecPre; lo + ew + 4 * k0 < hi; k0 += 4) {
+    int tl[4], ps[4];
+    float4 s0[4], s1[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      tl[k] = min(lo + ew + 4 * (k0 + k), hi - 1);
+      dec_token_inputs<EPI>(p, un, tok0, tl[k], lane, s0[k], s1[k], ps[k]);
+    }
+    step(k0, tl, s0, s1, ps);
   }
 }
 
@@ -697,6 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const uint32_t tmem_base = *tmem_holder;
   const int bn_rows = p.b_paired ? BN / 2 : BN;
   const unsigned long long budget = p.wait_ns;
+  DecSide dec_side;  // decode finishers only (epilogue warps)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -826,6 +892,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else {
     // ---------------- epilogue warps 2..5: TMEM lane quarter = warp % 4
     pdl_wait();  // the epilogue reads and writes activations of earlier kernels
+    if constexpr (is_dec_epi<EPI>())  // the finisher's per-token inputs, while the main loop runs
+      dec_load_side<BN, EPI>(p, decode_unit(p, blockIdx.x, bn_rows), warp - 2, lane, dec_side);
     const int quarter = warp & 3;
     int it = 0;
     bool failed = false;
@@ -859,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     __syncwarp();
     cluster_sync_all();
     if (warp >= 2) dec_finish<BN, EPI>(p, decode_unit(p, blockIdx.x, bn_rows), warp - 2, lane,
-                                       reinterpret_cast<const float*>(smem));
+                                       reinterpret_cast<const float*>(smem), dec_side);
     __syncwarp();
     cluster_sync_all();
   }
