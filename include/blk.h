@@ -97,11 +97,14 @@ typedef struct {
   const void* prepared; /* NULL, or the buffer blk_prepare_weights filled for these weights */
 } blk_weights;
 
-/* KV cache for decode: k, v are [batch, Hkv, capacity, d] in the descriptor's
- * dtype, holding keys AFTER k_norm and RoPE. lens is a device int
- * array [batch]: positions already filled. A decode step writes its new key and
- * value at slot lens[b], attends over lens[b] + 1 keys and then increments
- * lens[b] on the device. */
+/* KV cache: k, v are [batch, Hkv, capacity, d] in the descriptor's dtype,
+ * holding keys AFTER k_norm and RoPE. lens is a device int array [batch]:
+ * positions already filled. A forward over T new tokens per sequence puts token
+ * t at position lens[b] + t, writes its key and value at slot lens[b] + t,
+ * lets it attend to slots 0 .. lens[b] + t (causal over the cache and the new
+ * tokens) and then adds T to lens[b] on the device. T == 1 is a decode step;
+ * T > 1 is a prefill chunk (bf16 path). The pages have no cache: this is the
+ * prefill block restricted to the new rows, earlier keys read from the cache. */
 typedef struct {
   void *k, *v;
   int capacity;
@@ -147,18 +150,21 @@ blk_status blk_prepare_weights(blk_handle* h, const blk_weights* w, void* prepar
 blk_status blk_destroy(blk_handle* h);
 
 /* Bytes of caller-owned device workspace blk_forward needs for this batch and
- * sequence length (seq == 1 with a cache is a decode step; pass decode != 0).
+ * sequence length; decode != 0 when a cache is passed (a decode step when
+ * seq == 1; a prefill chunk needs the same as a prefill of seq tokens).
  * Returns 0 for invalid sizes. */
 size_t blk_workspace_bytes(const blk_handle* h, int batch, int seq, int decode);
 
 /* The whole block: out[B,T,D] = block(x[B,T,D]).
  * cache == NULL: prefill, positions 0..T-1 per sequence, causal.
- * cache != NULL: decode step, T must be 1; see blk_kv_cache.
+ * cache != NULL: T new tokens per sequence over the cache (see blk_kv_cache):
+ * a decode step (T == 1) or a prefill chunk (T > 1; bf16 only; its keys and
+ * values go to the cache, so the key/value taps are refused).
  * workspace: device scratch of at least blk_workspace_bytes(h, B, T, cache!=NULL).
  * out must not alias x. taps may be NULL. Errors: INVALID_ARG, ALIGNMENT,
- * UNSUPPORTED, WORKSPACE, CACHE_FULL (checked on the host only when the
- * caller passes host_lens_max >= 0: the largest lens[b] before the step),
- * CUDA. */
+ * UNSUPPORTED, WORKSPACE, CACHE_FULL (checked on the host when the caller
+ * passes host_lens_max >= 0, the largest lens[b] before the call; a prefill
+ * chunk requires it), CUDA. */
 blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const blk_weights* w,
                        blk_kv_cache* cache, int host_lens_max, void* out, void* workspace,
                        size_t workspace_bytes, const blk_taps* taps, void* stream);

@@ -194,7 +194,9 @@ class DecoderBlock:
         return self._ws
 
     def forward(self, x, weights, cache=None, out=None, workspace=None, taps=None, stream=None, host_lens_max=-1):
-        """out = block(x); x [B, T, D] device tensor. cache: dict(k, v, lens) for a decode step."""
+        """out = block(x); x [B, T, D] device tensor. cache: dict(k, v, lens): T new tokens per
+        sequence after lens[b] cached positions (a decode step for T == 1, a prefill chunk for
+        T > 1, which needs host_lens_max = max(lens))."""
         import torch
         B, T, _ = x.shape
         if out is None:

@@ -45,6 +45,10 @@ struct AttnParams {
   void* o;
   int o_f16;
   int B, H, Hkv, T, n_qtiles;
+  // K/V rows per (sequence, KV head): T, or a cache's capacity; q_off: positions already
+  // in that cache per sequence (the T queries sit at q_off[b] ..), or null for 0
+  int kv_stride;
+  const int* q_off;
   float sl2;
   DevStatus* status;
   unsigned long long wait_ns;
@@ -95,9 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int kvh = h / (p.H / p.Hkv);
   const int m0 = qt * kBQ;
   const int kv_end = min(p.T, m0 + kBQ);
-  const int n_tiles = (kv_end + kBKeys - 1) / kBKeys;
   const int q_row = (b * p.H + h) * p.T + m0;
-  const int kv_row = (b * p.Hkv + kvh) * p.T;
+  const int kv_row = (b * p.Hkv + kvh) * p.kv_stride;
   const unsigned long long budget = p.wait_ns;
 
   if (threadIdx.x == 0) {
@@ -125,8 +128,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  pdl_wait();  // q, k, v come from the previous kernel
-  const uint32_t tmem = *tmem_holder;  // S0: cols [0,128), S1: [128,256), O: [256,384)
+  pdl_wait();  // q, k, v (and the cache positions) come from earlier kernels
+  const uint32_t tmem = *tmem_holder;
+  const int off = p.q_off ? p.q_off[b] : 0;  // keys 0 .. off - 1 are earlier positions in the cache
+  const int n_keys = off + kv_end;           // keys this query tile can see
+  const int n_tiles = (n_keys + kBKeys - 1) / kBKeys;  // S0: cols [0,128), S1: [128,256), O: [256,384)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -237,12 +243,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int c = 0; c < kBKeys; c += 16) tmem_ld16(tmem + lane_off + s * kBKeys + c, *reinterpret_cast<float(*)[16]>(&x[c]));
       tc_wait_ld();
       const int n0 = j * kBKeys;
-      // raw scores: masked entries become -inf (only tiles on the diagonal or past T)
-      if ((n0 + kBKeys - 1 > m0) || (n0 + kBKeys > p.T)) {
-        const int lim = min(qi, p.T - 1) - n0;  // keys n0 + c with c <= lim are visible
+      // raw scores: masked entries become -inf (only tiles on the diagonal or past the last key)
+      if ((n0 + kBKeys - 1 > off + m0) || (n0 + kBKeys > off + p.T)) {
+        const int lim = off + min(qi, p.T - 1) - n0;  // keys n0 + c with c <= lim are visible
 #pragma unroll
         for (int c = 0; c < kBKeys; ++c)
           if (c > lim) x[c] = -INFINITY;
+      }
+      if (n0 + kBKeys > n_keys && r >= n_keys - n0) {
+        // V rows past the last key may hold anything (unused cache slots): zero them, so that
+        // P = 0 meets finite values in the PV product (the fence below orders this for the MMA)
+        uint8_t* vrow = sV + s * kTile + r * 128;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16) *reinterpret_cast<uint4*>(vrow + hb * kSub + c16 * 16) = make_uint4(0, 0, 0, 0);
       }
       float mx[8];
 #pragma unroll
@@ -348,16 +363,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
 cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int T,
                                    int d, bool f16, bool o_f16, DevStatus* st, unsigned long long wait_ns,
-                                   cudaStream_t s, const char** why) {
+                                   cudaStream_t s, const char** why, const int* q_off, int kv_stride) {
   if (d != kD) {
     *why = "tcgen05 attention: head_dim must be 128";
     return cudaErrorInvalidValue;
   }
   if (B <= 0 || T <= 0) return cudaSuccess;
+  if (kv_stride <= 0) kv_stride = T;
+  if (!q_off && kv_stride != T) {
+    *why = "tcgen05 attention: K/V rows per head differ from T only with cache positions";
+    return cudaErrorInvalidValue;
+  }
   AttnParams p;
   memset(static_cast<void*>(&p), 0, sizeof(p));
-  if (!make_tma_2d_16b(&p.tq, q, B * H * T, kD, kBQ, f16) || !make_tma_2d_16b(&p.tk, k, B * Hkv * T, kD, kBKeys, f16) ||
-      !make_tma_2d_16b(&p.tv, v, B * Hkv * T, kD, kBKeys, f16)) {
+  if (!make_tma_2d_16b(&p.tq, q, B * H * T, kD, kBQ, f16) ||
+      !make_tma_2d_16b(&p.tk, k, B * Hkv * kv_stride, kD, kBKeys, f16) ||
+      !make_tma_2d_16b(&p.tv, v, B * Hkv * kv_stride, kD, kBKeys, f16)) {
     *why = "cuTensorMapEncodeTiled failed for q/k/v";
     return cudaErrorInvalidValue;
   }
@@ -367,6 +388,8 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
   p.H = H;
   p.Hkv = Hkv;
   p.T = T;
+  p.kv_stride = kv_stride;
+  p.q_off = q_off;
   p.n_qtiles = (T + kBQ - 1) / kBQ;
   p.sl2 = kLog2e / sqrtf((float)kD);
   p.status = st;

@@ -231,8 +231,11 @@ blk_status tc(const blk_handle* h, const TcGemmDesc& g, cudaStream_t s, const ch
   return BLK_OK;
 }
 
+// cache_stride > 0: k and v are a KV cache of cache_stride rows per (sequence, KV head),
+// written at rows pos0[b] + t.
 blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, int B, int T, const int* pos0, void* q,
-                    void* k, void* v, cudaStream_t s, const float* row_scale = nullptr, bool f16 = false) {
+                    void* k, void* v, cudaStream_t s, const float* row_scale = nullptr, bool f16 = false,
+                    int cache_stride = 0) {
   const blk_desc& d = h->d;
   TcGemmDesc g;
   g.na = 1;
@@ -248,6 +251,10 @@ blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, in
   g.epi = Epi::kQkv;
   g.const_op = 2;
   g.e = qkv_epi(h, w, T, pos0, q, k, v);
+  if (cache_stride > 0) {
+    g.e.kv_stride = cache_stride;
+    g.e.kv_at_pos = 1;
+  }
   g.e.row_scale = row_scale;
   g.e.qkv_f16 = f16 ? 1 : 0;
   return tc(h, g, s, "QKV GEMM");
@@ -256,7 +263,8 @@ blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, in
 blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K, const void* W, int N,
                              const void* resid, bool resid_f32, void* out, bool out_f32, void* out2, void* tap,
                              cudaStream_t s, const char* what, void* norm_out = nullptr,
-                             const void* norm_gain = nullptr, float* norm_ss = nullptr, bool f16 = false) {
+                             const void* norm_gain = nullptr, float* norm_ss = nullptr, bool f16 = false,
+                             int* bump_lens = nullptr, int seq = 0) {
   TcGemmDesc g;
   g.na = 1;
   g.a[0] = {a, rows, 0};
@@ -278,6 +286,8 @@ blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K
   g.e.norm_ss = norm_ss;
   g.e.norm_parts = norm_parts(N, g.bn);
   g.e.norm_f16 = f16 ? 1 : 0;  // the MLP-up GEMM that reads norm_out has the same operand type
+  g.e.bump_lens = bump_lens;    // lens[b] += seq after the block (a prefill chunk appended to a cache)
+  g.e.seq = seq;
   g.f16 = f16;
   return tc(h, g, s, what);
 }
@@ -415,8 +425,10 @@ P tap_or(const blk_taps* t, P blk_taps::*m, P dflt) {
 
 // ------------------------------------------------------------------ forward variants
 
+// cache != null: a prefill chunk. The T new tokens of sequence b sit at positions
+// lens[b] .. lens[b] + T - 1, append their K/V to the cache and attend to it.
 blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, const blk_weights* w, void* out,
-                                const Ws& ws, const blk_taps* taps, cudaStream_t s) {
+                                const Ws& ws, const blk_taps* taps, cudaStream_t s, blk_kv_cache* cache = nullptr) {
   // Both RMSNorms are split around the GEMMs they feed: the gain multiplies the
   // GEMM's A rows (x * g1 is x itself when g1 == 1), the per-row 1/rms multiplies
   // the accumulator in the epilogue. q/k/v and P are kept in fp16 (3 more
@@ -430,8 +442,14 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
   prof_mark(h, "norm1_prep", 1, s);
   BLK_TRY(check_cuda(launch_norm_prep(x, w->ln1_g, M, d.hidden, d.eps, ws.y, ws.rs1, nullptr, s), "input norm"));
   prof_mark(h, "qkv_gemm_rope", 1, s);
-  BLK_TRY(bf16_qkv(h, ws.y, w, B, T, nullptr, ws.q, ws.k, ws.v, s, ws.rs1, true));
-  if (taps) {  // the taps are bf16
+  if (cache) {
+    // bf16 q (the cache's K/V are bf16, so the attention runs on bf16 operands); K/V into the cache
+    BLK_TRY(bf16_qkv(h, ws.y, w, B, T, cache->lens, tap_or(taps, &blk_taps::attention_queries, ws.q), cache->k,
+                     cache->v, s, ws.rs1, false, cache->capacity));
+  } else {
+    BLK_TRY(bf16_qkv(h, ws.y, w, B, T, nullptr, ws.q, ws.k, ws.v, s, ws.rs1, true));
+  }
+  if (taps && !cache) {  // the taps are bf16
     const size_t nq = (size_t)M * d.n_heads * d.head_dim, nkv = (size_t)M * d.n_kv_heads * d.head_dim;
     if (taps->attention_queries)
       BLK_TRY(check_cuda(launch_cast_f16_bf16(ws.q, taps->attention_queries, nq, s), "q tap"));
@@ -447,8 +465,12 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
   void* o_buf = f16 ? ws.o : o;
   prof_mark(h, "attention", 1, s);
   const char* why = nullptr;
-  cudaError_t e = launch_attn_prefill_tc(ws.q, ws.k, ws.v, o_buf, B, d.n_heads, d.n_kv_heads, T, d.head_dim, true,
-                                         f16, h->status, (unsigned long long)g_wait_ns.load(), s, &why);
+  cudaError_t e =
+      cache ? launch_attn_prefill_tc(tap_or(taps, &blk_taps::attention_queries, ws.q), cache->k, cache->v, o_buf, B,
+                                     d.n_heads, d.n_kv_heads, T, d.head_dim, false, f16, h->status,
+                                     (unsigned long long)g_wait_ns.load(), s, &why, cache->lens, cache->capacity)
+            : launch_attn_prefill_tc(ws.q, ws.k, ws.v, o_buf, B, d.n_heads, d.n_kv_heads, T, d.head_dim, true, f16,
+                                     h->status, (unsigned long long)g_wait_ns.load(), s, &why);
   BLK_TRY(check_cuda(e, "attention", why));
   if (f16 && taps && taps->attention_head_outputs)
     BLK_TRY(check_cuda(launch_cast_f16_bf16(o_buf, taps->attention_head_outputs,
@@ -463,7 +485,8 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
                       f16 ? &prep : nullptr));
   prof_mark(h, "down_gemm_resid", 1, s);
   BLK_TRY(bf16_linear_resid(h, neur, M, d.ffn, w->w_down, d.hidden, ws.mid, true, out, false, nullptr,
-                            taps ? taps->mlp_output : nullptr, s, "down GEMM"));
+                            taps ? taps->mlp_output : nullptr, s, "down GEMM", nullptr, nullptr, nullptr, false,
+                            cache ? cache->lens : nullptr, T));
   prof_end(h, s);
   return BLK_OK;
 }
@@ -793,7 +816,7 @@ blk_status blk_prepare_weights(blk_handle* h, const blk_weights* w, void* prepar
 size_t blk_workspace_bytes(const blk_handle* h, int batch, int seq, int decode) {
   if (!h || batch <= 0 || seq <= 0) return 0;
   size_t total = 0;
-  carve_forward(h, nullptr, batch, seq, decode != 0, &total);
+  carve_forward(h, nullptr, batch, seq, decode != 0 && seq == 1, &total);  // a chunk: the prefill layout
   return total;
 }
 
@@ -814,10 +837,20 @@ blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const b
     for (void* p : tp)
       if (p && !aligned16(p)) return fail(BLK_ERR_ALIGNMENT, "a tap pointer is not 16-byte aligned");
   }
-  const bool decode = cache != nullptr;
+  const bool decode = cache != nullptr && seq == 1;
+  const bool chunk = cache != nullptr && seq > 1;  // a prefill chunk appended to the cache
   int max_len = 0;
-  if (decode) {
-    if (seq != 1) return fail(BLK_ERR_INVALID_ARG, "a decode step takes seq == 1");
+  if (chunk) {
+    if (d.dtype != BLK_BF16) return fail(BLK_ERR_UNSUPPORTED, "a prefill chunk over a KV cache takes the bf16 path");
+    if (!cache->k || !cache->v || !cache->lens || cache->capacity <= 0)
+      return fail(BLK_ERR_INVALID_ARG, "incomplete KV cache");
+    if (!aligned16(cache->k) || !aligned16(cache->v)) return fail(BLK_ERR_ALIGNMENT, "cache not 16-byte aligned");
+    if (host_lens_max < 0) return fail(BLK_ERR_INVALID_ARG, "a prefill chunk needs host_lens_max (the largest lens)");
+    if (host_lens_max + seq > cache->capacity) return fail(BLK_ERR_CACHE_FULL, "cache capacity exceeded");
+    if (host_lens_max + seq > d.max_seq) return fail(BLK_ERR_INVALID_ARG, "position beyond max_seq");
+    if (taps && (taps->attention_keys || taps->attention_values))
+      return fail(BLK_ERR_UNSUPPORTED, "a prefill chunk writes its keys and values to the cache, not to taps");
+  } else if (decode) {
     if (!cache->k || !cache->v || !cache->lens || cache->capacity <= 0)
       return fail(BLK_ERR_INVALID_ARG, "incomplete KV cache");
     if (!aligned16(cache->k) || !aligned16(cache->v)) return fail(BLK_ERR_ALIGNMENT, "cache not 16-byte aligned");
@@ -839,7 +872,7 @@ blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const b
   prof_begin(h);
   if (d.dtype == BLK_F32) return forward_f32(h, x, batch, seq, w, cache, out, ws, taps, s);
   if (decode) return forward_decode_bf16(h, x, batch, w, cache, max_len, out, ws, taps, s);
-  return forward_prefill_bf16(h, x, batch, seq, w, out, ws, taps, s);
+  return forward_prefill_bf16(h, x, batch, seq, w, out, ws, taps, s, chunk ? cache : nullptr);
 }
 
 struct blk_graph {

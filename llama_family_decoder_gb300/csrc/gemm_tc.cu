@@ -260,7 +260,9 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
           dst = reinterpret_cast<uint16_t*>(e.q) + (((size_t)b * e.n_heads + head) * e.seq + t) * d;
         else
           dst = reinterpret_cast<uint16_t*>(seg == 1 ? e.k : e.v) +
-                (((size_t)b * e.n_kv_heads + head) * e.kv_stride + t) * d;
+                (((size_t)b * e.n_kv_heads + head) * e.kv_stride + (e.kv_at_pos ? pos : t)) * d;
+        // a cache slot past the capacity is never written (the host refuses such calls first)
+        const bool store_ok = row_ok && (seg == 0 || !e.kv_at_pos || (pos >= 0 && pos < e.kv_stride));
         if (seg == 2) {
 #pragma unroll 1
           for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -273,7 +275,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
               v0[j] *= rs;
               v1[j] *= rs;
             }
-            if (row_ok) {
+            if (store_ok) {
               store16_2b(dst + c0, v0, f16);
               store16_2b(dst + c0 + 16, v1, f16);
             }
@@ -314,7 +316,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
             y1[j] = a * sc.x - c * sc.y;
             y2[j] = c * sc.x + a * sc.y;
           }
-          if (row_ok) {
+          if (store_ok) {
             store16_2b(dst + i0, y1, f16);
             store16_2b(dst + 64 + i0, y2, f16);
           }
@@ -475,6 +477,9 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
       }
       if constexpr (EPI == (int)Epi::kResid) {
         if (e.norm_ss && row_ok) e.norm_ss[(size_t)row * e.norm_parts + un.b_row0 / BN] = ss_part;
+        // a prefill chunk appended to a KV cache: its sequence's length grows by seq, once
+        if (e.bump_lens && row_ok && un.b_row0 == 0 && un.b_seg == 0 && row % e.seq == e.seq - 1)
+          atomicAdd(e.bump_lens + row / e.seq, e.seq);
       }
     }
   }

@@ -84,6 +84,7 @@ struct TcEpiArgs {
   const float2* rope = nullptr;  // [max_pos][head_dim/2] (cos, sin)
   int rope_max_pos = 0;
   const int* pos0 = nullptr;     // [B] first position of each sequence, or null
+  int kv_at_pos = 0;             // kQkv: k/v go to row pos0[b] + t of a cache (kv_stride rows), not row t
   int qk_norm = 0;
   const float* row_scale = nullptr;  // kQkv: per-row factor of the accumulator (the input norm's 1/rms)
   int qkv_f16 = 0;                   // kQkv: store q/k/v as fp16 (else bf16)
@@ -107,7 +108,8 @@ struct TcEpiArgs {
   int n_tok = 0;    // valid tokens (B operand rows)
   // decode finishers
   const int* lens = nullptr;  // kDecQkv: positions already in the cache, per sequence
-  int* bump_lens = nullptr;   // kDecResid: lens[t] += 1 once per token (the tile of m_tile 0)
+  int* bump_lens = nullptr;   // kDecResid: lens[t] += 1 once per token (the tile of m_tile 0);
+                              // kResid: lens[b] += seq once per sequence (its last row, first N tile)
 };
 
 struct TcGemmDesc {
@@ -174,9 +176,13 @@ cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, floa
 
 // tcgen05/TMEM flash attention (prefill, causal, kv_len == T, head_dim 128).
 // f16: q, k, v are fp16 (else bf16); o_f16: o is fp16 (else bf16).
+// With q_off (positions already in a KV cache, per sequence) the T queries of sequence b sit at
+// q_off[b] .. q_off[b] + T - 1 and attend to cache rows 0 .. q_off[b] + t of k/v, which hold
+// kv_stride rows per (sequence, KV head); without it, kv_stride == T.
 cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int T,
                                    int d, bool f16, bool o_f16, DevStatus* st, unsigned long long wait_ns,
-                                   cudaStream_t s, const char** why);
+                                   cudaStream_t s, const char** why, const int* q_off = nullptr,
+                                   int kv_stride = 0);
 
 // Decode (Tq == 1), split over the keys: partial results in ws, combined into o.
 size_t attn_decode_ws_bytes(int B, int H, int d, int max_splits);

@@ -18,4 +18,5 @@ from .block import (  # noqa: F401
     block_forward,
     mlp,
     decode_step,
+    prefill_with_cache,
 )

@@ -321,6 +321,37 @@ def block_forward(cfg, w, x, rows=None, positions=None, return_pattern=False):
     return {key: np.stack([t[key] for t in per_batch]) for key in per_batch[0]}
 
 
+def prefill_with_cache(cfg, w, x, cache_k, cache_v, lens):
+    """T new tokens per sequence after lens[b] cached positions (a prefill chunk).
+
+    x: [B, T, D]; cache_k, cache_v: [B, Hkv, capacity, d] holding keys (after
+    k_norm and RoPE) and values for positions 0 .. lens[b]-1. Token t of
+    sequence b sits at position lens[b] + t; its key and value join the cache at
+    slot lens[b] + t, and it attends causally over slots 0 .. lens[b] + t. The
+    pages define no cache: this is the prefill block on the whole sequence,
+    restricted to the new rows, with the earlier keys read from the cache.
+
+    Returns the taps of the new rows ([B, T, ...]) plus new_keys / new_values
+    [B, Hkv, T, d].
+    """
+    x = np.asarray(x, dtype=F64)
+    B, T, D = x.shape
+    per_batch = []
+    for b in range(B):
+        L = int(lens[b])
+        pos = np.arange(L, L + T)
+        h = rms_norm(x[b], w["input_layernorm"], cfg.rms_norm_eps)  # [T, D]
+        k_new, v_new = _project_kv(cfg, w, h, pos)  # [Hkv, T, d]
+        q = _project_q(cfg, w, h, pos)  # [H, T, d]
+        k_all = np.concatenate([np.asarray(cache_k[b, :, :L], dtype=F64), k_new], axis=1)
+        v_all = np.concatenate([np.asarray(cache_v[b, :, :L], dtype=F64), v_new], axis=1)
+        heads = causal_gqa_attention(q, k_all, v_all, pos, np.arange(L + T))
+        taps = _finish_rows(cfg, w, x[b], heads)
+        taps.update(attention_norm_output=h, attention_queries=q, new_keys=k_new, new_values=v_new)
+        per_batch.append(taps)
+    return {key: np.stack([t[key] for t in per_batch]) for key in per_batch[0]}
+
+
 def decode_step(cfg, w, x, cache_k, cache_v, lens):
     """One decode step: one new token per sequence attends to its KV cache.
 

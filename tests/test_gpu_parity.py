@@ -243,6 +243,62 @@ def test_decode_step_bf16_variants_and_taps(act, qk_norm, batch, ffn):
         assert err <= max(TOL["bf16"], 2 * floor + 5e-3), (name, err, floor)
 
 
+@pytest.mark.parametrize("act,qk_norm,prepared", [("silu", False, False), ("xielu", True, False),
+                                                  ("silu", False, True)])
+def test_prefill_chunk_over_the_cache(act, qk_norm, prepared):
+    # T new tokens per sequence after ragged cached lengths: one chunk within a tile, one across
+    # tiles, one from an empty cache. Unused cache slots hold NaN: nothing of them may leak.
+    wl = Workload(f"chunk_{act}", "bf16", 3, 150, 512, 8, 2, 128, 1000, act, qk_norm=qk_norm, seed=26)
+    lens = [0, 37, 200]
+    cap = 400
+    w = make_weights(wl, gain_std=0.1 if qk_norm else 0.0)
+    x = make_input(wl)
+    g = torch.Generator().manual_seed(27)
+    kc = torch.full((wl.batch, wl.num_kv_heads, cap, wl.head_dim), float("nan"), dtype=torch.bfloat16)
+    vc = kc.clone()
+    for b, L in enumerate(lens):
+        kc[b, :, :L] = torch.randn(wl.num_kv_heads, L, wl.head_dim, generator=g).to(torch.bfloat16)
+        vc[b, :, :L] = torch.randn(wl.num_kv_heads, L, wl.head_dim, generator=g).to(torch.bfloat16)
+    blk = DecoderBlock.from_workload(wl, max_seq=cap + 1)
+    wd = to_dev(w)
+    if prepared:
+        wd = blk.prepare(wd)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    tb = _tap_buffers(wl, torch.bfloat16)
+    tb.pop("attention_keys")
+    tb.pop("attention_values")
+    out = blk.forward(x.to(DEV), wd, cache={"k": kd, "v": vd, "lens": lens_d}, host_lens_max=max(lens), taps=tb)
+    torch.cuda.synchronize()
+    assert blk.last_status() == 0
+    ref = oracle.prefill_with_cache(cfg_of(wl), weights_np(w), np64(x), np64(kc), np64(vc), np.array(lens))
+    err, floor = rel_err(out, ref["layer_output"]), bf16_floor(ref["layer_output"])
+    print(f"chunk {act}: max|err|/RMS {err:.4f} (bf16 floor {floor:.4f})")
+    assert err <= TOL["bf16"]
+    assert lens_d.tolist() == [L + wl.seq for L in lens]
+    T = wl.seq
+    kd_c, vd_c = kd.cpu(), vd.cpu()
+    for b, L in enumerate(lens):
+        assert rel_err(kd_c[b, :, L:L + T], ref["new_keys"][b]) <= TOL["bf16"]
+        assert rel_err(vd_c[b, :, L:L + T], ref["new_values"][b]) <= TOL["bf16"]
+        assert torch.equal(kd_c[b, :, :L], kc[b, :, :L])  # the cached prefix is untouched
+        assert torch.isnan(kd_c[b, :, L + T:].float()).all()  # nothing written past the chunk
+    for name in ("attention_output", "layer_mid", "mlp_neurons", "mlp_output"):
+        r = ref[name]
+        e2, f2 = rel_err(tb[name], r), bf16_floor(r)
+        assert e2 <= max(TOL["bf16"], 2 * f2 + 5e-3), (name, e2, f2)
+    assert rel_err(tb["attention_queries"], ref["attention_queries"]) <= TOL["bf16"]
+
+
+def test_prefill_chunk_needs_the_host_lengths():
+    wl = Workload("chunk_refused", "bf16", 1, 4, 512, 8, 2, 128, 1000, "silu", seed=28)
+    blk = DecoderBlock.from_workload(wl, max_seq=64)
+    kd = torch.zeros(1, 2, 32, 128, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(RuntimeError):
+        blk.forward(make_input(wl).to(DEV), to_dev(make_weights(wl)),
+                    cache={"k": kd, "v": kd.clone(), "lens": torch.zeros(1, dtype=torch.int32, device=DEV)})
+
+
 def test_decode_matches_prefill_last_row():
     wl = Workload("small_prefill_decode", "bf16", 2, 96, 512, 4, 2, 128, 1000, "silu", seed=23)
     w = to_dev(make_weights(wl))

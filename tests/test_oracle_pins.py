@@ -431,3 +431,45 @@ def test_decode_equals_last_prefill_row():
     for b in range(B):
         fb = oracle.block_forward(cfg, w, x[b:b + 1, : lens[b] + 1])
         np.testing.assert_allclose(dec["layer_output"][b], fb["layer_output"][0, -1], rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_chunk_equals_the_full_prefill_rows():
+    # A prefill chunk over a cache that holds the keys/values of the sequence's
+    # earlier tokens gives the full prefill's rows for the chunk's tokens.
+    rng = np.random.default_rng(15)
+    cfg = _tiny("silu", True, H=4, Hkv=2)
+    w = _weights(cfg, rng)
+    B, T, cap = 3, 5, 16
+    lens = np.array([0, 3, 9])
+    xs = rng.standard_normal((B, cap, cfg.hidden_size))
+    ck = np.zeros((B, 2, cap, 4))
+    cv = np.zeros((B, 2, cap, 4))
+    fulls = []
+    for b in range(B):
+        fb = oracle.block_forward(cfg, w, xs[b:b + 1, : lens[b] + T])
+        fulls.append(fb)
+        ck[b, :, : lens[b]] = fb["attention_keys"][0, :, : lens[b]]
+        cv[b, :, : lens[b]] = fb["attention_values"][0, :, : lens[b]]
+    x = np.stack([xs[b, lens[b]: lens[b] + T] for b in range(B)])
+    ch = oracle.prefill_with_cache(cfg, w, x, ck, cv, lens)
+    for b in range(B):
+        rows = slice(lens[b], lens[b] + T)
+        np.testing.assert_allclose(ch["layer_output"][b], fulls[b]["layer_output"][0, rows], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(ch["new_keys"][b], fulls[b]["attention_keys"][0, :, rows], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(ch["new_values"][b], fulls[b]["attention_values"][0, :, rows], rtol=1e-12,
+                                   atol=1e-14)
+
+
+def test_prefill_chunk_of_one_token_is_a_decode_step():
+    rng = np.random.default_rng(16)
+    cfg = _tiny("xielu", False, H=2, Hkv=1)
+    w = _weights(cfg, rng)
+    B, cap = 2, 7
+    lens = np.array([4, 1])
+    ck = rng.standard_normal((B, 1, cap, 4))
+    cv = rng.standard_normal((B, 1, cap, 4))
+    x = rng.standard_normal((B, 1, cfg.hidden_size))
+    ch = oracle.prefill_with_cache(cfg, w, x, ck, cv, lens)
+    dec = oracle.decode_step(cfg, w, x[:, 0], ck, cv, lens)
+    np.testing.assert_allclose(ch["layer_output"][:, 0], dec["layer_output"], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(ch["new_keys"][:, :, 0], dec["new_key"], rtol=1e-13, atol=1e-14)
