@@ -68,6 +68,17 @@ typedef enum { BLK_F32 = 0, BLK_BF16 = 1 } blk_dtype;
 /* Block description, in the pages' config keys (hidden_size, num_attention_heads,
  * num_key_value_heads, head_dim, intermediate_size, hidden_act, rms_norm_eps,
  * rope_theta). */
+/* Stretched rotaries (the pages name them with their settings: YaRN factor 20
+ * over 4096 positions on "arcee", "Loading and positions"; llama3 factor 8 over
+ * 8192, rope_theta 12,000,000 on "apertus"). Both keep fast components, divide
+ * slow ones by the factor and blend in between, after their published
+ * definitions; YaRN also multiplies cos and sin by 0.1 ln(factor) + 1. */
+typedef enum {
+  BLK_ROPE_PLAIN = 0,
+  BLK_ROPE_YARN = 1,   /* rope_low / rope_high: turns over the original context (1 and 32) */
+  BLK_ROPE_LLAMA3 = 2  /* rope_low / rope_high: low_freq_factor and high_freq_factor (1 and 4) */
+} blk_rope_type;
+
 typedef struct {
   int hidden;        /* hidden_size D */
   int n_heads;       /* num_attention_heads H */
@@ -85,6 +96,10 @@ typedef struct {
   blk_dtype dtype;   /* storage type of every tensor; accumulation is fp32 */
   int max_batch;     /* largest batch a call may pass */
   int max_seq;       /* largest rotary position + 1 a call may use (prefill length, or cache length + 1) */
+  blk_rope_type rope_type;  /* BLK_ROPE_PLAIN ignores the four fields below */
+  float rope_factor;        /* >= 1 */
+  int rope_orig_max_pos;    /* the original context length the scaling stretches */
+  float rope_low, rope_high;
 } blk_desc;
 
 /* Block weights: device pointers in the descriptor's dtype.

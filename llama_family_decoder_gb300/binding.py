@@ -24,7 +24,10 @@ class blk_desc(ctypes.Structure):
     _fields_ = [("hidden", c_int), ("n_heads", c_int), ("n_kv_heads", c_int), ("head_dim", c_int), ("ffn", c_int),
                 ("rope_theta", c_float), ("eps", c_float), ("act", c_int), ("xielu_alpha_p", c_float),
                 ("xielu_alpha_n", c_float), ("xielu_beta", c_float), ("xielu_eps", c_float), ("qk_norm", c_int),
-                ("dtype", c_int), ("max_batch", c_int), ("max_seq", c_int)]
+                ("dtype", c_int), ("max_batch", c_int), ("max_seq", c_int), ("rope_type", c_int),
+                ("rope_factor", c_float), ("rope_orig_max_pos", c_int), ("rope_low", c_float), ("rope_high", c_float)]
+
+ROPE_TYPES = {"yarn": 1, "llama3": 2}
 
 
 class blk_weights(ctypes.Structure):
@@ -145,10 +148,12 @@ class DecoderBlock:
 
     def __init__(self, hidden, n_heads, n_kv_heads, head_dim, ffn, act="silu", dtype="bf16", qk_norm=False,
                  rope_theta=10000.0, eps=1e-5, xielu_alpha_p=0.8, xielu_alpha_n=0.8, xielu_beta=0.5,
-                 xielu_eps=-1e-6, max_batch=64, max_seq=4096):
+                 xielu_eps=-1e-6, max_batch=64, max_seq=4096, rope_scaling=None):
+        # rope_scaling: None, or (kind, factor, original_max_position, low, high), kind "yarn" | "llama3"
+        rs = (ROPE_TYPES[rope_scaling[0]], *rope_scaling[1:]) if rope_scaling else (0, 1.0, 0, 0.0, 0.0)
         self.desc = blk_desc(hidden, n_heads, n_kv_heads, head_dim, ffn, rope_theta, eps, ACTS[act],
                              xielu_alpha_p, xielu_alpha_n, xielu_beta, xielu_eps, int(bool(qk_norm)), DTYPES[dtype],
-                             max_batch, max_seq)
+                             max_batch, max_seq, rs[0], float(rs[1]), int(rs[2]), float(rs[3]), float(rs[4]))
         h = c_void_p()
         _check(lib().blk_create(ctypes.byref(self.desc), ctypes.byref(h)))
         self.handle = h
@@ -159,7 +164,8 @@ class DecoderBlock:
         return cls(wl.hidden_size, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.intermediate_size,
                    act=wl.hidden_act, dtype=wl.dtype, qk_norm=wl.qk_norm, rope_theta=wl.rope_theta,
                    eps=wl.rms_norm_eps, xielu_alpha_p=wl.xielu_alpha_p, xielu_alpha_n=wl.xielu_alpha_n,
-                   max_batch=max_batch or wl.batch, max_seq=max_seq or max(wl.seq, wl.cache_len + 1))
+                   max_batch=max_batch or wl.batch, max_seq=max_seq or max(wl.seq, wl.cache_len + 1),
+                   rope_scaling=wl.rope_scaling)
 
     def close(self):
         if self.handle:

@@ -724,6 +724,12 @@ blk_status blk_create(const blk_desc* desc, blk_handle** out) {
   if (d.n_heads % d.n_kv_heads) return fail(BLK_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
   if (d.head_dim % 2) return fail(BLK_ERR_INVALID_ARG, "head_dim must be even");
   if (!(d.eps > 0.f) || !(d.rope_theta > 0.f)) return fail(BLK_ERR_INVALID_ARG, "eps and rope_theta must be > 0");
+  if (d.rope_type != BLK_ROPE_PLAIN) {
+    if (d.rope_type != BLK_ROPE_YARN && d.rope_type != BLK_ROPE_LLAMA3)
+      return fail(BLK_ERR_INVALID_ARG, "unknown rope_type");
+    if (!(d.rope_factor >= 1.f) || d.rope_orig_max_pos <= 0 || !(d.rope_low > 0.f) || !(d.rope_high > d.rope_low))
+      return fail(BLK_ERR_INVALID_ARG, "rope scaling needs factor >= 1, original positions > 0, high > low > 0");
+  }
   if (d.act != BLK_ACT_SWIGLU && d.act != BLK_ACT_RELU2 && d.act != BLK_ACT_XIELU)
     return fail(BLK_ERR_INVALID_ARG, "unknown activation");
   if (d.dtype != BLK_F32 && d.dtype != BLK_BF16) return fail(BLK_ERR_INVALID_ARG, "unknown dtype");
@@ -750,13 +756,37 @@ blk_status blk_create(const blk_desc* desc, blk_handle** out) {
     delete h;
     return cuda_fail(e, "blk_create: device query");
   }
+  // RoPE table [max_seq][head_dim / 2] of (cos, sin), in double: inv_freq_i = theta^(-2i/d),
+  // stretched by the descriptor's scaling (a frequency f of wavelength lam = 2 pi / f makes
+  // r = L / lam turns over the original context L; fast components are kept, slow ones
+  // divided by the factor s, and the rest blended: (1 - g) f / s + g f)
   const int half = d.head_dim / 2;
+  std::vector<double> inv_freq(half);
+  const double s_f = d.rope_factor, L = d.rope_orig_max_pos, lo = d.rope_low, hi = d.rope_high;
+  for (int i = 0; i < half; ++i) {
+    const double f = std::pow((double)d.rope_theta, -2.0 * i / (double)d.head_dim);
+    const double turns = d.rope_type == BLK_ROPE_PLAIN ? 0.0 : L * f / (2.0 * M_PI);
+    double fi = f;
+    if (d.rope_type == BLK_ROPE_LLAMA3) {
+      const double lam = 2.0 * M_PI / f;
+      if (lam > L / lo) {
+        fi = f / s_f;
+      } else if (lam >= L / hi) {
+        const double g = (turns - lo) / (hi - lo);
+        fi = (1.0 - g) * f / s_f + g * f;
+      }
+    } else if (d.rope_type == BLK_ROPE_YARN) {
+      const double g = std::min(1.0, std::max(0.0, (turns - lo) / (hi - lo)));
+      fi = (1.0 - g) * f / s_f + g * f;
+    }
+    inv_freq[i] = fi;
+  }
+  const double att = d.rope_type == BLK_ROPE_YARN ? 0.1 * std::log(s_f) + 1.0 : 1.0;  // YaRN's sqrt(1/t)
   std::vector<float2> table((size_t)d.max_seq * half);
   for (int p = 0; p < d.max_seq; ++p)
     for (int i = 0; i < half; ++i) {
-      const double inv_freq = std::pow((double)d.rope_theta, -2.0 * i / (double)d.head_dim);
-      const double ang = (double)p * inv_freq;
-      table[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      const double ang = (double)p * inv_freq[i];
+      table[(size_t)p * half + i] = make_float2((float)(att * std::cos(ang)), (float)(att * std::sin(ang)));
     }
   e = cudaMalloc(&h->rope, table.size() * sizeof(float2));
   if (e == cudaSuccess) e = cudaMemcpy(h->rope, table.data(), table.size() * sizeof(float2), cudaMemcpyHostToDevice);

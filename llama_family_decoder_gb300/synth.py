@@ -40,6 +40,7 @@ class Workload:
     cache_len: int = 0  # decode: positions already in the KV cache
     rms_norm_eps: float = 1e-5
     rope_theta: float = 10000.0
+    rope_scaling: tuple | None = None  # (kind, factor, original positions, low, high) of a stretched rotary
     xielu_alpha_p: float = 0.8
     xielu_alpha_n: float = 0.8
     seed: int = 0

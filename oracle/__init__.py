@@ -6,6 +6,8 @@ it. It shares no code with the CUDA path under ``llama_family_decoder_gb300``.
 """
 from .block import (  # noqa: F401
     BlockConfig,
+    RopeScaling,
+    rope_attention_factor,
     rms_norm,
     rope_inv_freq,
     rope,

@@ -45,6 +45,33 @@ F64 = np.float64
 
 
 @dataclass(frozen=True)
+class RopeScaling:
+    """A stretched rotary (the pages name the settings, not the formulas; these are
+    the published definitions).
+
+    kind "yarn": YaRN's by-parts interpolation, "arcee" page ("Loading and
+    positions": YaRN, factor 20 over 4096 original positions). low / high are
+    YaRN's alpha / beta in rotations over the original context (1 and 32).
+    kind "llama3": the frequency-dependent rule of Llama 3.1's rope_type llama3,
+    "apertus" page ("The default load runs the same attention as eager": factor 8
+    over 8192 original positions, rope_theta 12,000,000). low / high are its
+    low_freq_factor / high_freq_factor (1 and 4).
+    """
+
+    kind: str
+    factor: float
+    original_max_position: float
+    low: float
+    high: float
+
+    def __post_init__(self):
+        if self.kind not in ("yarn", "llama3"):
+            raise ValueError(f"unknown rope scaling {self.kind!r}")
+        if not (self.factor >= 1.0 and self.original_max_position > 0 and self.high > self.low > 0):
+            raise ValueError("rope scaling needs factor >= 1, original positions > 0 and high > low > 0")
+
+
+@dataclass(frozen=True)
 class BlockConfig:
     """The block's configuration, in the pages' config-key vocabulary.
 
@@ -66,6 +93,7 @@ class BlockConfig:
     xielu_alpha_n: float = 0.8  # effective value (after beta + softplus)
     xielu_beta: float = 0.5
     xielu_eps: float = -1e-6
+    rope_scaling: "RopeScaling | None" = None  # a stretched rotary, or None for the plain one
 
     def __post_init__(self):
         if self.hidden_act not in ("silu", "relu2", "xielu"):
@@ -93,26 +121,57 @@ def rms_norm(x, gain, eps):
     return x / np.sqrt(mean_sq + eps) * np.asarray(gain, dtype=F64)
 
 
-def rope_inv_freq(head_dim, theta):
-    """inv_freq_i = theta^(-2i/head_dim), i = 0 .. head_dim/2 - 1."""
+def rope_inv_freq(head_dim, theta, scaling=None):
+    """inv_freq_i = theta^(-2i/head_dim), i = 0 .. head_dim/2 - 1, then stretched.
+
+    With a scaling of factor s over L original positions, a frequency f has the
+    wavelength lam = 2 pi / f and makes r = L / lam turns over the original
+    context. Both published rules keep fast components, divide slow ones by s,
+    and blend in between:
+      llama3: kept when lam < L / high, divided when lam > L / low, otherwise
+              (1 - g) f / s + g f with g = (L / lam - low) / (high - low);
+      yarn:   g = clip((r - low) / (high - low), 0, 1), f' = (1 - g) f / s + g f
+              (YaRN's ramp over the turn count: alpha = low, beta = high).
+    """
     i = np.arange(head_dim // 2, dtype=F64)
-    return np.power(F64(theta), -2.0 * i / head_dim)
+    f = np.power(F64(theta), -2.0 * i / head_dim)
+    if scaling is None:
+        return f
+    s, L, lo, hi = scaling.factor, scaling.original_max_position, scaling.low, scaling.high
+    lam = 2.0 * np.pi / f
+    if scaling.kind == "llama3":
+        g = (L / lam - lo) / (hi - lo)
+        out = (1.0 - g) * f / s + g * f
+        out = np.where(lam < L / hi, f, out)
+        return np.where(lam > L / lo, f / s, out)
+    g = np.clip((L / lam - lo) / (hi - lo), 0.0, 1.0)
+    return (1.0 - g) * f / s + g * f
 
 
-def rope(x, positions, theta):
+def rope_attention_factor(scaling):
+    """YaRN scales cos and sin (so q.k by its square) by 0.1 ln(s) + 1, the paper's
+    sqrt(1/t); the llama3 rule and the plain rotary by 1."""
+    if scaling is None or scaling.kind != "yarn":
+        return 1.0
+    return 0.1 * np.log(scaling.factor) + 1.0
+
+
+def rope(x, positions, theta, scaling=None):
     """Rotary embedding of x[..., T, d] at the given positions (length T).
 
     Pages: "LlamaForCausalLM-32L-4096d" ``q, k = rope(q, k, theta=10000)``;
     "apertus" ("at position 0, where the rotation is the identity").
     Element i is rotated together with element i + d/2 by the angle
-    position * inv_freq_i.
+    position * inv_freq_i (stretched by `scaling`, whose attention factor then
+    multiplies the rotated vector).
     """
     x = np.asarray(x, dtype=F64)
     d = x.shape[-1]
     half = d // 2
     pos = np.asarray(positions, dtype=F64)
-    ang = pos[:, None] * rope_inv_freq(d, theta)[None, :]  # [T, d/2]
-    c, s = np.cos(ang), np.sin(ang)
+    ang = pos[:, None] * rope_inv_freq(d, theta, scaling)[None, :]  # [T, d/2]
+    m = rope_attention_factor(scaling)
+    c, s = m * np.cos(ang), m * np.sin(ang)
     x1, x2 = x[..., :half], x[..., half:]
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
@@ -215,7 +274,7 @@ def _project_kv(cfg, w, h_norm, positions):
     v = _heads(h_norm @ w["v_proj"].T, cfg.num_kv_heads, d)
     if cfg.qk_norm:
         k = rms_norm(k, w["k_norm"], cfg.rms_norm_eps)
-    k = rope(k, positions, cfg.rope_theta)
+    k = rope(k, positions, cfg.rope_theta, cfg.rope_scaling)
     return k, v
 
 
@@ -224,7 +283,7 @@ def _project_q(cfg, w, h_norm_rows, positions_rows):
     q = _heads(h_norm_rows @ w["q_proj"].T, cfg.num_heads, d)
     if cfg.qk_norm:
         q = rms_norm(q, w["q_norm"], cfg.rms_norm_eps)
-    return rope(q, positions_rows, cfg.rope_theta)
+    return rope(q, positions_rows, cfg.rope_theta, cfg.rope_scaling)
 
 
 def mlp(cfg, w, h):

@@ -299,6 +299,36 @@ def test_prefill_chunk_needs_the_host_lengths():
                     cache={"k": kd, "v": kd.clone(), "lens": torch.zeros(1, dtype=torch.int32, device=DEV)})
 
 
+YARN_ARCEE = ("yarn", 20.0, 4096, 1.0, 32.0)          # "arcee": YaRN, factor 20 over 4096, theta 10000
+LLAMA3_APERTUS = ("llama3", 8.0, 8192, 1.0, 4.0)      # "apertus": llama3, factor 8 over 8192, theta 12M
+
+
+@pytest.mark.parametrize("scaling,theta,qk_norm", [(YARN_ARCEE, 10000.0, True), (LLAMA3_APERTUS, 12_000_000.0, False)])
+def test_stretched_rotary_prefill_and_decode(scaling, theta, qk_norm):
+    wl = Workload(f"rope_{scaling[0]}", "bf16", 2, 256, 512, 8, 2, 128, 1000, "silu", qk_norm=qk_norm, seed=29,
+                  rope_theta=theta, rope_scaling=scaling)
+    w = make_weights(wl, gain_std=0.1 if qk_norm else 0.0)
+    x = make_input(wl)
+    blk = DecoderBlock.from_workload(wl, max_seq=600)
+    wd = to_dev(w)
+    out = blk.forward(x.to(DEV), wd)
+    torch.cuda.synchronize()
+    ref = oracle.block_forward(cfg_of(wl), weights_np(w), np64(x))
+    assert rel_err(out, ref["layer_output"]) <= TOL["bf16"]
+    # a decode step at positions past the prefill's, over a random cache
+    lens = [300, 517]
+    dw = wl.scaled(batch=2, seq=1)
+    kc, vc = make_kv_cache(dw.scaled(cache_len=max(lens)), capacity=max(lens) + 8)
+    xd = make_input(dw)[:, 0]
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    o1 = blk.forward(xd[:, None].to(DEV), wd, cache={"k": kd, "v": vd, "lens": lens_d}, host_lens_max=max(lens))
+    torch.cuda.synchronize()
+    r1 = oracle.decode_step(cfg_of(dw), weights_np(w), np64(xd), np64(kc), np64(vc), np.array(lens))
+    assert rel_err(o1[:, 0], r1["layer_output"]) <= TOL["bf16"]
+    assert rel_err(kd[[0, 1], :, lens].cpu(), r1["new_key"]) <= TOL["bf16"]
+
+
 def test_decode_matches_prefill_last_row():
     wl = Workload("small_prefill_decode", "bf16", 2, 96, 512, 4, 2, 128, 1000, "silu", seed=23)
     w = to_dev(make_weights(wl))

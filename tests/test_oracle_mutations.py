@@ -23,7 +23,7 @@ def _rms_sum(x, gain, eps):
     return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps) * gain
 
 
-def _rope_interleaved(x, positions, theta):
+def _rope_interleaved(x, positions, theta, scaling=None):
     x = np.asarray(x, dtype=F64)
     d = x.shape[-1]
     ang = np.asarray(positions, dtype=F64)[:, None] * ob.rope_inv_freq(d, theta)[None, :]
@@ -35,12 +35,12 @@ def _rope_interleaved(x, positions, theta):
     return out
 
 
-def _inv_freq_wrong(head_dim, theta):
+def _inv_freq_wrong(head_dim, theta, scaling=None):
     i = np.arange(head_dim // 2, dtype=F64)
     return np.power(F64(theta), -i / head_dim)
 
 
-def _rope_sign(x, positions, theta):
+def _rope_sign(x, positions, theta, scaling=None):
     x = np.asarray(x, dtype=F64)
     d = x.shape[-1]
     ang = np.asarray(positions, dtype=F64)[:, None] * ob.rope_inv_freq(d, theta)[None, :]
@@ -86,6 +86,18 @@ def _silu_wrong(u):
     return u / (1.0 + np.exp(u))
 
 
+_orig_inv_freq = ob.rope_inv_freq
+
+
+def _scaling_ramp_reversed(head_dim, theta, scaling=None):
+    # the blend weight turned around: fast components divided, slow ones kept
+    if scaling is None:
+        return _orig_inv_freq(head_dim, theta)
+    f = _orig_inv_freq(head_dim, theta)
+    s = _orig_inv_freq(head_dim, theta, scaling)
+    return f * (f / s) / scaling.factor
+
+
 def _relu_not_squared(u):
     return np.maximum(np.asarray(u, dtype=F64), 0.0)
 
@@ -122,6 +134,7 @@ MUTATIONS = {
     "relu_not_squared": [("relu2", _relu_not_squared)],
     "swiglu_gate_up_swapped": [("mlp", _mlp_swapped)],
     "missing_residual": [("_finish_rows", _finish_no_residual)],
+    "rope_scaling_ramp_reversed": [("rope_inv_freq", _scaling_ramp_reversed)],
 }
 
 PIN_TESTS = [
@@ -139,6 +152,8 @@ PIN_TESTS = [
     lambda: pins.test_block_brute_force("relu2", False, 4, 2),
     lambda: pins.test_block_brute_force("xielu", True, 4, 1),
     pins.test_block_identity_and_taps,
+    pins.test_llama3_scaling_keeps_fast_divides_slow_and_blends_between,
+    pins.test_yarn_scaling_keeps_fast_divides_slow_and_scales_attention,
 ]
 
 

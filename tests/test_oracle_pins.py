@@ -473,3 +473,57 @@ def test_prefill_chunk_of_one_token_is_a_decode_step():
     dec = oracle.decode_step(cfg, w, x[:, 0], ck, cv, lens)
     np.testing.assert_allclose(ch["layer_output"][:, 0], dec["layer_output"], rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(ch["new_keys"][:, :, 0], dec["new_key"], rtol=1e-13, atol=1e-14)
+
+
+# ---------------------------------------------------------------- stretched rotary
+
+LLAMA3_APERTUS = oracle.RopeScaling("llama3", 8.0, 8192, 1.0, 4.0)  # "apertus": factor 8 over 8192, theta 12M
+YARN_ARCEE = oracle.RopeScaling("yarn", 20.0, 4096, 1.0, 32.0)  # "arcee": factor 20 over 4096, theta 10000
+
+
+def test_rope_scaling_of_factor_one_is_the_plain_rotary():
+    for kind, lo, hi in (("llama3", 1.0, 4.0), ("yarn", 1.0, 32.0)):
+        sc = oracle.RopeScaling(kind, 1.0, 4096, lo, hi)
+        np.testing.assert_allclose(oracle.rope_inv_freq(128, 10000.0, sc), oracle.rope_inv_freq(128, 10000.0),
+                                   rtol=4e-16)  # the blend of f and f / 1 rounds once
+        assert oracle.rope_attention_factor(sc) == 1.0
+
+
+def _regimes(theta, sc):
+    base = oracle.rope_inv_freq(128, theta)
+    lam = 2 * np.pi / base
+    return base, lam, oracle.rope_inv_freq(128, theta, sc)
+
+
+def test_llama3_scaling_keeps_fast_divides_slow_and_blends_between():
+    base, lam, f = _regimes(12_000_000.0, LLAMA3_APERTUS)
+    fast, slow = lam < 8192 / 4.0, lam > 8192 / 1.0
+    mid = ~fast & ~slow
+    assert fast.sum() > 0 and slow.sum() > 0 and mid.sum() > 0
+    np.testing.assert_array_equal(f[fast], base[fast])
+    np.testing.assert_allclose(f[slow], base[slow] / 8.0, rtol=1e-15)
+    assert np.all(f[mid] < base[mid]) and np.all(f[mid] > base[mid] / 8.0)
+    assert np.all(np.diff(f) < 0)  # still strictly decreasing with the dimension
+    # continuous at both ends of the blend: a frequency exactly on a boundary gets the same value
+    for lam_b, want in ((8192 / 4.0, 1.0), (8192 / 1.0, 1.0 / 8.0)):
+        sc = LLAMA3_APERTUS
+        fb = 2 * np.pi / lam_b
+        g = (sc.original_max_position / lam_b - sc.low) / (sc.high - sc.low)
+        assert abs(((1 - g) * fb / sc.factor + g * fb) / fb - want) < 1e-15
+
+
+def test_yarn_scaling_keeps_fast_divides_slow_and_scales_attention():
+    base, lam, f = _regimes(10000.0, YARN_ARCEE)
+    turns = 4096 / lam
+    fast, slow = turns > 32.0, turns < 1.0
+    mid = ~fast & ~slow
+    assert fast.sum() > 0 and slow.sum() > 0 and mid.sum() > 0
+    np.testing.assert_array_equal(f[fast], base[fast])
+    np.testing.assert_allclose(f[slow], base[slow] / 20.0, rtol=1e-15)
+    assert np.all(f[mid] < base[mid]) and np.all(f[mid] > base[mid] / 20.0)
+    assert abs(oracle.rope_attention_factor(YARN_ARCEE) - (1.0 + 0.1 * np.log(20.0))) < 1e-15
+    # the factor multiplies the rotated vector: its norm grows by exactly that much
+    x = np.random.default_rng(17).standard_normal((3, 5, 128))
+    y = oracle.rope(x, np.arange(5) * 1000, 10000.0, YARN_ARCEE)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1) * (1 + 0.1 * np.log(20.0)),
+                               rtol=1e-13)
