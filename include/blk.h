@@ -184,6 +184,36 @@ blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const b
                        blk_kv_cache* cache, int host_lens_max, void* out, void* workspace,
                        size_t workspace_bytes, const blk_taps* taps, void* stream);
 
+/* The model around the block ("LlamaForCausalLM-32L-4096d" sheet, "Implementing
+ * it": embed_tokens, the decoder layers, norm, lm_head), all layers of one
+ * handle's shape. Device pointers in the handle's dtype, row-major:
+ *   embed   [vocab, D]   token embeddings (embed_tokens)
+ *   layers  [n_layers]   host array of per-layer weights (blk_weights)
+ *   norm_g  [D]          final RMSNorm gain
+ *   lm_head [vocab, D]   output projection (may equal embed when tied) */
+typedef struct {
+  const void* embed;
+  const blk_weights* layers;
+  int n_layers;
+  const void* norm_g;
+  const void* lm_head;
+  int vocab;
+} blk_model;
+
+/* Workspace for blk_model_forward: one layer's blk_workspace_bytes plus two
+ * [B, T, D] activation buffers and the final norm's output. */
+size_t blk_model_workspace_bytes(const blk_handle* h, int batch, int seq, int decode);
+
+/* logits[B, T, vocab] = lm_head(norm(layers(embed[tokens]))). tokens: device
+ * int32 [B, T]; an id outside [0, vocab) embeds as zeros and sets the status
+ * word to INVALID_ARG (blk_last_status). caches: NULL (prefill from position 0)
+ * or a host array of n_layers KV caches with T new tokens after lens[b] (as in
+ * blk_forward; each layer's cache needs its own lens array, since each layer
+ * advances its own). Errors: those of blk_forward, WORKSPACE, CUDA. */
+blk_status blk_model_forward(blk_handle* h, const blk_model* m, const int* tokens, int batch, int seq,
+                             blk_kv_cache* caches, int host_lens_max, void* logits, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 /* A recorded forward: the launches one blk_forward makes for fixed arguments,
  * captured once into a CUDA graph so that replaying it costs one launch. */
 typedef struct blk_graph blk_graph;

@@ -39,6 +39,11 @@ class blk_kv_cache(ctypes.Structure):
     _fields_ = [("k", c_void_p), ("v", c_void_p), ("capacity", c_int), ("lens", c_void_p)]
 
 
+class blk_model(ctypes.Structure):
+    _fields_ = [("embed", c_void_p), ("layers", POINTER(blk_weights)), ("n_layers", c_int), ("norm_g", c_void_p),
+                ("lm_head", c_void_p), ("vocab", c_int)]
+
+
 TAP_NAMES = ("attention_queries", "attention_keys", "attention_values", "attention_head_outputs",
              "attention_output", "layer_mid", "mlp_neurons", "mlp_output")
 
@@ -82,6 +87,9 @@ SIGNATURES = {
     "blk_prepare_weights": (c_int, [c_void_p, POINTER(blk_weights), c_void_p, c_size_t, c_void_p]),
     "blk_attn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                         c_void_p, c_void_p]),
+    "blk_model_workspace_bytes": (c_size_t, [c_void_p, c_int, c_int, c_int]),
+    "blk_model_forward": (c_int, [c_void_p, POINTER(blk_model), c_void_p, c_int, c_int, POINTER(blk_kv_cache), c_int,
+                                  c_void_p, c_void_p, c_size_t, c_void_p]),
 }
 
 _lib_handle = None
@@ -223,6 +231,30 @@ class DecoderBlock:
                                  _ptr(workspace), ws_bytes, ctypes.byref(tp) if tp is not None else None,
                                  _stream_ptr(stream)))
         return out
+
+    def model_forward(self, tokens, layers, embed, norm_g, lm_head, caches=None, host_lens_max=-1, logits=None,
+                      workspace=None, stream=None):
+        """logits [B, T, vocab] of the model around this block's shape: embed[tokens], the
+        layers (a list of weight dicts), the final norm and lm_head. tokens: device int32
+        [B, T]. caches: None, or one dict(k, v, lens) per layer (T new tokens after lens)."""
+        import torch
+        B, T = tokens.shape
+        vocab = embed.shape[0]
+        if logits is None:
+            logits = torch.empty(B, T, vocab, dtype=embed.dtype, device=tokens.device)
+        need = lib().blk_model_workspace_bytes(self.handle, B, T, int(caches is not None))
+        if workspace is None:
+            workspace = self._workspace(need, tokens.device)
+        wls = (blk_weights * len(layers))(*[make_weights_struct(w) for w in layers])
+        m = blk_model(_ptr(embed), wls, len(layers), _ptr(norm_g), _ptr(lm_head), vocab)
+        kvs = None
+        if caches is not None:
+            kvs = (blk_kv_cache * len(caches))(*[blk_kv_cache(_ptr(c["k"]), _ptr(c["v"]), c["k"].shape[2],
+                                                              _ptr(c["lens"])) for c in caches])
+        _check(lib().blk_model_forward(self.handle, ctypes.byref(m), _ptr(tokens), B, T, kvs, host_lens_max,
+                                       _ptr(logits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream_ptr(stream)))
+        return logits
 
     def forward_graph(self, x, weights, out, workspace, cache=None, taps=None, host_lens_max=-1):
         """Records blk_forward for these exact buffers into a CUDA graph (ForwardGraph)."""

@@ -905,6 +905,78 @@ blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const b
   return forward_prefill_bf16(h, x, batch, seq, w, out, ws, taps, s, chunk ? cache : nullptr);
 }
 
+// ------------------------------------------------------------------ the model around the block
+
+namespace {
+struct ModelWs {
+  void *block, *act0, *act1, *ynorm;
+  size_t block_bytes, total;
+};
+
+ModelWs carve_model(const blk_handle* h, void* base, int batch, int seq, bool decode) {
+  const blk_desc& d = h->d;
+  ModelWs m{};
+  m.block_bytes = blk_workspace_bytes(h, batch, seq, decode ? 1 : 0);
+  const size_t act = (size_t)batch * seq * d.hidden * esize(d);
+  Carve c(base);
+  m.block = c.take(m.block_bytes);
+  m.act0 = c.take(act);
+  m.act1 = c.take(act);
+  m.ynorm = c.take(act);
+  m.total = c.off;
+  return m;
+}
+}  // namespace
+
+size_t blk_model_workspace_bytes(const blk_handle* h, int batch, int seq, int decode) {
+  if (!h || batch <= 0 || seq <= 0) return 0;
+  return carve_model(h, nullptr, batch, seq, decode != 0).total;
+}
+
+blk_status blk_model_forward(blk_handle* h, const blk_model* m, const int* tokens, int batch, int seq,
+                             blk_kv_cache* caches, int host_lens_max, void* logits, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!h || !m || !tokens || !logits) return fail(BLK_ERR_INVALID_ARG, "handle, model, tokens and logits must be non-NULL");
+  const blk_desc& d = h->d;
+  if (m->n_layers < 1 || !m->layers || !m->embed || !m->norm_g || !m->lm_head || m->vocab <= 0)
+    return fail(BLK_ERR_INVALID_ARG, "model: n_layers >= 1, layers, embed, norm_g, lm_head and vocab > 0");
+  if (m->vocab % 8) return fail(BLK_ERR_UNSUPPORTED, "model: vocab must be a multiple of 8 (16-byte logit rows)");
+  if (batch <= 0 || seq <= 0) return fail(BLK_ERR_INVALID_ARG, "batch and seq must be positive");
+  if (!aligned16(m->embed) || !aligned16(m->lm_head) || !aligned16(logits) || !aligned16(workspace))
+    return fail(BLK_ERR_ALIGNMENT, "model: embed, lm_head, logits and workspace must be 16-byte aligned");
+  const ModelWs mw = carve_model(h, workspace, batch, seq, caches != nullptr);
+  if (!workspace || workspace_bytes < mw.total) return fail(BLK_ERR_WORKSPACE, "model workspace missing or too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int M = batch * seq;
+  BLK_TRY(check_cuda(launch_embed(tokens, m->embed, M, (int)(d.hidden * esize(d)), m->vocab, mw.act0, h->status,
+                                  h->num_sms, s),
+                     "embedding"));
+  void* bufs[2] = {mw.act0, mw.act1};
+  for (int l = 0; l < m->n_layers; ++l)  // each layer reads one buffer and writes the other
+    BLK_TRY(blk_forward(h, bufs[l & 1], batch, seq, &m->layers[l], caches ? &caches[l] : nullptr, host_lens_max,
+                        bufs[(l + 1) & 1], mw.block, mw.block_bytes, nullptr, stream));
+  const void* last = bufs[m->n_layers & 1];
+  const bool bf = d.dtype == BLK_BF16;
+  BLK_TRY(check_cuda(launch_rmsnorm(last, m->norm_g, M, d.hidden, d.eps, mw.ynorm, bf, s), "final norm"));
+  if (!bf)
+    return check_cuda(launch_gemm_f32(static_cast<const float*>(mw.ynorm), static_cast<const float*>(m->lm_head),
+                                      static_cast<float*>(logits), m->vocab, M, m->vocab, d.hidden, s),
+                      "lm_head GEMM");
+  TcGemmDesc g;
+  g.na = 1;
+  g.a[0] = {mw.ynorm, M, 0};
+  g.nb = 1;
+  g.b[0] = {m->lm_head, m->vocab, 0};
+  g.K = d.hidden;
+  static const int cands[] = {256, 224, 192, 128};
+  g.bn = choose_bn(M, m->vocab, false, cands, 4, h->num_sms);
+  g.epi = Epi::kStore;
+  g.const_op = 2;
+  g.e.out = logits;
+  g.e.ldo = m->vocab;
+  return tc(h, g, s, "lm_head GEMM");
+}
+
 struct blk_graph {
   blk_handle* h;
   cudaGraphExec_t exec;

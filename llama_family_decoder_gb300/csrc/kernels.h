@@ -22,6 +22,12 @@ cudaError_t launch_rmsnorm(const void* x, const void* g, int rows, int n, float 
 cudaError_t launch_norm_prep(const void* x, const void* g, int rows, int n, float eps, void* xg, float* row_scale,
                              float* zero_rows, cudaStream_t s);
 
+// ---------------------------------------------------------------- embedding
+// out[r, :] = table[tokens[r], :] (row_bytes per row, a multiple of 16); ids outside
+// [0, vocab) give zero rows and set the status word to INVALID_ARG.
+cudaError_t launch_embed(const int* tokens, const void* table, int rows, int row_bytes, int vocab, void* out,
+                         DevStatus* st, int num_sms, cudaStream_t s);
+
 // dst[i] = bf16(src[i]) for fp16 src (n elements).
 cudaError_t launch_cast_f16_bf16(const void* src, void* dst, size_t n, cudaStream_t s);
 

@@ -126,3 +126,18 @@ def make_kv_cache(w: Workload, capacity: int | None = None, seed: int | None = N
     k[:, :, :L] = _normal(gen, (w.batch, w.num_kv_heads, L, w.head_dim), 1.0, dt)
     v[:, :, :L] = _normal(gen, (w.batch, w.num_kv_heads, L, w.head_dim), 1.0, dt)
     return k, v
+
+
+def make_model(w: Workload, n_layers: int, vocab: int, seed: int | None = None):
+    """A synthetic model around the block: per-layer weights (make_weights, one seed per
+    layer), embeddings ~ N(0, 1), lm_head ~ N(0, 0.02), final gain 1, and token ids
+    uniform over the vocabulary, [batch, seq]. Returns (layers, embed, norm_g, lm_head, tokens)."""
+    s = w.seed if seed is None else seed
+    layers = [make_weights(w, seed=s + 101 * (l + 1)) for l in range(n_layers)]
+    gen = torch.Generator().manual_seed(s + 3000)
+    dt = torch_dtype(w)
+    embed = torch.randn(vocab, w.hidden_size, generator=gen).to(dt)
+    lm_head = (torch.randn(vocab, w.hidden_size, generator=gen) * 0.02).to(dt)
+    norm_g = torch.ones(w.hidden_size, dtype=dt)
+    tokens = torch.randint(0, vocab, (w.batch, w.seq), generator=gen, dtype=torch.int32)
+    return layers, embed, norm_g, lm_head, tokens

@@ -21,4 +21,5 @@ from .block import (  # noqa: F401
     mlp,
     decode_step,
     prefill_with_cache,
+    model_forward,
 )

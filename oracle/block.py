@@ -446,3 +446,17 @@ def decode_step(cfg, w, x, cache_k, cache_v, lens):
         )
         per_batch.append(taps)
     return {key: np.stack([t[key] for t in per_batch]) for key in per_batch[0]}
+
+
+def model_forward(cfg, layers, embed, norm_g, lm_head, tokens):
+    """Logits of the model around the block ("LlamaForCausalLM-32L-4096d" sheet,
+    "Implementing it": embed_tokens, the decoder layers in order, norm, lm_head).
+
+    tokens: int [B, T]; layers: a list of block weight dicts; embed and lm_head
+    [vocab, D]; norm_g [D]. Returns logits [B, T, vocab].
+    """
+    x = np.asarray(embed, dtype=F64)[np.asarray(tokens)]
+    for w in layers:
+        x = block_forward(cfg, w, x)["layer_output"]
+    h = rms_norm(x, norm_g, cfg.rms_norm_eps)
+    return h @ np.asarray(lm_head, dtype=F64).T

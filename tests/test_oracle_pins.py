@@ -527,3 +527,29 @@ def test_yarn_scaling_keeps_fast_divides_slow_and_scales_attention():
     y = oracle.rope(x, np.arange(5) * 1000, 10000.0, YARN_ARCEE)
     np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1) * (1 + 0.1 * np.log(20.0)),
                                rtol=1e-13)
+
+
+def test_model_with_identity_blocks_and_tied_embeddings_reads_its_own_token():
+    # Blocks whose o_proj and down_proj are zero pass the stream through unchanged, so
+    # the logits are rmsnorm(e_t) . e_v; with tied, nearly orthogonal embeddings the
+    # largest is the token's own id, and its value is |e_t| sqrt(D) exactly.
+    rng = np.random.default_rng(18)
+    cfg = _tiny("relu2", False, H=2, Hkv=1, d=4, D=64, F=5)
+    V, D = 40, 64
+    embed = rng.standard_normal((V, D))
+    layers = []
+    for _ in range(2):
+        w = _weights(cfg, rng)
+        w["o_proj"] = np.zeros_like(w["o_proj"])
+        w["down_proj"] = np.zeros_like(w["down_proj"])
+        layers.append(w)
+    tokens = rng.integers(0, V, size=(2, 7))
+    logits = oracle.model_forward(cfg, layers, embed, np.ones(D), embed, tokens)
+    assert logits.shape == (2, 7, V)
+    np.testing.assert_array_equal(logits.argmax(-1), tokens)
+    e = embed[tokens]
+    want = np.sqrt((e * e).sum(-1)) * np.sqrt(D) / np.sqrt(1 + cfg.rms_norm_eps / np.mean(e * e, -1))
+    np.testing.assert_allclose(np.take_along_axis(logits, tokens[..., None], -1)[..., 0], want, rtol=1e-12)
+    # and one real layer is block_forward's output, normed and projected
+    out1 = oracle.block_forward(cfg, layers[0], e)["layer_output"]
+    np.testing.assert_allclose(out1, e, rtol=0, atol=0)
