@@ -133,14 +133,22 @@ def work_counts(wl):
     n_up = 2 * F if wl.hidden_act == "silu" else F
     g = {"qkv": 2.0 * M * D * (H + 2 * Hkv) * d, "o": 2.0 * M * H * d * D, "up": 2.0 * M * D * n_up,
          "down": 2.0 * M * F * D}
-    if wl.cache_len:
+    if wl.cache_len and T == 1:
         L = wl.cache_len + 1
         g["attn"] = 4.0 * B * H * d * L
         kv_bytes = 2.0 * B * Hkv * L * d * es
+    elif wl.cache_len:  # a prefill chunk: query t sees cache_len + t + 1 keys
+        L = wl.cache_len
+        g["attn"] = 4.0 * B * H * d * (T * L + T * (T + 1) / 2)
+        kv_bytes = 2.0 * B * Hkv * (L + T) * d * es
     else:
         g["attn"] = 4.0 * B * H * d * T * (T + 1) / 2
         kv_bytes = 0.0
     weight_bytes = es * (D * (H + 2 * Hkv) * d + H * d * D + n_up * D + F * D + 2 * D)
+    if wl.n_layers:  # the model: every layer, plus lm_head
+        g = {k: v * wl.n_layers for k, v in g.items()}
+        g["lm_head"] = 2.0 * M * D * wl.vocab
+        weight_bytes = weight_bytes * wl.n_layers + es * (2 * wl.vocab * D + D)
     return g, weight_bytes, kv_bytes
 
 
@@ -156,7 +164,14 @@ def oracle_tokens_per_s(wl, w_cpu, x_cpu, cache_cpu, tokens_cap):
                              wl.xielu_alpha_n)
     wn = {k: v.double().numpy() for k, v in w_cpu.items()}
     t0 = time.perf_counter()
-    if wl.cache_len:
+    if wl.cache_len and wl.seq > 1:
+        n = min(wl.seq, tokens_cap)
+        kc, vc = cache_cpu
+        oracle.prefill_with_cache(cfg, wn, x_cpu[:1, :n].double().numpy(), kc[:1].double().numpy(),
+                                  vc[:1].double().numpy(), np.full(1, wl.cache_len))
+        ntok = n
+        sample = f"sequence 0, first {n} of {wl.seq} chunk tokens after a {wl.cache_len}-position cache"
+    elif wl.cache_len:
         nb = max(1, min(wl.batch, tokens_cap))
         kc, vc = cache_cpu
         lens = np.full(nb, wl.cache_len)
@@ -170,6 +185,9 @@ def oracle_tokens_per_s(wl, w_cpu, x_cpu, cache_cpu, tokens_cap):
         ntok = T
         sample = f"sequence 0, first {T} of {wl.seq} tokens (full block, causal prefix)"
     dt = time.perf_counter() - t0
+    if wl.n_layers:  # the model: one layer timed, counted once per layer (embedding and lm_head left out)
+        dt *= wl.n_layers
+        sample += f"; one layer timed and counted {wl.n_layers} times (embedding and lm_head not included)"
     return ntok / dt, sample, dt
 
 
@@ -182,14 +200,14 @@ def run_reference(args, wl):
     w = make_weights(wl)
     x = make_input(wl)
     cache = make_kv_cache(wl) if wl.cache_len else None
-    cap = 2 if wl.cache_len else 256  # per step: a bounded sample (seconds)
+    decode = wl.cache_len > 0 and wl.seq == 1
+    cap = 2 if decode else 256  # per step: a bounded sample (seconds)
     times, sample = [], ""
     for i in range(args.warmup + args.steps):
         tps, sample, dt = oracle_tokens_per_s(wl, w, x, cache, cap)
         if i >= args.warmup:
             times.append(dt)
-    ntok = cap if not wl.cache_len else min(cap, wl.batch)
-    ntok = min(ntok, wl.seq) if not wl.cache_len else ntok
+    ntok = min(cap, wl.batch) if decode else min(cap, wl.seq)
     value = ntok * len(times) / sum(times)
     cores = os.cpu_count()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
@@ -260,10 +278,11 @@ def run_ours(args, wl):
     x_cpu = make_input(wl, seed=rank_seed(wl, rank))
     w = {k: v.to(dev) for k, v in w_cpu.items()}
     x = x_cpu.to(dev)
-    decode = wl.cache_len > 0
+    cached = wl.cache_len > 0  # T new tokens after cache_len positions: a decode step (T == 1) or a chunk
+    decode = cached and wl.seq == 1
     cache = None
     cache_cpu = None
-    if decode:
+    if cached:
         cache_cpu = make_kv_cache(wl)
         kc, vc = (t.to(dev) for t in cache_cpu)
         lens0 = torch.full((wl.batch,), wl.cache_len, dtype=torch.int32, device=dev)
@@ -272,7 +291,7 @@ def run_ours(args, wl):
     if wl.dtype == "bf16" and not decode:
         w = blk.prepare(w)  # one-time load step: fp16 copies of wo / w_gate / w_up
     out = torch.empty_like(x)
-    ws = torch.empty(blk.workspace_bytes(wl.batch, wl.seq, decode), dtype=torch.uint8, device=dev)
+    ws = torch.empty(blk.workspace_bytes(wl.batch, wl.seq, cached), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def flush_l2():
@@ -284,10 +303,10 @@ def run_ours(args, wl):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        if decode:
-            cache["lens"].copy_(lens0)  # every step decodes the same token position
+        if cached:
+            cache["lens"].copy_(lens0)  # every step processes the same positions
         blk.forward(x, w, cache=cache, out=out, workspace=ws, stream=stream,
-                    host_lens_max=wl.cache_len if decode else -1)
+                    host_lens_max=wl.cache_len if cached else -1)
 
     for _ in range(args.warmup):
         step()
@@ -300,12 +319,12 @@ def run_ours(args, wl):
     # Every timed step replays one CUDA graph of the whole forward (captured once).
     # The headline times a graph without profiling events; a second graph, with
     # the per-stage events recorded inside it, is replayed for the stage times.
-    hl = wl.cache_len if decode else -1
+    hl = wl.cache_len if cached else -1
     graph = blk.forward_graph(x, w, out, ws, cache=cache, host_lens_max=hl)
     blk.profile(True)
     pgraph = blk.forward_graph(x, w, out, ws, cache=cache, host_lens_max=hl)
     for g in (graph, pgraph, graph, pgraph):
-        if decode:
+        if cached:
             cache["lens"].copy_(lens0)
         g.launch(stream)
     torch.cuda.synchronize()
@@ -317,7 +336,7 @@ def run_ours(args, wl):
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         for i in range(args.steps):
             flush_l2()
-            if decode:
+            if cached:
                 cache["lens"].copy_(lens0)
             starts[i].record(stream)
             g.launch(stream)
@@ -352,7 +371,7 @@ def run_ours(args, wl):
     e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for i in range(args.steps):
         flush_l2()
-        if decode:
+        if cached:
             cache["lens"].copy_(lens0)
         e_starts[i].record(stream)
         x.copy_(x_host, non_blocking=True)
@@ -416,6 +435,129 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def run_model(args, wl):
+    """The model around the block: embedding, wl.n_layers blocks, final norm, lm_head, one
+    blk_model_forward per step, replayed from a CUDA graph. Weights are drawn on the device
+    (N(0, 0.02) projections, unit gains, N(0, 1) embeddings): at 32 layers they are ~13 GB."""
+    import torch
+
+    from llama_family_decoder_gb300 import DecoderBlock
+    from llama_family_decoder_gb300.synth import make_input, make_weights
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import __graft_entry__
+    __graft_entry__.build()
+
+    D, H, Hkv, d, F, V = wl.hidden_size, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.intermediate_size, wl.vocab
+    gen = torch.Generator(device=dev).manual_seed(rank_seed(wl, rank))
+    bf = torch.bfloat16
+
+    def rnd(*shape, std=0.02):
+        return (torch.randn(*shape, generator=gen, device=dev) * std).to(bf)
+
+    blk = DecoderBlock.from_workload(wl)
+    layers = []
+    for _ in range(wl.n_layers):
+        w = {"input_layernorm": torch.ones(D, dtype=bf, device=dev), "q_proj": rnd(H * d, D),
+             "k_proj": rnd(Hkv * d, D), "v_proj": rnd(Hkv * d, D), "o_proj": rnd(D, H * d),
+             "post_attention_layernorm": torch.ones(D, dtype=bf, device=dev), "up_proj": rnd(F, D),
+             "down_proj": rnd(D, F)}
+        if wl.hidden_act == "silu":
+            w["gate_proj"] = rnd(F, D)
+        layers.append(blk.prepare(w))  # the one-time load step of each layer
+    embed, lm_head = rnd(V, D, std=1.0), rnd(V, D)
+    norm_g = torch.ones(D, dtype=bf, device=dev)
+    tokens = torch.randint(0, V, (wl.batch, wl.seq), generator=gen, device=dev, dtype=torch.int32)
+    logits = torch.empty(wl.batch, wl.seq, V, dtype=bf, device=dev)
+    ws = torch.empty(blk.model_workspace_bytes(wl.batch, wl.seq), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        flush.amax()
+
+    def fwd():
+        blk.model_forward(tokens, layers, embed, norm_g, lm_head, logits=logits, workspace=ws)
+
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+    if args.ncu:
+        fwd()
+        torch.cuda.synchronize()
+        return
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        fwd()  # one more warm-up on the capture stream
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            fwd()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
+    with ClockSampler(gpu_index) as clk:
+        clk.wait_first_sample()
+        for i in range(args.steps):
+            flush_l2()
+            starts[i].record(stream)
+            graph.replay()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    total_ms = max_over_ranks(sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)), dev)
+    ms_per_step = total_ms / args.steps
+    ntok = wl.batch * wl.seq
+    value = job_tokens_per_s(world, ntok, args.steps, total_ms)
+    # end to end: token ids from pinned host memory, the last position's logits back (the next-token scores)
+    tok_host = tokens.cpu().pin_memory()
+    last_host = torch.empty(wl.batch, V, dtype=bf).pin_memory()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush_l2()
+        e_s[i].record(stream)
+        tokens.copy_(tok_host, non_blocking=True)
+        graph.replay()
+        last_host.copy_(logits[:, -1], non_blocking=True)
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(s_.elapsed_time(e_) for s_, e_ in zip(e_s, e_e)) / args.steps, dev)
+    peaks = _peaks()
+    g, weight_bytes, _ = work_counts(wl)
+    flops = sum(g.values())
+    achieved = flops / (ms_per_step / 1e3) / 1e12
+    pk = peaks["bf16_tflops_sustained"]
+    roof = {"bound": "tensor", "kernel": "whole model step (every launch of the forward)", "achieved": achieved,
+            "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk, "traffic": None, "algorithmic_flops": flops,
+            "peak_source": f"{peaks['source']} sustained bf16 (burst {peaks['bf16_tflops']})"}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic (N(0,0.02) projections drawn on the device, N(0,1) embeddings, random token ids)",
+            "config": dict(config_of(wl, world), n_layers=wl.n_layers, vocab=V), "roofline": roof,
+            "e2e": {"value": job_tokens_per_s(world, ntok, 1, e2e_ms), "unit": "tokens/s",
+                    "h2d_bytes_per_step": tok_host.numel() * 4, "d2h_bytes_per_step": last_host.numel() * 2},
+            "gpu_launches": 1 + 6 * wl.n_layers + 2, "clocks": clk.summary(),
+            "block": {"tflops": achieved, "frac_of_bf16_spec_2250": achieved / 2250.0,
+                      "weight_bytes": weight_bytes}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, sample, dt = oracle_tokens_per_s(wl, make_weights(wl), make_input(wl), None, 64)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": sample, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -430,6 +572,8 @@ def main():
     wl = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, wl)
+    elif wl.n_layers:
+        run_model(args, wl)
     else:
         run_ours(args, wl)
 

@@ -172,7 +172,7 @@ class DecoderBlock:
         return cls(wl.hidden_size, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.intermediate_size,
                    act=wl.hidden_act, dtype=wl.dtype, qk_norm=wl.qk_norm, rope_theta=wl.rope_theta,
                    eps=wl.rms_norm_eps, xielu_alpha_p=wl.xielu_alpha_p, xielu_alpha_n=wl.xielu_alpha_n,
-                   max_batch=max_batch or wl.batch, max_seq=max_seq or max(wl.seq, wl.cache_len + 1),
+                   max_batch=max_batch or wl.batch, max_seq=max_seq or wl.cache_len + wl.seq,
                    rope_scaling=wl.rope_scaling)
 
     def close(self):
@@ -194,6 +194,9 @@ class DecoderBlock:
         wst = make_weights_struct(weights)
         _check(lib().blk_prepare_weights(self.handle, ctypes.byref(wst), _ptr(buf), buf.numel(), _stream_ptr(stream)))
         return dict(weights, prepared=buf)
+
+    def model_workspace_bytes(self, batch, seq, decode=False):
+        return lib().blk_model_workspace_bytes(self.handle, batch, seq, int(bool(decode)))
 
     def workspace_bytes(self, batch, seq, decode=False):
         return lib().blk_workspace_bytes(self.handle, batch, seq, int(decode))

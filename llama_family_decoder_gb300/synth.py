@@ -37,13 +37,15 @@ class Workload:
     intermediate_size: int
     hidden_act: str  # "silu" | "relu2" | "xielu"
     qk_norm: bool = False
-    cache_len: int = 0  # decode: positions already in the KV cache
+    cache_len: int = 0  # positions already in the KV cache (seq == 1: a decode step; seq > 1: a prefill chunk)
     rms_norm_eps: float = 1e-5
     rope_theta: float = 10000.0
     rope_scaling: tuple | None = None  # (kind, factor, original positions, low, high) of a stretched rotary
     xielu_alpha_p: float = 0.8
     xielu_alpha_n: float = 0.8
     seed: int = 0
+    n_layers: int = 0  # > 0: the model around the block (embeddings, n_layers blocks, norm, lm_head)
+    vocab: int = 0
 
     @property
     def tokens(self) -> int:
@@ -63,6 +65,10 @@ WORKLOADS = {
                  qk_norm=True, seed=3),
         Workload("llama7b_decode_bf16_B64_L4096", "bf16", 64, 1, 4096, 32, 8, 128, 10928, "silu",
                  cache_len=4096, seed=4),
+        Workload("llama7b_chunk_bf16_B4_T512_L1536", "bf16", 4, 512, 4096, 32, 8, 128, 10928, "silu",
+                 cache_len=1536, seed=5),
+        Workload("llama7b_model_bf16_B1_T2048_L32", "bf16", 1, 2048, 4096, 32, 32, 128, 10928, "silu", seed=6,
+                 n_layers=32, vocab=32000),
     ]
 }
 
@@ -116,7 +122,7 @@ def make_kv_cache(w: Workload, capacity: int | None = None, seed: int | None = N
 
     The first cache_len slots hold values; the rest are zero. Returns (k, v).
     """
-    cap = capacity if capacity is not None else w.cache_len + 1
+    cap = capacity if capacity is not None else w.cache_len + w.seq  # room for this call's new tokens
     gen = torch.Generator().manual_seed((w.seed if seed is None else seed) + 2000)
     dt = torch_dtype(w)
     shape = (w.batch, w.num_kv_heads, cap, w.head_dim)
