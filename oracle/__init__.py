@@ -13,6 +13,7 @@ from .block import (  # noqa: F401
     rope,
     causal_gqa_attention,
     silu,
+    sigmoid,
     relu2,
     xielu,
     xielu_effective,

@@ -21,13 +21,23 @@ Sources (page title, section):
     learned per block": xIELU and its parameter transform; "Queries and keys are
     normed per head, before the rotary": q_norm/k_norm over head_dim, one gain for
     every head, applied before RoPE.
+  * nnterp encyclopedia "afmoe", "The block, in order": the sandwich block, each
+    sublayer's output RMSNormed before the residual add; "Attention: per-head q/k
+    norms and a sigmoid gate on every head": o_proj reads the head outputs times
+    sigmoid(gate_proj(normed input)), one gate value per channel of every head;
+    "Rotary runs on the sliding-window blocks only": a window of the last
+    sliding_window tokens, and no rotary on the whole-prefix blocks.
 
 Readings where the pages leave a step open:
   * RMSNorm is x / sqrt(mean(x^2) + eps) * g over the last axis (eps inside the
     square root, no mean-centering, no bias).
   * RoPE pairs element i with element i + d/2 ("rotate half"), with
     inv_freq_i = theta^(-2i/d) for i < d/2 and angle = position * inv_freq_i.
-  * Key j is visible to query i iff position(j) <= position(i).
+  * Key j is visible to query i iff position(j) <= position(i), and, with a
+    sliding window W, position(i) - position(j) < W (the last W tokens, the
+    query's own included).
+  * The attention gate is projected from the attention's input, i.e. the
+    input_layernorm output, the same rows q/k/v are projected from.
   * xIELU at exactly x = 0 takes the negative branch (the positive one is
     written for x > 0 only).
 
@@ -94,6 +104,11 @@ class BlockConfig:
     xielu_beta: float = 0.5
     xielu_eps: float = -1e-6
     rope_scaling: "RopeScaling | None" = None  # a stretched rotary, or None for the plain one
+    # "afmoe" block variant
+    sliding_window: int = 0       # 0: the whole prefix; W > 0: the last W tokens
+    use_rope: bool = True         # False on afmoe's whole-prefix blocks
+    attn_gate: bool = False       # o_proj input = heads * sigmoid(attn_gate_proj(normed input))
+    sandwich_norm: bool = False   # RMSNorm of each sublayer's output before its residual add
 
     def __post_init__(self):
         if self.hidden_act not in ("silu", "relu2", "xielu"):
@@ -102,6 +117,8 @@ class BlockConfig:
             raise ValueError("num_heads must be a multiple of num_kv_heads")
         if self.head_dim % 2:
             raise ValueError("head_dim must be even for the rotary")
+        if self.sliding_window < 0:
+            raise ValueError("sliding_window must be >= 0")
 
 
 # --------------------------------------------------------------------------
@@ -176,13 +193,16 @@ def rope(x, positions, theta, scaling=None):
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
 
-def causal_gqa_attention(q, k, v, q_positions, k_positions, return_pattern=False):
+def causal_gqa_attention(q, k, v, q_positions, k_positions, return_pattern=False, window=0):
     """softmax(q k^T / sqrt(d), causal) v per query head, grouped over KV heads.
 
     q: [H, Tq, d], k, v: [Hkv, Tk, d] (one sequence). Query head h reads KV head
     h // (H / Hkv) ("arcee": "an edit to key/value head j reaches query heads 5j
-    to 5j + 4"). Key j is visible to query i iff k_positions[j] <= q_positions[i].
-    Returns head outputs [H, Tq, d] (and the masked scores and probabilities).
+    to 5j + 4"). Key j is visible to query i iff k_positions[j] <= q_positions[i]
+    and, when window > 0, q_positions[i] - k_positions[j] < window ("afmoe",
+    "Rotary runs on the sliding-window blocks only": the last sliding_window
+    tokens). Returns head outputs [H, Tq, d] (and the masked scores and
+    probabilities).
     """
     q = np.asarray(q, dtype=F64)
     k = np.asarray(k, dtype=F64)
@@ -190,7 +210,10 @@ def causal_gqa_attention(q, k, v, q_positions, k_positions, return_pattern=False
     H, Tq, d = q.shape
     Hkv = k.shape[0]
     group = H // Hkv
-    visible = np.asarray(k_positions)[None, :] <= np.asarray(q_positions)[:, None]
+    gap = np.asarray(q_positions)[:, None] - np.asarray(k_positions)[None, :]
+    visible = gap >= 0
+    if window > 0:
+        visible &= gap < window
     out = np.empty((H, Tq, d), dtype=F64)
     scores_all, probs_all = [], []
     for h in range(H):
@@ -274,7 +297,8 @@ def _project_kv(cfg, w, h_norm, positions):
     v = _heads(h_norm @ w["v_proj"].T, cfg.num_kv_heads, d)
     if cfg.qk_norm:
         k = rms_norm(k, w["k_norm"], cfg.rms_norm_eps)
-    k = rope(k, positions, cfg.rope_theta, cfg.rope_scaling)
+    if cfg.use_rope:
+        k = rope(k, positions, cfg.rope_theta, cfg.rope_scaling)
     return k, v
 
 
@@ -283,6 +307,8 @@ def _project_q(cfg, w, h_norm_rows, positions_rows):
     q = _heads(h_norm_rows @ w["q_proj"].T, cfg.num_heads, d)
     if cfg.qk_norm:
         q = rms_norm(q, w["q_norm"], cfg.rms_norm_eps)
+    if not cfg.use_rope:  # "afmoe": the whole-prefix blocks order tokens by the causal mask alone
+        return q
     return rope(q, positions_rows, cfg.rope_theta, cfg.rope_scaling)
 
 
@@ -308,18 +334,46 @@ def mlp(cfg, w, h):
     return taps
 
 
-def _finish_rows(cfg, w, x_rows, heads_out):
+def sigmoid(u):
+    """1 / (1 + exp(-u)) (the attention gate of "afmoe")."""
+    u = np.asarray(u, dtype=F64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-u))
+
+
+def _finish_rows(cfg, w, x_rows, heads_out, h_rows):
     """o_proj, residual, second norm, MLP and residual for a set of rows.
 
-    heads_out: [H, R, d] per-head outputs of those rows.
+    heads_out: [H, R, d] per-head outputs of those rows; h_rows: [R, D] their
+    input_layernorm outputs (the attention gate's input).
+
+    With cfg.attn_gate ("afmoe", "Attention: per-head q/k norms and a sigmoid
+    gate on every head") o_proj reads heads * sigmoid(h_rows attn_gate_proj^T);
+    attention_head_outputs stay ungated. With cfg.sandwich_norm ("afmoe", "The
+    block, in order") each sublayer's output passes an RMSNorm before its
+    residual add: "post_attn_norm" (afmoe's post_attention_layernorm) after
+    o_proj and "post_mlp_norm" after down_proj; the MLP's input norm keeps the
+    key "post_attention_layernorm" (afmoe's pre_mlp_layernorm). attention_output
+    and mlp_output are then the post-norms' outputs ("The contributions are the
+    post-norms' outputs").
     """
     R = x_rows.shape[0]
     premix = heads_out.transpose(1, 0, 2).reshape(R, -1)  # [R, H*d]
+    taps = {}
+    if cfg.attn_gate:
+        gate = np.asarray(h_rows, dtype=F64) @ w["attn_gate_proj"].T  # [R, H*d]
+        taps["attention_gate"] = gate
+        premix = premix * sigmoid(gate)
     attn_out = premix @ w["o_proj"].T
+    if cfg.sandwich_norm:
+        attn_out = rms_norm(attn_out, w["post_attn_norm"], cfg.rms_norm_eps)
     mid = x_rows + attn_out
     h2 = rms_norm(mid, w["post_attention_layernorm"], cfg.rms_norm_eps)
-    taps = mlp(cfg, w, h2)
+    taps.update(mlp(cfg, w, h2))
+    if cfg.sandwich_norm:
+        taps["mlp_output"] = rms_norm(taps["mlp_output"], w["post_mlp_norm"], cfg.rms_norm_eps)
     taps.update(
+        o_proj_input=premix,
         attention_head_outputs=heads_out.transpose(1, 0, 2),  # [R, H, d]
         attention_output=attn_out,
         layer_mid=mid,
@@ -343,8 +397,9 @@ def block_forward(cfg, w, x, rows=None, positions=None, return_pattern=False):
     Returns a dict of taps, each with a leading batch axis, named as the nnterp
     pages name them: attention_norm_output, attention_queries [B,H,R,d],
     attention_keys [B,Hkv,T,d], attention_values, attention_head_outputs
-    [B,R,H,d], attention_output, layer_mid, mlp_norm_output, mlp_up_output,
-    (mlp_gate_output), mlp_activation, mlp_neurons, mlp_output, layer_output.
+    [B,R,H,d], (attention_gate), o_proj_input, attention_output, layer_mid,
+    mlp_norm_output, mlp_up_output, (mlp_gate_output), mlp_activation,
+    mlp_neurons, mlp_output, layer_output.
     """
     x = np.asarray(x, dtype=F64)
     B, T, D = x.shape
@@ -361,14 +416,14 @@ def block_forward(cfg, w, x, rows=None, positions=None, return_pattern=False):
         h = rms_norm(x[b], w["input_layernorm"], cfg.rms_norm_eps)  # [T, D]
         k, v = _project_kv(cfg, w, h, positions)
         q = _project_q(cfg, w, h[rows], positions[rows])
-        res = causal_gqa_attention(q, k, v, positions[rows], positions, return_pattern)
+        res = causal_gqa_attention(q, k, v, positions[rows], positions, return_pattern, cfg.sliding_window)
         if return_pattern:
             heads, scores, probs = res
             taps["attention_scores"] = scores
             taps["attention_probabilities"] = probs
         else:
             heads = res
-        taps.update(_finish_rows(cfg, w, x[b][rows], heads))
+        taps.update(_finish_rows(cfg, w, x[b][rows], heads, h[rows]))
         taps.update(
             layer_input=x[b][rows],
             attention_norm_output=h[rows],
@@ -404,8 +459,8 @@ def prefill_with_cache(cfg, w, x, cache_k, cache_v, lens):
         q = _project_q(cfg, w, h, pos)  # [H, T, d]
         k_all = np.concatenate([np.asarray(cache_k[b, :, :L], dtype=F64), k_new], axis=1)
         v_all = np.concatenate([np.asarray(cache_v[b, :, :L], dtype=F64), v_new], axis=1)
-        heads = causal_gqa_attention(q, k_all, v_all, pos, np.arange(L + T))
-        taps = _finish_rows(cfg, w, x[b], heads)
+        heads = causal_gqa_attention(q, k_all, v_all, pos, np.arange(L + T), window=cfg.sliding_window)
+        taps = _finish_rows(cfg, w, x[b], heads, h)
         taps.update(attention_norm_output=h, attention_queries=q, new_keys=k_new, new_values=v_new)
         per_batch.append(taps)
     return {key: np.stack([t[key] for t in per_batch]) for key in per_batch[0]}
@@ -435,8 +490,8 @@ def decode_step(cfg, w, x, cache_k, cache_v, lens):
         q = _project_q(cfg, w, h, pos)  # [H, 1, d]
         k_all = np.concatenate([np.asarray(cache_k[b, :, :L], dtype=F64), k_new], axis=1)
         v_all = np.concatenate([np.asarray(cache_v[b, :, :L], dtype=F64), v_new], axis=1)
-        heads = causal_gqa_attention(q, k_all, v_all, pos, np.arange(L + 1))
-        taps = _finish_rows(cfg, w, x[b:b + 1], heads)
+        heads = causal_gqa_attention(q, k_all, v_all, pos, np.arange(L + 1), window=cfg.sliding_window)
+        taps = _finish_rows(cfg, w, x[b:b + 1], heads, h)
         taps = {key: val[0] for key, val in taps.items()}
         taps.update(
             attention_norm_output=h[0],

@@ -3,6 +3,8 @@
 This guards the pins themselves: a dropped term, a wrong sign or index, or a
 misread pairing in any oracle step must make at least one pin test fail.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -49,13 +51,15 @@ def _rope_sign(x, positions, theta, scaling=None):
     return np.concatenate([x1 * c + x2 * s, x2 * c - x1 * s], axis=-1)
 
 
-def _attn_factory(scale=True, gqa="div", strict=False):
-    def attn(q, k, v, q_positions, k_positions, return_pattern=False):
+def _attn_factory(scale=True, gqa="div", strict=False, window_slack=0):
+    def attn(q, k, v, q_positions, k_positions, return_pattern=False, window=0):
         q, k, v = (np.asarray(a, dtype=F64) for a in (q, k, v))
         H, Tq, d = q.shape
         Hkv = k.shape[0]
         qp, kp = np.asarray(q_positions), np.asarray(k_positions)
         vis = (kp[None, :] < qp[:, None]) | (kp[None, :] == 0) if strict else kp[None, :] <= qp[:, None]
+        if window > 0:
+            vis = vis & (qp[:, None] - kp[None, :] < window + window_slack)
         out = np.empty((H, Tq, d))
         ss, pp = [], []
         for h in range(H):
@@ -110,14 +114,56 @@ def _mlp_swapped(cfg, w, h):
     return _orig_mlp(cfg, w2, h)
 
 
-def _finish_no_residual(cfg, w, x_rows, heads_out):
-    taps = _orig_finish(cfg, w, x_rows, heads_out)
+def _finish_no_residual(cfg, w, x_rows, heads_out, h_rows):
+    taps = _orig_finish(cfg, w, x_rows, heads_out, h_rows)
     taps["layer_output"] = taps["layer_output"] - x_rows
     return taps
 
 
+def _finish_gate_from_raw_input(cfg, w, x_rows, heads_out, h_rows):
+    # the gate projected from the block's input instead of the normed rows
+    return _orig_finish(cfg, w, x_rows, heads_out, x_rows)
+
+
+def _sigmoid_sign(u):
+    u = np.asarray(u, dtype=F64)
+    return 1.0 / (1.0 + np.exp(u))
+
+
+def _finish_norm_after_residual(cfg, w, x_rows, heads_out, h_rows):
+    # the sandwich post-norms applied to the residual sums instead of the sublayer outputs
+    if not cfg.sandwich_norm:
+        return _orig_finish(cfg, w, x_rows, heads_out, h_rows)
+    plain = dataclasses.replace(cfg, sandwich_norm=False)
+    taps = _orig_finish(plain, w, x_rows, heads_out, h_rows)
+    mid = ob.rms_norm(taps["layer_mid"], w["post_attn_norm"], cfg.rms_norm_eps)
+    h2 = ob.rms_norm(mid, w["post_attention_layernorm"], cfg.rms_norm_eps)
+    m = ob.mlp(plain, w, h2)
+    taps.update(layer_mid=mid, attention_output=mid - x_rows, mlp_output=m["mlp_output"],
+                layer_output=ob.rms_norm(mid + m["mlp_output"], w["post_mlp_norm"], cfg.rms_norm_eps))
+    return taps
+
+
+def _finish_no_mlp_post_norm(cfg, w, x_rows, heads_out, h_rows):
+    taps = _orig_finish(cfg, w, x_rows, heads_out, h_rows)
+    if cfg.sandwich_norm:
+        raw = taps["mlp_neurons"] @ w["down_proj"].T
+        taps.update(mlp_output=raw, layer_output=taps["layer_mid"] + raw)
+    return taps
+
+
+def _project_q_rope_always(cfg, w, h_norm_rows, positions_rows):
+    return _orig_project_q(dataclasses.replace(cfg, use_rope=True), w, h_norm_rows, positions_rows)
+
+
+def _project_kv_rope_always(cfg, w, h_norm, positions):
+    return _orig_project_kv(dataclasses.replace(cfg, use_rope=True), w, h_norm, positions)
+
+
 _orig_finish = ob._finish_rows
 _orig_mlp = ob.mlp
+_orig_project_q = ob._project_q
+_orig_project_kv = ob._project_kv
 
 MUTATIONS = {
     "rms_eps_outside_sqrt": [("rms_norm", _rms_eps_outside)],
@@ -135,6 +181,14 @@ MUTATIONS = {
     "swiglu_gate_up_swapped": [("mlp", _mlp_swapped)],
     "missing_residual": [("_finish_rows", _finish_no_residual)],
     "rope_scaling_ramp_reversed": [("rope_inv_freq", _scaling_ramp_reversed)],
+    "attn_window_one_too_wide": [("causal_gqa_attention", _attn_factory(window_slack=1))],
+    "attn_window_one_too_narrow": [("causal_gqa_attention", _attn_factory(window_slack=-1))],
+    "gate_from_raw_input": [("_finish_rows", _finish_gate_from_raw_input)],
+    "gate_sigmoid_sign": [("sigmoid", _sigmoid_sign)],
+    "sandwich_norm_after_residual": [("_finish_rows", _finish_norm_after_residual)],
+    "sandwich_mlp_post_norm_dropped": [("_finish_rows", _finish_no_mlp_post_norm)],
+    "rotary_on_whole_prefix_blocks": [("_project_q", _project_q_rope_always),
+                                      ("_project_kv", _project_kv_rope_always)],
 }
 
 PIN_TESTS = [
@@ -154,6 +208,14 @@ PIN_TESTS = [
     pins.test_block_identity_and_taps,
     pins.test_llama3_scaling_keeps_fast_divides_slow_and_blends_between,
     pins.test_yarn_scaling_keeps_fast_divides_slow_and_scales_attention,
+    lambda: pins.test_attention_window_brute_force(3),
+    pins.test_attention_window_special_cases,
+    lambda: pins.test_afmoe_block_brute_force(3, True, True, True),
+    lambda: pins.test_afmoe_block_brute_force(0, False, True, True),
+    pins.test_afmoe_identity_and_post_norm_taps,
+    pins.test_afmoe_sandwich_scale_invariance,
+    pins.test_afmoe_gate_taps_and_half_gate,
+    pins.test_afmoe_whole_prefix_block_queries_are_q_norm_output,
 ]
 
 

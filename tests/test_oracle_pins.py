@@ -9,6 +9,7 @@ import dataclasses
 import json
 import math
 import os
+import zlib
 
 import numpy as np
 import pytest
@@ -99,19 +100,23 @@ def test_rope_identity_norm_and_relative_position():
 
 # ---------------------------------------------------------------- attention
 
-def _attention_loops(q, k, v, group):
-    """Pure-Python triple loop: softmax over visible keys, then the value mix."""
+def _attention_loops(q, k, v, group, window=0):
+    """Pure-Python triple loop: softmax over visible keys, then the value mix.
+
+    window > 0: query i sees keys i - window + 1 .. i only ("afmoe": the last
+    sliding_window tokens)."""
     H, T, d = len(q), len(q[0]), len(q[0][0])
     out = [[[0.0] * d for _ in range(T)] for _ in range(H)]
     for h in range(H):
         j = h // group
         for i in range(T):
-            s = [sum(q[h][i][c] * k[j][t][c] for c in range(d)) / math.sqrt(d) for t in range(i + 1)]
+            keys = list(range(max(0, i - window + 1) if window else 0, i + 1))
+            s = [sum(q[h][i][c] * k[j][t][c] for c in range(d)) / math.sqrt(d) for t in keys]
             m = max(s)
             e = [math.exp(x - m) for x in s]
             z = sum(e)
             for c in range(d):
-                out[h][i][c] = sum(e[t] / z * v[j][t][c] for t in range(i + 1))
+                out[h][i][c] = sum(e[n] / z * v[j][t][c] for n, t in enumerate(keys))
     return out
 
 
@@ -122,6 +127,40 @@ def test_attention_brute_force():
     got = oracle.causal_gqa_attention(q, k, v, np.arange(T), np.arange(T))
     want = _attention_loops(q.tolist(), k.tolist(), v.tolist(), H // Hkv)
     np.testing.assert_allclose(got, np.array(want), rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("window", [1, 2, 3, 5])
+def test_attention_window_brute_force(window):
+    rng = np.random.default_rng(30 + window)
+    H, Hkv, T, d = 4, 2, 7, 4
+    q, k, v = (rng.standard_normal((n, T, d)) for n in (H, Hkv, Hkv))
+    got = oracle.causal_gqa_attention(q, k, v, np.arange(T), np.arange(T), window=window)
+    want = _attention_loops(q.tolist(), k.tolist(), v.tolist(), H // Hkv, window)
+    np.testing.assert_allclose(got, np.array(want), rtol=1e-12, atol=1e-14)
+
+
+def test_attention_window_special_cases():
+    rng = np.random.default_rng(31)
+    H, T, d = 2, 8, 4
+    q, k, v = (rng.standard_normal((n, T, d)) for n in (H, 1, 1))
+    # a window of one token: every query reads its own value
+    o = oracle.causal_gqa_attention(q, k, v, np.arange(T), np.arange(T), window=1)
+    np.testing.assert_array_equal(o, np.broadcast_to(v[0], (H, T, d)))
+    # a window as long as the sequence is the plain causal mask
+    full = oracle.causal_gqa_attention(q, k, v, np.arange(T), np.arange(T))
+    np.testing.assert_array_equal(oracle.causal_gqa_attention(q, k, v, np.arange(T), np.arange(T), window=T), full)
+    # a window of two: query i mixes v[i-1] and v[i] by the softmax of their two scores
+    o = oracle.causal_gqa_attention(q, k, v, np.arange(T), np.arange(T), window=2)
+    for i in range(1, T):
+        s0, s1 = q[0, i] @ k[0, i - 1] / math.sqrt(d), q[0, i] @ k[0, i] / math.sqrt(d)
+        w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+        np.testing.assert_allclose(o[0, i], (1 - w1) * v[0, i - 1] + w1 * v[0, i], rtol=1e-12)
+    # positions, not indices, decide: queries at 10..13 over keys at 0..13 with a window of 3
+    qp, kp = np.arange(10, 14), np.arange(14)
+    k2, v2 = rng.standard_normal((1, 14, d)), rng.standard_normal((1, 14, d))
+    o = oracle.causal_gqa_attention(q[:, :4], k2, v2, qp, kp, window=3)
+    want = oracle.causal_gqa_attention(q[:, :4], k2[:, 8:], v2[:, 8:], qp, kp[8:], window=3)
+    np.testing.assert_allclose(o, want, rtol=1e-14)
 
 
 def test_attention_special_cases():
@@ -253,6 +292,10 @@ def _weights(cfg, rng, gain_std=0.3):
         "down_proj": 0.4 * rng.standard_normal((D, F)),
         "q_norm": 1 + gain_std * rng.standard_normal(d),
         "k_norm": 1 + gain_std * rng.standard_normal(d),
+        # "afmoe": the attention gate and the two sandwich post-norms
+        "attn_gate_proj": 0.4 * rng.standard_normal((H * d, D)),
+        "post_attn_norm": 1 + gain_std * rng.standard_normal(D),
+        "post_mlp_norm": 1 + gain_std * rng.standard_normal(D),
     }
     return w
 
@@ -261,18 +304,25 @@ def _block_loops(cfg, w, x):
     """Pure-Python restatement of one sequence's block, element by element.
 
     Written from the "LlamaForCausalLM-32L-4096d" pseudo-code with the "arcee" /
-    "apertus" MLP variants and q/k norms; RoPE as a complex rotation.
+    "apertus" MLP variants and q/k norms; RoPE as a complex rotation. The
+    "afmoe" options: a window of the last sliding_window keys, no rotary, the
+    sigmoid head gate projected from the normed input, and the sandwich
+    post-norms of both sublayers.
     """
     T, D = len(x), len(x[0])
     H, Hkv, d, F = cfg.num_heads, cfg.num_kv_heads, cfg.head_dim, cfg.intermediate_size
     eps = cfg.rms_norm_eps
+    W = cfg.sliding_window
 
     def norm(row, g):
         r = 1.0 / math.sqrt(sum(a * a for a in row) / len(row) + eps)
         return [a * r * gg for a, gg in zip(row, g)]
 
-    def lin(row, W):
-        return [sum(W[o][i] * row[i] for i in range(len(row))) for o in range(len(W))]
+    def lin(row, Wm):
+        return [sum(Wm[o][i] * row[i] for i in range(len(row))) for o in range(len(Wm))]
+
+    def rot(a, t):
+        return _rope_complex(a, t, cfg.rope_theta) if cfg.use_rope else list(a)
 
     g1, g2 = list(w["input_layernorm"]), list(w["post_attention_layernorm"])
     Wq, Wk, Wv = (w[n].tolist() for n in ("q_proj", "k_proj", "v_proj"))
@@ -286,20 +336,27 @@ def _block_loops(cfg, w, x):
         if cfg.qk_norm:
             qh = [norm(a, list(w["q_norm"])) for a in qh]
             kh = [norm(a, list(w["k_norm"])) for a in kh]
-        Q.append([_rope_complex(a, t, cfg.rope_theta) for a in qh])
-        K.append([_rope_complex(a, t, cfg.rope_theta) for a in kh])
+        Q.append([rot(a, t) for a in qh])
+        K.append([rot(a, t) for a in kh])
         V.append(vh)
     outs = []
     for t in range(T):
+        first = max(0, t - W + 1) if W > 0 else 0  # the last W keys, this one included
+        keys = range(first, t + 1)
         heads = []
         for n in range(H):
             j = n // (H // Hkv)
-            s = [sum(Q[t][n][c] * K[u][j][c] for c in range(d)) / math.sqrt(d) for u in range(t + 1)]
+            s = [sum(Q[t][n][c] * K[u][j][c] for c in range(d)) / math.sqrt(d) for u in keys]
             m = max(s)
             e = [math.exp(a - m) for a in s]
             z = sum(e)
-            heads += [sum(e[u] / z * V[u][j][c] for u in range(t + 1)) for c in range(d)]
+            heads += [sum(e[i] / z * V[u][j][c] for i, u in enumerate(keys)) for c in range(d)]
+        if cfg.attn_gate:
+            gate = lin(h[t], w["attn_gate_proj"].tolist())
+            heads = [a / (1.0 + math.exp(-gg)) for a, gg in zip(heads, gate)]
         attn = lin(heads, w["o_proj"].tolist())
+        if cfg.sandwich_norm:
+            attn = norm(attn, list(w["post_attn_norm"]))
         mid = [a + b for a, b in zip(x[t], attn)]
         h2 = norm(mid, g2)
         up = lin(h2, w["up_proj"].tolist())
@@ -313,6 +370,8 @@ def _block_loops(cfg, w, x):
             neu = [ap * uu * uu + b * uu if uu > 0 else an * (math.expm1(min(uu, ep)) - uu) + b * uu
                    for uu in up]
         mlp = lin(neu, w["down_proj"].tolist())
+        if cfg.sandwich_norm:
+            mlp = norm(mlp, list(w["post_mlp_norm"]))
         outs.append([a + b for a, b in zip(mid, mlp)])
     return outs
 
@@ -320,7 +379,7 @@ def _block_loops(cfg, w, x):
 @pytest.mark.parametrize("act,qk_norm,H,Hkv", [("silu", False, 2, 2), ("relu2", False, 4, 2),
                                                ("xielu", True, 4, 1), ("silu", True, 2, 1)])
 def test_block_brute_force(act, qk_norm, H, Hkv):
-    rng = np.random.default_rng(hash((act, qk_norm, H)) % 2**32)
+    rng = np.random.default_rng(zlib.crc32(f"{act}-{qk_norm}-{H}".encode()))
     cfg = _tiny(act, qk_norm, H=H, Hkv=Hkv)
     w = _weights(cfg, rng)
     x = rng.standard_normal((2, 5, cfg.hidden_size))
@@ -328,6 +387,126 @@ def test_block_brute_force(act, qk_norm, H, Hkv):
     for b in range(2):
         np.testing.assert_allclose(taps["layer_output"][b], _block_loops(cfg, w, x[b].tolist()),
                                    rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- the afmoe block variant
+
+def _afmoe(window=0, use_rope=True, gate=True, sandwich=True, act="silu", H=4, Hkv=2, eps=1e-5):
+    """A tiny "afmoe"-style block: q/k norms, and the options under test."""
+    return dataclasses.replace(_tiny(act, True, H=H, Hkv=Hkv), sliding_window=window, use_rope=use_rope,
+                               attn_gate=gate, sandwich_norm=sandwich, rms_norm_eps=eps)
+
+
+@pytest.mark.parametrize("window,use_rope,gate,sandwich", [(3, True, True, True), (0, False, True, True),
+                                                          (2, True, False, False), (0, True, True, False),
+                                                          (0, True, False, True), (4, False, False, False)])
+def test_afmoe_block_brute_force(window, use_rope, gate, sandwich):
+    rng = np.random.default_rng(zlib.crc32(f"afmoe-{window}-{use_rope}-{gate}-{sandwich}".encode()))
+    cfg = _afmoe(window, use_rope, gate, sandwich)
+    w = _weights(cfg, rng)
+    x = rng.standard_normal((2, 7, cfg.hidden_size))
+    taps = oracle.block_forward(cfg, w, x)
+    for b in range(2):
+        np.testing.assert_allclose(taps["layer_output"][b], _block_loops(cfg, w, x[b].tolist()),
+                                   rtol=1e-11, atol=1e-12)
+
+
+def test_afmoe_identity_and_post_norm_taps():
+    # "afmoe", "The block, in order": layer input + attention_output + mlp_output
+    # == layer_output, the contributions being the post-norms' outputs: with unit
+    # gains every row of each has mean square m / (m + eps), m the mean square of
+    # the tensor entering the norm.
+    rng = np.random.default_rng(40)
+    cfg = _afmoe(window=3)
+    w = _weights(cfg, rng)
+    w["post_attn_norm"] = np.ones(cfg.hidden_size)
+    w["post_mlp_norm"] = np.ones(cfg.hidden_size)
+    x = rng.standard_normal((2, 6, cfg.hidden_size))
+    t = oracle.block_forward(cfg, w, x)
+    np.testing.assert_allclose(x + t["attention_output"] + t["mlp_output"], t["layer_output"], rtol=0, atol=1e-14)
+    raw_attn = t["o_proj_input"] @ w["o_proj"].T
+    raw_mlp = t["mlp_neurons"] @ w["down_proj"].T
+    for out, raw in ((t["attention_output"], raw_attn), (t["mlp_output"], raw_mlp)):
+        m = np.mean(raw * raw, axis=-1)
+        np.testing.assert_allclose(np.mean(out * out, axis=-1), m / (m + cfg.rms_norm_eps), rtol=1e-12)
+
+
+def test_afmoe_sandwich_scale_invariance():
+    # "afmoe", "The contributions are the post-norms' outputs": RMSNorm is
+    # scale-invariant up to eps, so scaling o_proj or down_proj leaves the stream
+    # unchanged; without the post-norms it does not.
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((1, 5, 6))
+    for sandwich in (True, False):
+        cfg = _afmoe(sandwich=sandwich, eps=1e-300)
+        w = _weights(cfg, rng)
+        base = oracle.block_forward(cfg, w, x)["layer_output"]
+        w2 = dict(w, o_proj=7.0 * w["o_proj"], down_proj=0.25 * w["down_proj"])
+        scaled = oracle.block_forward(cfg, w2, x)["layer_output"]
+        if sandwich:
+            np.testing.assert_allclose(scaled, base, rtol=1e-12, atol=1e-13)
+        else:
+            assert np.max(np.abs(scaled - base)) > 1e-2
+
+
+def test_afmoe_gate_taps_and_half_gate():
+    # "afmoe", "Attention: per-head q/k norms and a sigmoid gate on every head":
+    # o_proj's input is heads.flatten(-2) * sigmoid(gate), the gate projected from
+    # the attention's input (the normed rows) and attention_head_outputs ungated.
+    rng = np.random.default_rng(42)
+    cfg = _afmoe(sandwich=False)
+    w = _weights(cfg, rng)
+    x = rng.standard_normal((2, 5, cfg.hidden_size))
+    t = oracle.block_forward(cfg, w, x)
+    gate = t["attention_norm_output"] @ w["attn_gate_proj"].T
+    np.testing.assert_allclose(t["attention_gate"], gate, rtol=1e-13, atol=1e-14)
+    sig = np.vectorize(lambda g: 1.0 / (1.0 + math.exp(-g)))(gate)
+    heads = t["attention_head_outputs"].reshape(2, 5, -1)
+    np.testing.assert_allclose(t["o_proj_input"], heads * sig, rtol=1e-13, atol=1e-15)
+    # zero gate weights: sigmoid(0) = 1/2 halves the attention's contribution
+    w0 = dict(w, attn_gate_proj=np.zeros_like(w["attn_gate_proj"]))
+    half = oracle.block_forward(cfg, w0, x)["attention_output"]
+    ungated = oracle.block_forward(dataclasses.replace(cfg, attn_gate=False), w, x)
+    np.testing.assert_allclose(half, 0.5 * ungated["attention_output"], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(t["attention_head_outputs"], ungated["attention_head_outputs"], rtol=0, atol=0)
+
+
+def test_afmoe_whole_prefix_block_queries_are_q_norm_output():
+    # "afmoe", "Rotary runs on the sliding-window blocks only": on a full block
+    # attention_queries is q_norm's output unchanged, at every position.
+    rng = np.random.default_rng(43)
+    cfg = _afmoe(use_rope=False)
+    w = _weights(cfg, rng)
+    x = rng.standard_normal((1, 6, cfg.hidden_size))
+    t = oracle.block_forward(cfg, w, x)
+    for pos in range(6):
+        qn = oracle.rms_norm((t["attention_norm_output"][0, pos] @ w["q_proj"].T).reshape(4, 4), w["q_norm"], 1e-5)
+        np.testing.assert_allclose(t["attention_queries"][0, :, pos], qn, rtol=1e-13, atol=1e-15)
+    # with the rotary the queries past position 0 differ
+    tr = oracle.block_forward(dataclasses.replace(cfg, use_rope=True), w, x)
+    assert np.max(np.abs(tr["attention_queries"][0, :, 1:] - t["attention_queries"][0, :, 1:])) > 1e-3
+
+
+def test_afmoe_window_decode_and_chunk_match_the_prefill():
+    # The cache forms of a windowed block (a decode step, a prefill chunk) give
+    # the windowed prefill's rows.
+    rng = np.random.default_rng(44)
+    cfg = _afmoe(window=3)
+    w = _weights(cfg, rng)
+    B, T = 2, 9
+    x = rng.standard_normal((B, T, cfg.hidden_size))
+    full = oracle.block_forward(cfg, w, x)
+    cap = T + 1
+    ck = np.zeros((B, 2, cap, 4))
+    cv = np.zeros((B, 2, cap, 4))
+    ck[:, :, :T] = full["attention_keys"]
+    cv[:, :, :T] = full["attention_values"]
+    dec = oracle.decode_step(cfg, w, x[:, T - 1], ck, cv, np.full(B, T - 1))
+    np.testing.assert_allclose(dec["layer_output"], full["layer_output"][:, T - 1], rtol=1e-12, atol=1e-13)
+    lens = np.array([2, 5])
+    ch = oracle.prefill_with_cache(cfg, w, np.stack([x[0, 2:6], x[1, 5:9]]), ck, cv, lens)
+    np.testing.assert_allclose(ch["layer_output"][0], full["layer_output"][0, 2:6], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(ch["layer_output"][1], full["layer_output"][1, 5:9], rtol=1e-12, atol=1e-13)
 
 
 def test_block_identity_and_taps():
