@@ -131,20 +131,26 @@ def work_counts(wl):
     M = B * T
     es = 2 if wl.dtype == "bf16" else 4
     n_up = 2 * F if wl.hidden_act == "silu" else F
-    g = {"qkv": 2.0 * M * D * (H + 2 * Hkv) * d, "o": 2.0 * M * H * d * D, "up": 2.0 * M * D * n_up,
+    n_qkv = (2 * H if wl.attn_gate else H) + 2 * Hkv  # heads of the fused projection (+ the attention gate)
+    W = wl.sliding_window
+
+    def keys_seen(first_pos, n):  # keys visible to the queries at positions first_pos .. first_pos + n - 1
+        return float(sum(min(p + 1, W) if W else p + 1 for p in range(first_pos, first_pos + n)))
+
+    g = {"qkv": 2.0 * M * D * n_qkv * d, "o": 2.0 * M * H * d * D, "up": 2.0 * M * D * n_up,
          "down": 2.0 * M * F * D}
     if wl.cache_len and T == 1:
-        L = wl.cache_len + 1
+        L = keys_seen(wl.cache_len, 1)
         g["attn"] = 4.0 * B * H * d * L
         kv_bytes = 2.0 * B * Hkv * L * d * es
-    elif wl.cache_len:  # a prefill chunk: query t sees cache_len + t + 1 keys
-        L = wl.cache_len
-        g["attn"] = 4.0 * B * H * d * (T * L + T * (T + 1) / 2)
-        kv_bytes = 2.0 * B * Hkv * (L + T) * d * es
+    elif wl.cache_len:  # a prefill chunk: query t sees the keys up to position cache_len + t
+        g["attn"] = 4.0 * B * H * d * keys_seen(wl.cache_len, T)
+        first = max(0, wl.cache_len - W + 1) if W else 0
+        kv_bytes = 2.0 * B * Hkv * (wl.cache_len + T - first) * d * es
     else:
-        g["attn"] = 4.0 * B * H * d * T * (T + 1) / 2
+        g["attn"] = 4.0 * B * H * d * keys_seen(0, T)
         kv_bytes = 0.0
-    weight_bytes = es * (D * (H + 2 * Hkv) * d + H * d * D + n_up * D + F * D + 2 * D)
+    weight_bytes = es * (D * n_qkv * d + H * d * D + n_up * D + F * D + (4 if wl.sandwich_norm else 2) * D)
     if wl.n_layers:  # the model: every layer, plus lm_head
         g = {k: v * wl.n_layers for k, v in g.items()}
         g["lm_head"] = 2.0 * M * D * wl.vocab
@@ -161,7 +167,10 @@ def oracle_tokens_per_s(wl, w_cpu, x_cpu, cache_cpu, tokens_cap):
     import oracle
     cfg = oracle.BlockConfig(wl.hidden_size, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.intermediate_size,
                              wl.hidden_act, wl.rms_norm_eps, wl.rope_theta, wl.qk_norm, wl.xielu_alpha_p,
-                             wl.xielu_alpha_n)
+                             wl.xielu_alpha_n,
+                             rope_scaling=oracle.RopeScaling(*wl.rope_scaling) if wl.rope_scaling else None,
+                             sliding_window=wl.sliding_window, use_rope=wl.use_rope, attn_gate=wl.attn_gate,
+                             sandwich_norm=wl.sandwich_norm)
     wn = {k: v.double().numpy() for k, v in w_cpu.items()}
     t0 = time.perf_counter()
     if wl.cache_len and wl.seq > 1:
@@ -224,7 +233,7 @@ def config_of(wl, n):
          "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "ffn": wl.intermediate_size, "act": wl.hidden_act,
          "qk_norm": wl.qk_norm, "l2": "flushed between timed steps (256 MiB written, then read back so that "
                                                        "its dirty lines are written back before the step)",
-         "weights": "bf16 (prefill: fp16 copies of o_proj/gate/up prepared once, outside the timed region)",
+         "weights": "bf16, with fp16 copies of q/k/v(/gate)/o_proj/gate/up prepared once, outside the timed region",
          "parallelism": "replicas" if n > 1 else "single"}
     if wl.cache_len:
         c["cache_len"] = wl.cache_len
@@ -288,8 +297,8 @@ def run_ours(args, wl):
         lens0 = torch.full((wl.batch,), wl.cache_len, dtype=torch.int32, device=dev)
         cache = {"k": kc, "v": vc, "lens": lens0.clone()}
     blk = DecoderBlock.from_workload(wl)
-    if wl.dtype == "bf16" and not decode:
-        w = blk.prepare(w)  # one-time load step: fp16 copies of wo / w_gate / w_up
+    if wl.dtype == "bf16":
+        w = blk.prepare(w)  # one-time load step: fp16 copies of the weights the GEMMs read
     out = torch.empty_like(x)
     ws = torch.empty(blk.workspace_bytes(wl.batch, wl.seq, cached), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)

@@ -17,6 +17,18 @@
  * heads j*G .. j*G+G-1, G = num_heads / num_kv_heads ("arcee", "Grouped-query
  * attention, 128-wide heads").
  *
+ * The "afmoe" block variant (dense MLP), four descriptor options:
+ *   sliding_window  attention over the last W positions ("Rotary runs on the
+ *                   sliding-window blocks only": 2048 on Trinity Nano and Mini)
+ *   no_rope         no rotary on q and k (afmoe's whole-prefix blocks)
+ *   attn_gate       o_proj reads heads * sigmoid(n1 W_attn_gate^T), one gate value
+ *                   per channel of every head ("Attention: per-head q/k norms and a
+ *                   sigmoid gate on every head")
+ *   sandwich_norm   h   = x + rmsnorm(o_proj(...), post_attn_g)
+ *                   out = h + rmsnorm(down_proj(...), post_mlp_g)
+ *                   ("The block, in order"); the MLP's input norm stays ln2_g
+ *                   (afmoe's pre_mlp_layernorm).
+ *
  * Conventions for every entry point:
  *  - Pointers named as device pointers are CUDA device addresses owned by the
  *    caller; the library never frees or keeps them past the call. Host
@@ -100,16 +112,24 @@ typedef struct {
   float rope_factor;        /* >= 1 */
   int rope_orig_max_pos;    /* the original context length the scaling stretches */
   float rope_low, rope_high;
+  /* the "afmoe" options (0 = off for each) */
+  int sliding_window;  /* W > 0: query at position p sees keys at positions p - W + 1 .. p */
+  int no_rope;         /* 1: no rotary (needs rope_type BLK_ROPE_PLAIN) */
+  int attn_gate;       /* 1: sigmoid gate on the head outputs (weights.w_attn_gate) */
+  int sandwich_norm;   /* 1: post-norms of both sublayers (weights.post_attn_g, post_mlp_g) */
 } blk_desc;
 
 /* Block weights: device pointers in the descriptor's dtype.
  * Shapes: ln1_g, ln2_g [D]; wq [H*d, D]; wk, wv [Hkv*d, D]; q_norm_g, k_norm_g
  * [d] (ignored unless qk_norm); wo [D, H*d]; w_gate [F, D] (SWIGLU only, else
- * NULL); w_up [F, D]; w_down [D, F]. */
+ * NULL); w_up [F, D]; w_down [D, F]; w_attn_gate [H*d, D] (attn_gate only);
+ * post_attn_g, post_mlp_g [D] (sandwich_norm only; afmoe's
+ * post_attention_layernorm and post_mlp_layernorm). */
 typedef struct {
   const void *ln1_g, *wq, *wk, *wv, *q_norm_g, *k_norm_g, *wo, *ln2_g;
   const void *w_gate, *w_up, *w_down;
   const void* prepared; /* NULL, or the buffer blk_prepare_weights filled for these weights */
+  const void *w_attn_gate, *post_attn_g, *post_mlp_g;
 } blk_weights;
 
 /* KV cache: k, v are [batch, Hkv, capacity, d] in the descriptor's dtype,
@@ -129,8 +149,9 @@ typedef struct {
 /* Optional debug outputs of blk_forward (nnterp tap names, "arcee", "The API").
  * Any member may be NULL. Device pointers in the descriptor's dtype:
  *   attention_queries [B,H,T,d], attention_keys / attention_values [B,Hkv,T,d]
- *   (prefill only), attention_head_outputs [B,T,H,d], attention_output,
- *   layer_mid, mlp_output [B,T,D], mlp_neurons [B,T,F].
+ *   (prefill only), attention_head_outputs [B,T,H,d] (before the attention
+ *   gate), attention_output, layer_mid, mlp_output [B,T,D] (after the sandwich
+ *   post-norms), mlp_neurons [B,T,F].
  * Requesting taps may launch extra copies; it does not change layer_output. */
 typedef struct {
   void *attention_queries, *attention_keys, *attention_values;
@@ -147,16 +168,20 @@ typedef struct blk_handle blk_handle;
 blk_status blk_create(const blk_desc* desc, blk_handle** out);
 
 /* Optional one-time weight preparation (bf16 path), the step an inference
- * engine does when it loads a model: fp16 copies of wo, w_gate and w_up are
- * written to `prepared`, a caller-owned device buffer of at least
- * blk_prepared_bytes(h) bytes. With weights.prepared set, the prefill's o_proj
- * and MLP-up GEMMs take fp16 operands (attention output and normed rows in fp16
- * too): 3 more mantissa bits than bf16 at the same tensor-core rate. The
- * conversion is exact for every bf16 weight with 2^-17 <= |w| <= 65504; smaller
- * ones move by at most 2^-25. The copies must be refreshed whenever the bf16
- * weights change. Synchronises `stream` (it checks the range on the device).
+ * engine does when it loads a model: fp16 copies of wq, wk, wv (and
+ * w_attn_gate), wo, w_gate and w_up are written to `prepared`, a caller-owned
+ * device buffer of at least blk_prepared_bytes(h) bytes. With weights.prepared
+ * set, the Q/K/V, o_proj and MLP-up GEMMs of prefills, prefill chunks and
+ * decode steps take fp16 operands (the input norm's rows, the attention output
+ * and the MLP's normed input in fp16 too): 3 more mantissa bits than bf16 at
+ * the same tensor-core rate and the same bytes streamed. The conversion is exact for every bf16 weight with
+ * 2^-17 <= |w| <= 65504; smaller ones move by at most 2^-25. The input norm's
+ * fp16 rows are normalized before rounding, so they stay finite when
+ * max|ln1_g| * sqrt(D) <= 65504 (likewise ln2_g on a sandwich block); larger
+ * gains are refused. The copies must be refreshed whenever the bf16 weights
+ * change. Synchronises `stream` (it checks the ranges).
  * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED (fp32 handle, or a
- * weight outside the fp16 range: then use the weights unprepared), CUDA. */
+ * weight or gain outside those ranges: then use the weights unprepared), CUDA. */
 size_t blk_prepared_bytes(const blk_handle* h);
 blk_status blk_prepare_weights(blk_handle* h, const blk_weights* w, void* prepared, size_t bytes, void* stream);
 

@@ -25,14 +25,16 @@ class blk_desc(ctypes.Structure):
                 ("rope_theta", c_float), ("eps", c_float), ("act", c_int), ("xielu_alpha_p", c_float),
                 ("xielu_alpha_n", c_float), ("xielu_beta", c_float), ("xielu_eps", c_float), ("qk_norm", c_int),
                 ("dtype", c_int), ("max_batch", c_int), ("max_seq", c_int), ("rope_type", c_int),
-                ("rope_factor", c_float), ("rope_orig_max_pos", c_int), ("rope_low", c_float), ("rope_high", c_float)]
+                ("rope_factor", c_float), ("rope_orig_max_pos", c_int), ("rope_low", c_float), ("rope_high", c_float),
+                ("sliding_window", c_int), ("no_rope", c_int), ("attn_gate", c_int), ("sandwich_norm", c_int)]
 
 ROPE_TYPES = {"yarn": 1, "llama3": 2}
 
 
 class blk_weights(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("ln1_g", "wq", "wk", "wv", "q_norm_g", "k_norm_g", "wo", "ln2_g",
-                                         "w_gate", "w_up", "w_down", "prepared")]
+                                         "w_gate", "w_up", "w_down", "prepared", "w_attn_gate", "post_attn_g",
+                                         "post_mlp_g")]
 
 
 class blk_kv_cache(ctypes.Structure):
@@ -144,11 +146,16 @@ def set_wait_timeout_ns(ns: int):
 
 
 def make_weights_struct(w: dict) -> blk_weights:
-    """Page-named weight tensors (input_layernorm, q_proj, ...) -> blk_weights."""
+    """Page-named weight tensors (input_layernorm, q_proj, ...) -> blk_weights.
+
+    The "afmoe" weights: attn_gate_proj (the attention gate), post_attn_norm and
+    post_mlp_norm (the sandwich post-norms); post_attention_layernorm stays the
+    MLP's input norm."""
     g = w.get
     return blk_weights(_ptr(g("input_layernorm")), _ptr(g("q_proj")), _ptr(g("k_proj")), _ptr(g("v_proj")),
                        _ptr(g("q_norm")), _ptr(g("k_norm")), _ptr(g("o_proj")), _ptr(g("post_attention_layernorm")),
-                       _ptr(g("gate_proj")), _ptr(g("up_proj")), _ptr(g("down_proj")), _ptr(g("prepared")))
+                       _ptr(g("gate_proj")), _ptr(g("up_proj")), _ptr(g("down_proj")), _ptr(g("prepared")),
+                       _ptr(g("attn_gate_proj")), _ptr(g("post_attn_norm")), _ptr(g("post_mlp_norm")))
 
 
 class DecoderBlock:
@@ -156,12 +163,14 @@ class DecoderBlock:
 
     def __init__(self, hidden, n_heads, n_kv_heads, head_dim, ffn, act="silu", dtype="bf16", qk_norm=False,
                  rope_theta=10000.0, eps=1e-5, xielu_alpha_p=0.8, xielu_alpha_n=0.8, xielu_beta=0.5,
-                 xielu_eps=-1e-6, max_batch=64, max_seq=4096, rope_scaling=None):
+                 xielu_eps=-1e-6, max_batch=64, max_seq=4096, rope_scaling=None, sliding_window=0, use_rope=True,
+                 attn_gate=False, sandwich_norm=False):
         # rope_scaling: None, or (kind, factor, original_max_position, low, high), kind "yarn" | "llama3"
         rs = (ROPE_TYPES[rope_scaling[0]], *rope_scaling[1:]) if rope_scaling else (0, 1.0, 0, 0.0, 0.0)
         self.desc = blk_desc(hidden, n_heads, n_kv_heads, head_dim, ffn, rope_theta, eps, ACTS[act],
                              xielu_alpha_p, xielu_alpha_n, xielu_beta, xielu_eps, int(bool(qk_norm)), DTYPES[dtype],
-                             max_batch, max_seq, rs[0], float(rs[1]), int(rs[2]), float(rs[3]), float(rs[4]))
+                             max_batch, max_seq, rs[0], float(rs[1]), int(rs[2]), float(rs[3]), float(rs[4]),
+                             int(sliding_window), int(not use_rope), int(bool(attn_gate)), int(bool(sandwich_norm)))
         h = c_void_p()
         _check(lib().blk_create(ctypes.byref(self.desc), ctypes.byref(h)))
         self.handle = h
@@ -173,7 +182,8 @@ class DecoderBlock:
                    act=wl.hidden_act, dtype=wl.dtype, qk_norm=wl.qk_norm, rope_theta=wl.rope_theta,
                    eps=wl.rms_norm_eps, xielu_alpha_p=wl.xielu_alpha_p, xielu_alpha_n=wl.xielu_alpha_n,
                    max_batch=max_batch or wl.batch, max_seq=max_seq or wl.cache_len + wl.seq,
-                   rope_scaling=wl.rope_scaling)
+                   rope_scaling=wl.rope_scaling, sliding_window=wl.sliding_window, use_rope=wl.use_rope,
+                   attn_gate=wl.attn_gate, sandwich_norm=wl.sandwich_norm)
 
     def close(self):
         if self.handle:

@@ -10,7 +10,10 @@
 // about 512 keys): the G = H/Hkv query heads of the group sit on the MMA's
 // rows, and the four compute warps each own 16 keys of every tile (their
 // partial softmax states merge at the end of the unit). Splits are merged by
-// a second small kernel.
+// a second small kernel, which also applies the "afmoe" head gate. With a
+// sliding window the splits cover only the last `window` keys.
+#include <cuda_fp16.h>
+
 #include <cstring>
 #include <mutex>
 
@@ -62,6 +65,7 @@ struct DecodeParams {
   float* ws_o;
   const int* kv_lens;
   int len_add, H, Hkv, kv_stride, chunk, splits, units;
+  int window;  // > 0: only the last `window` keys of each sequence
   DevStatus* status;
   unsigned long long wait_ns;
 };
@@ -82,7 +86,8 @@ __device__ __forceinline__ DecodeUnit decode_unit(const DecodeParams& p, int u) 
   r.kvh = (u / p.splits) % p.Hkv;
   r.b = u / (p.splits * p.Hkv);
   const int kv_len = min(p.kv_lens[r.b] + p.len_add, p.kv_stride);  // never read past the cache
-  r.k0 = r.split * p.chunk;
+  const int first = p.window > 0 ? max(0, kv_len - p.window) : 0;    // the oldest key in the window
+  r.k0 = first + r.split * p.chunk;
   r.n_keys = max(0, min(kv_len, r.k0 + p.chunk) - r.k0);
   r.n_tiles = (r.n_keys + kTileKeys - 1) / kTileKeys;
   return r;
@@ -331,8 +336,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
   }
 }
 
+// gate (fp16, o's layout) multiplies the result; ungated (bf16) receives it before the gate;
+// o is fp16 when o_f16 (the operand of an o_proj on prepared fp16 weights), else bf16.
 __global__ void attn_decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__ ws_o,
-                                           __nv_bfloat16* __restrict__ o, int H, int splits) {
+                                           void* __restrict__ o, int H, int splits,
+                                           const __half* __restrict__ gate, __nv_bfloat16* __restrict__ ungated,
+                                           int o_f16) {
   pdl_launch_dependents();
   pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
@@ -346,7 +355,14 @@ __global__ void attn_decode_combine_kernel(const float* __restrict__ ws_ml, cons
     l += ws_ml[(base + s) * 2 + 1] * f;
     acc += ws_o[(base + s) * kD + c] * f;
   }
-  o[((size_t)b * H + h) * kD + c] = __float2bfloat16_rn(acc / l);
+  const size_t i = ((size_t)b * H + h) * kD + c;
+  float r = acc / l;
+  if (ungated) ungated[i] = __float2bfloat16_rn(r);
+  if (gate) r *= __half2float(gate[i]);
+  if (o_f16)
+    static_cast<__half*>(o)[i] = __float2half_rn(r);
+  else
+    static_cast<__nv_bfloat16*>(o)[i] = __float2bfloat16_rn(r);
 }
 
 }  // namespace
@@ -371,7 +387,8 @@ namespace {
 
 cudaError_t decode_core(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int kv_stride,
                         const int* kv_lens, int len_add, int splits, int max_len, float* ws, int num_sms,
-                        DevStatus* st, unsigned long long wait_ns, cudaStream_t s, const char** why) {
+                        DevStatus* st, unsigned long long wait_ns, cudaStream_t s, const char** why,
+                        const AttnOpts& opt) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -385,6 +402,8 @@ cudaError_t decode_core(const void* q, const void* k, const void* v, void* o, in
     *why = "cuTensorMapEncodeTiled failed for the KV cache";
     return cudaErrorInvalidValue;
   }
+  // max_len: the most keys a sequence attends to (at most the window)
+  if (opt.window > 0 && opt.window < max_len) max_len = opt.window;
   int chunk = (max_len + splits - 1) / splits;
   chunk = (chunk + kTileKeys - 1) / kTileKeys * kTileKeys;
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -398,13 +417,15 @@ cudaError_t decode_core(const void* q, const void* k, const void* v, void* o, in
   p.chunk = chunk;
   p.splits = splits;
   p.units = B * Hkv * splits;
+  p.window = opt.window > 0 ? opt.window : 0;
   p.status = st;
   p.wait_ns = wait_ns;
   const int grid = p.units < num_sms ? p.units : num_sms;
   launch_pdl(attn_decode_kernel, grid, kThreads, kSmem, s, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  launch_pdl(attn_decode_combine_kernel, dim3(H, B), kD, 0, s, p.ws_ml, p.ws_o, static_cast<__nv_bfloat16*>(o), H, splits);
+  launch_pdl(attn_decode_combine_kernel, dim3(H, B), kD, 0, s, p.ws_ml, p.ws_o, o, H, splits,
+             static_cast<const __half*>(opt.gate), static_cast<__nv_bfloat16*>(opt.ungated), opt.o_f16 ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -413,7 +434,7 @@ cudaError_t decode_core(const void* q, const void* k, const void* v, void* o, in
 cudaError_t launch_attn_decode_bf16(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv,
                                     int d, int kv_stride, const int* kv_lens, int len_add, int max_len,
                                     int split_cap, void* ws, int num_sms, DevStatus* st, unsigned long long wait_ns,
-                                    cudaStream_t s, const char** why) {
+                                    cudaStream_t s, const char** why, const AttnOpts& opt) {
   if (d != kD) {
     *why = "bf16 attention: head_dim must be 128";
     return cudaErrorInvalidValue;
@@ -423,11 +444,12 @@ cudaError_t launch_attn_decode_bf16(const void* q, const void* k, const void* v,
     return cudaErrorInvalidValue;
   }
   if (B <= 0) return cudaSuccess;
-  // max_len: upper bound of the keys per sequence this step (lens + len_add)
-  int splits = attn_decode_splits(B, Hkv, max_len, num_sms);
+  // max_len: upper bound of the keys per sequence this step (lens + len_add); a window caps it
+  const int span = opt.window > 0 && opt.window < max_len ? opt.window : max_len;
+  int splits = attn_decode_splits(B, Hkv, span, num_sms);
   if (splits > split_cap) splits = split_cap;  // the workspace holds split_cap splits: chunks grow instead
   return decode_core(q, k, v, o, B, H, Hkv, kv_stride, kv_lens, len_add, splits, max_len, static_cast<float*>(ws),
-                     num_sms, st, wait_ns, s, why);
+                     num_sms, st, wait_ns, s, why, opt);
 }
 
 // ------------------------------------------------------------------ allocation-free decode variant
@@ -490,7 +512,7 @@ cudaError_t launch_attn_decode_bf16_static(const void* q, const void* k, const v
   if (splits > fit) splits = fit;
   // every partial the combine step reads is written by this call first: nothing to clear
   return decode_core(q, k, v, o, B, H, Hkv, kv_stride, kv_lens, 0, splits, kv_stride, scratch, num_sms, nullptr,
-                     2000000000ULL, s, why);
+                     2000000000ULL, s, why, AttnOpts());
 }
 
 }  // namespace blk

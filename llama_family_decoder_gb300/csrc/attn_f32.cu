@@ -3,6 +3,9 @@
 // kv = h / (H / Hkv), keys j visible iff position(j) <= position(i)
 // ("LlamaForCausalLM-32L-4096d": softmax(q @ k.T / sqrt(128), mask=causal) @ v;
 // "arcee", "Grouped-query attention, 128-wide heads").
+// Options of the "afmoe" block: a window over the last W positions and a
+// per-channel sigmoid gate on the output (the gate values come in already
+// passed through the sigmoid).
 // One warp per (b, h, query); scores held in shared memory.
 #include "common.cuh"
 #include "kernels.h"
@@ -13,7 +16,8 @@ namespace {
 
 __global__ void attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
                                 float* __restrict__ o, int H, int Hkv, int Tq, int d, int kv_stride,
-                                const int* __restrict__ kv_lens, int len_add) {
+                                const int* __restrict__ kv_lens, int len_add, int window,
+                                const float* __restrict__ gate, float* __restrict__ ungated) {
   pdl_launch_dependents();
   pdl_wait();
   extern __shared__ float sc[];
@@ -21,13 +25,14 @@ __global__ void attn_f32_kernel(const float* __restrict__ q, const float* __rest
   const int lane = threadIdx.x;
   const int kv_len = kv_lens ? min(kv_lens[b] + len_add, kv_stride) : Tq;  // never read past the cache
   const int qpos = kv_len - Tq + i;  // this query's position; keys 0..qpos are visible
+  const int j0 = window > 0 ? max(0, qpos - window + 1) : 0;  // ... from j0 on, with a window
   const int kvh = h / (H / Hkv);
   const float* qr = q + (((size_t)b * H + h) * Tq + i) * d;
   const float* kb = k + ((size_t)b * Hkv + kvh) * kv_stride * d;
   const float* vb = v + ((size_t)b * Hkv + kvh) * kv_stride * d;
   const float scale = 1.0f / sqrtf((float)d);
   float m = -INFINITY;
-  for (int j = lane; j <= qpos; j += 32) {
+  for (int j = j0 + lane; j <= qpos; j += 32) {
     float s = 0.f;
     for (int c = 0; c < d; ++c) s = fmaf(qr[c], kb[(size_t)j * d + c], s);
     s *= scale;
@@ -36,25 +41,28 @@ __global__ void attn_f32_kernel(const float* __restrict__ q, const float* __rest
   }
   m = warp_max(m);
   float l = 0.f;
-  for (int j = lane; j <= qpos; j += 32) {
+  for (int j = j0 + lane; j <= qpos; j += 32) {
     const float p = expf(sc[j] - m);
     sc[j] = p;
     l += p;
   }
   l = warp_sum(l);
   __syncwarp();
-  float* orow = o + (((size_t)b * Tq + i) * H + h) * d;
+  const size_t orow = (((size_t)b * Tq + i) * H + h) * d;
   for (int c = lane; c < d; c += 32) {
     float acc = 0.f;
-    for (int j = 0; j <= qpos; ++j) acc = fmaf(sc[j], vb[(size_t)j * d + c], acc);
-    orow[c] = acc / l;
+    for (int j = j0; j <= qpos; ++j) acc = fmaf(sc[j], vb[(size_t)j * d + c], acc);
+    const float r = acc / l;
+    if (ungated) ungated[orow + c] = r;
+    o[orow + c] = gate ? r * gate[orow + c] : r;
   }
 }
 
 }  // namespace
 
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, int B, int H, int Hkv, int Tq,
-                            int d, int kv_stride, const int* kv_lens, int len_add, cudaStream_t s) {
+                            int d, int kv_stride, const int* kv_lens, int len_add, cudaStream_t s,
+                            const AttnOpts& opt) {
   if (B <= 0 || Tq <= 0) return cudaSuccess;
   const size_t smem = (size_t)kv_stride * sizeof(float);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
@@ -63,7 +71,8 @@ cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, floa
     if (e != cudaSuccess) return e;
   }
   dim3 grid(Tq, H, B);
-  launch_pdl(attn_f32_kernel, grid, 32, smem, s, q, k, v, o, H, Hkv, Tq, d, kv_stride, kv_lens, len_add);
+  launch_pdl(attn_f32_kernel, grid, 32, smem, s, q, k, v, o, H, Hkv, Tq, d, kv_stride, kv_lens, len_add,
+             opt.window > 0 ? opt.window : 0, static_cast<const float*>(opt.gate), static_cast<float*>(opt.ungated));
   return cudaGetLastError();
 }
 

@@ -3,6 +3,11 @@
 // softmax(q @ k.T / sqrt(128), mask=causal) @ v per head; "arcee", "Grouped-
 // query attention, 128-wide heads": query head h reads KV head h / (H / Hkv)).
 //
+// Options of the "afmoe" block ("Rotary runs on the sliding-window blocks only";
+// "Attention: per-head q/k norms and a sigmoid gate on every head"): a window
+// over the last W positions (the key tiles before the first query's oldest key
+// are skipped, the rest masked), and a per-channel gate on the output.
+//
 // One CTA per (128-query tile, head, sequence), heaviest tiles first, 192 threads:
 //   warp 0      TMA producer: the Q tile once, then K and V tiles of 128 keys
 //               through a 2-stage ring (128-byte swizzle, two 64-column boxes).
@@ -49,6 +54,11 @@ struct AttnParams {
   // in that cache per sequence (the T queries sit at q_off[b] ..), or null for 0
   int kv_stride;
   const int* q_off;
+  // "afmoe": window > 0 keeps the keys at positions > query - window; gate (fp16, the
+  // output's layout) multiplies the output, ungated (bf16) receives it before the gate
+  int window;
+  const __half* gate;
+  __nv_bfloat16* ungated;
   float sl2;
   DevStatus* status;
   unsigned long long wait_ns;
@@ -132,7 +142,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const uint32_t tmem = *tmem_holder;
   const int off = p.q_off ? p.q_off[b] : 0;  // keys 0 .. off - 1 are earlier positions in the cache
   const int n_keys = off + kv_end;           // keys this query tile can see
-  const int n_tiles = (n_keys + kBKeys - 1) / kBKeys;  // S0: cols [0,128), S1: [128,256), O: [256,384)
+  // key tiles t0 .. t_end - 1: with a window, the first tile holds the first query's oldest key
+  const int t0 = p.window > 0 ? max(0, off + m0 - p.window + 1) / kBKeys : 0;
+  const int n_tiles = (n_keys + kBKeys - 1) / kBKeys - t0;  // S0: cols [0,128), S1: [128,256), O: [256,384)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -150,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           break;
         }
         mbar_arrive_expect_tx(kv_full(s), 2 * kTile);
-        const int row = kv_row + j * kBKeys;
+        const int row = kv_row + (t0 + j) * kBKeys;
         tma_load_2d(smem_u32(sK + s * kTile), &p.tk, 0, row, kv_full(s));
         tma_load_2d(smem_u32(sK + s * kTile + kSub), &p.tk, 64, row, kv_full(s));
         tma_load_2d(smem_u32(sV + s * kTile), &p.tv, 0, row, kv_full(s));
@@ -242,13 +254,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
       for (int c = 0; c < kBKeys; c += 16) tmem_ld16(tmem + lane_off + s * kBKeys + c, *reinterpret_cast<float(*)[16]>(&x[c]));
       tc_wait_ld();
-      const int n0 = j * kBKeys;
-      // raw scores: masked entries become -inf (only tiles on the diagonal or past the last key)
-      if ((n0 + kBKeys - 1 > off + m0) || (n0 + kBKeys > off + p.T)) {
-        const int lim = off + min(qi, p.T - 1) - n0;  // keys n0 + c with c <= lim are visible
+      const int n0 = (t0 + j) * kBKeys;
+      // raw scores: masked entries become -inf (only tiles on the diagonal, past the last key
+      // or, with a window, before the last query's oldest key)
+      const int qc = min(qi, p.T - 1);
+      if ((n0 + kBKeys - 1 > off + m0) || (n0 + kBKeys > off + p.T) ||
+          (p.window > 0 && n0 < off + min(m0 + kBQ - 1, p.T - 1) - p.window + 1)) {
+        const int lim = off + qc - n0;  // keys n0 + c with c <= lim are visible
+        const int first = p.window > 0 ? lim - p.window + 1 : -kBKeys;  // ... and c >= first
 #pragma unroll
         for (int c = 0; c < kBKeys; ++c)
-          if (c > lim) x[c] = -INFINITY;
+          if (c > lim || c < first) x[c] = -INFINITY;
       }
       if (n0 + kBKeys > n_keys && r >= n_keys - n0) {
         // V rows past the last key may hold anything (unused cache slots): zero them, so that
@@ -323,23 +339,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       __syncwarp();
       tc_fence_after();
       const float inv = 1.f / l;
-      uint16_t* orow = static_cast<uint16_t*>(p.o) + (((size_t)b * p.T + qi) * p.H + h) * kD;
+      const size_t orow_i = (((size_t)b * p.T + qi) * p.H + h) * kD;
+      uint16_t* orow = static_cast<uint16_t*>(p.o) + orow_i;
       const bool of16 = p.o_f16 != 0;
+      auto pack16 = [](const float (&v)[16], bool f16, uint4& w0, uint4& w1) {
+        w0 = make_uint4(pack2(v[0], v[1], f16), pack2(v[2], v[3], f16), pack2(v[4], v[5], f16),
+                        pack2(v[6], v[7], f16));
+        w1 = make_uint4(pack2(v[8], v[9], f16), pack2(v[10], v[11], f16), pack2(v[12], v[13], f16),
+                        pack2(v[14], v[15], f16));
+      };
 #pragma unroll 1
       for (int c = 0; c < kD; c += 16) {
         float ov[16];
         tmem_ld16(o_taddr + c, ov);
         tc_wait_ld();
         if (qi < p.T) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ov[i] *= inv;
           uint4 w0, w1;
-          w0.x = pack2(ov[0] * inv, ov[1] * inv, of16);
-          w0.y = pack2(ov[2] * inv, ov[3] * inv, of16);
-          w0.z = pack2(ov[4] * inv, ov[5] * inv, of16);
-          w0.w = pack2(ov[6] * inv, ov[7] * inv, of16);
-          w1.x = pack2(ov[8] * inv, ov[9] * inv, of16);
-          w1.y = pack2(ov[10] * inv, ov[11] * inv, of16);
-          w1.z = pack2(ov[12] * inv, ov[13] * inv, of16);
-          w1.w = pack2(ov[14] * inv, ov[15] * inv, of16);
+          if (p.ungated) {  // the head outputs before the gate (bf16)
+            pack16(ov, false, w0, w1);
+            reinterpret_cast<uint4*>(p.ungated + orow_i + c)[0] = w0;
+            reinterpret_cast<uint4*>(p.ungated + orow_i + c)[1] = w1;
+          }
+          if (p.gate) {
+            const uint4* g4 = reinterpret_cast<const uint4*>(p.gate + orow_i + c);
+            const uint4 ga = g4[0], gb = g4[1];
+            const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float2 gf = __half22float2(*reinterpret_cast<const __half2*>(&gw[i]));
+              ov[2 * i] *= gf.x;
+              ov[2 * i + 1] *= gf.y;
+            }
+          }
+          pack16(ov, of16, w0, w1);
           reinterpret_cast<uint4*>(orow + c)[0] = w0;
           reinterpret_cast<uint4*>(orow + c)[1] = w1;
         }
@@ -363,7 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
 cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int T,
                                    int d, bool f16, bool o_f16, DevStatus* st, unsigned long long wait_ns,
-                                   cudaStream_t s, const char** why, const int* q_off, int kv_stride) {
+                                   cudaStream_t s, const char** why, const int* q_off, int kv_stride,
+                                   const AttnOpts& opt) {
   if (d != kD) {
     *why = "tcgen05 attention: head_dim must be 128";
     return cudaErrorInvalidValue;
@@ -390,6 +425,9 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
   p.T = T;
   p.kv_stride = kv_stride;
   p.q_off = q_off;
+  p.window = opt.window > 0 ? opt.window : 0;
+  p.gate = static_cast<const __half*>(opt.gate);
+  p.ungated = static_cast<__nv_bfloat16*>(opt.ungated);
   p.n_qtiles = (T + kBQ - 1) / kBQ;
   p.sl2 = kLog2e / sqrtf((float)kD);
   p.status = st;

@@ -84,19 +84,26 @@ struct Carve {
 // fp16 copies of the weights the prefill's fp16 GEMMs read (blk_prepare_weights).
 struct Prepared {
   const void *wo, *wg, *wu;
+  const void *wq, *wk, *wv, *wag;  // the Q/K/V projection and the attention gate
 };
 
 size_t prepared_layout(const blk_desc& d, const void* base, Prepared* out) {
   Carve c(const_cast<void*>(base));
   Prepared p{};
-  p.wo = c.take((size_t)d.hidden * d.n_heads * d.head_dim * 2);
+  const size_t Hd = (size_t)d.n_heads * d.head_dim, KVd = (size_t)d.n_kv_heads * d.head_dim;
+  p.wo = c.take((size_t)d.hidden * Hd * 2);
   if (d.act == BLK_ACT_SWIGLU) p.wg = c.take((size_t)d.ffn * d.hidden * 2);
   p.wu = c.take((size_t)d.ffn * d.hidden * 2);
+  p.wq = c.take(Hd * d.hidden * 2);
+  p.wk = c.take(KVd * d.hidden * 2);
+  p.wv = c.take(KVd * d.hidden * 2);
+  if (d.attn_gate) p.wag = c.take(Hd * d.hidden * 2);
   if (out) *out = p;
   return c.off;
 }
 
-int qkv_cols(const blk_desc& d) { return (d.n_heads + 2 * d.n_kv_heads) * d.head_dim; }
+// Columns of the fused Q/K/V (and attention gate) projection.
+int qkv_cols(const blk_desc& d) { return (d.n_heads * (d.attn_gate ? 2 : 1) + 2 * d.n_kv_heads) * d.head_dim; }
 int mlp_cols(const blk_desc& d) { return d.act == BLK_ACT_SWIGLU ? 2 * d.ffn : d.ffn; }
 int max_cols(const blk_desc& d) {
   int n = qkv_cols(d);
@@ -110,7 +117,7 @@ constexpr int kMaxDecodeSplits = 16;
 // Decode GEMMs: weight tiles of 128 rows, token tiles of 64, 128 or 256.
 int dec_bn(int B) { return B <= 64 ? 64 : (B <= 128 ? 128 : 256); }
 int dec_tiles_qkv(const blk_desc& d) {
-  return (d.n_heads * d.head_dim + 127) / 128 + 2 * ((d.n_kv_heads * d.head_dim + 127) / 128);
+  return (d.attn_gate ? 2 : 1) * ((d.n_heads * d.head_dim + 127) / 128) + 2 * ((d.n_kv_heads * d.head_dim + 127) / 128);
 }
 
 // N-tile width for a GEMM with m_rows rows and n_cols output columns (per half
@@ -148,6 +155,7 @@ int norm_parts(int hidden, int bn) { return (hidden + bn - 1) / bn; }
 struct Ws {
   void *y, *q, *k, *v, *o, *mid, *neur, *C, *attn;
   float *rs1, *ss2;  // bf16: input-norm 1/rms per row (prefill); post-attention partial sums of squares
+  void* gate;        // attn_gate: sigmoid of the gate projection, o's layout (fp16; fp32 on the fp32 path)
 };
 
 Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, size_t* total) {
@@ -179,7 +187,9 @@ Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, siz
   } else {
     w.rs1 = static_cast<float*>(c.take(M * sizeof(float)));
     w.ss2 = static_cast<float*>(c.take(M * norm_parts(d.hidden, 128) * sizeof(float)));
+    if (d.sandwich_norm) w.C = c.take(M * d.hidden * sizeof(float));  // a sublayer's output before its post-norm
   }
+  if (d.attn_gate) w.gate = c.take(M * d.n_heads * d.head_dim * (d.dtype == BLK_BF16 ? 2 : 4));
   *total = c.off;
   return w;
 }
@@ -233,17 +243,24 @@ blk_status tc(const blk_handle* h, const TcGemmDesc& g, cudaStream_t s, const ch
 
 // cache_stride > 0: k and v are a KV cache of cache_stride rows per (sequence, KV head),
 // written at rows pos0[b] + t.
+// gate != null: the attention gate projection joins as a 4th segment; its sigmoid goes to gate (fp16).
+// f16: q/k/v stored as fp16; prep: the GEMM runs on the prepared fp16 weights (y is then fp16).
 blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, int B, int T, const int* pos0, void* q,
                     void* k, void* v, cudaStream_t s, const float* row_scale = nullptr, bool f16 = false,
-                    int cache_stride = 0) {
+                    int cache_stride = 0, void* gate = nullptr, const Prepared* prep = nullptr) {
   const blk_desc& d = h->d;
   TcGemmDesc g;
   g.na = 1;
   g.a[0] = {y, B * T, 0};
   g.nb = 3;
-  g.b[0] = {w->wq, d.n_heads * d.head_dim, 0};
-  g.b[1] = {w->wk, d.n_kv_heads * d.head_dim, d.n_heads * d.head_dim};
-  g.b[2] = {w->wv, d.n_kv_heads * d.head_dim, (d.n_heads + d.n_kv_heads) * d.head_dim};
+  g.b[0] = {prep ? prep->wq : w->wq, d.n_heads * d.head_dim, 0};
+  g.b[1] = {prep ? prep->wk : w->wk, d.n_kv_heads * d.head_dim, d.n_heads * d.head_dim};
+  g.b[2] = {prep ? prep->wv : w->wv, d.n_kv_heads * d.head_dim, (d.n_heads + d.n_kv_heads) * d.head_dim};
+  if (gate) {
+    g.nb = 4;
+    g.b[3] = {prep ? prep->wag : w->w_attn_gate, d.n_heads * d.head_dim, (d.n_heads + 2 * d.n_kv_heads) * d.head_dim};
+  }
+  g.f16 = prep != nullptr;
   g.K = d.hidden;
   const bool whole256 = (d.n_heads * d.head_dim) % 256 == 0 && (d.n_kv_heads * d.head_dim) % 256 == 0;
   static const int qkv_c[] = {256, 128};
@@ -257,6 +274,7 @@ blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, in
   }
   g.e.row_scale = row_scale;
   g.e.qkv_f16 = f16 ? 1 : 0;
+  g.e.gate = gate;
   return tc(h, g, s, "QKV GEMM");
 }
 
@@ -345,9 +363,11 @@ int dec_fused_splits(const blk_handle* h, int tiles, int num_kb, int B, Epi epi)
 
 // A fused decode GEMM: the weight segments on the MMA's M side, the B tokens of x
 // on N, each tile's K splits one cluster that finishes the tile's post-op.
+// f16: fp16 weights (prepared) and x.
 blk_status dec_gemm(const blk_handle* h, const TcSeg* segs, int nseg, const void* x, int B, int K, int splits,
-                    Epi epi, TcEpiArgs e, cudaStream_t s, const char* what) {
+                    Epi epi, TcEpiArgs e, cudaStream_t s, const char* what, bool f16 = false) {
   TcGemmDesc g;
+  g.f16 = f16;
   g.na = nseg;
   for (int i = 0; i < nseg; ++i) g.a[i] = segs[i];
   g.nb = 1;
@@ -364,8 +384,9 @@ blk_status dec_gemm(const blk_handle* h, const TcSeg* segs, int nseg, const void
 
 // The unfused form: transposed split-K partials [split][token][column], summed by a post kernel.
 blk_status bf16_stream_gemm(const blk_handle* h, const TcSeg* segs, int nseg, const void* x, int B, int K, float* C,
-                            int ldc, int* splits_out, cudaStream_t s, const char* what) {
+                            int ldc, int* splits_out, cudaStream_t s, const char* what, bool f16 = false) {
   TcGemmDesc g;
+  g.f16 = f16;
   g.na = nseg;
   int tiles = 0;
   for (int i = 0; i < nseg; ++i) {
@@ -433,21 +454,35 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
   // GEMM's A rows (x * g1 is x itself when g1 == 1), the per-row 1/rms multiplies
   // the accumulator in the epilogue. q/k/v and P are kept in fp16 (3 more
   // mantissa bits than bf16 at the same tensor-core rate); o and the neurons,
-  // which meet bf16 weights, stay bf16.
+  // which meet bf16 weights, stay bf16. With the sandwich norms, o_proj and down
+  // write their fp32 outputs and a row kernel applies the post-norm, the residual
+  // add and (after o_proj) the MLP's input norm.
   const blk_desc& d = h->d;
   const int M = B * T;
-  void* o = tap_or(taps, &blk_taps::attention_head_outputs, ws.o);
+  const bool gated = d.attn_gate != 0, sandwich = d.sandwich_norm != 0;
+  void* head_tap = taps ? taps->attention_head_outputs : nullptr;
+  void* o = (head_tap && !gated) ? head_tap : ws.o;
   void* mid_tap = taps ? taps->layer_mid : nullptr;
   void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
+  // with prepared (fp16) weights every GEMM operand formed from a norm or from the
+  // attention is fp16: 3 more mantissa bits than bf16 at the same tensor-core rate
+  Prepared prep{};
+  const bool f16 = w->prepared != nullptr;
+  if (f16) prepared_layout(d, w->prepared, &prep);
   prof_mark(h, "norm1_prep", 1, s);
-  BLK_TRY(check_cuda(launch_norm_prep(x, w->ln1_g, M, d.hidden, d.eps, ws.y, ws.rs1, nullptr, s), "input norm"));
+  if (f16)  // the normed rows in fp16 (normalized before rounding, so within fp16's range)
+    BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, M, d.hidden, d.eps, ws.y, true, s, false, true), "input norm"));
+  else      // x * g1 in bf16; the 1/rms of each row is applied in the QKV epilogue
+    BLK_TRY(check_cuda(launch_norm_prep(x, w->ln1_g, M, d.hidden, d.eps, ws.y, ws.rs1, nullptr, s), "input norm"));
+  const float* rs1 = f16 ? nullptr : ws.rs1;
   prof_mark(h, "qkv_gemm_rope", 1, s);
+  void* gate = gated ? ws.gate : nullptr;
   if (cache) {
     // bf16 q (the cache's K/V are bf16, so the attention runs on bf16 operands); K/V into the cache
     BLK_TRY(bf16_qkv(h, ws.y, w, B, T, cache->lens, tap_or(taps, &blk_taps::attention_queries, ws.q), cache->k,
-                     cache->v, s, ws.rs1, false, cache->capacity));
+                     cache->v, s, rs1, false, cache->capacity, gate, f16 ? &prep : nullptr));
   } else {
-    BLK_TRY(bf16_qkv(h, ws.y, w, B, T, nullptr, ws.q, ws.k, ws.v, s, ws.rs1, true));
+    BLK_TRY(bf16_qkv(h, ws.y, w, B, T, nullptr, ws.q, ws.k, ws.v, s, rs1, true, 0, gate, f16 ? &prep : nullptr));
   }
   if (taps && !cache) {  // the taps are bf16
     const size_t nq = (size_t)M * d.n_heads * d.head_dim, nkv = (size_t)M * d.n_kv_heads * d.head_dim;
@@ -457,29 +492,49 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
     if (taps->attention_values)
       BLK_TRY(check_cuda(launch_cast_f16_bf16(ws.v, taps->attention_values, nkv, s), "v tap"));
   }
-  // with prepared (fp16) weights, the attention output and the normed MLP input
-  // are fp16 operands of o_proj and of the MLP-up GEMM
-  Prepared prep{};
-  const bool f16 = w->prepared != nullptr;
-  if (f16) prepared_layout(d, w->prepared, &prep);
   void* o_buf = f16 ? ws.o : o;
+  AttnOpts opt;
+  opt.window = d.sliding_window;
+  opt.gate = gate;
+  opt.ungated = gated ? head_tap : nullptr;  // the tap reads the heads before the gate
   prof_mark(h, "attention", 1, s);
   const char* why = nullptr;
   cudaError_t e =
       cache ? launch_attn_prefill_tc(tap_or(taps, &blk_taps::attention_queries, ws.q), cache->k, cache->v, o_buf, B,
                                      d.n_heads, d.n_kv_heads, T, d.head_dim, false, f16, h->status,
-                                     (unsigned long long)g_wait_ns.load(), s, &why, cache->lens, cache->capacity)
+                                     (unsigned long long)g_wait_ns.load(), s, &why, cache->lens, cache->capacity, opt)
             : launch_attn_prefill_tc(ws.q, ws.k, ws.v, o_buf, B, d.n_heads, d.n_kv_heads, T, d.head_dim, true, f16,
-                                     h->status, (unsigned long long)g_wait_ns.load(), s, &why);
+                                     h->status, (unsigned long long)g_wait_ns.load(), s, &why, nullptr, 0, opt);
   BLK_TRY(check_cuda(e, "attention", why));
-  if (f16 && taps && taps->attention_head_outputs)
-    BLK_TRY(check_cuda(launch_cast_f16_bf16(o_buf, taps->attention_head_outputs,
-                                            (size_t)M * d.n_heads * d.head_dim, s),
+  if (f16 && head_tap && !gated)
+    BLK_TRY(check_cuda(launch_cast_f16_bf16(o_buf, head_tap, (size_t)M * d.n_heads * d.head_dim, s),
                        "head-output tap"));
+  const int Hd = d.n_heads * d.head_dim;
+  if (sandwich) {
+    prof_mark(h, "o_proj_gemm", 1, s);
+    BLK_TRY(bf16_linear_resid(h, o_buf, M, Hd, f16 ? prep.wo : w->wo, d.hidden, nullptr, false, ws.C, true, nullptr,
+                              nullptr, s, "o_proj GEMM", nullptr, nullptr, nullptr, f16));
+    prof_mark(h, "post_attn_norm_resid_norm2", 1, s);
+    BLK_TRY(check_cuda(launch_post_resid(static_cast<float*>(ws.C), 1, M, d.hidden, d.hidden, x, false, ws.mid, true,
+                                         mid_tap, taps ? taps->attention_output : nullptr, w->ln2_g, d.eps, ws.y,
+                                         nullptr, true, s, w->post_attn_g, f16),
+                       "post-attention norm"));
+    prof_mark(h, "mlp_up_gemm_act", 1, s);
+    BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s, nullptr, 0, f16 ? &prep : nullptr));
+    prof_mark(h, "down_gemm", 1, s);
+    BLK_TRY(bf16_linear_resid(h, neur, M, d.ffn, w->w_down, d.hidden, nullptr, false, ws.C, true, nullptr, nullptr, s,
+                              "down GEMM", nullptr, nullptr, nullptr, false, cache ? cache->lens : nullptr, T));
+    prof_mark(h, "post_mlp_norm_resid", 1, s);
+    BLK_TRY(check_cuda(launch_post_resid(static_cast<float*>(ws.C), 1, M, d.hidden, d.hidden, ws.mid, true, out,
+                                         false, nullptr, taps ? taps->mlp_output : nullptr, nullptr, d.eps, nullptr,
+                                         nullptr, true, s, w->post_mlp_g),
+                       "post-MLP norm"));
+    prof_end(h, s);
+    return BLK_OK;
+  }
   prof_mark(h, "o_proj_gemm_resid_norm2", 1, s);
-  BLK_TRY(bf16_linear_resid(h, o_buf, M, d.n_heads * d.head_dim, f16 ? prep.wo : w->wo, d.hidden, x, false, ws.mid,
-                            true, mid_tap, taps ? taps->attention_output : nullptr, s, "o_proj GEMM", ws.y, w->ln2_g,
-                            ws.ss2, f16));
+  BLK_TRY(bf16_linear_resid(h, o_buf, M, Hd, f16 ? prep.wo : w->wo, d.hidden, x, false, ws.mid, true, mid_tap,
+                            taps ? taps->attention_output : nullptr, s, "o_proj GEMM", ws.y, w->ln2_g, ws.ss2, f16));
   prof_mark(h, "mlp_up_gemm_act", 1, s);
   BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s, ws.ss2, norm_parts(d.hidden, resid_bn(h, M, d.hidden)),
                       f16 ? &prep : nullptr));
@@ -498,23 +553,35 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
   const int Hd = d.n_heads * d.head_dim, KVd = d.n_kv_heads * d.head_dim;
   const int parts = norm_parts(d.hidden, 128);
   float* C = static_cast<float*>(ws.C);
+  const bool gated = d.attn_gate != 0, sandwich = d.sandwich_norm != 0;
+  // prepared (fp16) weights: the normed rows, the attention output and the MLP's input are fp16 operands
+  Prepared prep{};
+  const bool f16 = w->prepared != nullptr;
+  if (f16) prepared_layout(d, w->prepared, &prep);
   void* q = tap_or(taps, &blk_taps::attention_queries, ws.q);
-  void* o = tap_or(taps, &blk_taps::attention_head_outputs, ws.o);
+  void* head_tap = taps ? taps->attention_head_outputs : nullptr;
+  void* o = (head_tap && !gated && !f16) ? head_tap : ws.o;
   void* mid_tap = taps ? taps->layer_mid : nullptr;
   void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
   // QKV, o_proj and down finish their tiles inside the GEMM when every unit fits
   // on the SMs at once; otherwise (and for the MLP-up GEMM, whose tiles outnumber
-  // the SMs) a post kernel sums the split partials.
+  // the SMs) a post kernel sums the split partials. A sandwich post-norm needs the
+  // whole row, so o_proj and down then always take the post kernel.
   const int hid_tiles = (d.hidden + 127) / 128;
   const int s_qkv = dec_fused_splits(h, dec_tiles_qkv(d), (d.hidden + 63) / 64, B, Epi::kDecQkv);
-  const int s_o = dec_fused_splits(h, hid_tiles, (Hd + 63) / 64, B, Epi::kDecResid);
-  const int s_down = dec_fused_splits(h, hid_tiles, (d.ffn + 63) / 64, B, Epi::kDecResid);
+  const int s_o = sandwich ? 0 : dec_fused_splits(h, hid_tiles, (Hd + 63) / 64, B, Epi::kDecResid);
+  const int s_down = sandwich ? 0 : dec_fused_splits(h, hid_tiles, (d.ffn + 63) / 64, B, Epi::kDecResid);
+  void* gate = gated ? ws.gate : nullptr;
   int sp = 1;
   prof_mark(h, "rmsnorm1", 1, s);
-  BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, B, d.hidden, d.eps, ws.y, bf, s), "rmsnorm 1"));
+  BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, B, d.hidden, d.eps, ws.y, bf, s, false, f16), "rmsnorm 1"));
   prof_mark(h, "qkv_gemm_rope_append", s_qkv ? 1 : 2, s);
   {
-    const TcSeg segs[3] = {{w->wq, Hd, 0}, {w->wk, KVd, Hd}, {w->wv, KVd, Hd + KVd}};
+    const TcSeg segs[4] = {{f16 ? prep.wq : w->wq, Hd, 0},
+                           {f16 ? prep.wk : w->wk, KVd, Hd},
+                           {f16 ? prep.wv : w->wv, KVd, Hd + KVd},
+                           {f16 ? prep.wag : w->w_attn_gate, Hd, Hd + 2 * KVd}};
+    const int nseg = gated ? 4 : 3;
     if (s_qkv) {
       TcEpiArgs e;
       e.q = q;
@@ -531,25 +598,31 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
       e.rope_max_pos = d.max_seq;
       e.qk_norm = d.qk_norm;
       e.lens = cache->lens;
-      BLK_TRY(dec_gemm(h, segs, 3, ws.y, B, d.hidden, s_qkv, Epi::kDecQkv, e, s, "decode QKV GEMM"));
+      e.gate = gate;
+      BLK_TRY(dec_gemm(h, segs, nseg, ws.y, B, d.hidden, s_qkv, Epi::kDecQkv, e, s, "decode QKV GEMM", f16));
     } else {
-      BLK_TRY(bf16_stream_gemm(h, segs, 3, ws.y, B, d.hidden, C, qkv_cols(d), &sp, s, "decode QKV GEMM"));
+      BLK_TRY(bf16_stream_gemm(h, segs, nseg, ws.y, B, d.hidden, C, qkv_cols(d), &sp, s, "decode QKV GEMM", f16));
       BLK_TRY(check_cuda(launch_post_qkv(C, sp, B, qkv_cols(d), 1, nullptr, cache->lens, d.n_heads, d.n_kv_heads,
                                          d.head_dim, d.qk_norm, w->q_norm_g, w->k_norm_g, d.eps, h->rope,
-                                         d.max_seq, q, cache->k, cache->v, cache->capacity, bf, s),
+                                         d.max_seq, q, cache->k, cache->v, cache->capacity, bf, s, gate),
                          "decode qkv post"));
     }
   }
   prof_mark(h, "attention_splitkv", 2, s);
   const char* why = nullptr;
+  AttnOpts opt;
+  opt.window = d.sliding_window;
+  opt.gate = gate;
+  opt.ungated = (gated || f16) ? head_tap : nullptr;  // the tap: bf16, before the gate
+  opt.o_f16 = f16;
   cudaError_t ce = launch_attn_decode_bf16(q, cache->k, cache->v, o, B, d.n_heads, d.n_kv_heads, d.head_dim,
                                            cache->capacity, cache->lens, 1, max_len,
                                            attn_decode_splits(B, d.n_kv_heads, d.max_seq, h->num_sms), ws.attn,
-                                           h->num_sms, h->status, (unsigned long long)g_wait_ns.load(), s, &why);
+                                           h->num_sms, h->status, (unsigned long long)g_wait_ns.load(), s, &why, opt);
   BLK_TRY(check_cuda(ce, "decode attention", why));
   prof_mark(h, "o_proj_gemm_resid_norm2", s_o ? 1 : 2, s);
   {
-    const TcSeg segs[1] = {{w->wo, d.hidden, 0}};
+    const TcSeg segs[1] = {{f16 ? prep.wo : w->wo, d.hidden, 0}};
     if (s_o) {
       // mid = x + o Wo^T (fp32), and the post-attention RMSNorm split: ws.y = mid * g2,
       // ws.ss2 = per-tile sums of squares (the activation kernel applies 1/rms)
@@ -564,22 +637,23 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
       e.norm_gain = w->ln2_g;
       e.norm_ss = ws.ss2;
       e.norm_parts = parts;
-      BLK_TRY(dec_gemm(h, segs, 1, o, B, Hd, s_o, Epi::kDecResid, e, s, "decode o_proj GEMM"));
+      e.norm_f16 = f16 ? 1 : 0;
+      BLK_TRY(dec_gemm(h, segs, 1, o, B, Hd, s_o, Epi::kDecResid, e, s, "decode o_proj GEMM", f16));
     } else {
-      BLK_TRY(bf16_stream_gemm(h, segs, 1, o, B, Hd, C, d.hidden, &sp, s, "decode o_proj GEMM"));
+      BLK_TRY(bf16_stream_gemm(h, segs, 1, o, B, Hd, C, d.hidden, &sp, s, "decode o_proj GEMM", f16));
       BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, x, false, ws.mid, true, mid_tap,
                                            taps ? taps->attention_output : nullptr, w->ln2_g, d.eps, ws.y, nullptr,
-                                           bf, s),
+                                           bf, s, sandwich ? w->post_attn_g : nullptr, f16),
                          "decode o_proj post"));
     }
   }
   prof_mark(h, "mlp_up_gemm", 1, s);
   if (d.act == BLK_ACT_SWIGLU) {
-    const TcSeg segs[2] = {{w->w_gate, d.ffn, 0}, {w->w_up, d.ffn, d.ffn}};
-    BLK_TRY(bf16_stream_gemm(h, segs, 2, ws.y, B, d.hidden, C, 2 * d.ffn, &sp, s, "decode gate/up GEMM"));
+    const TcSeg segs[2] = {{f16 ? prep.wg : w->w_gate, d.ffn, 0}, {f16 ? prep.wu : w->w_up, d.ffn, d.ffn}};
+    BLK_TRY(bf16_stream_gemm(h, segs, 2, ws.y, B, d.hidden, C, 2 * d.ffn, &sp, s, "decode gate/up GEMM", f16));
   } else {
-    const TcSeg segs[1] = {{w->w_up, d.ffn, 0}};
-    BLK_TRY(bf16_stream_gemm(h, segs, 1, ws.y, B, d.hidden, C, d.ffn, &sp, s, "decode up GEMM"));
+    const TcSeg segs[1] = {{f16 ? prep.wu : w->w_up, d.ffn, 0}};
+    BLK_TRY(bf16_stream_gemm(h, segs, 1, ws.y, B, d.hidden, C, d.ffn, &sp, s, "decode up GEMM", f16));
   }
   prof_mark(h, "mlp_act", 1, s);
   BLK_TRY(check_cuda(launch_post_act(C, sp, B, d.ffn, mlp_cols(d), (int)d.act, d.xielu_alpha_p, d.xielu_alpha_n,
@@ -601,8 +675,8 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
     } else {
       BLK_TRY(bf16_stream_gemm(h, segs, 1, neur, B, d.ffn, C, d.hidden, &sp, s, "decode down GEMM"));
       BLK_TRY(check_cuda(launch_post_resid(C, sp, B, d.hidden, d.hidden, ws.mid, true, out, false, nullptr,
-                                           taps ? taps->mlp_output : nullptr, nullptr, 0.f, nullptr, cache->lens,
-                                           bf, s),
+                                           taps ? taps->mlp_output : nullptr, nullptr, d.eps, nullptr, cache->lens,
+                                           bf, s, sandwich ? w->post_mlp_g : nullptr),
                          "decode down post"));
     }
   }
@@ -623,28 +697,38 @@ blk_status forward_f32(blk_handle* h, const void* x, int B, int T, const blk_wei
   void* k = decode ? cache->k : tap_or(taps, &blk_taps::attention_keys, ws.k);
   void* v = decode ? cache->v : tap_or(taps, &blk_taps::attention_values, ws.v);
   const int kv_stride = decode ? cache->capacity : T;
-  void* o = tap_or(taps, &blk_taps::attention_head_outputs, ws.o);
+  const bool gated = d.attn_gate != 0, sandwich = d.sandwich_norm != 0;
+  void* head_tap = taps ? taps->attention_head_outputs : nullptr;
+  void* o = (head_tap && !gated) ? head_tap : ws.o;
   void* mid = tap_or(taps, &blk_taps::layer_mid, ws.mid);
   void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
   const float* y = static_cast<const float*>(ws.y);
-  prof_mark(h, "fp32_block", d.act == BLK_ACT_SWIGLU ? 13 : 12, s);
+  prof_mark(h, "fp32_block", (d.act == BLK_ACT_SWIGLU ? 13 : 12) + (gated ? 1 : 0), s);
   BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, M, d.hidden, d.eps, ws.y, bf, s), "rmsnorm 1"));
   const int nq = qkv_cols(d);
   BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->wq, C, nq, M, Hd, d.hidden, s), "q GEMM"));
   BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->wk, C + Hd, nq, M, KVd, d.hidden, s), "k GEMM"));
   BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->wv, C + Hd + KVd, nq, M, KVd, d.hidden, s), "v GEMM"));
+  if (gated)
+    BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->w_attn_gate, C + Hd + 2 * KVd, nq, M, Hd, d.hidden, s),
+                       "attention gate GEMM"));
   BLK_TRY(check_cuda(launch_post_qkv(C, 1, M, nq, T, nullptr, decode ? cache->lens : nullptr, d.n_heads,
                                      d.n_kv_heads, d.head_dim, d.qk_norm, w->q_norm_g, w->k_norm_g, d.eps, h->rope,
-                                     d.max_seq, q, k, v, kv_stride, bf, s),
+                                     d.max_seq, q, k, v, kv_stride, bf, s, gated ? ws.gate : nullptr),
                      "qkv post"));
+  AttnOpts opt;
+  opt.window = d.sliding_window;
+  opt.gate = gated ? ws.gate : nullptr;
+  opt.ungated = gated ? head_tap : nullptr;
   BLK_TRY(check_cuda(launch_attn_f32((const float*)q, (const float*)k, (const float*)v, (float*)o, B, d.n_heads,
                                      d.n_kv_heads, T, d.head_dim, kv_stride, decode ? cache->lens : nullptr,
-                                     decode ? 1 : 0, s),
+                                     decode ? 1 : 0, s, opt),
                      "attention"));
   BLK_TRY(check_cuda(launch_gemm_f32((const float*)o, (const float*)w->wo, C, d.hidden, M, d.hidden, Hd, s),
                      "o_proj GEMM"));
   BLK_TRY(check_cuda(launch_post_resid(C, 1, M, d.hidden, d.hidden, x, true, mid, true, nullptr,
-                                       taps ? taps->attention_output : nullptr, w->ln2_g, d.eps, ws.y, nullptr, bf, s),
+                                       taps ? taps->attention_output : nullptr, w->ln2_g, d.eps, ws.y, nullptr, bf, s,
+                                       sandwich ? w->post_attn_g : nullptr),
                      "o_proj post"));
   const int nm = mlp_cols(d);
   if (d.act == BLK_ACT_SWIGLU) {
@@ -659,8 +743,8 @@ blk_status forward_f32(blk_handle* h, const void* x, int B, int T, const blk_wei
   BLK_TRY(check_cuda(launch_gemm_f32((const float*)neur, (const float*)w->w_down, C, d.hidden, M, d.hidden, d.ffn, s),
                      "down GEMM"));
   BLK_TRY(check_cuda(launch_post_resid(C, 1, M, d.hidden, d.hidden, mid, true, out, true, nullptr,
-                                       taps ? taps->mlp_output : nullptr, nullptr, 0.f, nullptr,
-                                       decode ? cache->lens : nullptr, bf, s),
+                                       taps ? taps->mlp_output : nullptr, nullptr, d.eps, nullptr,
+                                       decode ? cache->lens : nullptr, bf, s, sandwich ? w->post_mlp_g : nullptr),
                      "down post"));
   prof_end(h, s);
   return BLK_OK;
@@ -679,6 +763,10 @@ blk_status check_weights(const blk_desc& d, const blk_weights* w) {
     return fail(BLK_ERR_INVALID_ARG, "qk_norm needs aligned q_norm_g and k_norm_g");
   if (w->prepared && (d.dtype != BLK_BF16 || !aligned16(w->prepared)))
     return fail(BLK_ERR_INVALID_ARG, "prepared weights: bf16 handles only, 16-byte aligned");
+  if (d.attn_gate && (!w->w_attn_gate || !aligned16(w->w_attn_gate)))
+    return fail(w->w_attn_gate ? BLK_ERR_ALIGNMENT : BLK_ERR_INVALID_ARG, "attn_gate needs an aligned w_attn_gate");
+  if (d.sandwich_norm && (!w->post_attn_g || !w->post_mlp_g || !aligned16(w->post_attn_g) || !aligned16(w->post_mlp_g)))
+    return fail(BLK_ERR_INVALID_ARG, "sandwich_norm needs aligned post_attn_g and post_mlp_g");
   return BLK_OK;
 }
 
@@ -732,6 +820,10 @@ blk_status blk_create(const blk_desc* desc, blk_handle** out) {
   }
   if (d.act != BLK_ACT_SWIGLU && d.act != BLK_ACT_RELU2 && d.act != BLK_ACT_XIELU)
     return fail(BLK_ERR_INVALID_ARG, "unknown activation");
+  if (d.sliding_window < 0) return fail(BLK_ERR_INVALID_ARG, "sliding_window must be >= 0");
+  if ((d.no_rope | d.attn_gate | d.sandwich_norm) & ~1)
+    return fail(BLK_ERR_INVALID_ARG, "no_rope, attn_gate and sandwich_norm are 0 or 1");
+  if (d.no_rope && d.rope_type != BLK_ROPE_PLAIN) return fail(BLK_ERR_INVALID_ARG, "no_rope with a rope scaling");
   if (d.dtype != BLK_F32 && d.dtype != BLK_BF16) return fail(BLK_ERR_INVALID_ARG, "unknown dtype");
   if (d.dtype == BLK_BF16) {
     if (d.head_dim != 128) return fail(BLK_ERR_UNSUPPORTED, "bf16 path: head_dim must be 128");
@@ -779,7 +871,7 @@ blk_status blk_create(const blk_desc* desc, blk_handle** out) {
       const double g = std::min(1.0, std::max(0.0, (turns - lo) / (hi - lo)));
       fi = (1.0 - g) * f / s_f + g * f;
     }
-    inv_freq[i] = fi;
+    inv_freq[i] = d.no_rope ? 0.0 : fi;  // no rotary: every angle 0, the identity rotation
   }
   const double att = d.rope_type == BLK_ROPE_YARN ? 0.1 * std::log(s_f) + 1.0 : 1.0;  // YaRN's sqrt(1/t)
   std::vector<float2> table((size_t)d.max_seq * half);
@@ -823,8 +915,9 @@ blk_status blk_prepare_weights(blk_handle* h, const blk_weights* w, void* prepar
   if (!h || !w || !prepared) return fail(BLK_ERR_INVALID_ARG, "NULL argument");
   const blk_desc& d = h->d;
   if (d.dtype != BLK_BF16) return fail(BLK_ERR_UNSUPPORTED, "prepared weights exist for the bf16 path only");
-  if (!w->wo || !w->w_up || (d.act == BLK_ACT_SWIGLU && !w->w_gate))
-    return fail(BLK_ERR_INVALID_ARG, "wo / w_up / w_gate NULL");
+  if (!w->wo || !w->w_up || (d.act == BLK_ACT_SWIGLU && !w->w_gate) || !w->wq || !w->wk || !w->wv || !w->ln1_g ||
+      !w->ln2_g || (d.attn_gate && !w->w_attn_gate))
+    return fail(BLK_ERR_INVALID_ARG, "a weight to prepare is NULL");
   if (!aligned16(prepared)) return fail(BLK_ERR_ALIGNMENT, "prepared buffer not 16-byte aligned");
   if (bytes < blk_prepared_bytes(h)) return fail(BLK_ERR_WORKSPACE, "prepared buffer too small");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -836,6 +929,32 @@ blk_status blk_prepare_weights(blk_handle* h, const blk_weights* w, void* prepar
   if (p.wg)
     BLK_TRY(check_cuda(launch_cast_bf16_f16(w->w_gate, const_cast<void*>(p.wg), n_f, h->dev_flag, s), "prepare w_gate"));
   BLK_TRY(check_cuda(launch_cast_bf16_f16(w->w_up, const_cast<void*>(p.wu), n_f, h->dev_flag, s), "prepare w_up"));
+  const size_t n_q = (size_t)d.n_heads * d.head_dim * d.hidden, n_kv = (size_t)d.n_kv_heads * d.head_dim * d.hidden;
+  BLK_TRY(check_cuda(launch_cast_bf16_f16(w->wq, const_cast<void*>(p.wq), n_q, h->dev_flag, s), "prepare wq"));
+  BLK_TRY(check_cuda(launch_cast_bf16_f16(w->wk, const_cast<void*>(p.wk), n_kv, h->dev_flag, s), "prepare wk"));
+  BLK_TRY(check_cuda(launch_cast_bf16_f16(w->wv, const_cast<void*>(p.wv), n_kv, h->dev_flag, s), "prepare wv"));
+  if (p.wag)
+    BLK_TRY(check_cuda(launch_cast_bf16_f16(w->w_attn_gate, const_cast<void*>(p.wag), n_q, h->dev_flag, s),
+                       "prepare w_attn_gate"));
+  // A normed row has |x_i| / rms(x) <= sqrt(D), so its fp16 copy (x / rms * g) stays finite when
+  // max|g| * sqrt(D) <= 65504: checked for the norms whose fp16 output is normalized first
+  // (input_layernorm, and the MLP's input norm of the sandwich block).
+  std::vector<uint16_t> gains((size_t)d.hidden);
+  const void* checked[2] = {w->ln1_g, d.sandwich_norm ? w->ln2_g : nullptr};
+  for (const void* gp : checked) {
+    if (!gp) continue;
+    BLK_TRY(check_cuda(cudaMemcpyAsync(gains.data(), gp, gains.size() * 2, cudaMemcpyDeviceToHost, s), "prepare"));
+    BLK_TRY(check_cuda(cudaStreamSynchronize(s), "prepare"));
+    float gmax = 0.f;
+    for (uint16_t u : gains) {
+      uint32_t bits = (uint32_t)u << 16;
+      float f;
+      std::memcpy(&f, &bits, 4);
+      gmax = std::max(gmax, std::fabs(f));
+    }
+    if (!(gmax * std::sqrt((float)d.hidden) <= 65504.f))
+      return fail(BLK_ERR_UNSUPPORTED, "a norm gain is too large for fp16 normed rows: use the weights unprepared");
+  }
   int overflow = 0;
   BLK_TRY(check_cuda(cudaMemcpyAsync(&overflow, h->dev_flag, sizeof(int), cudaMemcpyDeviceToHost, s), "prepare"));
   BLK_TRY(check_cuda(cudaStreamSynchronize(s), "prepare"));
@@ -1086,16 +1205,19 @@ blk_status blk_attn_gqa(blk_handle* h, const void* q, const void* k, const void*
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return fail(BLK_ERR_ALIGNMENT, "alignment");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const char* why = nullptr;
+  AttnOpts opt;
+  opt.window = d.sliding_window;  // the head outputs: before any attention gate
   if (d.dtype == BLK_F32) {
     if ((size_t)kv_stride * 4 > 200 * 1024) return fail(BLK_ERR_UNSUPPORTED, "fp32 attention: kv_stride too large");
     return check_cuda(launch_attn_f32((const float*)q, (const float*)k, (const float*)v, (float*)o, batch, d.n_heads,
-                                      d.n_kv_heads, seq_q, d.head_dim, kv_stride, kv_lens, 0, s),
+                                      d.n_kv_heads, seq_q, d.head_dim, kv_stride, kv_lens, 0, s, opt),
                       "attention");
   }
   if (!kv_lens) {
     if (kv_stride != seq_q) return fail(BLK_ERR_UNSUPPORTED, "bf16 prefill attention: kv_stride must equal seq_q");
     return check_cuda(launch_attn_prefill_tc(q, k, v, o, batch, d.n_heads, d.n_kv_heads, seq_q, d.head_dim,
-                                             false, false, h->status, (unsigned long long)g_wait_ns.load(), s, &why),
+                                             false, false, h->status, (unsigned long long)g_wait_ns.load(), s, &why,
+                                             nullptr, 0, opt),
                       "attention", why);
   }
   if (seq_q != 1) return fail(BLK_ERR_UNSUPPORTED, "bf16 attention over a cache: one query per sequence");
@@ -1106,7 +1228,8 @@ blk_status blk_attn_gqa(blk_handle* h, const void* q, const void* k, const void*
   void* aw = c.take(0);
   return check_cuda(launch_attn_decode_bf16(q, k, v, o, batch, d.n_heads, d.n_kv_heads, d.head_dim, kv_stride, kv_lens,
                                             0, kv_stride, attn_decode_splits(batch, d.n_kv_heads, d.max_seq, h->num_sms),
-                                            aw, h->num_sms, h->status, (unsigned long long)g_wait_ns.load(), s, &why),
+                                            aw, h->num_sms, h->status, (unsigned long long)g_wait_ns.load(), s, &why,
+                                            opt),
                     "decode attention", why);
 }
 
@@ -1123,10 +1246,19 @@ blk_status blk_mlp(blk_handle* h, const void* resid, const void* h_normed, const
   Carve c(workspace);
   void* neur = c.take((size_t)rows * d.ffn * esize(d));
   float* C = static_cast<float*>(c.take((size_t)rows * max_cols(d) * sizeof(float)));
+  if (d.sandwich_norm && (!w->post_mlp_g || !aligned16(w->post_mlp_g)))
+    return fail(BLK_ERR_INVALID_ARG, "sandwich_norm needs an aligned post_mlp_g");
+  const void* g_post = d.sandwich_norm ? w->post_mlp_g : nullptr;
   if (d.dtype == BLK_BF16) {
     BLK_TRY(bf16_mlp_up(h, h_normed, rows, w, neur, s));
-    return bf16_linear_resid(h, neur, rows, d.ffn, w->w_down, d.hidden, resid, false, out, false, nullptr, nullptr, s,
-                             "down GEMM");
+    if (!g_post)
+      return bf16_linear_resid(h, neur, rows, d.ffn, w->w_down, d.hidden, resid, false, out, false, nullptr, nullptr,
+                               s, "down GEMM");
+    BLK_TRY(bf16_linear_resid(h, neur, rows, d.ffn, w->w_down, d.hidden, nullptr, false, C, true, nullptr, nullptr, s,
+                              "down GEMM"));
+    return check_cuda(launch_post_resid(C, 1, rows, d.hidden, d.hidden, resid, false, out, false, nullptr, nullptr,
+                                        nullptr, d.eps, nullptr, nullptr, true, s, g_post),
+                      "post-MLP norm");
   }
   const float* y = static_cast<const float*>(h_normed);
   const int nm = mlp_cols(d);
@@ -1142,7 +1274,7 @@ blk_status blk_mlp(blk_handle* h, const void* resid, const void* h_normed, const
   BLK_TRY(check_cuda(launch_gemm_f32((const float*)neur, (const float*)w->w_down, C, d.hidden, rows, d.hidden, d.ffn, s),
                      "down GEMM"));
   return check_cuda(launch_post_resid(C, 1, rows, d.hidden, d.hidden, resid, true, out, true, nullptr, nullptr,
-                                      nullptr, 0.f, nullptr, nullptr, false, s),
+                                      nullptr, d.eps, nullptr, nullptr, false, s, g_post),
                     "down post");
 }
 

@@ -66,6 +66,9 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
 
 // ---------------------------------------------------------------- warp reductions
 
+// 1 / (1 + e^-g): the attention gate of "afmoe" (0 at g = -inf, 1 at +inf).
+__device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + __expf(-g)); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

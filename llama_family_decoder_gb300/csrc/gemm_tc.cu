@@ -82,14 +82,14 @@ __host__ __device__ constexpr bool tc_supported() {
 }
 
 struct TcParams {
-  CUtensorMap ta[3];
-  CUtensorMap tb[3];
-  int a_tiles[4];  // prefix sums of m-tiles per A segment
-  int a_rows[3];
-  int a_out[3];
-  int b_tiles[4];  // prefix sums of n-tiles per B segment
-  int b_rows[3];
-  int b_out[3];
+  CUtensorMap ta[kMaxSegs];
+  CUtensorMap tb[kMaxSegs];
+  int a_tiles[kMaxSegs + 1];  // prefix sums of m-tiles per A segment
+  int a_rows[kMaxSegs];
+  int a_out[kMaxSegs];
+  int b_tiles[kMaxSegs + 1];  // prefix sums of n-tiles per B segment
+  int b_rows[kMaxSegs];
+  int b_out[kMaxSegs];
   int na, nb;
   int b_paired;
   int f16;  // fp16 operands (else bf16)
@@ -255,6 +255,28 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
       for (int hh = 0; hh < BN / 128; ++hh) {
         const int head = (un.b_row0 >> 7) + hh;
         const uint32_t tcol = taddr + hh * 128;
+        if (seg == 3) {
+          // the attention gate ("afmoe": one value per channel of every head): sigmoid, fp16,
+          // in the attention output's layout [row][head][d]
+          uint16_t* gd = reinterpret_cast<uint16_t*>(e.gate) + ((size_t)row * e.n_heads + head) * d;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            float v0[16], v1[16];
+            tmem_ld16(tcol + c0, v0);
+            tmem_ld16(tcol + c0 + 16, v1);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              v0[j] = sigmoid_f(v0[j] * rs);
+              v1[j] = sigmoid_f(v1[j] * rs);
+            }
+            if (row_ok) {
+              store16_2b(gd + c0, v0, true);
+              store16_2b(gd + c0 + 16, v1, true);
+            }
+          }
+          continue;
+        }
         uint16_t* dst;  // 2-byte elements (bf16 or fp16)
         if (seg == 0)
           dst = reinterpret_cast<uint16_t*>(e.q) + (((size_t)b * e.n_heads + head) * e.seq + t) * d;
@@ -352,7 +374,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
       __nv_bfloat16* tap = nullptr;
       float r2 = 1.0f, ss_part = 0.f;
       if constexpr (EPI == (int)Epi::kResid) {
-        res = reinterpret_cast<const __nv_bfloat16*>(e.resid) + (size_t)row * e.ldo + col0;
+        if (e.resid) res = reinterpret_cast<const __nv_bfloat16*>(e.resid) + (size_t)row * e.ldo + col0;
         if (e.tap) tap = reinterpret_cast<__nv_bfloat16*>(e.tap) + (size_t)row * e.ldo + col0;
       } else if constexpr (EPI == (int)Epi::kRelu2 || EPI == (int)Epi::kXielu) {
         r2 = row_norm_factor(e, row, row_ok);  // the post-attention RMSNorm's 1/rms
@@ -386,7 +408,10 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
           } else if constexpr (EPI == (int)Epi::kResid) {
             // residual stream carried in fp32: out = resid + acc, rounded once
             float rr[16];
-            if (e.resid_f32) {
+            if (!e.resid) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) rr[j] = 0.f;
+            } else if (e.resid_f32) {
               const float* rf = reinterpret_cast<const float*>(e.resid) + (size_t)row * e.ldo + col0 + cc;
               if (nv == 16) {
 #pragma unroll
@@ -548,7 +573,7 @@ __device__ __forceinline__ void dec_token_inputs(const TcParams& p, const Unit& 
   const TcEpiArgs& e = p.e;
   if constexpr (EPI == (int)Epi::kDecQkv) {
     pos = e.lens[tok0 + tl];
-    if (un.a_seg != 2) {
+    if (un.a_seg < 2) {  // q and k take the rotary; v and the attention gate do not
       const int rpos = min(max(pos, 0), e.rope_max_pos - 1);
       const float4* cs4 = reinterpret_cast<const float4*>(e.rope + (size_t)rpos * 64 + 4 * (lane & 15));
       a = cs4[0];
@@ -576,7 +601,7 @@ __device__ __forceinline__ void dec_load_side(const TcParams& p, const Unit& un,
   const DecSlice sl = dec_slice(p, un, BN);
   sd.gain = make_float4(1.f, 1.f, 1.f, 1.f);
   if constexpr (EPI == (int)Epi::kDecQkv) {
-    if (un.a_seg != 2 && e.qk_norm)
+    if (un.a_seg < 2 && e.qk_norm)
       sd.gain = ld_bf16x4(reinterpret_cast<const __nv_bfloat16*>(un.a_seg == 0 ? e.q_gain : e.k_gain) + 4 * lane);
   } else {
     const int f = un.m_tile * kBM + 4 * lane;
@@ -596,7 +621,7 @@ __device__ __forceinline__ void dec_finish(const TcParams& p, const Unit& un, in
   const int S = p.k_splits;
   const DecSlice sl = dec_slice(p, un, BN);
   const int lo = sl.lo, hi = sl.hi, tok0 = sl.tok0;
-  const bool rope = qkv && un.a_seg != 2;
+  const bool rope = qkv && un.a_seg < 2;
   const int f0 = un.m_tile * kBM;                     // kDecResid: first feature of the tile
   const bool fok = qkv || f0 + 4 * lane < e.ldo;      // kDecResid: this lane's features exist
   const uint32_t stage_s = smem_u32(stage) + 16 * lane;
@@ -636,8 +661,16 @@ __device__ __forceinline__ void dec_finish(const TcParams& p, const Unit& un, in
       float* vv = v[k];
       if constexpr (qkv) {
         // one head (head_dim 128) per tile; token t is sequence t, at position lens[t]
-        const int seg = un.a_seg;  // 0: q, 1: k, 2: v
+        const int seg = un.a_seg;  // 0: q, 1: k, 2: v, 3: the attention gate
         const int head = un.a_row0 >> 7;
+        if (seg == 3) {
+          const float g0 = sigmoid_f(vv[0]), g1 = sigmoid_f(vv[1]), g2 = sigmoid_f(vv[2]), g3 = sigmoid_f(vv[3]);
+          const __half2 h01 = __floats2half2_rn(g0, g1), h23 = __floats2half2_rn(g2, g3);
+          *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(e.gate) + ((size_t)t * e.n_heads + head) * 128 +
+                                    4 * lane) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+          continue;
+        }
         const bool write = seg == 0 || (pos[k] >= 0 && pos[k] < e.kv_stride);  // never past a full cache
         if (rope) {
           if (e.qk_norm) {
@@ -677,9 +710,17 @@ __device__ __forceinline__ void dec_finish(const TcParams& p, const Unit& un, in
           if (e.out2) st_bf16x4(reinterpret_cast<__nv_bfloat16*>(e.out2) + i, o0, o1, o2, o3);
           if (e.tap) st_bf16x4(reinterpret_cast<__nv_bfloat16*>(e.tap) + i, vv[0], vv[1], vv[2], vv[3]);
           // next RMSNorm, split: out * g here (the MLP GEMM's B), 1/rms from the tiles' sums of squares later
-          if (e.norm_out)
-            st_bf16x4(reinterpret_cast<__nv_bfloat16*>(e.norm_out) + i, o0 * gain.x, o1 * gain.y, o2 * gain.z,
-                      o3 * gain.w);
+          if (e.norm_out) {
+            if (e.norm_f16) {  // the operand of an MLP GEMM on prepared fp16 weights
+              const __half2 h01 = __floats2half2_rn(o0 * gain.x, o1 * gain.y);
+              const __half2 h23 = __floats2half2_rn(o2 * gain.z, o3 * gain.w);
+              *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(e.norm_out) + i) =
+                  make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+            } else {
+              st_bf16x4(reinterpret_cast<__nv_bfloat16*>(e.norm_out) + i, o0 * gain.x, o1 * gain.y, o2 * gain.z,
+                        o3 * gain.w);
+            }
+          }
         }
         if (e.norm_ss) {
           const float ss = warp_sum(fok ? o0 * o0 + o1 * o1 + o2 * o2 + o3 * o3 : 0.f);
@@ -1109,7 +1150,7 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
     *why = "tcgen05 GEMM: K must be a positive multiple of 8 (16-byte rows)";
     return cudaErrorInvalidValue;
   }
-  if (d.na < 1 || d.na > 3 || d.nb < 1 || d.nb > 3 || (d.b_paired && d.nb != 2)) {
+  if (d.na < 1 || d.na > kMaxSegs || d.nb < 1 || d.nb > kMaxSegs || (d.b_paired && d.nb != 2)) {
     *why = "tcgen05 GEMM: bad segment count";
     return cudaErrorInvalidValue;
   }

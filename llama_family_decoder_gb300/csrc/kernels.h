@@ -14,8 +14,9 @@ struct DevStatus;
 // ---------------------------------------------------------------- RMSNorm
 // y[r,:] = x[r,:] * rsqrt(mean(x[r,:]^2) + eps) * g   (fp32 statistics)
 // x_f32: x is fp32 while g and y have the storage type (the bf16 path's fp32 residual stream).
+// y_f16 (bf16 path): y is fp16, the operand of a GEMM with prepared fp16 weights.
 cudaError_t launch_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y, bool bf16,
-                           cudaStream_t s, bool x_f32 = false);
+                           cudaStream_t s, bool x_f32 = false, bool y_f16 = false);
 
 // The input RMSNorm split for the fused bf16 prefill: row_scale[r] = rsqrt(mean(x[r]^2) + eps),
 // xg[r, :] = bf16(x[r, :] * g) (the QKV GEMM's A; x itself when g == 1); zeroes zero_rows[r].
@@ -43,7 +44,8 @@ cudaError_t launch_gemm_f32(const float* A, const float* B, float* C, int ldc, i
 enum class Epi : int {
   kStore = 0,     // out[row, col] = bf16(acc)
   kResid = 1,     // out = resid + acc (fp32 sum, stored fp32 or bf16); optional bf16 copy and tap = bf16(acc)
-  kQkv = 2,       // per-head optional RMSNorm, RoPE, scatter to q/k/v head-major layouts
+  kQkv = 2,       // per-head optional RMSNorm, RoPE, scatter to q/k/v head-major layouts;
+                  // a 4th B segment (the attention gate) stores sigmoid(acc) as fp16
   kSwiglu = 3,    // paired B halves [gate | up]: out = bf16(silu(gate) * up)
   kRelu2 = 4,     // out = bf16(relu(acc)^2)
   kXielu = 5,     // out = bf16(xielu(acc))
@@ -52,7 +54,8 @@ enum class Epi : int {
   // cluster: each split keeps its fp32 partial in shared memory, and CTA r of
   // the cluster sums slice r of the tile's tokens over all splits (distributed
   // shared memory, split order) and applies the post-op.
-  kDecQkv = 7,    // per-head q/k RMSNorm, RoPE at position lens[t], q store, K/V cache append
+  kDecQkv = 7,    // per-head q/k RMSNorm, RoPE at position lens[t], q store, K/V cache append,
+                  // a 4th A segment (the attention gate): sigmoid(acc) as fp16
   kDecResid = 8,  // resid + acc (fp32), optional taps, next RMSNorm (gained rows + sum of squares)
 };
 
@@ -70,7 +73,7 @@ struct TcSeg {
 struct TcEpiArgs {
   void* out = nullptr;  // kStore/kResid/activations: bf16 [rows, ldo]; kPartialT: float partial base
   int ldo = 0;
-  const void* resid = nullptr;  // kResid: [rows, ldo], bf16 or (resid_f32) fp32
+  const void* resid = nullptr;  // kResid: [rows, ldo], bf16 or (resid_f32) fp32; null: out = acc
   int resid_f32 = 0;
   int out_f32 = 0;              // kResid: out is fp32 (the block's residual stream)
   void* out2 = nullptr;         // kResid: optional bf16 copy of out
@@ -94,6 +97,7 @@ struct TcEpiArgs {
   int qk_norm = 0;
   const float* row_scale = nullptr;  // kQkv: per-row factor of the accumulator (the input norm's 1/rms)
   int qkv_f16 = 0;                   // kQkv: store q/k/v as fp16 (else bf16)
+  void* gate = nullptr;              // kQkv/kDecQkv: fp16 [rows, n_heads * head_dim], sigmoid of the gate segment
   // activations: per-row RMSNorm of the A rows from a sum of squares, 1/rms = rsqrt(row_ss / ss_n + ss_eps)
   // (row_ss holds ss_parts partial sums per row, summed in order)
   const float* row_ss = nullptr;
@@ -118,10 +122,12 @@ struct TcEpiArgs {
                               // kResid: lens[b] += seq once per sequence (its last row, first N tile)
 };
 
+constexpr int kMaxSegs = 4;
+
 struct TcGemmDesc {
-  TcSeg a[3];
+  TcSeg a[kMaxSegs];
   int na = 1;
-  TcSeg b[3];
+  TcSeg b[kMaxSegs];
   int nb = 1;
   bool b_paired = false;  // B tile = halves from b[0] and b[1] at the same rows (gate/up)
   bool f16 = false;       // A and B are fp16 (else bf16)
@@ -153,19 +159,24 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
 // optional per-head RMSNorm (q/k), RoPE at pos, write q[b,h,t_q,:] (Tq rows per
 // (b,h)) and k/v at slot `pos` of [b, j, kv_stride, d] (prefill: slot t).
 // decode_lens != null: decode mode (seq == 1, pos = decode_lens[b]).
+// gate != null: columns [(H+2Hkv)*d, (2H+2Hkv)*d) are the attention gate;
+// gate[r, :] = sigmoid(them), fp16 on the bf16 path, fp32 on the fp32 path.
 cudaError_t launch_post_qkv(const float* C, int splits, int rows, int ldc, int seq, const int* pos0,
                             const int* decode_lens, int H, int Hkv, int d, int qk_norm, const void* q_gain,
                             const void* k_gain, float eps, const float2* rope, int rope_max_pos, void* q, void* k,
-                            void* v, int kv_stride, bool bf16, cudaStream_t s);
+                            void* v, int kv_stride, bool bf16, cudaStream_t s, void* gate = nullptr);
 
-// out[r, c] = resid[r, c] + sum_s C[s, r, c] for c < n (fp32 sum, stored as
-// fp32 when out_f32, else in the storage type); optional storage-type copy
-// out2 and contribution tap; optional fused RMSNorm of the new row into y
-// (gain g); optional lens bump (lens[r] += 1 for r < rows). resid is fp32 when
+// out[r, c] = resid[r, c] + a[r, c] for c < n, a = sum_s C[s, r, c] (fp32
+// sum, stored as fp32 when out_f32, else in the storage type); with g_post,
+// a = rmsnorm(sum_s C[s, r, :]) * g_post instead (a sandwich post-norm);
+// optional storage-type copy out2 and contribution tap (a); optional fused
+// RMSNorm of the new row into y (gain g; y in fp16 when y_f16 on the bf16
+// path); optional lens bump (lens[r] += 1 for r < rows). resid is fp32 when
 // resid_f32, else the storage type.
 cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int ldc, const void* resid, bool resid_f32,
                               void* out, bool out_f32, void* out2, void* tap, const void* g, float eps, void* y,
-                              int* bump_lens, bool bf16, cudaStream_t s);
+                              int* bump_lens, bool bf16, cudaStream_t s, const void* g_post = nullptr,
+                              bool y_f16 = false);
 
 // neurons[r, f] = act(C * rs[r]) for f < F; SwiGLU reads gate at column f and up at F + f.
 // rs[r] = rsqrt(sum of row_ss[r, 0..ss_parts) / ss_n + ss_eps) (the RMSNorm of the GEMM's
@@ -175,10 +186,22 @@ cudaError_t launch_post_act(const float* C, int splits, int rows, int F, int ldc
                             const float* row_ss = nullptr, int ss_parts = 0, int ss_n = 1, float ss_eps = 0.f);
 
 // ---------------------------------------------------------------- attention
+// The attention options of every kernel below: window > 0 limits query i to
+// the keys at positions i - window + 1 .. i; gate != null (layout of o, fp16
+// on the bf16 kernels, fp32 on the fp32 one) multiplies the output, and
+// ungated (bf16 / fp32, layout of o), when set, receives it before the gate.
+struct AttnOpts {
+  int window = 0;
+  const void* gate = nullptr;
+  void* ungated = nullptr;
+  bool o_f16 = false;  // decode: o in fp16 (else bf16)
+};
+
 // Causal GQA attention; q [B,H,Tq,d], k/v [B,Hkv,kv_stride,d], o [B,Tq,H,d].
 // kv_lens null: kv_len = Tq.
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, int B, int H, int Hkv, int Tq,
-                            int d, int kv_stride, const int* kv_lens, int len_add, cudaStream_t s);
+                            int d, int kv_stride, const int* kv_lens, int len_add, cudaStream_t s,
+                            const AttnOpts& opt = AttnOpts());
 
 // tcgen05/TMEM flash attention (prefill, causal, kv_len == T, head_dim 128).
 // f16: q, k, v are fp16 (else bf16); o_f16: o is fp16 (else bf16).
@@ -188,16 +211,16 @@ cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, floa
 cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int T,
                                    int d, bool f16, bool o_f16, DevStatus* st, unsigned long long wait_ns,
                                    cudaStream_t s, const char** why, const int* q_off = nullptr,
-                                   int kv_stride = 0);
+                                   int kv_stride = 0, const AttnOpts& opt = AttnOpts());
 
 // Decode (Tq == 1), split over the keys: partial results in ws, combined into o.
 size_t attn_decode_ws_bytes(int B, int H, int d, int max_splits);
 // Keys per sequence: kv_lens[b] + len_add (<= max_len, which sizes the splits; at most
-// split_cap of them, the number ws holds).
+// split_cap of them, the number ws holds); with a window, the last `window` of them.
 cudaError_t launch_attn_decode_bf16(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv,
                                     int d, int kv_stride, const int* kv_lens, int len_add, int max_len,
                                     int split_cap, void* ws, int num_sms, DevStatus* st, unsigned long long wait_ns,
-                                    cudaStream_t s, const char** why);
+                                    cudaStream_t s, const char** why, const AttnOpts& opt = AttnOpts());
 int attn_decode_splits(int B, int Hkv, int max_len, int num_sms);
 
 // Decode attention with its split partials in a fixed file-scope device array

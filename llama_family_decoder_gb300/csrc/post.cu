@@ -6,8 +6,11 @@
 //    to the K/V buffers or cache slots;
 //  * post_resid: residual add after o_proj / down_proj ("arcee", "The block, in
 //    order"), summed in fp32 (the residual stream stays fp32 inside the block),
-//    with the next RMSNorm fused;
+//    with the next RMSNorm fused and, for the sandwich block ("afmoe", "The
+//    block, in order"), the post-norm of the sublayer's output before the add;
 //  * post_act: SiLU-gated, squared-ReLU and xIELU activations.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -25,13 +28,22 @@ __device__ __forceinline__ float split_sum(const float* C, int splits, size_t sp
 constexpr int kMaxPairsPerLane = 4;  // head_dim <= 256
 constexpr int kQkvWarps = 4;
 
+// The attention gate's storage: fp16 beside bf16 tensors, fp32 on the fp32 path.
+template <typename T>
+__device__ __forceinline__ void store_gate(void* g, size_t i, float v) {
+  if constexpr (sizeof(T) == 4)
+    static_cast<float*>(g)[i] = v;
+  else
+    static_cast<__half*>(g)[i] = __float2half_rn(v);
+}
+
 template <typename T>
 __global__ void post_qkv_kernel(const float* __restrict__ C, int splits, int rows, int ldc, int seq,
                                 const int* __restrict__ pos0, const int* __restrict__ decode_lens, int H, int Hkv,
                                 int d, int qk_norm, const T* __restrict__ q_gain, const T* __restrict__ k_gain,
                                 float eps, const float2* __restrict__ rope, int rope_max_pos, T* __restrict__ q,
                                 T* __restrict__ k,
-                                T* __restrict__ v, int kv_stride) {
+                                T* __restrict__ v, int kv_stride, void* __restrict__ gate) {
   pdl_launch_dependents();
   pdl_wait();
   const int r = blockIdx.x;
@@ -45,10 +57,16 @@ __global__ void post_qkv_kernel(const float* __restrict__ C, int splits, int row
   const int half = d / 2;
   {
     const int hid = blockIdx.y * kQkvWarps + warp;  // one warp per (row, head)
-    if (hid >= H + 2 * Hkv) return;
+    if (hid >= H + 2 * Hkv + (gate ? H : 0)) return;
+    const size_t base = (size_t)r * ldc + (size_t)hid * d;
+    if (hid >= H + 2 * Hkv) {
+      // the attention gate of query head hid - H - 2 Hkv ("afmoe"): sigmoid, in o's layout
+      const size_t g0 = ((size_t)r * H + (hid - H - 2 * Hkv)) * d;
+      for (int i = lane; i < d; i += 32) store_gate<T>(gate, g0 + i, sigmoid_f(split_sum(C, splits, sstride, base + i)));
+      return;
+    }
     const int seg = hid < H ? 0 : (hid < H + Hkv ? 1 : 2);
     const int head = seg == 0 ? hid : (seg == 1 ? hid - H : hid - H - Hkv);
-    const size_t base = (size_t)r * ldc + (size_t)hid * d;
     float x1[kMaxPairsPerLane], x2[kMaxPairsPerLane];
     float ss = 0.f;
 #pragma unroll
@@ -145,11 +163,23 @@ constexpr int kResidThreads = 256;
 // One CTA per row; each thread owns VPT groups of 4 columns, issues all their
 // loads up front and keeps the sums in registers for the fused RMSNorm.
 // TR: residual type, TO: output type, TY: storage type (gain, y, out2, tap).
+// Sum of v over the CTA (every thread gets it); red holds one float per warp.
+__device__ __forceinline__ float cta_sum(float v, float* red) {
+  v = warp_sum(v);
+  __syncthreads();  // red may still be read from an earlier call
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kResidThreads / 32; ++w) tot += red[w];
+  return tot;
+}
+
 template <typename TR, typename TO, typename TY, int VPT>
 __global__ void __launch_bounds__(kResidThreads) post_resid_kernel(
     const float* __restrict__ C, int splits, int rows, int n, int ldc, const TR* __restrict__ resid,
     TO* __restrict__ out, TY* __restrict__ out2, TY* __restrict__ tap, const TY* __restrict__ g, float eps,
-    TY* __restrict__ y, int* __restrict__ bump_lens) {
+    TY* __restrict__ y, int* __restrict__ bump_lens, const TY* __restrict__ g_post, int y_f16) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float red[kResidThreads / 32];
@@ -157,13 +187,34 @@ __global__ void __launch_bounds__(kResidThreads) post_resid_kernel(
   if (r >= rows) return;
   const size_t sstride = (size_t)rows * ldc;
   const int nv = n / 4;
-  float4 o[VPT];
-  float ss = 0.f;
+  float4 o[VPT], a[VPT];
+  float ss = 0.f, ssa = 0.f;
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = threadIdx.x + j * kResidThreads;
+    a[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (v < nv) {
+      a[j] = split_sum4(C, splits, sstride, (size_t)r * ldc + 4 * v);
+      ssa += a[j].x * a[j].x + a[j].y * a[j].y + a[j].z * a[j].z + a[j].w * a[j].w;
+    }
+  }
+  if (g_post != nullptr) {
+    // the sandwich post-norm of the sublayer's output ("afmoe", "The block, in order")
+    const float inv = rsqrtf(cta_sum(ssa, red) / (float)n + eps);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int v = threadIdx.x + j * kResidThreads;
+      if (v < nv) {
+        const float4 gg = ld4<TY>(g_post + 4 * v);
+        a[j] = make_float4(a[j].x * inv * gg.x, a[j].y * inv * gg.y, a[j].z * inv * gg.z, a[j].w * inv * gg.w);
+      }
+    }
+  }
 #pragma unroll
   for (int j = 0; j < VPT; ++j) {
     const int v = threadIdx.x + j * kResidThreads;
     if (v < nv) {
-      const float4 contrib = split_sum4(C, splits, sstride, (size_t)r * ldc + 4 * v);
+      const float4 contrib = a[j];
       const float4 rr = ld4<TR>(resid + (size_t)r * n + 4 * v);
       // the residual stream, summed in fp32
       const float4 oo = make_float4(rr.x + contrib.x, rr.y + contrib.y, rr.z + contrib.z, rr.w + contrib.w);
@@ -175,20 +226,21 @@ __global__ void __launch_bounds__(kResidThreads) post_resid_kernel(
     }
   }
   if (g != nullptr) {
-    ss = warp_sum(ss);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kResidThreads / 32; ++w) tot += red[w];
-    const float inv = rsqrtf(tot / (float)n + eps);
+    const float inv = rsqrtf(cta_sum(ss, red) / (float)n + eps);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
       const int v = threadIdx.x + j * kResidThreads;
       if (v < nv) {
         const float4 gg = ld4<TY>(g + 4 * v);
-        st4<TY>(y + (size_t)r * n + 4 * v,
-                make_float4(o[j].x * inv * gg.x, o[j].y * inv * gg.y, o[j].z * inv * gg.z, o[j].w * inv * gg.w));
+        const float4 yy =
+            make_float4(o[j].x * inv * gg.x, o[j].y * inv * gg.y, o[j].z * inv * gg.z, o[j].w * inv * gg.w);
+        if (y_f16) {  // the fp16 operand of a GEMM with prepared (fp16) weights
+          const __half2 h01 = __floats2half2_rn(yy.x, yy.y), h23 = __floats2half2_rn(yy.z, yy.w);
+          *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(y) + (size_t)r * n + 4 * v) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+        } else {
+          st4<TY>(y + (size_t)r * n + 4 * v, yy);
+        }
       }
     }
   }
@@ -262,26 +314,27 @@ __global__ void post_act_kernel(const float* __restrict__ C, int splits, int row
 cudaError_t launch_post_qkv(const float* C, int splits, int rows, int ldc, int seq, const int* pos0,
                             const int* decode_lens, int H, int Hkv, int d, int qk_norm, const void* q_gain,
                             const void* k_gain, float eps, const float2* rope, int rope_max_pos, void* q, void* k,
-                            void* v, int kv_stride, bool bf16, cudaStream_t s) {
+                            void* v, int kv_stride, bool bf16, cudaStream_t s, void* gate) {
   if (rows <= 0) return cudaSuccess;
   if (d > 2 * 32 * kMaxPairsPerLane || d % 2) return cudaErrorInvalidValue;
+  const int heads = H + 2 * Hkv + (gate ? H : 0);
   if (bf16) {
     using T = __nv_bfloat16;
-    launch_pdl(post_qkv_kernel<T>, dim3(rows, (H + 2 * Hkv + kQkvWarps - 1) / kQkvWarps), 32 * kQkvWarps, 0, s, C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
+    launch_pdl(post_qkv_kernel<T>, dim3(rows, (heads + kQkvWarps - 1) / kQkvWarps), 32 * kQkvWarps, 0, s, C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
                                            static_cast<const T*>(q_gain), static_cast<const T*>(k_gain), eps, rope, rope_max_pos,
-                                           static_cast<T*>(q), static_cast<T*>(k), static_cast<T*>(v), kv_stride);
+                                           static_cast<T*>(q), static_cast<T*>(k), static_cast<T*>(v), kv_stride, gate);
   } else {
     using T = float;
-    launch_pdl(post_qkv_kernel<T>, dim3(rows, (H + 2 * Hkv + kQkvWarps - 1) / kQkvWarps), 32 * kQkvWarps, 0, s, C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
+    launch_pdl(post_qkv_kernel<T>, dim3(rows, (heads + kQkvWarps - 1) / kQkvWarps), 32 * kQkvWarps, 0, s, C, splits, rows, ldc, seq, pos0, decode_lens, H, Hkv, d, qk_norm,
                                            static_cast<const T*>(q_gain), static_cast<const T*>(k_gain), eps, rope, rope_max_pos,
-                                           static_cast<T*>(q), static_cast<T*>(k), static_cast<T*>(v), kv_stride);
+                                           static_cast<T*>(q), static_cast<T*>(k), static_cast<T*>(v), kv_stride, gate);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int ldc, const void* resid, bool resid_f32,
                               void* out, bool out_f32, void* out2, void* tap, const void* g, float eps, void* y,
-                              int* bump_lens, bool bf16, cudaStream_t s) {
+                              int* bump_lens, bool bf16, cudaStream_t s, const void* g_post, bool y_f16) {
   if (rows <= 0) return cudaSuccess;
   if (n % 4 || ldc % 4) return cudaErrorInvalidValue;
   const int nv = n / 4;
@@ -290,7 +343,8 @@ cudaError_t launch_post_resid(const float* C, int splits, int rows, int n, int l
 #define BLK_POST_RESID_V(TR, TO, TY, V)                                                                        \
   launch_pdl(post_resid_kernel<TR, TO, TY, V>, rows, kResidThreads, 0, s,                                            \
       C, splits, rows, n, ldc, static_cast<const TR*>(resid), static_cast<TO*>(out), static_cast<TY*>(out2),  \
-      static_cast<TY*>(tap), static_cast<const TY*>(g), eps, static_cast<TY*>(y), bump_lens)
+      static_cast<TY*>(tap), static_cast<const TY*>(g), eps, static_cast<TY*>(y), bump_lens,              \
+      static_cast<const TY*>(g_post), (bf16 && y_f16) ? 1 : 0)
 #define BLK_POST_RESID(TR, TO, TY)                  \
   do {                                              \
     if (vpt <= 1)                                   \

@@ -47,11 +47,21 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* p, const fl
   *reinterpret_cast<uint4*>(p) =
       make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
 }
+template <>
+__device__ __forceinline__ void store8<__half>(__half* p, const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
 
-// NC = chunks of 8 elements per thread
-template <typename TX, typename TY, int NC>
+// NC = chunks of 8 elements per thread; TX: x, TY: the gain, TO: y
+template <typename TX, typename TY, typename TO, int NC>
 __global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const TX* __restrict__ x, const TY* __restrict__ g,
-                                                           int rows, int n, float eps, TY* __restrict__ y) {
+                                                           int rows, int n, float eps, TO* __restrict__ y) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float red[kThreads / 32];
@@ -77,7 +87,7 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const TX* __restrict_
     for (int w = 0; w < kThreads / 32; ++w) tot += red[w];
     __syncthreads();  // red is reused by the next row
     const float inv = rsqrtf(tot / (float)n + eps);
-    TY* yr = y + (size_t)r * n;
+    TO* yr = y + (size_t)r * n;
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
       const int c = threadIdx.x + j * kThreads;
@@ -86,13 +96,13 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const TX* __restrict_
         load8<TY>(g + c * 8, gg);
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[i] = buf[j][i] * inv * gg[i];
-        store8<TY>(yr + c * 8, o);
+        store8<TO>(yr + c * 8, o);
       }
     }
   }
 }
 
-template <typename TX, typename TY>
+template <typename TX, typename TY, typename TO = TY>
 cudaError_t launch_t(const void* x, const void* g, int rows, int n, float eps, void* y, cudaStream_t s) {
   const int nc = (n / 8 + kThreads - 1) / kThreads;
   int dev = 0, sms = 148;
@@ -101,16 +111,16 @@ cudaError_t launch_t(const void* x, const void* g, int rows, int n, float eps, v
   const int grid = rows < sms * 8 ? rows : sms * 8;
   auto X = static_cast<const TX*>(x);
   auto G = static_cast<const TY*>(g);
-  auto Y = static_cast<TY*>(y);
+  auto Y = static_cast<TO*>(y);
   switch (nc) {
-    case 1: launch_pdl(rmsnorm_kernel<TX, TY, 1>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 2: launch_pdl(rmsnorm_kernel<TX, TY, 2>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 3: launch_pdl(rmsnorm_kernel<TX, TY, 3>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 4: launch_pdl(rmsnorm_kernel<TX, TY, 4>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 5: launch_pdl(rmsnorm_kernel<TX, TY, 5>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 6: launch_pdl(rmsnorm_kernel<TX, TY, 6>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 7: launch_pdl(rmsnorm_kernel<TX, TY, 7>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 8: launch_pdl(rmsnorm_kernel<TX, TY, 8>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 1: launch_pdl(rmsnorm_kernel<TX, TY, TO, 1>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 2: launch_pdl(rmsnorm_kernel<TX, TY, TO, 2>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 3: launch_pdl(rmsnorm_kernel<TX, TY, TO, 3>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 4: launch_pdl(rmsnorm_kernel<TX, TY, TO, 4>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 5: launch_pdl(rmsnorm_kernel<TX, TY, TO, 5>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 6: launch_pdl(rmsnorm_kernel<TX, TY, TO, 6>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 7: launch_pdl(rmsnorm_kernel<TX, TY, TO, 7>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
+    case 8: launch_pdl(rmsnorm_kernel<TX, TY, TO, 8>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -220,10 +230,14 @@ cudaError_t launch_cast_f16_bf16(const void* src, void* dst, size_t n, cudaStrea
 }
 
 cudaError_t launch_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y, bool bf16,
-                           cudaStream_t s, bool x_f32) {
+                           cudaStream_t s, bool x_f32, bool y_f16) {
   if (rows <= 0) return cudaSuccess;
   if (n % 8) return cudaErrorInvalidValue;
   if (!bf16) return launch_t<float, float>(x, g, rows, n, eps, y, s);
+  if (y_f16) {  // the fp16 A operand of a GEMM with prepared (fp16) weights: normalized first, so in range
+    if (x_f32) return launch_t<float, __nv_bfloat16, __half>(x, g, rows, n, eps, y, s);
+    return launch_t<__nv_bfloat16, __nv_bfloat16, __half>(x, g, rows, n, eps, y, s);
+  }
   if (x_f32) return launch_t<float, __nv_bfloat16>(x, g, rows, n, eps, y, s);
   return launch_t<__nv_bfloat16, __nv_bfloat16>(x, g, rows, n, eps, y, s);
 }

@@ -46,6 +46,11 @@ class Workload:
     seed: int = 0
     n_layers: int = 0  # > 0: the model around the block (embeddings, n_layers blocks, norm, lm_head)
     vocab: int = 0
+    # the "afmoe" block options
+    sliding_window: int = 0  # > 0: attention over the last sliding_window positions
+    use_rope: bool = True
+    attn_gate: bool = False
+    sandwich_norm: bool = False
 
     @property
     def tokens(self) -> int:
@@ -69,6 +74,15 @@ WORKLOADS = {
                  cache_len=1536, seed=5),
         Workload("llama7b_model_bf16_B1_T2048_L32", "bf16", 1, 2048, 4096, 32, 32, 128, 10928, "silu", seed=6,
                  n_layers=32, vocab=32000),
+        # Trinity Nano's dense block ("afmoe" Config: hidden 1024, 8 heads over 2 KV heads,
+        # head_dim 128, intermediate 3072, silu, window 2048), a sliding-window block with its
+        # rotary and a whole-prefix block without, both with q/k norms, head gate and sandwich norms
+        Workload("afmoe_nano_sliding_bf16_B8_T4096_W2048", "bf16", 8, 4096, 1024, 8, 2, 128, 3072, "silu",
+                 qk_norm=True, seed=7, sliding_window=2048, attn_gate=True, sandwich_norm=True),
+        Workload("afmoe_nano_global_bf16_B8_T4096", "bf16", 8, 4096, 1024, 8, 2, 128, 3072, "silu",
+                 qk_norm=True, seed=8, use_rope=False, attn_gate=True, sandwich_norm=True),
+        Workload("afmoe_nano_decode_bf16_B64_L8192_W2048", "bf16", 64, 1, 1024, 8, 2, 128, 3072, "silu",
+                 qk_norm=True, cache_len=8192, seed=9, sliding_window=2048, attn_gate=True, sandwich_norm=True),
     ]
 }
 
@@ -108,6 +122,11 @@ def make_weights(w: Workload, seed: int | None = None, gain_std: float = 0.0,
     if w.qk_norm:
         out["q_norm"] = gain(d)
         out["k_norm"] = gain(d)
+    if w.attn_gate:
+        out["attn_gate_proj"] = _normal(gen, (H * d, D), weight_std, dt)
+    if w.sandwich_norm:
+        out["post_attn_norm"] = gain(D)
+        out["post_mlp_norm"] = gain(D)
     return out
 
 

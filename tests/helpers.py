@@ -13,7 +13,9 @@ def cfg_of(wl: Workload) -> oracle.BlockConfig:
     return oracle.BlockConfig(wl.hidden_size, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.intermediate_size,
                               wl.hidden_act, wl.rms_norm_eps, wl.rope_theta, wl.qk_norm, wl.xielu_alpha_p,
                               wl.xielu_alpha_n,
-                              rope_scaling=oracle.RopeScaling(*wl.rope_scaling) if wl.rope_scaling else None)
+                              rope_scaling=oracle.RopeScaling(*wl.rope_scaling) if wl.rope_scaling else None,
+                              sliding_window=wl.sliding_window, use_rope=wl.use_rope, attn_gate=wl.attn_gate,
+                              sandwich_norm=wl.sandwich_norm)
 
 
 def np64(t: torch.Tensor) -> np.ndarray:

@@ -69,6 +69,9 @@ def _desc(**kw):
     (dict(act=7), 1),
     (dict(dtype=1, head_dim=64), 2),  # bf16 path wants head_dim 128
     (dict(dtype=1, head_dim=128, hidden=260), 2),
+    (dict(sliding_window=-1), 1),     # "afmoe" options: a negative window
+    (dict(attn_gate=2), 1),           # flags are 0 or 1
+    (dict(no_rope=1, rope_type=1, rope_factor=2.0, rope_orig_max_pos=64, rope_low=1.0, rope_high=32.0), 1),
 ])
 def test_create_rejects_bad_descriptors(L, kw, code):
     h = ctypes.c_void_p()

@@ -47,8 +47,8 @@ def test_decode_full_size_sampled_sequences():
     blk = DecoderBlock.from_workload(wl)
     lens = torch.full((wl.batch,), wl.cache_len, dtype=torch.int32, device="cuda")
     kd, vd = kc.cuda(), vc.cuda()
-    out = blk.forward(x[:, None].cuda(), {k: v.cuda() for k, v in w.items()},
-                      cache={"k": kd, "v": vd, "lens": lens}, host_lens_max=wl.cache_len)
+    wd = blk.prepare({k: v.cuda() for k, v in w.items()})  # as bench.py runs it
+    out = blk.forward(x[:, None].cuda(), wd, cache={"k": kd, "v": vd, "lens": lens}, host_lens_max=wl.cache_len)
     torch.cuda.synchronize()
     assert blk.last_status() == 0
     assert (lens == wl.cache_len + 1).all()

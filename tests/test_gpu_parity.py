@@ -208,11 +208,13 @@ def test_decode_step_small(dtype):
         assert torch.equal(kd[b, :, :L].cpu(), kc[b, :, :L])
 
 
+@pytest.mark.parametrize("prepared", [False, True], ids=["bf16_weights", "prepared_fp16"])
 @pytest.mark.parametrize("act,qk_norm,batch,ffn", [("relu2", False, 7, 1000), ("xielu", True, 3, 1024),
                                                    ("silu", True, 70, 968)])
-def test_decode_step_bf16_variants_and_taps(act, qk_norm, batch, ffn):
+def test_decode_step_bf16_variants_and_taps(act, qk_norm, batch, ffn, prepared):
     # every activation, q/k-norm with non-unit gains, a token tile wider than 64,
-    # ragged MLP tiles, and the per-stage taps of the decode path
+    # ragged MLP tiles, and the per-stage taps of the decode path (fp16 operands
+    # with prepared weights)
     wl = Workload(f"decode_{act}", "bf16", batch, 1, 512, 8, 2, 128, ffn, act, qk_norm=qk_norm, seed=25)
     lens = [(37 * b + 11) % 190 + 1 for b in range(batch)]
     w, x, kc, vc = _decode_case(wl, lens)
@@ -220,7 +222,10 @@ def test_decode_step_bf16_variants_and_taps(act, qk_norm, batch, ffn):
     kd, vd = kc.to(DEV), vc.to(DEV)
     lens_d = torch.tensor(lens, dtype=torch.int32, device=DEV)
     tb = _tap_buffers(wl, torch.bfloat16)
-    out = blk.forward(x[:, None].to(DEV), to_dev(w), cache={"k": kd, "v": vd, "lens": lens_d},
+    wd = to_dev(w)
+    if prepared:
+        wd = blk.prepare(wd)
+    out = blk.forward(x[:, None].to(DEV), wd, cache={"k": kd, "v": vd, "lens": lens_d},
                       host_lens_max=max(lens), taps=tb)
     torch.cuda.synchronize()
     assert blk.last_status() == 0
@@ -234,6 +239,7 @@ def test_decode_step_bf16_variants_and_taps(act, qk_norm, batch, ffn):
     assert rel_err(got_v, ref["new_value"]) <= TOL["bf16"]
     for name, key, sl in [("attention_queries", "attention_queries", lambda t: t[:, :, 0]),
                           ("attention_output", "attention_output", lambda t: t[:, 0]),
+                          ("attention_head_outputs", "attention_head_outputs", lambda t: t[:, 0]),
                           ("layer_mid", "layer_mid", lambda t: t[:, 0]),
                           ("mlp_neurons", "mlp_neurons", lambda t: t[:, 0]),
                           ("mlp_output", "mlp_output", lambda t: t[:, 0])]:
