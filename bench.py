@@ -49,8 +49,8 @@ def _traffic(kernel, workload):
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            t = json.load(f)[kernel]
-        if t["workload"] != workload:
+            t = json.load(f)[kernel].get(workload)  # {kernel: {workload: record}}
+        if t is None:
             return None
         src = open(os.path.join(ROOT, t["source"]), "rb").read()
         if hashlib.sha256(src).hexdigest()[:16] != t["sha256_16"]:

@@ -171,10 +171,11 @@ blk_status blk_create(const blk_desc* desc, blk_handle** out);
  * engine does when it loads a model: fp16 copies of wq, wk, wv (and
  * w_attn_gate), wo, w_gate and w_up are written to `prepared`, a caller-owned
  * device buffer of at least blk_prepared_bytes(h) bytes. With weights.prepared
- * set, the Q/K/V, o_proj and MLP-up GEMMs of prefills, prefill chunks and
- * decode steps take fp16 operands (the input norm's rows, the attention output
- * and the MLP's normed input in fp16 too): 3 more mantissa bits than bf16 at
- * the same tensor-core rate and the same bytes streamed. The conversion is exact for every bf16 weight with
+ * set, the o_proj and MLP-up GEMMs of prefills and prefill chunks, and the
+ * Q/K/V, o_proj and MLP-up GEMMs of decode steps (and of sandwich-block
+ * prefills) take fp16 operands (the input norm's rows, the attention output and
+ * the MLP's normed input in fp16 too): 3 more mantissa bits than bf16 at the
+ * same tensor-core rate and the same bytes streamed. The conversion is exact for every bf16 weight with
  * 2^-17 <= |w| <= 65504; smaller ones move by at most 2^-25. The input norm's
  * fp16 rows are normalized before rounding, so they stay finite when
  * max|ln1_g| * sqrt(D) <= 65504 (likewise ln2_g on a sandwich block); larger

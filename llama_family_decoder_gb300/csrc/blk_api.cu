@@ -464,25 +464,32 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
   void* o = (head_tap && !gated) ? head_tap : ws.o;
   void* mid_tap = taps ? taps->layer_mid : nullptr;
   void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
-  // with prepared (fp16) weights every GEMM operand formed from a norm or from the
-  // attention is fp16: 3 more mantissa bits than bf16 at the same tensor-core rate
+  // with prepared (fp16) weights the o_proj and MLP-up operands are fp16: 3 more
+  // mantissa bits than bf16 at the same tensor-core rate. On a sandwich block, whose
+  // post-norms scale each sublayer's relative error up to the size of the residual
+  // stream, the Q/K/V operand is fp16 too: the input norm then writes normalized
+  // rows (within fp16's range), which waits for each row's reduction; plain blocks
+  // keep the split norm (x * g1 in bf16 written in the same pass, 1/rms in the QKV
+  // epilogue), a few microseconds faster at the Llama-7B shape.
   Prepared prep{};
   const bool f16 = w->prepared != nullptr;
   if (f16) prepared_layout(d, w->prepared, &prep);
+  const bool qkv16 = f16 && sandwich;
   prof_mark(h, "norm1_prep", 1, s);
-  if (f16)  // the normed rows in fp16 (normalized before rounding, so within fp16's range)
+  if (qkv16)
     BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, M, d.hidden, d.eps, ws.y, true, s, false, true), "input norm"));
-  else      // x * g1 in bf16; the 1/rms of each row is applied in the QKV epilogue
+  else
     BLK_TRY(check_cuda(launch_norm_prep(x, w->ln1_g, M, d.hidden, d.eps, ws.y, ws.rs1, nullptr, s), "input norm"));
-  const float* rs1 = f16 ? nullptr : ws.rs1;
+  const float* rs1 = qkv16 ? nullptr : ws.rs1;
+  const Prepared* qprep = qkv16 ? &prep : nullptr;
   prof_mark(h, "qkv_gemm_rope", 1, s);
   void* gate = gated ? ws.gate : nullptr;
   if (cache) {
     // bf16 q (the cache's K/V are bf16, so the attention runs on bf16 operands); K/V into the cache
     BLK_TRY(bf16_qkv(h, ws.y, w, B, T, cache->lens, tap_or(taps, &blk_taps::attention_queries, ws.q), cache->k,
-                     cache->v, s, rs1, false, cache->capacity, gate, f16 ? &prep : nullptr));
+                     cache->v, s, rs1, false, cache->capacity, gate, qprep));
   } else {
-    BLK_TRY(bf16_qkv(h, ws.y, w, B, T, nullptr, ws.q, ws.k, ws.v, s, rs1, true, 0, gate, f16 ? &prep : nullptr));
+    BLK_TRY(bf16_qkv(h, ws.y, w, B, T, nullptr, ws.q, ws.k, ws.v, s, rs1, true, 0, gate, qprep));
   }
   if (taps && !cache) {  // the taps are bf16
     const size_t nq = (size_t)M * d.n_heads * d.head_dim, nkv = (size_t)M * d.n_kv_heads * d.head_dim;

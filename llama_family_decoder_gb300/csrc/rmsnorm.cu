@@ -58,10 +58,11 @@ __device__ __forceinline__ void store8<__half>(__half* p, const float (&f)[8]) {
   *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// NC = chunks of 8 elements per thread; TX: x, TY: the gain, TO: y
-template <typename TX, typename TY, typename TO, int NC>
-__global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const TX* __restrict__ x, const TY* __restrict__ g,
-                                                           int rows, int n, float eps, TO* __restrict__ y) {
+// NC = chunks of 8 elements per thread, NT threads; TX: x, TY: the gain, TO: y
+template <typename TX, typename TY, typename TO, int NC, int NT>
+__global__ void __launch_bounds__(NT) rmsnorm_kernel(const TX* __restrict__ x, const TY* __restrict__ g, int rows,
+                                                     int n, float eps, TO* __restrict__ y) {
+  constexpr int kThreads = NT;
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float red[kThreads / 32];
@@ -102,27 +103,43 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const TX* __restrict_
   }
 }
 
+// Rows of up to 8192 elements take 128 threads (up to 8 chunks of 8 each), so that
+// 16 CTAs fit on an SM and every row of a prefill normalises at once; longer rows 256.
 template <typename TX, typename TY, typename TO = TY>
 cudaError_t launch_t(const void* x, const void* g, int rows, int n, float eps, void* y, cudaStream_t s) {
-  const int nc = (n / 8 + kThreads - 1) / kThreads;
+  const int nt = n / 8 <= 128 * 8 ? 128 : 256;
+  const int nc = (n / 8 + nt - 1) / nt;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = rows < sms * 8 ? rows : sms * 8;
+  const int per_sm = nt == 128 ? 16 : 8;
+  const int grid = rows < sms * per_sm ? rows : sms * per_sm;
   auto X = static_cast<const TX*>(x);
   auto G = static_cast<const TY*>(g);
   auto Y = static_cast<TO*>(y);
-  switch (nc) {
-    case 1: launch_pdl(rmsnorm_kernel<TX, TY, TO, 1>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 2: launch_pdl(rmsnorm_kernel<TX, TY, TO, 2>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 3: launch_pdl(rmsnorm_kernel<TX, TY, TO, 3>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 4: launch_pdl(rmsnorm_kernel<TX, TY, TO, 4>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 5: launch_pdl(rmsnorm_kernel<TX, TY, TO, 5>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 6: launch_pdl(rmsnorm_kernel<TX, TY, TO, 6>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 7: launch_pdl(rmsnorm_kernel<TX, TY, TO, 7>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    case 8: launch_pdl(rmsnorm_kernel<TX, TY, TO, 8>, grid, kThreads, 0, s, X, G, rows, n, eps, Y); break;
-    default: return cudaErrorInvalidValue;
+#define BLK_RMS(NC, NT) launch_pdl(rmsnorm_kernel<TX, TY, TO, NC, NT>, grid, NT, 0, s, X, G, rows, n, eps, Y)
+  if (nt == 128) {
+    switch (nc) {
+      case 1: BLK_RMS(1, 128); break;
+      case 2: BLK_RMS(2, 128); break;
+      case 3: BLK_RMS(3, 128); break;
+      case 4: BLK_RMS(4, 128); break;
+      case 5: BLK_RMS(5, 128); break;
+      case 6: BLK_RMS(6, 128); break;
+      case 7: BLK_RMS(7, 128); break;
+      case 8: BLK_RMS(8, 128); break;
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    switch (nc) {
+      case 5: BLK_RMS(5, 256); break;
+      case 6: BLK_RMS(6, 256); break;
+      case 7: BLK_RMS(7, 256); break;
+      case 8: BLK_RMS(8, 256); break;
+      default: return cudaErrorInvalidValue;
+    }
   }
+#undef BLK_RMS
   return cudaGetLastError();
 }
 

@@ -57,12 +57,13 @@ def _run(wl, gain_std=0.0, taps=False, prepared=False):
 
 # ------------------------------------------------------------------ RMSNorm stage
 
+@pytest.mark.parametrize("n", [4096, 1000, 12288])  # 128 threads x 4 chunks, a ragged chunk count, 256 threads
 @pytest.mark.parametrize("dt,tol", [(torch.float32, 1e-6), (torch.bfloat16, None)])
-def test_rmsnorm_stage(dt, tol):
+def test_rmsnorm_stage(dt, tol, n):
     g = torch.Generator().manual_seed(5)
-    x = torch.randn(37, 4096, generator=g)
+    x = torch.randn(37, n, generator=g)
     x[3] *= 1e4  # a sink-like row
-    gain = 1 + 0.1 * torch.randn(4096, generator=g)
+    gain = 1 + 0.1 * torch.randn(n, generator=g)
     x, gain = x.to(dt), gain.to(dt)
     y = rmsnorm(x.to(DEV), gain.to(DEV), 1e-5)
     torch.cuda.synchronize()
