@@ -19,6 +19,7 @@ from .block import (  # noqa: F401
     xielu_effective,
     softplus,
     block_forward,
+    padding_run,
     mlp,
     decode_step,
     prefill_with_cache,

@@ -193,7 +193,7 @@ def rope(x, positions, theta, scaling=None):
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
 
-def causal_gqa_attention(q, k, v, q_positions, k_positions, return_pattern=False, window=0):
+def causal_gqa_attention(q, k, v, q_positions, k_positions, return_pattern=False, window=0, key_valid=None):
     """softmax(q k^T / sqrt(d), causal) v per query head, grouped over KV heads.
 
     q: [H, Tq, d], k, v: [Hkv, Tk, d] (one sequence). Query head h reads KV head
@@ -201,8 +201,10 @@ def causal_gqa_attention(q, k, v, q_positions, k_positions, return_pattern=False
     to 5j + 4"). Key j is visible to query i iff k_positions[j] <= q_positions[i]
     and, when window > 0, q_positions[i] - k_positions[j] < window ("afmoe",
     "Rotary runs on the sliding-window blocks only": the last sliding_window
-    tokens). Returns head outputs [H, Tq, d] (and the masked scores and
-    probabilities).
+    tokens). key_valid (bool [Tk], optional) hides the padding keys of an
+    attention_mask ("arcee", "The API": zeros are padding); a query that sees no
+    key at all gets a zero output. Returns head outputs [H, Tq, d] (and the
+    masked scores and probabilities).
     """
     q = np.asarray(q, dtype=F64)
     k = np.asarray(k, dtype=F64)
@@ -214,15 +216,19 @@ def causal_gqa_attention(q, k, v, q_positions, k_positions, return_pattern=False
     visible = gap >= 0
     if window > 0:
         visible &= gap < window
+    if key_valid is not None:
+        visible &= np.asarray(key_valid, dtype=bool)[None, :]
+    seen = np.any(visible, axis=-1)  # [Tq]: queries with at least one visible key
     out = np.empty((H, Tq, d), dtype=F64)
     scores_all, probs_all = [], []
     for h in range(H):
         j = h // group
         s = (q[h] @ k[j].T) / np.sqrt(F64(d))
         s = np.where(visible, s, -np.inf)
-        m = np.max(s, axis=-1, keepdims=True)
+        m = np.where(seen[:, None], np.max(s, axis=-1, keepdims=True), 0.0)
         e = np.exp(s - m)
-        p = e / np.sum(e, axis=-1, keepdims=True)
+        z = np.sum(e, axis=-1, keepdims=True)
+        p = e / np.where(z > 0, z, 1.0)
         out[h] = p @ v[j]
         if return_pattern:
             scores_all.append(s)
@@ -383,7 +389,22 @@ def _finish_rows(cfg, w, x_rows, heads_out, h_rows):
     return taps
 
 
-def block_forward(cfg, w, x, rows=None, positions=None, return_pattern=False):
+def padding_run(mask_row):
+    """[lo, hi): the contiguous run of ones of one attention_mask row (left
+    padding, right padding or both); (T, T) for a row of zeros. Other patterns
+    are refused."""
+    m = np.asarray(mask_row) != 0
+    T = m.shape[0]
+    ones = np.flatnonzero(m)
+    if ones.size == 0:
+        return T, T
+    lo, hi = int(ones[0]), int(ones[-1]) + 1
+    if ones.size != hi - lo:
+        raise ValueError("attention_mask rows must hold one contiguous run of ones")
+    return lo, hi
+
+
+def block_forward(cfg, w, x, rows=None, positions=None, return_pattern=False, attention_mask=None):
     """Forward pass of one decoder block over x[B, T, D] (fp64).
 
     Follows the "LlamaForCausalLM-32L-4096d" pseudo-code, with the MLP variant
@@ -393,6 +414,10 @@ def block_forward(cfg, w, x, rows=None, positions=None, return_pattern=False):
     rows: optional sorted list of sequence positions whose outputs are wanted
     (keys/values are still formed for every position, as attention needs them).
     positions: optional rotary positions of the T rows (default 0 .. T-1).
+    attention_mask: optional [B, T] of 0/1 ("arcee", "The API": zeros are
+    padding), each row one contiguous run of ones [lo, hi): padding keys are
+    hidden and row t takes position t - lo, so a real row equals the unpadded
+    sequence's row; rows before lo see no key (zero head outputs).
 
     Returns a dict of taps, each with a leading batch axis, named as the nnterp
     pages name them: attention_norm_output, attention_queries [B,H,R,d],
@@ -410,13 +435,20 @@ def block_forward(cfg, w, x, rows=None, positions=None, return_pattern=False):
     if positions is None:
         positions = np.arange(T)
     positions = np.asarray(positions)
+    if attention_mask is not None and positions is not None and not np.array_equal(positions, np.arange(T)):
+        raise ValueError("attention_mask sets the positions itself")
     per_batch = []
     for b in range(B):
         taps = {}
+        pos_b, valid = positions, None
+        if attention_mask is not None:
+            lo, _ = padding_run(attention_mask[b])
+            pos_b = np.arange(T) - lo
+            valid = np.asarray(attention_mask[b]) != 0
         h = rms_norm(x[b], w["input_layernorm"], cfg.rms_norm_eps)  # [T, D]
-        k, v = _project_kv(cfg, w, h, positions)
-        q = _project_q(cfg, w, h[rows], positions[rows])
-        res = causal_gqa_attention(q, k, v, positions[rows], positions, return_pattern, cfg.sliding_window)
+        k, v = _project_kv(cfg, w, h, pos_b)
+        q = _project_q(cfg, w, h[rows], pos_b[rows])
+        res = causal_gqa_attention(q, k, v, pos_b[rows], pos_b, return_pattern, cfg.sliding_window, valid)
         if return_pattern:
             heads, scores, probs = res
             taps["attention_scores"] = scores

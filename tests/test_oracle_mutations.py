@@ -51,8 +51,8 @@ def _rope_sign(x, positions, theta, scaling=None):
     return np.concatenate([x1 * c + x2 * s, x2 * c - x1 * s], axis=-1)
 
 
-def _attn_factory(scale=True, gqa="div", strict=False, window_slack=0):
-    def attn(q, k, v, q_positions, k_positions, return_pattern=False, window=0):
+def _attn_factory(scale=True, gqa="div", strict=False, window_slack=0, use_key_valid=True):
+    def attn(q, k, v, q_positions, k_positions, return_pattern=False, window=0, key_valid=None):
         q, k, v = (np.asarray(a, dtype=F64) for a in (q, k, v))
         H, Tq, d = q.shape
         Hkv = k.shape[0]
@@ -60,14 +60,17 @@ def _attn_factory(scale=True, gqa="div", strict=False, window_slack=0):
         vis = (kp[None, :] < qp[:, None]) | (kp[None, :] == 0) if strict else kp[None, :] <= qp[:, None]
         if window > 0:
             vis = vis & (qp[:, None] - kp[None, :] < window + window_slack)
+        if key_valid is not None and use_key_valid:
+            vis = vis & np.asarray(key_valid, dtype=bool)[None, :]
         out = np.empty((H, Tq, d))
         ss, pp = [], []
         for h in range(H):
             j = h // (H // Hkv) if gqa == "div" else h % Hkv
             s = q[h] @ k[j].T / (np.sqrt(F64(d)) if scale else 1.0)
             s = np.where(vis, s, -np.inf)
-            e = np.exp(s - s.max(-1, keepdims=True))
-            p = e / e.sum(-1, keepdims=True)
+            mx = s.max(-1, keepdims=True)
+            e = np.exp(s - np.where(np.isfinite(mx), mx, 0.0))
+            p = e / np.maximum(e.sum(-1, keepdims=True), 1e-300)
             out[h] = p @ v[j]
             ss.append(s)
             pp.append(p)
@@ -160,6 +163,13 @@ def _project_kv_rope_always(cfg, w, h_norm, positions):
     return _orig_project_kv(dataclasses.replace(cfg, use_rope=True), w, h_norm, positions)
 
 
+def _padding_run_unshifted(mask_row):
+    # the padding keys hidden, but the real tokens' positions left unshifted
+    lo, hi = _orig_padding_run(mask_row)
+    return 0, hi
+
+
+_orig_padding_run = ob.padding_run
 _orig_finish = ob._finish_rows
 _orig_mlp = ob.mlp
 _orig_project_q = ob._project_q
@@ -189,6 +199,8 @@ MUTATIONS = {
     "sandwich_mlp_post_norm_dropped": [("_finish_rows", _finish_no_mlp_post_norm)],
     "rotary_on_whole_prefix_blocks": [("_project_q", _project_q_rope_always),
                                       ("_project_kv", _project_kv_rope_always)],
+    "padding_keys_visible": [("causal_gqa_attention", _attn_factory(use_key_valid=False))],
+    "padding_positions_unshifted": [("padding_run", _padding_run_unshifted)],
 }
 
 PIN_TESTS = [
@@ -216,6 +228,7 @@ PIN_TESTS = [
     pins.test_afmoe_sandwich_scale_invariance,
     pins.test_afmoe_gate_taps_and_half_gate,
     pins.test_afmoe_whole_prefix_block_queries_are_q_norm_output,
+    pins.test_padded_batch_real_rows_equal_the_unpadded_rows,
 ]
 
 

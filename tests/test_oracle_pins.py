@@ -509,6 +509,44 @@ def test_afmoe_window_decode_and_chunk_match_the_prefill():
     np.testing.assert_allclose(ch["layer_output"][1], full["layer_output"][1, 5:9], rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------- padded batches
+
+def test_padded_batch_real_rows_equal_the_unpadded_rows():
+    # "arcee", "The API": attention_mask [batch seq], zeros are padding. Left, right and
+    # two-sided padding: every real row equals the block over the unpadded sequence,
+    # for the plain block and for a windowed afmoe block.
+    rng = np.random.default_rng(70)
+    for cfg in (_tiny("silu", True, H=4, Hkv=2), _afmoe(window=3)):
+        w = _weights(cfg, rng)
+        T = 9
+        x = rng.standard_normal((4, T, cfg.hidden_size))
+        runs = [(3, 9), (0, 6), (2, 7), (0, 9)]
+        mask = np.zeros((4, T), dtype=np.int32)
+        for b, (lo, hi) in enumerate(runs):
+            mask[b, lo:hi] = 1
+        t = oracle.block_forward(cfg, w, x, attention_mask=mask)
+        for b, (lo, hi) in enumerate(runs):
+            ref = oracle.block_forward(cfg, w, x[b:b + 1, lo:hi])
+            np.testing.assert_allclose(t["layer_output"][b, lo:hi], ref["layer_output"][0], rtol=1e-12, atol=1e-12)
+            # the real tokens' rotary positions restart at 0 (the rotary is relative, so only the
+            # query/key values, not the output, show the shift)
+            np.testing.assert_allclose(t["attention_queries"][b, :, lo:hi], ref["attention_queries"][0], rtol=1e-12,
+                                       atol=1e-12)
+            np.testing.assert_allclose(t["attention_keys"][b, :, lo:hi], ref["attention_keys"][0], rtol=1e-12,
+                                       atol=1e-12)
+            # rows before the run see no key: zero head outputs
+            np.testing.assert_array_equal(t["attention_head_outputs"][b, :lo], 0.0)
+            assert np.all(np.isfinite(t["layer_output"][b]))
+
+
+def test_padding_run_shapes():
+    assert oracle.padding_run([0, 0, 1, 1, 1]) == (2, 5)
+    assert oracle.padding_run([1, 1, 0]) == (0, 2)
+    assert oracle.padding_run([0, 0, 0]) == (3, 3)
+    with pytest.raises(ValueError):
+        oracle.padding_run([1, 0, 1])
+
+
 def test_block_identity_and_taps():
     # "arcee"/"apertus": layer_input + attention_output + mlp_output == layer_output
     rng = np.random.default_rng(8)
