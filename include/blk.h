@@ -210,6 +210,22 @@ blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const b
                        blk_kv_cache* cache, int host_lens_max, void* out, void* workspace,
                        size_t workspace_bytes, const blk_taps* taps, void* stream);
 
+/* A padded prefill batch (nnterp's attention_mask, "arcee", "The API": [batch
+ * seq], zeros are padding). attention_mask: device int32 [B, T], 16-byte
+ * aligned; the ones of each row form one contiguous run [lo_b, hi_b) (left
+ * padding, right padding, or both). Key j of sequence b is visible to query t
+ * iff lo_b <= j < hi_b and j <= t (and within the sliding window), and row t
+ * takes rotary position t - lo_b, so every real row equals the row of the
+ * unpadded sequence. Padding rows are computed like the others and carry no
+ * meaning: rows before lo_b see no key (their head outputs are zero), rows from
+ * hi_b on see the real keys. A row whose ones are not contiguous sets the
+ * status word to INVALID_ARG (blk_last_status) and is treated as its hull.
+ * Otherwise as blk_forward without a cache (same workspace). Errors: those of
+ * blk_forward. */
+blk_status blk_forward_masked(blk_handle* h, const void* x, int batch, int seq, const int* attention_mask,
+                              const blk_weights* w, void* out, void* workspace, size_t workspace_bytes,
+                              const blk_taps* taps, void* stream);
+
 /* The model around the block ("LlamaForCausalLM-32L-4096d" sheet, "Implementing
  * it": embed_tokens, the decoder layers, norm, lm_head), all layers of one
  * handle's shape. Device pointers in the handle's dtype, row-major:

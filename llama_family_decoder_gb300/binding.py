@@ -61,6 +61,8 @@ SIGNATURES = {
     "blk_workspace_bytes": (c_size_t, [c_void_p, c_int, c_int, c_int]),
     "blk_forward": (c_int, [c_void_p, c_void_p, c_int, c_int, POINTER(blk_weights), POINTER(blk_kv_cache), c_int,
                             c_void_p, c_void_p, c_size_t, POINTER(blk_taps), c_void_p]),
+    "blk_forward_masked": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, POINTER(blk_weights), c_void_p,
+                                   c_void_p, c_size_t, POINTER(blk_taps), c_void_p]),
     "blk_rmsnorm": (c_int, [c_void_p, c_void_p, c_int, c_int, c_float, c_void_p, c_int, c_void_p]),
     "blk_qkv_rope": (c_int, [c_void_p, c_void_p, POINTER(blk_weights), c_int, c_int, c_void_p, c_void_p, c_void_p,
                              c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -220,10 +222,12 @@ class DecoderBlock:
             self._ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
         return self._ws
 
-    def forward(self, x, weights, cache=None, out=None, workspace=None, taps=None, stream=None, host_lens_max=-1):
+    def forward(self, x, weights, cache=None, out=None, workspace=None, taps=None, stream=None, host_lens_max=-1,
+                attention_mask=None):
         """out = block(x); x [B, T, D] device tensor. cache: dict(k, v, lens): T new tokens per
         sequence after lens[b] cached positions (a decode step for T == 1, a prefill chunk for
-        T > 1, which needs host_lens_max = max(lens))."""
+        T > 1, which needs host_lens_max = max(lens)). attention_mask: device int32 [B, T] of a
+        padded prefill batch (blk_forward_masked; zeros are padding)."""
         import torch
         B, T, _ = x.shape
         if out is None:
@@ -239,6 +243,13 @@ class DecoderBlock:
         tp = None
         if taps:
             tp = blk_taps(*[_ptr(taps.get(n)) for n in TAP_NAMES])
+        if attention_mask is not None:
+            if cache is not None:
+                raise ValueError("attention_mask: prefill batches only")
+            _check(lib().blk_forward_masked(self.handle, _ptr(x), B, T, _ptr(attention_mask), ctypes.byref(wst),
+                                            _ptr(out), _ptr(workspace), ws_bytes,
+                                            ctypes.byref(tp) if tp is not None else None, _stream_ptr(stream)))
+            return out
         _check(lib().blk_forward(self.handle, _ptr(x), B, T, ctypes.byref(wst),
                                  ctypes.byref(kvc) if kvc is not None else None, int(host_lens_max), _ptr(out),
                                  _ptr(workspace), ws_bytes, ctypes.byref(tp) if tp is not None else None,

@@ -59,6 +59,7 @@ struct AttnParams {
   int window;
   const __half* gate;
   __nv_bfloat16* ungated;
+  const int2* key_range;  // per sequence [lo, hi): the visible (non-padding) keys, or null
   float sl2;
   DevStatus* status;
   unsigned long long wait_ns;
@@ -141,10 +142,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   pdl_wait();  // q, k, v (and the cache positions) come from earlier kernels
   const uint32_t tmem = *tmem_holder;
   const int off = p.q_off ? p.q_off[b] : 0;  // keys 0 .. off - 1 are earlier positions in the cache
-  const int n_keys = off + kv_end;           // keys this query tile can see
-  // key tiles t0 .. t_end - 1: with a window, the first tile holds the first query's oldest key
-  const int t0 = p.window > 0 ? max(0, off + m0 - p.window + 1) / kBKeys : 0;
-  const int n_tiles = (n_keys + kBKeys - 1) / kBKeys - t0;  // S0: cols [0,128), S1: [128,256), O: [256,384)
+  // visible keys: [kv_lo, kv_hi) (an attention_mask's run of real tokens, else all)
+  const int2 kr = p.key_range ? p.key_range[b] : make_int2(0, off + p.T);
+  const int kv_lo = kr.x, kv_hi = kr.y;
+  const int n_keys = min(off + kv_end, kv_hi);  // keys this query tile can see
+  // key tiles t0 .. t_end - 1: the first holds the first query's oldest visible key
+  const int first_key = max(kv_lo, p.window > 0 ? off + m0 - p.window + 1 : 0);
+  const int t0 = max(0, first_key) / kBKeys;
+  // S0: cols [0,128), S1: [128,256), O: [256,384); no tile at all when every query is padding
+  const int n_tiles = max(0, (n_keys + kBKeys - 1) / kBKeys - t0);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -258,10 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       // raw scores: masked entries become -inf (only tiles on the diagonal, past the last key
       // or, with a window, before the last query's oldest key)
       const int qc = min(qi, p.T - 1);
-      if ((n0 + kBKeys - 1 > off + m0) || (n0 + kBKeys > off + p.T) ||
+      if ((n0 + kBKeys - 1 > off + m0) || (n0 + kBKeys > kv_hi) || n0 < kv_lo ||
           (p.window > 0 && n0 < off + min(m0 + kBQ - 1, p.T - 1) - p.window + 1)) {
-        const int lim = off + qc - n0;  // keys n0 + c with c <= lim are visible
-        const int first = p.window > 0 ? lim - p.window + 1 : -kBKeys;  // ... and c >= first
+        const int causal = off + qc - n0;                    // keys n0 + c with c <= causal are not ahead
+        const int lim = min(causal, kv_hi - 1 - n0);         // ... nor padding after the run
+        const int first = max(p.window > 0 ? causal - p.window + 1 : -kBKeys, kv_lo - n0);  // c >= first
 #pragma unroll
         for (int c = 0; c < kBKeys; ++c)
           if (c > lim || c < first) x[c] = -INFINITY;
@@ -338,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (!failed) {
       __syncwarp();
       tc_fence_after();
-      const float inv = 1.f / l;
+      const bool seen = l > 0.f;  // false: a padding query that sees no key (its output is 0)
+      const float inv = seen ? 1.f / l : 0.f;
       const size_t orow_i = (((size_t)b * p.T + qi) * p.H + h) * kD;
       uint16_t* orow = static_cast<uint16_t*>(p.o) + orow_i;
       const bool of16 = p.o_f16 != 0;
@@ -355,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         tc_wait_ld();
         if (qi < p.T) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) ov[i] *= inv;
+          for (int i = 0; i < 16; ++i) ov[i] = seen ? ov[i] * inv : 0.f;
           uint4 w0, w1;
           if (p.ungated) {  // the head outputs before the gate (bf16)
             pack16(ov, false, w0, w1);
@@ -426,6 +434,7 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
   p.kv_stride = kv_stride;
   p.q_off = q_off;
   p.window = opt.window > 0 ? opt.window : 0;
+  p.key_range = opt.key_range;
   p.gate = static_cast<const __half*>(opt.gate);
   p.ungated = static_cast<__nv_bfloat16*>(opt.ungated);
   p.n_qtiles = (T + kBQ - 1) / kBQ;

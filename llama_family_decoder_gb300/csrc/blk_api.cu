@@ -156,6 +156,8 @@ struct Ws {
   void *y, *q, *k, *v, *o, *mid, *neur, *C, *attn;
   float *rs1, *ss2;  // bf16: input-norm 1/rms per row (prefill); post-attention partial sums of squares
   void* gate;        // attn_gate: sigmoid of the gate projection, o's layout (fp16; fp32 on the fp32 path)
+  int2* ranges;      // prefill with an attention_mask: each sequence's run of real tokens [lo, hi)
+  int* pos0;         // ... and its rotary offset -lo
 };
 
 Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, size_t* total) {
@@ -190,6 +192,10 @@ Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, siz
     if (d.sandwich_norm) w.C = c.take(M * d.hidden * sizeof(float));  // a sublayer's output before its post-norm
   }
   if (d.attn_gate) w.gate = c.take(M * d.n_heads * d.head_dim * (d.dtype == BLK_BF16 ? 2 : 4));
+  if (!decode) {
+    w.ranges = static_cast<int2*>(c.take((size_t)B * sizeof(int2)));
+    w.pos0 = static_cast<int*>(c.take((size_t)B * sizeof(int)));
+  }
   *total = c.off;
   return w;
 }
@@ -448,8 +454,10 @@ P tap_or(const blk_taps* t, P blk_taps::*m, P dflt) {
 
 // cache != null: a prefill chunk. The T new tokens of sequence b sit at positions
 // lens[b] .. lens[b] + T - 1, append their K/V to the cache and attend to it.
+// mask != null (no cache): a padded batch, attention_mask [B, T] (zeros are padding).
 blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, const blk_weights* w, void* out,
-                                const Ws& ws, const blk_taps* taps, cudaStream_t s, blk_kv_cache* cache = nullptr) {
+                                const Ws& ws, const blk_taps* taps, cudaStream_t s, blk_kv_cache* cache = nullptr,
+                                const int* mask = nullptr) {
   // Both RMSNorms are split around the GEMMs they feed: the gain multiplies the
   // GEMM's A rows (x * g1 is x itself when g1 == 1), the per-row 1/rms multiplies
   // the accumulator in the epilogue. q/k/v and P are kept in fp16 (3 more
@@ -475,6 +483,10 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
   const bool f16 = w->prepared != nullptr;
   if (f16) prepared_layout(d, w->prepared, &prep);
   const bool qkv16 = f16 && sandwich;
+  if (mask) {  // each sequence's run of real tokens: hidden padding keys, positions from the run's start
+    prof_mark(h, "mask_ranges", 1, s);
+    BLK_TRY(check_cuda(launch_mask_ranges(mask, B, T, ws.ranges, ws.pos0, h->status, s), "attention mask"));
+  }
   prof_mark(h, "norm1_prep", 1, s);
   if (qkv16)
     BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, M, d.hidden, d.eps, ws.y, true, s, false, true), "input norm"));
@@ -489,7 +501,7 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
     BLK_TRY(bf16_qkv(h, ws.y, w, B, T, cache->lens, tap_or(taps, &blk_taps::attention_queries, ws.q), cache->k,
                      cache->v, s, rs1, false, cache->capacity, gate, qprep));
   } else {
-    BLK_TRY(bf16_qkv(h, ws.y, w, B, T, nullptr, ws.q, ws.k, ws.v, s, rs1, true, 0, gate, qprep));
+    BLK_TRY(bf16_qkv(h, ws.y, w, B, T, mask ? ws.pos0 : nullptr, ws.q, ws.k, ws.v, s, rs1, true, 0, gate, qprep));
   }
   if (taps && !cache) {  // the taps are bf16
     const size_t nq = (size_t)M * d.n_heads * d.head_dim, nkv = (size_t)M * d.n_kv_heads * d.head_dim;
@@ -504,6 +516,7 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
   opt.window = d.sliding_window;
   opt.gate = gate;
   opt.ungated = gated ? head_tap : nullptr;  // the tap reads the heads before the gate
+  opt.key_range = mask ? ws.ranges : nullptr;
   prof_mark(h, "attention", 1, s);
   const char* why = nullptr;
   cudaError_t e =
@@ -693,7 +706,7 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
 
 // fp32 path: prefill (cache == null) or decode (cache != null, T == 1).
 blk_status forward_f32(blk_handle* h, const void* x, int B, int T, const blk_weights* w, blk_kv_cache* cache,
-                       void* out, const Ws& ws, const blk_taps* taps, cudaStream_t s) {
+                       void* out, const Ws& ws, const blk_taps* taps, cudaStream_t s, const int* mask = nullptr) {
   const blk_desc& d = h->d;
   const bool bf = false;
   const int M = B * T;
@@ -710,7 +723,8 @@ blk_status forward_f32(blk_handle* h, const void* x, int B, int T, const blk_wei
   void* mid = tap_or(taps, &blk_taps::layer_mid, ws.mid);
   void* neur = tap_or(taps, &blk_taps::mlp_neurons, ws.neur);
   const float* y = static_cast<const float*>(ws.y);
-  prof_mark(h, "fp32_block", (d.act == BLK_ACT_SWIGLU ? 13 : 12) + (gated ? 1 : 0), s);
+  prof_mark(h, "fp32_block", (d.act == BLK_ACT_SWIGLU ? 13 : 12) + (gated ? 1 : 0) + (mask ? 1 : 0), s);
+  if (mask) BLK_TRY(check_cuda(launch_mask_ranges(mask, B, T, ws.ranges, ws.pos0, h->status, s), "attention mask"));
   BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, M, d.hidden, d.eps, ws.y, bf, s), "rmsnorm 1"));
   const int nq = qkv_cols(d);
   BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->wq, C, nq, M, Hd, d.hidden, s), "q GEMM"));
@@ -719,7 +733,7 @@ blk_status forward_f32(blk_handle* h, const void* x, int B, int T, const blk_wei
   if (gated)
     BLK_TRY(check_cuda(launch_gemm_f32(y, (const float*)w->w_attn_gate, C + Hd + 2 * KVd, nq, M, Hd, d.hidden, s),
                        "attention gate GEMM"));
-  BLK_TRY(check_cuda(launch_post_qkv(C, 1, M, nq, T, nullptr, decode ? cache->lens : nullptr, d.n_heads,
+  BLK_TRY(check_cuda(launch_post_qkv(C, 1, M, nq, T, mask ? ws.pos0 : nullptr, decode ? cache->lens : nullptr, d.n_heads,
                                      d.n_kv_heads, d.head_dim, d.qk_norm, w->q_norm_g, w->k_norm_g, d.eps, h->rope,
                                      d.max_seq, q, k, v, kv_stride, bf, s, gated ? ws.gate : nullptr),
                      "qkv post"));
@@ -727,6 +741,7 @@ blk_status forward_f32(blk_handle* h, const void* x, int B, int T, const blk_wei
   opt.window = d.sliding_window;
   opt.gate = gated ? ws.gate : nullptr;
   opt.ungated = gated ? head_tap : nullptr;
+  opt.key_range = mask ? ws.ranges : nullptr;
   BLK_TRY(check_cuda(launch_attn_f32((const float*)q, (const float*)k, (const float*)v, (float*)o, B, d.n_heads,
                                      d.n_kv_heads, T, d.head_dim, kv_stride, decode ? cache->lens : nullptr,
                                      decode ? 1 : 0, s, opt),
@@ -976,9 +991,13 @@ size_t blk_workspace_bytes(const blk_handle* h, int batch, int seq, int decode) 
   return total;
 }
 
-blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const blk_weights* w, blk_kv_cache* cache,
-                       int host_lens_max, void* out, void* workspace, size_t workspace_bytes, const blk_taps* taps,
-                       void* stream) {
+}  // extern "C"
+
+namespace {
+
+blk_status forward_impl(blk_handle* h, const void* x, int batch, int seq, const blk_weights* w, blk_kv_cache* cache,
+                        int host_lens_max, const int* mask, void* out, void* workspace, size_t workspace_bytes,
+                        const blk_taps* taps, void* stream) {
   if (!h || !x || !out) return fail(BLK_ERR_INVALID_ARG, "handle, x and out must be non-NULL");
   const blk_desc& d = h->d;
   if (batch <= 0 || seq <= 0) return fail(BLK_ERR_INVALID_ARG, "batch and seq must be positive");
@@ -1024,11 +1043,32 @@ blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const b
   Ws ws = carve_forward(h, workspace, batch, seq, decode, &need);
   if (!workspace || workspace_bytes < need) return fail(BLK_ERR_WORKSPACE, "workspace missing or too small");
   if (!aligned16(workspace)) return fail(BLK_ERR_ALIGNMENT, "workspace not 16-byte aligned");
+  if (mask && (cache || !aligned16(mask)))
+    return fail(cache ? BLK_ERR_UNSUPPORTED : BLK_ERR_ALIGNMENT, "attention_mask: prefill only, 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   prof_begin(h);
-  if (d.dtype == BLK_F32) return forward_f32(h, x, batch, seq, w, cache, out, ws, taps, s);
+  if (d.dtype == BLK_F32) return forward_f32(h, x, batch, seq, w, cache, out, ws, taps, s, mask);
   if (decode) return forward_decode_bf16(h, x, batch, w, cache, max_len, out, ws, taps, s);
-  return forward_prefill_bf16(h, x, batch, seq, w, out, ws, taps, s, chunk ? cache : nullptr);
+  return forward_prefill_bf16(h, x, batch, seq, w, out, ws, taps, s, chunk ? cache : nullptr, mask);
+}
+
+}  // namespace
+
+extern "C" {
+
+blk_status blk_forward(blk_handle* h, const void* x, int batch, int seq, const blk_weights* w, blk_kv_cache* cache,
+                       int host_lens_max, void* out, void* workspace, size_t workspace_bytes, const blk_taps* taps,
+                       void* stream) {
+  return forward_impl(h, x, batch, seq, w, cache, host_lens_max, nullptr, out, workspace, workspace_bytes, taps,
+                      stream);
+}
+
+blk_status blk_forward_masked(blk_handle* h, const void* x, int batch, int seq, const int* attention_mask,
+                              const blk_weights* w, void* out, void* workspace, size_t workspace_bytes,
+                              const blk_taps* taps, void* stream) {
+  if (!attention_mask) return fail(BLK_ERR_INVALID_ARG, "attention_mask is NULL");
+  return forward_impl(h, x, batch, seq, w, nullptr, -1, attention_mask, out, workspace, workspace_bytes, taps,
+                      stream);
 }
 
 // ------------------------------------------------------------------ the model around the block

@@ -247,7 +247,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
       const int b = row_ok ? row / e.seq : 0;
       const int t = row_ok ? row - b * e.seq : 0;
       const int pos = (e.pos0 ? e.pos0[b] : 0) + t;
-      const float2* cs = e.rope + (size_t)min(pos, e.rope_max_pos - 1) * (d / 2);
+      // (a padding row of a left-padded batch sits at a negative position: never read before the table)
+      const float2* cs = e.rope + (size_t)min(max(pos, 0), e.rope_max_pos - 1) * (d / 2);
       // the input RMSNorm's 1/rms, applied here instead of to the GEMM's A rows
       const float rs = (e.row_scale && row_ok) ? e.row_scale[row] : 1.0f;
       const bool f16 = e.qkv_f16 != 0;

@@ -29,6 +29,12 @@ cudaError_t launch_norm_prep(const void* x, const void* g, int rows, int n, floa
 cudaError_t launch_embed(const int* tokens, const void* table, int rows, int row_bytes, int vocab, void* out,
                          DevStatus* st, int num_sms, cudaStream_t s);
 
+// attention_mask [B, T] (int32, zeros are padding) -> ranges[b] = [lo, hi) of row b's ones
+// ((T, T) for a row of zeros) and pos0[b] = -lo. A row whose ones are not contiguous records
+// INVALID_ARG in the status word and is treated as its hull.
+cudaError_t launch_mask_ranges(const int* mask, int B, int T, int2* ranges, int* pos0, DevStatus* st,
+                               cudaStream_t s);
+
 // dst[i] = bf16(src[i]) for fp16 src (n elements).
 cudaError_t launch_cast_f16_bf16(const void* src, void* dst, size_t n, cudaStream_t s);
 
@@ -189,12 +195,15 @@ cudaError_t launch_post_act(const float* C, int splits, int rows, int F, int ldc
 // The attention options of every kernel below: window > 0 limits query i to
 // the keys at positions i - window + 1 .. i; gate != null (layout of o, fp16
 // on the bf16 kernels, fp32 on the fp32 one) multiplies the output, and
-// ungated (bf16 / fp32, layout of o), when set, receives it before the gate.
+// ungated (bf16 / fp32, layout of o), when set, receives it before the gate;
+// key_range (prefill) hides padding keys. A query that sees no key gets a
+// zero output.
 struct AttnOpts {
   int window = 0;
   const void* gate = nullptr;
   void* ungated = nullptr;
-  bool o_f16 = false;  // decode: o in fp16 (else bf16)
+  bool o_f16 = false;            // decode: o in fp16 (else bf16)
+  const int2* key_range = nullptr;  // prefill: per sequence, only keys lo <= j < hi are visible
 };
 
 // Causal GQA attention; q [B,H,Tq,d], k/v [B,Hkv,kv_stride,d], o [B,Tq,H,d].
