@@ -1,27 +1,32 @@
-// Prefill attention on the 5th-generation tensor core (tcgen05 + TMEM), bf16,
-// causal, grouped-query, head_dim 128 ("LlamaForCausalLM-32L-4096d" sheet:
-// softmax(q @ k.T / sqrt(128), mask=causal) @ v per head; "arcee", "Grouped-
-// query attention, 128-wide heads": query head h reads KV head h / (H / Hkv)).
+// Prefill attention on the 5th-generation tensor core (tcgen05 + TMEM), causal,
+// grouped-query, head_dim 128 ("LlamaForCausalLM-32L-4096d" sheet: softmax(q @
+// k.T / sqrt(128), mask=causal) @ v per head; "arcee", "Grouped-query attention,
+// 128-wide heads": query head h reads KV head h / (H / Hkv)).
 //
+// One CTA per work item of two 128-query slots that share every K/V tile: two
+// query heads of one KV group at the same query tile (an even group size), or
+// two consecutive query tiles of one head (otherwise); heaviest items first.
+// 320 threads:
+//   warp 0      TMA producer: both slots' Q tiles once, then K and V tiles of 64
+//               keys through a 3-stage ring (128-byte swizzle, 64-column boxes).
+//   warp 1      TMEM allocation; lane 0 issues S = Q K_j^T for both slots (M=128,
+//               N=64, K=16 x 8) into each slot's pair of TMEM score buffers, and
+//               O += P_j V_j (A = P from shared memory, B = V as an MN-major
+//               operand) into each slot's TMEM output accumulator.
+//   warps 2..9  softmax, four warps per slot, one query row per thread: read S_j
+//               from TMEM, mask, exponentiate in the log2 domain against a running
+//               reference max, write P_j (swizzled K-major) to the slot's shared
+//               buffer; rescale O in TMEM only when the row max grew by more than
+//               2^8 (exact: softmax does not depend on the reference); finally
+//               O / l to the head-major output.
+// The tensor pipe interleaves the slots: S_{j+1} of both slots and PV_j of one
+// run while the softmax warps work on the other. Sharing K/V halves its traffic
+// per FLOP.
 // Options of the "afmoe" block ("Rotary runs on the sliding-window blocks only";
 // "Attention: per-head q/k norms and a sigmoid gate on every head"): a window
-// over the last W positions (the key tiles before the first query's oldest key
-// are skipped, the rest masked), and a per-channel gate on the output.
-//
-// One CTA per (128-query tile, head, sequence), heaviest tiles first, 192 threads:
-//   warp 0      TMA producer: the Q tile once, then K and V tiles of 128 keys
-//               through a 2-stage ring (128-byte swizzle, two 64-column boxes).
-//   warp 1      TMEM allocation; lane 0 issues S_j = Q K_j^T (M=128, N=128,
-//               K=16 x 8) into one of two TMEM score buffers, and O += P_j V_j
-//               (A = P from shared memory, B = V as an MN-major operand) into
-//               the TMEM output accumulator.
-//   warps 2..5  softmax, one query row per thread: read S_j from TMEM, mask,
-//               exponentiate in the log2 domain against a running reference
-//               max, write P_j (bf16, swizzled K-major) to shared memory;
-//               rescale O in TMEM only when the row max grew by more than 2^8
-//               (exact: softmax does not depend on the reference); finally
-//               O / l to the head-major output.
-// S_{j+1} runs on the tensor core while the softmax works on S_j.
+// over the last W positions (key tiles before the first query's oldest key are
+// skipped, the rest masked), and a per-channel gate on the output; a padded batch
+// hides the keys outside each sequence's run of real tokens.
 // Every wait is bounded; on expiry the CTA records a timeout, drains its own
 // copies and MMAs, frees its TMEM and returns.
 #include <cuda_fp16.h>
@@ -34,22 +39,29 @@ namespace blk {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kBQ = 128;  // queries per CTA (MMA M)
-constexpr int kBKeys = 128;  // keys per tile
-constexpr int kThreads = 192;
-constexpr int kSub = 128 * 128;          // one 64-column sub-tile of a 128-row tile (bytes)
-constexpr int kTile = 2 * kSub;          // 128 rows x 128 bf16
-constexpr int kStages = 2;
-constexpr int kSmem = 1024 + kTile * (2 + 2 * kStages) + 256;
+constexpr int kBQ = 128;                    // queries per slot (MMA M)
+constexpr int kBK = 64;                     // keys per tile
+constexpr int kSlots = 2;
+constexpr int kThreads = 64 + kSlots * 128;
+constexpr int kQSub = kBQ * 128;            // one 64-column half of a Q tile (bytes)
+constexpr int kQBytes = 2 * kQSub;          // 128 queries x 128 dims
+constexpr int kKVSub = kBK * 128;           // one 64-column half of a K or V tile
+constexpr int kKVBytes = 2 * kKVSub;        // 64 keys x 128 dims
+constexpr int kPBytes = kBQ * 128;          // 128 queries x 64 keys, one swizzled tile
+constexpr int kStages = 3;
+constexpr int kSmem = 1024 + kSlots * kQBytes + kStages * 2 * kKVBytes + kSlots * kPBytes + 256;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr unsigned long long kDrainNs = 2000000000ULL;
 constexpr float kLog2e = 1.4426950408889634f;
+static_assert(kSmem <= 227 * 1024, "shared memory");
 
 struct AttnParams {
   CUtensorMap tq, tk, tv;
   void* o;
   int o_f16;
   int B, H, Hkv, T, n_qtiles;
+  int head_pairs;  // 1: the two slots are heads 2i, 2i+1 at one query tile; 0: query tiles 2k, 2k+1 of one head
+  int n_items;
   // K/V rows per (sequence, KV head): T, or a cache's capacity; q_off: positions already
   // in that cache per sequence (the T queries sit at q_off[b] ..), or null for 0
   int kv_stride;
@@ -80,37 +92,59 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
   return pack_bf16x2(lo, hi);
 }
 
-// F16: q, k, v (and so P) are fp16; otherwise bf16. The output is bf16 either way.
+struct Slot {
+  int h, qt, m0, valid;
+};
+
+// F16: q, k, v (and so P) are fp16; otherwise bf16.
 template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + kTile;
-  uint8_t* sV = sK + kStages * kTile;
-  uint8_t* sP = sV + kStages * kTile;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTile);
-  // q_full, kv_full[2], kv_empty[2], s_full[2], p_ready, pv_done, drain
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 10);
+  uint8_t* sQ = smem;                                   // [slot]: two 64-column halves of 16 KB
+  uint8_t* sK = sQ + kSlots * kQBytes;                  // [stage]: two halves of 8 KB
+  uint8_t* sV = sK + kStages * kKVBytes;
+  uint8_t* sP = sV + kStages * kKVBytes;                // [slot]: 16 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kSlots * kPBytes);
+  // q_full, kv_full[3], kv_empty[3], s_full[2][2], p_ready[2], pv_done[2], drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const uint32_t q_full = smem_u32(&bars[0]);
   auto kv_full = [&](int s) { return smem_u32(&bars[1 + s]); };
-  auto kv_empty = [&](int s) { return smem_u32(&bars[3 + s]); };
-  auto s_full = [&](int s) { return smem_u32(&bars[5 + s]); };
-  const uint32_t p_ready = smem_u32(&bars[7]);
-  const uint32_t pv_done = smem_u32(&bars[8]);
-  const uint32_t drain = smem_u32(&bars[9]);
+  auto kv_empty = [&](int s) { return smem_u32(&bars[4 + s]); };
+  auto s_full = [&](int g, int b) { return smem_u32(&bars[7 + 2 * g + b]); };
+  auto p_ready = [&](int g) { return smem_u32(&bars[11 + g]); };
+  auto pv_done = [&](int g) { return smem_u32(&bars[13 + g]); };
+  const uint32_t drain = smem_u32(&bars[15]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // ---- the work item: two slots over one KV head of one sequence, heaviest first
   const int id = blockIdx.x;
-  const int hb = id % (p.H * p.B);
-  const int qt = p.n_qtiles - 1 - id / (p.H * p.B);
-  const int h = hb % p.H, b = hb / p.H;
-  const int kvh = h / (p.H / p.Hkv);
-  const int m0 = qt * kBQ;
-  const int kv_end = min(p.T, m0 + kBQ);
-  const int q_row = (b * p.H + h) * p.T + m0;
+  Slot sl[kSlots];
+  int b, kvh;
+  if (p.head_pairs) {
+    const int hp_n = p.H / 2;
+    const int qt = p.n_qtiles - 1 - id / (p.B * hp_n);
+    const int r = id % (p.B * hp_n);
+    const int hp = r % hp_n;
+    b = r / hp_n;
+#pragma unroll
+    for (int g = 0; g < kSlots; ++g) sl[g] = {2 * hp + g, qt, qt * kBQ, 1};
+  } else {
+    const int np = (p.n_qtiles + 1) / 2;
+    const int k = np - 1 - id / (p.B * p.H);
+    const int r = id % (p.B * p.H);
+    const int h = r % p.H;
+    b = r / p.H;
+#pragma unroll
+    for (int g = 0; g < kSlots; ++g) {
+      const int qt = 2 * k + g;
+      const int ok = qt < p.n_qtiles;
+      sl[g] = {h, ok ? qt : 2 * k, (ok ? qt : 2 * k) * kBQ, ok};
+    }
+  }
+  kvh = sl[0].h / (p.H / p.Hkv);
   const int kv_row = (b * p.Hkv + kvh) * p.kv_stride;
   const unsigned long long budget = p.wait_ns;
 
@@ -119,10 +153,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     for (int s = 0; s < kStages; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
-      mbar_init(s_full(s), 1);
     }
-    mbar_init(p_ready, 128);
-    mbar_init(pv_done, 1);
+    for (int g = 0; g < kSlots; ++g) {
+      mbar_init(s_full(g, 0), 1);
+      mbar_init(s_full(g, 1), 1);
+      mbar_init(p_ready(g), 128);
+      mbar_init(pv_done(g), 1);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -139,40 +176,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  pdl_wait();  // q, k, v (and the cache positions) come from earlier kernels
-  const uint32_t tmem = *tmem_holder;
+  pdl_wait();  // q, k, v (and the cache positions, the key ranges) come from earlier kernels
+  const uint32_t tmem = *tmem_holder;  // S[g][buf]: cols (2g + buf) * 64; O[g]: 256 + 128 g
   const int off = p.q_off ? p.q_off[b] : 0;  // keys 0 .. off - 1 are earlier positions in the cache
   // visible keys: [kv_lo, kv_hi) (an attention_mask's run of real tokens, else all)
   const int2 kr = p.key_range ? p.key_range[b] : make_int2(0, off + p.T);
   const int kv_lo = kr.x, kv_hi = kr.y;
-  const int n_keys = min(off + kv_end, kv_hi);  // keys this query tile can see
-  // key tiles t0 .. t_end - 1: the first holds the first query's oldest visible key
-  const int first_key = max(kv_lo, p.window > 0 ? off + m0 - p.window + 1 : 0);
-  const int t0 = max(0, first_key) / kBKeys;
-  // S0: cols [0,128), S1: [128,256), O: [256,384); no tile at all when every query is padding
-  const int n_tiles = max(0, (n_keys + kBKeys - 1) / kBKeys - t0);
+  // the key tiles the item needs: the union of both slots' ranges
+  int n_keys = 0, first_key = 1 << 30;
+#pragma unroll
+  for (int g = 0; g < kSlots; ++g) {
+    const int kv_end = min(p.T, sl[g].m0 + kBQ);
+    n_keys = max(n_keys, min(off + kv_end, kv_hi));
+    first_key = min(first_key, max(kv_lo, p.window > 0 ? off + sl[g].m0 - p.window + 1 : 0));
+  }
+  const int t0 = max(0, first_key) / kBK;
+  const int n_tiles = max(0, (n_keys + kBK - 1) / kBK - t0);  // none when every query is padding
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
       bool failed = false;
       uint32_t issued = 0, parity = 0;
-      mbar_arrive_expect_tx(q_full, kTile);
-      tma_load_2d(smem_u32(sQ), &p.tq, 0, q_row, q_full);
-      tma_load_2d(smem_u32(sQ + kSub), &p.tq, 64, q_row, q_full);
+      mbar_arrive_expect_tx(q_full, kSlots * kQBytes);
+#pragma unroll
+      for (int g = 0; g < kSlots; ++g) {
+        const int q_row = (b * p.H + sl[g].h) * p.T + sl[g].m0;
+        tma_load_2d(smem_u32(sQ + g * kQBytes), &p.tq, 0, q_row, q_full);
+        tma_load_2d(smem_u32(sQ + g * kQBytes + kQSub), &p.tq, 64, q_row, q_full);
+      }
       for (int j = 0; j < n_tiles; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
         if (!mbar_wait(kv_empty(s), ph ^ 1, budget, abort_flag)) {
           failed = true;
           break;
         }
-        mbar_arrive_expect_tx(kv_full(s), 2 * kTile);
-        const int row = kv_row + (t0 + j) * kBKeys;
-        tma_load_2d(smem_u32(sK + s * kTile), &p.tk, 0, row, kv_full(s));
-        tma_load_2d(smem_u32(sK + s * kTile + kSub), &p.tk, 64, row, kv_full(s));
-        tma_load_2d(smem_u32(sV + s * kTile), &p.tv, 0, row, kv_full(s));
-        tma_load_2d(smem_u32(sV + s * kTile + kSub), &p.tv, 64, row, kv_full(s));
+        mbar_arrive_expect_tx(kv_full(s), 2 * kKVBytes);
+        const int row = kv_row + (t0 + j) * kBK;
+        tma_load_2d(smem_u32(sK + s * kKVBytes), &p.tk, 0, row, kv_full(s));
+        tma_load_2d(smem_u32(sK + s * kKVBytes + kKVSub), &p.tk, 64, row, kv_full(s));
+        tma_load_2d(smem_u32(sV + s * kKVBytes), &p.tv, 0, row, kv_full(s));
+        tma_load_2d(smem_u32(sV + s * kKVBytes + kKVSub), &p.tv, 64, row, kv_full(s));
         issued |= 1u << s;
         parity = (parity & ~(1u << s)) | (ph << s);
       }
@@ -190,41 +235,50 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       // ---------------- MMA issuer
       // kind::f16 operand formats: bf16 (1) or fp16 (0) for both A and B
       constexpr uint32_t fmt_clear = F16 ? ~((7u << 7) | (7u << 10)) : ~0u;
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBKeys) & fmt_clear;
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK) & fmt_clear;
       constexpr uint32_t idesc_pv = (idesc_bf16_f32(kBQ, kD) & fmt_clear) | (1u << 16);  // B (V) is MN-major
       bool failed = !mbar_wait(q_full, 0, budget, abort_flag);
       bool issued_any = false;
       for (int j = 0; j <= n_tiles && !failed; ++j) {
         if (j < n_tiles) {
-          const int s = j & 1;
-          if (!mbar_wait(kv_full(s), (j >> 1) & 1, budget, abort_flag)) {
+          const int s = j % kStages;
+          if (!mbar_wait(kv_full(s), (j / kStages) & 1, budget, abort_flag)) {
             failed = true;
             break;
           }
           tc_fence_after();
+          // S_j of both slots (each slot's buffer j & 1 was read by its softmax of tile j - 2,
+          // which this thread waited for before PV_{j-2})
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint64_t a = smem_desc_sw128(smem_u32(sQ + (kk >> 2) * kSub)) + (uint64_t)((kk & 3) * 2);
-            const uint64_t bd = smem_desc_sw128(smem_u32(sK + s * kTile + (kk >> 2) * kSub)) + (uint64_t)((kk & 3) * 2);
-            tc_mma_bf16(tmem + s * kBKeys, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+          for (int g = 0; g < kSlots; ++g) {
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint64_t a = smem_desc_sw128(smem_u32(sQ + g * kQBytes + (kk >> 2) * kQSub)) + (uint64_t)((kk & 3) * 2);
+              const uint64_t bd = smem_desc_sw128(smem_u32(sK + s * kKVBytes + (kk >> 2) * kKVSub)) + (uint64_t)((kk & 3) * 2);
+              tc_mma_bf16(tmem + (2 * g + (j & 1)) * kBK, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(s_full(g, j & 1));
           }
           issued_any = true;
-          tc_commit(s_full(s));
         }
         if (j >= 1) {
-          const int jj = j - 1, s = jj & 1;
-          if (!mbar_wait(p_ready, jj & 1, budget, abort_flag)) {
-            failed = true;
-            break;
-          }
-          tc_fence_after();
+          const int jj = j - 1, s = jj % kStages;
 #pragma unroll
-          for (int kk = 0; kk < kBKeys / 16; ++kk) {
-            const uint64_t a = smem_desc_sw128(smem_u32(sP + (kk >> 2) * kSub)) + (uint64_t)((kk & 3) * 2);
-            const uint64_t bd = smem_desc_sw128_mn(smem_u32(sV + s * kTile + kk * 16 * 128), kSub, 1024);
-            tc_mma_bf16(tmem + 2 * kBKeys, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+          for (int g = 0; g < kSlots; ++g) {
+            if (!mbar_wait(p_ready(g), jj & 1, budget, abort_flag)) {
+              failed = true;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t a = smem_desc_sw128(smem_u32(sP + g * kPBytes)) + (uint64_t)(kk * 2);
+              const uint64_t bd = smem_desc_sw128_mn(smem_u32(sV + s * kKVBytes + kk * 16 * 128), kKVSub, 1024);
+              tc_mma_bf16(tmem + 256 + g * kD, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(pv_done(g));
           }
-          tc_commit(pv_done);
+          if (failed) break;
           tc_commit(kv_empty(s));
         }
       }
@@ -239,54 +293,50 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       }
     }
   } else {
-    // ---------------- softmax / correction / epilogue: one query row per thread
+    // ---------------- softmax / correction / epilogue: slot g, one query row per thread
+    const int g = (warp - 2) / 4;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
+    const Slot me = g == 0 ? sl[0] : sl[1];  // a select, not a run-time index into local memory
+    const int m0 = me.m0;
     const int qi = m0 + r;
+    const int qc = min(qi, p.T - 1);
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t o_taddr = tmem + lane_off + 2 * kBKeys;
+    const uint32_t o_taddr = tmem + lane_off + 256 + g * kD;
+    uint8_t* my_p = sP + g * kPBytes;
     float m_ref = -INFINITY, l = 0.f;
     bool failed = false;
     for (int j = 0; j < n_tiles; ++j) {
-      const int s = j & 1;
+      const int buf = j & 1;
       // warp-uniform: every lane waits, the warp gives up together
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full(s), (j >> 1) & 1, budget, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full(g, buf), (j >> 1) & 1, budget, abort_flag))) {
         failed = true;
         break;
       }
       __syncwarp();
       tc_fence_after();
-      float x[kBKeys];
+      float x[kBK];
 #pragma unroll
-      for (int c = 0; c < kBKeys; c += 16) tmem_ld16(tmem + lane_off + s * kBKeys + c, *reinterpret_cast<float(*)[16]>(&x[c]));
+      for (int c = 0; c < kBK; c += 16)
+        tmem_ld16(tmem + lane_off + (2 * g + buf) * kBK + c, *reinterpret_cast<float(*)[16]>(&x[c]));
       tc_wait_ld();
-      const int n0 = (t0 + j) * kBKeys;
-      // raw scores: masked entries become -inf (only tiles on the diagonal, past the last key
-      // or, with a window, before the last query's oldest key)
-      const int qc = min(qi, p.T - 1);
-      if ((n0 + kBKeys - 1 > off + m0) || (n0 + kBKeys > kv_hi) || n0 < kv_lo ||
+      const int n0 = (t0 + j) * kBK;
+      // raw scores: masked entries become -inf (tiles on the diagonal, past the last key,
+      // before the first visible key, or before the window)
+      if ((n0 + kBK - 1 > off + m0) || (n0 + kBK > kv_hi) || n0 < kv_lo ||
           (p.window > 0 && n0 < off + min(m0 + kBQ - 1, p.T - 1) - p.window + 1)) {
         const int causal = off + qc - n0;                    // keys n0 + c with c <= causal are not ahead
         const int lim = min(causal, kv_hi - 1 - n0);         // ... nor padding after the run
-        const int first = max(p.window > 0 ? causal - p.window + 1 : -kBKeys, kv_lo - n0);  // c >= first
+        const int first = max(p.window > 0 ? causal - p.window + 1 : -kBK, kv_lo - n0);  // c >= first
 #pragma unroll
-        for (int c = 0; c < kBKeys; ++c)
+        for (int c = 0; c < kBK; ++c)
           if (c > lim || c < first) x[c] = -INFINITY;
-      }
-      if (n0 + kBKeys > n_keys && r >= n_keys - n0) {
-        // V rows past the last key may hold anything (unused cache slots): zero them, so that
-        // P = 0 meets finite values in the PV product (the fence below orders this for the MMA)
-        uint8_t* vrow = sV + s * kTile + r * 128;
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-          for (int c16 = 0; c16 < 8; ++c16) *reinterpret_cast<uint4*>(vrow + hb * kSub + c16 * 16) = make_uint4(0, 0, 0, 0);
       }
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = x[i];
 #pragma unroll
-      for (int c = 8; c < kBKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+      for (int c = 8; c < kBK; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
       const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float mt = mraw * p.sl2;  // the scale is positive: the max commutes with it
@@ -298,18 +348,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         m_ref = mt;
       }
       const float neg_mu = m_ref == -INFINITY ? 0.f : -m_ref;
-      uint32_t pk[kBKeys / 2];
+      uint32_t pk[kBK / 2];
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kBKeys; c += 2) {
+      for (int c = 0; c < kBK; c += 2) {
         const float p0 = ex2_approx(fmaf(x[c], p.sl2, neg_mu));
         const float p1 = ex2_approx(fmaf(x[c + 1], p.sl2, neg_mu));
         ls[(c >> 1) & 3] += p0 + p1;
         pk[c / 2] = pack2(p0, p1, F16);
       }
       l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-      if (j >= 1) {  // P buffer and O are free once PV_{j-1} is done
-        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, budget, abort_flag))) {
+      if (j >= 1) {  // the slot's P buffer and O are free once its PV_{j-1} is done
+        if (!__all_sync(0xffffffffu, mbar_wait(pv_done(g), (j - 1) & 1, budget, abort_flag))) {
           failed = true;
           break;
         }
@@ -328,28 +378,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           tc_wait_st();
         }
       }
-      // P row r: two 64-key sub-tiles, 128-byte rows, 16-byte chunks XOR-swizzled by (r & 7)
+      if (g == 0 && r < kBK && n0 + kBK > n_keys && r >= n_keys - n0) {
+        // V rows past the item's last key may hold anything (unused cache slots): zero them,
+        // so that P = 0 meets finite values in both slots' PV products (the fence below
+        // orders this before slot 0's p_ready, and slot 1's PV is issued after slot 0's)
+        uint8_t* vrow = sV + (j % kStages) * kKVBytes + r * 128;
 #pragma unroll
-      for (int ch = 0; ch < kBKeys / 8; ++ch) {
-        const int sub = ch >> 3, c8 = ch & 7;
-        uint4 val = make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-        *reinterpret_cast<uint4*>(sP + sub * kSub + r * 128 + ((c8 ^ (r & 7)) << 4)) = val;
+        for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16) *reinterpret_cast<uint4*>(vrow + hb * kKVSub + c16 * 16) = make_uint4(0, 0, 0, 0);
+      }
+      // P row r: one 64-key tile, 128-byte rows, 16-byte chunks XOR-swizzled by (r & 7)
+#pragma unroll
+      for (int c8 = 0; c8 < kBK / 8; ++c8) {
+        uint4 val = make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
+        *reinterpret_cast<uint4*>(my_p + r * 128 + ((c8 ^ (r & 7)) << 4)) = val;
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_ready);
+      mbar_arrive(p_ready(g));
     }
     if (!failed && n_tiles > 0) {
-      if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (n_tiles - 1) & 1, budget, abort_flag))) failed = true;
+      if (!__all_sync(0xffffffffu, mbar_wait(pv_done(g), (n_tiles - 1) & 1, budget, abort_flag))) failed = true;
     }
     if (!failed) {
       __syncwarp();
       tc_fence_after();
       const bool seen = l > 0.f;  // false: a padding query that sees no key (its output is 0)
       const float inv = seen ? 1.f / l : 0.f;
-      const size_t orow_i = (((size_t)b * p.T + qi) * p.H + h) * kD;
+      const size_t orow_i = (((size_t)b * p.T + qi) * p.H + me.h) * kD;
       uint16_t* orow = static_cast<uint16_t*>(p.o) + orow_i;
       const bool of16 = p.o_f16 != 0;
+      const bool store = me.valid && qi < p.T;
       auto pack16 = [](const float (&v)[16], bool f16, uint4& w0, uint4& w1) {
         w0 = make_uint4(pack2(v[0], v[1], f16), pack2(v[2], v[3], f16), pack2(v[4], v[5], f16),
                         pack2(v[6], v[7], f16));
@@ -361,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         float ov[16];
         tmem_ld16(o_taddr + c, ov);
         tc_wait_ld();
-        if (qi < p.T) {
+        if (store) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) ov[i] = seen ? ov[i] * inv : 0.f;
           uint4 w0, w1;
@@ -420,8 +480,8 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
   AttnParams p;
   memset(static_cast<void*>(&p), 0, sizeof(p));
   if (!make_tma_2d_16b(&p.tq, q, B * H * T, kD, kBQ, f16) ||
-      !make_tma_2d_16b(&p.tk, k, B * Hkv * kv_stride, kD, kBKeys, f16) ||
-      !make_tma_2d_16b(&p.tv, v, B * Hkv * kv_stride, kD, kBKeys, f16)) {
+      !make_tma_2d_16b(&p.tk, k, B * Hkv * kv_stride, kD, kBK, f16) ||
+      !make_tma_2d_16b(&p.tv, v, B * Hkv * kv_stride, kD, kBK, f16)) {
     *why = "cuTensorMapEncodeTiled failed for q/k/v";
     return cudaErrorInvalidValue;
   }
@@ -438,6 +498,8 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
   p.gate = static_cast<const __half*>(opt.gate);
   p.ungated = static_cast<__nv_bfloat16*>(opt.ungated);
   p.n_qtiles = (T + kBQ - 1) / kBQ;
+  p.head_pairs = (H / Hkv) % 2 == 0 ? 1 : 0;
+  p.n_items = p.head_pairs ? B * (H / 2) * p.n_qtiles : B * H * ((p.n_qtiles + 1) / 2);
   p.sl2 = kLog2e / sqrtf((float)kD);
   p.status = st;
   p.wait_ns = wait_ns;
@@ -449,9 +511,9 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
     configured[f16] = true;
   }
   if (f16)
-    launch_pdl(attn_tc_kernel<true>, p.n_qtiles * H * B, kThreads, kSmem, s, p);
+    launch_pdl(attn_tc_kernel<true>, p.n_items, kThreads, kSmem, s, p);
   else
-    launch_pdl(attn_tc_kernel<false>, p.n_qtiles * H * B, kThreads, kSmem, s, p);
+    launch_pdl(attn_tc_kernel<false>, p.n_items, kThreads, kSmem, s, p);
   return cudaGetLastError();
 }
 
