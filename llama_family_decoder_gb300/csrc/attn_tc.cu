@@ -7,21 +7,24 @@
 // query heads of one KV group at the same query tile (an even group size), or
 // two consecutive query tiles of one head (otherwise); heaviest items first.
 // 320 threads:
-//   warp 0      TMA producer: both slots' Q tiles once, then K and V tiles of 64
-//               keys through a 3-stage ring (128-byte swizzle, 64-column boxes).
+//   warp 0      TMA producers: lane 0 both slots' Q tiles once, then K tiles of
+//               128 keys through a 2-stage ring; lane 1 the V tiles through one
+//               stage (128-byte swizzle, 64-column boxes).
 //   warp 1      TMEM allocation; lane 0 issues S = Q K_j^T for both slots (M=128,
-//               N=64, K=16 x 8) into each slot's pair of TMEM score buffers, and
-//               O += P_j V_j (A = P from shared memory, B = V as an MN-major
-//               operand) into each slot's TMEM output accumulator.
+//               N=128, K=16 x 8) into each slot's TMEM score buffer as soon as the
+//               slot's softmax has read the previous scores, and O += P_j V_j (A = P
+//               from shared memory, B = V as an MN-major operand) into each slot's
+//               TMEM output accumulator as soon as P_j is written.
 //   warps 2..9  softmax, four warps per slot, one query row per thread: read S_j
 //               from TMEM, mask, exponentiate in the log2 domain against a running
 //               reference max, write P_j (swizzled K-major) to the slot's shared
 //               buffer; rescale O in TMEM only when the row max grew by more than
 //               2^8 (exact: softmax does not depend on the reference); finally
 //               O / l to the head-major output.
-// The tensor pipe interleaves the slots: S_{j+1} of both slots and PV_j of one
-// run while the softmax warps work on the other. Sharing K/V halves its traffic
-// per FLOP.
+// S_{j+1} runs on the tensor pipe while the softmax works on S_j, PV_j while it
+// starts on S_{j+1}. Sharing K/V halves its traffic per FLOP; 128-key tiles keep
+// both MMAs at N = 128, where their shared-memory operand reads keep up with the
+// tensor pipe.
 // Options of the "afmoe" block ("Rotary runs on the sliding-window blocks only";
 // "Attention: per-head q/k norms and a sigmoid gate on every head"): a window
 // over the last W positions (key tiles before the first query's oldest key are
@@ -40,16 +43,17 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kBQ = 128;                    // queries per slot (MMA M)
-constexpr int kBK = 64;                     // keys per tile
+constexpr int kBK = 128;                    // keys per tile
 constexpr int kSlots = 2;
 constexpr int kThreads = 64 + kSlots * 128;
 constexpr int kQSub = kBQ * 128;            // one 64-column half of a Q tile (bytes)
 constexpr int kQBytes = 2 * kQSub;          // 128 queries x 128 dims
 constexpr int kKVSub = kBK * 128;           // one 64-column half of a K or V tile
-constexpr int kKVBytes = 2 * kKVSub;        // 64 keys x 128 dims
-constexpr int kPBytes = kBQ * 128;          // 128 queries x 64 keys, one swizzled tile
-constexpr int kStages = 3;
-constexpr int kSmem = 1024 + kSlots * kQBytes + kStages * 2 * kKVBytes + kSlots * kPBytes + 256;
+constexpr int kKVBytes = 2 * kKVSub;        // 128 keys x 128 dims
+constexpr int kPSub = kBQ * 128;            // one 64-key half of a P tile
+constexpr int kPBytes = 2 * kPSub;          // 128 queries x 128 keys
+constexpr int kKStages = 2;                 // K ring; V has one stage
+constexpr int kSmem = 1024 + kSlots * kQBytes + (kKStages + 1) * kKVBytes + kSlots * kPBytes + 256;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr unsigned long long kDrainNs = 2000000000ULL;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -103,17 +107,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                                   // [slot]: two 64-column halves of 16 KB
-  uint8_t* sK = sQ + kSlots * kQBytes;                  // [stage]: two halves of 8 KB
-  uint8_t* sV = sK + kStages * kKVBytes;
-  uint8_t* sP = sV + kStages * kKVBytes;                // [slot]: 16 KB
+  uint8_t* sK = sQ + kSlots * kQBytes;                  // [stage]: two halves of 16 KB
+  uint8_t* sV = sK + kKStages * kKVBytes;               // one tile
+  uint8_t* sP = sV + kKVBytes;                          // [slot]: two 64-key halves of 16 KB
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kSlots * kPBytes);
-  // q_full, kv_full[3], kv_empty[3], s_full[2][2], p_ready[2], pv_done[2], drain
+  // q_full, k_full[2], k_empty[2], v_full, v_empty, s_full[2], s_free[2], p_ready[2], pv_done[2], drain
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const uint32_t q_full = smem_u32(&bars[0]);
-  auto kv_full = [&](int s) { return smem_u32(&bars[1 + s]); };
-  auto kv_empty = [&](int s) { return smem_u32(&bars[4 + s]); };
-  auto s_full = [&](int g, int b) { return smem_u32(&bars[7 + 2 * g + b]); };
+  auto k_full = [&](int s) { return smem_u32(&bars[1 + s]); };
+  auto k_empty = [&](int s) { return smem_u32(&bars[3 + s]); };
+  const uint32_t v_full = smem_u32(&bars[5]);
+  const uint32_t v_empty = smem_u32(&bars[6]);
+  auto s_full = [&](int g) { return smem_u32(&bars[7 + g]); };
+  auto s_free = [&](int g) { return smem_u32(&bars[9 + g]); };
   auto p_ready = [&](int g) { return smem_u32(&bars[11 + g]); };
   auto pv_done = [&](int g) { return smem_u32(&bars[13 + g]); };
   const uint32_t drain = smem_u32(&bars[15]);
@@ -150,13 +157,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
     }
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
     for (int g = 0; g < kSlots; ++g) {
-      mbar_init(s_full(g, 0), 1);
-      mbar_init(s_full(g, 1), 1);
+      mbar_init(s_full(g), 1);
+      mbar_init(s_free(g), 128);
       mbar_init(p_ready(g), 128);
       mbar_init(pv_done(g), 1);
     }
@@ -177,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   pdl_wait();  // q, k, v (and the cache positions, the key ranges) come from earlier kernels
-  const uint32_t tmem = *tmem_holder;  // S[g][buf]: cols (2g + buf) * 64; O[g]: 256 + 128 g
+  const uint32_t tmem = *tmem_holder;  // S[g]: cols 128 g; O[g]: 256 + 128 g
   const int off = p.q_off ? p.q_off[b] : 0;  // keys 0 .. off - 1 are earlier positions in the cache
   // visible keys: [kv_lo, kv_hi) (an attention_mask's run of real tokens, else all)
   const int2 kr = p.key_range ? p.key_range[b] : make_int2(0, off + p.T);
@@ -195,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer: Q, then the K ring
       bool failed = false;
       uint32_t issued = 0, parity = 0;
       mbar_arrive_expect_tx(q_full, kSlots * kQBytes);
@@ -206,18 +215,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         tma_load_2d(smem_u32(sQ + g * kQBytes + kQSub), &p.tq, 64, q_row, q_full);
       }
       for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        if (!mbar_wait(kv_empty(s), ph ^ 1, budget, abort_flag)) {
+        const int s = j % kKStages;
+        const uint32_t ph = (j / kKStages) & 1;
+        if (!mbar_wait(k_empty(s), ph ^ 1, budget, abort_flag)) {
           failed = true;
           break;
         }
-        mbar_arrive_expect_tx(kv_full(s), 2 * kKVBytes);
+        mbar_arrive_expect_tx(k_full(s), kKVBytes);
         const int row = kv_row + (t0 + j) * kBK;
-        tma_load_2d(smem_u32(sK + s * kKVBytes), &p.tk, 0, row, kv_full(s));
-        tma_load_2d(smem_u32(sK + s * kKVBytes + kKVSub), &p.tk, 64, row, kv_full(s));
-        tma_load_2d(smem_u32(sV + s * kKVBytes), &p.tv, 0, row, kv_full(s));
-        tma_load_2d(smem_u32(sV + s * kKVBytes + kKVSub), &p.tv, 64, row, kv_full(s));
+        tma_load_2d(smem_u32(sK + s * kKVBytes), &p.tk, 0, row, k_full(s));
+        tma_load_2d(smem_u32(sK + s * kKVBytes + kKVSub), &p.tk, 64, row, k_full(s));
         issued |= 1u << s;
         parity = (parity & ~(1u << s)) | (ph << s);
       }
@@ -226,8 +233,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         report_timeout(p.status, 0x20 + 0);
         volatile int never = 0;
         mbar_wait(q_full, 0, kDrainNs, &never);
-        for (int s = 0; s < kStages; ++s)
-          if (issued & (1u << s)) mbar_wait(kv_full(s), (parity >> s) & 1, kDrainNs, &never);
+        for (int s = 0; s < kKStages; ++s)
+          if (issued & (1u << s)) mbar_wait(k_full(s), (parity >> s) & 1, kDrainNs, &never);
+      }
+    } else if (lane == 1) {
+      // ---------------- TMA producer: the V stage (its own thread, so that K never waits behind V)
+      bool failed = false, issued = false;
+      uint32_t last = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        if (!mbar_wait(v_empty, (j & 1) ^ 1, budget, abort_flag)) {
+          failed = true;
+          break;
+        }
+        mbar_arrive_expect_tx(v_full, kKVBytes);
+        const int row = kv_row + (t0 + j) * kBK;
+        tma_load_2d(smem_u32(sV), &p.tv, 0, row, v_full);
+        tma_load_2d(smem_u32(sV + kKVSub), &p.tv, 64, row, v_full);
+        issued = true;
+        last = j & 1;
+      }
+      if (failed) {
+        *abort_flag = 1;
+        report_timeout(p.status, 0x20 + 3);
+        volatile int never = 0;
+        if (issued) mbar_wait(v_full, last, kDrainNs, &never);
       }
     }
   } else if (warp == 1) {
@@ -239,48 +268,66 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       constexpr uint32_t idesc_pv = (idesc_bf16_f32(kBQ, kD) & fmt_clear) | (1u << 16);  // B (V) is MN-major
       bool failed = !mbar_wait(q_full, 0, budget, abort_flag);
       bool issued_any = false;
-      for (int j = 0; j <= n_tiles && !failed; ++j) {
-        if (j < n_tiles) {
-          const int s = j % kStages;
-          if (!mbar_wait(kv_full(s), (j / kStages) & 1, budget, abort_flag)) {
+      auto issue_s = [&](int g, int j) {  // S_j of slot g into its score buffer
+        const int s = j % kKStages;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t a = smem_desc_sw128(smem_u32(sQ + g * kQBytes + (kk >> 2) * kQSub)) + (uint64_t)((kk & 3) * 2);
+          const uint64_t bd = smem_desc_sw128(smem_u32(sK + s * kKVBytes + (kk >> 2) * kKVSub)) + (uint64_t)((kk & 3) * 2);
+          tc_mma_bf16(tmem + g * kBK, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full(g));
+        issued_any = true;
+      };
+      if (!failed && n_tiles > 0) {
+        if (!mbar_wait(k_full(0), 0, budget, abort_flag)) {
+          failed = true;
+        } else {
+          tc_fence_after();
+          for (int g = 0; g < kSlots; ++g) issue_s(g, 0);
+          tc_commit(k_empty(0));
+        }
+      }
+      for (int j = 0; j < n_tiles && !failed; ++j) {
+        if (j + 1 < n_tiles) {
+          // S_{j+1}: each slot's buffer is free once its softmax has read S_j
+          const int s = (j + 1) % kKStages;
+          if (!mbar_wait(k_full(s), ((j + 1) / kKStages) & 1, budget, abort_flag)) {
             failed = true;
             break;
           }
-          tc_fence_after();
-          // S_j of both slots (each slot's buffer j & 1 was read by its softmax of tile j - 2,
-          // which this thread waited for before PV_{j-2})
-#pragma unroll
           for (int g = 0; g < kSlots; ++g) {
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint64_t a = smem_desc_sw128(smem_u32(sQ + g * kQBytes + (kk >> 2) * kQSub)) + (uint64_t)((kk & 3) * 2);
-              const uint64_t bd = smem_desc_sw128(smem_u32(sK + s * kKVBytes + (kk >> 2) * kKVSub)) + (uint64_t)((kk & 3) * 2);
-              tc_mma_bf16(tmem + (2 * g + (j & 1)) * kBK, a, bd, idesc_s, kk > 0 ? 1u : 0u);
-            }
-            tc_commit(s_full(g, j & 1));
-          }
-          issued_any = true;
-        }
-        if (j >= 1) {
-          const int jj = j - 1, s = jj % kStages;
-#pragma unroll
-          for (int g = 0; g < kSlots; ++g) {
-            if (!mbar_wait(p_ready(g), jj & 1, budget, abort_flag)) {
+            if (!mbar_wait(s_free(g), j & 1, budget, abort_flag)) {
               failed = true;
               break;
             }
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              const uint64_t a = smem_desc_sw128(smem_u32(sP + g * kPBytes)) + (uint64_t)(kk * 2);
-              const uint64_t bd = smem_desc_sw128_mn(smem_u32(sV + s * kKVBytes + kk * 16 * 128), kKVSub, 1024);
-              tc_mma_bf16(tmem + 256 + g * kD, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
-            }
-            tc_commit(pv_done(g));
+            issue_s(g, j + 1);
           }
           if (failed) break;
-          tc_commit(kv_empty(s));
+          tc_commit(k_empty(s));
         }
+        // PV_j of each slot as soon as its P_j is written
+        if (!mbar_wait(v_full, j & 1, budget, abort_flag)) {
+          failed = true;
+          break;
+        }
+        for (int g = 0; g < kSlots; ++g) {
+          if (!mbar_wait(p_ready(g), j & 1, budget, abort_flag)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t a = smem_desc_sw128(smem_u32(sP + g * kPBytes + (kk >> 2) * kPSub)) + (uint64_t)((kk & 3) * 2);
+            const uint64_t bd = smem_desc_sw128_mn(smem_u32(sV + kk * 16 * 128), kKVSub, 1024);
+            tc_mma_bf16(tmem + 256 + g * kD, a, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(pv_done(g));
+        }
+        if (failed) break;
+        tc_commit(v_empty);
       }
       if (failed) {
         *abort_flag = 1;
@@ -307,9 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     float m_ref = -INFINITY, l = 0.f;
     bool failed = false;
     for (int j = 0; j < n_tiles; ++j) {
-      const int buf = j & 1;
       // warp-uniform: every lane waits, the warp gives up together
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full(g, buf), (j >> 1) & 1, budget, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full(g), j & 1, budget, abort_flag))) {
         failed = true;
         break;
       }
@@ -318,8 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       float x[kBK];
 #pragma unroll
       for (int c = 0; c < kBK; c += 16)
-        tmem_ld16(tmem + lane_off + (2 * g + buf) * kBK + c, *reinterpret_cast<float(*)[16]>(&x[c]));
+        tmem_ld16(tmem + lane_off + g * kBK + c, *reinterpret_cast<float(*)[16]>(&x[c]));
       tc_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free(g));  // the score buffer may now take S_{j+1}
       const int n0 = (t0 + j) * kBK;
       // raw scores: masked entries become -inf (tiles on the diagonal, past the last key,
       // before the first visible key, or before the window)
@@ -348,16 +396,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         m_ref = mt;
       }
       const float neg_mu = m_ref == -INFINITY ? 0.f : -m_ref;
-      uint32_t pk[kBK / 2];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < kBK; c += 2) {
-        const float p0 = ex2_approx(fmaf(x[c], p.sl2, neg_mu));
-        const float p1 = ex2_approx(fmaf(x[c + 1], p.sl2, neg_mu));
-        ls[(c >> 1) & 3] += p0 + p1;
-        pk[c / 2] = pack2(p0, p1, F16);
-      }
-      l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       if (j >= 1) {  // the slot's P buffer and O are free once its PV_{j-1} is done
         if (!__all_sync(0xffffffffu, mbar_wait(pv_done(g), (j - 1) & 1, budget, abort_flag))) {
           failed = true;
@@ -378,22 +416,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           tc_wait_st();
         }
       }
-      if (g == 0 && r < kBK && n0 + kBK > n_keys && r >= n_keys - n0) {
+      if (g == 0 && n0 + kBK > n_keys) {
         // V rows past the item's last key may hold anything (unused cache slots): zero them,
-        // so that P = 0 meets finite values in both slots' PV products (the fence below
-        // orders this before slot 0's p_ready, and slot 1's PV is issued after slot 0's)
-        uint8_t* vrow = sV + (j % kStages) * kKVBytes + r * 128;
+        // so that P = 0 meets finite values in both slots' PV products, once the tile has
+        // landed (the fence below orders this before slot 0's p_ready; slot 1's PV is
+        // issued after slot 0's)
+        if (!__all_sync(0xffffffffu, mbar_wait(v_full, j & 1, budget, abort_flag))) {
+          failed = true;
+          break;
+        }
+        if (r >= n_keys - n0) {
+          uint8_t* vrow = sV + r * 128;
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb)
+          for (int hb = 0; hb < 2; ++hb)
 #pragma unroll
-          for (int c16 = 0; c16 < 8; ++c16) *reinterpret_cast<uint4*>(vrow + hb * kKVSub + c16 * 16) = make_uint4(0, 0, 0, 0);
+            for (int c16 = 0; c16 < 8; ++c16) *reinterpret_cast<uint4*>(vrow + hb * kKVSub + c16 * 16) = make_uint4(0, 0, 0, 0);
+        }
       }
-      // P row r: one 64-key tile, 128-byte rows, 16-byte chunks XOR-swizzled by (r & 7)
+      // P row r straight to shared memory: two 64-key halves, 128-byte rows, 16-byte chunks
+      // XOR-swizzled by (r & 7)
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c8 = 0; c8 < kBK / 8; ++c8) {
-        uint4 val = make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
-        *reinterpret_cast<uint4*>(my_p + r * 128 + ((c8 ^ (r & 7)) << 4)) = val;
+      for (int ch = 0; ch < kBK / 8; ++ch) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = ch * 8 + 2 * i;
+          const float p0 = ex2_approx(fmaf(x[c], p.sl2, neg_mu));
+          const float p1 = ex2_approx(fmaf(x[c + 1], p.sl2, neg_mu));
+          ls[i] += p0 + p1;
+          w[i] = pack2(p0, p1, F16);
+        }
+        const int sub = ch >> 3, c8 = ch & 7;
+        *reinterpret_cast<uint4*>(my_p + sub * kPSub + r * 128 + ((c8 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
+      l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_ready(g));
