@@ -338,14 +338,14 @@ void blk_xielu_effective(float raw_alpha_p, float raw_alpha_n, float beta, float
  * [B, 1, H, 128]); k, v [B, Hkv, kv_stride, 128]; kv_lens device int[B] with
  * 1 <= kv_lens[b] <= kv_stride; all bf16 device pointers, 16-byte aligned.
  *
- * Its per-split partial results live in one file-scope 16 MiB device array
- * that every GPU loading the library holds until exit. The limit is
- * batch * n_heads * (head_dim + 2) * 4 bytes <= 16 MiB (e.g. 64 x 32 heads);
- * larger calls return BLK_ERR_UNSUPPORTED with that reason. Every call shares
- * the array and it keeps the last call's contents; every value a call reads
- * from it is written earlier in the same call, so nothing needs clearing, but
- * calls that overlap on the GPU (other streams, other host threads) race on
- * it and must be serialised by the caller. The first call on a device looks up
+ * Its per-split partial results and its work counter live in one file-scope
+ * 16 MiB device array that every GPU loading the library holds until exit. The
+ * limit is batch * n_heads * (head_dim + 2) * 4 bytes <= 16 MiB - 256 (e.g.
+ * 64 x 32 heads); larger calls return BLK_ERR_UNSUPPORTED with that reason.
+ * Every call shares the array and it keeps the last call's contents; each call
+ * zeroes the counter (cudaMemsetAsync on `stream`) and writes every partial it
+ * reads, but calls that overlap on the GPU (other streams, other host threads)
+ * race on it and must be serialised by the caller. The first call on a device looks up
  * the array's device address (cudaGetSymbolAddress, with that device current);
  * make that first call before any stream capture. It calls no cudaMalloc,
  * cudaFree or allocating library routine.

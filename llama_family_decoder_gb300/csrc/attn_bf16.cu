@@ -14,6 +14,7 @@
 // sliding window the splits cover only the last `window` keys.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -55,7 +56,8 @@ constexpr int kStageBytes = 4 * kHalfBytes;      // K and V, two halves each (32
 constexpr int kCompute = 4;                      // compute warps; warp 4 is the TMA producer
 constexpr int kThreads = (kCompute + 1) * 32;
 constexpr int kMergeFloats = 2 * 64 + kCompute * 16 * kD;
-constexpr int kSmem = 1024 + kStages * kStageBytes + kMergeFloats * 4 + 128;
+constexpr int kUq = 4;  // units handed from the producer to the compute warps, in flight
+constexpr int kSmem = 1024 + kStages * kStageBytes + kMergeFloats * 4 + 256;
 constexpr unsigned long long kDrainNs = 2000000000ULL;
 
 struct DecodeParams {
@@ -64,7 +66,8 @@ struct DecodeParams {
   float* ws_ml;
   float* ws_o;
   const int* kv_lens;
-  int len_add, H, Hkv, kv_stride, chunk, splits, units;
+  int* work;  // units taken so far beyond the first round (zero at launch), or null: round robin
+  int len_add, B, H, Hkv, kv_stride, chunk, splits, units;
   int window;  // > 0: only the last `window` keys of each sequence
   DevStatus* status;
   unsigned long long wait_ns;
@@ -82,21 +85,27 @@ struct DecodeUnit {
 
 __device__ __forceinline__ DecodeUnit decode_unit(const DecodeParams& p, int u) {
   DecodeUnit r;
+  // the splits of one (sequence, KV head) are consecutive units: the CTAs working
+  // at the same time stream neighbouring stretches of the cache
   r.split = u % p.splits;
   r.kvh = (u / p.splits) % p.Hkv;
   r.b = u / (p.splits * p.Hkv);
   const int kv_len = min(p.kv_lens[r.b] + p.len_add, p.kv_stride);  // never read past the cache
   const int first = p.window > 0 ? max(0, kv_len - p.window) : 0;    // the oldest key in the window
   r.k0 = first + r.split * p.chunk;
-  r.n_keys = max(0, min(kv_len, r.k0 + p.chunk) - r.k0);
+  // the last split takes every key left (up to a chunk more): no unit of a handful of keys
+  const int end = r.split == p.splits - 1 ? kv_len : min(kv_len, r.k0 + p.chunk);
+  r.n_keys = max(0, end - r.k0);
   r.n_tiles = (r.n_keys + kTileKeys - 1) / kTileKeys;
   return r;
 }
 
-// Persistent split-KV decode attention: each CTA walks the units (sequence, KV
-// head, key split) blockIdx.x, blockIdx.x + gridDim.x, ...; its producer warp
-// streams every unit's K/V tiles through a 4-stage TMA ring without pausing
-// between units, and the 4 compute warps each own 16 keys of every tile.
+// Persistent split-KV decode attention: each CTA starts on unit blockIdx.x (a
+// sequence, a KV head, a key split) and takes its next ones from a shared
+// counter, so that CTAs the memory system serves faster take more; its producer
+// lane streams every unit's K/V tiles through a 4-stage TMA ring without pausing
+// between units and hands the unit indices to the 4 compute warps (a queue of
+// kUq, mbarriers both ways), which each own 16 keys of every tile.
 __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -104,11 +113,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
   uint8_t* ring = smem;
   float* merge = reinterpret_cast<float*>(ring + kStages * kStageBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(merge + kMergeFloats);
-  // full[kStages], empty[kStages], csync
+  // full[kStages], empty[kStages], csync, (abort flag), uq_full[kUq], uq_empty[kUq], unit ids[kUq]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages + 1);
   auto full = [&](int s) { return smem_u32(&bars[s]); };
   auto empty = [&](int s) { return smem_u32(&bars[kStages + s]); };
   const uint32_t csync = smem_u32(&bars[2 * kStages]);
+  auto uq_full = [&](int s) { return smem_u32(&bars[2 * kStages + 2 + s]); };
+  auto uq_empty = [&](int s) { return smem_u32(&bars[2 * kStages + 2 + kUq + s]); };
+  volatile int* unit_q = reinterpret_cast<volatile int*>(bars + 2 * kStages + 2 + 2 * kUq);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.H / p.Hkv;
   const unsigned long long budget = p.wait_ns;
@@ -119,6 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
       mbar_init(empty(st), kCompute);
     }
     mbar_init(csync, kCompute * 32);
+    for (int i = 0; i < kUq; ++i) {
+      mbar_init(uq_full(i), 1);
+      mbar_init(uq_empty(i), kCompute);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -134,7 +150,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
       uint32_t ph = 0, issued = 0, parity = 0;
       bool failed = false;
       const uint64_t stream_once = l2_policy_evict_first();  // the cache is read once per step
-      for (int u = blockIdx.x; u < p.units && !failed; u += gridDim.x) {
+      int u = blockIdx.x;
+      for (int k = 0; !failed; ++k) {
+        // hand unit u (p.units or more: none left) to the compute warps
+        const int slot = k % kUq;
+        if (!mbar_wait(uq_empty(slot), ((k / kUq) & 1) ^ 1, budget, abort_flag)) {
+          failed = true;
+          break;
+        }
+        unit_q[slot] = u;
+        mbar_arrive(uq_full(slot));
+        if (u >= p.units) break;
+        // the next unit, asked for now: the answer is needed only after this unit's tiles
+        const int next = p.work ? atomicAdd(p.work, 1) + (int)gridDim.x : u + (int)gridDim.x;
         const DecodeUnit un = decode_unit(p, u);
         const int row0 = (un.b * p.Hkv + un.kvh) * p.kv_stride + un.k0;
         for (int t = 0; t < un.n_tiles; ++t) {
@@ -156,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
             ph ^= 1;
           }
         }
+        u = next;
       }
       if (failed) {
         *abort_flag = 1;
@@ -180,7 +209,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
     ++n_sync;
     return ok;
   };
-  for (int u = blockIdx.x; u < p.units && !failed; u += gridDim.x) {
+  for (int k = 0; !failed; ++k) {
+    const int slot = k % kUq;
+    if (!__all_sync(0xffffffffu, mbar_wait(uq_full(slot), (k / kUq) & 1, budget, abort_flag))) {
+      failed = true;
+      break;
+    }
+    const int u = unit_q[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(uq_empty(slot));
+    if (u >= p.units) break;
     const DecodeUnit un = decode_unit(p, u);
     // Q fragments straight from global memory: rows = the group's heads (zero past G)
     const __nv_bfloat16* qg = p.q + ((size_t)un.b * p.H + (size_t)un.kvh * G) * kD;
@@ -336,51 +374,99 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
   }
 }
 
-// gate (fp16, o's layout) multiplies the result; ungated (bf16) receives it before the gate;
-// o is fp16 when o_f16 (the operand of an o_proj on prepared fp16 weights), else bf16.
-__global__ void attn_decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__ ws_o,
-                                           void* __restrict__ o, int H, int splits,
-                                           const __half* __restrict__ gate, __nv_bfloat16* __restrict__ ungated,
-                                           int o_f16) {
+// Merge of the KV splits. One warp per (sequence, head), four channels a lane;
+// one 256-thread block per SM with at most 128 registers a thread, so that the
+// o_proj GEMM's CTA fits beside it and streams its first weight stages while
+// the merge runs. gate (fp16, o's layout) multiplies the result; ungated (bf16)
+// receives it before the gate; o is fp16 when o_f16 (the operand of an o_proj
+// on prepared fp16 weights), else bf16.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineBatch = 8;  // splits whose loads are issued together
+
+__global__ void __launch_bounds__(kCombineThreads, 2)
+    attn_decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__ ws_o, void* __restrict__ o,
+                               int pairs, int splits, const __half* __restrict__ gate,
+                               __nv_bfloat16* __restrict__ ungated, int o_f16) {
   pdl_launch_dependents();
   pdl_wait();
-  const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
-  const size_t base = ((size_t)b * H + h) * splits;
-  float m = -INFINITY;
-  for (int s = 0; s < splits; ++s) m = fmaxf(m, ws_ml[(base + s) * 2]);
-  const float mu = m == -INFINITY ? 0.f : m;
-  float l = 0.f, acc = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const float f = exp2f(ws_ml[(base + s) * 2] - mu);
-    l += ws_ml[(base + s) * 2 + 1] * f;
-    acc += ws_o[(base + s) * kD + c] * f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = kCombineThreads / 32;
+  for (int pr = blockIdx.x * kWarps + warp; pr < pairs; pr += gridDim.x * kWarps) {
+    const size_t base = (size_t)pr * splits;  // pr = b * H + h
+    // groups of kCombineBatch splits whose loads are all in flight together; a
+    // later group with a larger maximum rescales what the earlier ones summed
+    float m = -INFINITY, l = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < splits; s0 += kCombineBatch) {
+      float2 ml[kCombineBatch];
+      float4 ov[kCombineBatch];
+#pragma unroll
+      for (int j = 0; j < kCombineBatch; ++j) {
+        const bool in = s0 + j < splits;
+        ml[j] = in ? *reinterpret_cast<const float2*>(ws_ml + (base + s0 + j) * 2) : make_float2(-INFINITY, 0.f);
+        ov[j] = in ? *reinterpret_cast<const float4*>(ws_o + (base + s0 + j) * kD + 4 * lane)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float gm = m;
+#pragma unroll
+      for (int j = 0; j < kCombineBatch; ++j) gm = fmaxf(gm, ml[j].x);
+      const float mu = gm == -INFINITY ? 0.f : gm;
+      const float sc = exp2f(m - mu);  // 0 for the first group
+      l *= sc;
+      acc = make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+#pragma unroll
+      for (int j = 0; j < kCombineBatch; ++j) {
+        const float f = exp2f(ml[j].x - mu);
+        l += ml[j].y * f;
+        acc = make_float4(acc.x + ov[j].x * f, acc.y + ov[j].y * f, acc.z + ov[j].z * f, acc.w + ov[j].w * f);
+      }
+      m = gm;
+    }
+    const size_t i = (size_t)pr * kD + 4 * lane;
+    float r[4] = {acc.x / l, acc.y / l, acc.z / l, acc.w / l};
+    if (ungated) {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(r[0], r[1]), b = __floats2bfloat162_rn(r[2], r[3]);
+      *reinterpret_cast<uint2*>(ungated + i) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    }
+    if (gate) {
+      const uint2 gw = *reinterpret_cast<const uint2*>(gate + i);
+      const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&gw.x));
+      const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&gw.y));
+      r[0] *= g01.x;
+      r[1] *= g01.y;
+      r[2] *= g23.x;
+      r[3] *= g23.y;
+    }
+    uint2 ow;
+    if (o_f16) {
+      const __half2 a = __floats2half2_rn(r[0], r[1]), b = __floats2half2_rn(r[2], r[3]);
+      ow = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+      *reinterpret_cast<uint2*>(static_cast<__half*>(o) + i) = ow;
+    } else {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(r[0], r[1]), b = __floats2bfloat162_rn(r[2], r[3]);
+      ow = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o) + i) = ow;
+    }
   }
-  const size_t i = ((size_t)b * H + h) * kD + c;
-  float r = acc / l;
-  if (ungated) ungated[i] = __float2bfloat16_rn(r);
-  if (gate) r *= __half2float(gate[i]);
-  if (o_f16)
-    static_cast<__half*>(o)[i] = __float2half_rn(r);
-  else
-    static_cast<__nv_bfloat16*>(o)[i] = __float2bfloat16_rn(r);
 }
 
 }  // namespace
 
-// Splits of about 512 keys (8 tiles): fine-grained units that the persistent
-// CTAs share evenly.
+// Splits of 512 keys (8 tiles), the last one up to twice that: units that the
+// persistent CTAs take in turn from a shared counter. (Smaller splits shorten the
+// last round but add each unit's fixed cost: q fragments, merge, partial writes.)
 int attn_decode_splits(int B, int Hkv, int max_len, int num_sms) {
   (void)B;
   (void)Hkv;
   (void)num_sms;
-  int splits = (max_len + 511) / 512;
-  if (splits < 1) splits = 1;
-  if (splits > 64) splits = 64;
-  return splits;
+  return attn_decode_split_cap(max_len);
 }
 
+int attn_decode_split_cap(int max_len) { return std::min(64, std::max(1, max_len / 512)); }
+
 size_t attn_decode_ws_bytes(int B, int H, int d, int max_splits) {
-  return (size_t)B * H * max_splits * (2 + d) * sizeof(float);
+  return kAttnCounterBytes + (size_t)B * H * max_splits * (2 + d) * sizeof(float);
 }
 
 namespace {
@@ -404,13 +490,20 @@ cudaError_t decode_core(const void* q, const void* k, const void* v, void* o, in
   }
   // max_len: the most keys a sequence attends to (at most the window)
   if (opt.window > 0 && opt.window < max_len) max_len = opt.window;
-  int chunk = (max_len + splits - 1) / splits;
-  chunk = (chunk + kTileKeys - 1) / kTileKeys * kTileKeys;
+  // whole 64-key tiles per split; the last split also takes the remainder
+  const int chunk = std::max(kTileKeys, max_len / splits / kTileKeys * kTileKeys);
   p.q = static_cast<const __nv_bfloat16*>(q);
-  p.ws_ml = ws;
-  p.ws_o = ws + (size_t)B * H * splits * 2;
+  // the unit counter, then the partials
+  p.work = reinterpret_cast<int*>(ws);
+  if (!opt.counter_zeroed) {
+    cudaError_t e = cudaMemsetAsync(p.work, 0, sizeof(int), s);
+    if (e != cudaSuccess) return e;
+  }
+  p.ws_ml = ws + kAttnCounterBytes / sizeof(float);
+  p.ws_o = p.ws_ml + (size_t)B * H * splits * 2;
   p.kv_lens = kv_lens;
   p.len_add = len_add;
+  p.B = B;
   p.H = H;
   p.Hkv = Hkv;
   p.kv_stride = kv_stride;
@@ -424,7 +517,10 @@ cudaError_t decode_core(const void* q, const void* k, const void* v, void* o, in
   launch_pdl(attn_decode_kernel, grid, kThreads, kSmem, s, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  launch_pdl(attn_decode_combine_kernel, dim3(H, B), kD, 0, s, p.ws_ml, p.ws_o, o, H, splits,
+  const int pairs = B * H;
+  const int cwarps = kCombineThreads / 32;
+  const int cgrid = std::min(num_sms, (pairs + cwarps - 1) / cwarps);
+  launch_pdl(attn_decode_combine_kernel, cgrid, kCombineThreads, 0, s, p.ws_ml, p.ws_o, o, pairs, splits,
              static_cast<const __half*>(opt.gate), static_cast<__nv_bfloat16*>(opt.ungated), opt.o_f16 ? 1 : 0);
   return cudaGetLastError();
 }
@@ -497,7 +593,7 @@ cudaError_t launch_attn_decode_bf16_static(const void* q, const void* k, const v
   }
   if (B <= 0) return cudaSuccess;
   const size_t per_split = (size_t)B * H * (2 + d) * sizeof(float);
-  if (per_split > kDecodeStaticScratchBytes) {
+  if (per_split > kDecodeStaticScratchBytes - kAttnCounterBytes) {
     *why = "allocation-free decode attention: batch * n_heads * (head_dim + 2) * 4 bytes exceeds the 16 MiB scratch";
     return cudaErrorInvalidValue;
   }
@@ -508,9 +604,10 @@ cudaError_t launch_attn_decode_bf16_static(const void* q, const void* k, const v
     return e;
   }
   int splits = attn_decode_splits(B, Hkv, kv_stride, num_sms);
-  const int fit = (int)(kDecodeStaticScratchBytes / per_split);
+  const int fit = (int)((kDecodeStaticScratchBytes - kAttnCounterBytes) / per_split);
   if (splits > fit) splits = fit;
-  // every partial the combine step reads is written by this call first: nothing to clear
+  // every partial the combine step reads is written by this call first; the unit
+  // counter at the scratch's start is zeroed before the launch
   return decode_core(q, k, v, o, B, H, Hkv, kv_stride, kv_lens, 0, splits, kv_stride, scratch, num_sms, nullptr,
                      2000000000ULL, s, why, AttnOpts());
 }

@@ -178,7 +178,7 @@ Ws carve_forward(const blk_handle* h, void* base, int B, int T, bool decode, siz
   if (decode) {
     if (d.dtype == BLK_BF16) {
       w.C = c.take((size_t)kMaxDecodeSplits * M * max_cols(d) * sizeof(float));
-      const int s = attn_decode_splits(B, d.n_kv_heads, d.max_seq, h->num_sms);
+      const int s = attn_decode_split_cap(d.max_seq);
       w.attn = c.take(attn_decode_ws_bytes(B, d.n_heads, d.head_dim, s));
       w.ss2 = static_cast<float*>(c.take(M * norm_parts(d.hidden, 128) * sizeof(float)));
     } else {
@@ -365,6 +365,82 @@ int dec_fused_splits(const blk_handle* h, int tiles, int num_kb, int B, Epi epi)
   for (; sp >= 1; --sp)
     if (tc_dec_max_clusters(bn, epi, sp) >= units1) return sp;
   return 0;
+}
+
+// Cluster size of the decode MLP-up + activation GEMM (kDecAct): persistent clusters
+// of S K-splits walk the tiles (64 gate over 64 up features when paired, else 128 up
+// features). A tile's epilogue (the partials' hand-off and the activation, about
+// 3.4 us) overlaps the next tile's weight stream, so a CTA takes about
+//   t_unit + (rounds - 1) * max(t_unit, t_epi) + t_epi,
+// t_unit = its 128 x K/S weight bytes at min(55 GB/s, 7 TB/s / active CTAs).
+// 0 when the form does not apply (more than 64 tokens, a width not a multiple of
+// 4, no cluster fits).
+int dec_act_splits(const blk_handle* h, int B, int* clusters_out) {
+  const blk_desc& d = h->d;
+  if (dec_bn(B) != 64 || d.ffn % 4 != 0) return 0;
+  const bool paired = d.act == BLK_ACT_SWIGLU;
+  const int tiles = paired ? (d.ffn + 63) / 64 : (d.ffn + 127) / 128;
+  const int num_kb = (d.hidden + 63) / 64;
+  constexpr double kCtaBw = 55e9, kHbmBw = 7.0e12, kEpi = 3.4e-6;
+  int best = 0, best_nc = 0;
+  double best_t = 1e30;
+  for (int sp = 1; sp <= 8 && sp <= num_kb; ++sp) {
+    const int nc = std::min(tiles, tc_dec_max_clusters(64, Epi::kDecAct, sp));
+    if (nc <= 0) continue;
+    const int rounds = (tiles + nc - 1) / nc;
+    const double bw = std::min(kCtaBw, kHbmBw / (nc * sp));
+    const double t_unit = 128.0 * 64.0 * ((num_kb + sp - 1) / sp) * 2.0 / bw;
+    const double t = t_unit + (rounds - 1) * std::max(t_unit, kEpi) + kEpi;
+    if (t < best_t * 0.99) {
+      best_t = t;
+      best = sp;
+      best_nc = nc;
+    }
+  }
+  *clusters_out = best_nc;
+  return best;
+}
+
+// The decode MLP up GEMM with its activation (kDecAct): neurons[B, F] (bf16) from the
+// MLP input rows y; row_ss: the o_proj epilogue's per-tile sums of squares (1/rms
+// applied after the product), or null when y is already normalised.
+blk_status dec_act_gemm(const blk_handle* h, const blk_weights* w, const Prepared& prep, bool f16, const void* y,
+                        int B, int splits, int clusters, const float* row_ss, int parts, void* neur, cudaStream_t s) {
+  const blk_desc& d = h->d;
+  TcGemmDesc g;
+  g.f16 = f16;
+  if (d.act == BLK_ACT_SWIGLU) {
+    g.na = 2;
+    g.a[0] = {f16 ? prep.wg : w->w_gate, d.ffn, 0};
+    g.a[1] = {f16 ? prep.wu : w->w_up, d.ffn, 0};
+    g.a_paired = true;
+  } else {
+    g.na = 1;
+    g.a[0] = {f16 ? prep.wu : w->w_up, d.ffn, 0};
+  }
+  g.nb = 1;
+  g.b[0] = {y, B, 0};
+  g.K = d.hidden;
+  g.bn = 64;
+  g.k_splits = splits;
+  g.epi = Epi::kDecAct;
+  g.const_op = 1;  // A = the weights
+  g.e.out = neur;
+  g.e.ldo = d.ffn;
+  g.e.n_tok = B;
+  g.e.act = (int)d.act;
+  g.e.alpha_p = d.xielu_alpha_p;
+  g.e.alpha_n = d.xielu_alpha_n;
+  g.e.beta = d.xielu_beta;
+  g.e.xeps = d.xielu_eps;
+  g.e.row_ss = row_ss;
+  g.e.ss_parts = parts;
+  g.e.ss_n = d.hidden;
+  g.e.ss_eps = d.eps;
+  const char* why = nullptr;
+  cudaError_t e = launch_tc_gemm(g, clusters * splits, h->status, (unsigned long long)g_wait_ns.load(), s, &why);
+  if (e != cudaSuccess) return cuda_fail(e, "decode MLP-up GEMM with activation", why);
+  return BLK_OK;
 }
 
 // A fused decode GEMM: the weight segments on the MMA's M side, the B tokens of x
@@ -594,7 +670,10 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
   void* gate = gated ? ws.gate : nullptr;
   int sp = 1;
   prof_mark(h, "rmsnorm1", 1, s);
-  BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, B, d.hidden, d.eps, ws.y, bf, s, false, f16), "rmsnorm 1"));
+  // (it also zeroes the attention's unit counter, at the start of its workspace)
+  BLK_TRY(check_cuda(launch_rmsnorm(x, w->ln1_g, B, d.hidden, d.eps, ws.y, bf, s, false, f16,
+                                    static_cast<int*>(ws.attn)),
+                     "rmsnorm 1"));
   prof_mark(h, "qkv_gemm_rope_append", s_qkv ? 1 : 2, s);
   {
     const TcSeg segs[4] = {{f16 ? prep.wq : w->wq, Hd, 0},
@@ -635,9 +714,10 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
   opt.gate = gate;
   opt.ungated = (gated || f16) ? head_tap : nullptr;  // the tap: bf16, before the gate
   opt.o_f16 = f16;
+  opt.counter_zeroed = true;  // by the input norm above
   cudaError_t ce = launch_attn_decode_bf16(q, cache->k, cache->v, o, B, d.n_heads, d.n_kv_heads, d.head_dim,
                                            cache->capacity, cache->lens, 1, max_len,
-                                           attn_decode_splits(B, d.n_kv_heads, d.max_seq, h->num_sms), ws.attn,
+                                           attn_decode_split_cap(d.max_seq), ws.attn,
                                            h->num_sms, h->status, (unsigned long long)g_wait_ns.load(), s, &why, opt);
   BLK_TRY(check_cuda(ce, "decode attention", why));
   prof_mark(h, "o_proj_gemm_resid_norm2", s_o ? 1 : 2, s);
@@ -667,19 +747,27 @@ blk_status forward_decode_bf16(blk_handle* h, const void* x, int B, const blk_we
                          "decode o_proj post"));
     }
   }
-  prof_mark(h, "mlp_up_gemm", 1, s);
-  if (d.act == BLK_ACT_SWIGLU) {
-    const TcSeg segs[2] = {{f16 ? prep.wg : w->w_gate, d.ffn, 0}, {f16 ? prep.wu : w->w_up, d.ffn, d.ffn}};
-    BLK_TRY(bf16_stream_gemm(h, segs, 2, ws.y, B, d.hidden, C, 2 * d.ffn, &sp, s, "decode gate/up GEMM", f16));
+  int act_clusters = 0;
+  const int s_act = dec_act_splits(h, B, &act_clusters);
+  if (s_act) {
+    // the activation inside the GEMM: the splits of each tile meet in a cluster's shared memory
+    prof_mark(h, "mlp_up_gemm_act", 1, s);
+    BLK_TRY(dec_act_gemm(h, w, prep, f16, ws.y, B, s_act, act_clusters, s_o ? ws.ss2 : nullptr, parts, neur, s));
   } else {
-    const TcSeg segs[1] = {{f16 ? prep.wu : w->w_up, d.ffn, 0}};
-    BLK_TRY(bf16_stream_gemm(h, segs, 1, ws.y, B, d.hidden, C, d.ffn, &sp, s, "decode up GEMM", f16));
+    prof_mark(h, "mlp_up_gemm", 1, s);
+    if (d.act == BLK_ACT_SWIGLU) {
+      const TcSeg segs[2] = {{f16 ? prep.wg : w->w_gate, d.ffn, 0}, {f16 ? prep.wu : w->w_up, d.ffn, d.ffn}};
+      BLK_TRY(bf16_stream_gemm(h, segs, 2, ws.y, B, d.hidden, C, 2 * d.ffn, &sp, s, "decode gate/up GEMM", f16));
+    } else {
+      const TcSeg segs[1] = {{f16 ? prep.wu : w->w_up, d.ffn, 0}};
+      BLK_TRY(bf16_stream_gemm(h, segs, 1, ws.y, B, d.hidden, C, d.ffn, &sp, s, "decode up GEMM", f16));
+    }
+    prof_mark(h, "mlp_act", 1, s);
+    BLK_TRY(check_cuda(launch_post_act(C, sp, B, d.ffn, mlp_cols(d), (int)d.act, d.xielu_alpha_p, d.xielu_alpha_n,
+                                       d.xielu_beta, d.xielu_eps, neur, bf, s, s_o ? ws.ss2 : nullptr, parts,
+                                       d.hidden, d.eps),
+                       "decode activation"));
   }
-  prof_mark(h, "mlp_act", 1, s);
-  BLK_TRY(check_cuda(launch_post_act(C, sp, B, d.ffn, mlp_cols(d), (int)d.act, d.xielu_alpha_p, d.xielu_alpha_n,
-                                     d.xielu_beta, d.xielu_eps, neur, bf, s, s_o ? ws.ss2 : nullptr, parts,
-                                     d.hidden, d.eps),
-                     "decode activation"));
   prof_mark(h, "down_gemm_resid", s_down ? 1 : 2, s);
   {
     const TcSeg segs[1] = {{w->w_down, d.hidden, 0}};
@@ -1212,7 +1300,7 @@ size_t blk_stage_workspace_bytes(const blk_handle* h, int rows) {
   Carve c(nullptr);
   c.take((size_t)rows * d.ffn * esize(d));                              // neurons
   c.take((size_t)rows * max_cols(d) * sizeof(float));                   // fp32 GEMM output
-  const int s = attn_decode_splits(rows, d.n_kv_heads, d.max_seq, h->num_sms);
+  const int s = attn_decode_split_cap(d.max_seq);
   c.take(attn_decode_ws_bytes(rows, d.n_heads, d.head_dim, s));         // decode attention partials
   return c.off;
 }
@@ -1274,7 +1362,7 @@ blk_status blk_attn_gqa(blk_handle* h, const void* q, const void* k, const void*
   c.take((size_t)batch * max_cols(d) * sizeof(float));
   void* aw = c.take(0);
   return check_cuda(launch_attn_decode_bf16(q, k, v, o, batch, d.n_heads, d.n_kv_heads, d.head_dim, kv_stride, kv_lens,
-                                            0, kv_stride, attn_decode_splits(batch, d.n_kv_heads, d.max_seq, h->num_sms),
+                                            0, kv_stride, attn_decode_split_cap(d.max_seq),
                                             aw, h->num_sms, h->status, (unsigned long long)g_wait_ns.load(), s, &why,
                                             opt),
                     "decode attention", why);
@@ -1424,7 +1512,7 @@ blk_status blk_attn_decode_noalloc(const void* q, const void* k, const void* v, 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return fail(BLK_ERR_ALIGNMENT, "alignment");
   if (head_dim != 128) return fail(BLK_ERR_UNSUPPORTED, "head_dim must be 128");
   if (n_heads / n_kv_heads > 16) return fail(BLK_ERR_UNSUPPORTED, "at most 16 query heads per KV head");
-  if ((size_t)batch * n_heads * (head_dim + 2) * sizeof(float) > kDecodeStaticScratchBytes)
+  if ((size_t)batch * n_heads * (head_dim + 2) * sizeof(float) > kDecodeStaticScratchBytes - kAttnCounterBytes)
     return fail(BLK_ERR_UNSUPPORTED,
                 "batch * n_heads * (head_dim + 2) * 4 bytes exceeds the 16 MiB allocation-free scratch");
   int dev = 0, sms = 0;

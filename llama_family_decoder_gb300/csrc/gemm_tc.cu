@@ -39,6 +39,7 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kThreads = 192;
+constexpr int kThreadsEpi = 128;  // epilogue warps 2..5
 // Drains after an abort wait for copies/MMAs already issued; they use their
 // own limit so that a tiny debug timeout cannot cut them short.
 constexpr unsigned long long kDrainNs = 2000000000ULL;
@@ -51,16 +52,19 @@ constexpr int pow2_at_least(int x) {
   return p;
 }
 
-template <int BN>
+template <int BN, int EPI = -1>
 struct TcCfg {
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarBytes = 256;
-  static constexpr int kFit = (kMaxSmem - 1024 - kBarBytes) / kStageBytes;
+  // kDecAct: two partial-tile buffers [BN tokens][128 rows] fp32 and the 1/rms of up to BN tokens
+  static constexpr int kPartBytes = BN * kBM * 4;
+  static constexpr int kExtraBytes = EPI == (int)Epi::kDecAct ? 2 * kPartBytes + 4 * BN : 0;
+  static constexpr int kFit = (kMaxSmem - 1024 - kBarBytes - kExtraBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;  // as deep a TMA ring as fits
   static constexpr int kTmemCols = pow2_at_least(2 * BN);  // two accumulators
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kExtraBytes + kBarBytes;
   static_assert(BN % 16 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory");
 };
@@ -70,10 +74,17 @@ __host__ __device__ constexpr bool is_dec_epi() {
   return EPI == (int)Epi::kDecQkv || EPI == (int)Epi::kDecResid;
 }
 
+// Launched as thread-block clusters of the K splits.
+template <int EPI>
+__host__ __device__ constexpr bool is_cluster_epi() {
+  return is_dec_epi<EPI>() || EPI == (int)Epi::kDecAct;
+}
+
 // Tile widths built per epilogue (a GEMM picks its width on the host).
 template <int BN, int EPI>
 __host__ __device__ constexpr bool tc_supported() {
   if (is_dec_epi<EPI>()) return BN == 64 || BN == 128 || BN == 256;
+  if (EPI == (int)Epi::kDecAct) return BN == 64;
   if (EPI == (int)Epi::kQkv) return BN == 128 || BN == 256;  // whole heads
   if (EPI == (int)Epi::kPartialT) return BN == 64 || BN == 128 || BN == 256;
   if (EPI == (int)Epi::kStore) return true;
@@ -92,8 +103,10 @@ struct TcParams {
   int b_out[kMaxSegs];
   int na, nb;
   int b_paired;
+  int a_paired;  // A tile = 64 rows of ta[0] over 64 rows of ta[1] (kDecAct: gate over up)
   int f16;  // fp16 operands (else bf16)
   int const_op;  // 1: A, 2: B is constant over the stream (may be loaded before pdl_wait)
+  int a_once;    // every A tile is read by one unit only (a weight stream): L2 evict-first
   int num_kb;
   int k_splits;
   int m_tiles, n_tiles;
@@ -120,7 +133,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u, int bn_row
   int s = 0;
   while (s + 1 < p.na && m_tile >= p.a_tiles[s + 1]) ++s;
   r.a_seg = s;
-  r.a_row0 = (m_tile - p.a_tiles[s]) * kBM;
+  r.a_row0 = (m_tile - p.a_tiles[s]) * (p.a_paired ? kBM / 2 : kBM);
   s = 0;
   while (s + 1 < p.nb && n_tile >= p.b_tiles[s + 1]) ++s;
   r.b_seg = p.b_paired ? 0 : s;
@@ -194,9 +207,9 @@ template <int BN, int EPI>
 __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, uint32_t taddr, int r_in_tile,
                                              float* stage) {
   const TcEpiArgs& e = p.e;
-  if constexpr (is_dec_epi<EPI>()) {
+  if constexpr (is_cluster_epi<EPI>()) {
     // decode finishers: this split's partial tile [token in tile][128 tile rows] in shared memory
-    // (the idle operand ring), read by the cluster's CTAs after a cluster barrier
+    // (the idle operand ring, or a kDecAct partial buffer), read by the cluster's CTAs
     float* blk = stage + r_in_tile;
     const int ntok = min(BN, e.n_tok - un.b_row0);
 #pragma unroll 1
@@ -758,20 +771,82 @@ __device__ __forceinline__ void dec_finish(const TcParams& p, const Unit& un, in
   }
 }
 
+// kDecAct: CTA r of the cluster sums its token slice [lo, hi) of the tile over the
+// splits' partial buffers (distributed shared memory, split order), multiplies by the
+// tokens' 1/rms and applies the activation; 128 threads, four features a thread.
+template <int BN>
+__device__ __forceinline__ void dec_act_reduce(const TcParams& p, const Unit& un, uint32_t part_s, int tid,
+                                               const float* rs_s, int lo, int hi) {
+  const TcEpiArgs& e = p.e;
+  const int S = p.k_splits;
+  const bool paired = p.a_paired != 0;
+  const int nf = paired ? kBM / 2 : kBM;  // output features of the tile
+  const int tpt = nf / 4;                 // threads per token
+  const int f_local = 4 * (tid % tpt);
+  const int feat = un.m_tile * nf + f_local;
+  const bool fok = feat < e.ldo;          // ldo = features (a multiple of 4)
+  const uint32_t u_off = (uint32_t)(paired ? kBM / 2 + f_local : f_local) * 4, g_off = (uint32_t)f_local * 4;
+  for (int t0 = lo; t0 < hi; t0 += kThreadsEpi / tpt) {
+    const int tl = t0 + tid / tpt;
+    const int tc = tl < hi ? tl : lo;  // clamped: every address is valid
+    float4 ag[8], au[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < S) {
+        const uint32_t base = map_shared_rank(part_s, (uint32_t)j) + (uint32_t)tc * (kBM * 4);
+        au[j] = ld_dsmem_f4(base + u_off);
+        ag[j] = paired ? ld_dsmem_f4(base + g_off) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < S) {
+        u = make_float4(u.x + au[j].x, u.y + au[j].y, u.z + au[j].z, u.w + au[j].w);
+        g = make_float4(g.x + ag[j].x, g.y + ag[j].y, g.z + ag[j].z, g.w + ag[j].w);
+      }
+    }
+    if (tl >= hi || !fok) continue;
+    const float rs = rs_s[tl - lo];
+    float v[4] = {u.x * rs, u.y * rs, u.z * rs, u.w * rs};
+    if (e.act == 0) {
+      const float gg[4] = {g.x * rs, g.y * rs, g.z * rs, g.w * rs};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[c] = silu_f(gg[c]) * v[c];
+    } else if (e.act == 1) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float r = fmaxf(v[c], 0.0f);
+        v[c] = r * r;
+      }
+    } else {
+      const float ap = e.alpha_p, an = e.alpha_n, be = e.beta, xe = e.xeps;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float x = v[c];
+        v[c] = x > 0.0f ? ap * x * x + be * x : an * (expm1_nonpos(fminf(x, xe)) - x) + be * x;
+      }
+    }
+    st_bf16x4(reinterpret_cast<__nv_bfloat16*>(e.out) + (size_t)(un.b_row0 + tl) * e.ldo + feat, v[0], v[1], v[2],
+              v[3]);
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, EPI>;
   constexpr int S = C::kStages;
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + S * C::kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::kBBytes);
-  // bars: full[S], empty[S], tfull[2], tempty[2], drain
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  float* pb = reinterpret_cast<float*>(sB + S * C::kBBytes);  // kDecAct: partial buffers, then 1/rms
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::kBBytes + C::kExtraBytes);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain, pbfull[2], pbfree[2] (kDecAct)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 9);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -781,6 +856,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * S + a]); };
   auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * S + 2 + a]); };
   const uint32_t drain_bar = smem_u32(&bars[2 * S + 4]);
+  auto pbfull_bar = [&](int b) { return smem_u32(&bars[2 * S + 5 + b]); };
+  auto pbfree_bar = [&](int b) { return smem_u32(&bars[2 * S + 7 + b]); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -792,6 +869,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       mbar_init(tempty_bar(a), 128);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (EPI == (int)Epi::kDecAct)
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(pbfull_bar(b), p.k_splits);  // one arrival from each split's CTA
+        mbar_init(pbfree_bar(b), p.k_splits);
+      }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -804,7 +886,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (EPI == (int)Epi::kDecAct)
+    cluster_sync_all();  // every CTA's barriers are initialised before any peer arrives on them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int bn_rows = p.b_paired ? BN / 2 : BN;
@@ -818,8 +903,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       uint32_t ph = 0;
       uint32_t issued_mask = 0, parity_mask = 0;
       bool failed = false;
+      // A streamed once (decode weights) must not push the activations that the
+      // next kernels read out of L2
+      const uint64_t a_policy = l2_policy_evict_first();
       auto load_a = [&](int st, const Unit& un, int kb) {
-        tma_load_2d(smem_u32(sA + st * C::kABytes), &p.ta[un.a_seg], kb * kBK, un.a_row0, full_bar(st));
+        if (p.a_paired) {  // gate rows over up rows: two 64-row boxes make one 128-row swizzled tile
+          const uint32_t dst = smem_u32(sA + st * C::kABytes);
+          tma_load_2d_hint(dst, &p.ta[0], kb * kBK, un.a_row0, full_bar(st), a_policy);
+          tma_load_2d_hint(dst + (kBM / 2) * kBK * 2, &p.ta[1], kb * kBK, un.a_row0, full_bar(st), a_policy);
+        } else if (p.a_once)
+          tma_load_2d_hint(smem_u32(sA + st * C::kABytes), &p.ta[un.a_seg], kb * kBK, un.a_row0, full_bar(st),
+                           a_policy);
+        else
+          tma_load_2d(smem_u32(sA + st * C::kABytes), &p.ta[un.a_seg], kb * kBK, un.a_row0, full_bar(st));
       };
       auto load_b = [&](int st, const Unit& un, int kb) {
         const uint32_t b_dst = smem_u32(sB + st * C::kBBytes);
@@ -942,23 +1038,72 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     if constexpr (is_dec_epi<EPI>())  // the finisher's per-token inputs, while the main loop runs
       dec_load_side<BN, EPI>(p, decode_unit(p, blockIdx.x, bn_rows), warp - 2, lane, dec_side);
     const int quarter = warp & 3;
+    const int tid = threadIdx.x - 64;  // 0..127
+    // kDecAct: this CTA's token slice and its tokens' 1/rms (the MLP input's RMSNorm, applied after the product)
+    DecSlice act_sl{0, 0, 0};
+    float* rs_s = pb + 2 * (C::kPartBytes / 4);
+    if constexpr (EPI == (int)Epi::kDecAct) {
+      act_sl = dec_slice(p, decode_unit(p, blockIdx.x, bn_rows), BN);
+      const TcEpiArgs& e = p.e;
+      for (int t = act_sl.lo + (warp - 2); t < act_sl.hi; t += 4) {
+        float ss = 0.f;
+        if (e.row_ss)
+          for (int i = lane; i < e.ss_parts; i += 32) ss += e.row_ss[(size_t)(act_sl.tok0 + t) * e.ss_parts + i];
+        ss = warp_sum(ss);
+        if (lane == 0) rs_s[t - act_sl.lo] = e.row_ss ? rsqrtf(ss / (float)e.ss_n + e.ss_eps) : 1.0f;
+      }
+      named_bar_sync(1, kThreadsEpi);
+    }
     int it = 0;
     bool failed = false;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
       const Unit un = decode_unit(p, u, bn_rows);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      // warp-uniform: every lane waits, the warp gives up together
-      if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, budget, abort_flag))) {
-        failed = true;
-        break;
-      }
-      __syncwarp();
-      tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane, reinterpret_cast<float*>(smem));
-      tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      if constexpr (EPI == (int)Epi::kDecAct) {
+        // The four epilogue warps decide together (barrier-OR) whether to go on, so
+        // that none is left alone at a named barrier after another gave up.
+        float* part = pb + acc * (C::kPartBytes / 4);
+        bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, budget, abort_flag));
+        // partial buffer acc is free once every split's CTA has read this CTA's tile it - 2 from it
+        if (ok && it >= 2)
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_cluster(pbfree_bar(acc), ((it >> 1) - 1) & 1, budget, abort_flag));
+        if (ok) {
+          __syncwarp();
+          tc_fence_after();
+          run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane, part);
+          tc_fence_before();
+          mbar_arrive(tempty_bar(acc));
+        }
+        if (named_bar_or(1, kThreadsEpi, !ok)) {
+          failed = true;
+          break;
+        }
+        // hand the partial to the cluster: every split's CTA arrives on every CTA's pbfull
+        // (lane r of the first epilogue warp on CTA r's: the arrivals travel in parallel)
+        if (tid < p.k_splits) mbar_arrive_cluster(map_shared_rank(pbfull_bar(acc), (uint32_t)tid));
+        ok = __all_sync(0xffffffffu, mbar_wait_cluster(pbfull_bar(acc), (it >> 1) & 1, budget, abort_flag));
+        if (ok) dec_act_reduce<BN>(p, un, smem_u32(part), tid, rs_s, act_sl.lo, act_sl.hi);
+        if (named_bar_or(1, kThreadsEpi, !ok)) {
+          failed = true;
+          break;
+        }
+        // this CTA has read every split's buffer acc: release them for tile it + 2
+        if (tid < p.k_splits) mbar_arrive_cluster(map_shared_rank(pbfree_bar(acc), (uint32_t)tid));
+      } else {
+        // warp-uniform: every lane waits, the warp gives up together
+        if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, budget, abort_flag))) {
+          failed = true;
+          break;
+        }
+        __syncwarp();
+        tc_fence_after();
+        run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane, reinterpret_cast<float*>(smem));
+        tc_fence_before();
+        mbar_arrive(tempty_bar(acc));
+      }
     }
     if (failed) {
       *abort_flag = 1;
@@ -966,6 +1111,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
   }
 
+  if constexpr (EPI == (int)Epi::kDecAct) {
+    // no CTA leaves while another CTA of its cluster may still read its partial
+    // buffers (every thread gets here: all earlier waits are bounded)
+    __syncwarp();
+    cluster_sync_all();
+  }
   if constexpr (is_dec_epi<EPI>()) {
     // Every thread of every CTA of the cluster reaches both barriers, whatever
     // happened above (all earlier waits are bounded): the split partials are in
@@ -1027,7 +1178,7 @@ namespace {
 template <int BN, int EPI>
 cudaError_t configure() {
   static cudaError_t st = cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               TcCfg<BN>::kSmemBytes);  // once per instantiation
+                                               TcCfg<BN, EPI>::kSmemBytes);  // once per instantiation
   return st;
 }
 
@@ -1037,7 +1188,7 @@ void cluster_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(grid);
   cfg->blockDim = dim3(kThreads);
-  cfg->dynamicSmemBytes = TcCfg<BN>::kSmemBytes;
+  cfg->dynamicSmemBytes = TcCfg<BN, EPI>::kSmemBytes;
   cfg->stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = splits;
@@ -1053,14 +1204,14 @@ template <int BN, int EPI>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t s) {
   cudaError_t e = configure<BN, EPI>();
   if (e != cudaSuccess) return e;
-  if constexpr (is_dec_epi<EPI>()) {
+  if constexpr (is_cluster_epi<EPI>()) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     cluster_config<BN, EPI>(&cfg, attr, grid, p.k_splits, s);
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, EPI>, p);
     if (e != cudaSuccess) return e;
   } else {
-    launch_pdl(tc_gemm_kernel<BN, EPI>, grid, kThreads, TcCfg<BN>::kSmemBytes, s, p);
+    launch_pdl(tc_gemm_kernel<BN, EPI>, grid, kThreads, TcCfg<BN, EPI>::kSmemBytes, s, p);
   }
   return cudaGetLastError();
 }
@@ -1100,6 +1251,7 @@ cudaError_t dispatch_epi(const TcParams& p, Epi epi, int grid, cudaStream_t s) {
     case Epi::kPartialT: return launch_if<BN, (int)Epi::kPartialT>(p, grid, s);
     case Epi::kDecQkv: return launch_if<BN, (int)Epi::kDecQkv>(p, grid, s);
     case Epi::kDecResid: return launch_if<BN, (int)Epi::kDecResid>(p, grid, s);
+    case Epi::kDecAct: return launch_if<BN, (int)Epi::kDecAct>(p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -1109,15 +1261,18 @@ cudaError_t dispatch_epi(const TcParams& p, Epi epi, int grid, cudaStream_t s) {
 int tc_dec_max_clusters(int bn, Epi epi, int splits) {
   if (splits < 1 || splits > 8) return 0;
   static std::mutex mu;
-  static int cache[5][2][9] = {};  // bn index, epilogue, splits (0: not queried yet)
+  static int cache[5][3][9] = {};  // bn index, epilogue, splits (0: not queried yet)
   const int bi = bn == 64 ? 0 : bn == 128 ? 1 : bn == 256 ? 2 : -1;
-  const int ei = epi == Epi::kDecQkv ? 0 : epi == Epi::kDecResid ? 1 : -1;
-  if (bi < 0 || ei < 0) return 0;
+  const int ei = epi == Epi::kDecQkv ? 0 : epi == Epi::kDecResid ? 1 : epi == Epi::kDecAct ? 2 : -1;
+  if (bi < 0 || ei < 0 || (ei == 2 && bn != 64)) return 0;
   std::lock_guard<std::mutex> lock(mu);
   int& c = cache[bi][ei][splits];
   if (c == 0) {
     int n = 0;
-    if (bn == 64) n = ei == 0 ? max_clusters<64, (int)Epi::kDecQkv>(splits) : max_clusters<64, (int)Epi::kDecResid>(splits);
+    if (ei == 2)
+      n = max_clusters<64, (int)Epi::kDecAct>(splits);
+    else if (bn == 64)
+      n = ei == 0 ? max_clusters<64, (int)Epi::kDecQkv>(splits) : max_clusters<64, (int)Epi::kDecResid>(splits);
     if (bn == 128)
       n = ei == 0 ? max_clusters<128, (int)Epi::kDecQkv>(splits) : max_clusters<128, (int)Epi::kDecResid>(splits);
     if (bn == 256)
@@ -1157,16 +1312,23 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
   }
   p.na = d.na;
   p.nb = d.nb;
+  if (d.a_paired && (d.epi != Epi::kDecAct || d.na != 2 || d.a[0].rows != d.a[1].rows)) {
+    *why = "tcgen05 GEMM: paired A operands are two equal segments of a decode activation GEMM";
+    return cudaErrorInvalidValue;
+  }
+  const int a_box = d.a_paired ? kBM / 2 : kBM;
   p.a_tiles[0] = 0;
   for (int i = 0; i < d.na; ++i) {
-    if (!make_map(&p.ta[i], d.a[i].ptr, d.a[i].rows, d.K, kBM, d.f16)) {
+    if (!make_map(&p.ta[i], d.a[i].ptr, d.a[i].rows, d.K, a_box, d.f16)) {
       *why = "cuTensorMapEncodeTiled failed for an A operand";
       return cudaErrorInvalidValue;
     }
     p.a_rows[i] = d.a[i].rows;
     p.a_out[i] = d.a[i].out_offset;
-    p.a_tiles[i + 1] = p.a_tiles[i] + (d.a[i].rows + kBM - 1) / kBM;
+    // paired: one tile sequence over both segments (rows of a[0] and a[1] side by side)
+    p.a_tiles[i + 1] = d.a_paired ? (d.a[0].rows + a_box - 1) / a_box : p.a_tiles[i] + (d.a[i].rows + kBM - 1) / kBM;
   }
+  p.a_paired = d.a_paired ? 1 : 0;
   p.b_tiles[0] = 0;
   for (int i = 0; i < d.nb; ++i) {
     if (!make_map(&p.tb[i], d.b[i].ptr, d.b[i].rows, d.K, bn_rows, d.f16)) {
@@ -1185,6 +1347,16 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
   p.num_kb = (d.K + kBK - 1) / kBK;
   p.k_splits = d.k_splits < 1 ? 1 : (d.k_splits > p.num_kb ? p.num_kb : d.k_splits);
   p.num_units = p.m_tiles * p.n_tiles * p.k_splits;
+  p.a_once = d.const_op == 1 && p.n_tiles == 1;
+  if (d.epi == Epi::kDecAct) {
+    // persistent clusters of the K splits: the grid (max_ctas) is whole clusters; one N tile
+    if (d.nb != 1 || d.b_paired || d.e.n_tok != d.b[0].rows || p.n_tiles != 1 || p.k_splits > 8 ||
+        d.k_splits != p.k_splits || max_ctas < p.k_splits || max_ctas % p.k_splits != 0 || d.e.ldo % 4 != 0 ||
+        d.e.ldo != d.a[0].rows || d.na != (d.a_paired ? 2 : 1)) {
+      *why = "tcgen05 GEMM: a decode activation GEMM needs one N tile, whole clusters of at most 8 K splits";
+      return cudaErrorInvalidValue;
+    }
+  }
   if (d.epi == Epi::kDecQkv || d.epi == Epi::kDecResid) {
     // one unit per CTA, the K splits of a tile forming one cluster (at most 8), all resident at once
     if (d.nb != 1 || d.b_paired || d.e.n_tok != d.b[0].rows || p.k_splits > 8 || p.num_units > max_ctas ||

@@ -15,8 +15,10 @@ struct DevStatus;
 // y[r,:] = x[r,:] * rsqrt(mean(x[r,:]^2) + eps) * g   (fp32 statistics)
 // x_f32: x is fp32 while g and y have the storage type (the bf16 path's fp32 residual stream).
 // y_f16 (bf16 path): y is fp16, the operand of a GEMM with prepared fp16 weights.
+// zero_word (optional): set to 0 once the kernel's predecessors are done (a later
+// kernel's counter, e.g. the decode attention's).
 cudaError_t launch_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y, bool bf16,
-                           cudaStream_t s, bool x_f32 = false, bool y_f16 = false);
+                           cudaStream_t s, bool x_f32 = false, bool y_f16 = false, int* zero_word = nullptr);
 
 // The input RMSNorm split for the fused bf16 prefill: row_scale[r] = rsqrt(mean(x[r]^2) + eps),
 // xg[r, :] = bf16(x[r, :] * g) (the QKV GEMM's A; x itself when g == 1); zeroes zero_rows[r].
@@ -63,6 +65,12 @@ enum class Epi : int {
   kDecQkv = 7,    // per-head q/k RMSNorm, RoPE at position lens[t], q store, K/V cache append,
                   // a 4th A segment (the attention gate): sigmoid(acc) as fp16
   kDecResid = 8,  // resid + acc (fp32), optional taps, next RMSNorm (gained rows + sum of squares)
+  // Decode MLP up + activation: persistent clusters of K splits walk the tiles,
+  // the splits' partials of a tile meet in shared memory (two buffers, mbarrier
+  // hand-off across the cluster) while the next tile streams; with paired A
+  // (64 gate rows over 64 up rows) out = bf16(silu(gate * rs) * (up * rs)), else
+  // relu^2 or xIELU of up * rs; rs = the MLP input's 1/rms (row_ss), or 1.
+  kDecAct = 9,
 };
 
 // How many clusters of `splits` CTAs of the decode GEMM kernel (tile width bn,
@@ -122,6 +130,7 @@ struct TcEpiArgs {
   // kPartialT
   int part_ld = 0;  // features per token row of the partial buffer
   int n_tok = 0;    // valid tokens (B operand rows)
+  int act = 0;  // kDecAct: 0 SwiGLU (paired A), 1 relu^2, 2 xIELU
   // decode finishers
   const int* lens = nullptr;  // kDecQkv: positions already in the cache, per sequence
   int* bump_lens = nullptr;   // kDecResid: lens[t] += 1 once per token (the tile of m_tile 0);
@@ -136,6 +145,7 @@ struct TcGemmDesc {
   TcSeg b[kMaxSegs];
   int nb = 1;
   bool b_paired = false;  // B tile = halves from b[0] and b[1] at the same rows (gate/up)
+  bool a_paired = false;  // A tile = 64 rows of a[0] over 64 rows of a[1] at the same rows (kDecAct)
   bool f16 = false;       // A and B are fp16 (else bf16)
   int K = 0;              // inner dimension; every segment has row stride K
   int k_splits = 1;
@@ -203,6 +213,7 @@ struct AttnOpts {
   const void* gate = nullptr;
   void* ungated = nullptr;
   bool o_f16 = false;            // decode: o in fp16 (else bf16)
+  bool counter_zeroed = false;   // decode: an earlier kernel of the stream zeroed the workspace's unit counter
   const int2* key_range = nullptr;  // prefill: per sequence, only keys lo <= j < hi are visible
 };
 
@@ -223,6 +234,9 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
                                    int kv_stride = 0, const AttnOpts& opt = AttnOpts());
 
 // Decode (Tq == 1), split over the keys: partial results in ws, combined into o.
+// The decode attention workspace starts with its unit counter (kAttnCounterBytes,
+// an int the attention kernel counts up from 0), then the split partials.
+constexpr size_t kAttnCounterBytes = 256;
 size_t attn_decode_ws_bytes(int B, int H, int d, int max_splits);
 // Keys per sequence: kv_lens[b] + len_add (<= max_len, which sizes the splits; at most
 // split_cap of them, the number ws holds); with a window, the last `window` of them.
@@ -231,6 +245,8 @@ cudaError_t launch_attn_decode_bf16(const void* q, const void* k, const void* v,
                                     int split_cap, void* ws, int num_sms, DevStatus* st, unsigned long long wait_ns,
                                     cudaStream_t s, const char** why, const AttnOpts& opt = AttnOpts());
 int attn_decode_splits(int B, int Hkv, int max_len, int num_sms);
+// Most splits attn_decode_splits picks for keys up to max_len (size workspaces with it).
+int attn_decode_split_cap(int max_len);
 
 // Decode attention with its split partials in a fixed file-scope device array
 // (no workspace, no allocation); kv_lens[b] keys per sequence, <= kv_stride.

@@ -61,10 +61,11 @@ __device__ __forceinline__ void store8<__half>(__half* p, const float (&f)[8]) {
 // NC = chunks of 8 elements per thread, NT threads; TX: x, TY: the gain, TO: y
 template <typename TX, typename TY, typename TO, int NC, int NT>
 __global__ void __launch_bounds__(NT) rmsnorm_kernel(const TX* __restrict__ x, const TY* __restrict__ g, int rows,
-                                                     int n, float eps, TO* __restrict__ y) {
+                                                     int n, float eps, TO* __restrict__ y, int* zero_word) {
   constexpr int kThreads = NT;
   pdl_launch_dependents();
   pdl_wait();
+  if (zero_word && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0;
   __shared__ float red[kThreads / 32];
   const int nchunk = n / 8;
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -106,7 +107,8 @@ __global__ void __launch_bounds__(NT) rmsnorm_kernel(const TX* __restrict__ x, c
 // Rows of up to 8192 elements take 128 threads (up to 8 chunks of 8 each), so that
 // 16 CTAs fit on an SM and every row of a prefill normalises at once; longer rows 256.
 template <typename TX, typename TY, typename TO = TY>
-cudaError_t launch_t(const void* x, const void* g, int rows, int n, float eps, void* y, cudaStream_t s) {
+cudaError_t launch_t(const void* x, const void* g, int rows, int n, float eps, void* y, cudaStream_t s,
+                     int* zero_word) {
   const int nt = n / 8 <= 128 * 8 ? 128 : 256;
   const int nc = (n / 8 + nt - 1) / nt;
   int dev = 0, sms = 148;
@@ -117,7 +119,7 @@ cudaError_t launch_t(const void* x, const void* g, int rows, int n, float eps, v
   auto X = static_cast<const TX*>(x);
   auto G = static_cast<const TY*>(g);
   auto Y = static_cast<TO*>(y);
-#define BLK_RMS(NC, NT) launch_pdl(rmsnorm_kernel<TX, TY, TO, NC, NT>, grid, NT, 0, s, X, G, rows, n, eps, Y)
+#define BLK_RMS(NC, NT) launch_pdl(rmsnorm_kernel<TX, TY, TO, NC, NT>, grid, NT, 0, s, X, G, rows, n, eps, Y, zero_word)
   if (nt == 128) {
     switch (nc) {
       case 1: BLK_RMS(1, 128); break;
@@ -247,16 +249,16 @@ cudaError_t launch_cast_f16_bf16(const void* src, void* dst, size_t n, cudaStrea
 }
 
 cudaError_t launch_rmsnorm(const void* x, const void* g, int rows, int n, float eps, void* y, bool bf16,
-                           cudaStream_t s, bool x_f32, bool y_f16) {
+                           cudaStream_t s, bool x_f32, bool y_f16, int* zero_word) {
   if (rows <= 0) return cudaSuccess;
   if (n % 8) return cudaErrorInvalidValue;
-  if (!bf16) return launch_t<float, float>(x, g, rows, n, eps, y, s);
+  if (!bf16) return launch_t<float, float>(x, g, rows, n, eps, y, s, zero_word);
   if (y_f16) {  // the fp16 A operand of a GEMM with prepared (fp16) weights: normalized first, so in range
-    if (x_f32) return launch_t<float, __nv_bfloat16, __half>(x, g, rows, n, eps, y, s);
-    return launch_t<__nv_bfloat16, __nv_bfloat16, __half>(x, g, rows, n, eps, y, s);
+    if (x_f32) return launch_t<float, __nv_bfloat16, __half>(x, g, rows, n, eps, y, s, zero_word);
+    return launch_t<__nv_bfloat16, __nv_bfloat16, __half>(x, g, rows, n, eps, y, s, zero_word);
   }
-  if (x_f32) return launch_t<float, __nv_bfloat16>(x, g, rows, n, eps, y, s);
-  return launch_t<__nv_bfloat16, __nv_bfloat16>(x, g, rows, n, eps, y, s);
+  if (x_f32) return launch_t<float, __nv_bfloat16>(x, g, rows, n, eps, y, s, zero_word);
+  return launch_t<__nv_bfloat16, __nv_bfloat16>(x, g, rows, n, eps, y, s, zero_word);
 }
 
 }  // namespace blk

@@ -211,11 +211,12 @@ def test_decode_step_small(dtype):
 
 @pytest.mark.parametrize("prepared", [False, True], ids=["bf16_weights", "prepared_fp16"])
 @pytest.mark.parametrize("act,qk_norm,batch,ffn", [("relu2", False, 7, 1000), ("xielu", True, 3, 1024),
-                                                   ("silu", True, 70, 968)])
+                                                   ("silu", True, 70, 968), ("silu", False, 5, 968)])
 def test_decode_step_bf16_variants_and_taps(act, qk_norm, batch, ffn, prepared):
-    # every activation, q/k-norm with non-unit gains, a token tile wider than 64,
-    # ragged MLP tiles, and the per-stage taps of the decode path (fp16 operands
-    # with prepared weights)
+    # every activation, q/k-norm with non-unit gains, a token tile wider than 64
+    # (the MLP-up GEMM then leaves the activation to a post kernel), ragged MLP
+    # tiles (968 = 15 paired tiles of 64 and 8 features), and the per-stage taps
+    # of the decode path (fp16 operands with prepared weights)
     wl = Workload(f"decode_{act}", "bf16", batch, 1, 512, 8, 2, 128, ffn, act, qk_norm=qk_norm, seed=25)
     lens = [(37 * b + 11) % 190 + 1 for b in range(batch)]
     w, x, kc, vc = _decode_case(wl, lens)
