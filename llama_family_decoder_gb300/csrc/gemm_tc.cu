@@ -907,15 +907,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       // next kernels read out of L2
       const uint64_t a_policy = l2_policy_evict_first();
       auto load_a = [&](int st, const Unit& un, int kb) {
-        if (p.a_paired) {  // gate rows over up rows: two 64-row boxes make one 128-row swizzled tile
-          const uint32_t dst = smem_u32(sA + st * C::kABytes);
-          tma_load_2d_hint(dst, &p.ta[0], kb * kBK, un.a_row0, full_bar(st), a_policy);
-          tma_load_2d_hint(dst + (kBM / 2) * kBK * 2, &p.ta[1], kb * kBK, un.a_row0, full_bar(st), a_policy);
-        } else if (p.a_once)
-          tma_load_2d_hint(smem_u32(sA + st * C::kABytes), &p.ta[un.a_seg], kb * kBK, un.a_row0, full_bar(st),
-                           a_policy);
-        else
-          tma_load_2d(smem_u32(sA + st * C::kABytes), &p.ta[un.a_seg], kb * kBK, un.a_row0, full_bar(st));
+        if constexpr (EPI == (int)Epi::kPartialT || is_cluster_epi<EPI>()) {  // the decode GEMMs
+          if (p.a_paired) {  // gate rows over up rows: two 64-row boxes make one 128-row swizzled tile
+            const uint32_t dst = smem_u32(sA + st * C::kABytes);
+            tma_load_2d_hint(dst, &p.ta[0], kb * kBK, un.a_row0, full_bar(st), a_policy);
+            tma_load_2d_hint(dst + (kBM / 2) * kBK * 2, &p.ta[1], kb * kBK, un.a_row0, full_bar(st), a_policy);
+            return;
+          }
+          if (p.a_once) {
+            tma_load_2d_hint(smem_u32(sA + st * C::kABytes), &p.ta[un.a_seg], kb * kBK, un.a_row0, full_bar(st),
+                             a_policy);
+            return;
+          }
+        }
+        tma_load_2d(smem_u32(sA + st * C::kABytes), &p.ta[un.a_seg], kb * kBK, un.a_row0, full_bar(st));
       };
       auto load_b = [&](int st, const Unit& un, int kb) {
         const uint32_t b_dst = smem_u32(sB + st * C::kBBytes);
