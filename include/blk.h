@@ -388,10 +388,11 @@ void blk_profile_reset(blk_handle* h);
 /* Debug/test entry: the bare tcgen05 GEMM, c[M, N] = bf16(a[M, K] @ b[N, K]^T)
  * with fp32 accumulation, all bf16 row-major device pointers, N-tile bn in
  * {64, 128, 192, 224, 256}, split_k >= 1 (bn == 64 only: fp32 partial sums are then
- * written to c as float [split_k][N][M] instead). K % 8 == 0.
+ * written to c as float [split_k][N][M] instead). K % 8 == 0. pair != 0: CTA pairs
+ * (tcgen05 cta_group::2, 256-row tiles, bn in {192, 224, 256}, split_k == 1).
  * Errors: INVALID_ARG, ALIGNMENT, CUDA. */
 blk_status blk_debug_gemm_bf16(const void* a, const void* b, void* c, int M, int N, int K, int bn, int split_k,
-                               void* stream);
+                               int pair, void* stream);
 
 /* Library version string. */
 const char* blk_version(void);

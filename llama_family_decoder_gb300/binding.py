@@ -81,7 +81,8 @@ SIGNATURES = {
     "blk_profile_collect": (c_int, [c_void_p, POINTER(ctypes.c_double), POINTER(c_longlong), c_int]),
     "blk_profile_stage_name": (c_char_p, [c_void_p, c_int]),
     "blk_profile_reset": (None, [c_void_p]),
-    "blk_debug_gemm_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "blk_debug_gemm_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                    c_void_p]),
     "blk_forward_graph_create": (c_int, [c_void_p, c_void_p, c_int, c_int, POINTER(blk_weights),
                                          POINTER(blk_kv_cache), c_int, c_void_p, c_void_p, c_size_t,
                                          POINTER(blk_taps), POINTER(c_void_p)]),
@@ -369,8 +370,9 @@ def rmsnorm(x, g, eps=1e-5, out=None, stream=None):
     return out
 
 
-def debug_gemm_bf16(a, b, bn=256, split_k=1, out=None, stream=None):
-    """c = a @ b.T on the bare tcgen05 GEMM (bf16 out), or fp32 split-K partials [split, N, M]."""
+def debug_gemm_bf16(a, b, bn=256, split_k=1, out=None, stream=None, pair=False):
+    """c = a @ b.T on the bare tcgen05 GEMM (bf16 out), or fp32 split-K partials [split, N, M];
+    pair: CTA pairs with 256-row tiles."""
     import torch
     M, K = a.shape
     N = b.shape[0]
@@ -379,7 +381,8 @@ def debug_gemm_bf16(a, b, bn=256, split_k=1, out=None, stream=None):
             out = torch.empty(M, N, dtype=torch.bfloat16, device=a.device)
         else:
             out = torch.empty(split_k, M, N, dtype=torch.float32, device=a.device)
-    _check(lib().blk_debug_gemm_bf16(_ptr(a), _ptr(b), _ptr(out), M, N, K, bn, split_k, _stream_ptr(stream)))
+    _check(lib().blk_debug_gemm_bf16(_ptr(a), _ptr(b), _ptr(out), M, N, K, bn, split_k, 1 if pair else 0,
+                                     _stream_ptr(stream)))
     return out
 
 

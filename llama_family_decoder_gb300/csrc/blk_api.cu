@@ -120,32 +120,57 @@ int dec_tiles_qkv(const blk_desc& d) {
   return (d.attn_gate ? 2 : 1) * ((d.n_heads * d.head_dim + 127) / 128) + 2 * ((d.n_kv_heads * d.head_dim + 127) / 128);
 }
 
+// Tile of a prefill GEMM: one CTA per 128-row tile, or (pair) a CTA pair per
+// 256-row tile, each CTA loading half of the B tile (a third less operand traffic
+// per MMA than one CTA with the same width, which the measured per-SM TMA feed
+// rate caps). The fewest waves of tiles, weighted by each form's per-tile rate.
+struct TileChoice {
+  int bn;
+  bool pair;
+};
+constexpr double kPairRate = 1.12;  // a pair tile's MMA rate over a single CTA's at BN >= 192
+// Pairs pay off when a tile's main loop is long against its epilogue and the
+// accumulator hand-off across the pair: K >= 2048 (measured: Llama-7B, Arcee and
+// Apertus shapes 6-8% faster per block; at K = 1024 slower). The SwiGLU MLP-up
+// GEMM already runs at the sustained MMA rate with one CTA per tile.
+constexpr int kPairMinK = 2048;
+
+TileChoice choose_tile(int m_rows, int n_cols, bool paired, const int* cands, int ncand, int num_sms,
+                       bool allow_pair) {
+  TileChoice best{cands[0], false};
+  double best_cost = 1e30;
+  for (int pr = 0; pr < (allow_pair && num_sms >= 2 ? 2 : 1); ++pr)
+    for (int i = 0; i < ncand; ++i) {
+      const int bn = cands[i];
+      if (pr && bn < 192) continue;
+      const int cols = paired ? bn / 2 : bn;
+      const int rows = pr ? 256 : 128;
+      const int slots = pr ? num_sms / 2 : num_sms;
+      const long long tiles = (long long)((m_rows + rows - 1) / rows) * ((n_cols + cols - 1) / cols);
+      const long long waves = (tiles + slots - 1) / slots;
+      const double eff = (bn >= 256 ? 1.0 : bn >= 224 ? 0.99 : bn >= 192 ? 0.90 : 0.88) * (pr ? kPairRate : 1.0);
+      const double cost = (double)waves * cols / eff;
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = {bn, pr != 0};
+      }
+    }
+  return best;
+}
+
 // N-tile width for a GEMM with m_rows rows and n_cols output columns (per half
 // when paired): the fewest waves of tiles over the SMs, weighted by each width's
 // per-tile efficiency (narrower tiles re-read A more often).
 int choose_bn(int m_rows, int n_cols, bool paired, const int* cands, int ncand, int num_sms) {
-  int best = cands[0];
-  double best_cost = 1e30;
-  for (int i = 0; i < ncand; ++i) {
-    const int bn = cands[i];
-    const int cols = paired ? bn / 2 : bn;
-    const long long tiles = (long long)((m_rows + 127) / 128) * ((n_cols + cols - 1) / cols);
-    const long long waves = (tiles + num_sms - 1) / num_sms;
-    const double eff = bn >= 256 ? 1.0 : bn >= 224 ? 0.99 : bn >= 192 ? 0.90 : 0.88;
-    const double cost = (double)waves * cols / eff;
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = bn;
-    }
-  }
-  return best;
+  return choose_tile(m_rows, n_cols, paired, cands, ncand, num_sms, false).bn;
 }
 
-// Tile width of the residual GEMMs (o_proj, down) for `rows` rows of hidden outputs.
-int resid_bn(const blk_handle* h, int rows, int n) {
+// Tile of the residual GEMMs (o_proj, down) for `rows` rows of hidden outputs.
+TileChoice resid_tile(const blk_handle* h, int rows, int n, int K) {
   static const int c[] = {256, 224, 192, 128};
-  return choose_bn(rows, n, false, c, 4, h->num_sms);
+  return choose_tile(rows, n, false, c, 4, h->num_sms, K >= kPairMinK);
 }
+int resid_bn(const blk_handle* h, int rows, int n, int K) { return resid_tile(h, rows, n, K).bn; }
 
 // Partial sums of squares per row that the o_proj epilogue leaves for the MLP's
 // norm: one per o_proj N-tile (at most hidden / 128 of them).
@@ -270,7 +295,11 @@ blk_status bf16_qkv(const blk_handle* h, const void* y, const blk_weights* w, in
   g.K = d.hidden;
   const bool whole256 = (d.n_heads * d.head_dim) % 256 == 0 && (d.n_kv_heads * d.head_dim) % 256 == 0;
   static const int qkv_c[] = {256, 128};
-  g.bn = whole256 ? choose_bn(B * T, qkv_cols(d), false, qkv_c, 2, h->num_sms) : 128;
+  const TileChoice tq = whole256 ? choose_tile(B * T, qkv_cols(d), false, qkv_c, 2, h->num_sms,
+                                             d.hidden >= kPairMinK)
+                                 : TileChoice{128, false};
+  g.bn = tq.bn;
+  g.pair = tq.pair;
   g.epi = Epi::kQkv;
   g.const_op = 2;
   g.e = qkv_epi(h, w, T, pos0, q, k, v);
@@ -295,7 +324,9 @@ blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K
   g.nb = 1;
   g.b[0] = {W, N, 0};
   g.K = K;
-  g.bn = resid_bn(h, rows, N);
+  const TileChoice tr = resid_tile(h, rows, N, K);
+  g.bn = tr.bn;
+  g.pair = tr.pair;
   g.epi = Epi::kResid;
   g.const_op = 2;
   g.e.out = out;
@@ -329,7 +360,10 @@ blk_status bf16_mlp_up(const blk_handle* h, const void* y2, int rows, const blk_
   g.a[0] = {y2, rows, 0};
   g.K = d.hidden;
   static const int act_c[] = {256, 224, 192, 128};
-  g.bn = choose_bn(rows, d.ffn, d.act == BLK_ACT_SWIGLU, act_c, 4, h->num_sms);
+  const TileChoice ta = choose_tile(rows, d.ffn, d.act == BLK_ACT_SWIGLU, act_c, 4, h->num_sms,
+                                    d.hidden >= kPairMinK && d.act != BLK_ACT_SWIGLU);
+  g.bn = ta.bn;
+  g.pair = ta.pair;
   g.e.out = neur;
   g.e.ldo = d.ffn;
   if (d.act == BLK_ACT_SWIGLU) {
@@ -632,7 +666,7 @@ blk_status forward_prefill_bf16(blk_handle* h, const void* x, int B, int T, cons
   BLK_TRY(bf16_linear_resid(h, o_buf, M, Hd, f16 ? prep.wo : w->wo, d.hidden, x, false, ws.mid, true, mid_tap,
                             taps ? taps->attention_output : nullptr, s, "o_proj GEMM", ws.y, w->ln2_g, ws.ss2, f16));
   prof_mark(h, "mlp_up_gemm_act", 1, s);
-  BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s, ws.ss2, norm_parts(d.hidden, resid_bn(h, M, d.hidden)),
+  BLK_TRY(bf16_mlp_up(h, ws.y, M, w, neur, s, ws.ss2, norm_parts(d.hidden, resid_bn(h, M, d.hidden, d.n_heads * d.head_dim)),
                       f16 ? &prep : nullptr));
   prof_mark(h, "down_gemm_resid", 1, s);
   BLK_TRY(bf16_linear_resid(h, neur, M, d.ffn, w->w_down, d.hidden, ws.mid, true, out, false, nullptr,
@@ -1223,7 +1257,9 @@ blk_status blk_model_forward(blk_handle* h, const blk_model* m, const int* token
   g.b[0] = {m->lm_head, m->vocab, 0};
   g.K = d.hidden;
   static const int cands[] = {256, 224, 192, 128};
-  g.bn = choose_bn(M, m->vocab, false, cands, 4, h->num_sms);
+  const TileChoice tl = choose_tile(M, m->vocab, false, cands, 4, h->num_sms, d.hidden >= kPairMinK);
+  g.bn = tl.bn;
+  g.pair = tl.pair;
   g.epi = Epi::kStore;
   g.const_op = 2;
   g.e.out = logits;
@@ -1467,12 +1503,13 @@ void blk_profile_reset(blk_handle* h) {
 }
 
 blk_status blk_debug_gemm_bf16(const void* a, const void* b, void* c, int M, int N, int K, int bn, int split_k,
-                               void* stream) {
+                               int pair, void* stream) {
   if (!a || !b || !c) return fail(BLK_ERR_INVALID_ARG, "NULL argument");
   if (M <= 0 || N <= 0 || K <= 0 || K % 8 || (bn != 64 && bn != 128 && bn != 192 && bn != 224 && bn != 256) ||
       split_k < 1)
     return fail(BLK_ERR_INVALID_ARG, "bad sizes");
   if (split_k > 1 && bn != 64) return fail(BLK_ERR_INVALID_ARG, "split_k > 1 needs bn == 64");
+  if (pair && (split_k != 1 || bn < 192)) return fail(BLK_ERR_INVALID_ARG, "pair needs split_k == 1, bn >= 192");
   if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return fail(BLK_ERR_ALIGNMENT, "alignment");
   if (split_k == 1 && N % 8) return fail(BLK_ERR_INVALID_ARG, "N % 8 != 0");
   int dev = 0, sms = 0;
@@ -1484,6 +1521,7 @@ blk_status blk_debug_gemm_bf16(const void* a, const void* b, void* c, int M, int
   g.K = K;
   g.bn = bn;
   g.k_splits = split_k;
+  g.pair = pair != 0;
   if (split_k == 1) {
     g.a[0] = {a, M, 0};
     g.b[0] = {b, N, 0};

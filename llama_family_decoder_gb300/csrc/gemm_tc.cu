@@ -29,6 +29,8 @@
 
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -52,10 +54,10 @@ constexpr int pow2_at_least(int x) {
   return p;
 }
 
-template <int BN, int EPI = -1>
+template <int BN, int EPI = -1, bool PAIR = false>
 struct TcCfg {
   static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * kBK * 2;  // a pair: each CTA holds half of B
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarBytes = 256;
   // kDecAct: two partial-tile buffers [BN tokens][128 rows] fp32 and the 1/rms of up to BN tokens
@@ -140,6 +142,25 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u, int bn_row
   r.b_row0 = (n_tile - p.b_tiles[r.b_seg]) * bn_rows;
   r.kb_begin = (int)(((long long)r.ks * p.num_kb) / p.k_splits);
   r.kb_end = (int)(((long long)(r.ks + 1) * p.num_kb) / p.k_splits);
+  return r;
+}
+
+// Work unit of a CTA pair (M = 256 tiles, no K split): m_tiles counts 256-row
+// tiles; this CTA's A rows and epilogue rows are the pair tile's half prank.
+__device__ __forceinline__ Unit pair_unit(const TcParams& p, int u, int bn_rows, int prank) {
+  Unit r;
+  const int m_pair = u % p.m_tiles;
+  const int n_tile = u / p.m_tiles;
+  r.ks = 0;
+  r.kb_begin = 0;
+  r.kb_end = p.num_kb;
+  r.m_tile = 2 * m_pair + prank;
+  r.a_seg = 0;
+  r.a_row0 = r.m_tile * kBM;
+  int s = 0;
+  while (s + 1 < p.nb && n_tile >= p.b_tiles[s + 1]) ++s;
+  r.b_seg = p.b_paired ? 0 : s;
+  r.b_row0 = (n_tile - p.b_tiles[r.b_seg]) * bn_rows;
   return r;
 }
 
@@ -834,9 +855,9 @@ __device__ __forceinline__ void dec_act_reduce(const TcParams& p, const Unit& un
 
 // ------------------------------------------------------------------ the kernel
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  using C = TcCfg<BN, EPI>;
+  using C = TcCfg<BN, EPI, PAIR>;
   constexpr int S = C::kStages;
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -858,6 +879,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const uint32_t drain_bar = smem_u32(&bars[2 * S + 4]);
   auto pbfull_bar = [&](int b) { return smem_u32(&bars[2 * S + 5 + b]); };
   auto pbfree_bar = [&](int b) { return smem_u32(&bars[2 * S + 7 + b]); };
+  // A CTA pair (cluster of 2): the even CTA issues the MMAs and owns the full and
+  // tempty barriers both CTAs' copies and epilogues count on.
+  const int prank = PAIR ? (int)(cluster_ctarank() & 1u) : 0;
+  const bool mma_cta = prank == 0;
+  const uint32_t lead_rank = PAIR ? (cluster_ctarank() & ~1u) : 0u;
+  constexpr uint16_t kPairMask = 3;  // both CTAs of the (only) pair of the cluster
+  const int u0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ustep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -866,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 128);
+      mbar_init(tempty_bar(a), PAIR ? 8 : 128);  // a pair: one lane of each epilogue warp of both CTAs
     }
     mbar_init(drain_bar, 1);
     if constexpr (EPI == (int)Epi::kDecAct)
@@ -882,11 +911,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     for (int i = 0; i < p.nb; ++i) tma_prefetch_desc(&p.tb[i]);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_holder), C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  if constexpr (EPI == (int)Epi::kDecAct)
+  if constexpr (EPI == (int)Epi::kDecAct || PAIR)
     cluster_sync_all();  // every CTA's barriers are initialised before any peer arrives on them
   else
     __syncthreads();
@@ -906,7 +940,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       // A streamed once (decode weights) must not push the activations that the
       // next kernels read out of L2
       const uint64_t a_policy = l2_policy_evict_first();
+      // a pair: both CTAs' copies complete on the even CTA's full barrier
+      auto full_tx = [&](int st) { return PAIR ? map_shared_rank(full_bar(st), lead_rank) : full_bar(st); };
       auto load_a = [&](int st, const Unit& un, int kb) {
+        if constexpr (PAIR) {
+          tma_load_2d_pair(smem_u32(sA + st * C::kABytes), &p.ta[0], kb * kBK, un.a_row0, full_tx(st));
+          return;
+        }
         if constexpr (EPI == (int)Epi::kPartialT || is_cluster_epi<EPI>()) {  // the decode GEMMs
           if (p.a_paired) {  // gate rows over up rows: two 64-row boxes make one 128-row swizzled tile
             const uint32_t dst = smem_u32(sA + st * C::kABytes);
@@ -924,6 +964,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       };
       auto load_b = [&](int st, const Unit& un, int kb) {
         const uint32_t b_dst = smem_u32(sB + st * C::kBBytes);
+        if constexpr (PAIR) {
+          // the even CTA holds B's first N/2 rows, the odd one the rest: paired B
+          // (gate | up) splits into its halves, a plain B tile into two row ranges
+          if (p.b_paired)
+            tma_load_2d_pair(b_dst, &p.tb[prank], kb * kBK, un.b_row0, full_tx(st));
+          else
+            tma_load_2d_pair(b_dst, &p.tb[un.b_seg], kb * kBK, un.b_row0 + prank * (BN / 2), full_tx(st));
+          return;
+        }
         if (p.b_paired) {
           tma_load_2d(b_dst, &p.tb[0], kb * kBK, un.b_row0, full_bar(st));
           tma_load_2d(b_dst + (BN / 2) * kBK * 2, &p.tb[1], kb * kBK, un.b_row0, full_bar(st));
@@ -933,12 +982,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       };
       // The weights of the first unit's first stages are fetched while the
       // previous kernel finishes; the activations only after pdl_wait().
+      // (a pair: the even CTA expects both CTAs' bytes)
+      constexpr uint32_t kTxBytes = (PAIR ? 2 : 1) * C::kStageBytes;
+      auto unit_of = [&](int u) { return PAIR ? pair_unit(p, u, bn_rows, prank) : decode_unit(p, u, bn_rows); };
       int pre = 0;
-      if (p.const_op != 0 && blockIdx.x < p.num_units) {
-        const Unit un = decode_unit(p, blockIdx.x, bn_rows);
+      if (p.const_op != 0 && u0 < p.num_units) {
+        const Unit un = unit_of(u0);
         pre = min(S, un.kb_end - un.kb_begin);
         for (int i = 0; i < pre; ++i) {  // fresh ring: every stage is free
-          mbar_arrive_expect_tx(full_bar(i), C::kStageBytes);
+          if (mma_cta) mbar_arrive_expect_tx(full_bar(i), kTxBytes);
           if (p.const_op == 1)
             load_a(i, un, un.kb_begin + i);
           else
@@ -948,8 +1000,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       }
       pdl_wait();
       int g = 0;  // k-blocks issued by this CTA
-      for (int u = blockIdx.x; u < p.num_units && !failed; u += gridDim.x) {
-        const Unit un = decode_unit(p, u, bn_rows);
+      for (int u = u0; u < p.num_units && !failed; u += ustep) {
+        const Unit un = unit_of(u);
         for (int kb = un.kb_begin; kb < un.kb_end; ++kb, ++g) {
           if (g < pre) {  // the stage's constant half is already in flight
             if (p.const_op == 1)
@@ -961,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               failed = true;
               break;
             }
-            mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
+            if (mma_cta) mbar_arrive_expect_tx(full_bar(stage), kTxBytes);
             load_a(stage, un, kb);
             load_b(stage, un, kb);
           }
@@ -976,8 +1028,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       if (failed) {
         *abort_flag = 1;
         report_timeout(p.status, 0x10 + 0);
-        // drain: every issued load must land before the CTA exits
-        for (int s = 0; s < S; ++s)
+        // drain: every issued load must land before the CTA exits (a pair's odd CTA
+        // cannot see its loads land: the even CTA's drain and the final cluster
+        // barrier cover them)
+        for (int s = 0; s < S && mma_cta; ++s)
           if (issued_mask & (1u << s)) {
             volatile int never = 0;
             mbar_wait(full_bar(s), (parity_mask >> s) & 1, kDrainNs, &never);
@@ -985,16 +1039,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    if (lane == 0 && mma_cta) {
+      // ---------------- MMA issuer (a pair: the even CTA's, for both)
       // kind::f16 operand formats: bf16 (1) or fp16 (0) for A and B
-      const uint32_t idesc = p.f16 ? (idesc_bf16_f32(kBM, BN) & ~((7u << 7) | (7u << 10))) : idesc_bf16_f32(kBM, BN);
+      constexpr int kM = PAIR ? 2 * kBM : kBM;
+      const uint32_t idesc = p.f16 ? (idesc_bf16_f32(kM, BN) & ~((7u << 7) | (7u << 10))) : idesc_bf16_f32(kM, BN);
       int stage = 0;
       uint32_t ph = 0;
       int it = 0;
       bool failed = false, issued_any = false;
-      for (int u = blockIdx.x; u < p.num_units && !failed; u += gridDim.x, ++it) {
-        const Unit un = decode_unit(p, u, bn_rows);
+      for (int u = u0; u < p.num_units && !failed; u += ustep, ++it) {
+        const Unit un = PAIR ? pair_unit(p, u, bn_rows, prank) : decode_unit(p, u, bn_rows);
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
         if (!mbar_wait(tempty_bar(acc), aph ^ 1, budget, abort_flag)) {
@@ -1014,24 +1069,37 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // advance 16 elements (32 bytes) along K inside the swizzle atom
-            tc_mma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                        (kb > un.kb_begin || kk > 0) ? 1u : 0u);
+            if constexpr (PAIR)
+              tc_mma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                               (kb > un.kb_begin || kk > 0) ? 1u : 0u);
+            else
+              tc_mma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                          (kb > un.kb_begin || kk > 0) ? 1u : 0u);
           }
           issued_any = true;
-          tc_commit(empty_bar(stage));
+          if constexpr (PAIR)
+            tc_commit_pair(empty_bar(stage), kPairMask);  // the stage is free in both CTAs
+          else
+            tc_commit(empty_bar(stage));
           if (++stage == S) {
             stage = 0;
             ph ^= 1;
           }
         }
         if (failed) break;
-        tc_commit(tfull_bar(acc));
+        if constexpr (PAIR)
+          tc_commit_pair(tfull_bar(acc), kPairMask);  // both CTAs' halves of D are ready
+        else
+          tc_commit(tfull_bar(acc));
       }
       if (failed) {
         *abort_flag = 1;
         report_timeout(p.status, 0x10 + 1);
         if (issued_any) {
-          tc_commit(drain_bar);
+          if constexpr (PAIR)
+            tc_commit_pair(drain_bar, (uint16_t)(1u << lead_rank));
+          else
+            tc_commit(drain_bar);
           volatile int never = 0;
           mbar_wait(drain_bar, 0, kDrainNs, &never);
         }
@@ -1061,8 +1129,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
     int it = 0;
     bool failed = false;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
-      const Unit un = decode_unit(p, u, bn_rows);
+    for (int u = u0; u < p.num_units; u += ustep, ++it) {
+      const Unit un = PAIR ? pair_unit(p, u, bn_rows, prank) : decode_unit(p, u, bn_rows);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
@@ -1107,7 +1175,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         tc_fence_after();
         run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane, reinterpret_cast<float*>(smem));
         tc_fence_before();
-        mbar_arrive(tempty_bar(acc));
+        if constexpr (PAIR) {  // one lane a warp, on the even CTA's barrier
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(map_shared_rank(tempty_bar(acc), lead_rank));
+        } else {
+          mbar_arrive(tempty_bar(acc));
+        }
       }
     }
     if (failed) {
@@ -1135,11 +1208,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     cluster_sync_all();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    // neither CTA of a pair leaves (or frees TMEM, a collective step) while the
+    // other's copies or the pair's MMAs may still use its memory
+    __syncwarp();
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
@@ -1180,23 +1263,25 @@ bool make_tma_2d_16b(CUtensorMap* m, const void* ptr, int rows, int cols, int bo
 
 namespace {
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR = false>
 cudaError_t configure() {
-  static cudaError_t st = cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               TcCfg<BN, EPI>::kSmemBytes);  // once per instantiation
+  static cudaError_t st =
+      cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           TcCfg<BN, EPI, PAIR>::kSmemBytes);  // once per instantiation
   return st;
 }
 
-// Launch configuration of a decode GEMM: clusters of `splits` CTAs along x.
-template <int BN, int EPI>
-void cluster_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, int splits, cudaStream_t s) {
+// Launch configuration of a clustered GEMM: clusters of `csize` CTAs along x
+// (a decode GEMM's K splits, or a CTA pair).
+template <int BN, int EPI, bool PAIR = false>
+void cluster_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, int csize, cudaStream_t s) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(grid);
   cfg->blockDim = dim3(kThreads);
-  cfg->dynamicSmemBytes = TcCfg<BN, EPI>::kSmemBytes;
+  cfg->dynamicSmemBytes = TcCfg<BN, EPI, PAIR>::kSmemBytes;
   cfg->stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = splits;
+  attr[0].val.clusterDim.x = csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1205,18 +1290,18 @@ void cluster_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid
   cfg->numAttrs = 2;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t s) {
-  cudaError_t e = configure<BN, EPI>();
+  cudaError_t e = configure<BN, EPI, PAIR>();
   if (e != cudaSuccess) return e;
-  if constexpr (is_cluster_epi<EPI>()) {
+  if constexpr (is_cluster_epi<EPI>() || PAIR) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    cluster_config<BN, EPI>(&cfg, attr, grid, p.k_splits, s);
-    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, EPI>, p);
+    cluster_config<BN, EPI, PAIR>(&cfg, attr, grid, PAIR ? 2 : p.k_splits, s);
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, EPI, PAIR>, p);
     if (e != cudaSuccess) return e;
   } else {
-    launch_pdl(tc_gemm_kernel<BN, EPI>, grid, kThreads, TcCfg<BN, EPI>::kSmemBytes, s, p);
+    launch_pdl(tc_gemm_kernel<BN, EPI, PAIR>, grid, kThreads, TcCfg<BN, EPI, PAIR>::kSmemBytes, s, p);
   }
   return cudaGetLastError();
 }
@@ -1229,34 +1314,50 @@ int max_clusters(int splits) {
   cluster_config<BN, EPI>(&cfg, attr, splits, splits, nullptr);
   cfg.numAttrs = 1;  // the cluster shape alone
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, EPI>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, EPI, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
 }
 
+// CTA-pair (M = 256) instantiations: the prefill epilogues, B halves of 96-128 rows.
 template <int BN, int EPI>
-cudaError_t launch_if(const TcParams& p, int grid, cudaStream_t s) {
+constexpr bool tc_pair_supported() {
+  if (EPI == (int)Epi::kQkv) return BN == 256;  // whole heads
+  if (EPI == (int)Epi::kResid || EPI == (int)Epi::kSwiglu || EPI == (int)Epi::kRelu2 || EPI == (int)Epi::kXielu ||
+      EPI == (int)Epi::kStore)
+    return BN == 192 || BN == 224 || BN == 256;
+  return false;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_if(const TcParams& p, bool pair, int grid, cudaStream_t s) {
+  if (pair) {
+    if constexpr (tc_pair_supported<BN, EPI>())
+      return launch_one<BN, EPI, true>(p, grid, s);
+    else
+      return cudaErrorInvalidValue;
+  }
   if constexpr (tc_supported<BN, EPI>())
-    return launch_one<BN, EPI>(p, grid, s);
+    return launch_one<BN, EPI, false>(p, grid, s);
   else
     return cudaErrorInvalidValue;
 }
 
 template <int BN>
-cudaError_t dispatch_epi(const TcParams& p, Epi epi, int grid, cudaStream_t s) {
+cudaError_t dispatch_epi(const TcParams& p, Epi epi, bool pair, int grid, cudaStream_t s) {
   switch (epi) {
-    case Epi::kStore: return launch_if<BN, (int)Epi::kStore>(p, grid, s);
-    case Epi::kResid: return launch_if<BN, (int)Epi::kResid>(p, grid, s);
-    case Epi::kQkv: return launch_if<BN, (int)Epi::kQkv>(p, grid, s);
-    case Epi::kSwiglu: return launch_if<BN, (int)Epi::kSwiglu>(p, grid, s);
-    case Epi::kRelu2: return launch_if<BN, (int)Epi::kRelu2>(p, grid, s);
-    case Epi::kXielu: return launch_if<BN, (int)Epi::kXielu>(p, grid, s);
-    case Epi::kPartialT: return launch_if<BN, (int)Epi::kPartialT>(p, grid, s);
-    case Epi::kDecQkv: return launch_if<BN, (int)Epi::kDecQkv>(p, grid, s);
-    case Epi::kDecResid: return launch_if<BN, (int)Epi::kDecResid>(p, grid, s);
-    case Epi::kDecAct: return launch_if<BN, (int)Epi::kDecAct>(p, grid, s);
+    case Epi::kStore: return launch_if<BN, (int)Epi::kStore>(p, pair, grid, s);
+    case Epi::kResid: return launch_if<BN, (int)Epi::kResid>(p, pair, grid, s);
+    case Epi::kQkv: return launch_if<BN, (int)Epi::kQkv>(p, pair, grid, s);
+    case Epi::kSwiglu: return launch_if<BN, (int)Epi::kSwiglu>(p, pair, grid, s);
+    case Epi::kRelu2: return launch_if<BN, (int)Epi::kRelu2>(p, pair, grid, s);
+    case Epi::kXielu: return launch_if<BN, (int)Epi::kXielu>(p, pair, grid, s);
+    case Epi::kPartialT: return launch_if<BN, (int)Epi::kPartialT>(p, pair, grid, s);
+    case Epi::kDecQkv: return launch_if<BN, (int)Epi::kDecQkv>(p, pair, grid, s);
+    case Epi::kDecResid: return launch_if<BN, (int)Epi::kDecResid>(p, pair, grid, s);
+    case Epi::kDecAct: return launch_if<BN, (int)Epi::kDecAct>(p, pair, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -1298,6 +1399,10 @@ int tc_gemm_units(const TcGemmDesc& d) {
   return mt * nt * d.k_splits;
 }
 
+namespace {
+bool is_dec(Epi e) { return e == Epi::kDecQkv || e == Epi::kDecResid || e == Epi::kDecAct; }
+}  // namespace
+
 cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, unsigned long long wait_ns,
                            cudaStream_t s, const char** why) {
   TcParams p;
@@ -1334,9 +1439,16 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
     p.a_tiles[i + 1] = d.a_paired ? (d.a[0].rows + a_box - 1) / a_box : p.a_tiles[i] + (d.a[i].rows + kBM - 1) / kBM;
   }
   p.a_paired = d.a_paired ? 1 : 0;
+  if (d.pair && (is_dec(d.epi) || d.epi == Epi::kPartialT || d.k_splits > 1 || d.na != 1 || d.a_paired ||
+                 max_ctas < 2)) {
+    *why = "tcgen05 GEMM: a CTA pair runs a prefill GEMM (one A segment, no K split)";
+    return cudaErrorInvalidValue;
+  }
+  // a pair's CTA loads half of the B tile: BN / 2 rows (a paired B's half is one segment's tile)
+  const int b_box = d.pair ? d.bn / 2 : bn_rows;
   p.b_tiles[0] = 0;
   for (int i = 0; i < d.nb; ++i) {
-    if (!make_map(&p.tb[i], d.b[i].ptr, d.b[i].rows, d.K, bn_rows, d.f16)) {
+    if (!make_map(&p.tb[i], d.b[i].ptr, d.b[i].rows, d.K, b_box, d.f16)) {
       *why = "cuTensorMapEncodeTiled failed for a B operand";
       return cudaErrorInvalidValue;
     }
@@ -1347,7 +1459,7 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
   p.b_paired = d.b_paired ? 1 : 0;
   p.f16 = d.f16 ? 1 : 0;
   p.const_op = d.const_op;
-  p.m_tiles = p.a_tiles[d.na];
+  p.m_tiles = d.pair ? (d.a[0].rows + 2 * kBM - 1) / (2 * kBM) : p.a_tiles[d.na];  // a pair: 256-row tiles
   p.n_tiles = d.b_paired ? (d.b[0].rows + bn_rows - 1) / bn_rows : p.b_tiles[d.nb];
   p.num_kb = (d.K + kBK - 1) / kBK;
   p.k_splits = d.k_splits < 1 ? 1 : (d.k_splits > p.num_kb ? p.num_kb : d.k_splits);
@@ -1374,14 +1486,15 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
   p.status = st;
   p.wait_ns = wait_ns;
   if (p.num_units == 0) return cudaSuccess;
-  const int grid = p.num_units < max_ctas ? p.num_units : max_ctas;
+  // a pair: two CTAs per unit, whole pairs
+  const int grid = d.pair ? 2 * std::min(p.num_units, max_ctas / 2) : std::min(p.num_units, max_ctas);
   cudaError_t e;
   switch (d.bn) {
-    case 64: e = dispatch_epi<64>(p, d.epi, grid, s); break;
-    case 128: e = dispatch_epi<128>(p, d.epi, grid, s); break;
-    case 192: e = dispatch_epi<192>(p, d.epi, grid, s); break;
-    case 224: e = dispatch_epi<224>(p, d.epi, grid, s); break;
-    default: e = dispatch_epi<256>(p, d.epi, grid, s); break;
+    case 64: e = dispatch_epi<64>(p, d.epi, d.pair, grid, s); break;
+    case 128: e = dispatch_epi<128>(p, d.epi, d.pair, grid, s); break;
+    case 192: e = dispatch_epi<192>(p, d.epi, d.pair, grid, s); break;
+    case 224: e = dispatch_epi<224>(p, d.epi, d.pair, grid, s); break;
+    default: e = dispatch_epi<256>(p, d.epi, d.pair, grid, s); break;
   }
   if (e == cudaErrorInvalidValue && !*why) *why = "tcgen05 GEMM: tile width not built for this epilogue";
   return e;

@@ -146,6 +146,10 @@ struct TcGemmDesc {
   int nb = 1;
   bool b_paired = false;  // B tile = halves from b[0] and b[1] at the same rows (gate/up)
   bool a_paired = false;  // A tile = 64 rows of a[0] over 64 rows of a[1] at the same rows (kDecAct)
+  // A CTA pair (cluster of 2, tcgen05 cta_group::2) computes each 256 x BN tile: the
+  // even CTA issues M = 256 MMAs over both CTAs' shared memory, each CTA loading its
+  // 128 A rows and half of B. Prefill epilogues, one A segment, no K split.
+  bool pair = false;
   bool f16 = false;       // A and B are fp16 (else bf16)
   int K = 0;              // inner dimension; every segment has row stride K
   int k_splits = 1;

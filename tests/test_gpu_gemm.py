@@ -37,6 +37,24 @@ def test_gemm_matches_fp64(M, N, K, bn):
     assert bad == 0, int(bad)
 
 
+@pytest.mark.parametrize("M,N,K,bn", [
+    (256, 256, 64, 256),      # one pair tile, one k-block
+    (512, 768, 1024, 256),    # several pair tiles and k-blocks
+    (300, 1000, 1000, 224),   # ragged M (the odd CTA's rows past M), N and K
+    (100, 400, 520, 192),     # the odd CTA's rows all past M, its B half of the last tile too
+    (2048, 4096, 4096, 256),  # more tiles than pairs: the persistent loop
+])
+def test_gemm_cta_pair_matches_fp64(M, N, K, bn):
+    # tcgen05 cta_group::2: 256-row tiles over two CTAs, each holding half of B
+    a, b = _operands(M, N, K, seed=3 * M + N + K)
+    c = debug_gemm_bf16(a.cuda(), b.cuda(), bn=bn, pair=True)
+    torch.cuda.synchronize()
+    ref = a.double() @ b.double().T
+    bound = 2.0 ** -8 * ref.abs() + 1e-4 * ref.pow(2).mean().sqrt()
+    bad = ((c.double().cpu() - ref).abs() > bound).sum()
+    assert bad == 0, int(bad)
+
+
 @pytest.mark.parametrize("M,N,K,splits", [(64, 384, 4096, 4), (5, 1000, 1000, 3), (64, 6144, 512, 2)])
 def test_gemm_split_partials(M, N, K, splits):
     a, b = _operands(M, N, K, seed=7 * M + N)
