@@ -1388,17 +1388,6 @@ int tc_dec_max_clusters(int bn, Epi epi, int splits) {
   return c > 0 ? c : 0;
 }
 
-int tc_gemm_units(const TcGemmDesc& d) {
-  const int bn_rows = d.b_paired ? d.bn / 2 : d.bn;
-  int mt = 0, nt = 0;
-  for (int i = 0; i < d.na; ++i) mt += (d.a[i].rows + kBM - 1) / kBM;
-  if (d.b_paired)
-    nt = (d.b[0].rows + bn_rows - 1) / bn_rows;
-  else
-    for (int i = 0; i < d.nb; ++i) nt += (d.b[i].rows + bn_rows - 1) / bn_rows;
-  return mt * nt * d.k_splits;
-}
-
 namespace {
 bool is_dec(Epi e) { return e == Epi::kDecQkv || e == Epi::kDecResid || e == Epi::kDecAct; }
 }  // namespace

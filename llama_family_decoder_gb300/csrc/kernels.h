@@ -166,9 +166,6 @@ struct TcGemmDesc {
 // columns x box_rows rows, 128-byte swizzle, zero fill out of bounds.
 bool make_tma_2d_16b(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows, bool f16);
 
-// Number of work units (tiles x splits) the descriptor produces.
-int tc_gemm_units(const TcGemmDesc& d);
-
 cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, unsigned long long wait_ns,
                            cudaStream_t s, const char** why);
 
