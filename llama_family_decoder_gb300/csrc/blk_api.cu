@@ -1349,6 +1349,8 @@ blk_status blk_qkv_rope(blk_handle* h, const void* y, const blk_weights* w, int 
   if (!aligned16(y) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return fail(BLK_ERR_ALIGNMENT, "alignment");
   if (!w->wq || !w->wk || !w->wv) return fail(BLK_ERR_INVALID_ARG, "wq/wk/wv NULL");
   if (d.qk_norm && (!w->q_norm_g || !w->k_norm_g)) return fail(BLK_ERR_INVALID_ARG, "q/k norm gains NULL");
+  if (d.qk_norm && (!aligned16(w->q_norm_g) || !aligned16(w->k_norm_g)))
+    return fail(BLK_ERR_ALIGNMENT, "q/k norm gains not 16-byte aligned");
   if (!pos0 && seq > d.max_seq) return fail(BLK_ERR_INVALID_ARG, "seq exceeds max_seq");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d.dtype == BLK_BF16) return bf16_qkv(h, y, w, batch, seq, pos0, q, k, v, s);

@@ -286,7 +286,10 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
       // the input RMSNorm's 1/rms, applied here instead of to the GEMM's A rows
       const float rs = (e.row_scale && row_ok) ? e.row_scale[row] : 1.0f;
       const bool f16 = e.qkv_f16 != 0;
-#pragma unroll 1
+      int qk_heads = 0;  // the tile's q/k heads (bit hh), handled after the loop
+      uint16_t* qk_dst[BN / 128];
+      bool qk_ok = false;
+#pragma unroll
       for (int hh = 0; hh < BN / 128; ++hh) {
         const int head = (un.b_row0 >> 7) + hh;
         const uint32_t tcol = taddr + hh * 128;
@@ -339,43 +342,82 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
           }
           continue;
         }
-        float r = 1.0f;
-        const __nv_bfloat16* gain = nullptr;
-        if (e.qk_norm) {
-          gain = reinterpret_cast<const __nv_bfloat16*>(seg == 0 ? e.q_gain : e.k_gain);
-          float ss = 0.f;
-#pragma unroll 1
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            float v0[16], v1[16];
-            tmem_ld16(tcol + c0, v0);
-            tmem_ld16(tcol + c0 + 16, v1);
-            tc_wait_ld();
+        qk_heads |= 1 << hh;  // q or k: normed and rotated below, both heads of the tile at once
+        qk_dst[hh] = dst;
+        qk_ok = store_ok;
+      }
+      if (qk_heads) {
+        // q/k heads: the optional RMSNorm per head, then the rotary with the row's (cos, sin)
+        // read once for the tile's heads (16-byte loads, a 16-pair chunk at a time)
+        const int nh = BN / 128;
+        const __nv_bfloat16* gain =
+            e.qk_norm ? reinterpret_cast<const __nv_bfloat16*>(seg == 0 ? e.q_gain : e.k_gain) : nullptr;
+        float rn[BN / 128];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) ss += v0[j] * v0[j] + v1[j] * v1[j];
+        for (int hh = 0; hh < nh; ++hh) {
+          rn[hh] = 1.0f;
+          if (gain) {
+            float ss = 0.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+              float v0[16], v1[16];
+              tmem_ld16(taddr + hh * 128 + c0, v0);
+              tmem_ld16(taddr + hh * 128 + c0 + 16, v1);
+              tc_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) ss += v0[j] * v0[j] + v1[j] * v1[j];
+            }
+            rn[hh] = rsqrtf(ss * rs * rs / 128.0f + e.eps);
           }
-          r = rsqrtf(ss * rs * rs / 128.0f + e.eps);
         }
 #pragma unroll 1
         for (int i0 = 0; i0 < 64; i0 += 16) {
-          float x1[16], x2[16];
-          tmem_ld16(tcol + i0, x1);
-          tmem_ld16(tcol + 64 + i0, x2);
-          tc_wait_ld();
-          float y1[16], y2[16];
+          float2 sc[16];
+          const float4* cs4 = reinterpret_cast<const float4*>(cs + i0);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float a = x1[j] * rs, c = x2[j] * rs;
-            if (gain) {
-              a = a * r * __bfloat162float(gain[i0 + j]);
-              c = c * r * __bfloat162float(gain[64 + i0 + j]);
-            }
-            const float2 sc = cs[i0 + j];
-            y1[j] = a * sc.x - c * sc.y;
-            y2[j] = c * sc.x + a * sc.y;
+          for (int j = 0; j < 8; ++j) {
+            const float4 f = cs4[j];
+            sc[2 * j] = make_float2(f.x, f.y);
+            sc[2 * j + 1] = make_float2(f.z, f.w);
           }
-          if (store_ok) {
-            store16_2b(dst + i0, y1, f16);
-            store16_2b(dst + 64 + i0, y2, f16);
+          float g1[16], g2[16];
+          if (gain) {
+            const uint4* ga = reinterpret_cast<const uint4*>(gain + i0);
+            const uint4* gb = reinterpret_cast<const uint4*>(gain + 64 + i0);
+            const uint4 a0 = ga[0], a1 = ga[1], b0 = gb[0], b1 = gb[1];
+            const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float2 fa = unpack_bf16x2(wa[j]), fb = unpack_bf16x2(wb[j]);
+              g1[2 * j] = fa.x;
+              g1[2 * j + 1] = fa.y;
+              g2[2 * j] = fb.x;
+              g2[2 * j + 1] = fb.y;
+            }
+          }
+#pragma unroll
+          for (int hh = 0; hh < nh; ++hh) {
+            if (!((qk_heads >> hh) & 1)) continue;
+            float x1[16], x2[16];
+            tmem_ld16(taddr + hh * 128 + i0, x1);
+            tmem_ld16(taddr + hh * 128 + 64 + i0, x2);
+            tc_wait_ld();
+            float y1[16], y2[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float a = x1[j] * rs, c = x2[j] * rs;
+              if (gain) {
+                a = a * rn[hh] * g1[j];
+                c = c * rn[hh] * g2[j];
+              }
+              y1[j] = a * sc[j].x - c * sc[j].y;
+              y2[j] = c * sc[j].x + a * sc[j].y;
+            }
+            if (qk_ok) {
+              store16_2b(qk_dst[hh] + i0, y1, f16);
+              store16_2b(qk_dst[hh] + 64 + i0, y2, f16);
+            }
           }
         }
       }
