@@ -91,3 +91,16 @@ def test_stage_argument_checks_on_host(L):
     assert L.blk_forward(None, None, 1, 1, None, None, -1, None, None, 0, None, None) == 1
     assert L.blk_workspace_bytes(None, 1, 1, 0) == 0
     assert L.blk_destroy(None) == 0
+
+
+def test_debug_gemm_argument_checks_on_host(L):
+    # the bare GEMM's sizes, split and CTA-pair options are checked before any device work
+    a, b, c = (ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000))
+    gemm = L.blk_debug_gemm_bf16
+    assert gemm(a, b, c, 256, 256, 64, 96, 1, 0, None) == 1    # a tile width not built
+    assert gemm(a, b, c, 256, 256, 60, 256, 1, 0, None) == 1   # K not a multiple of 8
+    assert gemm(a, b, c, 256, 256, 64, 256, 2, 0, None) == 1   # split-K needs 64-wide tiles
+    assert gemm(a, b, c, 256, 256, 64, 64, 2, 1, None) == 1    # a CTA pair takes no K split
+    assert gemm(a, b, c, 256, 256, 64, 128, 1, 1, None) == 1   # ... and tiles of 192 columns or more
+    assert b"pair" in L.blk_last_error_message()
+    assert gemm(ctypes.c_void_p(0x1008), b, c, 256, 256, 64, 256, 1, 1, None) == 3  # misaligned
