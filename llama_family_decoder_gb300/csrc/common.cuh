@@ -67,7 +67,9 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
 // ---------------------------------------------------------------- warp reductions
 
 // 1 / (1 + e^-g): the attention gate of "afmoe" (0 at g = -inf, 1 at +inf).
-__device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + __expf(-g)); }
+// 1 / (1 + e^-g) with the fast reciprocal-based division (2 ulp; for g below about -87
+// the denominator passes 2^126 and the result is 0, as the true value rounds in fp16)
+__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

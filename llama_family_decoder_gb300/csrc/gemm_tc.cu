@@ -202,7 +202,8 @@ __device__ __forceinline__ void store16_2b(void* dst, const float* v, bool f16) 
   reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// g / (1 + e^-g) with the fast division, as sigmoid_f
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // e^x - 1 for x <= 0 to well within bf16 output precision: the Taylor series
 // x + x^2/2! + ... + x^5/5! near 0 (truncation below 1e-9 relative for |x| < 1/16),
