@@ -187,13 +187,16 @@ __global__ void __launch_bounds__(kResidThreads) post_resid_kernel(
   if (r >= rows) return;
   const size_t sstride = (size_t)rows * ldc;
   const int nv = n / 4;
-  float4 o[VPT], a[VPT];
+  float4 o[VPT], a[VPT], rr[VPT];
   float ss = 0.f, ssa = 0.f;
+  // the residual is loaded with the sublayer's output: it does not wait for the post-norm
 #pragma unroll
   for (int j = 0; j < VPT; ++j) {
     const int v = threadIdx.x + j * kResidThreads;
     a[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    rr[j] = a[j];
     if (v < nv) {
+      rr[j] = ld4<TR>(resid + (size_t)r * n + 4 * v);
       a[j] = split_sum4(C, splits, sstride, (size_t)r * ldc + 4 * v);
       ssa += a[j].x * a[j].x + a[j].y * a[j].y + a[j].z * a[j].z + a[j].w * a[j].w;
     }
@@ -215,9 +218,9 @@ __global__ void __launch_bounds__(kResidThreads) post_resid_kernel(
     const int v = threadIdx.x + j * kResidThreads;
     if (v < nv) {
       const float4 contrib = a[j];
-      const float4 rr = ld4<TR>(resid + (size_t)r * n + 4 * v);
       // the residual stream, summed in fp32
-      const float4 oo = make_float4(rr.x + contrib.x, rr.y + contrib.y, rr.z + contrib.z, rr.w + contrib.w);
+      const float4 oo =
+          make_float4(rr[j].x + contrib.x, rr[j].y + contrib.y, rr[j].z + contrib.z, rr[j].w + contrib.w);
       st4<TO>(out + (size_t)r * n + 4 * v, oo);
       if (out2) st4<TY>(out2 + (size_t)r * n + 4 * v, oo);
       if (tap) st4<TY>(tap + (size_t)r * n + 4 * v, contrib);
