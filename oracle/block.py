@@ -60,8 +60,11 @@ class RopeScaling:
     the published definitions).
 
     kind "yarn": YaRN's by-parts interpolation, "arcee" page ("Loading and
-    positions": YaRN, factor 20 over 4096 original positions). low / high are
-    YaRN's alpha / beta in rotations over the original context (1 and 32).
+    positions": YaRN, factor 20 over 4096 original positions, the model loaded
+    through transformers). low / high are the turn counts over the original
+    context that bound the blend (beta_slow 1 and beta_fast 32); the blend runs
+    linearly over the pair index between the indices where those turn counts
+    fall, as the published YaRN implementation builds it.
     kind "llama3": the frequency-dependent rule of Llama 3.1's rope_type llama3,
     "apertus" page ("The default load runs the same attention as eager": factor 8
     over 8192 original positions, rope_theta 12,000,000). low / high are its
@@ -144,11 +147,15 @@ def rope_inv_freq(head_dim, theta, scaling=None):
     With a scaling of factor s over L original positions, a frequency f has the
     wavelength lam = 2 pi / f and makes r = L / lam turns over the original
     context. Both published rules keep fast components, divide slow ones by s,
-    and blend in between:
-      llama3: kept when lam < L / high, divided when lam > L / low, otherwise
-              (1 - g) f / s + g f with g = (L / lam - low) / (high - low);
-      yarn:   g = clip((r - low) / (high - low), 0, 1), f' = (1 - g) f / s + g f
-              (YaRN's ramp over the turn count: alpha = low, beta = high).
+    and blend in between; they differ in what the blend is linear in:
+      llama3 (Llama 3.1's rule, "apertus"): kept when lam < L / high, divided
+              when lam > L / low, otherwise (1 - g) f / s + g f with
+              g = (L / lam - low) / (high - low), linear in the turn count;
+      yarn (the published YaRN implementation, which transformers runs for
+              "arcee"): the pair index where a component makes R turns is
+              i(R) = d ln(L / (2 pi R)) / (2 ln theta); with a = floor(i(high))
+              and b = ceil(i(low)) (clamped to [0, d - 1]), the weight of f / s is
+              clip((i - a) / (b - a), 0, 1), linear in the pair index.
     """
     i = np.arange(head_dim // 2, dtype=F64)
     f = np.power(F64(theta), -2.0 * i / head_dim)
@@ -161,8 +168,16 @@ def rope_inv_freq(head_dim, theta, scaling=None):
         out = (1.0 - g) * f / s + g * f
         out = np.where(lam < L / hi, f, out)
         return np.where(lam > L / lo, f / s, out)
-    g = np.clip((L / lam - lo) / (hi - lo), 0.0, 1.0)
-    return (1.0 - g) * f / s + g * f
+
+    def index_of_turns(r):
+        return head_dim * np.log(L / (2.0 * np.pi * r)) / (2.0 * np.log(F64(theta)))
+
+    a = max(np.floor(index_of_turns(hi)), 0.0)
+    b = min(np.ceil(index_of_turns(lo)), head_dim - 1.0)
+    if b == a:
+        b = a + 0.001
+    w = np.clip((i - a) / (b - a), 0.0, 1.0)  # weight of the interpolated frequency
+    return (1.0 - w) * f + w * f / s
 
 
 def rope_attention_factor(scaling):

@@ -105,6 +105,51 @@ def _scaling_ramp_reversed(head_dim, theta, scaling=None):
     return f * (f / s) / scaling.factor
 
 
+def _yarn_ramp_over_turns(head_dim, theta, scaling=None):
+    # YaRN's blend taken linear in the turn count r = L / lam (the paper's gamma(r))
+    # instead of the published implementation's ramp over the pair index
+    if scaling is None or scaling.kind != "yarn":
+        return _orig_inv_freq(head_dim, theta, scaling)
+    f = _orig_inv_freq(head_dim, theta)
+    r = scaling.original_max_position * f / (2 * np.pi)
+    g = np.clip((r - scaling.low) / (scaling.high - scaling.low), 0.0, 1.0)
+    return (1 - g) * f / scaling.factor + g * f
+
+
+def _yarn_unrounded_indices(head_dim, theta, scaling=None):
+    # the correction indices used as computed, without the floor / ceil
+    if scaling is None or scaling.kind != "yarn":
+        return _orig_inv_freq(head_dim, theta, scaling)
+    f = _orig_inv_freq(head_dim, theta)
+    L = scaling.original_max_position
+    idx = lambda r: head_dim * np.log(L / (2 * np.pi * r)) / (2 * np.log(theta))
+    a, b = idx(scaling.high), idx(scaling.low)
+    w = np.clip((np.arange(head_dim // 2) - a) / (b - a), 0.0, 1.0)
+    return (1 - w) * f + w * f / scaling.factor
+
+
+def _llama3_ramp_over_index(head_dim, theta, scaling=None):
+    # llama3's blend taken linear in the pair index between the band's edges
+    if scaling is None or scaling.kind != "llama3":
+        return _orig_inv_freq(head_dim, theta, scaling)
+    f = _orig_inv_freq(head_dim, theta)
+    L, s, lo, hi = scaling.original_max_position, scaling.factor, scaling.low, scaling.high
+    idx = lambda r: head_dim * np.log(L / (2 * np.pi * r)) / (2 * np.log(theta))
+    g = np.clip(1 - (np.arange(head_dim // 2) - idx(hi)) / (idx(lo) - idx(hi)), 0.0, 1.0)
+    return (1 - g) * f / s + g * f
+
+
+def _llama3_ramp_over_wavelength(head_dim, theta, scaling=None):
+    # llama3's blend taken linear in the wavelength instead of the turn count
+    if scaling is None or scaling.kind != "llama3":
+        return _orig_inv_freq(head_dim, theta, scaling)
+    f = _orig_inv_freq(head_dim, theta)
+    L, s, lo, hi = scaling.original_max_position, scaling.factor, scaling.low, scaling.high
+    lam = 2 * np.pi / f
+    g = np.clip(1 - (lam - L / hi) / (L / lo - L / hi), 0.0, 1.0)
+    return (1 - g) * f / s + g * f
+
+
 def _relu_not_squared(u):
     return np.maximum(np.asarray(u, dtype=F64), 0.0)
 
@@ -191,6 +236,10 @@ MUTATIONS = {
     "swiglu_gate_up_swapped": [("mlp", _mlp_swapped)],
     "missing_residual": [("_finish_rows", _finish_no_residual)],
     "rope_scaling_ramp_reversed": [("rope_inv_freq", _scaling_ramp_reversed)],
+    "yarn_ramp_over_turns": [("rope_inv_freq", _yarn_ramp_over_turns)],
+    "yarn_correction_indices_unrounded": [("rope_inv_freq", _yarn_unrounded_indices)],
+    "llama3_ramp_over_pair_index": [("rope_inv_freq", _llama3_ramp_over_index)],
+    "llama3_ramp_over_wavelength": [("rope_inv_freq", _llama3_ramp_over_wavelength)],
     "attn_window_one_too_wide": [("causal_gqa_attention", _attn_factory(window_slack=1))],
     "attn_window_one_too_narrow": [("causal_gqa_attention", _attn_factory(window_slack=-1))],
     "gate_from_raw_input": [("_finish_rows", _finish_gate_from_raw_input)],
@@ -220,6 +269,7 @@ PIN_TESTS = [
     pins.test_block_identity_and_taps,
     pins.test_llama3_scaling_keeps_fast_divides_slow_and_blends_between,
     pins.test_yarn_scaling_keeps_fast_divides_slow_and_scales_attention,
+    pins.test_rope_scaling_golden_values,
     lambda: pins.test_attention_window_brute_force(3),
     pins.test_attention_window_special_cases,
     lambda: pins.test_afmoe_block_brute_force(3, True, True, True),

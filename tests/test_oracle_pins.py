@@ -11,6 +11,8 @@ import math
 import os
 import zlib
 
+from fractions import Fraction
+
 import numpy as np
 import pytest
 
@@ -721,12 +723,35 @@ def test_llama3_scaling_keeps_fast_divides_slow_and_blends_between():
     np.testing.assert_allclose(f[slow], base[slow] / 8.0, rtol=1e-15)
     assert np.all(f[mid] < base[mid]) and np.all(f[mid] > base[mid] / 8.0)
     assert np.all(np.diff(f) < 0)  # still strictly decreasing with the dimension
-    # continuous at both ends of the blend: a frequency exactly on a boundary gets the same value
-    for lam_b, want in ((8192 / 4.0, 1.0), (8192 / 1.0, 1.0 / 8.0)):
-        sc = LLAMA3_APERTUS
-        fb = 2 * np.pi / lam_b
-        g = (sc.original_max_position / lam_b - sc.low) / (sc.high - sc.low)
-        assert abs(((1 - g) * fb / sc.factor + g * fb) / fb - want) < 1e-15
+
+
+def _golden_rope_cases():
+    with open(os.path.join(GOLDEN, "rope_scaling.json")) as fh:
+        return json.load(fh)["cases"]
+
+
+def test_rope_scaling_golden_values():
+    # hand-derived inverse frequencies of both published rules (tests/golden/rope_scaling.json):
+    # two small settings whose blend weights are exact fractions, YaRN at the "arcee"
+    # setting (pair indices 20 .. 46 of 64, from its floored and ceiled correction
+    # indices 20.94 and 45.03), and the llama3 band at the "apertus" setting
+    for c in _golden_rope_cases():
+        L = c["original_positions"] if "original_positions" in c else 2 * np.pi * c["original_positions_over_2pi"]
+        sc = oracle.RopeScaling(c["kind"], c["factor"], L, c["low"], c["high"])
+        d, theta = c["head_dim"], c["theta"]
+        got = oracle.rope_inv_freq(d, theta, sc)
+        if "multiplier_of_f" in c:
+            idx = c.get("indices", list(range(d // 2)))
+            for i, frac in zip(idx, c["multiplier_of_f"]):
+                want = float(Fraction(frac)) * theta ** (-2.0 * i / d)
+                assert abs(got[i] - want) <= 1e-14 * want, (c["name"], i, got[i], want)
+        else:
+            plain = theta ** (-2.0 * np.arange(d // 2) / d)
+            lo, hi = c["kept_below"], c["divided_from"]
+            np.testing.assert_array_equal(got[:lo], plain[:lo])
+            np.testing.assert_allclose(got[hi:], plain[hi:] / c["factor"], rtol=1e-15)
+            assert np.all(got[lo:hi] < plain[lo:hi] * (1 - 1e-12))
+            assert np.all(got[lo:hi] > plain[lo:hi] / c["factor"] * (1 + 1e-12))
 
 
 def test_yarn_scaling_keeps_fast_divides_slow_and_scales_attention():
