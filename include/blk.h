@@ -84,7 +84,11 @@ typedef enum { BLK_F32 = 0, BLK_BF16 = 1 } blk_dtype;
  * over 4096 positions on "arcee", "Loading and positions"; llama3 factor 8 over
  * 8192, rope_theta 12,000,000 on "apertus"). Both keep fast components, divide
  * slow ones by the factor and blend in between, after their published
- * definitions; YaRN also multiplies cos and sin by 0.1 ln(factor) + 1. */
+ * definitions: llama3 linearly in the turn count over the original context,
+ * YaRN (as its published implementation, which transformers runs) linearly in
+ * the pair index between the floored and ceiled indices where the components
+ * make rope_high and rope_low turns; YaRN also multiplies cos and sin by
+ * 0.1 ln(factor) + 1. */
 typedef enum {
   BLK_ROPE_PLAIN = 0,
   BLK_ROPE_YARN = 1,   /* rope_low / rope_high: turns over the original context (1 and 32) */
@@ -116,7 +120,8 @@ typedef struct {
   int sliding_window;  /* W > 0: query at position p sees keys at positions p - W + 1 .. p */
   int no_rope;         /* 1: no rotary (needs rope_type BLK_ROPE_PLAIN) */
   int attn_gate;       /* 1: sigmoid gate on the head outputs (weights.w_attn_gate) */
-  int sandwich_norm;   /* 1: post-norms of both sublayers (weights.post_attn_g, post_mlp_g) */
+  int sandwich_norm;   /* 1: post-norms of both sublayers (weights.post_attn_g, post_mlp_g); on the
+                          bf16 path it needs prepared weights (see blk_prepare_weights) */
 } blk_desc;
 
 /* Block weights: device pointers in the descriptor's dtype.
@@ -202,7 +207,12 @@ size_t blk_workspace_bytes(const blk_handle* h, int batch, int seq, int decode);
  * a decode step (T == 1) or a prefill chunk (T > 1; bf16 only; its keys and
  * values go to the cache, so the key/value taps are refused).
  * workspace: device scratch of at least blk_workspace_bytes(h, B, T, cache!=NULL).
- * out must not alias x. taps may be NULL. Errors: INVALID_ARG, ALIGNMENT,
+ * out must not alias x. taps may be NULL. A sandwich_norm block on the bf16
+ * path needs weights.prepared: each post-norm scales its sublayer's output to
+ * the size of the residual stream, and with it the rounding of that sublayer's
+ * GEMM operands; bf16 operands (all that bf16 weights allow) would spend the
+ * whole bf16 tolerance there, so such calls return UNSUPPORTED.
+ * Errors: INVALID_ARG, ALIGNMENT,
  * UNSUPPORTED, WORKSPACE, CACHE_FULL (checked on the host when the caller
  * passes host_lens_max >= 0, the largest lens[b] before the call; a prefill
  * chunk requires it), CUDA. */
@@ -306,7 +316,9 @@ blk_status blk_attn_gqa(blk_handle* h, const void* q, const void* k, const void*
 /* Stage: MLP sublayer with the residual add of its rows:
  * out[r] = resid[r] + down(act(h_normed[r])) for rows r < rows, shapes [rows, D].
  * workspace: device scratch of blk_stage_workspace_bytes(h, rows).
- * out may not alias h_normed; it may alias resid. */
+ * out may not alias h_normed; it may alias resid. On the bf16 path a
+ * sandwich_norm handle returns UNSUPPORTED (its bf16 h_normed rounding would be
+ * scaled up by the post-norm; blk_forward runs such blocks on prepared weights). */
 blk_status blk_mlp(blk_handle* h, const void* resid, const void* h_normed, const blk_weights* w,
                    int rows, void* out, void* workspace, size_t workspace_bytes, void* stream);
 
@@ -349,6 +361,10 @@ void blk_xielu_effective(float raw_alpha_p, float raw_alpha_n, float beta, float
  * the array's device address (cudaGetSymbolAddress, with that device current);
  * make that first call before any stream capture. It calls no cudaMalloc,
  * cudaFree or allocating library routine.
+ * A device-side wait that runs out (the limit of blk_debug_set_wait_timeout_ns,
+ * 2 s by default) cannot be returned by this asynchronous call, and there is no
+ * handle to read a status from: the call then writes NaN to every element of o
+ * (the status word that decides it sits in the same array, zeroed per call).
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA. */
 blk_status blk_attn_decode_noalloc(const void* q, const void* k, const void* v, const int* kv_lens, int batch,
                                    int n_heads, int n_kv_heads, int head_dim, int kv_stride, void* o, void* stream);
@@ -361,10 +377,16 @@ const char* blk_last_error_message(void);
 
 /* Debug knob: wall-time limit, in nanoseconds, of every device-side mbarrier
  * wait in later launches; <= 0 restores the default (2 s). A wait that runs
- * out records BLK_ERR_TIMEOUT in the handle's status word, waits (again with a
- * limit) for its own copies and MMAs in flight, frees its TMEM and returns,
- * leaving the CUDA context usable. Process-wide. */
+ * out records BLK_ERR_TIMEOUT in the handle's status word (blk_last_status),
+ * makes every role of its CTA stop, then waits (with a separate 2 s limit) for
+ * the CTA's copies and MMAs in flight, frees its TMEM and returns, leaving the
+ * CUDA context usable; the outputs of that call are invalid. Process-wide. */
 void blk_debug_set_wait_timeout_ns(long long ns);
+
+/* Status of the debug GEMM entry point (blk_debug_gemm_bf16, which has no
+ * handle), read after the caller has synchronised: BLK_OK or BLK_ERR_TIMEOUT.
+ * Clears the word. Reads device memory synchronously. Errors: CUDA. */
+blk_status blk_debug_last_status(void);
 
 /* Per-stage device timing of later blk_forward calls on this handle: when on,
  * each stage's launches are bracketed by CUDA events recorded on the caller's

@@ -48,10 +48,19 @@ struct blk_handle {
   StageProfile prof;
 };
 
+// Status word of the debug GEMM entry point (it runs without a handle).
+static __device__ DevStatus g_debug_status;
+
 namespace {
 
 thread_local std::string g_err;
 std::atomic<long long> g_wait_ns{2000000000LL};
+
+// Device address of g_debug_status on the current device (host code cannot use
+// the symbol itself as a device pointer).
+cudaError_t debug_status_address(DevStatus** out) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_debug_status);
+}
 
 blk_status fail(blk_status s, const std::string& msg) {
   g_err = msg;
@@ -911,6 +920,13 @@ blk_status check_weights(const blk_desc& d, const blk_weights* w) {
     return fail(w->w_attn_gate ? BLK_ERR_ALIGNMENT : BLK_ERR_INVALID_ARG, "attn_gate needs an aligned w_attn_gate");
   if (d.sandwich_norm && (!w->post_attn_g || !w->post_mlp_g || !aligned16(w->post_attn_g) || !aligned16(w->post_mlp_g)))
     return fail(BLK_ERR_INVALID_ARG, "sandwich_norm needs aligned post_attn_g and post_mlp_g");
+  // A sandwich post-norm rescales its sublayer's output to the size of the residual
+  // stream, and with it the relative error of that sublayer's GEMM operands. With bf16
+  // operands (the only type that meets bf16 weights) that error reaches the block's
+  // output at the size of its whole bf16 tolerance; the prepared fp16 operands keep it
+  // at a fraction of it. So the bf16 path runs sandwich blocks on prepared weights only.
+  if (d.dtype == BLK_BF16 && d.sandwich_norm && !w->prepared)
+    return fail(BLK_ERR_UNSUPPORTED, "sandwich_norm on the bf16 path needs prepared weights (blk_prepare_weights)");
   return BLK_OK;
 }
 
@@ -993,27 +1009,38 @@ blk_status blk_create(const blk_desc* desc, blk_handle** out) {
     return cuda_fail(e, "blk_create: device query");
   }
   // RoPE table [max_seq][head_dim / 2] of (cos, sin), in double: inv_freq_i = theta^(-2i/d),
-  // stretched by the descriptor's scaling (a frequency f of wavelength lam = 2 pi / f makes
+  // stretched by the descriptor's scaling. A frequency f of wavelength lam = 2 pi / f makes
   // r = L / lam turns over the original context L; fast components are kept, slow ones
-  // divided by the factor s, and the rest blended: (1 - g) f / s + g f)
+  // divided by the factor s, and the rest blended. llama3 blends linearly in r:
+  // (1 - g) f / s + g f, g = (r - lo) / (hi - lo). YaRN, as its published implementation
+  // builds it, blends linearly in the pair index: the index where a component makes R turns
+  // is i(R) = d ln(L / (2 pi R)) / (2 ln theta), and between a = floor(i(hi)) and
+  // b = ceil(i(lo)) the weight of f / s grows from 0 to 1.
   const int half = d.head_dim / 2;
   std::vector<double> inv_freq(half);
   const double s_f = d.rope_factor, L = d.rope_orig_max_pos, lo = d.rope_low, hi = d.rope_high;
+  const double theta = (double)d.rope_theta, dd = (double)d.head_dim;
+  auto index_of_turns = [&](double r) { return dd * std::log(L / (2.0 * M_PI * r)) / (2.0 * std::log(theta)); };
+  double ya = 0.0, yb = 1.0;
+  if (d.rope_type == BLK_ROPE_YARN) {
+    ya = std::max(std::floor(index_of_turns(hi)), 0.0);
+    yb = std::min(std::ceil(index_of_turns(lo)), dd - 1.0);
+    if (yb == ya) yb = ya + 0.001;
+  }
   for (int i = 0; i < half; ++i) {
-    const double f = std::pow((double)d.rope_theta, -2.0 * i / (double)d.head_dim);
-    const double turns = d.rope_type == BLK_ROPE_PLAIN ? 0.0 : L * f / (2.0 * M_PI);
+    const double f = std::pow(theta, -2.0 * i / dd);
     double fi = f;
     if (d.rope_type == BLK_ROPE_LLAMA3) {
       const double lam = 2.0 * M_PI / f;
       if (lam > L / lo) {
         fi = f / s_f;
       } else if (lam >= L / hi) {
-        const double g = (turns - lo) / (hi - lo);
+        const double g = (L / lam - lo) / (hi - lo);
         fi = (1.0 - g) * f / s_f + g * f;
       }
     } else if (d.rope_type == BLK_ROPE_YARN) {
-      const double g = std::min(1.0, std::max(0.0, (turns - lo) / (hi - lo)));
-      fi = (1.0 - g) * f / s_f + g * f;
+      const double w = std::min(1.0, std::max(0.0, (i - ya) / (yb - ya)));
+      fi = (1.0 - w) * f + w * f / s_f;
     }
     inv_freq[i] = d.no_rope ? 0.0 : fi;  // no rotary: every angle 0, the identity rotation
   }
@@ -1421,6 +1448,10 @@ blk_status blk_mlp(blk_handle* h, const void* resid, const void* h_normed, const
   float* C = static_cast<float*>(c.take((size_t)rows * max_cols(d) * sizeof(float)));
   if (d.sandwich_norm && (!w->post_mlp_g || !aligned16(w->post_mlp_g)))
     return fail(BLK_ERR_INVALID_ARG, "sandwich_norm needs an aligned post_mlp_g");
+  // the stage's operand h_normed is the caller's bf16: a post-norm would scale its
+  // rounding up to the residual's size (the whole block runs it on prepared weights)
+  if (d.dtype == BLK_BF16 && d.sandwich_norm)
+    return fail(BLK_ERR_UNSUPPORTED, "the MLP stage of a sandwich_norm block takes the fp32 path or blk_forward");
   const void* g_post = d.sandwich_norm ? w->post_mlp_g : nullptr;
   if (d.dtype == BLK_BF16) {
     BLK_TRY(bf16_mlp_up(h, h_normed, rows, w, neur, s));
@@ -1539,9 +1570,26 @@ blk_status blk_debug_gemm_bf16(const void* a, const void* b, void* c, int M, int
     g.e.n_tok = M;
   }
   const char* why = nullptr;
-  cudaError_t e = launch_tc_gemm(g, sms, nullptr, (unsigned long long)g_wait_ns.load(),
-                                 static_cast<cudaStream_t>(stream), &why);
+  DevStatus* st = nullptr;
+  cudaError_t e = debug_status_address(&st);
+  if (e != cudaSuccess) return cuda_fail(e, "debug GEMM status word");
+  e = launch_tc_gemm(g, sms, st, (unsigned long long)g_wait_ns.load(), static_cast<cudaStream_t>(stream), &why);
   return e == cudaSuccess ? BLK_OK : cuda_fail(e, "debug GEMM", why);
+}
+
+blk_status blk_debug_last_status(void) {
+  DevStatus* dst = nullptr;
+  cudaError_t e = debug_status_address(&dst);
+  DevStatus st{0, 0};
+  if (e == cudaSuccess) e = cudaMemcpy(&st, dst, sizeof(st), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "blk_debug_last_status");
+  if (st.code != 0) {
+    cudaMemset(dst, 0, sizeof(DevStatus));
+    char buf[96];
+    snprintf(buf, sizeof(buf), "device wait timed out (site 0x%x)", st.where);
+    return fail((blk_status)st.code, buf);
+  }
+  return BLK_OK;
 }
 
 blk_status blk_attn_decode_noalloc(const void* q, const void* k, const void* v, const int* kv_lens, int batch,
@@ -1561,7 +1609,7 @@ blk_status blk_attn_decode_noalloc(const void* q, const void* k, const void* v, 
   if (e != cudaSuccess) return cuda_fail(e, "device query");
   const char* why = nullptr;
   e = launch_attn_decode_bf16_static(q, k, v, o, batch, n_heads, n_kv_heads, head_dim, kv_stride, kv_lens, sms,
-                                     static_cast<cudaStream_t>(stream), &why);
+                                     (unsigned long long)g_wait_ns.load(), static_cast<cudaStream_t>(stream), &why);
   return e == cudaSuccess ? BLK_OK : cuda_fail(e, "allocation-free decode attention", why);
 }
 
