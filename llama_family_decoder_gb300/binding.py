@@ -76,6 +76,7 @@ SIGNATURES = {
     "blk_error_string": (c_char_p, [c_int]),
     "blk_last_error_message": (c_char_p, []),
     "blk_debug_set_wait_timeout_ns": (None, [c_longlong]),
+    "blk_debug_last_status": (c_int, []),
     "blk_version": (c_char_p, []),
     "blk_profile_enable": (c_int, [c_void_p, c_int]),
     "blk_profile_collect": (c_int, [c_void_p, POINTER(ctypes.c_double), POINTER(c_longlong), c_int]),

@@ -140,6 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
   }
   __syncthreads();
   pdl_wait();  // the new key/value rows and q come from the previous kernel
+  // the ring stages the producer issued (with the parity of their last phase): an abort
+  // drains them after the CTA's final barrier
+  uint32_t issued = 0, parity = 0;
 
   if (warp == kCompute) {
     if (lane == 0) {
@@ -147,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
       tma_prefetch_desc(&p.tk);
       tma_prefetch_desc(&p.tv);
       int stage = 0;
-      uint32_t ph = 0, issued = 0, parity = 0;
+      uint32_t ph = 0;
       bool failed = false;
       const uint64_t stream_once = l2_policy_evict_first();  // the cache is read once per step
       int u = blockIdx.x;
@@ -189,188 +192,192 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
       if (failed) {
         *abort_flag = 1;
         report_timeout(p.status, 0x30);
-        volatile int never = 0;
-        for (int st = 0; st < kStages; ++st)
-          if (issued & (1u << st)) mbar_wait(full(st), (parity >> st) & 1, kDrainNs, &never);
       }
     }
-    return;
-  }
-
-  // ---------------- compute warps 0..3
-  const int g = lane >> 2, tq = lane & 3;
-  const float sl2 = kLog2e * rsqrtf((float)kD);
-  int stage = 0, n_sync = 0;
-  uint32_t ph = 0;
-  bool failed = false;
-  auto csync_all = [&]() {  // the 128 compute threads meet (bounded)
-    mbar_arrive(csync);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(csync, n_sync & 1, budget, abort_flag));
-    ++n_sync;
-    return ok;
-  };
-  for (int k = 0; !failed; ++k) {
-    const int slot = k % kUq;
-    if (!__all_sync(0xffffffffu, mbar_wait(uq_full(slot), (k / kUq) & 1, budget, abort_flag))) {
-      failed = true;
-      break;
-    }
-    const int u = unit_q[slot];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(uq_empty(slot));
-    if (u >= p.units) break;
-    const DecodeUnit un = decode_unit(p, u);
-    // Q fragments straight from global memory: rows = the group's heads (zero past G)
-    const __nv_bfloat16* qg = p.q + ((size_t)un.b * p.H + (size_t)un.kvh * G) * kD;
-    uint32_t qf[8][4];
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int c = kk * 16 + 2 * tq;
-      qf[kk][0] = g < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)g * kD + c) : 0u;
-      qf[kk][1] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)(g + 8) * kD + c) : 0u;
-      qf[kk][2] = g < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)g * kD + c + 8) : 0u;
-      qf[kk][3] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)(g + 8) * kD + c + 8) : 0u;
-    }
-    float acc[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-    for (int t = 0; t < un.n_tiles; ++t) {
-      if (!__all_sync(0xffffffffu, mbar_wait(full(stage), ph, budget, abort_flag))) {
+  } else {
+    // ---------------- compute warps 0..3
+    const int g = lane >> 2, tq = lane & 3;
+    const float sl2 = kLog2e * rsqrtf((float)kD);
+    int stage = 0, n_sync = 0;
+    uint32_t ph = 0;
+    bool failed = false;
+    auto csync_all = [&]() {  // the 128 compute threads meet (bounded)
+      mbar_arrive(csync);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(csync, n_sync & 1, budget, abort_flag));
+      ++n_sync;
+      return ok;
+    };
+    for (int k = 0; !failed; ++k) {
+      const int slot = k % kUq;
+      if (!__all_sync(0xffffffffu, mbar_wait(uq_full(slot), (k / kUq) & 1, budget, abort_flag))) {
         failed = true;
         break;
       }
-      const uint32_t sK = smem_u32(ring + stage * kStageBytes), sV = sK + 2 * kHalfBytes;
-      const int n0 = t * kTileKeys + warp * 16;  // this warp's 16 keys (within the unit)
-      const int valid = un.n_keys - n0;           // < 16: the rest of this warp's V rows are stale
-      if (valid < 16) {
-        // cache slots past the valid keys may hold anything: zero this warp's stale V rows
-        uint8_t* vb = ring + stage * kStageBytes + 2 * kHalfBytes;
-        for (int i = lane; i < 16 * 16; i += 32) {
-          const int rr = i >> 4, C = i & 15;
-          if (rr >= valid) *reinterpret_cast<uint4*>(vb + tsw(warp * 16 + rr, C)) = make_uint4(0, 0, 0, 0);
-        }
-        __syncwarp();
-      }
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const int u = unit_q[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(uq_empty(slot));
+      if (u >= p.units) break;
+      const DecodeUnit un = decode_unit(p, u);
+      // Q fragments straight from global memory: rows = the group's heads (zero past G)
+      const __nv_bfloat16* qg = p.q + ((size_t)un.b * p.H + (size_t)un.kvh * G) * kD;
+      uint32_t qf[8][4];
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const int mi = lane >> 3, rr = lane & 7;
-        uint32_t bb[4];
-        ldsm_x4(sK + tsw(warp * 16 + rr + 8 * (mi >> 1), kk * 2 + (mi & 1)), bb);
-        mma_bf16(sc[0], qf[kk], bb[0], bb[1]);
-        mma_bf16(sc[1], qf[kk], bb[2], bb[3]);
+        const int c = kk * 16 + 2 * tq;
+        qf[kk][0] = g < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)g * kD + c) : 0u;
+        qf[kk][1] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)(g + 8) * kD + c) : 0u;
+        qf[kk][2] = g < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)g * kD + c + 8) : 0u;
+        qf[kk][3] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(qg + (size_t)(g + 8) * kD + c + 8) : 0u;
       }
-      float mx[2] = {-INFINITY, -INFINITY};
+      float acc[16][4];
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float x = sc[j][e] * sl2;
-          if (j * 8 + 2 * tq + (e & 1) >= valid) x = -INFINITY;
-          sc[j][e] = x;
-          mx[e >> 1] = fmaxf(mx[e >> 1], x);
+      for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+      float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+      for (int t = 0; t < un.n_tiles; ++t) {
+        if (!__all_sync(0xffffffffu, mbar_wait(full(stage), ph, budget, abort_flag))) {
+          failed = true;
+          break;
         }
-      float alpha[2], mu[2];
+        const uint32_t sK = smem_u32(ring + stage * kStageBytes), sV = sK + 2 * kHalfBytes;
+        const int n0 = t * kTileKeys + warp * 16;  // this warp's 16 keys (within the unit)
+        const int valid = un.n_keys - n0;           // < 16: the rest of this warp's V rows are stale
+        if (valid < 16) {
+          // cache slots past the valid keys may hold anything: zero this warp's stale V rows
+          uint8_t* vb = ring + stage * kStageBytes + 2 * kHalfBytes;
+          for (int i = lane; i < 16 * 16; i += 32) {
+            const int rr = i >> 4, C = i & 15;
+            if (rr >= valid) *reinterpret_cast<uint4*>(vb + tsw(warp * 16 + rr, C)) = make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+        }
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int mi = lane >> 3, rr = lane & 7;
+          uint32_t bb[4];
+          ldsm_x4(sK + tsw(warp * 16 + rr + 8 * (mi >> 1), kk * 2 + (mi & 1)), bb);
+          mma_bf16(sc[0], qf[kk], bb[0], bb[1]);
+          mma_bf16(sc[1], qf[kk], bb[2], bb[3]);
+        }
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float x = sc[j][e] * sl2;
+            if (j * 8 + 2 * tq + (e & 1) >= valid) x = -INFINITY;
+            sc[j][e] = x;
+            mx[e >> 1] = fmaxf(mx[e >> 1], x);
+          }
+        float alpha[2], mu[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+          const float mnew = fmaxf(mrow[r], mx[r]);
+          mu[r] = mnew == -INFINITY ? 0.f : mnew;
+          alpha[r] = exp2f(mrow[r] - mu[r]);
+          mrow[r] = mnew;
+          lrow[r] *= alpha[r];
+        }
+        uint32_t a[4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float p0 = exp2f(sc[j][0] - mu[0]), p1 = exp2f(sc[j][1] - mu[0]);
+          const float p2 = exp2f(sc[j][2] - mu[1]), p3 = exp2f(sc[j][3] - mu[1]);
+          lrow[0] += p0 + p1;
+          lrow[1] += p2 + p3;
+          a[j * 2 + 0] = pack_bf16x2(p0, p1);
+          a[j * 2 + 1] = pack_bf16x2(p2, p3);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          acc[i][0] *= alpha[0];
+          acc[i][1] *= alpha[0];
+          acc[i][2] *= alpha[1];
+          acc[i][3] *= alpha[1];
+        }
+#pragma unroll
+        for (int dp = 0; dp < 8; ++dp) {
+          const int mi = lane >> 3, rr = lane & 7;
+          uint32_t bb[4];
+          ldsm_x4_t(sV + tsw(warp * 16 + rr + 8 * (mi & 1), dp * 2 + (mi >> 1)), bb);
+          mma_bf16(acc[2 * dp], a, bb[0], bb[1]);
+          mma_bf16(acc[2 * dp + 1], a, bb[2], bb[3]);
+        }
+        if (valid < 16) fence_proxy_async_smem();  // generic writes before the next TMA into this stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(stage));
+        if (++stage == kStages) {
+          stage = 0;
+          ph ^= 1;
+        }
+      }
+      if (failed) break;
+      // merge the four warps' softmax states (rows < G) and write this split's partial
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-        const float mnew = fmaxf(mrow[r], mx[r]);
-        mu[r] = mnew == -INFINITY ? 0.f : mnew;
-        alpha[r] = exp2f(mrow[r] - mu[r]);
-        mrow[r] = mnew;
-        lrow[r] *= alpha[r];
+        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
+        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
       }
-      uint32_t a[4];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float p0 = exp2f(sc[j][0] - mu[0]), p1 = exp2f(sc[j][1] - mu[0]);
-        const float p2 = exp2f(sc[j][2] - mu[1]), p3 = exp2f(sc[j][3] - mu[1]);
-        lrow[0] += p0 + p1;
-        lrow[1] += p2 + p3;
-        a[j * 2 + 0] = pack_bf16x2(p0, p1);
-        a[j * 2 + 1] = pack_bf16x2(p2, p3);
+      float* sm_m = merge;
+      float* sm_l = merge + 64;
+      float* sm_o = merge + 128;
+      if (tq == 0) {
+        sm_m[warp * 16 + g] = mrow[0];
+        sm_m[warp * 16 + g + 8] = mrow[1];
+        sm_l[warp * 16 + g] = lrow[0];
+        sm_l[warp * 16 + g + 8] = lrow[1];
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        acc[i][0] *= alpha[0];
-        acc[i][1] *= alpha[0];
-        acc[i][2] *= alpha[1];
-        acc[i][3] *= alpha[1];
+      for (int dt = 0; dt < 16; ++dt) {
+        const int c = dt * 8 + 2 * tq;
+        sm_o[(warp * 16 + g) * kD + c] = acc[dt][0];
+        sm_o[(warp * 16 + g) * kD + c + 1] = acc[dt][1];
+        sm_o[(warp * 16 + g + 8) * kD + c] = acc[dt][2];
+        sm_o[(warp * 16 + g + 8) * kD + c + 1] = acc[dt][3];
       }
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        const int mi = lane >> 3, rr = lane & 7;
-        uint32_t bb[4];
-        ldsm_x4_t(sV + tsw(warp * 16 + rr + 8 * (mi & 1), dp * 2 + (mi >> 1)), bb);
-        mma_bf16(acc[2 * dp], a, bb[0], bb[1]);
-        mma_bf16(acc[2 * dp + 1], a, bb[2], bb[3]);
+      if (!csync_all()) {
+        failed = true;
+        break;
       }
-      if (valid < 16) fence_proxy_async_smem();  // generic writes before the next TMA into this stage
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty(stage));
-      if (++stage == kStages) {
-        stage = 0;
-        ph ^= 1;
+      for (int idx = threadIdx.x; idx < G * kD; idx += kCompute * 32) {
+        const int r = idx / kD, c = idx - r * kD;
+        float m = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kCompute; ++w) m = fmaxf(m, sm_m[w * 16 + r]);
+        const float mu = m == -INFINITY ? 0.f : m;
+        float l = 0.f, oo = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCompute; ++w) {
+          const float f = exp2f(sm_m[w * 16 + r] - mu);
+          l += sm_l[w * 16 + r] * f;
+          oo += sm_o[(w * 16 + r) * kD + c] * f;
+        }
+        const size_t hs = ((size_t)un.b * p.H + (size_t)un.kvh * G + r) * p.splits + un.split;
+        p.ws_o[hs * kD + c] = oo;
+        if (c == 0) {
+          p.ws_ml[hs * 2 + 0] = m;
+          p.ws_ml[hs * 2 + 1] = l;
+        }
       }
-    }
-    if (failed) break;
-    // merge the four warps' softmax states (rows < G) and write this split's partial
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-    }
-    float* sm_m = merge;
-    float* sm_l = merge + 64;
-    float* sm_o = merge + 128;
-    if (tq == 0) {
-      sm_m[warp * 16 + g] = mrow[0];
-      sm_m[warp * 16 + g + 8] = mrow[1];
-      sm_l[warp * 16 + g] = lrow[0];
-      sm_l[warp * 16 + g + 8] = lrow[1];
-    }
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-      const int c = dt * 8 + 2 * tq;
-      sm_o[(warp * 16 + g) * kD + c] = acc[dt][0];
-      sm_o[(warp * 16 + g) * kD + c + 1] = acc[dt][1];
-      sm_o[(warp * 16 + g + 8) * kD + c] = acc[dt][2];
-      sm_o[(warp * 16 + g + 8) * kD + c + 1] = acc[dt][3];
-    }
-    if (!csync_all()) {
-      failed = true;
-      break;
-    }
-    for (int idx = threadIdx.x; idx < G * kD; idx += kCompute * 32) {
-      const int r = idx / kD, c = idx - r * kD;
-      float m = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kCompute; ++w) m = fmaxf(m, sm_m[w * 16 + r]);
-      const float mu = m == -INFINITY ? 0.f : m;
-      float l = 0.f, oo = 0.f;
-#pragma unroll
-      for (int w = 0; w < kCompute; ++w) {
-        const float f = exp2f(sm_m[w * 16 + r] - mu);
-        l += sm_l[w * 16 + r] * f;
-        oo += sm_o[(w * 16 + r) * kD + c] * f;
-      }
-      const size_t hs = ((size_t)un.b * p.H + (size_t)un.kvh * G + r) * p.splits + un.split;
-      p.ws_o[hs * kD + c] = oo;
-      if (c == 0) {
-        p.ws_ml[hs * 2 + 0] = m;
-        p.ws_ml[hs * 2 + 1] = l;
+      if (!csync_all()) {  // the merge buffer is reused by the next unit
+        failed = true;
+        break;
       }
     }
-    if (!csync_all()) {  // the merge buffer is reused by the next unit
-      failed = true;
-      break;
+    if (failed) {
+      *abort_flag = 1;
+      if (lane == 0) report_timeout(p.status, 0x31);
     }
   }
-  if (failed) {
-    *abort_flag = 1;
-    if (lane == 0) report_timeout(p.status, 0x31);
+  __syncthreads();
+  // Every role has stopped. After an abort, tiles that no compute warp waited for may
+  // still be landing: they complete before the CTA exits (every thread reads the same flag).
+  if (*abort_flag && warp == kCompute && lane == 0) {
+    volatile int never = 0;
+    for (int st = 0; st < kStages; ++st)
+      if (issued & (1u << st)) mbar_wait(full(st), (parity >> st) & 1, kDrainNs, &never);
   }
 }
 
@@ -386,9 +393,12 @@ constexpr int kCombineBatch = 8;  // splits whose loads are issued together
 __global__ void __launch_bounds__(kCombineThreads, 2)
     attn_decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__ ws_o, void* __restrict__ o,
                                int pairs, int splits, const __half* __restrict__ gate,
-                               __nv_bfloat16* __restrict__ ungated, int o_f16) {
+                               __nv_bfloat16* __restrict__ ungated, int o_f16, const DevStatus* poison) {
   pdl_launch_dependents();
   pdl_wait();
+  // a split that gave up a wait wrote no partial: every output becomes NaN, so that a
+  // caller without a status word to read cannot take stale partials for a result
+  const bool bad = poison != nullptr && *reinterpret_cast<const volatile int*>(&poison->code) != 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kWarps = kCombineThreads / 32;
   for (int pr = blockIdx.x * kWarps + warp; pr < pairs; pr += gridDim.x * kWarps) {
@@ -424,6 +434,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
     }
     const size_t i = (size_t)pr * kD + 4 * lane;
     float r[4] = {acc.x / l, acc.y / l, acc.z / l, acc.w / l};
+    if (bad) r[0] = r[1] = r[2] = r[3] = __int_as_float(0x7fc00000);
     if (ungated) {
       const __nv_bfloat162 a = __floats2bfloat162_rn(r[0], r[1]), b = __floats2bfloat162_rn(r[2], r[3]);
       *reinterpret_cast<uint2*>(ungated + i) =
@@ -475,11 +486,10 @@ cudaError_t decode_core(const void* q, const void* k, const void* v, void* o, in
                         const int* kv_lens, int len_add, int splits, int max_len, float* ws, int num_sms,
                         DevStatus* st, unsigned long long wait_ns, cudaStream_t s, const char** why,
                         const AttnOpts& opt) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  static std::atomic<unsigned long long> configured{0};  // one bit per device
+  {
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(attn_decode_kernel), kSmem, configured);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   DecodeParams p;
   memset(static_cast<void*>(&p), 0, sizeof(p));
@@ -521,7 +531,8 @@ cudaError_t decode_core(const void* q, const void* k, const void* v, void* o, in
   const int cwarps = kCombineThreads / 32;
   const int cgrid = std::min(num_sms, (pairs + cwarps - 1) / cwarps);
   launch_pdl(attn_decode_combine_kernel, cgrid, kCombineThreads, 0, s, p.ws_ml, p.ws_o, o, pairs, splits,
-             static_cast<const __half*>(opt.gate), static_cast<__nv_bfloat16*>(opt.ungated), opt.o_f16 ? 1 : 0);
+             static_cast<const __half*>(opt.gate), static_cast<__nv_bfloat16*>(opt.ungated), opt.o_f16 ? 1 : 0,
+             opt.poison_on_timeout);
   return cudaGetLastError();
 }
 
@@ -558,6 +569,8 @@ static __device__ __align__(256) float g_decode_scratch[kDecodeStaticScratchByte
 
 namespace {
 std::mutex g_scratch_mu;
+constexpr size_t kStaticStatusOffset = 64;  // the status word's byte offset in the counter region
+static_assert(kStaticStatusOffset + sizeof(DevStatus) <= kAttnCounterBytes, "counter region");
 constexpr int kMaxDevices = 64;
 float* g_scratch_addr[kMaxDevices] = {};
 
@@ -582,7 +595,7 @@ cudaError_t scratch_address(float** out) {
 
 cudaError_t launch_attn_decode_bf16_static(const void* q, const void* k, const void* v, void* o, int B, int H,
                                            int Hkv, int d, int kv_stride, const int* kv_lens, int num_sms,
-                                           cudaStream_t s, const char** why) {
+                                           unsigned long long wait_ns, cudaStream_t s, const char** why) {
   if (d != kD) {
     *why = "bf16 attention: head_dim must be 128";
     return cudaErrorInvalidValue;
@@ -606,10 +619,18 @@ cudaError_t launch_attn_decode_bf16_static(const void* q, const void* k, const v
   int splits = attn_decode_splits(B, Hkv, kv_stride, num_sms);
   const int fit = (int)((kDecodeStaticScratchBytes - kAttnCounterBytes) / per_split);
   if (splits > fit) splits = fit;
-  // every partial the combine step reads is written by this call first; the unit
-  // counter at the scratch's start is zeroed before the launch
-  return decode_core(q, k, v, o, B, H, Hkv, kv_stride, kv_lens, 0, splits, kv_stride, scratch, num_sms, nullptr,
-                     2000000000ULL, s, why, AttnOpts());
+  // The scratch's first kAttnCounterBytes hold the unit counter (byte 0) and this
+  // call's status word (byte kStaticStatusOffset); both are zeroed before the launch.
+  // Every partial the combine step reads is written by this call first, unless a wait
+  // gave up: the status word then records it and the combine step writes NaN to o.
+  cudaError_t e2 = cudaMemsetAsync(scratch, 0, kStaticStatusOffset + sizeof(DevStatus), s);
+  if (e2 != cudaSuccess) return e2;
+  DevStatus* st = reinterpret_cast<DevStatus*>(reinterpret_cast<uint8_t*>(scratch) + kStaticStatusOffset);
+  AttnOpts opt;
+  opt.counter_zeroed = true;
+  opt.poison_on_timeout = st;
+  return decode_core(q, k, v, o, B, H, Hkv, kv_stride, kv_lens, 0, splits, kv_stride, scratch, num_sms, st, wait_ns,
+                     s, why, opt);
 }
 
 }  // namespace blk

@@ -201,12 +201,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   }
   const int t0 = max(0, first_key) / kBK;
   const int n_tiles = max(0, (n_keys + kBK - 1) / kBK - t0);  // none when every query is padding
+  // What the producer lanes and the MMA lane have in flight, for the drain after an
+  // abort: the K stages issued (with the parity of their last phase), the V stage's
+  // last phase, and whether any MMA was issued.
+  uint32_t issued = 0, parity = 0, v_last = 0;
+  bool v_issued = false, mma_issued = false;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer: Q, then the K ring
       bool failed = false;
-      uint32_t issued = 0, parity = 0;
       mbar_arrive_expect_tx(q_full, kSlots * kQBytes);
 #pragma unroll
       for (int g = 0; g < kSlots; ++g) {
@@ -228,18 +232,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         issued |= 1u << s;
         parity = (parity & ~(1u << s)) | (ph << s);
       }
-      if (failed) {
+      if (failed) {  // the loads in flight are drained after the CTA's final barrier
         *abort_flag = 1;
         report_timeout(p.status, 0x20 + 0);
-        volatile int never = 0;
-        mbar_wait(q_full, 0, kDrainNs, &never);
-        for (int s = 0; s < kKStages; ++s)
-          if (issued & (1u << s)) mbar_wait(k_full(s), (parity >> s) & 1, kDrainNs, &never);
       }
     } else if (lane == 1) {
       // ---------------- TMA producer: the V stage (its own thread, so that K never waits behind V)
-      bool failed = false, issued = false;
-      uint32_t last = 0;
+      bool failed = false;
       for (int j = 0; j < n_tiles; ++j) {
         if (!mbar_wait(v_empty, (j & 1) ^ 1, budget, abort_flag)) {
           failed = true;
@@ -249,14 +248,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int row = kv_row + (t0 + j) * kBK;
         tma_load_2d(smem_u32(sV), &p.tv, 0, row, v_full);
         tma_load_2d(smem_u32(sV + kKVSub), &p.tv, 64, row, v_full);
-        issued = true;
-        last = j & 1;
+        v_issued = true;
+        v_last = j & 1;
       }
       if (failed) {
         *abort_flag = 1;
         report_timeout(p.status, 0x20 + 3);
-        volatile int never = 0;
-        if (issued) mbar_wait(v_full, last, kDrainNs, &never);
       }
     }
   } else if (warp == 1) {
@@ -267,7 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK) & fmt_clear;
       constexpr uint32_t idesc_pv = (idesc_bf16_f32(kBQ, kD) & fmt_clear) | (1u << 16);  // B (V) is MN-major
       bool failed = !mbar_wait(q_full, 0, budget, abort_flag);
-      bool issued_any = false;
       auto issue_s = [&](int g, int j) {  // S_j of slot g into its score buffer
         const int s = j % kKStages;
 #pragma unroll
@@ -277,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           tc_mma_bf16(tmem + g * kBK, a, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(s_full(g));
-        issued_any = true;
+        mma_issued = true;
       };
       if (!failed && n_tiles > 0) {
         if (!mbar_wait(k_full(0), 0, budget, abort_flag)) {
@@ -329,14 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (failed) break;
         tc_commit(v_empty);
       }
-      if (failed) {
+      if (failed) {  // the MMAs in flight are drained after the CTA's final barrier
         *abort_flag = 1;
         report_timeout(p.status, 0x20 + 1);
-        if (issued_any) {
-          tc_commit(drain);
-          volatile int never = 0;
-          mbar_wait(drain, 0, kDrainNs, &never);
-        }
       }
     }
   } else {
@@ -511,6 +502,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
   tc_fence_before();
   __syncthreads();
+  // Every role has stopped issuing. After an abort (a wait that ran out anywhere in
+  // the CTA), copies and MMAs that no role waited for may still be in flight: they
+  // complete before TMEM is freed and the CTA exits. Every thread reads the same flag.
+  if (*abort_flag) {
+    volatile int never = 0;
+    if (warp == 0 && lane == 0) {
+      mbar_wait(q_full, 0, kDrainNs, &never);
+      for (int s = 0; s < kKStages; ++s)
+        if (issued & (1u << s)) mbar_wait(k_full(s), (parity >> s) & 1, kDrainNs, &never);
+    } else if (warp == 0 && lane == 1) {
+      if (v_issued) mbar_wait(v_full, v_last, kDrainNs, &never);
+    } else if (warp == 1 && lane == 0 && mma_issued) {
+      tc_commit(drain);
+      mbar_wait(drain, 0, kDrainNs, &never);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -560,13 +569,10 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
   p.sl2 = kLog2e / sqrtf((float)kD);
   p.status = st;
   p.wait_ns = wait_ns;
-  static bool configured[2] = {false, false};
-  if (!configured[f16]) {
-    cudaError_t e = f16 ? cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)
-                        : cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    configured[f16] = true;
-  }
+  static std::atomic<unsigned long long> configured[2];  // per instantiation, one bit per device
+  cudaError_t ce = f16 ? set_smem_limit_once(reinterpret_cast<const void*>(attn_tc_kernel<true>), kSmem, configured[1])
+                       : set_smem_limit_once(reinterpret_cast<const void*>(attn_tc_kernel<false>), kSmem, configured[0]);
+  if (ce != cudaSuccess) return ce;
   if (f16)
     launch_pdl(attn_tc_kernel<true>, p.n_items, kThreads, kSmem, s, p);
   else

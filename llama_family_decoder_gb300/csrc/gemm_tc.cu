@@ -45,6 +45,9 @@ constexpr int kThreadsEpi = 128;  // epilogue warps 2..5
 // Drains after an abort wait for copies/MMAs already issued; they use their
 // own limit so that a tiny debug timeout cannot cut them short.
 constexpr unsigned long long kDrainNs = 2000000000ULL;
+// After an abort, how long the odd CTA of a pair stays resident past its last
+// load issue (it cannot observe its loads complete; a load takes microseconds).
+constexpr unsigned long long kSettleNs = 2000000ULL;
 
 constexpr int kMaxSmem = 232448;  // 227 KB of dynamic shared memory per CTA
 
@@ -972,13 +975,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const int bn_rows = p.b_paired ? BN / 2 : BN;
   const unsigned long long budget = p.wait_ns;
   DecSide dec_side;  // decode finishers only (epilogue warps)
+  // What the producer and MMA lanes have in flight, for the drain after an abort:
+  // the stages whose loads were issued (with the parity of their last phase), and
+  // whether any MMA was issued.
+  uint32_t issued_mask = 0, parity_mask = 0;
+  unsigned long long last_issue_ns = 0;
+  bool mma_issued = false;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
       int stage = 0;
       uint32_t ph = 0;
-      uint32_t issued_mask = 0, parity_mask = 0;
       bool failed = false;
       // A streamed once (decode weights) must not push the activations that the
       // next kernels read out of L2
@@ -1039,6 +1047,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           else
             load_b(i, un, un.kb_begin + i);
           issued_mask |= 1u << i;
+          if constexpr (PAIR) last_issue_ns = globaltimer_ns();
         }
       }
       pdl_wait();
@@ -1062,23 +1071,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           }
           issued_mask |= 1u << stage;
           parity_mask = (parity_mask & ~(1u << stage)) | (ph << stage);
+          if constexpr (PAIR) last_issue_ns = globaltimer_ns();
           if (++stage == S) {
             stage = 0;
             ph ^= 1;
           }
         }
       }
-      if (failed) {
+      if (failed) {  // the loads in flight are drained after the CTA's final barrier
         *abort_flag = 1;
         report_timeout(p.status, 0x10 + 0);
-        // drain: every issued load must land before the CTA exits (a pair's odd CTA
-        // cannot see its loads land: the even CTA's drain and the final cluster
-        // barrier cover them)
-        for (int s = 0; s < S && mma_cta; ++s)
-          if (issued_mask & (1u << s)) {
-            volatile int never = 0;
-            mbar_wait(full_bar(s), (parity_mask >> s) & 1, kDrainNs, &never);
-          }
       }
     }
   } else if (warp == 1) {
@@ -1090,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       int stage = 0;
       uint32_t ph = 0;
       int it = 0;
-      bool failed = false, issued_any = false;
+      bool failed = false;
       for (int u = u0; u < p.num_units && !failed; u += ustep, ++it) {
         const Unit un = PAIR ? pair_unit(p, u, bn_rows, prank) : decode_unit(p, u, bn_rows);
         const int acc = it & 1;
@@ -1119,7 +1121,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               tc_mma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
                           (kb > un.kb_begin || kk > 0) ? 1u : 0u);
           }
-          issued_any = true;
+          mma_issued = true;
           if constexpr (PAIR)
             tc_commit_pair(empty_bar(stage), kPairMask);  // the stage is free in both CTAs
           else
@@ -1135,17 +1137,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         else
           tc_commit(tfull_bar(acc));
       }
-      if (failed) {
+      if (failed) {  // the MMAs in flight are drained after the CTA's final barrier
         *abort_flag = 1;
         report_timeout(p.status, 0x10 + 1);
-        if (issued_any) {
-          if constexpr (PAIR)
-            tc_commit_pair(drain_bar, (uint16_t)(1u << lead_rank));
-          else
-            tc_commit(drain_bar);
-          volatile int never = 0;
-          mbar_wait(drain_bar, 0, kDrainNs, &never);
-        }
       }
     }
   } else {
@@ -1259,6 +1253,44 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else {
     __syncthreads();
   }
+  // Every role has stopped issuing. After an abort (a wait that ran out anywhere in
+  // the CTA, or in either CTA of a pair) loads and MMAs that no role waited for may
+  // still be in flight: they must complete before TMEM is freed and the CTA exits.
+  // The decision is uniform: every thread reads the same flags after the barrier.
+  bool aborted = *abort_flag != 0;
+  if constexpr (PAIR)
+    aborted = aborted || ld_dsmem_u32(map_shared_rank(smem_u32((const void*)abort_flag), cluster_ctarank() ^ 1u)) != 0;
+  if (aborted) {
+    volatile int never = 0;
+    if (warp == 0 && lane == 0) {
+      if (mma_cta) {
+        // both CTAs' bytes of a pair complete on the even CTA's full barriers
+        for (int s = 0; s < S; ++s)
+          if (issued_mask & (1u << s)) mbar_wait(full_bar(s), (parity_mask >> s) & 1, kDrainNs, &never);
+      } else if constexpr (PAIR) {
+        // the odd CTA of a pair cannot watch its loads land (they count on the even
+        // CTA's barriers, which cannot complete a phase the even CTA never armed): it
+        // stays resident for kSettleNs after its last issue, far beyond a load's latency
+        if (issued_mask != 0)
+          while (globaltimer_ns() - last_issue_ns < kSettleNs) {
+          }
+      }
+    }
+    if (warp == 1 && lane == 0 && mma_cta && mma_issued) {
+      if constexpr (PAIR)
+        tc_commit_pair(drain_bar, (uint16_t)(1u << lead_rank));
+      else
+        tc_commit(drain_bar);
+      mbar_wait(drain_bar, 0, kDrainNs, &never);
+    }
+    tc_fence_before();
+    if constexpr (PAIR) {
+      __syncwarp();
+      cluster_sync_all();  // the pair's MMAs are done before either CTA frees its TMEM
+    } else {
+      __syncthreads();
+    }
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -1308,10 +1340,9 @@ namespace {
 
 template <int BN, int EPI, bool PAIR = false>
 cudaError_t configure() {
-  static cudaError_t st =
-      cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           TcCfg<BN, EPI, PAIR>::kSmemBytes);  // once per instantiation
-  return st;
+  static std::atomic<unsigned long long> done{0};  // once per instantiation and device
+  return set_smem_limit_once(reinterpret_cast<const void*>(tc_gemm_kernel<BN, EPI, PAIR>),
+                             TcCfg<BN, EPI, PAIR>::kSmemBytes, done);
 }
 
 // Launch configuration of a clustered GEMM: clusters of `csize` CTAs along x

@@ -215,6 +215,9 @@ struct AttnOpts {
   void* ungated = nullptr;
   bool o_f16 = false;            // decode: o in fp16 (else bf16)
   bool counter_zeroed = false;   // decode: an earlier kernel of the stream zeroed the workspace's unit counter
+  // decode: when this status word records a timeout, the combine step writes NaN to o (for
+  // callers that have no handle to read a status from)
+  const DevStatus* poison_on_timeout = nullptr;
   const int2* key_range = nullptr;  // prefill: per sequence, only keys lo <= j < hi are visible
 };
 
@@ -254,6 +257,6 @@ int attn_decode_split_cap(int max_len);
 constexpr size_t kDecodeStaticScratchBytes = 16u << 20;
 cudaError_t launch_attn_decode_bf16_static(const void* q, const void* k, const void* v, void* o, int B, int H,
                                            int Hkv, int d, int kv_stride, const int* kv_lens, int num_sms,
-                                           cudaStream_t s, const char** why);
+                                           unsigned long long wait_ns, cudaStream_t s, const char** why);
 
 }  // namespace blk
