@@ -41,3 +41,27 @@ def bf16_floor(ref) -> float:
     """Error of storing the exact result in bf16 alone (the unavoidable floor)."""
     r = torch.from_numpy(np.asarray(ref, dtype=np.float64))
     return rel_err(r.to(torch.bfloat16), ref)
+
+
+def check_relu2_zeros(neurons, pre):
+    """relu(u)^2 is exactly zero wherever the pre-activation is not positive ("arcee",
+    "A neuron is relu(x)^2, exactly zero below zero"). The GPU's pre-activation u differs
+    from the oracle's by its GEMM's rounding: with bf16 operands (unit roundoff 2^-8)
+    about 0.003 RMS(u) per element over a K-term product, under 0.015 RMS(u) at the 5-sigma
+    tail of these sizes. So delta = 0.05 RMS(u): every neuron whose oracle pre-activation
+    is <= -delta must be exactly 0.0, every one at >= +delta must be > 0, none negative.
+    Where the GPU neuron is positive, sqrt of it is the GPU's own u: its distance from the
+    oracle's u must stay below delta / 2, which checks that delta sits above the measured
+    error rather than hiding it. Returns (fraction of exact zeros, measured max |du|/RMS)."""
+    n = np64(neurons).reshape(-1)
+    u = np.asarray(pre, dtype=np.float64).reshape(-1)
+    rms = float(np.sqrt(np.mean(u * u)))
+    delta = 0.05 * rms
+    assert n.min() >= 0.0
+    neg, pos = u <= -delta, u >= delta
+    assert np.all(n[neg] == 0.0), int(np.sum(n[neg] != 0.0))
+    assert np.all(n[pos] > 0.0), int(np.sum(n[pos] == 0.0))
+    both = (n > 0) & (u > 0)
+    du = float(np.max(np.abs(np.sqrt(n[both]) - u[both]))) / rms if both.any() else 0.0
+    assert du <= 0.5 * delta / rms, du
+    return float(np.mean(n == 0.0)), du

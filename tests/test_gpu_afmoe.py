@@ -8,17 +8,16 @@ Prefill, prefill chunks over a KV cache, decode steps (fused and unfused QKV
 finishers), the fp32 path and the attention stage, at sizes the oracle finishes in
 seconds (several tiles and ragged tails, windows shorter and longer than a key
 tile, windows reaching into the cache), plus the full-size workloads checked on
-sampled rows. Bounds: max|err| / RMS(oracle) <= 2e-2 (bf16 with prepared fp16
-weights, as the benchmark runs it; fp32: 1e-4).
+sampled rows. Bounds: max|err| / RMS(oracle) <= 2e-2 on the bf16 path, 1e-4 on
+the fp32 path, for every case.
 
 With bf16 weights left unprepared, every GEMM operand that meets a weight is bf16
 (one operand type per tensor-core product), so each sublayer's output carries a
 relative error of order 2^-9; the sandwich post-norms rescale that output to the
-size of the residual stream, which puts the block's error at about twice the
-error of storing the output in bf16 alone. Those cases are held to
-2 * storage floor + 5e-3, the bound the other suites use for twice-rounded values,
-and their intermediate taps downstream of a post-norm (which inherit that relative
-error on top of their own rounding) to 2.5 * their storage floor + 5e-3.
+size of the residual stream, which would spend the whole bf16 tolerance there.
+The library therefore refuses sandwich blocks on unprepared bf16 weights
+(BLK_ERR_UNSUPPORTED, checked here); the unprepared cases below run the same
+window, rotary and gate options without the post-norms.
 """
 import dataclasses
 
@@ -53,18 +52,23 @@ def _taps(wl, dt, kv=True):
 
 
 def _bound(wl, prepared, ref_out):
-    """The layer-output bound of a case (see the module docstring)."""
-    if wl.dtype == "f32":
-        return TOL["f32"]
-    if wl.sandwich_norm and not prepared:
-        return max(TOL["bf16"], 2.0 * bf16_floor(ref_out) + 5e-3)
-    return TOL["bf16"]
+    """The layer-output bound of a case."""
+    return TOL["f32"] if wl.dtype == "f32" else TOL["bf16"]
 
 
 def _tap_bound(wl, prepared, floor):
-    """An intermediate tap's bound, from its own bf16 storage floor."""
-    c = 2.5 if (wl.sandwich_norm and not prepared) else 2.0
-    return max(TOL["bf16"], c * floor + 5e-3)
+    """An intermediate tap's bound: the tolerance, or twice its own bf16 storage floor
+    plus 5e-3 (max|err|/RMS of a tap whose RMS is far below its largest entries is set by
+    the rounding of those entries, as in the other suites)."""
+    return max(TOL["bf16"], 2.0 * floor + 5e-3)
+
+
+def _runnable(wl, prepared):
+    """Sandwich blocks need prepared weights on the bf16 path; an unprepared case runs
+    the same options without the post-norms."""
+    if wl.dtype == "bf16" and wl.sandwich_norm and not prepared:
+        return wl.scaled(name=wl.name + "_nosandwich", sandwich_norm=False)
+    return wl
 
 
 def _check_taps(tb, ref, wl, prepared, prefix=""):
@@ -112,6 +116,7 @@ PREFILL = [
 @pytest.mark.parametrize("wl,prepared", PREFILL,
                          ids=lambda v: v.name if isinstance(v, Workload) else ("prepared" if v else "bf16_weights"))
 def test_afmoe_prefill_small(wl, prepared):
+    wl = _runnable(wl, prepared)
     w = make_weights(wl, gain_std=0.1)
     x = make_input(wl)
     blk = DecoderBlock.from_workload(wl)
@@ -147,7 +152,8 @@ def test_afmoe_prefill_small(wl, prepared):
 def test_afmoe_chunk_over_the_cache_with_window(window, prepared):
     # T new tokens after ragged cached lengths; the window reaches back into the cache
     # (or not, for the empty one). Unused slots hold NaN: nothing of them may leak.
-    wl = _afmoe(f"chunk_w{window}", "bf16", 3, 150, 512, 8, 2, 128, 1000, window=window, seed=58)
+    wl = _runnable(_afmoe(f"chunk_w{window}", "bf16", 3, 150, 512, 8, 2, 128, 1000, window=window, seed=58),
+                   prepared)
     lens = [0, 37, 300]
     cap = 500
     w = make_weights(wl, gain_std=0.1)
@@ -215,7 +221,8 @@ def _decode(wl, lens, taps=True, gain_std=0.1, prepared=False):
 @pytest.mark.parametrize("window,rope", [(64, True), (200, True), (0, False)])
 def test_afmoe_decode_small(window, rope, prepared):
     # sequences shorter and longer than the window (the split-KV units start at the window)
-    wl = _afmoe(f"decode_w{window}", "bf16", 7, 1, 512, 8, 2, 128, 1000, window=window, rope=rope, seed=60)
+    wl = _runnable(_afmoe(f"decode_w{window}", "bf16", 7, 1, 512, 8, 2, 128, 1000, window=window, rope=rope,
+                          seed=60), prepared)
     lens = [1, 30, 63, 64, 65, 190, 400]
     out, tb, ref = _decode(wl, lens, prepared=prepared)
     err, bound = rel_err(out, ref["layer_output"]), _bound(wl, prepared, ref["layer_output"])
@@ -233,13 +240,38 @@ def test_afmoe_decode_small(window, rope, prepared):
 def test_afmoe_decode_unfused_qkv(prepared):
     # 80 weight tiles (q, k, v, gate) x 2 token tiles exceed the SMs: the QKV partials are
     # summed by the post kernel, which also forms the gate
-    wl = _afmoe("decode_wide", "bf16", 260, 1, 4096, 32, 8, 128, 1024, window=48, seed=61)
+    wl = _runnable(_afmoe("decode_wide", "bf16", 260, 1, 4096, 32, 8, 128, 1024, window=48, seed=61), prepared)
     lens = [(53 * b + 7) % 120 + 1 for b in range(wl.batch)]
     out, _, ref = _decode(wl, lens, taps=False, gain_std=0.0, prepared=prepared)
     err, bound = rel_err(out, ref["layer_output"]), _bound(wl, prepared, ref["layer_output"])
     print(f"decode wide prepared={prepared}: {err:.4f} (floor {bf16_floor(ref['layer_output']):.4f}, "
           f"bound {bound:.4f})")
     assert err <= bound
+
+
+def test_afmoe_sandwich_refused_on_unprepared_bf16_weights():
+    # prefill, prefill chunk, decode and the MLP stage: refused on the host, nothing launched
+    from llama_family_decoder_gb300.binding import BlkError
+    wl = _afmoe("refused", "bf16", 2, 64, 512, 4, 2, 128, 1000, window=32, seed=65)
+    w = to_dev(make_weights(wl))
+    x = make_input(wl).to(DEV)
+    blk = DecoderBlock.from_workload(wl, max_seq=200)
+    kc = torch.zeros(2, 2, 160, 128, dtype=torch.bfloat16, device=DEV)
+    lens = torch.tensor([3, 9], dtype=torch.int32, device=DEV)
+    calls = [lambda: blk.forward(x, w),
+             lambda: blk.forward(x, w, cache={"k": kc, "v": kc.clone(), "lens": lens}, host_lens_max=9),
+             lambda: blk.forward(x[:, :1].contiguous(), w, cache={"k": kc, "v": kc.clone(), "lens": lens},
+                                 host_lens_max=9),
+             lambda: blk.mlp(x.view(-1, 512), x.view(-1, 512), w, torch.empty_like(x).view(-1, 512))]
+    for call in calls:
+        with pytest.raises(BlkError) as e:
+            call()
+        assert e.value.status == 2  # BLK_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert lens.tolist() == [3, 9]  # no launch touched the cache
+    out = blk.forward(x, blk.prepare(w))  # the same block on prepared weights runs
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
 
 
 @pytest.mark.parametrize("window,rope,gate,sandwich", [(5, True, True, True), (0, False, True, True),

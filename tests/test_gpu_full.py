@@ -8,7 +8,7 @@ import torch
 import oracle
 from llama_family_decoder_gb300 import DecoderBlock
 from llama_family_decoder_gb300.synth import WORKLOADS, make_input, make_kv_cache, make_weights
-from tests.helpers import TOL, bf16_floor, cfg_of, np64, rel_err, weights_np
+from tests.helpers import TOL, bf16_floor, cfg_of, check_relu2_zeros, np64, rel_err, weights_np
 
 pytestmark = pytest.mark.gpu
 
@@ -22,7 +22,10 @@ def test_prefill_full_size_sampled_rows(name):
     x = make_input(wl)
     blk = DecoderBlock.from_workload(wl)
     wd = blk.prepare({k: v.cuda() for k, v in w.items()})  # as bench.py runs it
-    out = blk.forward(x.cuda(), wd)
+    relu2 = wl.hidden_act == "relu2"
+    taps = {"mlp_neurons": torch.empty(wl.batch, wl.seq, wl.intermediate_size, dtype=torch.bfloat16,
+                                       device="cuda")} if relu2 else None
+    out = blk.forward(x.cuda(), wd, taps=taps)
     torch.cuda.synchronize()
     assert blk.last_status() == 0
     out = out.cpu()
@@ -31,12 +34,15 @@ def test_prefill_full_size_sampled_rows(name):
     T = wl.seq
     rows = sorted({0, 1, 63, 64, 127, 128, 129, 1000, T // 2 + 3, T - 129, T - 2, T - 1})
     for b in sorted({0, wl.batch - 1}):
-        ref = oracle.block_forward(cfg_of(wl), wn, np64(x[b:b + 1]), rows=rows)["layer_output"][0]
+        ref = oracle.block_forward(cfg_of(wl), wn, np64(x[b:b + 1]), rows=rows)
         got = out[b, rows]
-        err, floor = rel_err(got, ref), bf16_floor(ref)
+        err, floor = rel_err(got, ref["layer_output"][0]), bf16_floor(ref["layer_output"][0])
         print(f"{name} batch {b}: max|err|/RMS {err:.4f} (bf16 floor {floor:.4f})")
         assert err <= TOL["bf16"], (err, floor)
         assert torch.isfinite(out[b]).all()
+        if relu2:  # the sampled rows' neurons, element by element
+            zeros, du = check_relu2_zeros(taps["mlp_neurons"][b, rows].cpu(), ref["mlp_up_output"][0])
+            print(f"  relu2: {zeros:.3f} exact zeros, pre-activation max|du|/RMS {du:.4f}")
 
 
 def test_decode_full_size_sampled_sequences():
