@@ -1,19 +1,24 @@
 """Benchmark of one decoder-block forward pass on GB300, as one JSON line.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+                [--no-sub-configs] [--no-cpu-baseline]
 
 A step is one blk_forward over the workload's synthetic batch (all stages of the
-block). Default workload: the Llama-7B-shape bf16 prefill block, batch 1 x 2048
-tokens. Inputs and weights are resident in HBM before timing; L2 is flushed
-between timed steps, outside the timed events: a 256 MiB buffer is written and
-then read, so the flush's own dirty lines are written back before the step
-starts and the step begins with none of its operands in L2. value is
-whole-job tokens/s; e2e repeats the measurement with the input copied from
-pinned host memory and the output read back inside each step.
+block). Default workload: the largest configuration, the Apertus-shape bf16
+prefill block (batch 2 x 4096 tokens, q/k-norm, xIELU 16384). The same process
+then times the Llama-7B-shape prefill (1 x 2048), the Arcee-shape prefill
+(4 x 2048) and the decode step (64 sequences over 4096 cached positions) the same
+way, each as its own record under "configs". Inputs and weights are resident in
+HBM before timing; L2 is flushed between timed steps, outside the timed events:
+a 256 MiB buffer is written and then read, so the flush's own dirty lines are
+written back before the step starts and the step begins with none of its
+operands in L2. value is whole-job tokens/s; e2e repeats the measurement with
+the input copied from pinned host memory and the output read back inside each
+step.
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
-workload (the only other place this script runs the oracle is the
-cpu_baseline leg of our own line).
+workload, one sample per step (the only other place this script runs the oracle
+is the cpu_baseline leg of our own line, which repeats that same sample).
 """
 from __future__ import annotations
 
@@ -29,7 +34,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decoder-block tokens/s (bf16, 1×GB300) and % of BF16 tensor-core / HBM roofline"
-DEFAULT_WORKLOAD = "llama7b_bf16_B1_T2048"
+DEFAULT_WORKLOAD = "apertus_qknorm_bf16_B2_T4096"
+# timed after the headline in the same process, each as its own record under "configs"
+SUB_CONFIGS = ("llama7b_bf16_B1_T2048", "arcee_gqa_bf16_B4_T2048", "llama7b_decode_bf16_B64_L4096")
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -160,6 +167,11 @@ def work_counts(wl):
 
 # ---------------------------------------------------------------- oracle (CPU)
 
+def cpu_sample_cap(wl):
+    """Tokens (prefill) or sequences (decode) of one bounded oracle sample, the same on both arms."""
+    return 2 if (wl.cache_len and wl.seq == 1) else min(wl.seq, 1024)
+
+
 def oracle_tokens_per_s(wl, w_cpu, x_cpu, cache_cpu, tokens_cap):
     """fp64 oracle on a bounded sample of the workload; returns (tokens/s, sample text, seconds)."""
     import numpy as np
@@ -200,6 +212,20 @@ def oracle_tokens_per_s(wl, w_cpu, x_cpu, cache_cpu, tokens_cap):
     return ntok / dt, sample, dt
 
 
+def cpu_baseline(wl, w_cpu, x_cpu, cache_cpu, min_seconds):
+    """The oracle on repeated bounded samples (the reference arm's per-step sample) for at
+    least min_seconds of host time; tokens/s over all repetitions."""
+    cap = cpu_sample_cap(wl)
+    reps, secs, ntok, sample = 0, 0.0, 0.0, ""
+    while reps == 0 or secs < min_seconds:
+        tps, sample, dt = oracle_tokens_per_s(wl, w_cpu, x_cpu, cache_cpu, cap)
+        reps += 1
+        secs += dt
+        ntok += tps * dt
+    return {"value": ntok / secs, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{sample}; {reps} repetition(s), {secs:.1f} s of host time", "seconds": secs}
+
+
 def run_reference(args, wl):
     """--impl reference: the fp64 oracle on the host cores, same metric/unit/config."""
     rank = int(os.environ.get("RANK", "0"))
@@ -209,21 +235,21 @@ def run_reference(args, wl):
     w = make_weights(wl)
     x = make_input(wl)
     cache = make_kv_cache(wl) if wl.cache_len else None
-    decode = wl.cache_len > 0 and wl.seq == 1
-    cap = 2 if decode else 256  # per step: a bounded sample (seconds)
-    times, sample = [], ""
+    cap = cpu_sample_cap(wl)  # per step: a bounded sample (about a second or two)
+    times, sample, ntok = [], "", 0.0
     for i in range(args.warmup + args.steps):
         tps, sample, dt = oracle_tokens_per_s(wl, w, x, cache, cap)
         if i >= args.warmup:
             times.append(dt)
-    ntok = min(cap, wl.batch) if decode else min(cap, wl.seq)
-    value = ntok * len(times) / sum(times)
+            ntok += tps * dt
+    value = ntok / sum(times)
     cores = os.cpu_count()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(wl, args.gpus),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{sample}, one per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -265,24 +291,29 @@ def job_tokens_per_s(world, tokens_per_step, steps, total_ms):
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args, wl):
+# Stage names of blk_profile_* -> (roofline kernel name, work key of work_counts)
+PREFILL_STAGES = {
+    "qkv_gemm_rope": ("tc_gemm_kernel (QKV + q/k-norm + RoPE)", "qkv"),
+    "attention": ("attn_tc_kernel (causal flash attention)", "attn"),
+    "o_proj_gemm_resid_norm2": ("tc_gemm_kernel (o_proj + residual + norm-2 fold)", "o"),
+    "mlp_up_gemm_act": ("tc_gemm_kernel (MLP up/gate + activation)", "up"),
+    "down_gemm_resid": ("tc_gemm_kernel (down + residual)", "down"),
+}
+
+SPEC_BF16_TFLOPS = 2250.0
+SPEC_HBM_GBS = 8000.0
+
+
+def measure(args, wl, dev, world, rank, cpu_seconds):
+    """Times wl.steps graph replays of one forward of workload wl on this rank; returns the
+    record of one bench line (without the job-level keys)."""
     import torch
     import torch.distributed as dist
 
     from llama_family_decoder_gb300 import DecoderBlock
     from llama_family_decoder_gb300.synth import make_input, make_kv_cache, make_weights
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-
-    import __graft_entry__
-    __graft_entry__.build()
-
+    local = dev.index
     w_cpu = make_weights(wl, seed=rank_seed(wl, rank))
     x_cpu = make_input(wl, seed=rank_seed(wl, rank))
     w = {k: v.to(dev) for k, v in w_cpu.items()}
@@ -323,7 +354,8 @@ def run_ours(args, wl):
     if args.ncu:  # one more forward for a profiler to capture, nothing timed
         step()
         torch.cuda.synchronize()
-        return
+        blk.close()
+        return None
 
     # Every timed step replays one CUDA graph of the whole forward (captured once).
     # The headline times a graph without profiling events; a second graph, with
@@ -373,7 +405,8 @@ def run_ours(args, wl):
     tokens = wl.batch * wl.seq
     value = job_tokens_per_s(world, tokens, args.steps, total_ms)
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end with host buffers: the input copied from pinned host memory and the
+    # output read back inside every timed step
     x_host = x_cpu.pin_memory()
     out_host = torch.empty_like(x_cpu).pin_memory()
     e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -392,52 +425,102 @@ def run_ours(args, wl):
     e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)) / args.steps, dev)
     nbytes = x_cpu.numel() * x_cpu.element_size()
 
-    # ---- roofline of the dominant kernel (its live event times)
+    # ---- roofline of the dominant kernel (its live event times, on the forward's stream).
+    # Every kernel here runs for well under a second inside a sub-second step, so a
+    # tensor-bound kernel is held to the burst bf16 peak (the fp16 kind runs at the same rate).
     peaks = _peaks()
     g, weight_bytes, kv_bytes = work_counts(wl)
     launches = sum(n for _, n in stages.values())
+    stage_ms = {k: v[0] / args.steps for k, v in stages.items()}
     if decode:
         name = "attention_splitkv"
-        ms = stages[name][0] / args.steps
+        ms = stage_ms[name]
         es = 2 if wl.dtype == "bf16" else 4
         algo = kv_bytes + wl.batch * wl.num_heads * wl.head_dim * es * 2
         achieved = algo / (ms / 1e3) / 1e9
         kname = "attn_decode_kernel (split-KV)"
-        roof = {"bound": "hbm", "kernel": kname, "achieved": achieved,
+        roof = {"bound": "hbm", "kernel": kname, "stage": name, "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": _traffic(kname, wl.name),
-                "algorithmic_bytes": algo, "peak_source": peaks["source"]}
+                "frac_of_spec_8000": achieved / SPEC_HBM_GBS, "traffic": _traffic(kname, wl.name),
+                "algorithmic_bytes": algo, "stage_us": ms * 1e3,
+                "peak_source": f"{peaks['source']} copy bandwidth"}
     else:
-        name = "mlp_up_gemm_act"
-        ms = stages[name][0] / args.steps
-        achieved = g["up"] / (ms / 1e3) / 1e12
-        pk = peaks["bf16_tflops_sustained"]
-        kname = "tc_gemm_kernel (MLP up/gate + activation)"
-        roof = {"bound": "tensor", "kernel": kname, "achieved": achieved,
-                "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk, "traffic": _traffic(kname, wl.name),
-                "algorithmic_flops": g["up"],
-                "peak_source": f"{peaks['source']} sustained bf16 (burst {peaks['bf16_tflops']})"}
+        name = max((s for s in PREFILL_STAGES if s in stage_ms), key=lambda s: stage_ms[s])
+        kname, key = PREFILL_STAGES[name]
+        ms = stage_ms[name]
+        achieved = g[key] / (ms / 1e3) / 1e12
+        pk = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "kernel": kname, "stage": name, "achieved": achieved,
+                "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
+                "frac_of_spec_2250": achieved / SPEC_BF16_TFLOPS, "traffic": _traffic(kname, wl.name),
+                "algorithmic_flops": g[key], "stage_us": ms * 1e3,
+                "peak_source": f"{peaks['source']} burst bf16 (sustained {peaks['bf16_tflops_sustained']})"}
     total_flops = sum(g.values())
-    block = {"tflops": total_flops / (ms_per_step / 1e3) / 1e12,
-             "frac_of_bf16_sustained": total_flops / (ms_per_step / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
-             "frac_of_bf16_spec_2250": total_flops / (ms_per_step / 1e3) / 1e12 / 2250.0,
-             "hbm_gbs_weights_plus_kv": (weight_bytes + kv_bytes) / (ms_per_step / 1e3) / 1e9}
+    step_s = ms_per_step / 1e3
+    block = {"tflops": total_flops / step_s / 1e12,
+             "frac_of_bf16_burst": total_flops / step_s / 1e12 / peaks["bf16_tflops"],
+             "frac_of_bf16_spec_2250": total_flops / step_s / 1e12 / SPEC_BF16_TFLOPS,
+             "hbm_gbs_weights_plus_kv": (weight_bytes + kv_bytes) / step_s / 1e9}
+    if decode:
+        step_bytes = weight_bytes + kv_bytes + 2.0 * wl.batch * wl.hidden_size * 2
+        block.update({"step_us": ms_per_step * 1e3, "step_bytes": step_bytes,
+                      "frac_of_hbm_measured": step_bytes / step_s / 1e9 / peaks["hbm_gbs"],
+                      "frac_of_hbm_spec_8000": step_bytes / step_s / 1e9 / SPEC_HBM_GBS,
+                      "target_us_at_70pct_of_8000": step_bytes / (0.7 * SPEC_HBM_GBS * 1e9) * 1e6})
+    stage_roof = {}
+    for s, (kn, key) in PREFILL_STAGES.items():
+        if s in stage_ms and not decode:
+            a = g[key] / (stage_ms[s] / 1e3) / 1e12
+            stage_roof[s] = {"us": stage_ms[s] * 1e3, "tflops": a, "frac_of_bf16_burst": a / peaks["bf16_tflops"]}
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded N(0,0.02) weights, N(0,1) input)",
-            "config": config_of(wl, world), "roofline": roof,
-            "e2e": {"value": job_tokens_per_s(world, tokens, 1, e2e_ms), "unit": "tokens/s",
-                    "h2d_bytes_per_step": nbytes,
-                    "d2h_bytes_per_step": nbytes},
-            "gpu_launches": launches, "clocks": clk.summary(),
-            "stages_ms": {k: v[0] / args.steps for k, v in stages.items()},
-            "ms_per_step_with_stage_events": sum(prof_ms) / args.steps, "block": block}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cap = 4 if decode else wl.seq
-        tps, sample, dt = oracle_tokens_per_s(wl, w_cpu, x_cpu, cache_cpu, cap)
-        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": sample, "seconds": dt}
+    rec = {"value": value, "unit": "tokens/s", "ms_per_step": ms_per_step, "dtype": wl.dtype,
+           "config": config_of(wl, world), "roofline": roof,
+           "e2e": {"value": job_tokens_per_s(world, tokens, 1, e2e_ms), "unit": "tokens/s",
+                   "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes},
+           "gpu_launches": launches, "clocks": clk.summary(), "stages_ms": stage_ms,
+           "stage_roofline": stage_roof,
+           "ms_per_step_with_stage_events": sum(prof_ms) / args.steps, "block": block}
+    blk.close()
+    del w, x, out, ws, flush, cache
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and cpu_seconds > 0:
+        rec["cpu_baseline"] = cpu_baseline(wl, w_cpu, x_cpu, cache_cpu, cpu_seconds)
+    return rec
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    from llama_family_decoder_gb300.synth import WORKLOADS
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+
+    cpu_s = 0.0 if args.no_cpu_baseline else 10.0
+    head = measure(args, wl, dev, world, rank, cpu_s)
+    if head is None:  # --ncu: nothing timed
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic (seeded N(0,0.02) weights, N(0,1) input)"}
+    line.update({k: v for k, v in head.items() if k not in line and k != "unit"})
+    subs = [] if (args.workload != DEFAULT_WORKLOAD or args.no_sub_configs) else SUB_CONFIGS
+    if subs:
+        line["configs"] = {}
+        for name in subs:  # the other configurations, timed the same way in this process
+            line["configs"][name] = measure(args, WORKLOADS[name], dev, world, rank, 0.0 if cpu_s == 0 else 2.0)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -575,6 +658,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-configs", action="store_true", help="time the headline workload only")
     ap.add_argument("--ncu", action="store_true", help="warm up, run one more forward for a profiler, exit")
     args = ap.parse_args()
     from llama_family_decoder_gb300.synth import WORKLOADS
