@@ -22,7 +22,7 @@ import torch
 import oracle
 from llama_family_decoder_gb300 import DecoderBlock
 from llama_family_decoder_gb300.binding import attn_decode_noalloc, lib, set_wait_timeout_ns
-from tests.helpers import TOL, np64, rel_err
+from tests.helpers import TOL, bf16_floor, np64, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +59,13 @@ def _splits(B, H, cap):
     return ws, min(ws, fit)
 
 
+def _stage_bound(ref):
+    """The bound of the other attention-stage tests, per sequence: the tolerance, or 1.5x
+    the error of storing the exact output in bf16 plus 2e-3 (an attention output whose
+    RMS is far below its largest entries has max|err|/RMS set by their rounding)."""
+    return max(TOL["bf16"], 1.5 * bf16_floor(ref) + 2e-3)
+
+
 def _check(B, H, Hkv, cap, cases, seqs):
     blk = DecoderBlock(hidden=H * D, n_heads=H, n_kv_heads=Hkv, head_dim=D, ffn=1024, act="silu", dtype="bf16",
                        max_batch=B, max_seq=cap + 1)
@@ -71,9 +78,11 @@ def _check(B, H, Hkv, cap, cases, seqs):
         torch.cuda.synchronize()
         assert torch.isfinite(got).all()
         ref = _oracle(q, k, v, lens, seqs)
-        err = rel_err(got[seqs, 0], ref)
-        print(f"B{B} H{H} cap {cap} seed {seed}: oracle {err:.4f}, workspace path {rel_err(got, np64(want)):.4f}")
-        assert err <= TOL["bf16"], (seed, err)
+        for j, b in enumerate(seqs):  # each sequence on its own scale
+            err, bound = rel_err(got[b, 0], ref[j]), _stage_bound(ref[j])
+            print(f"B{B} H{H} cap {cap} seed {seed} sequence {b} ({lens[b]} keys): oracle {err:.4f} "
+                  f"(bound {bound:.4f})")
+            assert err <= bound, (seed, b, err, bound)
         assert rel_err(got, np64(want)) <= TOL["bf16"], seed
     blk.close()
 
@@ -123,14 +132,14 @@ def test_noalloc_wait_running_out_gives_nan():
                 poisoned = True
                 break
             assert torch.isfinite(got).all()
-            assert rel_err(got[[0, 63], 0], ref) <= TOL["bf16"]
+            assert all(rel_err(got[b, 0], ref[j]) <= _stage_bound(ref[j]) for j, b in enumerate((0, 63)))
     finally:
         set_wait_timeout_ns(0)
     assert poisoned
     attn_decode_noalloc(q, k, v, kl, got)
     torch.cuda.synchronize()
     assert torch.isfinite(got).all()
-    assert rel_err(got[[0, 63], 0], ref) <= TOL["bf16"]
+    assert all(rel_err(got[b, 0], ref[j]) <= _stage_bound(ref[j]) for j, b in enumerate((0, 63)))
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
