@@ -6,25 +6,27 @@
 // One CTA per work item of two 128-query slots that share every K/V tile: two
 // query heads of one KV group at the same query tile (an even group size), or
 // two consecutive query tiles of one head (otherwise); heaviest items first.
-// 320 threads:
+// 352 threads:
 //   warp 0      TMA producers: lane 0 both slots' Q tiles once, then K tiles of
-//               128 keys through a 2-stage ring; lane 1 the V tiles through one
-//               stage (128-byte swizzle, 64-column boxes).
-//   warp 1      TMEM allocation; lane 0 issues S = Q K_j^T for both slots (M=128,
-//               N=128, K=16 x 8) into each slot's TMEM score buffer as soon as the
-//               slot's softmax has read the previous scores, and O += P_j V_j (A = P
-//               from shared memory, B = V as an MN-major operand) into each slot's
-//               TMEM output accumulator as soon as P_j is written.
+//               128 keys through a 2-stage ring; lane 1 the V tiles through their
+//               own 2-stage ring (128-byte swizzle, 64-column boxes).
+//   warps 1, 10 MMA issuers, lane 0 of warp 1 for slot 0 and of warp 10 for slot 1
+//               (warp 1 also allocates TMEM): per key tile j, O_g += P_g V_j (A = P
+//               from tensor memory, B = V as an MN-major operand) as soon as the
+//               slot's P_j is written, then at once S_g = Q_g K_{j+1}^T (M=128,
+//               N=128) into the slot's score buffer.
 //   warps 2..9  softmax, four warps per slot, one query row per thread: read S_j
 //               from TMEM, mask, exponentiate in the log2 domain against a running
-//               reference max, write P_j (swizzled K-major) to the slot's shared
-//               buffer; rescale O in TMEM only when the row max grew by more than
-//               2^8 (exact: softmax does not depend on the reference); finally
-//               O / l to the head-major output.
-// S_{j+1} runs on the tensor pipe while the softmax works on S_j, PV_j while it
-// starts on S_{j+1}. Sharing K/V halves its traffic per FLOP; 128-key tiles keep
-// both MMAs at N = 128, where their shared-memory operand reads keep up with the
-// tensor pipe.
+//               reference max, and write P_j (fp16 or bf16 pairs) over the first 64
+//               columns of the same TMEM buffer; rescale O in TMEM only when the row
+//               max grew by more than 2^8 (exact: softmax does not depend on the
+//               reference); finally O / l to the head-major output.
+// The slots take turns: while one slot's softmax works on its tile, the tensor
+// core runs the other slot's PV and next score product. P never touches shared
+// memory, so the tensor core's shared-memory reads are Q, K and V alone. The MMAs
+// of one thread run in issue order: S_{j+1} of a slot, issued after that slot's
+// PV_j, overwrites P_j only once PV_j has read it, and a commit after S_j also
+// covers PV_{j-1} (so O is stable whenever S_j is ready).
 // Options of the "afmoe" block ("Rotary runs on the sliding-window blocks only";
 // "Attention: per-head q/k norms and a sigmoid gate on every head"): a window
 // over the last W positions (key tiles before the first query's oldest key are
@@ -45,15 +47,14 @@ constexpr int kD = 128;
 constexpr int kBQ = 128;                    // queries per slot (MMA M)
 constexpr int kBK = 128;                    // keys per tile
 constexpr int kSlots = 2;
-constexpr int kThreads = 64 + kSlots * 128;
+constexpr int kThreads = 64 + kSlots * 128 + 32;  // + warp 10: the second slot's MMA issuer
 constexpr int kQSub = kBQ * 128;            // one 64-column half of a Q tile (bytes)
 constexpr int kQBytes = 2 * kQSub;          // 128 queries x 128 dims
 constexpr int kKVSub = kBK * 128;           // one 64-column half of a K or V tile
 constexpr int kKVBytes = 2 * kKVSub;        // 128 keys x 128 dims
-constexpr int kPSub = kBQ * 128;            // one 64-key half of a P tile
-constexpr int kPBytes = 2 * kPSub;          // 128 queries x 128 keys
-constexpr int kKStages = 2;                 // K ring; V has one stage
-constexpr int kSmem = 1024 + kSlots * kQBytes + (kKStages + 1) * kKVBytes + kSlots * kPBytes + 256;
+constexpr int kKStages = 2;                 // K ring
+constexpr int kVStages = 2;                 // V ring
+constexpr int kSmem = 1024 + kSlots * kQBytes + (kKStages + kVStages) * kKVBytes + 256;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr unsigned long long kDrainNs = 2000000000ULL;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -96,6 +97,17 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
   return pack_bf16x2(lo, hi);
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]: the A operand (M rows on the TMEM lanes, K
+// 16-bit elements packed two per 32-bit column) read from tensor memory.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 struct Slot {
   int h, qt, m0, valid;
 };
@@ -108,22 +120,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                                   // [slot]: two 64-column halves of 16 KB
   uint8_t* sK = sQ + kSlots * kQBytes;                  // [stage]: two halves of 16 KB
-  uint8_t* sV = sK + kKStages * kKVBytes;               // one tile
-  uint8_t* sP = sV + kKVBytes;                          // [slot]: two 64-key halves of 16 KB
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kSlots * kPBytes);
-  // q_full, k_full[2], k_empty[2], v_full, v_empty, s_full[2], s_free[2], p_ready[2], pv_done[2], drain
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
+  uint8_t* sV = sK + kKStages * kKVBytes;               // [stage]: two halves of 16 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kVStages * kKVBytes);
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_ready[2], o_done[2], drain[2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const uint32_t q_full = smem_u32(&bars[0]);
   auto k_full = [&](int s) { return smem_u32(&bars[1 + s]); };
   auto k_empty = [&](int s) { return smem_u32(&bars[3 + s]); };
-  const uint32_t v_full = smem_u32(&bars[5]);
-  const uint32_t v_empty = smem_u32(&bars[6]);
-  auto s_full = [&](int g) { return smem_u32(&bars[7 + g]); };
-  auto s_free = [&](int g) { return smem_u32(&bars[9 + g]); };
+  auto v_full = [&](int s) { return smem_u32(&bars[5 + s]); };
+  auto v_empty = [&](int s) { return smem_u32(&bars[7 + s]); };
+  auto s_full = [&](int g) { return smem_u32(&bars[9 + g]); };
   auto p_ready = [&](int g) { return smem_u32(&bars[11 + g]); };
-  auto pv_done = [&](int g) { return smem_u32(&bars[13 + g]); };
-  const uint32_t drain = smem_u32(&bars[15]);
+  auto o_done = [&](int g) { return smem_u32(&bars[13 + g]); };
+  auto drain = [&](int g) { return smem_u32(&bars[15 + g]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // ---- the work item: two slots over one KV head of one sequence, heaviest first
@@ -159,17 +169,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     mbar_init(q_full, 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(k_full(s), 1);
-      mbar_init(k_empty(s), 1);
+      mbar_init(k_empty(s), kSlots);  // one commit from each slot's MMA issuer
     }
-    mbar_init(v_full, 1);
-    mbar_init(v_empty, 1);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), kSlots);
+    }
     for (int g = 0; g < kSlots; ++g) {
       mbar_init(s_full(g), 1);
-      mbar_init(s_free(g), 128);
       mbar_init(p_ready(g), 128);
-      mbar_init(pv_done(g), 1);
+      mbar_init(o_done(g), 1);
+      mbar_init(drain(g), 1);
     }
-    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -186,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   pdl_wait();  // q, k, v (and the cache positions, the key ranges) come from earlier kernels
-  const uint32_t tmem = *tmem_holder;  // S[g]: cols 128 g; O[g]: 256 + 128 g
+  const uint32_t tmem = *tmem_holder;  // S[g] (and P[g] over its first 64 columns): cols 128 g; O[g]: 256 + 128 g
   const int off = p.q_off ? p.q_off[b] : 0;  // keys 0 .. off - 1 are earlier positions in the cache
   // visible keys: [kv_lo, kv_hi) (an attention_mask's run of real tokens, else all)
   const int2 kr = p.key_range ? p.key_range[b] : make_int2(0, off + p.T);
@@ -202,10 +213,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int t0 = max(0, first_key) / kBK;
   const int n_tiles = max(0, (n_keys + kBK - 1) / kBK - t0);  // none when every query is padding
   // What the producer lanes and the MMA lane have in flight, for the drain after an
-  // abort: the K stages issued (with the parity of their last phase), the V stage's
-  // last phase, and whether any MMA was issued.
-  uint32_t issued = 0, parity = 0, v_last = 0;
-  bool v_issued = false, mma_issued = false;
+  // abort: the K and V stages issued (with the parity of their last phase), and
+  // whether any MMA was issued.
+  uint32_t issued = 0, parity = 0;
+  bool mma_issued = false;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -237,34 +248,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         report_timeout(p.status, 0x20 + 0);
       }
     } else if (lane == 1) {
-      // ---------------- TMA producer: the V stage (its own thread, so that K never waits behind V)
+      // ---------------- TMA producer: the V ring (its own thread, so that K never waits behind V)
       bool failed = false;
       for (int j = 0; j < n_tiles; ++j) {
-        if (!mbar_wait(v_empty, (j & 1) ^ 1, budget, abort_flag)) {
+        const int s = j % kVStages;
+        const uint32_t ph = (j / kVStages) & 1;
+        if (!mbar_wait(v_empty(s), ph ^ 1, budget, abort_flag)) {
           failed = true;
           break;
         }
-        mbar_arrive_expect_tx(v_full, kKVBytes);
+        mbar_arrive_expect_tx(v_full(s), kKVBytes);
         const int row = kv_row + (t0 + j) * kBK;
-        tma_load_2d(smem_u32(sV), &p.tv, 0, row, v_full);
-        tma_load_2d(smem_u32(sV + kKVSub), &p.tv, 64, row, v_full);
-        v_issued = true;
-        v_last = j & 1;
+        tma_load_2d(smem_u32(sV + s * kKVBytes), &p.tv, 0, row, v_full(s));
+        tma_load_2d(smem_u32(sV + s * kKVBytes + kKVSub), &p.tv, 64, row, v_full(s));
+        issued |= 1u << s;
+        parity = (parity & ~(1u << s)) | (ph << s);
       }
       if (failed) {
         *abort_flag = 1;
         report_timeout(p.status, 0x20 + 3);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kThreads / 32 - 1) {
     if (lane == 0) {
-      // ---------------- MMA issuer
+      // ---------------- MMA issuer of slot g (warp 1: slot 0, the last warp: slot 1). Each
+      // slot has its own issuing thread, so that a slot whose P is ready never waits
+      // behind the other slot's waits and commits: its PV queues on the tensor pipe at once.
+      const int g = warp == 1 ? 0 : 1;
       // kind::f16 operand formats: bf16 (1) or fp16 (0) for both A and B
       constexpr uint32_t fmt_clear = F16 ? ~((7u << 7) | (7u << 10)) : ~0u;
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK) & fmt_clear;
       constexpr uint32_t idesc_pv = (idesc_bf16_f32(kBQ, kD) & fmt_clear) | (1u << 16);  // B (V) is MN-major
       bool failed = !mbar_wait(q_full, 0, budget, abort_flag);
-      auto issue_s = [&](int g, int j) {  // S_j of slot g into its score buffer
+      auto issue_s = [&](int j) {  // S_j of slot g into its score buffer
         const int s = j % kKStages;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -273,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           tc_mma_bf16(tmem + g * kBK, a, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(s_full(g));
+        tc_commit(k_empty(s));  // this slot is done with the K stage once S_j is
         mma_issued = true;
       };
       if (!failed && n_tiles > 0) {
@@ -280,51 +297,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           failed = true;
         } else {
           tc_fence_after();
-          for (int g = 0; g < kSlots; ++g) issue_s(g, 0);
-          tc_commit(k_empty(0));
+          issue_s(0);
         }
       }
       for (int j = 0; j < n_tiles && !failed; ++j) {
-        if (j + 1 < n_tiles) {
-          // S_{j+1}: each slot's buffer is free once its softmax has read S_j
-          const int s = (j + 1) % kKStages;
-          if (!mbar_wait(k_full(s), ((j + 1) / kKStages) & 1, budget, abort_flag)) {
-            failed = true;
-            break;
-          }
-          for (int g = 0; g < kSlots; ++g) {
-            if (!mbar_wait(s_free(g), j & 1, budget, abort_flag)) {
-              failed = true;
-              break;
-            }
-            tc_fence_after();
-            issue_s(g, j + 1);
-          }
-          if (failed) break;
-          tc_commit(k_empty(s));
-        }
-        // PV_j of each slot as soon as its P_j is written
-        if (!mbar_wait(v_full, j & 1, budget, abort_flag)) {
+        // PV_j as soon as V_j has landed and P_j is in tensor memory ...
+        const int vs = j % kVStages;
+        if (!mbar_wait(v_full(vs), (j / kVStages) & 1, budget, abort_flag) ||
+            !mbar_wait(p_ready(g), j & 1, budget, abort_flag)) {
           failed = true;
           break;
         }
-        for (int g = 0; g < kSlots; ++g) {
-          if (!mbar_wait(p_ready(g), j & 1, budget, abort_flag)) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t bd = smem_desc_sw128_mn(smem_u32(sV + vs * kKVBytes + kk * 16 * 128), kKVSub, 1024);
+          tc_mma_ts(tmem + 256 + g * kD, tmem + g * kBK + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(v_empty(vs));  // this slot is done with the V stage once PV_j is
+        // ... then S_{j+1}, which overwrites P_j after PV_j has read it (issue order)
+        if (j + 1 < n_tiles) {
+          if (!mbar_wait(k_full((j + 1) % kKStages), ((j + 1) / kKStages) & 1, budget, abort_flag)) {
             failed = true;
             break;
           }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t a = smem_desc_sw128(smem_u32(sP + g * kPBytes + (kk >> 2) * kPSub)) + (uint64_t)((kk & 3) * 2);
-            const uint64_t bd = smem_desc_sw128_mn(smem_u32(sV + kk * 16 * 128), kKVSub, 1024);
-            tc_mma_bf16(tmem + 256 + g * kD, a, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(pv_done(g));
+          issue_s(j + 1);
         }
-        if (failed) break;
-        tc_commit(v_empty);
       }
+      if (!failed && n_tiles > 0) tc_commit(o_done(g));  // every PV of the slot is complete
       if (failed) {  // the MMAs in flight are drained after the CTA's final barrier
         *abort_flag = 1;
         report_timeout(p.status, 0x20 + 1);
@@ -340,12 +341,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const int qi = m0 + r;
     const int qc = min(qi, p.T - 1);
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_taddr = tmem + lane_off + g * kBK;
     const uint32_t o_taddr = tmem + lane_off + 256 + g * kD;
-    uint8_t* my_p = sP + g * kPBytes;
     float m_ref = -INFINITY, l = 0.f;
     bool failed = false;
     for (int j = 0; j < n_tiles; ++j) {
-      // warp-uniform: every lane waits, the warp gives up together
+      // The slots take turns (slot 0 tile 0, slot 1 tile 0, slot 0 tile 1, ...): each
+      // softmax runs alone on the SM's exponential units while the tensor core works on
+      // the other slot's PV and next scores. Slot 1 starts tile j once slot 0's P_j is
+      // written, slot 0 starts tile j + 1 once slot 1's P_j is.
+      if (g == 1 || j >= 1) {
+        if (!__all_sync(0xffffffffu, mbar_wait(p_ready(1 - g), (g == 1 ? j : j - 1) & 1, budget, abort_flag))) {
+          failed = true;
+          break;
+        }
+      }
+      // warp-uniform: every lane waits, the warp gives up together. S_j ready also means
+      // that this slot's PV_{j-1} is done: O is stable and the P buffer free
       if (!__all_sync(0xffffffffu, mbar_wait(s_full(g), j & 1, budget, abort_flag))) {
         failed = true;
         break;
@@ -354,11 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       tc_fence_after();
       float x[kBK];
 #pragma unroll
-      for (int c = 0; c < kBK; c += 16)
-        tmem_ld16(tmem + lane_off + g * kBK + c, *reinterpret_cast<float(*)[16]>(&x[c]));
+      for (int c = 0; c < kBK; c += 16) tmem_ld16(s_taddr + c, *reinterpret_cast<float(*)[16]>(&x[c]));
       tc_wait_ld();
-      tc_fence_before();
-      mbar_arrive(s_free(g));  // the score buffer may now take S_{j+1}
       const int n0 = (t0 + j) * kBK;
       // raw scores: masked entries become -inf (tiles on the diagonal, past the last key,
       // before the first visible key, or before the window)
@@ -387,67 +396,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         m_ref = mt;
       }
       const float neg_mu = m_ref == -INFINITY ? 0.f : -m_ref;
-      if (j >= 1) {  // the slot's P buffer and O are free once its PV_{j-1} is done
-        if (!__all_sync(0xffffffffu, mbar_wait(pv_done(g), (j - 1) & 1, budget, abort_flag))) {
-          failed = true;
-          break;
-        }
-        __syncwarp();
-        tc_fence_after();
-        if (any) {
+      if (j >= 1 && any) {  // PV_{j-1} is done (see above): rescale this warp's O rows
 #pragma unroll 1
-          for (int c = 0; c < kD; c += 16) {
-            float ov[16];
-            tmem_ld16(o_taddr + c, ov);
-            tc_wait_ld();
+        for (int c = 0; c < kD; c += 16) {
+          float ov[16];
+          tmem_ld16(o_taddr + c, ov);
+          tc_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) ov[i] *= alpha;
-            tmem_st16(o_taddr + c, ov);
-          }
-          tc_wait_st();
+          for (int i = 0; i < 16; ++i) ov[i] *= alpha;
+          tmem_st16(o_taddr + c, ov);
         }
       }
-      if (g == 0 && n0 + kBK > n_keys) {
+      if (n0 + kBK > n_keys) {
         // V rows past the item's last key may hold anything (unused cache slots): zero them,
-        // so that P = 0 meets finite values in both slots' PV products, once the tile has
-        // landed (the fence below orders this before slot 0's p_ready; slot 1's PV is
-        // issued after slot 0's)
-        if (!__all_sync(0xffffffffu, mbar_wait(v_full, j & 1, budget, abort_flag))) {
+        // so that P = 0 meets finite values, once the tile has landed. Both slots write the
+        // same zeros, each before its own p_ready (the fence below), as either slot's PV
+        // may run first
+        const int vs = j % kVStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(v_full(vs), (j / kVStages) & 1, budget, abort_flag))) {
           failed = true;
           break;
         }
         if (r >= n_keys - n0) {
-          uint8_t* vrow = sV + r * 128;
+          uint8_t* vrow = sV + vs * kKVBytes + r * 128;
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb)
 #pragma unroll
             for (int c16 = 0; c16 < 8; ++c16) *reinterpret_cast<uint4*>(vrow + hb * kKVSub + c16 * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
       }
-      // P row r straight to shared memory: two 64-key halves, 128-byte rows, 16-byte chunks
-      // XOR-swizzled by (r & 7)
+      // P row r into tensor memory over the scores it came from: 64 columns of element
+      // pairs (keys 2c, 2c + 1 in column c), written 16 columns at a time
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ch = 0; ch < kBK / 8; ++ch) {
-        uint32_t w[4];
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float w[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = ch * 8 + 2 * i;
+        for (int i = 0; i < 16; ++i) {
+          const int c = q4 * 32 + 2 * i;
           const float p0 = ex2_approx(fmaf(x[c], p.sl2, neg_mu));
           const float p1 = ex2_approx(fmaf(x[c + 1], p.sl2, neg_mu));
-          ls[i] += p0 + p1;
-          w[i] = pack2(p0, p1, F16);
+          ls[i & 3] += p0 + p1;
+          w[i] = __uint_as_float(pack2(p0, p1, F16));
         }
-        const int sub = ch >> 3, c8 = ch & 7;
-        *reinterpret_cast<uint4*>(my_p + sub * kPSub + r * 128 + ((c8 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        tmem_st16(s_taddr + q4 * 16, w);
       }
       l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-      fence_proxy_async_smem();
+      tc_wait_st();  // P (and a rescaled O) are in tensor memory before the MMA may read them
       tc_fence_before();
       mbar_arrive(p_ready(g));
     }
     if (!failed && n_tiles > 0) {
-      if (!__all_sync(0xffffffffu, mbar_wait(pv_done(g), (n_tiles - 1) & 1, budget, abort_flag))) failed = true;
+      if (!__all_sync(0xffffffffu, mbar_wait(o_done(g), 0, budget, abort_flag))) failed = true;
     }
     if (!failed) {
       __syncwarp();
@@ -512,10 +513,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int s = 0; s < kKStages; ++s)
         if (issued & (1u << s)) mbar_wait(k_full(s), (parity >> s) & 1, kDrainNs, &never);
     } else if (warp == 0 && lane == 1) {
-      if (v_issued) mbar_wait(v_full, v_last, kDrainNs, &never);
-    } else if (warp == 1 && lane == 0 && mma_issued) {
-      tc_commit(drain);
-      mbar_wait(drain, 0, kDrainNs, &never);
+      for (int s = 0; s < kVStages; ++s)
+        if (issued & (1u << s)) mbar_wait(v_full(s), (parity >> s) & 1, kDrainNs, &never);
+    } else if ((warp == 1 || warp == kThreads / 32 - 1) && lane == 0 && mma_issued) {
+      const int g = warp == 1 ? 0 : 1;
+      tc_commit(drain(g));
+      mbar_wait(drain(g), 0, kDrainNs, &never);
     }
     tc_fence_before();
     __syncthreads();
