@@ -30,6 +30,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -116,6 +117,7 @@ struct TcParams {
   int k_splits;
   int m_tiles, n_tiles;
   int num_units;
+  int group_m;  // > 1: tiles walk bands of group_m M tiles, N within a band (L2 reuse of A and B)
   TcEpiArgs e;
   DevStatus* status;
   unsigned long long wait_ns;
@@ -128,12 +130,32 @@ struct Unit {
   int ks, kb_begin, kb_end;
 };
 
+// (M tile, N tile) of tile index t. The CTAs working at one time hold consecutive
+// indices; walking bands of group_m M tiles with N varying across the band makes
+// that set a near-square patch of tiles, whose A row blocks and B column blocks are
+// each read by several of them while in L2 (M fastest over all M tiles would make
+// every round of the grid stream the whole of A again).
+__device__ __forceinline__ void tile_mn(const TcParams& p, int t, int& m_tile, int& n_tile) {
+  if (p.group_m <= 1) {
+    m_tile = t % p.m_tiles;
+    n_tile = t / p.m_tiles;
+    return;
+  }
+  const int per_band = p.group_m * p.n_tiles;
+  const int band = t / per_band;
+  const int idx = t - band * per_band;
+  const int m0 = band * p.group_m;
+  const int gm = min(p.group_m, p.m_tiles - m0);  // the last band may be narrower
+  m_tile = m0 + idx % gm;
+  n_tile = idx / gm;
+}
+
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u, int bn_rows) {
   Unit r;
   const int tile = u / p.k_splits;
   r.ks = u - tile * p.k_splits;
-  const int m_tile = tile % p.m_tiles;
-  const int n_tile = tile / p.m_tiles;
+  int m_tile, n_tile;
+  tile_mn(p, tile, m_tile, n_tile);
   r.m_tile = m_tile;
   int s = 0;
   while (s + 1 < p.na && m_tile >= p.a_tiles[s + 1]) ++s;
@@ -152,8 +174,8 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u, int bn_row
 // tiles; this CTA's A rows and epilogue rows are the pair tile's half prank.
 __device__ __forceinline__ Unit pair_unit(const TcParams& p, int u, int bn_rows, int prank) {
   Unit r;
-  const int m_pair = u % p.m_tiles;
-  const int n_tile = u / p.m_tiles;
+  int m_pair, n_tile;
+  tile_mn(p, u, m_pair, n_tile);
   r.ks = 0;
   r.kb_begin = 0;
   r.kb_end = p.num_kb;
@@ -1551,6 +1573,18 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
   if (p.num_units == 0) return cudaSuccess;
   // a pair: two CTAs per unit, whole pairs
   const int grid = d.pair ? 2 * std::min(p.num_units, max_ctas / 2) : std::min(p.num_units, max_ctas);
+  // Prefill GEMMs (one unit per tile) walk bands of group_m M tiles: the units in flight
+  // at once (one per CTA or pair) then form a patch of about sqrt(units * BN / tile rows)
+  // M tiles by the rest in N, so that the A and B blocks a round reads are about equal in
+  // bytes. Decode GEMMs keep M fastest (their clusters and splits assume it).
+  p.group_m = 1;
+  if (p.k_splits == 1 && d.epi != Epi::kPartialT && d.epi != Epi::kDecQkv && d.epi != Epi::kDecResid &&
+      d.epi != Epi::kDecAct) {
+    const int in_flight = d.pair ? grid / 2 : grid;
+    const double rows = d.pair ? 2.0 * kBM : (double)kBM;
+    const int gm = (int)std::lround(std::sqrt(in_flight * (double)d.bn / rows));
+    p.group_m = std::max(1, std::min(gm, p.m_tiles));
+  }
   cudaError_t e;
   switch (d.bn) {
     case 64: e = dispatch_epi<64>(p, d.epi, d.pair, grid, s); break;
