@@ -135,8 +135,9 @@ struct Unit {
 // that set a near-square patch of tiles, whose A row blocks and B column blocks are
 // each read by several of them while in L2 (M fastest over all M tiles would make
 // every round of the grid stream the whole of A again).
+template <bool kGrouped>
 __device__ __forceinline__ void tile_mn(const TcParams& p, int t, int& m_tile, int& n_tile) {
-  if (p.group_m <= 1) {
+  if (!kGrouped || p.group_m <= 1) {
     m_tile = t % p.m_tiles;
     n_tile = t / p.m_tiles;
     return;
@@ -150,12 +151,14 @@ __device__ __forceinline__ void tile_mn(const TcParams& p, int t, int& m_tile, i
   n_tile = idx / gm;
 }
 
+// kGrouped: the prefill GEMMs' banded order (the decode GEMMs keep M fastest)
+template <bool kGrouped = false>
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u, int bn_rows) {
   Unit r;
   const int tile = u / p.k_splits;
   r.ks = u - tile * p.k_splits;
   int m_tile, n_tile;
-  tile_mn(p, tile, m_tile, n_tile);
+  tile_mn<kGrouped>(p, tile, m_tile, n_tile);
   r.m_tile = m_tile;
   int s = 0;
   while (s + 1 < p.na && m_tile >= p.a_tiles[s + 1]) ++s;
@@ -175,7 +178,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u, int bn_row
 __device__ __forceinline__ Unit pair_unit(const TcParams& p, int u, int bn_rows, int prank) {
   Unit r;
   int m_pair, n_tile;
-  tile_mn(p, u, m_pair, n_tile);
+  tile_mn<true>(p, u, m_pair, n_tile);
   r.ks = 0;
   r.kb_begin = 0;
   r.kb_end = p.num_kb;
@@ -927,6 +930,8 @@ template <int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<BN, EPI, PAIR>;
   constexpr int S = C::kStages;
+  // the prefill epilogues walk the banded tile order; the decode ones keep M fastest
+  constexpr bool kGrp = !is_cluster_epi<EPI>() && EPI != (int)Epi::kPartialT;
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1057,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       // previous kernel finishes; the activations only after pdl_wait().
       // (a pair: the even CTA expects both CTAs' bytes)
       constexpr uint32_t kTxBytes = (PAIR ? 2 : 1) * C::kStageBytes;
-      auto unit_of = [&](int u) { return PAIR ? pair_unit(p, u, bn_rows, prank) : decode_unit(p, u, bn_rows); };
+      auto unit_of = [&](int u) { return PAIR ? pair_unit(p, u, bn_rows, prank) : decode_unit<kGrp>(p, u, bn_rows); };
       int pre = 0;
       if (p.const_op != 0 && u0 < p.num_units) {
         const Unit un = unit_of(u0);
@@ -1116,7 +1121,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       int it = 0;
       bool failed = false;
       for (int u = u0; u < p.num_units && !failed; u += ustep, ++it) {
-        const Unit un = PAIR ? pair_unit(p, u, bn_rows, prank) : decode_unit(p, u, bn_rows);
+        const Unit un = PAIR ? pair_unit(p, u, bn_rows, prank) : decode_unit<kGrp>(p, u, bn_rows);
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
         if (!mbar_wait(tempty_bar(acc), aph ^ 1, budget, abort_flag)) {
@@ -1189,7 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int it = 0;
     bool failed = false;
     for (int u = u0; u < p.num_units; u += ustep, ++it) {
-      const Unit un = PAIR ? pair_unit(p, u, bn_rows, prank) : decode_unit(p, u, bn_rows);
+      const Unit un = PAIR ? pair_unit(p, u, bn_rows, prank) : decode_unit<kGrp>(p, u, bn_rows);
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
