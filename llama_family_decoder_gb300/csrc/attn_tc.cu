@@ -59,6 +59,7 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr unsigned long long kDrainNs = 2000000000ULL;
 constexpr float kLog2e = 1.4426950408889634f;
 static_assert(kSmem <= 227 * 1024, "shared memory");
+static_assert(kQSub == kKVSub && kKStages == 2 && kVStages == 2, "the MMA issuers' descriptor steps and stage selects");
 
 struct AttnParams {
   CUtensorMap tq, tk, tv;
@@ -280,14 +281,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK) & fmt_clear;
       constexpr uint32_t idesc_pv = (idesc_bf16_f32(kBQ, kD) & fmt_clear) | (1u << 16);  // B (V) is MN-major
       bool failed = !mbar_wait(q_full, 0, budget, abort_flag);
+      // Shared-memory descriptors, built once: a descriptor's start-address field counts
+      // 16-byte units, so K step kk of a 128-byte-swizzled operand sits (kk / 4) halves of
+      // 16 KB and (kk % 4) 32-byte steps further; V's 16-key steps are 2 KB apart.
+      const uint64_t dq = smem_desc_sw128(smem_u32(sQ + g * kQBytes));
+      uint64_t dk[kKStages], dv[kVStages];
+#pragma unroll
+      for (int st = 0; st < kKStages; ++st) dk[st] = smem_desc_sw128(smem_u32(sK + st * kKVBytes));
+#pragma unroll
+      for (int st = 0; st < kVStages; ++st) dv[st] = smem_desc_sw128_mn(smem_u32(sV + st * kKVBytes), kKVSub, 1024);
+      auto kstep = [](int kk) { return (uint64_t)((kk >> 2) * (kQSub >> 4) + (kk & 3) * 2); };
+      const uint32_t s_tmem = tmem + g * kBK, o_tmem = tmem + 256 + g * kD;
       auto issue_s = [&](int j) {  // S_j of slot g into its score buffer
         const int s = j % kKStages;
+        const uint64_t dks = s == 0 ? dk[0] : dk[1];
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(smem_u32(sQ + g * kQBytes + (kk >> 2) * kQSub)) + (uint64_t)((kk & 3) * 2);
-          const uint64_t bd = smem_desc_sw128(smem_u32(sK + s * kKVBytes + (kk >> 2) * kKVSub)) + (uint64_t)((kk & 3) * 2);
-          tc_mma_bf16(tmem + g * kBK, a, bd, idesc_s, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kD / 16; ++kk) tc_mma_bf16(s_tmem, dq + kstep(kk), dks + kstep(kk), idesc_s, kk > 0 ? 1u : 0u);
         tc_commit(s_full(g));
         tc_commit(k_empty(s));  // this slot is done with the K stage once S_j is
         mma_issued = true;
@@ -309,11 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           break;
         }
         tc_fence_after();
+        const uint64_t dvs = vs == 0 ? dv[0] : dv[1];
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128_mn(smem_u32(sV + vs * kKVBytes + kk * 16 * 128), kKVSub, 1024);
-          tc_mma_ts(tmem + 256 + g * kD, tmem + g * kBK + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          tc_mma_ts(o_tmem, s_tmem + kk * 8, dvs + (uint64_t)(kk * (16 * 128 >> 4)), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(v_empty(vs));  // this slot is done with the V stage once PV_j is
         // ... then S_{j+1}, which overwrites P_j after PV_j has read it (issue order)
         if (j + 1 < n_tiles) {
