@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   uint8_t* sK = sQ + kSlots * kQBytes;                  // [stage]: two halves of 16 KB
   uint8_t* sV = sK + kKStages * kKVBytes;               // [stage]: two halves of 16 KB
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kVStages * kKVBytes);
-  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_ready[2], o_done[2], drain[2]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 18);
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_ready[2][4], o_done[2], drain[2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 24);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const uint32_t q_full = smem_u32(&bars[0]);
   auto k_full = [&](int s) { return smem_u32(&bars[1 + s]); };
@@ -132,9 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   auto v_full = [&](int s) { return smem_u32(&bars[5 + s]); };
   auto v_empty = [&](int s) { return smem_u32(&bars[7 + s]); };
   auto s_full = [&](int g) { return smem_u32(&bars[9 + g]); };
-  auto p_ready = [&](int g) { return smem_u32(&bars[11 + g]); };
-  auto o_done = [&](int g) { return smem_u32(&bars[13 + g]); };
-  auto drain = [&](int g) { return smem_u32(&bars[15 + g]); };
+  // P is released in quarters of 32 keys, each on its own barrier (one phase per tile):
+  // the PV steps of a quarter run while the softmax computes the next quarter
+  auto p_ready = [&](int g, int q) { return smem_u32(&bars[11 + 4 * g + q]); };
+  auto o_done = [&](int g) { return smem_u32(&bars[19 + g]); };
+  auto drain = [&](int g) { return smem_u32(&bars[21 + g]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // ---- the work item: two slots over one KV head of one sequence, heaviest first
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     for (int g = 0; g < kSlots; ++g) {
       mbar_init(s_full(g), 1);
-      mbar_init(p_ready(g), 128);
+      for (int q = 0; q < 4; ++q) mbar_init(p_ready(g, q), 128);
       mbar_init(o_done(g), 1);
       mbar_init(drain(g), 1);
     }
@@ -312,16 +314,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int j = 0; j < n_tiles && !failed; ++j) {
         // PV_j as soon as V_j has landed and P_j is in tensor memory ...
         const int vs = j % kVStages;
-        if (!mbar_wait(v_full(vs), (j / kVStages) & 1, budget, abort_flag) ||
-            !mbar_wait(p_ready(g), j & 1, budget, abort_flag)) {
+        if (!mbar_wait(v_full(vs), (j / kVStages) & 1, budget, abort_flag)) {
           failed = true;
           break;
         }
-        tc_fence_after();
         const uint64_t dvs = vs == 0 ? dv[0] : dv[1];
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          tc_mma_ts(o_tmem, s_tmem + kk * 8, dvs + (uint64_t)(kk * (16 * 128 >> 4)), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int q = 0; q < 4; ++q) {  // each quarter of P as soon as it is written: two K steps of 16 keys
+          if (!mbar_wait(p_ready(g, q), j & 1, budget, abort_flag)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 2 * q; kk < 2 * q + 2; ++kk)
+            tc_mma_ts(o_tmem, s_tmem + kk * 8, dvs + (uint64_t)(kk * (16 * 128 >> 4)), idesc_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (failed) break;
         tc_commit(v_empty(vs));  // this slot is done with the V stage once PV_j is
         // ... then S_{j+1}, which overwrites P_j after PV_j has read it (issue order)
         if (j + 1 < n_tiles) {
@@ -359,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       // the other slot's PV and next scores. Slot 1 starts tile j once slot 0's P_j is
       // written, slot 0 starts tile j + 1 once slot 1's P_j is.
       if (g == 1 || j >= 1) {
-        if (!__all_sync(0xffffffffu, mbar_wait(p_ready(1 - g), (g == 1 ? j : j - 1) & 1, budget, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(p_ready(1 - g, 3), (g == 1 ? j : j - 1) & 1, budget, abort_flag))) {
           failed = true;
           break;
         }
@@ -449,11 +459,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           w[i] = __uint_as_float(pack2(p0, p1, F16));
         }
         tmem_st16(s_taddr + q4 * 16, w);
+        tc_wait_st();  // this quarter of P (and a rescaled O) in tensor memory before its PV steps
+        tc_fence_before();
+        mbar_arrive(p_ready(g, q4));
       }
       l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-      tc_wait_st();  // P (and a rescaled O) are in tensor memory before the MMA may read them
-      tc_fence_before();
-      mbar_arrive(p_ready(g));
     }
     if (!failed && n_tiles > 0) {
       if (!__all_sync(0xffffffffu, mbar_wait(o_done(g), 0, budget, abort_flag))) failed = true;
