@@ -3,9 +3,12 @@
 // k.T / sqrt(128), mask=causal) @ v per head; "arcee", "Grouped-query attention,
 // 128-wide heads": query head h reads KV head h / (H / Hkv)).
 //
-// One CTA per work item of two 128-query slots that share every K/V tile: two
-// query heads of one KV group at the same query tile (an even group size), or
-// two consecutive query tiles of one head (otherwise); heaviest items first.
+// Work items of two 128-query slots that share every K/V tile: two query heads of
+// one KV group at the same query tile (an even group size), or two consecutive
+// query tiles of one head (otherwise). Persistent: one CTA per SM walks the items,
+// heaviest first, dealt out in a snake order; barrier phases and ring positions run
+// on across items, so that the next item's Q, first K/V tiles and first score
+// products overlap the current item's last softmax, PV and output store.
 // 352 threads:
 //   warp 0      TMA producers: lane 0 both slots' Q tiles once, then K tiles of
 //               128 keys through a 2-stage ring; lane 1 the V tiles through their
@@ -35,6 +38,8 @@
 // Every wait is bounded; on expiry the CTA records a timeout, drains its own
 // copies and MMAs, frees its TMEM and returns.
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -113,7 +118,66 @@ struct Slot {
   int h, qt, m0, valid;
 };
 
-// F16: q, k, v (and so P) are fp16; otherwise bf16.
+// A work item: two slots over one KV head of one sequence, and its key-tile range.
+struct Item {
+  Slot sl[kSlots];
+  int b, kv_row, off, kv_lo, kv_hi, n_keys, t0, n_tiles;
+};
+
+// Item id, heaviest first: the far query tiles (more keys) get the small ids. Reads
+// the cache positions and key ranges, so it runs after pdl_wait.
+__device__ __forceinline__ Item item_of(const AttnParams& p, int id) {
+  Item it;
+  if (p.head_pairs) {
+    const int hp_n = p.H / 2;
+    const int qt = p.n_qtiles - 1 - id / (p.B * hp_n);
+    const int r = id % (p.B * hp_n);
+    const int hp = r % hp_n;
+    it.b = r / hp_n;
+#pragma unroll
+    for (int g = 0; g < kSlots; ++g) it.sl[g] = {2 * hp + g, qt, qt * kBQ, 1};
+  } else {
+    const int np = (p.n_qtiles + 1) / 2;
+    const int k = np - 1 - id / (p.B * p.H);
+    const int r = id % (p.B * p.H);
+    const int h = r % p.H;
+    it.b = r / p.H;
+#pragma unroll
+    for (int g = 0; g < kSlots; ++g) {
+      const int qt = 2 * k + g;
+      const int ok = qt < p.n_qtiles;
+      it.sl[g] = {h, ok ? qt : 2 * k, (ok ? qt : 2 * k) * kBQ, ok};
+    }
+  }
+  const int kvh = it.sl[0].h / (p.H / p.Hkv);
+  it.kv_row = (it.b * p.Hkv + kvh) * p.kv_stride;
+  it.off = p.q_off ? p.q_off[it.b] : 0;  // keys 0 .. off - 1 are earlier positions in the cache
+  // visible keys: [kv_lo, kv_hi) (an attention_mask's run of real tokens, else all)
+  const int2 kr = p.key_range ? p.key_range[it.b] : make_int2(0, it.off + p.T);
+  it.kv_lo = kr.x;
+  it.kv_hi = kr.y;
+  // the key tiles the item needs: the union of both slots' ranges
+  int n_keys = 0, first_key = 1 << 30;
+#pragma unroll
+  for (int g = 0; g < kSlots; ++g) {
+    const int kv_end = min(p.T, it.sl[g].m0 + kBQ);
+    n_keys = max(n_keys, min(it.off + kv_end, it.kv_hi));
+    first_key = min(first_key, max(it.kv_lo, p.window > 0 ? it.off + it.sl[g].m0 - p.window + 1 : 0));
+  }
+  it.n_keys = n_keys;
+  it.t0 = max(0, first_key) / kBK;
+  it.n_tiles = max(0, (n_keys + kBK - 1) / kBK - it.t0);  // none when every query is padding
+  return it;
+}
+
+// Round k of CTA c among G: the heaviest-first ids dealt out in a snake (c, then
+// 2G - 1 - c, ...), so that every CTA's rounds sum to about the same work.
+__device__ __forceinline__ int item_id(int k, int G, int c) { return k * G + ((k & 1) ? G - 1 - c : c); }
+
+// F16: q, k, v (and so P) are fp16; otherwise bf16. Persistent: CTA c runs items
+// item_id(0, G, c), item_id(1, G, c), ... Barrier phases and ring positions run on
+// across items, so that the next item's Q, first K/V tiles and first score products
+// overlap the current item's last softmax, PV and output store.
 template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
   pdl_launch_dependents();
@@ -123,53 +187,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   uint8_t* sK = sQ + kSlots * kQBytes;                  // [stage]: two halves of 16 KB
   uint8_t* sV = sK + kKStages * kKVBytes;               // [stage]: two halves of 16 KB
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kVStages * kKVBytes);
-  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_ready[2][4], o_done[2], drain[2]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 24);
+  // q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_ready[2][4],
+  // o_done[2], o_free[2], drain[2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 26);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const uint32_t q_full = smem_u32(&bars[0]);
-  auto k_full = [&](int s) { return smem_u32(&bars[1 + s]); };
-  auto k_empty = [&](int s) { return smem_u32(&bars[3 + s]); };
-  auto v_full = [&](int s) { return smem_u32(&bars[5 + s]); };
-  auto v_empty = [&](int s) { return smem_u32(&bars[7 + s]); };
-  auto s_full = [&](int g) { return smem_u32(&bars[9 + g]); };
+  const uint32_t q_empty = smem_u32(&bars[1]);
+  auto k_full = [&](int s) { return smem_u32(&bars[2 + s]); };
+  auto k_empty = [&](int s) { return smem_u32(&bars[4 + s]); };
+  auto v_full = [&](int s) { return smem_u32(&bars[6 + s]); };
+  auto v_empty = [&](int s) { return smem_u32(&bars[8 + s]); };
+  auto s_full = [&](int g) { return smem_u32(&bars[10 + g]); };
   // P is released in quarters of 32 keys, each on its own barrier (one phase per tile):
   // the PV steps of a quarter run while the softmax computes the next quarter
-  auto p_ready = [&](int g, int q) { return smem_u32(&bars[11 + 4 * g + q]); };
-  auto o_done = [&](int g) { return smem_u32(&bars[19 + g]); };
-  auto drain = [&](int g) { return smem_u32(&bars[21 + g]); };
+  auto p_ready = [&](int g, int q) { return smem_u32(&bars[12 + 4 * g + q]); };
+  auto o_done = [&](int g) { return smem_u32(&bars[20 + g]); };
+  auto o_free = [&](int g) { return smem_u32(&bars[22 + g]); };
+  auto drain = [&](int g) { return smem_u32(&bars[24 + g]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // ---- the work item: two slots over one KV head of one sequence, heaviest first
-  const int id = blockIdx.x;
-  Slot sl[kSlots];
-  int b, kvh;
-  if (p.head_pairs) {
-    const int hp_n = p.H / 2;
-    const int qt = p.n_qtiles - 1 - id / (p.B * hp_n);
-    const int r = id % (p.B * hp_n);
-    const int hp = r % hp_n;
-    b = r / hp_n;
-#pragma unroll
-    for (int g = 0; g < kSlots; ++g) sl[g] = {2 * hp + g, qt, qt * kBQ, 1};
-  } else {
-    const int np = (p.n_qtiles + 1) / 2;
-    const int k = np - 1 - id / (p.B * p.H);
-    const int r = id % (p.B * p.H);
-    const int h = r % p.H;
-    b = r / p.H;
-#pragma unroll
-    for (int g = 0; g < kSlots; ++g) {
-      const int qt = 2 * k + g;
-      const int ok = qt < p.n_qtiles;
-      sl[g] = {h, ok ? qt : 2 * k, (ok ? qt : 2 * k) * kBQ, ok};
-    }
-  }
-  kvh = sl[0].h / (p.H / p.Hkv);
-  const int kv_row = (b * p.Hkv + kvh) * p.kv_stride;
   const unsigned long long budget = p.wait_ns;
+  const int G = gridDim.x, cta = blockIdx.x;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, kSlots);  // one commit from each slot's MMA issuer after its item's last S
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), kSlots);  // one commit from each slot's MMA issuer
@@ -182,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       mbar_init(s_full(g), 1);
       for (int q = 0; q < 4; ++q) mbar_init(p_ready(g, q), 128);
       mbar_init(o_done(g), 1);
+      mbar_init(o_free(g), 128);  // the slot's softmax threads, once they have read O out
       mbar_init(drain(g), 1);
     }
     *abort_flag = 0;
@@ -201,50 +244,49 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   tc_fence_after();
   pdl_wait();  // q, k, v (and the cache positions, the key ranges) come from earlier kernels
   const uint32_t tmem = *tmem_holder;  // S[g] (and P[g] over its first 64 columns): cols 128 g; O[g]: 256 + 128 g
-  const int off = p.q_off ? p.q_off[b] : 0;  // keys 0 .. off - 1 are earlier positions in the cache
-  // visible keys: [kv_lo, kv_hi) (an attention_mask's run of real tokens, else all)
-  const int2 kr = p.key_range ? p.key_range[b] : make_int2(0, off + p.T);
-  const int kv_lo = kr.x, kv_hi = kr.y;
-  // the key tiles the item needs: the union of both slots' ranges
-  int n_keys = 0, first_key = 1 << 30;
-#pragma unroll
-  for (int g = 0; g < kSlots; ++g) {
-    const int kv_end = min(p.T, sl[g].m0 + kBQ);
-    n_keys = max(n_keys, min(off + kv_end, kv_hi));
-    first_key = min(first_key, max(kv_lo, p.window > 0 ? off + sl[g].m0 - p.window + 1 : 0));
-  }
-  const int t0 = max(0, first_key) / kBK;
-  const int n_tiles = max(0, (n_keys + kBK - 1) / kBK - t0);  // none when every query is padding
-  // What the producer lanes and the MMA lane have in flight, for the drain after an
-  // abort: the K and V stages issued (with the parity of their last phase), and
-  // whether any MMA was issued.
-  uint32_t issued = 0, parity = 0;
-  bool mma_issued = false;
+  // What the producer lanes and the MMA lanes have in flight, for the drain after an
+  // abort: the ring stages issued (with the parity of their last phase), the last Q
+  // load's parity, and whether any MMA was issued.
+  uint32_t issued = 0, parity = 0, q_parity = 0;
+  bool q_issued = false, mma_issued = false;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer: Q, then the K ring
+      // ---------------- TMA producer: each item's Q, then its K tiles through the ring
       bool failed = false;
-      mbar_arrive_expect_tx(q_full, kSlots * kQBytes);
-#pragma unroll
-      for (int g = 0; g < kSlots; ++g) {
-        const int q_row = (b * p.H + sl[g].h) * p.T + sl[g].m0;
-        tma_load_2d(smem_u32(sQ + g * kQBytes), &p.tq, 0, q_row, q_full);
-        tma_load_2d(smem_u32(sQ + g * kQBytes + kQSub), &p.tq, 64, q_row, q_full);
-      }
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kKStages;
-        const uint32_t ph = (j / kKStages) & 1;
-        if (!mbar_wait(k_empty(s), ph ^ 1, budget, abort_flag)) {
+      int J = 0;  // K tiles issued over all items
+      for (int k = 0; !failed; ++k) {
+        const int id = item_id(k, G, cta);
+        if (id >= p.n_items) break;
+        const Item it = item_of(p, id);
+        // the Q buffer is free once both slots' score products of the previous item are done
+        if (!mbar_wait(q_empty, (k & 1) ^ 1, budget, abort_flag)) {
           failed = true;
           break;
         }
-        mbar_arrive_expect_tx(k_full(s), kKVBytes);
-        const int row = kv_row + (t0 + j) * kBK;
-        tma_load_2d(smem_u32(sK + s * kKVBytes), &p.tk, 0, row, k_full(s));
-        tma_load_2d(smem_u32(sK + s * kKVBytes + kKVSub), &p.tk, 64, row, k_full(s));
-        issued |= 1u << s;
-        parity = (parity & ~(1u << s)) | (ph << s);
+        mbar_arrive_expect_tx(q_full, kSlots * kQBytes);
+#pragma unroll
+        for (int g = 0; g < kSlots; ++g) {
+          const int q_row = (it.b * p.H + it.sl[g].h) * p.T + it.sl[g].m0;
+          tma_load_2d(smem_u32(sQ + g * kQBytes), &p.tq, 0, q_row, q_full);
+          tma_load_2d(smem_u32(sQ + g * kQBytes + kQSub), &p.tq, 64, q_row, q_full);
+        }
+        q_issued = true;
+        q_parity = k & 1;
+        for (int j = 0; j < it.n_tiles; ++j, ++J) {
+          const int s = J % kKStages;
+          const uint32_t ph = (J / kKStages) & 1;
+          if (!mbar_wait(k_empty(s), ph ^ 1, budget, abort_flag)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_expect_tx(k_full(s), kKVBytes);
+          const int row = it.kv_row + (it.t0 + j) * kBK;
+          tma_load_2d(smem_u32(sK + s * kKVBytes), &p.tk, 0, row, k_full(s));
+          tma_load_2d(smem_u32(sK + s * kKVBytes + kKVSub), &p.tk, 64, row, k_full(s));
+          issued |= 1u << s;
+          parity = (parity & ~(1u << s)) | (ph << s);
+        }
       }
       if (failed) {  // the loads in flight are drained after the CTA's final barrier
         *abort_flag = 1;
@@ -253,19 +295,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     } else if (lane == 1) {
       // ---------------- TMA producer: the V ring (its own thread, so that K never waits behind V)
       bool failed = false;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kVStages;
-        const uint32_t ph = (j / kVStages) & 1;
-        if (!mbar_wait(v_empty(s), ph ^ 1, budget, abort_flag)) {
-          failed = true;
-          break;
+      int J = 0;
+      for (int k = 0; !failed; ++k) {
+        const int id = item_id(k, G, cta);
+        if (id >= p.n_items) break;
+        const Item it = item_of(p, id);
+        for (int j = 0; j < it.n_tiles; ++j, ++J) {
+          const int s = J % kVStages;
+          const uint32_t ph = (J / kVStages) & 1;
+          if (!mbar_wait(v_empty(s), ph ^ 1, budget, abort_flag)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_expect_tx(v_full(s), kKVBytes);
+          const int row = it.kv_row + (it.t0 + j) * kBK;
+          tma_load_2d(smem_u32(sV + s * kKVBytes), &p.tv, 0, row, v_full(s));
+          tma_load_2d(smem_u32(sV + s * kKVBytes + kKVSub), &p.tv, 64, row, v_full(s));
+          issued |= 1u << s;
+          parity = (parity & ~(1u << s)) | (ph << s);
         }
-        mbar_arrive_expect_tx(v_full(s), kKVBytes);
-        const int row = kv_row + (t0 + j) * kBK;
-        tma_load_2d(smem_u32(sV + s * kKVBytes), &p.tv, 0, row, v_full(s));
-        tma_load_2d(smem_u32(sV + s * kKVBytes + kKVSub), &p.tv, 64, row, v_full(s));
-        issued |= 1u << s;
-        parity = (parity & ~(1u << s)) | (ph << s);
       }
       if (failed) {
         *abort_flag = 1;
@@ -282,7 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       constexpr uint32_t fmt_clear = F16 ? ~((7u << 7) | (7u << 10)) : ~0u;
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK) & fmt_clear;
       constexpr uint32_t idesc_pv = (idesc_bf16_f32(kBQ, kD) & fmt_clear) | (1u << 16);  // B (V) is MN-major
-      bool failed = !mbar_wait(q_full, 0, budget, abort_flag);
       // Shared-memory descriptors, built once: a descriptor's start-address field counts
       // 16-byte units, so K step kk of a 128-byte-swizzled operand sits (kk / 4) halves of
       // 16 KB and (kk % 4) 32-byte steps further; V's 16-key steps are 2 KB apart.
@@ -294,56 +341,78 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int st = 0; st < kVStages; ++st) dv[st] = smem_desc_sw128_mn(smem_u32(sV + st * kKVBytes), kKVSub, 1024);
       auto kstep = [](int kk) { return (uint64_t)((kk >> 2) * (kQSub >> 4) + (kk & 3) * 2); };
       const uint32_t s_tmem = tmem + g * kBK, o_tmem = tmem + 256 + g * kD;
-      auto issue_s = [&](int j) {  // S_j of slot g into its score buffer
-        const int s = j % kKStages;
+      auto issue_s = [&](int J) {  // S of global tile J (K stage J % 2) into the slot's score buffer
+        const int s = J % kKStages;
         const uint64_t dks = s == 0 ? dk[0] : dk[1];
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) tc_mma_bf16(s_tmem, dq + kstep(kk), dks + kstep(kk), idesc_s, kk > 0 ? 1u : 0u);
         tc_commit(s_full(g));
-        tc_commit(k_empty(s));  // this slot is done with the K stage once S_j is
+        tc_commit(k_empty(s));  // this slot is done with the K stage once this S is
         mma_issued = true;
       };
-      if (!failed && n_tiles > 0) {
-        if (!mbar_wait(k_full(0), 0, budget, abort_flag)) {
-          failed = true;
-        } else {
-          tc_fence_after();
-          issue_s(0);
-        }
-      }
-      for (int j = 0; j < n_tiles && !failed; ++j) {
-        // PV_j as soon as V_j has landed and P_j is in tensor memory ...
-        const int vs = j % kVStages;
-        if (!mbar_wait(v_full(vs), (j / kVStages) & 1, budget, abort_flag)) {
+      bool failed = false;
+      int J = 0;  // tiles over all items
+      for (int k = 0; !failed; ++k) {
+        const int id = item_id(k, G, cta);
+        if (id >= p.n_items) break;
+        const Item it = item_of(p, id);
+        if (!mbar_wait(q_full, k & 1, budget, abort_flag)) {
           failed = true;
           break;
         }
-        const uint64_t dvs = vs == 0 ? dv[0] : dv[1];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {  // each quarter of P as soon as it is written: two K steps of 16 keys
-          if (!mbar_wait(p_ready(g, q), j & 1, budget, abort_flag)) {
+        if (it.n_tiles > 0) {
+          if (!mbar_wait(k_full(J % kKStages), (J / kKStages) & 1, budget, abort_flag)) {
             failed = true;
             break;
           }
           tc_fence_after();
+          issue_s(J);
+        }
+        if (it.n_tiles <= 1) tc_commit(q_empty);  // no further score product of this item reads Q
+        for (int j = 0; j < it.n_tiles; ++j, ++J) {
+          // PV_j as soon as V_j has landed, O is free (the previous item's output read out)
+          // and each quarter of P_j is in tensor memory ...
+          const int vs = J % kVStages;
+          if (!mbar_wait(v_full(vs), (J / kVStages) & 1, budget, abort_flag) ||
+              (j == 0 && k >= 1 && !mbar_wait(o_free(g), (k - 1) & 1, budget, abort_flag))) {
+            failed = true;
+            break;
+          }
+          const uint64_t dvs = vs == 0 ? dv[0] : dv[1];
 #pragma unroll
-          for (int kk = 2 * q; kk < 2 * q + 2; ++kk)
-            tc_mma_ts(o_tmem, s_tmem + kk * 8, dvs + (uint64_t)(kk * (16 * 128 >> 4)), idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+          for (int q = 0; q < 4; ++q) {
+            if (!mbar_wait(p_ready(g, q), J & 1, budget, abort_flag)) {
+              failed = true;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 2 * q; kk < 2 * q + 2; ++kk)
+              tc_mma_ts(o_tmem, s_tmem + kk * 8, dvs + (uint64_t)(kk * (16 * 128 >> 4)), idesc_pv,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (failed) break;
+          tc_commit(v_empty(vs));  // this slot is done with the V stage once PV_j is
+          // ... then S_{j+1}, which overwrites P_j after PV_j has read it (issue order)
+          if (j + 1 < it.n_tiles) {
+            if (!mbar_wait(k_full((J + 1) % kKStages), ((J + 1) / kKStages) & 1, budget, abort_flag)) {
+              failed = true;
+              break;
+            }
+            tc_fence_after();
+            issue_s(J + 1);
+            if (j + 2 == it.n_tiles) tc_commit(q_empty);  // that was the item's last score product
+          }
         }
         if (failed) break;
-        tc_commit(v_empty(vs));  // this slot is done with the V stage once PV_j is
-        // ... then S_{j+1}, which overwrites P_j after PV_j has read it (issue order)
-        if (j + 1 < n_tiles) {
-          if (!mbar_wait(k_full((j + 1) % kKStages), ((j + 1) / kKStages) & 1, budget, abort_flag)) {
-            failed = true;
-            break;
-          }
-          tc_fence_after();
-          issue_s(j + 1);
+        // An item without key tiles has no PV that waited for the previous item's O to be
+        // read out: wait here, so that o_done runs at most one phase ahead of its waiter.
+        if (it.n_tiles == 0 && k >= 1 && !mbar_wait(o_free(g), (k - 1) & 1, budget, abort_flag)) {
+          failed = true;
+          break;
         }
+        tc_commit(o_done(g));  // every PV of the slot's item is complete
       }
-      if (!failed && n_tiles > 0) tc_commit(o_done(g));  // every PV of the slot is complete
       if (failed) {  // the MMAs in flight are drained after the CTA's final barrier
         *abort_flag = 1;
         report_timeout(p.status, 0x20 + 1);
@@ -354,126 +423,134 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const int g = (warp - 2) / 4;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    const Slot me = g == 0 ? sl[0] : sl[1];  // a select, not a run-time index into local memory
-    const int m0 = me.m0;
-    const int qi = m0 + r;
-    const int qc = min(qi, p.T - 1);
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_taddr = tmem + lane_off + g * kBK;
     const uint32_t o_taddr = tmem + lane_off + 256 + g * kD;
-    float m_ref = -INFINITY, l = 0.f;
     bool failed = false;
-    for (int j = 0; j < n_tiles; ++j) {
-      // The slots take turns (slot 0 tile 0, slot 1 tile 0, slot 0 tile 1, ...): each
-      // softmax runs alone on the SM's exponential units while the tensor core works on
-      // the other slot's PV and next scores. Slot 1 starts tile j once slot 0's P_j is
-      // written, slot 0 starts tile j + 1 once slot 1's P_j is.
-      if (g == 1 || j >= 1) {
-        if (!__all_sync(0xffffffffu, mbar_wait(p_ready(1 - g, 3), (g == 1 ? j : j - 1) & 1, budget, abort_flag))) {
+    int J = 0;  // tiles over all items
+    for (int k = 0; !failed; ++k) {
+      const int id = item_id(k, G, cta);
+      if (id >= p.n_items) break;
+      const Item it = item_of(p, id);
+      const Slot me = g == 0 ? it.sl[0] : it.sl[1];  // a select, not a run-time index into local memory
+      const int m0 = me.m0;
+      const int qi = m0 + r;
+      const int qc = min(qi, p.T - 1);
+      const int off = it.off, kv_lo = it.kv_lo, kv_hi = it.kv_hi, n_keys = it.n_keys;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < it.n_tiles; ++j, ++J) {
+        // The slots take turns (slot 0 tile J, slot 1 tile J, slot 0 tile J + 1, ...): each
+        // softmax runs alone on the SM's exponential units while the tensor core works on
+        // the other slot's PV and next scores. Slot 1 starts tile J once slot 0's P_J is
+        // written, slot 0 starts tile J + 1 once slot 1's P_J is.
+        if (g == 1 || J >= 1) {
+          if (!__all_sync(0xffffffffu, mbar_wait(p_ready(1 - g, 3), (g == 1 ? J : J - 1) & 1, budget, abort_flag))) {
+            failed = true;
+            break;
+          }
+        }
+        // warp-uniform: every lane waits, the warp gives up together. S_J ready also means
+        // that this slot's PV_{J-1} is done: O is stable and the P buffer free
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full(g), J & 1, budget, abort_flag))) {
           failed = true;
           break;
         }
+        __syncwarp();
+        tc_fence_after();
+        float x[kBK];
+#pragma unroll
+        for (int c = 0; c < kBK; c += 16) tmem_ld16(s_taddr + c, *reinterpret_cast<float(*)[16]>(&x[c]));
+        tc_wait_ld();
+        const int n0 = (it.t0 + j) * kBK;
+        // raw scores: masked entries become -inf (tiles on the diagonal, past the last key,
+        // before the first visible key, or before the window)
+        if ((n0 + kBK - 1 > off + m0) || (n0 + kBK > kv_hi) || n0 < kv_lo ||
+            (p.window > 0 && n0 < off + min(m0 + kBQ - 1, p.T - 1) - p.window + 1)) {
+          const int causal = off + qc - n0;                    // keys n0 + c with c <= causal are not ahead
+          const int lim = min(causal, kv_hi - 1 - n0);         // ... nor padding after the run
+          const int first = max(p.window > 0 ? causal - p.window + 1 : -kBK, kv_lo - n0);  // c >= first
+#pragma unroll
+          for (int c = 0; c < kBK; ++c)
+            if (c > lim || c < first) x[c] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = x[i];
+#pragma unroll
+        for (int c = 8; c < kBK; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+        const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float mt = mraw * p.sl2;  // the scale is positive: the max commutes with it
+        const bool need = mt > m_ref + kRescaleLog2;
+        const bool any = __any_sync(0xffffffffu, need);
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m_ref - mt);
+          m_ref = mt;
+        }
+        const float neg_mu = m_ref == -INFINITY ? 0.f : -m_ref;
+        if (j >= 1 && any) {  // PV_{J-1} is done (see above): rescale this warp's O rows
+#pragma unroll 1
+          for (int c = 0; c < kD; c += 16) {
+            float ov[16];
+            tmem_ld16(o_taddr + c, ov);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] *= alpha;
+            tmem_st16(o_taddr + c, ov);
+          }
+        }
+        if (n0 + kBK > n_keys) {
+          // V rows past the item's last key may hold anything (unused cache slots): zero them,
+          // so that P = 0 meets finite values, once the tile has landed. Both slots write the
+          // same zeros, each before its own p_ready (the fence below), as either slot's PV
+          // may run first
+          const int vs = J % kVStages;
+          if (!__all_sync(0xffffffffu, mbar_wait(v_full(vs), (J / kVStages) & 1, budget, abort_flag))) {
+            failed = true;
+            break;
+          }
+          if (r >= n_keys - n0) {
+            uint8_t* vrow = sV + vs * kKVBytes + r * 128;
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+              for (int c16 = 0; c16 < 8; ++c16) *reinterpret_cast<uint4*>(vrow + hb * kKVSub + c16 * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        // P row r into tensor memory over the scores it came from: 64 columns of element
+        // pairs (keys 2c, 2c + 1 in column c), a quarter (16 columns) at a time
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = q4 * 32 + 2 * i;
+            const float p0 = ex2_approx(fmaf(x[c], p.sl2, neg_mu));
+            const float p1 = ex2_approx(fmaf(x[c + 1], p.sl2, neg_mu));
+            ls[i & 3] += p0 + p1;
+            w[i] = __uint_as_float(pack2(p0, p1, F16));
+          }
+          tmem_st16(s_taddr + q4 * 16, w);
+          tc_wait_st();  // this quarter of P (and a rescaled O) in tensor memory before its PV steps
+          tc_fence_before();
+          mbar_arrive(p_ready(g, q4));
+        }
+        l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       }
-      // warp-uniform: every lane waits, the warp gives up together. S_j ready also means
-      // that this slot's PV_{j-1} is done: O is stable and the P buffer free
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full(g), j & 1, budget, abort_flag))) {
+      if (failed) break;
+      // the slot's last PV of this item is complete (every item commits, with tiles or not)
+      if (!__all_sync(0xffffffffu, mbar_wait(o_done(g), k & 1, budget, abort_flag))) {
         failed = true;
         break;
       }
       __syncwarp();
       tc_fence_after();
-      float x[kBK];
-#pragma unroll
-      for (int c = 0; c < kBK; c += 16) tmem_ld16(s_taddr + c, *reinterpret_cast<float(*)[16]>(&x[c]));
-      tc_wait_ld();
-      const int n0 = (t0 + j) * kBK;
-      // raw scores: masked entries become -inf (tiles on the diagonal, past the last key,
-      // before the first visible key, or before the window)
-      if ((n0 + kBK - 1 > off + m0) || (n0 + kBK > kv_hi) || n0 < kv_lo ||
-          (p.window > 0 && n0 < off + min(m0 + kBQ - 1, p.T - 1) - p.window + 1)) {
-        const int causal = off + qc - n0;                    // keys n0 + c with c <= causal are not ahead
-        const int lim = min(causal, kv_hi - 1 - n0);         // ... nor padding after the run
-        const int first = max(p.window > 0 ? causal - p.window + 1 : -kBK, kv_lo - n0);  // c >= first
-#pragma unroll
-        for (int c = 0; c < kBK; ++c)
-          if (c > lim || c < first) x[c] = -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = x[i];
-#pragma unroll
-      for (int c = 8; c < kBK; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
-      const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float mt = mraw * p.sl2;  // the scale is positive: the max commutes with it
-      const bool need = mt > m_ref + kRescaleLog2;
-      const bool any = __any_sync(0xffffffffu, need);
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2_approx(m_ref - mt);
-        m_ref = mt;
-      }
-      const float neg_mu = m_ref == -INFINITY ? 0.f : -m_ref;
-      if (j >= 1 && any) {  // PV_{j-1} is done (see above): rescale this warp's O rows
-#pragma unroll 1
-        for (int c = 0; c < kD; c += 16) {
-          float ov[16];
-          tmem_ld16(o_taddr + c, ov);
-          tc_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) ov[i] *= alpha;
-          tmem_st16(o_taddr + c, ov);
-        }
-      }
-      if (n0 + kBK > n_keys) {
-        // V rows past the item's last key may hold anything (unused cache slots): zero them,
-        // so that P = 0 meets finite values, once the tile has landed. Both slots write the
-        // same zeros, each before its own p_ready (the fence below), as either slot's PV
-        // may run first
-        const int vs = j % kVStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(v_full(vs), (j / kVStages) & 1, budget, abort_flag))) {
-          failed = true;
-          break;
-        }
-        if (r >= n_keys - n0) {
-          uint8_t* vrow = sV + vs * kKVBytes + r * 128;
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-            for (int c16 = 0; c16 < 8; ++c16) *reinterpret_cast<uint4*>(vrow + hb * kKVSub + c16 * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-      }
-      // P row r into tensor memory over the scores it came from: 64 columns of element
-      // pairs (keys 2c, 2c + 1 in column c), written 16 columns at a time
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = q4 * 32 + 2 * i;
-          const float p0 = ex2_approx(fmaf(x[c], p.sl2, neg_mu));
-          const float p1 = ex2_approx(fmaf(x[c + 1], p.sl2, neg_mu));
-          ls[i & 3] += p0 + p1;
-          w[i] = __uint_as_float(pack2(p0, p1, F16));
-        }
-        tmem_st16(s_taddr + q4 * 16, w);
-        tc_wait_st();  // this quarter of P (and a rescaled O) in tensor memory before its PV steps
-        tc_fence_before();
-        mbar_arrive(p_ready(g, q4));
-      }
-      l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-    }
-    if (!failed && n_tiles > 0) {
-      if (!__all_sync(0xffffffffu, mbar_wait(o_done(g), 0, budget, abort_flag))) failed = true;
-    }
-    if (!failed) {
-      __syncwarp();
-      tc_fence_after();
       const bool seen = l > 0.f;  // false: a padding query that sees no key (its output is 0)
       const float inv = seen ? 1.f / l : 0.f;
-      const size_t orow_i = (((size_t)b * p.T + qi) * p.H + me.h) * kD;
+      const size_t orow_i = (((size_t)it.b * p.T + qi) * p.H + me.h) * kD;
       uint16_t* orow = static_cast<uint16_t*>(p.o) + orow_i;
       const bool of16 = p.o_f16 != 0;
       const bool store = me.valid && qi < p.T;
@@ -513,7 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           reinterpret_cast<uint4*>(orow + c)[1] = w1;
         }
       }
-    } else {
+      tc_fence_before();
+      mbar_arrive(o_free(g));  // O is read out: the next item's first PV may overwrite it
+    }
+    if (failed) {
       *abort_flag = 1;
       if (lane == 0) report_timeout(p.status, 0x20 + 2);
     }
@@ -527,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   if (*abort_flag) {
     volatile int never = 0;
     if (warp == 0 && lane == 0) {
-      mbar_wait(q_full, 0, kDrainNs, &never);
+      if (q_issued) mbar_wait(q_full, q_parity, kDrainNs, &never);
       for (int s = 0; s < kKStages; ++s)
         if (issued & (1u << s)) mbar_wait(k_full(s), (parity >> s) & 1, kDrainNs, &never);
     } else if (warp == 0 && lane == 1) {
@@ -594,10 +674,16 @@ cudaError_t launch_attn_prefill_tc(const void* q, const void* k, const void* v, 
   cudaError_t ce = f16 ? set_smem_limit_once(reinterpret_cast<const void*>(attn_tc_kernel<true>), kSmem, configured[1])
                        : set_smem_limit_once(reinterpret_cast<const void*>(attn_tc_kernel<false>), kSmem, configured[0]);
   if (ce != cudaSuccess) return ce;
+  // persistent: one CTA per SM (at most one per item) walks the items
+  int dev = 0, sms = 0;
+  ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return ce;
+  const int grid = std::min(p.n_items, sms);
   if (f16)
-    launch_pdl(attn_tc_kernel<true>, p.n_items, kThreads, kSmem, s, p);
+    launch_pdl(attn_tc_kernel<true>, grid, kThreads, kSmem, s, p);
   else
-    launch_pdl(attn_tc_kernel<false>, p.n_items, kThreads, kSmem, s, p);
+    launch_pdl(attn_tc_kernel<false>, grid, kThreads, kSmem, s, p);
   return cudaGetLastError();
 }
 
