@@ -243,6 +243,59 @@ __device__ __forceinline__ float expm1_nonpos(float x) {
   return x > -0.0625f ? taylor : e2 - 1.0f;
 }
 
+// 32 values of a residual row from the element at off (fp32 or bf16 stream), zero where
+// n_valid (the row's valid columns from off) runs out or there is no residual.
+__device__ __forceinline__ void load_resid32(const TcEpiArgs& e, size_t off, int n_valid, float (&rr)[32]) {
+  if (!e.resid || n_valid <= 0) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) rr[j] = 0.f;
+  } else if (e.resid_f32) {
+    const float* rf = reinterpret_cast<const float*>(e.resid) + off;
+    if (n_valid >= 32) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 f4 = reinterpret_cast<const float4*>(rf)[j];
+        rr[4 * j] = f4.x;
+        rr[4 * j + 1] = f4.y;
+        rr[4 * j + 2] = f4.z;
+        rr[4 * j + 3] = f4.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) rr[j] = j < n_valid ? rf[j] : 0.f;
+    }
+  } else {
+    const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(e.resid) + off;
+    if (n_valid >= 32) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 u = reinterpret_cast<const uint4*>(rb)[j];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f2 = unpack_bf16x2(w[i]);
+          rr[8 * j + 2 * i] = f2.x;
+          rr[8 * j + 2 * i + 1] = f2.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) rr[j] = j < n_valid ? __bfloat162float(rb[j]) : 0.f;
+    }
+  }
+}
+
+// Pulls a residual row segment [off, off + n) into L2 ahead of the epilogue that reads it.
+__device__ __forceinline__ void prefetch_resid_l2(const TcEpiArgs& e, size_t off, int n) {
+  if (!e.resid || n <= 0) return;
+  const int es = e.resid_f32 ? 4 : 2;
+  const char* base = reinterpret_cast<const char*>(e.resid) + off * es;
+  const char* end = base + (size_t)n * es;
+  for (const char* a = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(base) & ~uintptr_t(127)); a < end;
+       a += 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
 // Per-row RMSNorm factor rsqrt(mean(row^2) + eps) from an accumulated sum of squares.
 // The partial sums of a row (one per producer tile) are added in a fixed order: deterministic.
 __device__ __forceinline__ float row_norm_factor(const TcEpiArgs& e, int row, bool row_ok) {
@@ -476,20 +529,28 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
       const int col0 = p.b_out[un.b_seg] + un.b_row0;
       const int n_valid = p.b_rows[un.b_seg] - un.b_row0;
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(e.out) + (size_t)row * e.ldo + col0;
-      const __nv_bfloat16* res = nullptr;
       __nv_bfloat16* tap = nullptr;
       float r2 = 1.0f, ss_part = 0.f;
       if constexpr (EPI == (int)Epi::kResid) {
-        if (e.resid) res = reinterpret_cast<const __nv_bfloat16*>(e.resid) + (size_t)row * e.ldo + col0;
         if (e.tap) tap = reinterpret_cast<__nv_bfloat16*>(e.tap) + (size_t)row * e.ldo + col0;
       } else if constexpr (EPI == (int)Epi::kRelu2 || EPI == (int)Epi::kXielu) {
         r2 = row_norm_factor(e, row, row_ok);  // the post-attention RMSNorm's 1/rms
       }
+      // kResid: the residual of the next 32 columns is loaded while this chunk is stored
+      const size_t roff = (size_t)row * e.ldo + col0;
+      float rnext[32];
+      if constexpr (EPI == (int)Epi::kResid) load_resid32(e, roff, row_ok ? n_valid : 0, rnext);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         float v[32];
         tmem_ld16(taddr + c0, *reinterpret_cast<float(*)[16]>(&v[0]));
         tmem_ld16(taddr + c0 + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
+        float rcur[32];
+        if constexpr (EPI == (int)Epi::kResid) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) rcur[j] = rnext[j];
+          if (c0 + 32 < BN) load_resid32(e, roff + c0 + 32, row_ok ? n_valid - c0 - 32 : 0, rnext);
+        }
         tc_wait_ld();
         if (!row_ok || c0 >= n_valid) continue;
 #pragma unroll
@@ -513,39 +574,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
             });
           } else if constexpr (EPI == (int)Epi::kResid) {
             // residual stream carried in fp32: out = resid + acc, rounded once
-            float rr[16];
-            if (!e.resid) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) rr[j] = 0.f;
-            } else if (e.resid_f32) {
-              const float* rf = reinterpret_cast<const float*>(e.resid) + (size_t)row * e.ldo + col0 + cc;
-              if (nv == 16) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const float4 f4 = reinterpret_cast<const float4*>(rf)[j];
-                  rr[4 * j] = f4.x;
-                  rr[4 * j + 1] = f4.y;
-                  rr[4 * j + 2] = f4.z;
-                  rr[4 * j + 3] = f4.w;
-                }
-              } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) rr[j] = j < nv ? rf[j] : 0.f;
-              }
-            } else if (nv == 16) {
-              const uint4 ra = reinterpret_cast<const uint4*>(res + cc)[0];
-              const uint4 rb = reinterpret_cast<const uint4*>(res + cc)[1];
-              const uint32_t w[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float2 f2 = unpack_bf16x2(w[j]);
-                rr[2 * j] = f2.x;
-                rr[2 * j + 1] = f2.y;
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) rr[j] = j < nv ? __bfloat162float(res[cc + j]) : 0.f;
-            }
+            const float* rr = &rcur[16 * h];
             float o[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) o[j] = rr[j] + vv[j];
@@ -1230,6 +1259,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         // this CTA has read every split's buffer acc: release them for tile it + 2
         if (tid < p.k_splits) mbar_arrive_cluster(map_shared_rank(pbfree_bar(acc), (uint32_t)tid));
       } else {
+        if constexpr (EPI == (int)Epi::kResid) {  // this row's residual into L2 while the MMAs run
+          const int row = un.m_tile * kBM + quarter * 32 + lane;
+          if (row < p.a_rows[0])
+            prefetch_resid_l2(p.e, (size_t)row * p.e.ldo + p.b_out[un.b_seg] + un.b_row0,
+                              min(BN, p.b_rows[un.b_seg] - un.b_row0));
+        }
         // warp-uniform: every lane waits, the warp gives up together
         if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, budget, abort_flag))) {
           failed = true;
