@@ -2,7 +2,7 @@
 // softmax(q @ k.T / sqrt(128)) @ v, per head; "arcee", "Grouped-query
 // attention, 128-wide heads": query head h reads KV head h / (H / Hkv)).
 // HBM-bound: a persistent kernel whose producer warp streams K/V tiles of 64
-// keys through a 4-stage TMA ring (128-byte swizzle); the small products run
+// keys through a 6-stage TMA ring (128-byte swizzle); the small products run
 // on bf16 mma.sync with fp32 accumulation and an online softmax (running max
 // and sum in the log2 domain).
 //
@@ -50,7 +50,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 
 // ------------------------------------------------------------------ decode
 
-constexpr int kStages = 4;                       // TMA ring depth (tiles of 64 keys)
+constexpr int kStages = 6;                       // TMA ring depth (tiles of 64 keys)
 constexpr int kHalfBytes = kTileKeys * 128;      // one 64-column half of a 64-key tile (8 KB)
 constexpr int kStageBytes = 4 * kHalfBytes;      // K and V, two halves each (32 KB)
 constexpr int kCompute = 4;                      // compute warps; warp 4 is the TMA producer
@@ -103,7 +103,7 @@ __device__ __forceinline__ DecodeUnit decode_unit(const DecodeParams& p, int u) 
 // Persistent split-KV decode attention: each CTA starts on unit blockIdx.x (a
 // sequence, a KV head, a key split) and takes its next ones from a shared
 // counter, so that CTAs the memory system serves faster take more; its producer
-// lane streams every unit's K/V tiles through a 4-stage TMA ring without pausing
+// lane streams every unit's K/V tiles through a 6-stage TMA ring without pausing
 // between units and hands the unit indices to the 4 compute warps (a queue of
 // kUq, mbarriers both ways), which each own 16 keys of every tile.
 __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
