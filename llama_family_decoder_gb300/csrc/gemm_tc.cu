@@ -10,6 +10,12 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
 //               fused post-processing, stores to global memory.
 // The two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// A CTA pair (cluster of 2, tcgen05 cta_group::2) computes a 256 x BN tile: each
+// CTA loads its 128 A rows and half of the B tile, the even CTA issues the MMAs for
+// both. The prefill GEMMs walk their tiles in bands of M tiles (all N tiles of a band
+// before the next), so that a band's A rows stay in L2 while the B panels stream.
+// The decode GEMMs put the weights on the MMA's M side, split K over the CTAs of a
+// cluster and finish each tile inside the cluster (distributed shared memory).
 //
 // Fused epilogues cover the projections of the decoder block ("LlamaForCausalLM-
 // 32L-4096d" sheet, "Implementing it"): per-head q/k RMSNorm + RoPE + scatter
