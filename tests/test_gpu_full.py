@@ -82,3 +82,35 @@ def test_prefill_full_size_every_row():
     print(f"llama7b every row: max {e.max():.4f}, 99.99th pct {np.quantile(e, 0.9999):.4f}, "
           f"bf16 floor {bf16_floor(ref):.4f}")
     assert e.max() <= TOL["bf16"]
+
+
+def test_full_size_runs_are_bitwise_repeatable():
+    """Every reduction on the path has a fixed order (split partials summed in split order,
+    per-tile sums of squares in tile order, persistent work lists whose per-unit results do
+    not depend on the CTA that computes them), so two runs of the same step agree to the bit:
+    the Apertus-shape prefill (CTA pairs, persistent attention) and the decode step (units
+    taken from an atomic counter, splits combined afterwards)."""
+    wl = WORKLOADS["apertus_qknorm_bf16_B2_T4096"]
+    x = make_input(wl).cuda()
+    blk = DecoderBlock.from_workload(wl)
+    wd = blk.prepare({k: v.cuda() for k, v in make_weights(wl).items()})
+    first = blk.forward(x, wd)
+    second = blk.forward(x, wd)
+    torch.cuda.synchronize()
+    assert blk.last_status() == 0
+    assert torch.equal(first, second)
+    del blk, wd, first, second, x
+
+    wl = WORKLOADS["llama7b_decode_bf16_B64_L4096"]
+    x = make_input(wl)[:, 0][:, None].cuda()
+    kc, vc = make_kv_cache(wl)
+    kd, vd = kc.cuda(), vc.cuda()
+    blk = DecoderBlock.from_workload(wl)
+    wd = blk.prepare({k: v.cuda() for k, v in make_weights(wl).items()})
+    outs = []
+    for _ in range(2):
+        lens = torch.full((wl.batch,), wl.cache_len, dtype=torch.int32, device="cuda")  # the same slot each time
+        outs.append(blk.forward(x, wd, cache={"k": kd, "v": vd, "lens": lens}, host_lens_max=wl.cache_len))
+    torch.cuda.synchronize()
+    assert blk.last_status() == 0
+    assert torch.equal(outs[0], outs[1])
