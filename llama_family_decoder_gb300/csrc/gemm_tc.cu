@@ -72,7 +72,10 @@ struct TcCfg {
   static constexpr int kBarBytes = 256;
   // kDecAct: two partial-tile buffers [BN tokens][128 rows] fp32 and the 1/rms of up to BN tokens
   static constexpr int kPartBytes = BN * kBM * 4;
-  static constexpr int kExtraBytes = EPI == (int)Epi::kDecAct ? 2 * kPartBytes + 4 * BN : 0;
+  // kResidTma: two 4 KB staging buffers (32 rows x 32 fp32 columns) per epilogue warp
+  static constexpr int kStoreBytes = 4 * 2 * 4096;
+  static constexpr int kExtraBytes =
+      EPI == (int)Epi::kDecAct ? 2 * kPartBytes + 4 * BN : (EPI == (int)Epi::kResidTma ? kStoreBytes : 0);
   static constexpr int kFit = (kMaxSmem - 1024 - kBarBytes - kExtraBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;  // as deep a TMA ring as fits
   static constexpr int kTmemCols = pow2_at_least(2 * BN);  // two accumulators
@@ -80,6 +83,12 @@ struct TcCfg {
   static_assert(BN % 16 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory");
 };
+
+// the residual epilogues: kResid, and kResidTma (its fp32 output through TMA stores)
+template <int EPI>
+__host__ __device__ constexpr bool is_resid() {
+  return EPI == (int)Epi::kResid || EPI == (int)Epi::kResidTma;
+}
 
 template <int EPI>
 __host__ __device__ constexpr bool is_dec_epi() {
@@ -107,6 +116,7 @@ __host__ __device__ constexpr bool tc_supported() {
 struct TcParams {
   CUtensorMap ta[kMaxSegs];
   CUtensorMap tb[kMaxSegs];
+  CUtensorMap tout;  // kResidTma: the fp32 output [rows, ldo], boxes of 32 x 32, 128-byte swizzle
   int a_tiles[kMaxSegs + 1];  // prefix sums of m-tiles per A segment
   int a_rows[kMaxSegs];
   int a_out[kMaxSegs];
@@ -312,9 +322,23 @@ __device__ __forceinline__ float row_norm_factor(const TcEpiArgs& e, int row, bo
   return rsqrtf(t / (float)e.ss_n + e.ss_eps);
 }
 
+// kResid, after a row of a tile is stored: its sum of squares for the next RMSNorm, and a
+// prefill chunk's length bump (once per sequence).
+template <int BN>
+__device__ __forceinline__ void resid_row_done(const TcParams& p, const Unit& un, int row, bool row_ok,
+                                               float ss_part) {
+  const TcEpiArgs& e = p.e;
+  if (e.norm_ss && row_ok) e.norm_ss[(size_t)row * e.norm_parts + un.b_row0 / BN] = ss_part;
+  // a prefill chunk appended to a KV cache: its sequence's length grows by seq, once
+  if (e.bump_lens && row_ok && un.b_row0 == 0 && un.b_seg == 0 && row % e.seq == e.seq - 1)
+    atomicAdd(e.bump_lens + row / e.seq, e.seq);
+}
+
+// stage: the decode finishers' partial tile, or (kResidTma) this warp's staging buffers;
+// store_chunks (kResidTma): the warp's count of chunks stored so far (its buffer parity).
 template <int BN, int EPI>
 __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, uint32_t taddr, int r_in_tile,
-                                             float* stage) {
+                                             float* stage, int* store_chunks = nullptr) {
   const TcEpiArgs& e = p.e;
   if constexpr (is_cluster_epi<EPI>()) {
     // decode finishers: this split's partial tile [token in tile][128 tile rows] in shared memory
@@ -530,6 +554,104 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
           store_bf16_row(out + c0, v, min(16, n_valid - c0), id);
         }
       }
+      return;
+    } else if constexpr (EPI == (int)Epi::kResidTma) {
+      // kResid whose fp32 output goes through shared memory: each 32-column chunk of the
+      // warp's 32 rows is written into one of the warp's two 4 KB staging buffers (the
+      // 128-byte swizzle the output's tensor map uses: 16-byte chunk q of row r at q ^ (r % 8)),
+      // and one lane stores the 32 x 32 box with a bulk tensor copy, so the residual stream
+      // leaves the SM as whole lines. Rows past the output and columns past its width are
+      // clipped by the tensor map. The fp16 normed rows, the taps and the row's sum of
+      // squares are stored as in kResid.
+      const int lane = r_in_tile & 31;
+      const int row0 = un.m_tile * kBM + (r_in_tile & ~31);  // the warp's first row
+      const int col0 = p.b_out[un.b_seg] + un.b_row0;
+      const int n_valid = p.b_rows[un.b_seg] - un.b_row0;
+      __nv_bfloat16* tap = (e.tap && row_ok) ? reinterpret_cast<__nv_bfloat16*>(e.tap) + (size_t)row * e.ldo + col0
+                                             : nullptr;
+      const uint32_t sbase = smem_u32(stage);
+      auto id = [](float x, int) { return x; };
+      float ss_part = 0.f;
+      const size_t roff = (size_t)row * e.ldo + col0;
+      float rnext[32];
+      load_resid32(e, roff, row_ok ? n_valid : 0, rnext);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tmem_ld16(taddr + c0, *reinterpret_cast<float(*)[16]>(&v[0]));
+        tmem_ld16(taddr + c0 + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
+        float rcur[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) rcur[j] = rnext[j];
+        if (c0 + 32 < BN) load_resid32(e, roff + c0 + 32, row_ok ? n_valid - c0 - 32 : 0, rnext);
+        tc_wait_ld();
+        if (c0 >= n_valid) continue;  // uniform across the warp
+        float o[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = rcur[j] + v[j];
+        // this chunk's buffer is free once the store issued two chunks back has read it
+        const uint32_t buf = sbase + (static_cast<uint32_t>(*store_chunks & 1) << 12);
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st_shared_f4(buf + lane * 128 + ((q ^ (lane & 7)) << 4), o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        fence_proxy_async_smem();  // the generic-proxy writes, before the bulk copy reads them
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&p.tout, buf, col0 + c0, row0);
+          bulk_commit_group();
+        }
+        ++*store_chunks;
+        if (!row_ok) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int cc = c0 + 16 * h;
+          if (cc >= n_valid) break;
+          const int nv = min(16, n_valid - cc);
+          const float* oo = &o[16 * h];
+          if (tap) store_bf16_row(tap + cc, &v[16 * h], nv, id);
+          if (e.out2)
+            store_bf16_row(reinterpret_cast<__nv_bfloat16*>(e.out2) + (size_t)row * e.ldo + col0 + cc, oo, nv, id);
+          if (e.norm_out) {
+            // next RMSNorm, split: its gain here (the next GEMM's A), its 1/rms from the
+            // row's sum of squares, applied in that GEMM's epilogue
+            const __nv_bfloat16* gn = reinterpret_cast<const __nv_bfloat16*>(e.norm_gain) + col0 + cc;
+            uint16_t* nd = reinterpret_cast<uint16_t*>(e.norm_out) + (size_t)row * e.ldo + col0 + cc;
+            float og[16];
+            if (nv == 16) {
+              uint4 g2[2];
+              g2[0] = reinterpret_cast<const uint4*>(gn)[0];
+              g2[1] = reinterpret_cast<const uint4*>(gn)[1];
+              const uint32_t* gw = reinterpret_cast<const uint32_t*>(g2);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float2 gf = unpack_bf16x2(gw[j]);
+                ss_part += oo[2 * j] * oo[2 * j] + oo[2 * j + 1] * oo[2 * j + 1];
+                og[2 * j] = oo[2 * j] * gf.x;
+                og[2 * j + 1] = oo[2 * j + 1] * gf.y;
+              }
+              store16_2b(nd, og, e.norm_f16 != 0);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (j < nv) {
+                  ss_part += oo[j] * oo[j];
+                  const float g = oo[j] * __bfloat162float(gn[j]);
+                  if (e.norm_f16) {
+                    const __half hv = __float2half_rn(g);
+                    nd[j] = *reinterpret_cast<const uint16_t*>(&hv);
+                  } else {
+                    const __nv_bfloat16 bv = __float2bfloat16_rn(g);
+                    nd[j] = *reinterpret_cast<const uint16_t*>(&bv);
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+      resid_row_done<BN>(p, un, row, row_ok, ss_part);
       return;
     } else {
       const int col0 = p.b_out[un.b_seg] + un.b_row0;
@@ -1228,6 +1350,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
     int it = 0;
     bool failed = false;
+    int store_chunks = 0;  // kResidTma: bulk stores issued by this warp
     for (int u = u0; u < p.num_units; u += ustep, ++it) {
       const Unit un = PAIR ? pair_unit(p, u, bn_rows, prank) : decode_unit<kGrp>(p, u, bn_rows);
       const int acc = it & 1;
@@ -1265,7 +1388,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         // this CTA has read every split's buffer acc: release them for tile it + 2
         if (tid < p.k_splits) mbar_arrive_cluster(map_shared_rank(pbfree_bar(acc), (uint32_t)tid));
       } else {
-        if constexpr (EPI == (int)Epi::kResid) {  // this row's residual into L2 while the MMAs run
+        if constexpr (is_resid<EPI>()) {  // this row's residual into L2 while the MMAs run
           const int row = un.m_tile * kBM + quarter * 32 + lane;
           if (row < p.a_rows[0])
             prefetch_resid_l2(p.e, (size_t)row * p.e.ldo + p.b_out[un.b_seg] + un.b_row0,
@@ -1278,7 +1401,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         }
         __syncwarp();
         tc_fence_after();
-        run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane, reinterpret_cast<float*>(smem));
+        if constexpr (EPI == (int)Epi::kResidTma)
+          run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane, pb + (warp - 2) * 2048, &store_chunks);
+        else
+          run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane, reinterpret_cast<float*>(smem));
         tc_fence_before();
         if constexpr (PAIR) {  // one lane a warp, on the even CTA's barrier
           __syncwarp();
@@ -1291,6 +1417,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     if (failed) {
       *abort_flag = 1;
       if (lane == 0) report_timeout(p.status, 0x10 + 2);
+    }
+    if constexpr (EPI == (int)Epi::kResidTma) {
+      // every bulk store of the warp complete (its shared-memory reads and its global writes)
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
     }
   }
 
@@ -1467,7 +1598,7 @@ int max_clusters(int splits) {
 template <int BN, int EPI>
 constexpr bool tc_pair_supported() {
   if (EPI == (int)Epi::kQkv) return BN == 256;  // whole heads
-  if (EPI == (int)Epi::kResid || EPI == (int)Epi::kSwiglu || EPI == (int)Epi::kRelu2 || EPI == (int)Epi::kXielu ||
+  if (is_resid<EPI>() || EPI == (int)Epi::kSwiglu || EPI == (int)Epi::kRelu2 || EPI == (int)Epi::kXielu ||
       EPI == (int)Epi::kStore)
     return BN == 192 || BN == 224 || BN == 256;
   return false;
@@ -1492,6 +1623,7 @@ cudaError_t dispatch_epi(const TcParams& p, Epi epi, bool pair, int grid, cudaSt
   switch (epi) {
     case Epi::kStore: return launch_if<BN, (int)Epi::kStore>(p, pair, grid, s);
     case Epi::kResid: return launch_if<BN, (int)Epi::kResid>(p, pair, grid, s);
+    case Epi::kResidTma: return launch_if<BN, (int)Epi::kResidTma>(p, pair, grid, s);
     case Epi::kQkv: return launch_if<BN, (int)Epi::kQkv>(p, pair, grid, s);
     case Epi::kSwiglu: return launch_if<BN, (int)Epi::kSwiglu>(p, pair, grid, s);
     case Epi::kRelu2: return launch_if<BN, (int)Epi::kRelu2>(p, pair, grid, s);
@@ -1610,6 +1742,25 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
     if (d.nb != 1 || d.b_paired || d.e.n_tok != d.b[0].rows || p.k_splits > 8 || p.num_units > max_ctas ||
         tc_dec_max_clusters(d.bn, d.epi, p.k_splits) < p.m_tiles * p.n_tiles) {
       *why = "tcgen05 GEMM: a decode finisher needs one unit per CTA and every cluster of K splits resident";
+      return cudaErrorInvalidValue;
+    }
+  }
+  if (d.epi == Epi::kResidTma) {
+    // the fp32 output [rows, ldo] as a tensor of 32 x 32 boxes: one B segment covering its columns
+    auto fn = encode_fn();
+    if (d.nb != 1 || d.b_paired || d.na != 1 || !d.e.out_f32 || !d.e.out || d.b[0].out_offset != 0 ||
+        d.b[0].rows != d.e.ldo || d.e.ldo % 4 != 0 || (reinterpret_cast<uintptr_t>(d.e.out) & 15) || !fn) {
+      *why = "tcgen05 GEMM: a TMA-stored residual output is fp32, one B segment as wide as the output";
+      return cudaErrorInvalidValue;
+    }
+    cuuint64_t dims[2] = {(cuuint64_t)d.e.ldo, (cuuint64_t)d.a[0].rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d.e.ldo * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn(&p.tout, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, d.e.out, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      *why = "cuTensorMapEncodeTiled failed for the residual output";
       return cudaErrorInvalidValue;
     }
   }

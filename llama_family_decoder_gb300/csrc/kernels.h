@@ -71,6 +71,9 @@ enum class Epi : int {
   // (64 gate rows over 64 up rows) out = bf16(silu(gate * rs) * (up * rs)), else
   // relu^2 or xIELU of up * rs; rs = the MLP input's 1/rms (row_ss), or 1.
   kDecAct = 9,
+  // kResid with an fp32 output written through shared memory by TMA bulk tensor stores
+  // (one B segment covering the output's columns): the o_proj of the prefill block
+  kResidTma = 10,
 };
 
 // How many clusters of `splits` CTAs of the decode GEMM kernel (tile width bn,
