@@ -21,6 +21,8 @@ SMALL_BF16 = [
     Workload("small_relu2_gqa", "bf16", 1, 320, 1024, 8, 2, 128, 1536, "relu2", seed=12),
     Workload("small_xielu_qknorm", "bf16", 3, 130, 512, 4, 1, 128, 776, "xielu", qk_norm=True, seed=13),
     Workload("small_swiglu_gqa_qknorm", "bf16", 1, 64, 256, 4, 2, 128, 512, "silu", qk_norm=True, seed=14),
+    # hidden not a multiple of 32: the o_proj's last N tile and its last 32-column output box are ragged
+    Workload("small_relu2_odd_hidden", "bf16", 2, 150, 1000, 4, 2, 128, 1000, "relu2", seed=16),
     # enough tiles x k-blocks that every GEMM splits tiles across CTAs (stream-K)
     Workload("medium_streamk_swiglu", "bf16", 2, 600, 2048, 16, 4, 128, 2000, "silu", seed=15),
 ]
