@@ -338,7 +338,7 @@ blk_status bf16_linear_resid(const blk_handle* h, const void* a, int rows, int K
   g.pair = tr.pair;
   // o_proj (the fp32 residual stream plus the next norm's rows) stores its fp32 output
   // through shared memory with TMA; the others store from registers
-  g.epi = (out_f32 && norm_out) ? Epi::kResidTma : Epi::kResid;
+  g.epi = out_f32 ? Epi::kResidTma : Epi::kResid;
   g.const_op = 2;
   g.e.out = out;
   g.e.ldo = N;
