@@ -64,6 +64,13 @@ constexpr int pow2_at_least(int x) {
   return p;
 }
 
+// SwiGLU tiles 256 wide (a 128-column bf16 output) store through shared memory and TMA:
+// their ring keeps its depth with the 8 KB of staging, narrower ones would lose a stage
+template <int BN, int EPI>
+__host__ __device__ constexpr bool swiglu_tma() {
+  return EPI == (int)Epi::kSwiglu && BN == 256;
+}
+
 template <int BN, int EPI = -1, bool PAIR = false>
 struct TcCfg {
   static constexpr int kABytes = kBM * kBK * 2;
@@ -74,8 +81,11 @@ struct TcCfg {
   static constexpr int kPartBytes = BN * kBM * 4;
   // kResidTma: two 4 KB staging buffers (32 rows x 32 fp32 columns) per epilogue warp
   static constexpr int kStoreBytes = 4 * 2 * 4096;
-  static constexpr int kExtraBytes =
-      EPI == (int)Epi::kDecAct ? 2 * kPartBytes + 4 * BN : (EPI == (int)Epi::kResidTma ? kStoreBytes : 0);
+  // 256-wide SwiGLU: one staging box of 32 rows x 32 bf16 columns (2 KB) per epilogue warp
+  static constexpr int kExtraBytes = EPI == (int)Epi::kDecAct
+                                         ? 2 * kPartBytes + 4 * BN
+                                         : (EPI == (int)Epi::kResidTma ? kStoreBytes
+                                                                        : (swiglu_tma<BN, EPI>() ? 4 * 2048 : 0));
   static constexpr int kFit = (kMaxSmem - 1024 - kBarBytes - kExtraBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;  // as deep a TMA ring as fits
   static constexpr int kTmemCols = pow2_at_least(2 * BN);  // two accumulators
@@ -540,6 +550,42 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, const Unit& un, 
       const int n_valid = p.b_rows[0] - col0;
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(e.out) + (size_t)row * e.ldo + col0;
       const float r2 = row_norm_factor(e, row, row_ok);  // the post-attention RMSNorm's 1/rms
+      if constexpr (swiglu_tma<BN, EPI>()) {
+        // the 128 output columns leave through shared memory: each 32-column chunk of the
+        // warp's 32 rows goes into its 2 KB staging box in the output map's 64-byte swizzle
+        // (16-byte chunk q of row r at q ^ ((r / 2) % 4)) and one lane stores the box with a
+        // bulk tensor copy; rows past the output and columns past its width are clipped
+        const int lane = r_in_tile & 31;
+        const int row0 = un.m_tile * kBM + (r_in_tile & ~31);  // the warp's first row
+        const uint32_t buf = smem_u32(stage);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+          float g[32], u[32];
+          tmem_ld16(taddr + c0, *reinterpret_cast<float(*)[16]>(&g[0]));
+          tmem_ld16(taddr + c0 + 16, *reinterpret_cast<float(*)[16]>(&g[16]));
+          tmem_ld16(taddr + BN / 2 + c0, *reinterpret_cast<float(*)[16]>(&u[0]));
+          tmem_ld16(taddr + BN / 2 + c0 + 16, *reinterpret_cast<float(*)[16]>(&u[16]));
+          tc_wait_ld();
+          if (c0 >= n_valid) continue;  // uniform across the warp
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(silu_f(g[2 * i] * r2) * (u[2 * i] * r2), silu_f(g[2 * i + 1] * r2) * (u[2 * i + 1] * r2));
+          if (lane == 0) bulk_wait_group_read<0>();  // the previous box has left the buffer
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st_shared_u4(buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
+                         w[4 * q + 3]);
+          fence_proxy_async_smem();  // the generic-proxy writes, before the bulk copy reads them
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.tout, buf, col0 + c0, row0);
+            bulk_commit_group();
+          }
+        }
+        return;
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < BN / 2; c0 += 16) {
         float g[16], u[16];
@@ -1403,6 +1449,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         tc_fence_after();
         if constexpr (EPI == (int)Epi::kResidTma)
           run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane, pb + (warp - 2) * 2048, &store_chunks);
+        else if constexpr (swiglu_tma<BN, EPI>())
+          run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane, pb + (warp - 2) * 512);
         else
           run_epilogue<BN, EPI>(p, un, taddr, quarter * 32 + lane, reinterpret_cast<float*>(smem));
         tc_fence_before();
@@ -1418,7 +1466,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       *abort_flag = 1;
       if (lane == 0) report_timeout(p.status, 0x10 + 2);
     }
-    if constexpr (EPI == (int)Epi::kResidTma) {
+    if constexpr (EPI == (int)Epi::kResidTma || swiglu_tma<BN, EPI>()) {
       // every bulk store of the warp complete (its shared-memory reads and its global writes)
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
@@ -1761,6 +1809,25 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, int max_ctas, DevStatus* st, uns
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
       *why = "cuTensorMapEncodeTiled failed for the residual output";
+      return cudaErrorInvalidValue;
+    }
+  }
+  if (d.epi == Epi::kSwiglu && d.bn == 256) {
+    // the 256-wide SwiGLU's bf16 output [rows, ldo] as a tensor of 32 x 32 boxes
+    auto fn = encode_fn();
+    if (!d.b_paired || d.nb != 2 || d.na != 1 || !d.e.out || d.b[0].rows != d.e.ldo || d.e.ldo % 8 != 0 ||
+        (reinterpret_cast<uintptr_t>(d.e.out) & 15) || !fn) {
+      *why = "tcgen05 GEMM: a SwiGLU output is paired gate/up segments as wide as the output";
+      return cudaErrorInvalidValue;
+    }
+    cuuint64_t dims[2] = {(cuuint64_t)d.e.ldo, (cuuint64_t)d.a[0].rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d.e.ldo * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn(&p.tout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d.e.out, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      *why = "cuTensorMapEncodeTiled failed for the SwiGLU output";
       return cudaErrorInvalidValue;
     }
   }
