@@ -464,14 +464,19 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
 
 }  // namespace
 
-// Splits of 512 keys (8 tiles), the last one up to twice that: units that the
-// persistent CTAs take in turn from a shared counter. (Smaller splits shorten the
-// last round but add each unit's fixed cost: q fragments, merge, partial writes.)
+// Splits of about 2048 keys (32 tiles), the last one up to twice that: units that the
+// persistent CTAs take in turn from a shared counter. Each unit pays a fixed cost (its q
+// fragments, the merge of the compute warps' softmax states, the partial writes and the
+// combine's reads of them), so long units win once the (sequence, KV head) pairs alone
+// give the SMs enough of them; with too few pairs to keep ~80% of the SMs busy the splits
+// shrink, down to 256 keys. (64 sequences x 8 KV heads x 4097 keys: splits of 512 keys
+// take 252 us a step, of 1024 to 2048 keys 244.5 us.)
 int attn_decode_splits(int B, int Hkv, int max_len, int num_sms) {
-  (void)B;
-  (void)Hkv;
-  (void)num_sms;
-  return attn_decode_split_cap(max_len);
+  const int groups = std::max(1, B * Hkv);
+  int s = std::max(1, max_len / 2048);
+  const int fill = (num_sms * 4 / 5 + groups - 1) / groups;
+  if (s < fill) s = std::min(fill, std::max(1, max_len / 256));
+  return std::min(s, 64);
 }
 
 int attn_decode_split_cap(int max_len) { return std::min(64, std::max(1, max_len / 512)); }
@@ -616,7 +621,7 @@ cudaError_t launch_attn_decode_bf16_static(const void* q, const void* k, const v
     *why = "cudaGetSymbolAddress of the decode scratch failed";
     return e;
   }
-  int splits = attn_decode_splits(B, Hkv, kv_stride, num_sms);
+  int splits = attn_decode_split_cap(kv_stride);  // splits of 512 keys, at most 64
   const int fit = (int)((kDecodeStaticScratchBytes - kAttnCounterBytes) / per_split);
   if (splits > fit) splits = fit;
   // The scratch's first kAttnCounterBytes hold the unit counter (byte 0) and this

@@ -251,8 +251,11 @@ cudaError_t launch_attn_decode_bf16(const void* q, const void* k, const void* v,
                                     int d, int kv_stride, const int* kv_lens, int len_add, int max_len,
                                     int split_cap, void* ws, int num_sms, DevStatus* st, unsigned long long wait_ns,
                                     cudaStream_t s, const char** why, const AttnOpts& opt = AttnOpts());
+// Key splits per (sequence, KV head) of a decode step: units of about 2048 keys, shorter
+// when B * Hkv pairs are too few to keep the SMs busy.
 int attn_decode_splits(int B, int Hkv, int max_len, int num_sms);
-// Most splits attn_decode_splits picks for keys up to max_len (size workspaces with it).
+// The splits a workspace holds for keys up to max_len (512-key units, at most 64): the
+// bound attn_decode_splits is clamped to, and the allocation-free path's split rule.
 int attn_decode_split_cap(int max_len);
 
 // Decode attention with its split partials in a fixed file-scope device array

@@ -53,7 +53,7 @@ def _oracle(q, k, v, lens, seqs):
 
 
 def _splits(B, H, cap):
-    """Splits of the workspace path (512-key units, at most 64) and of the fixed array."""
+    """Splits of this entry point: 512-key units (at most 64), then what the fixed array holds."""
     ws = min(64, max(1, cap // 512))
     fit = (SCRATCH - 256) // (B * H * (D + 2) * 4)
     return ws, min(ws, fit)
@@ -83,7 +83,9 @@ def _check(B, H, Hkv, cap, cases, seqs):
             print(f"B{B} H{H} cap {cap} seed {seed} sequence {b} ({lens[b]} keys): oracle {err:.4f} "
                   f"(bound {bound:.4f})")
             assert err <= bound, (seed, b, err, bound)
-        assert rel_err(got, np64(want)) <= TOL["bf16"], seed
+            # the workspace path (its own split count) against this one: both within the
+            # bound of the oracle, so within twice it of each other
+            assert rel_err(got[b, 0], np64(want[b, 0])) <= 2 * bound, (seed, b)
     blk.close()
 
 
@@ -103,7 +105,7 @@ def test_noalloc_many_splits_ragged_matches_oracle():
 
 
 def test_noalloc_split_count_capped_by_its_scratch():
-    # 64 x 32 heads x 8192 keys: the workspace path takes 16 splits, the fixed array
+    # 64 x 32 heads x 8192 keys: 512-key units would make 16 splits, the fixed array
     # holds 15 (64 * 32 * 130 * 4 bytes each); the chunks grow instead
     B, H, Hkv, cap = 64, 32, 8, 8192
     assert _splits(B, H, cap) == (16, 15)
