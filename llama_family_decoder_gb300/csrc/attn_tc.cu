@@ -95,6 +95,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Blackwell's packed fp32 arithmetic: two lanes of fp32 in one 64-bit register pair,
+// one instruction for both (each lane rounded as its scalar form would be).
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2_make(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max of three (one instruction; like fmaxf, a NaN operand is ignored)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
   if (f16) {
     __half2 h = __floats2half2_rn(lo, hi);
@@ -477,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = x[i];
 #pragma unroll
-        for (int c = 8; c < kBK; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+        for (int c = 8; c < kBK; c += 2) mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], x[c], x[c + 1]);
         const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float mt = mraw * p.sl2;  // the scale is positive: the max commutes with it
@@ -520,24 +548,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           fence_proxy_async_smem();
         }
         // P row r into tensor memory over the scores it came from: 64 columns of element
-        // pairs (keys 2c, 2c + 1 in column c), a quarter (16 columns) at a time
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // pairs (keys 2c, 2c + 1 in column c), a quarter (16 columns) at a time. Keys 2c and
+        // 2c + 1 go as one packed pair through the scale and shift and the row sum. A
+        // quarter is released to the PV steps once its store has landed, which the warp
+        // waits for only after computing the next quarter.
+        const f32x2 sl2x2 = f2_make(p.sl2, p.sl2), mu2 = f2_make(neg_mu, neg_mu);
+        f32x2 ls2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
+        float w[2][16];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          float w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int c = q4 * 32 + 2 * i;
-            const float p0 = ex2_approx(fmaf(x[c], p.sl2, neg_mu));
-            const float p1 = ex2_approx(fmaf(x[c + 1], p.sl2, neg_mu));
-            ls[i & 3] += p0 + p1;
-            w[i] = __uint_as_float(pack2(p0, p1, F16));
+            float t0, t1;
+            f2_split(f2_fma(f2_make(x[c], x[c + 1]), sl2x2, mu2), t0, t1);
+            const float p0 = ex2_approx(t0);
+            const float p1 = ex2_approx(t1);
+            ls2[i & 1] = f2_add(ls2[i & 1], f2_make(p0, p1));
+            w[q4 & 1][i] = __uint_as_float(pack2(p0, p1, F16));
           }
-          tmem_st16(s_taddr + q4 * 16, w);
-          tc_wait_st();  // this quarter of P (and a rescaled O) in tensor memory before its PV steps
-          tc_fence_before();
-          mbar_arrive(p_ready(g, q4));
+          if (q4 >= 1) {
+            tc_wait_st();  // quarter q4 - 1 of P (and a rescaled O) in tensor memory before its PV steps
+            tc_fence_before();
+            mbar_arrive(p_ready(g, q4 - 1));
+          }
+          tmem_st16(s_taddr + q4 * 16, w[q4 & 1]);
         }
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_ready(g, 3));
+        float ls[4];
+        f2_split(ls2[0], ls[0], ls[1]);
+        f2_split(ls2[1], ls[2], ls[3]);
         l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       }
       if (failed) break;
