@@ -214,6 +214,70 @@ def _padding_run_unshifted(mask_row):
     return 0, hi
 
 
+def _yarn_attention_factor_dropped(scaling):
+    return 1.0
+
+
+def _xielu_alpha_n_without_beta(raw_alpha_p, raw_alpha_n, beta=0.5):
+    return float(ob.softplus(raw_alpha_p)), float(ob.softplus(raw_alpha_n))
+
+
+def _xielu_raw_parameters(raw_alpha_p, raw_alpha_n, beta=0.5):
+    return float(raw_alpha_p), float(beta + raw_alpha_n)
+
+
+def _decode_factory(shift=0, own_key=True):
+    # decode_step with the new token's rotary position shifted, or without its own key
+    def decode_step(cfg, w, x, cache_k, cache_v, lens):
+        x = np.asarray(x, dtype=F64)
+        outs = []
+        for b in range(x.shape[0]):
+            L = int(lens[b])
+            pos = np.array([L + shift])
+            h = ob.rms_norm(x[b:b + 1], w["input_layernorm"], cfg.rms_norm_eps)
+            k_new, v_new = ob._project_kv(cfg, w, h, pos)
+            q = ob._project_q(cfg, w, h, pos)
+            k_all = np.asarray(cache_k[b, :, :L], dtype=F64)
+            v_all = np.asarray(cache_v[b, :, :L], dtype=F64)
+            if own_key:
+                k_all = np.concatenate([k_all, k_new], axis=1)
+                v_all = np.concatenate([v_all, v_new], axis=1)
+            heads = ob.causal_gqa_attention(q, k_all, v_all, np.array([L]), np.arange(k_all.shape[1]),
+                                            window=cfg.sliding_window)
+            taps = {key: val[0] for key, val in ob._finish_rows(cfg, w, x[b:b + 1], heads, h).items()}
+            taps.update(new_key=k_new[:, 0], new_value=v_new[:, 0])
+            outs.append(taps)
+        return {key: np.stack([t[key] for t in outs]) for key in outs[0]}
+    return decode_step
+
+
+def _prefill_chunk_positions_from_zero(cfg, w, x, cache_k, cache_v, lens):
+    # the chunk's rotary positions restart at 0 instead of following the cache
+    x = np.asarray(x, dtype=F64)
+    B, T, _ = x.shape
+    outs = []
+    for b in range(B):
+        L = int(lens[b])
+        h = ob.rms_norm(x[b], w["input_layernorm"], cfg.rms_norm_eps)
+        k_new, v_new = ob._project_kv(cfg, w, h, np.arange(T))
+        q = ob._project_q(cfg, w, h, np.arange(T))
+        k_all = np.concatenate([np.asarray(cache_k[b, :, :L], dtype=F64), k_new], axis=1)
+        v_all = np.concatenate([np.asarray(cache_v[b, :, :L], dtype=F64), v_new], axis=1)
+        heads = ob.causal_gqa_attention(q, k_all, v_all, np.arange(L, L + T), np.arange(L + T),
+                                        window=cfg.sliding_window)
+        taps = ob._finish_rows(cfg, w, x[b], heads, h)
+        taps.update(new_keys=k_new, new_values=v_new)
+        outs.append(taps)
+    return {key: np.stack([t[key] for t in outs]) for key in outs[0]}
+
+
+def _model_without_final_norm(cfg, layers, embed, norm_g, lm_head, tokens):
+    x = np.asarray(embed, dtype=F64)[np.asarray(tokens)]
+    for w in layers:
+        x = ob.block_forward(cfg, w, x)["layer_output"]
+    return (x * np.asarray(norm_g, dtype=F64)) @ np.asarray(lm_head, dtype=F64).T
+
+
 _orig_padding_run = ob.padding_run
 _orig_finish = ob._finish_rows
 _orig_mlp = ob.mlp
@@ -250,6 +314,13 @@ MUTATIONS = {
                                       ("_project_kv", _project_kv_rope_always)],
     "padding_keys_visible": [("causal_gqa_attention", _attn_factory(use_key_valid=False))],
     "padding_positions_unshifted": [("padding_run", _padding_run_unshifted)],
+    "yarn_attention_factor_dropped": [("rope_attention_factor", _yarn_attention_factor_dropped)],
+    "xielu_alpha_n_without_beta": [("xielu_effective", _xielu_alpha_n_without_beta)],
+    "xielu_parameters_without_softplus": [("xielu_effective", _xielu_raw_parameters)],
+    "decode_rotary_one_position_early": [("decode_step", _decode_factory(shift=-1))],
+    "decode_without_its_own_key": [("decode_step", _decode_factory(own_key=False))],
+    "prefill_chunk_positions_from_zero": [("prefill_with_cache", _prefill_chunk_positions_from_zero)],
+    "model_without_final_norm": [("model_forward", _model_without_final_norm)],
 }
 
 PIN_TESTS = [
@@ -279,6 +350,11 @@ PIN_TESTS = [
     pins.test_afmoe_gate_taps_and_half_gate,
     pins.test_afmoe_whole_prefix_block_queries_are_q_norm_output,
     pins.test_padded_batch_real_rows_equal_the_unpadded_rows,
+    pins.test_xielu_parameter_transform,
+    pins.test_decode_equals_last_prefill_row,
+    pins.test_prefill_chunk_equals_the_full_prefill_rows,
+    pins.test_prefill_chunk_of_one_token_is_a_decode_step,
+    pins.test_model_with_identity_blocks_and_tied_embeddings_reads_its_own_token,
 ]
 
 
