@@ -434,8 +434,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-__device__ __forceinline__ bool elect_one_lane() { return (threadIdx.x & 31) == 0; }
-
 // ---------------------------------------------------------------- programmatic dependent launch
 // Every kernel of a forward is launched with programmatic stream serialization:
 // it may start while its predecessor on the stream still runs, once every CTA of
